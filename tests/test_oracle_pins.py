@@ -1,0 +1,521 @@
+"""Pins for the CPU oracle: each checks it against something other than itself.
+
+Sources (the MiX paper as digested on the pchao.org page
+'MiX：面向端到端低比特视觉语言模型加速的微反缩放'):
+  * section 方法概览 (Method), MiX-4.25b / MiX-4.5b bullets: bit layouts,
+    dequantisation (-1)^s (1.mshared)_2 2^(Emax - de), de = 7 as zero;
+  * same section, Algorithm 1 bullet: Emax from the block maximum, mshared from
+    the maximum's mantissa, refinement over {de-1, de, de+1} for minimum error;
+  * same section, Eq. (6) bullet: the factorised block dot product;
+  * same section, accelerator bullet: asymmetric zero (the -0 code recycled
+    for positives), K-smoothing gamma(K) = K - mean(K), softmax shift invariance;
+  * section 关键结果 (Key results): about 40% of block maxima unrepresentable
+    under the OCP floor rule for MXFP4.
+
+Pins used: brute force with exact rationals (fractions.Fraction) over every
+code, closed-form special values, invariants (round trip, softmax shift
+invariance, zero-mean after smoothing), the printed bit accounting and the
+printed ~40% statistic.  ``test_planted_mistakes_are_caught`` plants each of
+the oracle's deliberate mutations and checks that some pin fails.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from quantized_vlm_gemm_mix_b300 import synth
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(1234)
+
+
+# ----------------------------------------------------------------------------
+# Independent helpers written from the definitions (not from the oracle).
+# ----------------------------------------------------------------------------
+
+def bf16_to_fraction(bits: int) -> Fraction:
+    """Exact value of a finite bf16 bit pattern, from the IEEE field definition."""
+    s = (bits >> 15) & 1
+    e = (bits >> 7) & 0xFF
+    m = bits & 0x7F
+    if e == 0:
+        v = Fraction(m, 128) * Fraction(2) ** -126
+    else:
+        v = (1 + Fraction(m, 128)) * Fraction(2) ** (e - 127)
+    return -v if s else v
+
+
+def f32_to_fraction(x: float) -> Fraction:
+    return Fraction(float(np.float32(x)))
+
+
+def mix_code_value(code: int, emax: int, m3: int) -> Fraction:
+    """Dequantisation rule of the Method section, with the recycled -0 code."""
+    s, d = code >> 3, code & 7
+    M = 1 + Fraction(m3, 8)
+    if d == 7:
+        return M * Fraction(2) ** (emax - 7) if s else Fraction(0)
+    v = M * Fraction(2) ** (emax - d)
+    return -v if s else v
+
+
+def brute_mix_code(x: Fraction, emax: int, m3: int, asym: bool) -> int:
+    """argmin over all 16 codes of |x - value|; ties to the larger magnitude,
+    and between two zero codes to 0x7."""
+    best = None
+    for code in range(16):
+        if code == 0xF and not asym:
+            continue
+        v = mix_code_value(code, emax, m3)
+        key = (abs(x - v), -abs(v), code != 0x7)
+        if best is None or key < best[0]:
+            best = (key, code)
+    return best[1]
+
+
+def nearest_mantissa(amax: Fraction):
+    """Round amax to 4 significant bits (nearest, ties to even); returns (f, m3)."""
+    f = math.floor(math.log2(amax))
+    while Fraction(2) ** f > amax:
+        f -= 1
+    while Fraction(2) ** (f + 1) <= amax:
+        f += 1
+    cands = [(Fraction(8 + j, 8) * Fraction(2) ** f, j) for j in range(9)]
+    best = min(cands, key=lambda c: (abs(amax - c[0]), c[1] % 2))
+    j = best[1]
+    return (f + 1, 0) if j == 8 else (f, j)
+
+
+def unpack_nibbles(codes: np.ndarray) -> np.ndarray:
+    lo = codes & 0xF
+    hi = codes >> 4
+    return np.stack([lo, hi], axis=-1).reshape(codes.shape[0], -1)
+
+
+def t1_fields(sh):
+    return int(sh) & 0xF, [(int(sh) >> 4) & 7] * 4
+
+
+def t2_fields(sh):
+    sh = int(sh)
+    return sh & 0xF, [(sh >> (4 + 3 * k)) & 7 for k in range(4)]
+
+
+def e2m1_magnitudes():
+    """E2M1 magnitudes from the field definition: e = 0 subnormal m * 0.5,
+    else (1 + m/2) * 2^(e-1)."""
+    out = []
+    for code in range(8):
+        e, m = code >> 1, code & 1
+        out.append(Fraction(m, 2) if e == 0 else (1 + Fraction(m, 2)) * Fraction(2) ** (e - 1))
+    return out
+
+
+def random_bf16_block_bits(n_blocks, spread=12, zeros=0.1):
+    """Random bf16 bit patterns with a wide exponent spread and some zeros."""
+    exps = RNG.integers(127 - spread, 127 + 4, size=(n_blocks, 32))
+    mant = RNG.integers(0, 128, size=(n_blocks, 32))
+    sign = RNG.integers(0, 2, size=(n_blocks, 32))
+    bits = (sign << 15) | (exps << 7) | mant
+    bits[RNG.random((n_blocks, 32)) < zeros] = 0
+    return bits.astype(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+# Pins (plain functions so the planted-mistake test can re-run them).
+# ----------------------------------------------------------------------------
+
+def pin_bit_accounting(orc):
+    g = json.load(open(os.path.join(GOLD, "bit_accounting.json")))
+    rows, k = 8, 256
+    x = synth.to_bf16_bits(synth.laplace(0, 1, rows * k, 0.3).reshape(rows, k))
+    c1, s1 = orc.mix_quantize(x, orc.T1)
+    c2, s2 = orc.mix_quantize(x, orc.T2)
+    assert (c1.nbytes + s1.nbytes) * 8 == rows * k * g["mix_4p25"]["bits_per_element"]
+    assert (c2.nbytes + s2.nbytes) * 8 == rows * k * g["mix_4p5"]["bits_per_element"]
+    assert (c2.nbytes + s2.nbytes) * 8 // (rows * k // 32) == g["mix_4p5"]["bits_per_block"]
+    # T1 shared field: Emax (4 bits) + mshared (3 bits) padded to 8 bits -> bit 7 unused
+    assert int(np.max(s1)) < 128
+    # T2: 4 + 4 x 3 bits occupy the whole 16-bit field, nothing more
+    assert s2.dtype == np.uint16
+
+
+def pin_dequant_special_values(orc):
+    """Closed-form values of single codes: implicit leading one, de = 7 zero,
+    one binade per de step, sign, and the recycled -0."""
+    ebias = -8
+    for ec in (0, 5, 8, 15):
+        emax = ec + ebias
+        for m3 in range(8):
+            codes = np.zeros((1, 16), dtype=np.uint8)
+            nib = [0x0, 0x1, 0x2, 0x3, 0x4, 0x5, 0x6, 0x7, 0x8, 0x9, 0xA, 0xE, 0xF] + [0x7] * 19
+            for j in range(16):
+                codes[0, j] = nib[2 * j] | (nib[2 * j + 1] << 4)
+            sh = np.array([[ec | (m3 << 4)]], dtype=np.uint8)
+            v = orc.mix_dequantize(codes, sh, orc.T1, ebias)[0]
+            M = 1.0 + m3 / 8.0
+            assert v[0] == M * 2.0 ** emax                   # de = 0 is the block maximum
+            for d in range(6):
+                assert v[d] == 2.0 * v[d + 1]                # one binade per de
+            assert v[7] == 0.0                               # de = 7 encodes zero
+            assert v[8] == -v[0] and v[9] == -v[1] and v[10] == -v[2] and v[11] == -v[6]
+            assert v[12] == M * 2.0 ** (emax - 7) and v[12] > 0   # recycled -0
+    # a worked value: m3 = 4 is (1.100)_2 = 1.5; Emax = 3, de = 2 -> 1.5 * 2 = 3
+    codes = np.full((1, 16), 0x77, dtype=np.uint8)
+    codes[0, 0] = 0x72
+    sh = np.array([[(3 + 8) | (4 << 4)]], dtype=np.uint8)
+    assert orc.mix_dequantize(codes, sh, orc.T1, -8)[0, 0] == 3.0
+
+
+def pin_refinement_brute_force(orc, n_blocks=300):
+    """Every element code is the exact minimum-error code (all 16 tried),
+    and Emax / mshared come from the block (sub-block) maximum rounded to
+    nearest-even at 4 significant bits."""
+    bits = random_bf16_block_bits(n_blocks)
+    for mix_type in (1, 2):
+        for asym in (True, False):
+            flags = 1 if asym else 0
+            ebias = -12
+            codes, shared = orc.mix_quantize(bits, mix_type, ebias, flags)
+            nib = unpack_nibbles(codes)
+            for b in range(n_blocks):
+                xs = [bf16_to_fraction(int(v)) for v in bits[b]]
+                ec, m3s = (t1_fields if mix_type == 1 else t2_fields)(shared[b, 0])
+                amax = max(abs(v) for v in xs)
+                if amax == 0:
+                    assert all(int(c) == 7 for c in nib[b]) and ec == 0
+                    continue
+                f, m3 = nearest_mantissa(amax)
+                emax = min(max(f, ebias), ebias + 15)
+                all_zero = all(int(c) == 7 for c in nib[b])
+                if not all_zero:
+                    assert ec + ebias == emax
+                for k in range(4):
+                    sub = xs[8 * k:8 * k + 8]
+                    smax = max(abs(v) for v in sub)
+                    want_m3 = m3 if mix_type == 1 else (nearest_mantissa(smax)[1] if smax else 0)
+                    sub_zero = all(int(c) == 7 for c in nib[b, 8 * k:8 * k + 8])
+                    if (mix_type == 2 and sub_zero) or all_zero:
+                        want_m3 = 0
+                        assert m3s[k] == 0
+                    else:
+                        assert m3s[k] == want_m3
+                    for i in range(8):
+                        x = sub[i]
+                        use_m3 = m3 if mix_type == 1 else (nearest_mantissa(smax)[1] if smax else 0)
+                        want = brute_mix_code(x, emax, use_m3, asym)
+                        assert int(nib[b, 8 * k + i]) == want, (b, k, i, x, emax, use_m3)
+
+
+def pin_exhaustive_sweep(orc):
+    """Every bf16 magnitude in [2^(Emax-10), 2^(Emax+1)) of either sign, for
+    each of the 8 shared mantissas, as the second element of a block whose
+    first element M * 2^Emax fixes the block maximum."""
+    emax = 0
+    xs = []
+    for e in range(127 + emax - 10, 127 + emax + 1):
+        for m in range(128):
+            xs.append((e << 7) | m)
+    xs = np.array(xs, dtype=np.uint16)
+    for m3 in range(8):
+        M_bits = ((127 + emax) << 7) | (m3 << 4)           # (1.m3) * 2^emax exactly
+        Mv = bf16_to_fraction(M_bits)
+        for sgn in (0, 0x8000):
+            blk = np.full((len(xs), 32), 0, dtype=np.uint16)
+            blk[:, 0] = M_bits
+            blk[:, 1] = xs | sgn
+            for mix_type in (1, 2):
+                codes, shared = orc.mix_quantize(blk, mix_type, -8, 1)
+                nib = unpack_nibbles(codes)
+                for r in range(len(xs)):
+                    x = bf16_to_fraction(int(blk[r, 1]))
+                    if abs(x) > Mv:
+                        continue                               # x became the maximum
+                    want = brute_mix_code(x, emax, m3, True)
+                    assert int(nib[r, 1]) == want, (m3, hex(int(blk[r, 1])))
+                    assert int(nib[r, 0]) == 0                 # the maximum: de = 0
+
+
+def pin_asymmetric_zero(orc):
+    """The recycled -0 code gives positive values one more binade (accelerator
+    bullet of the Method section)."""
+    emax, m3 = 2, 5
+    M = 1 + m3 / 8
+    base = np.zeros((1, 32), dtype=np.float32)
+    base[0, 0] = M * 2.0 ** emax
+    vmin_pos = M * 2.0 ** (emax - 7)
+    for x, asym, want in [
+        (vmin_pos, True, 0xF),              # exactly the recycled level
+        (vmin_pos * 0.51, True, 0xF),       # above half-way to zero
+        (vmin_pos * 0.49, True, 0x7),       # below half-way: zero
+        (-vmin_pos * 0.99, True, 0x7),      # negative side has no such level: zero
+        (-vmin_pos, True, 0xE),             # half-way to -2*vmin: the tie goes to the larger
+        (vmin_pos * 0.99, False, 0x7),      # flag off: nearest of {0, 2*vmin} is 0
+        (vmin_pos, False, 0x6),             # flag off: the tie goes to de = 6
+        (vmin_pos * 2.0, True, 0x6),
+    ]:
+        b = base.copy()
+        b[0, 5] = x
+        codes, _ = orc.mix_quantize(b, orc.T1, -8, 1 if asym else 0)
+        got = unpack_nibbles(codes)[0, 5]
+        assert int(got) == want, (x, asym, int(got), want)
+
+
+def pin_round_trip(orc, n=400):
+    """quantise(decode(c)) == c for canonical code blocks with a de = 0 element."""
+    for mix_type in (1, 2):
+        ebias = -8
+        nib = RNG.integers(0, 16, size=(n, 32))
+        nib[:, 0] = RNG.integers(0, 2, size=n) << 3        # a de = 0 element
+        ec = RNG.integers(0, 16, size=n)
+        m3 = RNG.integers(0, 8, size=(n, 4))
+        if mix_type == 1:
+            m3[:, 1:] = m3[:, :1]
+        for b in range(n):                                  # canonical: all-zero sub-blocks
+            for k in range(4):
+                if mix_type == 2 and all(nib[b, 8 * k:8 * k + 8] == 7):
+                    m3[b, k] = 0
+        codes = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+        if mix_type == 1:
+            sh = (ec | (m3[:, 0] << 4)).astype(np.uint8)[:, None]
+        else:
+            sh = (ec | (m3[:, 0] << 4) | (m3[:, 1] << 7) | (m3[:, 2] << 10) | (m3[:, 3] << 13)).astype(np.uint16)[:, None]
+        v = orc.mix_dequantize(codes, sh, mix_type, ebias).astype(np.float32)
+        c2, s2 = orc.mix_quantize(v, mix_type, ebias, 1)
+        assert np.array_equal(c2, codes)
+        assert np.array_equal(s2, sh)
+
+
+def pin_nonfinite_and_zero_blocks(orc):
+    x = np.zeros((3, 32), dtype=np.float32)
+    x[0, 3] = np.nan                                     # NaN alone: zero block
+    x[1, 0] = np.inf
+    x[1, 1] = 1.0
+    x[1, 2] = -np.inf
+    x[2, :] = 1e-30                                      # far below 2^ebias: all zero codes
+    codes, sh = orc.mix_quantize(x, orc.T1, -8, 1)
+    nib = unpack_nibbles(codes)
+    assert all(nib[0] == 7) and sh[0, 0] == 0
+    assert nib[1, 0] == 0 and nib[1, 2] == 8 and (sh[1, 0] & 0xF) == 15
+    assert all(nib[2] == 7) and sh[2, 0] == 0            # canonical zero block
+
+
+def pin_e2m1_and_int4_brute_force(orc):
+    grid = e2m1_magnitudes()
+    assert [float(g) for g in grid] == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    # a block whose maximum fixes X, then sweep the other elements
+    vals = np.linspace(-7.5, 7.5, 961).astype(np.float32)
+    for mx_type in (0, 1):
+        nblk = (len(vals) + 30) // 31
+        x = np.zeros((nblk, 32), dtype=np.float32)
+        x[:, 0] = 4.0 if mx_type == 1 else 7.0               # X = 0 (FP4, floor rule) / X = 2 (INT4)
+        flat = np.concatenate([vals, np.zeros(nblk * 31 - len(vals), np.float32)])
+        x[:, 1:] = flat.reshape(nblk, 31)
+        # the OCP floor rule keeps X = 0 for every block here, so the rounding
+        # and the saturation above 6 are both exercised
+        codes, scales = orc.mx_quantize(x, 1, mx_type, orc.MX_FLOOR if mx_type == 1 else 0)
+        nib = unpack_nibbles(codes)
+        for b in range(nblk):
+            X = int(scales[b, 0]) - 127
+            for i in range(1, 32):
+                xv = Fraction(float(x[b, i]))
+                if mx_type == 1:
+                    assert X == 0
+                    y = xv / Fraction(2) ** X
+                    if abs(y) >= 6:
+                        want = 7
+                    else:
+                        want = min(range(8), key=lambda c: (abs(abs(y) - grid[c]), c % 2))
+                    want |= (8 if (y < 0 and want != 0) else 0)
+                else:
+                    assert X == 2
+                    y = xv / Fraction(2) ** (X - 2)
+                    q = round(y)                          # Python rounds half to even
+                    q = max(-7, min(7, q))
+                    want = q & 0xF
+                assert int(nib[b, i]) == want, (mx_type, float(xv), int(nib[b, i]), want)
+
+
+def pin_mx_scale_rule(orc):
+    """About 40% of block maxima are unrepresentable under the floor rule; none
+    under ceil (Key results section); ceil puts amax / 2^X in (2, 4]."""
+    g = json.load(open(os.path.join(GOLD, "mxfp4_floor_rule.json")))
+    w = synth.to_bf16_bits(synth.gaussian_weights(7, 3, 1024, 512))
+    xf = synth.bf16_bits_to_f32(w).astype(np.float64)
+    for flags, lo, hi in ((2, 0.35, 0.46), (0, 0.0, 0.0)):
+        codes, scales = orc.mx_quantize(w, 0, orc.MXFP4, flags)
+        X = scales.astype(np.int64) - 127                   # [N, K/32]
+        amax = np.abs(xf).reshape(32, 32, 512).max(axis=1).T  # [N, K/32]
+        frac = float(np.mean(amax / np.exp2(X) > 6.0))
+        assert lo <= frac <= hi, (flags, frac)
+        if flags == 0:
+            r = amax / np.exp2(X)
+            assert np.all((r > 2) & (r <= 4))
+    assert abs(g["floor_unrepresentable_fraction_about"] - math.log2(2 / 1.5)) < 0.02
+
+
+def pin_mx_axis_consistency(orc):
+    x = synth.to_bf16_bits(synth.normal(3, 9, 96 * 160, 0, 0.02).reshape(96, 160))
+    for t in (0, 1):
+        c0, s0 = orc.mx_quantize(x, 0, t)                   # blocks down the columns
+        c1, s1 = orc.mx_quantize(np.ascontiguousarray(x.T), 1, t)
+        assert np.array_equal(c0, c1) and np.array_equal(s0, s1)
+
+
+def frac_mx_value(code, scale, mx_type):
+    X = int(scale) - 127
+    if mx_type == 1:
+        v = e2m1_magnitudes()[code & 7] * Fraction(2) ** X
+        return -v if code & 8 else v
+    q = code - 16 if code & 8 else code
+    return q * Fraction(2) ** (X - 2)
+
+
+def pin_gemm_eq6_exact(orc):
+    """Eq. (6) evaluated as int64 shift-add equals the exact sum of products of
+    dequantised values (the plain definition), on tiny matrices, exactly."""
+    M, N, K = 3, 4, 96
+    a = synth.to_bf16_bits(synth.vlm_activations(5, 0, M, K, visual_rows=2))
+    w = synth.to_bf16_bits(synth.gaussian_weights(5, 1, K, N))
+    for at in (1, 2):
+        ac, ash = orc.mix_quantize(a, at, -8, 1)
+        an = unpack_nibbles(ac)
+        for bt in (0, 1):
+            bc, bs = orc.mx_quantize(w, 0, bt)
+            bn = unpack_nibbles(bc)
+            c = orc.gemm(ac, ash, at, -8, bc, bs, bt)
+            for m in range(M):
+                for n in range(N):
+                    tot = Fraction(0)
+                    for kk in range(K):
+                        ec, m3s = (t1_fields if at == 1 else t2_fields)(ash[m, kk // 32])
+                        av = mix_code_value(int(an[m, kk]), ec - 8, m3s[(kk % 32) // 8])
+                        bv = frac_mx_value(int(bn[n, kk]), bs[n, kk // 32], bt)
+                        tot += av * bv
+                    assert Fraction(c[m, n]) == tot, (at, bt, m, n)
+
+
+def pin_gemm_against_dequant_matmul(orc):
+    M, N, K = 24, 40, 320
+    a = synth.to_f32(synth.vlm_activations(6, 0, M, K, visual_rows=16))
+    w = synth.to_bf16_bits(synth.gaussian_weights(6, 1, K, N))
+    for at in (1, 2):
+        ac, ash = orc.mix_quantize(a, at, -8, 1)
+        ad = orc.mix_dequantize(ac, ash, at, -8)
+        for bt in (0, 1):
+            bc, bs = orc.mx_quantize(w, 0, bt)
+            bd = orc.mx_dequantize(bc, bs, bt)
+            c = orc.gemm(ac, ash, at, -8, bc, bs, bt)
+            ref = ad @ bd.T
+            scale = np.abs(ad) @ np.abs(bd).T + 1e-300
+            assert np.max(np.abs(c - ref) / scale) < 1e-13
+
+
+def pin_gemm_reduces_to_mx_dot(orc):
+    """m3 = 0 and every de = 0: each A element is +-2^Emax, so the product is a
+    plain MX dot product with a sign vector."""
+    N, K = 6, 64
+    sgn = RNG.integers(0, 2, size=(1, K))
+    a = np.where(sgn == 1, -1.0, 1.0).astype(np.float32) * 2.0
+    w = synth.to_bf16_bits(synth.gaussian_weights(8, 1, K, N))
+    ac, ash = orc.mix_quantize(a, orc.T1, -8, 1)
+    assert np.all((unpack_nibbles(ac) & 7) == 0) and int(ash[0, 0]) >> 4 == 0
+    for bt in (0, 1):
+        bc, bs = orc.mx_quantize(w, 0, bt)
+        bd = orc.mx_dequantize(bc, bs, bt)
+        c = orc.gemm(ac, ash, orc.T1, -8, bc, bs, bt)
+        want = np.array([sum(float(a[0, k]) * bd[n, k] for k in range(K)) for n in range(N)])
+        assert np.array_equal(c[0], want)
+
+
+def pin_gemm_batch_gqa_indexing(orc):
+    B, G, M, N, K = 6, 3, 5, 7, 64
+    a = synth.to_f32(synth.laplace(9, 0, B * M * K, 0.3).reshape(B * M, K))
+    w = synth.to_bf16_bits(synth.normal(9, 1, (B // G) * N * K, 0, 0.02).reshape((B // G) * N, K))
+    ac, ash = orc.mix_quantize(a, orc.T2, -8, 1)
+    bc, bs = orc.mx_quantize(w, 1, orc.MXINT4)
+    c = orc.gemm(ac.reshape(B, M, -1), ash.reshape(B, M, -1), orc.T2, -8,
+                 bc.reshape(B // G, N, -1), bs.reshape(B // G, N, -1), orc.MXINT4, b_group=G)
+    for b in range(B):
+        g = b // G
+        c2 = orc.gemm(ac[b * M:(b + 1) * M], ash[b * M:(b + 1) * M], orc.T2, -8,
+                      bc[g * N:(g + 1) * N], bs[g * N:(g + 1) * N], orc.MXINT4)
+        assert np.array_equal(c[b], c2)
+
+
+def pin_ksmooth(orc):
+    """gamma(K) = K - mean(K): zero mean per channel afterwards, exact means of
+    closed-form inputs, and softmax(qK^T) unchanged (shift invariance)."""
+    T, H, D = 64, 2, 32
+    # closed form: K[t, h, d] = c[h, d] + t * delta (exact in fp32) -> mean = c + delta (T-1)/2
+    c = np.arange(H * D, dtype=np.float32).reshape(H, D) * 0.25 - 3.0
+    delta = np.float32(0.125)
+    k = (c[None] + delta * np.arange(T, dtype=np.float32)[:, None, None]).astype(np.float32)
+    mu = orc.ksmooth_mean(k)
+    assert np.array_equal(mu, c.astype(np.float64) + float(delta) * (T - 1) / 2)
+    q, kk, _ = synth.attention_qkv(11, T, q_heads=2, kv_heads=2, head_dim=D)
+    kb = synth.to_bf16_bits(kk)
+    mu = orc.ksmooth_mean(kb)
+    ks = orc.ksmooth_apply(kb, mu.astype(np.float32))
+    assert np.max(np.abs(ks.astype(np.float64).mean(axis=0))) < 1e-5 * np.max(np.abs(mu))
+    kf = synth.bf16_bits_to_f32(kb).astype(np.float64)
+    for h in range(2):
+        s0 = q[:, h] @ kf[:, h].T
+        s1 = q[:, h] @ (kf[:, h] - mu[h]).T
+        p0 = np.exp(s0 - s0.max(1, keepdims=True)); p0 /= p0.sum(1, keepdims=True)
+        p1 = np.exp(s1 - s1.max(1, keepdims=True)); p1 /= p1.sum(1, keepdims=True)
+        assert np.max(np.abs(p0 - p1)) < 1e-12
+    # a frozen mean (from a prefix of the tokens) is still a per-channel shift
+    mu_f = orc.ksmooth_mean(kb[: T // 2])
+    ks_f = orc.ksmooth_apply(kb, mu_f.astype(np.float32)).astype(np.float64)
+    want = kf - mu_f.astype(np.float32).astype(np.float64)[None]
+    assert np.max(np.abs(ks_f - want)) <= np.max(np.abs(want)) * 2.0 ** -23
+
+
+ALL_PINS = [pin_bit_accounting, pin_dequant_special_values, pin_refinement_brute_force,
+            pin_exhaustive_sweep, pin_asymmetric_zero, pin_round_trip,
+            pin_nonfinite_and_zero_blocks, pin_e2m1_and_int4_brute_force, pin_mx_scale_rule,
+            pin_mx_axis_consistency, pin_gemm_eq6_exact, pin_gemm_against_dequant_matmul,
+            pin_gemm_reduces_to_mx_dot, pin_gemm_batch_gqa_indexing, pin_ksmooth]
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
+def test_pin(orc, pin):
+    orc.set_mutation(0)
+    pin(orc)
+
+
+# Mutations planted in the oracle (see orc_set_mutation): 1 mshared truncated
+# instead of rounded, 2 implicit leading one dropped, 3 naive de off by one,
+# 4 refinement search removed, 5 MXFP4 floor instead of ceil, 6 FP4 exponent
+# dropped from the Eq. (6) shift, 7 smoothing adds the mean.
+FAST_PINS = [pin_dequant_special_values, pin_round_trip, pin_asymmetric_zero,
+             pin_e2m1_and_int4_brute_force, pin_mx_scale_rule, pin_gemm_eq6_exact,
+             pin_gemm_against_dequant_matmul, pin_ksmooth, pin_nonfinite_and_zero_blocks,
+             lambda o: pin_refinement_brute_force(o, n_blocks=40)]
+
+
+@pytest.mark.parametrize("mutation", [1, 2, 3, 4, 5, 6, 7])
+def test_planted_mistakes_are_caught(orc, mutation):
+    failed = []
+    try:
+        orc.set_mutation(mutation)
+        for pin in FAST_PINS:
+            try:
+                pin(orc)
+            except AssertionError:
+                failed.append(getattr(pin, "__name__", "pin"))
+    finally:
+        orc.set_mutation(0)
+    assert failed, f"mutation {mutation} slipped through every pin"
+
+
+def test_synthetic_activation_ratio():
+    """Visual vs text mean |x| follows the Fig. 1 statistics (about 34x)."""
+    g = json.load(open(os.path.join(GOLD, "activation_stats.json")))
+    x = synth.vlm_activations(0, 0, 512, 512, visual_rows=384, outlier_frac=0.0)
+    r = np.abs(x[:384]).mean() / np.abs(x[384:]).mean()
+    assert abs(r - g["ratio_about"]) < 3.0
