@@ -1,0 +1,228 @@
+/*
+ * mix.h -- C ABI of libmix.so: the MiX (Micro-Inverted-Scaling) hot path on
+ * one NVIDIA B300 (sm_103a).
+ *
+ * Source of every operation: "MiX: Micro-Inverted-Scaling for End-to-End
+ * Low-Bit Vision-Language Model Acceleration" (Liao and Seo, MICRO 2026), as
+ * digested on the pchao.org page "MiX：面向端到端低比特视觉语言模型加速的微反缩放"
+ * (sections named below are that page's).
+ *
+ * Bit layouts (the page gives field widths only; orders are this library's):
+ *  - MiX element nibble: bit 3 sign, bits 2..0 delta-e; 0x7 is zero; 0xF is
+ *    the recycled "-0", a positive value (1.mshared) * 2^(Emax - 7).
+ *  - MiX-4.25b shared byte: bits 3..0 Emax - ebias, bits 6..4 mshared, bit 7 0.
+ *  - MiX-4.5b shared uint16: bits 3..0 Emax - ebias, then the mshared of
+ *    sub-blocks 0..3 in bits 6..4, 9..7, 12..10, 15..13.
+ *  - MX element nibble: OCP E2M1 (MXFP4) or two's complement q (MXINT4);
+ *    scale byte X + 127 (E8M0).
+ *
+ * Conventions for every call:
+ *  - Pointers named x, codes, shared, scales, c, out_*, mean, k_out and
+ *    workspace are DEVICE pointers owned by the caller; the library allocates
+ *    no device memory and keeps no pointer after a call returns.
+ *  - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *  - Arguments are validated on the host before any launch; a rejected call
+ *    launches nothing and returns a MIX_ERR_* status.  A launch failure
+ *    returns MIX_ERR_CUDA.
+ *  - Non-finite inputs never fault: NaN is coded as zero and +-Inf saturates.
+ *  - Sizes are in elements unless a name ends in _bytes.  The packed planes
+ *    of a matrix with R rows and K columns are: codes R x K/2 bytes (element
+ *    2j in the low nibble of byte j, 16-byte aligned rows), shared R x K/32
+ *    entries (uint8 for MiX-4.25b, uint16 for MiX-4.5b), scales R x K/32
+ *    E8M0 bytes.  K must be a multiple of 32.
+ */
+#ifndef MIX_H_
+#define MIX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MIX_API __attribute__((visibility("default")))
+#else
+#define MIX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* mix_stream_t; /* same handle as cudaStream_t */
+
+typedef enum {
+  MIX_OK = 0,
+  MIX_ERR_INVALID_ARG = 1, /* null pointer, unknown enum value, negative size  */
+  MIX_ERR_SHAPE = 2,       /* K % 32 != 0, N % 32 != 0 for a quantising epilogue */
+  MIX_ERR_ALIGN = 3,       /* a plane or stride breaks its alignment rule       */
+  MIX_ERR_UNSUPPORTED = 4, /* a valid request this build does not implement     */
+  MIX_ERR_CUDA = 5,        /* a CUDA runtime error at launch                     */
+  MIX_ERR_WORKSPACE = 6,   /* workspace missing or smaller than required         */
+  MIX_ERR_DEVICE = 7       /* a kernel's bounded wait ran out (see below)        */
+} mix_status_t;
+
+typedef enum { MIX_T1_4P25 = 1, MIX_T2_4P5 = 2 } mix_type_t;
+typedef enum { MX_INT4 = 0, MX_FP4_E2M1 = 1 } mx_type_t;
+typedef enum { MIX_DT_F32 = 0, MIX_DT_BF16 = 1 } mix_dtype_t;
+
+/* Quantiser flags. */
+enum {
+  MIX_ASYM_ZERO = 1,  /* MiX: recycle the -0 code for one more positive binade
+                         (Method section, accelerator bullet).  Default on.   */
+  MX_SCALE_FLOOR = 2  /* MXFP4: OCP floor shared exponent instead of the ceil
+                         rule the paper uses for every MXFP4 (Key results).   */
+};
+
+/* ---------------------------------------------------------------------- */
+/* Plane sizes (host only, no device work).                                */
+/* ---------------------------------------------------------------------- */
+
+/* rows * k / 2.  Returns 0 for negative sizes or k % 32 != 0. */
+MIX_API size_t mix_codes_bytes(int64_t rows, int64_t k);
+/* rows * k/32 * (1 for MiX-4.25b, 2 for MiX-4.5b).  4.25 and 4.5 bits per
+ * element together with the codes (Method section, MiX-4.25b and MiX-4.5b
+ * bullets: (8 + 128)/32 and (4 + 4*3 + 32*4)/32 bits). */
+MIX_API size_t mix_shared_bytes(mix_type_t type, int64_t rows, int64_t k);
+/* rows * k / 32 E8M0 scale bytes of an MX plane. */
+MIX_API size_t mx_scales_bytes(int64_t rows, int64_t k);
+
+/* ---------------------------------------------------------------------- */
+/* MiX activation quantiser -- Algorithm 1 (Method section).               */
+/* ---------------------------------------------------------------------- */
+/* Per 32-element block along k: Emax from the block's largest magnitude,
+ * mshared from that element's mantissa (rounded to 3 bits, nearest-even), then
+ * per element the delta-e of least error among {de-1, de, de+1}; de = 7 codes
+ * zero; with MIX_ASYM_ZERO the -0 code is a positive level below de = 6.
+ * MiX-4.5b (Type 2) keeps one Emax per block and one mshared per 8-element
+ * sub-block.  Emax is stored as Emax - ebias in 4 bits (clamped).
+ *   x      rows x k input, row stride ld >= k elements, fp32 or bf16,
+ *          16-byte aligned with ld * sizeof(elem) a multiple of 16.
+ *   ebias  -100 .. 100; -8 suits activations, -15 softmax probabilities.
+ *   codes  rows x k/2 bytes (dense, 16-byte aligned).
+ *   shared rows x k/32 uint8 (Type 1) or uint16 (Type 2), dense.
+ * Output is bit-identical to the plain CPU definition. */
+MIX_API mix_status_t mix_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,
+                          mix_type_t type, int ebias, unsigned flags, uint8_t* codes,
+                          void* shared, mix_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* W-MX quantiser (MXINT4 / MXFP4, block 32, E8M0 scale).                  */
+/* ---------------------------------------------------------------------- */
+/* Blocks run along the reduction dimension K; outputs are N x K planes.
+ *   axis = 1: x is N x K (rows = N, cols = K), row stride ld >= K.
+ *   axis = 0: x is K x N (rows = K, cols = N), row stride ld >= N -- a
+ *             weight stored for x @ W; it is read down its columns and the
+ *             planes are written transposed (N x K).
+ * MXFP4 shared exponent: ceil(log2 amax) - 2 (the paper's ceil rule, Key
+ * results section), or the OCP floor with MX_SCALE_FLOOR; elements E2M1,
+ * nearest-even, saturating at 6.  MXINT4: X = floor(log2 amax), elements
+ * q * 2^(X-2), q in [-7, 7] two's complement, nearest-even.
+ *   codes  N x K/2 bytes; scales N x K/32 bytes (X + 127). */
+MIX_API mix_status_t mx_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t cols, int64_t ld,
+                         int axis, mx_type_t type, unsigned flags, uint8_t* codes,
+                         uint8_t* scales, mix_stream_t stream);
+
+/* Test aids: decode packed planes to fp32 (rows x k, dense).  MiX: the rule
+ * (-1)^s (1.mshared)_2 2^(Emax - de) of the Method section, de = 7 zero, code
+ * 0xF the recycled positive level.  MX: w * 2^X. */
+MIX_API mix_status_t mix_dequantize(const uint8_t* codes, const void* shared, int64_t rows, int64_t k,
+                            mix_type_t type, int ebias, float* out, mix_stream_t stream);
+MIX_API mix_status_t mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t k,
+                           mx_type_t type, float* out, mix_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* A-MiX x W-MX block matmul with optional fused output quantiser.         */
+/* ---------------------------------------------------------------------- */
+/* C[b][m][n] = sum over 32-blocks of Eq. (6) (Method section, dual-format
+ * matmul bullet): per block (1.mshared) * 2^(Emax + X) * sum_i s_i w_i
+ * 2^(-de_i), per 8-sub-block mshared for MiX-4.5b.  A (activations, MiX) is
+ * batch x M x K; B (weights or K/V, MX) is (batch / b_group) x N x K with
+ * blocks along K -- exactly what mx_quantize writes.  fp32 accumulation.
+ *
+ * Epilogue (Method section, accelerator bullet: accumulator -> fused MiX/MX
+ * quantiser -> DRAM): each 32-column block of each output row is quantised
+ * as mix_quantize / mx_quantize(axis 1) would quantise the fp32 row, into
+ * out_codes / out_shared (MiX shared, or MX scales).  C may be written too.
+ *
+ * Strides are in ELEMENTS of the logical matrix and must be multiples of 32:
+ * the codes of row m, batch b of A start at byte (b*a_batch_stride +
+ * m*a_ld)/2 of a_codes, its shared entries at index (b*a_batch_stride +
+ * m*a_ld)/32 of a_shared; likewise for B and the epilogue planes.  C is fp32
+ * with its own element strides ldc and c_batch_stride.
+ *
+ * algo: MIX_GEMM_AUTO picks the integer shift-add path for M <= 16 and the
+ * tcgen05 tensor-core path otherwise; the others force a path.  The
+ * shift-add path evaluates Eq. (6) literally (integer shift-add trees, one
+ * multiply by the shared mantissa, one exponent add) and splits K across
+ * CTAs when there are few outputs, summing the partials in a fixed order in
+ * the caller's workspace (see mix_mx_gemm_workspace_bytes).
+ */
+typedef enum { MIX_EPI_NONE = 0, MIX_EPI_MIX_T1 = 1, MIX_EPI_MIX_T2 = 2,
+               MIX_EPI_MXINT4 = 3, MIX_EPI_MXFP4 = 4 } mix_epilogue_t;
+typedef enum { MIX_GEMM_AUTO = 0, MIX_GEMM_TCGEN05 = 1, MIX_GEMM_SHIFTADD = 2 } mix_gemm_algo_t;
+
+typedef struct {
+  int64_t M, N, K;
+  int64_t batch;   /* >= 1 */
+  int64_t b_group; /* >= 1; batch b reads B batch b / b_group (GQA) */
+  const uint8_t* a_codes;
+  const void* a_shared;
+  mix_type_t a_type;
+  int a_ebias;
+  int64_t a_ld, a_batch_stride;
+  const uint8_t* b_codes;
+  const uint8_t* b_scales;
+  mx_type_t b_type;
+  int64_t b_ld, b_batch_stride;
+  float* c; /* optional fp32 output (NULL: epilogue planes only) */
+  int64_t ldc, c_batch_stride;
+  mix_epilogue_t epi;
+  int epi_ebias;       /* MiX epilogues */
+  unsigned epi_flags;  /* MIX_ASYM_ZERO / MX_SCALE_FLOOR */
+  uint8_t* out_codes;  /* batch x M x N/2 codes of the quantised output */
+  void* out_shared;    /* MiX shared entries or MX scale bytes */
+  int64_t out_ld, out_batch_stride;
+  mix_gemm_algo_t algo;
+} mix_gemm_desc_t;
+
+/* Bytes of device workspace mix_mx_gemm needs for this descriptor (0 if
+ * none).  The workspace is scratch owned by the caller; its contents on entry
+ * do not matter. */
+MIX_API size_t mix_mx_gemm_workspace_bytes(const mix_gemm_desc_t* desc);
+MIX_API mix_status_t mix_mx_gemm(const mix_gemm_desc_t* desc, void* workspace, size_t workspace_bytes,
+                         mix_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* K-smoothing (SageAttention style; Method section, accelerator bullet,   */
+/* and Caveats section on the static prefill mean).                        */
+/* ---------------------------------------------------------------------- */
+/* k: tokens x heads x head_dim keys (bf16 or fp32), token stride ld >= heads *
+ * head_dim elements.  KSMOOTH_COMPUTE: mean[h][d] = mean over the tokens,
+ * summed in fp64 in a fixed order and rounded once to fp32 (the prefill
+ * mean).  KSMOOTH_APPLY_FROZEN: mean is an input (frozen at prefill; decode
+ * does not re-read the cache).  Both modes write k_out = fp32(k) - mean (one
+ * fp32 subtraction), tokens x heads x head_dim dense, when k_out != NULL.
+ * COMPUTE splits the tokens across CTAs and keeps fp64 partial sums in the
+ * caller's workspace (ksmooth_workspace_bytes); APPLY needs none. */
+enum { KSMOOTH_COMPUTE = 0, KSMOOTH_APPLY_FROZEN = 1 };
+MIX_API size_t ksmooth_workspace_bytes(int64_t tokens, int heads, int head_dim);
+MIX_API mix_status_t ksmooth_kv(const void* k, mix_dtype_t dtype, int64_t tokens, int heads, int head_dim,
+                        int64_t ld, float* mean, int mode, float* k_out, void* workspace,
+                        size_t workspace_bytes, mix_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Status and device error word.                                           */
+/* ---------------------------------------------------------------------- */
+MIX_API const char* mix_status_str(mix_status_t status);
+/* Kernels never spin without bound: a wait that runs out records a bit in a
+ * per-device error word and the kernel returns early (its outputs are then
+ * undefined).  This reads the word for the current device (synchronising the
+ * device) and clears it when `clear` is nonzero.  MIX_OK if the read worked. */
+MIX_API mix_status_t mix_device_error(unsigned* word, int clear);
+/* Library version, major * 10000 + minor * 100 + patch. */
+MIX_API int mix_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MIX_H_ */

@@ -14,9 +14,11 @@
  * (bf16 / fp32) are widened to double exactly; code values are (1.m3) * 2^j
  * with a 3-bit m3; GEMM block sums are int64; the cross-block sum is fp64.
  *
- * Readings of points the pages leave open are the ones listed in the format
- * contract of this repository (field order, RNE for mshared, tie-breaks,
- * canonical zero blocks, NaN/Inf, MX scale rules).
+ * Readings of points the page leaves open: field orders as in the library
+ * header; mshared rounded to nearest-even with a carry into Emax; equal
+ * errors resolved toward the larger magnitude; an all-zero (sub-)block stores
+ * zero shared fields; NaN counts as zero, +-Inf saturates; MXFP4 scale
+ * ceil(log2 amax) - 2, MXINT4 scale floor(log2 amax) with q in [-7, 7].
  */
 #include <math.h>
 #include <stdint.h>

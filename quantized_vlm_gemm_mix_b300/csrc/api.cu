@@ -1,0 +1,224 @@
+// C ABI of libmix.so (include/mix.h): host-side validation, then one or more
+// launches on the caller's stream.  Nothing here allocates device memory.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mix_internal.h"
+
+using namespace mixk;
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+mix_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MIX_OK : MIX_ERR_CUDA; }
+
+bool valid_dtype(mix_dtype_t d) { return d == MIX_DT_F32 || d == MIX_DT_BF16; }
+int esize(mix_dtype_t d) { return d == MIX_DT_F32 ? 4 : 2; }
+
+// A packed plane addressed by element offsets: codes at offset/2 bytes,
+// shared (or scales) at offset/32 entries.  Strides must keep every row on a
+// 16-byte codes boundary.
+bool plane_strides_ok(int64_t ld, int64_t bs, int64_t k) {
+  return ld >= k && ld % 32 == 0 && bs % 32 == 0 && bs >= 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mix_codes_bytes(int64_t rows, int64_t k) {
+  if (rows < 0 || k < 0 || k % 32 != 0) return 0;
+  return (size_t)rows * (size_t)(k / 2);
+}
+
+size_t mix_shared_bytes(mix_type_t type, int64_t rows, int64_t k) {
+  if (rows < 0 || k < 0 || k % 32 != 0 || (type != MIX_T1_4P25 && type != MIX_T2_4P5)) return 0;
+  return (size_t)rows * (size_t)(k / 32) * (type == MIX_T1_4P25 ? 1u : 2u);
+}
+
+size_t mx_scales_bytes(int64_t rows, int64_t k) {
+  if (rows < 0 || k < 0 || k % 32 != 0) return 0;
+  return (size_t)rows * (size_t)(k / 32);
+}
+
+const char* mix_status_str(mix_status_t s) {
+  switch (s) {
+    case MIX_OK: return "ok";
+    case MIX_ERR_INVALID_ARG: return "invalid argument";
+    case MIX_ERR_SHAPE: return "unsupported shape (K and quantised N must be multiples of 32)";
+    case MIX_ERR_ALIGN: return "misaligned pointer or stride";
+    case MIX_ERR_UNSUPPORTED: return "unsupported combination";
+    case MIX_ERR_CUDA: return "CUDA error";
+    case MIX_ERR_WORKSPACE: return "workspace missing or too small";
+    case MIX_ERR_DEVICE: return "a kernel wait ran out (device error word set)";
+  }
+  return "unknown status";
+}
+
+int mix_version(void) { return kVersion; }
+
+mix_status_t mix_device_error(unsigned* word, int clear) {
+  if (word == nullptr) return MIX_ERR_INVALID_ARG;
+  return from_cuda(read_device_error(word, clear != 0));
+}
+
+mix_status_t mix_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,
+                          mix_type_t type, int ebias, unsigned flags, uint8_t* codes, void* shared,
+                          mix_stream_t stream) {
+  if (!valid_dtype(dtype) || (type != MIX_T1_4P25 && type != MIX_T2_4P5)) return MIX_ERR_INVALID_ARG;
+  if (rows < 0 || k < 0 || ld < k || ebias < -100 || ebias > 100 || (flags & ~1u)) return MIX_ERR_INVALID_ARG;
+  if (k % 32 != 0) return MIX_ERR_SHAPE;
+  if (rows == 0 || k == 0) return MIX_OK;
+  if (x == nullptr || codes == nullptr || shared == nullptr) return MIX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(codes, 16) ||
+      !aligned(shared, type == MIX_T1_4P25 ? 1 : 2))
+    return MIX_ERR_ALIGN;
+  return from_cuda(launch_mix_quantize(x, dtype == MIX_DT_BF16, rows, k, ld, (int)type, ebias,
+                                       (flags & MIX_ASYM_ZERO) != 0, codes, shared,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mix_status_t mx_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t cols, int64_t ld,
+                         int axis, mx_type_t type, unsigned flags, uint8_t* codes, uint8_t* scales,
+                         mix_stream_t stream) {
+  if (!valid_dtype(dtype) || (type != MX_INT4 && type != MX_FP4_E2M1) || (axis != 0 && axis != 1))
+    return MIX_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ld < cols || (flags & ~2u)) return MIX_ERR_INVALID_ARG;
+  const int64_t K = axis ? cols : rows, N = axis ? rows : cols;
+  if (K % 32 != 0) return MIX_ERR_SHAPE;
+  if (N == 0 || K == 0) return MIX_OK;
+  if (x == nullptr || codes == nullptr || scales == nullptr) return MIX_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(codes, 16)) return MIX_ERR_ALIGN;
+  const bool fp4 = type == MX_FP4_E2M1, fl = (flags & MX_SCALE_FLOOR) != 0;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (axis == 1)
+    return from_cuda(launch_mx_quantize_rows(x, dtype == MIX_DT_BF16, N, K, ld, fp4, fl, codes, scales, st));
+  return from_cuda(launch_mx_quantize_cols(x, dtype == MIX_DT_BF16, K, N, ld, fp4, fl, codes, scales, st));
+}
+
+mix_status_t mix_dequantize(const uint8_t* codes, const void* shared, int64_t rows, int64_t k,
+                            mix_type_t type, int ebias, float* out, mix_stream_t stream) {
+  if ((type != MIX_T1_4P25 && type != MIX_T2_4P5) || rows < 0 || k < 0 || ebias < -100 || ebias > 100)
+    return MIX_ERR_INVALID_ARG;
+  if (k % 32 != 0) return MIX_ERR_SHAPE;
+  if (rows == 0 || k == 0) return MIX_OK;
+  if (codes == nullptr || shared == nullptr || out == nullptr) return MIX_ERR_INVALID_ARG;
+  if (!aligned(codes, 16) || !aligned(out, 16) || !aligned(shared, type == MIX_T1_4P25 ? 1 : 2))
+    return MIX_ERR_ALIGN;
+  return from_cuda(launch_mix_dequantize(codes, shared, rows, k, (int)type, ebias, out,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mix_status_t mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t k,
+                           mx_type_t type, float* out, mix_stream_t stream) {
+  if ((type != MX_INT4 && type != MX_FP4_E2M1) || rows < 0 || k < 0) return MIX_ERR_INVALID_ARG;
+  if (k % 32 != 0) return MIX_ERR_SHAPE;
+  if (rows == 0 || k == 0) return MIX_OK;
+  if (codes == nullptr || scales == nullptr || out == nullptr) return MIX_ERR_INVALID_ARG;
+  if (!aligned(codes, 16) || !aligned(out, 16)) return MIX_ERR_ALIGN;
+  return from_cuda(launch_mx_dequantize(codes, scales, rows, k, type == MX_FP4_E2M1, out,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static mix_status_t validate_gemm(const mix_gemm_desc_t* d) {
+  if (d == nullptr) return MIX_ERR_INVALID_ARG;
+  if (d->M < 0 || d->N < 0 || d->K < 0 || d->batch < 1 || d->b_group < 1) return MIX_ERR_INVALID_ARG;
+  if (d->a_type != MIX_T1_4P25 && d->a_type != MIX_T2_4P5) return MIX_ERR_INVALID_ARG;
+  if (d->b_type != MX_INT4 && d->b_type != MX_FP4_E2M1) return MIX_ERR_INVALID_ARG;
+  if (d->a_ebias < -100 || d->a_ebias > 100 || d->epi_ebias < -100 || d->epi_ebias > 100)
+    return MIX_ERR_INVALID_ARG;
+  if (d->epi < MIX_EPI_NONE || d->epi > MIX_EPI_MXFP4) return MIX_ERR_INVALID_ARG;
+  if (d->algo < MIX_GEMM_AUTO || d->algo > MIX_GEMM_SHIFTADD) return MIX_ERR_INVALID_ARG;
+  if (d->K % 32 != 0) return MIX_ERR_SHAPE;
+  if (d->epi != MIX_EPI_NONE && d->N % 32 != 0) return MIX_ERR_SHAPE;
+  if (d->epi == MIX_EPI_NONE && d->c == nullptr) return MIX_ERR_INVALID_ARG;
+  if (d->M == 0 || d->N == 0) return MIX_OK;
+  if (d->K > 0) {
+    if (d->a_codes == nullptr || d->a_shared == nullptr || d->b_codes == nullptr || d->b_scales == nullptr)
+      return MIX_ERR_INVALID_ARG;
+    if (!plane_strides_ok(d->a_ld, d->a_batch_stride, d->K) || !plane_strides_ok(d->b_ld, d->b_batch_stride, d->K))
+      return MIX_ERR_ALIGN;
+    if (!aligned(d->a_codes, 16) || !aligned(d->b_codes, 16) ||
+        !aligned(d->a_shared, d->a_type == MIX_T1_4P25 ? 1 : 2))
+      return MIX_ERR_ALIGN;
+  }
+  if (d->c != nullptr) {
+    if (d->ldc < d->N || d->c_batch_stride < 0 || !aligned(d->c, 16) || d->ldc % 4 != 0 || d->c_batch_stride % 4 != 0)
+      return MIX_ERR_ALIGN;
+  }
+  if (d->epi != MIX_EPI_NONE) {
+    if (d->out_codes == nullptr || d->out_shared == nullptr) return MIX_ERR_INVALID_ARG;
+    if (!plane_strides_ok(d->out_ld, d->out_batch_stride, d->N) || !aligned(d->out_codes, 16) ||
+        !aligned(d->out_shared, d->epi == MIX_EPI_MIX_T2 ? 2 : 1))
+      return MIX_ERR_ALIGN;
+  }
+  return MIX_OK;
+}
+
+static bool use_shiftadd(const mix_gemm_desc_t* d) {
+  if (d->algo == MIX_GEMM_SHIFTADD) return true;
+  if (d->algo == MIX_GEMM_TCGEN05) return false;
+  return d->M <= 16;
+}
+
+size_t mix_mx_gemm_workspace_bytes(const mix_gemm_desc_t* d) {
+  if (validate_gemm(d) != MIX_OK || d->M == 0 || d->N == 0) return 0;
+  if (use_shiftadd(d)) return gemv_workspace_bytes(*d);
+  return 0;
+}
+
+mix_status_t mix_mx_gemm(const mix_gemm_desc_t* d, void* workspace, size_t workspace_bytes,
+                         mix_stream_t stream) {
+  mix_status_t s = validate_gemm(d);
+  if (s != MIX_OK || d->M == 0 || d->N == 0) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (use_shiftadd(d)) {
+    if (d->M > 16) return MIX_ERR_UNSUPPORTED;
+    if (d->epi != MIX_EPI_NONE) {
+      // the shift-add path quantises dense fp32 rows into dense planes
+      if (d->out_ld != d->N || d->out_batch_stride != d->M * d->N) return MIX_ERR_UNSUPPORTED;
+      if (d->c != nullptr && (d->ldc % 4 != 0)) return MIX_ERR_UNSUPPORTED;
+    }
+    const size_t need = gemv_workspace_bytes(*d);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return MIX_ERR_WORKSPACE;
+    if (d->K == 0) return MIX_ERR_UNSUPPORTED;
+    return from_cuda(launch_gemv_shiftadd(*d, workspace, st));
+  }
+  mix_status_t why = MIX_OK;
+  cudaError_t e = launch_gemm_tc(*d, st, &why);
+  if (why != MIX_OK) return why;
+  return from_cuda(e);
+}
+
+size_t ksmooth_workspace_bytes(int64_t tokens, int heads, int head_dim) {
+  if (tokens <= 0 || heads <= 0 || head_dim <= 0) return 0;
+  return ksmooth_ws_bytes(tokens, heads, head_dim);
+}
+
+mix_status_t ksmooth_kv(const void* k, mix_dtype_t dtype, int64_t tokens, int heads, int head_dim,
+                        int64_t ld, float* mean, int mode, float* k_out, void* workspace,
+                        size_t workspace_bytes, mix_stream_t stream) {
+  if (!valid_dtype(dtype) || tokens < 0 || heads <= 0 || head_dim <= 0) return MIX_ERR_INVALID_ARG;
+  if (mode != KSMOOTH_COMPUTE && mode != KSMOOTH_APPLY_FROZEN) return MIX_ERR_INVALID_ARG;
+  const int64_t C = (int64_t)heads * head_dim;
+  if (ld < C) return MIX_ERR_INVALID_ARG;
+  if (C % 8 != 0) return MIX_ERR_SHAPE;
+  if (mean == nullptr) return MIX_ERR_INVALID_ARG;
+  if (mode == KSMOOTH_COMPUTE && tokens == 0) return MIX_ERR_INVALID_ARG;  // mean of nothing
+  if (tokens > 0 && (k == nullptr)) return MIX_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(mean, 16) || (k_out && !aligned(k_out, 16)))
+    return MIX_ERR_ALIGN;
+  if (mode == KSMOOTH_COMPUTE) {
+    const size_t need = ksmooth_ws_bytes(tokens, heads, head_dim);
+    if (workspace == nullptr || workspace_bytes < need) return MIX_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return MIX_ERR_ALIGN;
+  }
+  return from_cuda(launch_ksmooth(k, dtype == MIX_DT_BF16, tokens, heads, head_dim, ld, mean, mode, k_out,
+                                  workspace, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

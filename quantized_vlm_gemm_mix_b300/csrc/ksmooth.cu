@@ -1,0 +1,140 @@
+// K-smoothing (SageAttention's gamma(K) = K - mean(K); Method section,
+// accelerator bullet, and Caveats section of the pchao.org digest of "MiX:
+// Micro-Inverted-Scaling ...": the mean is taken once over the prefill tokens
+// and frozen for decode, so the Key cache is never re-read to update it).
+//
+// COMPUTE: the tokens are split into chunks across CTAs (the whole tensor has
+// to be in flight to reach HBM bandwidth); each CTA sums its chunk per
+// channel in fp64 and writes one fp64 partial row to the caller's workspace.
+// A second kernel adds the partial rows in chunk order and divides by the
+// token count, so the result does not depend on scheduling.  APPLY (both
+// modes): k_out = fp32(k) - mean, one fp32 subtraction per element.
+#include <cuda_runtime.h>
+
+#include "mix_internal.h"
+
+namespace mixk {
+namespace {
+
+constexpr int kThreads = 256;  // 8 warps x 32 lanes x 8 channels = 256 channels
+
+__device__ __forceinline__ void load8f(const void* base, bool bf16, int64_t elem, float* v) {
+  if (bf16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem);
+    const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(a[i] << 16);
+      v[2 * i + 1] = __uint_as_float(a[i] & 0xFFFF0000u);
+    }
+  } else {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem);
+    const float4 a = p[0], b = p[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  }
+}
+
+// grid (channel tiles of 256, chunks).  Warp w sums tokens t0 + w, t0 + w + 8,
+// ... of the chunk; lane l owns channels c0 + 8l .. c0 + 8l + 7.
+__global__ void __launch_bounds__(kThreads) ksmooth_partial_kernel(
+    const void* __restrict__ k, int bf16, int64_t tokens, int64_t C, int64_t ld, int64_t chunk,
+    double* __restrict__ partial) {
+  __shared__ double red[8][256];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t c = (int64_t)blockIdx.x * 256 + lane * 8;
+  const int64_t t0 = (int64_t)blockIdx.y * chunk;
+  const int64_t t1 = min(tokens, t0 + chunk);
+  double s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (c < C) {
+    for (int64_t t = t0 + warp; t < t1; t += 8) {
+      float v[8];
+      load8f(k, bf16 != 0, t * ld + c, v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s[i] += (double)v[i];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[warp][lane * 8 + i] = s[i];
+  __syncthreads();
+  const int64_t cc = (int64_t)blockIdx.x * 256 + threadIdx.x;
+  if (cc < C) {
+    double acc = 0.0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) acc += red[w][threadIdx.x];
+    partial[(int64_t)blockIdx.y * C + cc] = acc;
+  }
+}
+
+__global__ void ksmooth_finalize_kernel(const double* __restrict__ partial, int64_t nchunks, int64_t C,
+                                        int64_t tokens, float* __restrict__ mean) {
+  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= C) return;
+  double acc = 0.0;
+  for (int64_t j = 0; j < nchunks; ++j) acc += partial[j * C + c];
+  mean[c] = (float)(acc / (double)tokens);
+}
+
+__global__ void __launch_bounds__(kThreads) ksmooth_apply_kernel(
+    const void* __restrict__ k, int bf16, int64_t tokens, int64_t C, int64_t ld,
+    const float* __restrict__ mean, float* __restrict__ out) {
+  const int64_t groups = C / 8;
+  const int64_t total = tokens * groups;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = g / groups, c = (g - t * groups) * 8;
+    float v[8];
+    load8f(k, bf16 != 0, t * ld + c, v);
+    const float4 m0 = *reinterpret_cast<const float4*>(mean + c);
+    const float4 m1 = *reinterpret_cast<const float4*>(mean + c + 4);
+    float4* o = reinterpret_cast<float4*>(out + t * C + c);
+    o[0] = make_float4(__fsub_rn(v[0], m0.x), __fsub_rn(v[1], m0.y), __fsub_rn(v[2], m0.z), __fsub_rn(v[3], m0.w));
+    o[1] = make_float4(__fsub_rn(v[4], m1.x), __fsub_rn(v[5], m1.y), __fsub_rn(v[6], m1.z), __fsub_rn(v[7], m1.w));
+  }
+}
+
+int64_t ksmooth_chunks(int64_t tokens, int64_t C) {
+  const int64_t tiles = (C + 255) / 256;
+  int64_t want = (4 * (int64_t)num_sms() + tiles - 1) / tiles;  // about four CTAs per SM
+  const int64_t by_len = (tokens + 31) / 32;                    // at least 32 tokens per chunk
+  if (want > by_len) want = by_len;
+  return want > 0 ? want : 1;
+}
+
+}  // namespace
+
+size_t ksmooth_ws_bytes(int64_t tokens, int heads, int head_dim) {
+  const int64_t C = (int64_t)heads * head_dim;
+  if (tokens <= 0 || C <= 0) return 0;
+  return (size_t)ksmooth_chunks(tokens, C) * (size_t)C * sizeof(double);
+}
+
+cudaError_t launch_ksmooth(const void* k, bool bf16, int64_t tokens, int heads, int head_dim,
+                           int64_t ld, float* mean, int mode, float* k_out, void* ws,
+                           cudaStream_t st) {
+  const int64_t C = (int64_t)heads * head_dim;
+  if (mode == KSMOOTH_COMPUTE) {
+    const int64_t nch = ksmooth_chunks(tokens, C);
+    const int64_t chunk = (tokens + nch - 1) / nch;
+    const int64_t used = (tokens + chunk - 1) / chunk;
+    const dim3 grid((unsigned)((C + 255) / 256), (unsigned)used);
+    ksmooth_partial_kernel<<<grid, kThreads, 0, st>>>(k, bf16 ? 1 : 0, tokens, C, ld, chunk,
+                                                      static_cast<double*>(ws));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ksmooth_finalize_kernel<<<(unsigned)((C + 127) / 128), 128, 0, st>>>(
+        static_cast<const double*>(ws), used, C, tokens, mean);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (k_out != nullptr && tokens > 0) {
+    const int64_t total = tokens * (C / 8);
+    int64_t g = (total + kThreads - 1) / kThreads;
+    if (g > (int64_t)num_sms() * 8) g = (int64_t)num_sms() * 8;
+    ksmooth_apply_kernel<<<(unsigned)g, kThreads, 0, st>>>(k, bf16 ? 1 : 0, tokens, C, ld, mean, k_out);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
+}
+
+}  // namespace mixk

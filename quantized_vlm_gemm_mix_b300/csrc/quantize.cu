@@ -1,0 +1,365 @@
+// MiX and MX quantiser kernels (sm_103a).
+//
+// MiX (Algorithm 1, Method section of the pchao.org digest of "MiX:
+// Micro-Inverted-Scaling ..."): four lanes own one 32-element block, eight
+// elements each (one 16-byte load of bf16, two of fp32).  The block maximum
+// is two butterfly shuffles; for MiX-4.5b each lane's eight elements are
+// exactly one sub-block, so a lane computes its own mshared.  Codes leave as
+// one 32-bit store per lane (a warp stores 128 contiguous bytes).
+//
+// The kernels are HBM-bound: a bf16 element costs 2 bytes in and 0.53125
+// (T1) / 0.5625 (T2) bytes out.  Each thread keeps two blocks in flight and
+// the grid is a multiple of the SM count.
+#include <cuda_runtime.h>
+
+#include "mix_common.cuh"
+#include "mix_internal.h"
+
+namespace mixk {
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kQuadsPerCta = kThreads / 4;
+constexpr int kUnroll = 2;
+
+// Eight consecutive elements as fp32 bit patterns.
+template <bool BF16>
+__device__ __forceinline__ void load8(const void* base, int64_t elem, uint32_t* u) {
+  if (BF16) {
+    uint4 v = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem));
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      u[2 * i] = w[i] << 16;
+      u[2 * i + 1] = w[i] & 0xFFFF0000u;
+    }
+  } else {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(base) + elem);
+    uint4 a = __ldcs(p), b = __ldcs(p + 1);
+    u[0] = a.x; u[1] = a.y; u[2] = a.z; u[3] = a.w;
+    u[4] = b.x; u[5] = b.y; u[6] = b.z; u[7] = b.w;
+  }
+}
+
+__device__ __forceinline__ uint32_t quad_max(uint32_t v) {
+  v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+  return max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
+}
+__device__ __forceinline__ uint32_t quad_or(uint32_t v) {
+  v |= __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+  return v | __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+}
+__device__ __forceinline__ uint32_t quad_and(uint32_t v) {
+  v &= __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+  return v & __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+}
+
+template <bool BF16, int TYPE>
+__global__ void __launch_bounds__(kThreads) mix_quantize_kernel(
+    const void* __restrict__ x, int64_t rows, int64_t nb, int64_t ld, int ebias, int asym,
+    uint8_t* __restrict__ codes, void* __restrict__ shared) {
+  const int q = threadIdx.x & 3;
+  const int64_t total = rows * nb;
+  const int64_t stride = (int64_t)gridDim.x * kQuadsPerCta;
+  for (int64_t base = (int64_t)blockIdx.x * kQuadsPerCta; base < total; base += stride * kUnroll) {
+    uint32_t u[kUnroll][8];
+    int64_t g[kUnroll];
+#pragma unroll
+    for (int r = 0; r < kUnroll; ++r) {
+      g[r] = base + r * stride + (threadIdx.x >> 2);
+      if (g[r] < total) {
+        const int64_t row = g[r] / nb, b = g[r] - row * nb;
+        load8<BF16>(x, row * ld + b * 32 + q * 8, u[r]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) u[r][i] = 0;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kUnroll; ++r) {
+      const uint32_t kl = max_key8(u[r]);
+      const uint32_t kb = quad_max(kl);
+      uint32_t word = 0x77777777u;
+      int emax = ebias, m3 = 0, m3l = 0;
+      if (kb != 0u) {
+        int f;
+        max_exp_mant(kb, &f, &m3);
+        emax = clampi(f, ebias, ebias + 15);
+        m3l = m3;
+        if (TYPE == 2) {
+          m3l = 0;
+          if (kl != 0u) { int fl; max_exp_mant(kl, &fl, &m3l); }
+        }
+        word = mix_codes8(u[r], emax, 8 + m3l, asym != 0);
+      }
+      const uint32_t lane_zero = (word == 0x77777777u) ? 1u : 0u;
+      if (TYPE == 2 && lane_zero) m3l = 0;
+      const uint32_t all_zero = quad_and(lane_zero);
+      const uint32_t m3_bits = quad_or((uint32_t)m3l << (4 + 3 * q));
+      if (g[r] < total) {
+        const int64_t row = g[r] / nb, b = g[r] - row * nb;
+        __stcs(reinterpret_cast<uint32_t*>(codes + row * nb * 16 + b * 16 + q * 4), word);
+        if (q == 0) {
+          const uint32_t ec = all_zero ? 0u : (uint32_t)(emax - ebias);
+          if (TYPE == 1) {
+            static_cast<uint8_t*>(shared)[g[r]] = (uint8_t)(all_zero ? 0u : (ec | ((uint32_t)m3 << 4)));
+          } else {
+            static_cast<uint16_t*>(shared)[g[r]] = (uint16_t)(all_zero ? 0u : (ec | m3_bits));
+          }
+        }
+      }
+    }
+  }
+}
+
+template <bool BF16, bool FP4>
+__global__ void __launch_bounds__(kThreads) mx_quantize_rows_kernel(
+    const void* __restrict__ x, int64_t rows, int64_t nb, int64_t ld, int floor_rule,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const int q = threadIdx.x & 3;
+  const int64_t total = rows * nb;
+  const int64_t stride = (int64_t)gridDim.x * kQuadsPerCta;
+  for (int64_t base = (int64_t)blockIdx.x * kQuadsPerCta; base < total; base += stride * kUnroll) {
+    uint32_t u[kUnroll][8];
+    int64_t g[kUnroll];
+#pragma unroll
+    for (int r = 0; r < kUnroll; ++r) {
+      g[r] = base + r * stride + (threadIdx.x >> 2);
+      if (g[r] < total) {
+        const int64_t row = g[r] / nb, b = g[r] - row * nb;
+        load8<BF16>(x, row * ld + b * 32 + q * 8, u[r]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) u[r][i] = 0;
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kUnroll; ++r) {
+      const uint32_t kb = quad_max(max_key8(u[r]));
+      uint32_t word = 0u, sc = 0u;
+      if (kb != 0u) {
+        const int X = mx_shared_exp(kb, FP4, floor_rule != 0);
+        word = mx_codes8(u[r], X, FP4);
+        sc = (uint32_t)(X + 127);
+      }
+      if (g[r] < total) {
+        const int64_t row = g[r] / nb, b = g[r] - row * nb;
+        __stcs(reinterpret_cast<uint32_t*>(codes + row * nb * 16 + b * 16 + q * 4), word);
+        if (q == 0) scales[g[r]] = (uint8_t)sc;
+      }
+    }
+  }
+}
+
+// axis 0: x is K x N row-major; block kb of column n is x[32kb .. 32kb+31][n].
+// A warp owns one k-block and 64 columns (two per lane): every load is a
+// contiguous 128-byte (bf16) or 256-byte (fp32) row segment.  The eight warps
+// of a CTA own eight consecutive k-blocks, so each column's 128 code bytes are
+// written by one CTA.
+template <bool BF16, bool FP4>
+__global__ void __launch_bounds__(kThreads) mx_quantize_cols_kernel(
+    const void* __restrict__ x, int64_t kdim, int64_t n, int64_t ld, int floor_rule,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t nbk = kdim / 32;
+  const int64_t kb = (int64_t)blockIdx.y * 8 + warp;
+  const int64_t n0 = (int64_t)blockIdx.x * 64 + 2 * lane;
+  if (kb >= nbk || n0 >= n) return;
+  const bool two = n0 + 1 < n;
+  uint32_t u0[32], u1[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int64_t off = (kb * 32 + i) * ld + n0;
+    if (BF16) {
+      const uint16_t* p = static_cast<const uint16_t*>(x) + off;
+      if (two) {
+        const uint32_t v = __ldcs(reinterpret_cast<const unsigned int*>(p));
+        u0[i] = v << 16;
+        u1[i] = v & 0xFFFF0000u;
+      } else {
+        u0[i] = (uint32_t)__ldcs(p) << 16;
+        u1[i] = 0;
+      }
+    } else {
+      const float* p = static_cast<const float*>(x) + off;
+      if (two) {
+        const float2 v = __ldcs(reinterpret_cast<const float2*>(p));
+        u0[i] = __float_as_uint(v.x);
+        u1[i] = __float_as_uint(v.y);
+      } else {
+        u0[i] = __float_as_uint(__ldcs(p));
+        u1[i] = 0;
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    if (c == 1 && !two) break;
+    const uint32_t* u = c ? u1 : u0;
+    uint32_t key = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) key = max(key, mag_key(u[i]));
+    uint4 w = make_uint4(0, 0, 0, 0);
+    uint32_t sc = 0;
+    if (key != 0u) {
+      const int X = mx_shared_exp(key, FP4, floor_rule != 0);
+      w.x = mx_codes8(u, X, FP4);
+      w.y = mx_codes8(u + 8, X, FP4);
+      w.z = mx_codes8(u + 16, X, FP4);
+      w.w = mx_codes8(u + 24, X, FP4);
+      sc = (uint32_t)(X + 127);
+    }
+    const int64_t col = n0 + c;
+    *reinterpret_cast<uint4*>(codes + col * (kdim / 2) + kb * 16) = w;
+    scales[col * nbk + kb] = (uint8_t)sc;
+  }
+}
+
+// Test aid: the dequantisation rule (-1)^s (1.mshared)_2 2^(Emax - de).
+__global__ void mix_dequant_kernel(const uint8_t* __restrict__ codes, const void* __restrict__ shared,
+                                   int64_t rows, int64_t k, int type, int ebias, float* __restrict__ out) {
+  const int64_t words = rows * (k / 8);
+  for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < words;
+       w += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = w / (k / 8), j = w - row * (k / 8);
+    const int64_t blk = row * (k / 32) + j / 4;
+    uint32_t ec, m3;
+    if (type == 1) {
+      const uint32_t s = static_cast<const uint8_t*>(shared)[blk];
+      ec = s & 0xF; m3 = (s >> 4) & 7;
+    } else {
+      const uint32_t s = static_cast<const uint16_t*>(shared)[blk];
+      ec = s & 0xF; m3 = (s >> (4 + 3 * (j & 3))) & 7;
+    }
+    const int emax = (int)ec + ebias;
+    const uint32_t cw = reinterpret_cast<const uint32_t*>(codes + row * (k / 2))[j];
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t c = (cw >> (4 * i)) & 0xF;
+      const int d = c & 7;
+      const float mag = ldexpf((float)(8 + m3), emax - 3 - d);
+      v[i] = (d == 7) ? ((c >> 3) ? mag : 0.0f) : ((c >> 3) ? -mag : mag);
+    }
+    float4* o = reinterpret_cast<float4*>(out + row * k + j * 8);
+    o[0] = make_float4(v[0], v[1], v[2], v[3]);
+    o[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+}
+
+__global__ void mx_dequant_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                                  int64_t rows, int64_t k, int fp4, float* __restrict__ out) {
+  const int64_t words = rows * (k / 8);
+  for (int64_t w = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; w < words;
+       w += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = w / (k / 8), j = w - row * (k / 8);
+    const int X = (int)scales[row * (k / 32) + j / 4] - 127;
+    const uint32_t cw = reinterpret_cast<const uint32_t*>(codes + row * (k / 2))[j];
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t c = (cw >> (4 * i)) & 0xF;
+      if (fp4) {
+        const uint32_t e = (c >> 1) & 3, m = c & 1;
+        const int half_units = e ? (int)((2 + m) << (e - 1)) : (int)m;  // value * 2
+        const float mag = ldexpf((float)half_units, X - 1);
+        v[i] = (c & 8) ? -mag : mag;
+      } else {
+        const int qv = (c & 8) ? (int)c - 16 : (int)c;
+        v[i] = ldexpf((float)qv, X - 2);
+      }
+    }
+    float4* o = reinterpret_cast<float4*>(out + row * k + j * 8);
+    o[0] = make_float4(v[0], v[1], v[2], v[3]);
+    o[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
+}
+
+int grid_for(int64_t quads) {
+  const int64_t want = (quads + kQuadsPerCta * kUnroll - 1) / (kQuadsPerCta * kUnroll);
+  const int64_t cap = (int64_t)num_sms() * 8;  // 8 resident CTAs of 256 threads per SM
+  int64_t g = want < cap ? want : cap;
+  return (int)(g > 0 ? g : 1);
+}
+
+}  // namespace
+
+cudaError_t launch_mix_quantize(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld,
+                                int type, int ebias, bool asym, uint8_t* codes, void* shared,
+                                cudaStream_t st) {
+  const int64_t nb = k / 32;
+  const int grid = grid_for(rows * nb);
+  if (bf16) {
+    if (type == 1) mix_quantize_kernel<true, 1><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared);
+    else mix_quantize_kernel<true, 2><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared);
+  } else {
+    if (type == 1) mix_quantize_kernel<false, 1><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared);
+    else mix_quantize_kernel<false, 2><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quantize_rows(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld,
+                                    bool fp4, bool floor_rule, uint8_t* codes, uint8_t* scales,
+                                    cudaStream_t st) {
+  const int64_t nb = k / 32;
+  const int grid = grid_for(rows * nb);
+  const int fr = floor_rule ? 1 : 0;
+  if (bf16) {
+    if (fp4) mx_quantize_rows_kernel<true, true><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales);
+    else mx_quantize_rows_kernel<true, false><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales);
+  } else {
+    if (fp4) mx_quantize_rows_kernel<false, true><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales);
+    else mx_quantize_rows_kernel<false, false><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_quantize_cols(const void* x, bool bf16, int64_t kdim, int64_t n, int64_t ld,
+                                    bool fp4, bool floor_rule, uint8_t* codes, uint8_t* scales,
+                                    cudaStream_t st) {
+  const dim3 grid((unsigned)((n + 63) / 64), (unsigned)((kdim / 32 + 7) / 8));
+  const int fr = floor_rule ? 1 : 0;
+  if (bf16) {
+    if (fp4) mx_quantize_cols_kernel<true, true><<<grid, kThreads, 0, st>>>(x, kdim, n, ld, fr, codes, scales);
+    else mx_quantize_cols_kernel<true, false><<<grid, kThreads, 0, st>>>(x, kdim, n, ld, fr, codes, scales);
+  } else {
+    if (fp4) mx_quantize_cols_kernel<false, true><<<grid, kThreads, 0, st>>>(x, kdim, n, ld, fr, codes, scales);
+    else mx_quantize_cols_kernel<false, false><<<grid, kThreads, 0, st>>>(x, kdim, n, ld, fr, codes, scales);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mix_dequantize(const uint8_t* codes, const void* shared, int64_t rows, int64_t k,
+                                  int type, int ebias, float* out, cudaStream_t st) {
+  const int64_t words = rows * (k / 8);
+  int64_t g = (words + 255) / 256;
+  if (g > (int64_t)num_sms() * 16) g = (int64_t)num_sms() * 16;
+  mix_dequant_kernel<<<(int)(g > 0 ? g : 1), 256, 0, st>>>(codes, shared, rows, k, type, ebias, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t k,
+                                 bool fp4, float* out, cudaStream_t st) {
+  const int64_t words = rows * (k / 8);
+  int64_t g = (words + 255) / 256;
+  if (g > (int64_t)num_sms() * 16) g = (int64_t)num_sms() * 16;
+  mx_dequant_kernel<<<(int)(g > 0 ? g : 1), 256, 0, st>>>(codes, scales, rows, k, fp4 ? 1 : 0, out);
+  return cudaGetLastError();
+}
+
+}  // namespace mixk

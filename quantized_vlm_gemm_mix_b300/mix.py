@@ -1,0 +1,245 @@
+"""Thin ctypes binding of libmix.so (include/mix.h).
+
+Argument marshalling only: every step of the hot path runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors (PyTorch supplies device memory
+and streams); the calls are asynchronous on the current torch stream unless a
+stream is given.  There is no CPU fallback: importing this module without the
+built library, or calling it on a machine without a GPU, raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmix.so")
+
+# enums and flags (mirror include/mix.h)
+MIX_OK, MIX_ERR_INVALID_ARG, MIX_ERR_SHAPE, MIX_ERR_ALIGN = 0, 1, 2, 3
+MIX_ERR_UNSUPPORTED, MIX_ERR_CUDA, MIX_ERR_WORKSPACE, MIX_ERR_DEVICE = 4, 5, 6, 7
+MIX_T1_4P25, MIX_T2_4P5 = 1, 2
+MX_INT4, MX_FP4_E2M1 = 0, 1
+MIX_DT_F32, MIX_DT_BF16 = 0, 1
+MIX_ASYM_ZERO, MX_SCALE_FLOOR = 1, 2
+MIX_EPI_NONE, MIX_EPI_MIX_T1, MIX_EPI_MIX_T2, MIX_EPI_MXINT4, MIX_EPI_MXFP4 = 0, 1, 2, 3, 4
+MIX_GEMM_AUTO, MIX_GEMM_TCGEN05, MIX_GEMM_SHIFTADD = 0, 1, 2
+KSMOOTH_COMPUTE, KSMOOTH_APPLY_FROZEN = 0, 1
+
+EXPORTS = ["mix_codes_bytes", "mix_shared_bytes", "mx_scales_bytes", "mix_quantize", "mx_quantize",
+           "mix_dequantize", "mx_dequantize", "mix_mx_gemm_workspace_bytes", "mix_mx_gemm",
+           "ksmooth_workspace_bytes", "ksmooth_kv", "mix_status_str", "mix_device_error", "mix_version"]
+
+
+class MixError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {status_str(status)} (status {status})")
+        self.status = status
+
+
+class GemmDesc(ctypes.Structure):
+    """mix_gemm_desc_t."""
+    _fields_ = [
+        ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+        ("batch", ctypes.c_int64), ("b_group", ctypes.c_int64),
+        ("a_codes", ctypes.c_void_p), ("a_shared", ctypes.c_void_p),
+        ("a_type", ctypes.c_int), ("a_ebias", ctypes.c_int),
+        ("a_ld", ctypes.c_int64), ("a_batch_stride", ctypes.c_int64),
+        ("b_codes", ctypes.c_void_p), ("b_scales", ctypes.c_void_p), ("b_type", ctypes.c_int),
+        ("b_ld", ctypes.c_int64), ("b_batch_stride", ctypes.c_int64),
+        ("c", ctypes.c_void_p), ("ldc", ctypes.c_int64), ("c_batch_stride", ctypes.c_int64),
+        ("epi", ctypes.c_int), ("epi_ebias", ctypes.c_int), ("epi_flags", ctypes.c_uint),
+        ("out_codes", ctypes.c_void_p), ("out_shared", ctypes.c_void_p),
+        ("out_ld", ctypes.c_int64), ("out_batch_stride", ctypes.c_int64),
+        ("algo", ctypes.c_int),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmix.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I64, I, U, S = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+    sig = {
+        "mix_codes_bytes": (S, [I64, I64]),
+        "mix_shared_bytes": (S, [I, I64, I64]),
+        "mx_scales_bytes": (S, [I64, I64]),
+        "mix_quantize": (I, [P, I, I64, I64, I64, I, I, U, P, P, P]),
+        "mx_quantize": (I, [P, I, I64, I64, I64, I, I, U, P, P, P]),
+        "mix_dequantize": (I, [P, P, I64, I64, I, I, P, P]),
+        "mx_dequantize": (I, [P, P, I64, I64, I, P, P]),
+        "mix_mx_gemm_workspace_bytes": (S, [ctypes.POINTER(GemmDesc)]),
+        "mix_mx_gemm": (I, [ctypes.POINTER(GemmDesc), P, S, P]),
+        "ksmooth_workspace_bytes": (S, [I64, I, I]),
+        "ksmooth_kv": (I, [P, I, I64, I, I, I64, P, I, P, P, S, P]),
+        "mix_status_str": (ctypes.c_char_p, [I]),
+        "mix_device_error": (I, [ctypes.POINTER(ctypes.c_uint), I]),
+        "mix_version": (I, []),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
+lib = _load()
+
+
+def status_str(status: int) -> str:
+    return lib.mix_status_str(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != MIX_OK:
+        raise MixError(status, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    if not t.is_cuda:
+        raise ValueError("libmix takes CUDA tensors (device pointers)")
+    return t.data_ptr()
+
+
+def _dtype(t) -> int:
+    if t.dtype == torch.float32:
+        return MIX_DT_F32
+    if t.dtype == torch.bfloat16:
+        return MIX_DT_BF16
+    raise TypeError(f"unsupported input dtype {t.dtype}")
+
+
+# ----------------------------------------------------------------------------
+# 1:1 wrappers (same names as the C ABI)
+# ----------------------------------------------------------------------------
+
+def mix_codes_bytes(rows: int, k: int) -> int:
+    return lib.mix_codes_bytes(rows, k)
+
+
+def mix_shared_bytes(mix_type: int, rows: int, k: int) -> int:
+    return lib.mix_shared_bytes(mix_type, rows, k)
+
+
+def mx_scales_bytes(rows: int, k: int) -> int:
+    return lib.mx_scales_bytes(rows, k)
+
+
+def mix_quantize(x, rows, k, ld, mix_type, ebias, flags, codes, shared, stream=None) -> None:
+    _check(lib.mix_quantize(_ptr(x), _dtype(x), rows, k, ld, mix_type, ebias, flags, _ptr(codes),
+                            _ptr(shared), _stream(stream)), "mix_quantize")
+
+
+def mx_quantize(x, rows, cols, ld, axis, mx_type, flags, codes, scales, stream=None) -> None:
+    _check(lib.mx_quantize(_ptr(x), _dtype(x), rows, cols, ld, axis, mx_type, flags, _ptr(codes),
+                           _ptr(scales), _stream(stream)), "mx_quantize")
+
+
+def mix_dequantize(codes, shared, rows, k, mix_type, ebias, out, stream=None) -> None:
+    _check(lib.mix_dequantize(_ptr(codes), _ptr(shared), rows, k, mix_type, ebias, _ptr(out),
+                              _stream(stream)), "mix_dequantize")
+
+
+def mx_dequantize(codes, scales, rows, k, mx_type, out, stream=None) -> None:
+    _check(lib.mx_dequantize(_ptr(codes), _ptr(scales), rows, k, mx_type, _ptr(out), _stream(stream)),
+           "mx_dequantize")
+
+
+def mix_mx_gemm_workspace_bytes(desc: GemmDesc) -> int:
+    return lib.mix_mx_gemm_workspace_bytes(ctypes.byref(desc))
+
+
+def mix_mx_gemm(desc: GemmDesc, workspace=None, stream=None) -> None:
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.mix_mx_gemm(ctypes.byref(desc), _ptr(workspace), ws_bytes, _stream(stream)), "mix_mx_gemm")
+
+
+def ksmooth_workspace_bytes(tokens: int, heads: int, head_dim: int) -> int:
+    return lib.ksmooth_workspace_bytes(tokens, heads, head_dim)
+
+
+def ksmooth_kv(k, tokens, heads, head_dim, ld, mean, mode, k_out, workspace=None, stream=None) -> None:
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.ksmooth_kv(_ptr(k), _dtype(k), tokens, heads, head_dim, ld, _ptr(mean), mode, _ptr(k_out),
+                          _ptr(workspace), ws_bytes, _stream(stream)), "ksmooth_kv")
+
+
+def mix_device_error(clear: bool = True) -> int:
+    w = ctypes.c_uint(0)
+    _check(lib.mix_device_error(ctypes.byref(w), 1 if clear else 0), "mix_device_error")
+    return w.value
+
+
+def mix_version() -> int:
+    return lib.mix_version()
+
+
+# ----------------------------------------------------------------------------
+# Allocating helpers (torch owns the memory)
+# ----------------------------------------------------------------------------
+
+def quantize_mix(x: torch.Tensor, mix_type: int = MIX_T2_4P5, ebias: int = -8, flags: int = MIX_ASYM_ZERO,
+                 stream=None):
+    """x [rows, k] (row stride x.stride(0)) -> (codes uint8 [rows, k/2], shared [rows, k/32])."""
+    rows, k = x.shape
+    assert x.stride(1) == 1
+    codes = torch.empty((rows, k // 2), dtype=torch.uint8, device=x.device)
+    shared = torch.empty((rows, k // 32), dtype=torch.uint8 if mix_type == MIX_T1_4P25 else torch.int16,
+                         device=x.device)
+    mix_quantize(x, rows, k, x.stride(0), mix_type, ebias, flags, codes, shared, stream)
+    return codes, shared
+
+
+def quantize_mx(x: torch.Tensor, axis: int, mx_type: int, flags: int = 0, stream=None):
+    """axis=1: x [N, K]; axis=0: x [K, N] -> (codes [N, K/2], scales [N, K/32])."""
+    rows, cols = x.shape
+    assert x.stride(1) == 1
+    N, K = (rows, cols) if axis == 1 else (cols, rows)
+    codes = torch.empty((N, K // 2), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((N, K // 32), dtype=torch.uint8, device=x.device)
+    mx_quantize(x, rows, cols, x.stride(0), axis, mx_type, flags, codes, scales, stream)
+    return codes, scales
+
+
+def gemm_desc(M, N, K, a_codes, a_shared, a_type, a_ebias, b_codes, b_scales, b_type, c=None,
+              epi=MIX_EPI_NONE, epi_ebias=-8, epi_flags=MIX_ASYM_ZERO, out_codes=None, out_shared=None,
+              batch=1, b_group=1, a_ld=None, a_batch_stride=None, b_ld=None, b_batch_stride=None,
+              ldc=None, c_batch_stride=None, out_ld=None, out_batch_stride=None, algo=MIX_GEMM_AUTO) -> GemmDesc:
+    d = GemmDesc()
+    d.M, d.N, d.K, d.batch, d.b_group = M, N, K, batch, b_group
+    d.a_codes, d.a_shared, d.a_type, d.a_ebias = _ptr(a_codes), _ptr(a_shared), a_type, a_ebias
+    d.a_ld = K if a_ld is None else a_ld
+    d.a_batch_stride = M * d.a_ld if a_batch_stride is None else a_batch_stride
+    d.b_codes, d.b_scales, d.b_type = _ptr(b_codes), _ptr(b_scales), b_type
+    d.b_ld = K if b_ld is None else b_ld
+    d.b_batch_stride = N * d.b_ld if b_batch_stride is None else b_batch_stride
+    d.c = _ptr(c)
+    d.ldc = N if ldc is None else ldc
+    d.c_batch_stride = M * d.ldc if c_batch_stride is None else c_batch_stride
+    d.epi, d.epi_ebias, d.epi_flags = epi, epi_ebias, epi_flags
+    d.out_codes, d.out_shared = _ptr(out_codes), _ptr(out_shared)
+    d.out_ld = N if out_ld is None else out_ld
+    d.out_batch_stride = M * d.out_ld if out_batch_stride is None else out_batch_stride
+    d.algo = algo
+    return d
+
+
+def gemm(desc: GemmDesc, device=None, stream=None) -> None:
+    """mix_mx_gemm with a workspace allocated by torch when one is needed."""
+    need = mix_mx_gemm_workspace_bytes(desc)
+    ws = None
+    if need:
+        ws = torch.empty(need, dtype=torch.uint8, device=device or torch.device("cuda"))
+    mix_mx_gemm(desc, ws, stream)
+    return ws

@@ -1,0 +1,186 @@
+"""GPU parity of the quantiser kernels against the CPU oracle: bit-exact codes
+and packed bytes (MiX-4.25b / MiX-4.5b, MXINT4 / MXFP4 along rows and down
+columns), on the paper-shaped workloads and on edge cases."""
+import numpy as np
+import pytest
+
+from quantized_vlm_gemm_mix_b300 import synth
+from helpers import to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mix():
+    import torch
+    assert torch.cuda.is_available()
+    from quantized_vlm_gemm_mix_b300 import mix as m
+    return m
+
+
+def gpu_mix(mix, x_np, mix_type, ebias=-8, flags=1):
+    codes, shared = mix.quantize_mix(to_dev(x_np), mix_type, ebias, flags)
+    return to_host(codes), to_host(shared)
+
+
+def check_mix(mix, orc, x_np, mix_type, ebias=-8, flags=1):
+    c_ref, s_ref = orc.mix_quantize(x_np, mix_type, ebias, flags)
+    c, s = gpu_mix(mix, x_np, mix_type, ebias, flags)
+    assert np.array_equal(c, c_ref), f"codes differ at {np.argwhere(c != c_ref)[:5]}"
+    assert np.array_equal(s.astype(s_ref.dtype), s_ref), f"shared differs at {np.argwhere(s != s_ref)[:5]}"
+
+
+# ---------------------------------------------------------------------------
+# MiX
+
+
+def test_mix_tiny_fp32_config(mix, orc):
+    """fp32 A [128 x 512]: visual rows with 4 outlier channels x30, text rows."""
+    a = synth.to_f32(synth.vlm_activations(0, 0, 128, 512, visual_rows=96, n_outlier=4))
+    for t in (1, 2):
+        check_mix(mix, orc, a, t)
+
+
+@pytest.mark.parametrize("t", [1, 2])
+def test_mix_quantizer_sweep_bf16_full(mix, orc, t):
+    """bf16 activations 4096 x 3584 (3072 visual rows, 1% outlier channels x30)."""
+    a = synth.to_bf16_bits(synth.vlm_activations(0, 1, 4096, 3584, visual_rows=3072))
+    check_mix(mix, orc, a, t)
+
+
+@pytest.mark.parametrize("rows,k", [(1, 32), (3, 96), (7, 160), (33, 224), (5, 4128)])
+@pytest.mark.parametrize("t", [1, 2])
+@pytest.mark.parametrize("asym", [0, 1])
+def test_mix_ragged_shapes(mix, orc, rows, k, t, asym):
+    a = synth.to_bf16_bits(synth.vlm_activations(3, rows, rows, k, visual_rows=rows // 2 + 1))
+    check_mix(mix, orc, a, t, flags=asym)
+    f = synth.to_f32(synth.laplace(4, rows, rows * k, 0.5).reshape(rows, k))
+    check_mix(mix, orc, f, t, ebias=-12, flags=asym)
+
+
+def test_mix_edge_values(mix, orc):
+    """Zeros, NaN, +-Inf, subnormals, saturation above 2^(ebias+15), values far
+    below 2^ebias, and every bf16 magnitude of a 12-binade window."""
+    rng = np.random.default_rng(5)
+    blocks = []
+    z = np.zeros(32, np.float32)
+    blocks.append(z.copy())
+    b = z.copy(); b[3] = np.nan; blocks.append(b)
+    b = z.copy(); b[0] = np.inf; b[1] = -np.inf; b[2] = 1.0; b[5] = np.nan; blocks.append(b)
+    b = (rng.standard_normal(32) * 1e-41).astype(np.float32); blocks.append(b)       # subnormal fp32
+    b = (rng.standard_normal(32) * 1e6).astype(np.float32); blocks.append(b)         # saturates
+    b = (rng.standard_normal(32) * 1e-9).astype(np.float32); blocks.append(b)        # under 2^ebias
+    b = z.copy(); b[:8] = 1e-30; b[8:] = rng.standard_normal(24); blocks.append(b)   # one dead sub-block
+    b = z.copy(); b[0] = 1.9375; b[1:] = rng.standard_normal(31) * 0.1; blocks.append(b)  # carry
+    x = np.stack(blocks).astype(np.float32)
+    for t in (1, 2):
+        for flags in (0, 1):
+            check_mix(mix, orc, x, t, flags=flags)
+            check_mix(mix, orc, x, t, ebias=-100, flags=flags)
+            check_mix(mix, orc, x, t, ebias=100, flags=flags)
+    bits = np.arange(0x3A00, 0x4000 + 0x600, dtype=np.uint32)
+    bits = np.concatenate([bits, bits | 0x8000]).astype(np.uint16)
+    bits = bits[: (len(bits) // 31) * 31].reshape(-1, 31)
+    for m3 in range(8):
+        head = np.full((bits.shape[0], 1), (127 << 7) | (m3 << 4), dtype=np.uint16)
+        xb = np.concatenate([head, bits], axis=1)
+        for t in (1, 2):
+            check_mix(mix, orc, xb, t)
+
+
+def test_mix_strided_input(mix, orc):
+    import torch
+    a = synth.to_bf16_bits(synth.vlm_activations(8, 0, 64, 512, visual_rows=48))
+    big = np.zeros((64, 640), np.uint16)
+    big[:, :512] = a
+    x = to_dev(big)
+    codes = torch.empty((64, 256), dtype=torch.uint8, device="cuda")
+    shared = torch.empty((64, 16), dtype=torch.int16, device="cuda")
+    mix.mix_quantize(x, 64, 512, 640, mix.MIX_T2_4P5, -8, 1, codes, shared)
+    c_ref, s_ref = orc.mix_quantize(a, 2)
+    assert np.array_equal(to_host(codes), c_ref) and np.array_equal(to_host(shared), s_ref)
+
+
+def test_mix_dequantize_matches_oracle(mix, orc):
+    import torch
+    a = synth.to_bf16_bits(synth.vlm_activations(9, 0, 64, 256, visual_rows=40))
+    for t in (1, 2):
+        c, s = orc.mix_quantize(a, t)
+        out = torch.empty((64, 256), dtype=torch.float32, device="cuda")
+        mix.mix_dequantize(to_dev(c), to_dev(s), 64, 256, t, -8, out)
+        assert np.array_equal(to_host(out).astype(np.float64), orc.mix_dequantize(c, s, t))
+
+
+# ---------------------------------------------------------------------------
+# MX
+
+
+def check_mx(mix, orc, x_np, axis, t, flags=0):
+    c_ref, s_ref = orc.mx_quantize(x_np, axis, t, flags)
+    c, s = mix.quantize_mx(to_dev(x_np), axis, t, flags)
+    c, s = to_host(c), to_host(s)
+    assert np.array_equal(c, c_ref), f"codes differ at {np.argwhere(c != c_ref)[:5]}"
+    assert np.array_equal(s, s_ref), f"scales differ at {np.argwhere(s != s_ref)[:5]}"
+
+
+@pytest.mark.parametrize("axis", [0, 1])
+@pytest.mark.parametrize("t", [0, 1])
+def test_mx_tiny_weights(mix, orc, axis, t):
+    w = synth.to_f32(synth.gaussian_weights(0, 2, 512, 256))
+    x = w if axis == 0 else np.ascontiguousarray(w.T)
+    check_mx(mix, orc, x, axis, t)
+    check_mx(mix, orc, x, axis, t, flags=2)
+
+
+@pytest.mark.parametrize("t", [0, 1])
+def test_mx_sweep_weights_full_sampled(mix, orc, t):
+    """bf16 W 3584 x 18944 quantised down its columns on the GPU; every code of
+    a sampled set of 512 columns checked against the oracle."""
+    w = synth.to_bf16_bits(synth.gaussian_weights(0, 3, 3584, 18944))
+    c, s = mix.quantize_mx(to_dev(w), 0, t)
+    c, s = to_host(c), to_host(s)
+    cols = np.sort(np.random.default_rng(0).choice(18944, 512, replace=False))
+    c_ref, s_ref = orc.mx_quantize(np.ascontiguousarray(w[:, cols]), 0, t)
+    assert np.array_equal(c[cols], c_ref) and np.array_equal(s[cols], s_ref)
+
+
+@pytest.mark.parametrize("shape", [(32, 1), (64, 63), (96, 130), (4128, 5)])
+@pytest.mark.parametrize("t", [0, 1])
+def test_mx_cols_ragged(mix, orc, shape, t):
+    kdim, n = shape
+    ldn = (n + 7) // 8 * 8
+    w = synth.to_bf16_bits(synth.normal(1, n, kdim * ldn, 0, 0.02).reshape(kdim, ldn))
+    import torch
+    x = to_dev(w)
+    codes = torch.empty((n, kdim // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty((n, kdim // 32), dtype=torch.uint8, device="cuda")
+    mix.mx_quantize(x, kdim, n, ldn, 0, t, 0, codes, scales)
+    c_ref, s_ref = orc.mx_quantize(np.ascontiguousarray(w[:, :n]), 0, t)
+    assert np.array_equal(to_host(codes), c_ref) and np.array_equal(to_host(scales), s_ref)
+
+
+def test_mx_edge_values(mix, orc):
+    rng = np.random.default_rng(6)
+    rows = [np.zeros(32, np.float32)]
+    b = np.zeros(32, np.float32); b[2] = np.nan; b[3] = 1.0; rows.append(b)
+    b = rng.standard_normal(32).astype(np.float32); b[4] = np.inf; b[9] = -np.inf; rows.append(b)
+    rows.append((rng.standard_normal(32) * 1e-40).astype(np.float32))
+    rows.append((rng.standard_normal(32) * 3e38).astype(np.float32))
+    rows.append(np.linspace(-7.5, 7.5, 32).astype(np.float32))
+    b = np.full(32, 0.25, np.float32); b[0] = 4.0; rows.append(b)
+    rows.append(np.linspace(-6.5, 0.25, 32).astype(np.float32))
+    x = np.stack(rows)                      # 8 rows: the transposed copy has ld = 8
+    for t in (0, 1):
+        for flags in (0, 2):
+            check_mx(mix, orc, x, 1, t, flags)
+            check_mx(mix, orc, np.ascontiguousarray(x.T), 0, t, flags)
+
+
+def test_mx_dequantize_matches_oracle(mix, orc):
+    import torch
+    w = synth.to_bf16_bits(synth.gaussian_weights(2, 2, 128, 96))
+    for t in (0, 1):
+        c, s = orc.mx_quantize(w, 0, t)
+        out = torch.empty((96, 128), dtype=torch.float32, device="cuda")
+        mix.mx_dequantize(to_dev(c), to_dev(s), 96, 128, t, out)
+        assert np.array_equal(to_host(out).astype(np.float64), orc.mx_dequantize(c, s, t))
