@@ -1,8 +1,35 @@
-// tcgen05 tensor-core path of the A-MiX x W-MX matmul (placeholder until the
-// kernel lands) and the per-device error word used by bounded waits.
+// tcgen05 tensor-core path of the A-MiX x W-MX matmul (sm_103a).
+//
+// Eq. (6) of the pchao.org digest of "MiX: Micro-Inverted-Scaling ..."
+// (Method section, dual-format matmul bullet) factors the shared MiX mantissa
+// and both block exponents out of each 32-element block product.  On the
+// tensor core that factorisation reads right to left: every MiX element is
+// decoded exactly to e4m3 as +-(1.mshared) * 2^(1 - de) (always a normal
+// e4m3: de in 0..7 maps to exponents 1..-6, the mantissa is mshared), the
+// block's 2^(Emax - 1) becomes the UE8M0 block scale of A, and the W-MX
+// element (E2M1 value, or q/4 for MXINT4) with its 2^X scale becomes B and
+// its UE8M0 scale.  tcgen05.mma.kind::mxf8f6f4.block_scale then forms the
+// same products exactly and accumulates in fp32 in TMEM.  mshared must stay
+// inside the element: a block scale has to be a power of two.
+//
+// CTA tile 128 (M) x 256 (N) x 128 (K per stage = four 32-blocks = four MMAs
+// of K 32), one CTA per tile.  Warp roles:
+//   warp 0      TMA producer: packed A and B code tiles into a 4-deep ring.
+//   warp 1      TMEM allocator and the single MMA-issuing thread.
+//   warps 4-11  decoders: nibbles -> e4m3 in the 128-byte-swizzled K-major
+//               operand layout (2-deep ring); block scales -> TMEM; then
+//               warps 4-7 run the epilogue (tcgen05.ld, optional fp32 store,
+//               optional fused MiX/MX quantiser of each 32-column block).
+// Every wait is bounded; a wait that runs out sets the device error word and
+// the CTA drains and exits.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <cstdint>
+
+#include "mix_common.cuh"
 #include "mix_internal.h"
+#include "tc_ptx.cuh"
 
 namespace mixk {
 
@@ -20,10 +47,450 @@ cudaError_t read_device_error(unsigned* word, bool clear) {
   return e;
 }
 
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 128;
+constexpr int KB = BK / 2;  // code bytes per row per stage
+constexpr int S_CODES = 4, S_OPS = 2;
+constexpr int A_CODES = BM * KB, B_CODES = BN * KB;  // 8 KB, 16 KB
+constexpr int A_OPS = BM * BK, B_OPS = BN * BK;      // 16 KB, 32 KB
+constexpr int NUM_THREADS = 384;
+constexpr int DEC_WARP0 = 4, NUM_DEC_WARPS = 8;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SF_COL = 256;  // stage s: A scales at SF_COL + 16 s (4 cols), B at + 4 (8 cols)
+constexpr long long WAIT_LIMIT = 1LL << 31;  // SM clocks, about one second
+
+// Shared memory plan (offsets from a 1024-byte aligned base).
+constexpr int OFF_AOPS = 0;
+constexpr int OFF_BOPS = OFF_AOPS + S_OPS * A_OPS;
+constexpr int OFF_ACODES = OFF_BOPS + S_OPS * B_OPS;
+constexpr int OFF_BCODES = OFF_ACODES + S_CODES * A_CODES;
+constexpr int OFF_SFA = OFF_BCODES + S_CODES * B_CODES;  // [S_OPS][BM] scale words
+constexpr int OFF_SFB = OFF_SFA + S_OPS * BM * 4;        // [S_OPS][BN]
+constexpr int OFF_BAR = OFF_SFB + S_OPS * BN * 4;
+constexpr int NUM_BARS = 2 * S_CODES + 3 * S_OPS + 2;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for the 1024-byte alignment
+
+struct TcParams {
+  int64_t M, N, K, batch, b_group;
+  const void* a_shared;
+  int64_t a_ld, a_bs;
+  int a_type, a_ebias, b_fp4;
+  const uint8_t* b_scales;
+  int64_t b_ld, b_bs;
+  float* c;
+  int64_t ldc, cbs;
+  int epi, epi_ebias;
+  unsigned epi_flags;
+  uint8_t* out_codes;
+  void* out_shared;
+  int64_t out_ld, out_bs;
+};
+
+// ------------------------------------------------------------------ decode
+// Four MiX nibbles (low 16 bits of v) -> four e4m3 bytes +-(1.m3) 2^(1-de);
+// 0x7 -> 0, 0xF (recycled -0) -> +(1.m3) 2^-6.
+__device__ __forceinline__ uint32_t mix_to_e4m3_x4(uint32_t v, uint32_t m3) {
+  const uint32_t m3x = m3 * 0x01010101u;
+  const uint32_t mag = ptx::prmt(0x28303840u | m3x, 0x00101820u | (m3 * 0x00010101u), v & 0x7777u);
+  const uint32_t z = ptx::prmt(0u, 0x80000000u, v & 0xFFFFu);  // 0xFF at 0xF, 0x80 at 0x7
+  const uint32_t t = ptx::prmt(v, 0u, 0x1100u);
+  const uint32_t sgn = (t & 0x80008000u) | ((t << 4) & 0x00800080u);
+  const uint32_t asym = z & 0x7F7F7F7Fu & (0x08080808u | m3x);
+  return mag | asym | (sgn & ~z & 0x80808080u);
+}
+// Four E2M1 nibbles -> e4m3.
+__device__ __forceinline__ uint32_t fp4_to_e4m3_x4(uint32_t v) {
+  const uint32_t mag = ptx::prmt(0x3C383000u, 0x4C484440u, v & 0x7777u);
+  const uint32_t t = ptx::prmt(v, 0u, 0x1100u);
+  return mag | (t & 0x80008000u) | ((t << 4) & 0x00800080u);
+}
+// Four INT4 nibbles (two's complement q) -> e4m3 of q / 4.
+__device__ __forceinline__ uint32_t int4_to_e4m3_x4(uint32_t v) {
+  const uint32_t sel = v & 0x7777u;
+  const uint32_t pos = ptx::prmt(0x34302800u, 0x3E3C3A38u, sel);
+  const uint32_t neg = ptx::prmt(0xBABCBEC0u, 0xA8B0B4B8u, sel);
+  uint32_t m = ptx::prmt(0x80808080u, 0x80808080u, v & 0xFFFFu) ^ 0x80808080u;  // 0x7F where negative
+  m |= (m << 1) & 0x80808080u;
+  return (pos & ~m) | (neg & m);
+}
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a K-major operand tile
+// with 128-byte rows and the 128-byte swizzle (chunk index XOR row mod 8).
+__device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
+  return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void flag_error(unsigned bit, volatile int* abort_flag) {
+  atomicOr(&g_mix_device_error, bit);
+  *abort_flag = 1;
+}
+
+// ----------------------------------------------------------- fused epilogue
+// Quantise one 32-column block of one output row held by one thread.
+__device__ __forceinline__ void epi_quant_block(const uint32_t* u, const TcParams& p, uint4& codes,
+                                                uint32_t& shared) {
+  uint32_t ks[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) ks[s] = max_key8(u + 8 * s);
+  const uint32_t kb = max(max(ks[0], ks[1]), max(ks[2], ks[3]));
+  uint32_t w[4] = {0, 0, 0, 0};
+  shared = 0;
+  if (p.epi == MIX_EPI_MIX_T1 || p.epi == MIX_EPI_MIX_T2) {
+    const bool asym = (p.epi_flags & MIX_ASYM_ZERO) != 0;
+    if (kb == 0u) {
+      w[0] = w[1] = w[2] = w[3] = 0x77777777u;
+    } else {
+      int f, m3;
+      max_exp_mant(kb, &f, &m3);
+      const int emax = clampi(f, p.epi_ebias, p.epi_ebias + 15);
+      uint32_t m3bits = 0;
+      bool all_zero = true;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        int ms = m3;
+        if (p.epi == MIX_EPI_MIX_T2) {
+          ms = 0;
+          if (ks[s] != 0u) { int fs; max_exp_mant(ks[s], &fs, &ms); }
+        }
+        w[s] = mix_codes8(u + 8 * s, emax, 8 + ms, asym);
+        const bool z = w[s] == 0x77777777u;
+        all_zero &= z;
+        if (z) ms = 0;
+        m3bits |= (uint32_t)ms << (4 + 3 * s);
+      }
+      if (!all_zero) {
+        const uint32_t ec = (uint32_t)(emax - p.epi_ebias);
+        shared = (p.epi == MIX_EPI_MIX_T1) ? (ec | ((uint32_t)m3 << 4)) : (ec | m3bits);
+      }
+    }
+  } else {
+    const bool fp4 = p.epi == MIX_EPI_MXFP4;
+    if (kb != 0u) {
+      const int X = mx_shared_exp(kb, fp4, (p.epi_flags & MX_SCALE_FLOOR) != 0);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) w[s] = mx_codes8(u + 8 * s, X, fp4);
+      shared = (uint32_t)(X + 127);
+    }
+  }
+  codes = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                   const TcParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* codes_full = bars;
+  uint64_t* codes_empty = bars + S_CODES;
+  uint64_t* ops_full = bars + 2 * S_CODES;
+  uint64_t* ops_empty = bars + 2 * S_CODES + S_OPS;
+  uint64_t* sf_ready = bars + 2 * S_CODES + 2 * S_OPS;
+  uint64_t* acc_full = bars + 2 * S_CODES + 3 * S_OPS;
+  uint64_t* drain = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  volatile int* never = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);  // drains ignore aborts
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m0 = (int64_t)blockIdx.x * BM, n0 = (int64_t)blockIdx.y * BN, bt = blockIdx.z;
+  const int num_k = (int)((p.K + BK - 1) / BK);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S_CODES; ++i) { ptx::mbar_init(&codes_full[i], 1); ptx::mbar_init(&codes_empty[i], NUM_DEC_WARPS); }
+    for (int i = 0; i < S_OPS; ++i) {
+      ptx::mbar_init(&ops_full[i], NUM_DEC_WARPS);
+      ptx::mbar_init(&ops_empty[i], 1);
+      ptx::mbar_init(&sf_ready[i], NUM_DEC_WARPS);
+    }
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    *never = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmap_a);
+    ptx::prefetch_tmap(&tmap_b);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int kt = 0; kt < num_k; ++kt) {
+        const int s = kt % S_CODES, n = kt / S_CODES;
+        if (n > 0 && !ptx::mbar_wait(&codes_empty[s], (n - 1) & 1, WAIT_LIMIT, abort_flag)) { flag_error(1u, abort_flag); break; }
+        if (*abort_flag) break;
+        ptx::mbar_arrive_expect_tx(&codes_full[s], A_CODES + B_CODES);
+        ptx::tma_load_3d(smem + OFF_ACODES + s * A_CODES, &tmap_a, &codes_full[s], kt * KB, (int)m0, (int)bt);
+        ptx::tma_load_3d(smem + OFF_BCODES + s * B_CODES, &tmap_b, &codes_full[s], kt * KB, (int)n0,
+                         (int)(bt / p.b_group));
+        ++issued;
+      }
+      // drain: every issued copy lands before the CTA may exit
+      for (int kt = (issued > S_CODES ? issued - S_CODES : 0); kt < issued; ++kt)
+        ptx::mbar_wait(&codes_full[kt % S_CODES], (kt / S_CODES) & 1, WAIT_LIMIT, never);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t b_fmt = 0;  // B decoded to E4M3
+      for (int kt = 0; kt < num_k; ++kt) {
+        const int s = kt % S_OPS, n = kt / S_OPS;
+        if (!ptx::mbar_wait(&ops_full[s], n & 1, WAIT_LIMIT, abort_flag)) { flag_error(2u, abort_flag); break; }
+        if (*abort_flag) break;
+        ptx::tc_fence_after();
+        const uint32_t a_addr = ptx::smem_u32(smem + OFF_AOPS + s * A_OPS);
+        const uint32_t b_addr = ptx::smem_u32(smem + OFF_BOPS + s * B_OPS);
+        const uint32_t sfa = tmem + SF_COL + 16u * s, sfb = sfa + 4u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          ptx::mma_mxf8f6f4(tmem, ptx::sdesc_sw128(a_addr + 32u * j), ptx::sdesc_sw128(b_addr + 32u * j),
+                            ptx::idesc_mxf8(BM, BN, 0u, b_fmt, (uint32_t)j), sfa, sfb, (kt > 0 || j > 0) ? 1u : 0u);
+        }
+        ptx::tc_commit(&ops_empty[s]);
+      }
+      ptx::tc_commit(acc_full);
+      ptx::tc_commit(drain);
+      ptx::mbar_wait(drain, 0, WAIT_LIMIT, never);
+    }
+  } else if (warp >= DEC_WARP0) {
+    // ------------------------------------------------------------ decoders
+    const int dt = threadIdx.x - DEC_WARP0 * 32;
+    const int arow = dt >> 1, ahalf = dt & 1;  // A: two threads per row, 64 elements each
+    const int64_t am = m0 + arow;
+    const int brow = dt;  // B: one thread per row, 128 elements
+    const int64_t bn = n0 + brow;
+    const int64_t a_row_elem = bt * p.a_bs + am * p.a_ld;
+    const int64_t b_row_elem = (bt / p.b_group) * p.b_bs + bn * p.b_ld;
+    uint32_t* sfa_s = reinterpret_cast<uint32_t*>(smem + OFF_SFA);
+    uint32_t* sfb_s = reinterpret_cast<uint32_t*>(smem + OFF_SFB);
+    bool ok = true;
+    for (int kt = 0; kt < num_k && ok; ++kt) {
+      const int cs = kt % S_CODES, cn = kt / S_CODES;
+      const int os = kt % S_OPS, on = kt / S_OPS;
+      // shared fields of A (two blocks) and B scales (four blocks), from L2
+      uint32_t a_sh[2] = {0, 0};
+      bool a_in[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int64_t k = (int64_t)kt * BK + ahalf * 64 + 32 * i;
+        a_in[i] = am < p.M && k < p.K;
+        if (a_in[i]) {
+          const int64_t idx = (a_row_elem + k) / 32;
+          a_sh[i] = p.a_type == 1 ? (uint32_t)static_cast<const uint8_t*>(p.a_shared)[idx]
+                                  : (uint32_t)static_cast<const uint16_t*>(p.a_shared)[idx];
+        }
+      }
+      uint32_t bsw = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t k = (int64_t)kt * BK + 32 * i;
+        const uint32_t sc = (bn < p.N && k < p.K) ? (uint32_t)p.b_scales[(b_row_elem + k) / 32] : 127u;
+        bsw |= sc << (8 * i);
+      }
+      if (!ptx::mbar_wait(&codes_full[cs], cn & 1, WAIT_LIMIT, abort_flag)) { flag_error(4u, abort_flag); ok = false; break; }
+      if (on > 0) {
+        if (!ptx::mbar_wait(&ops_empty[os], (on - 1) & 1, WAIT_LIMIT, abort_flag)) { flag_error(8u, abort_flag); ok = false; break; }
+        ptx::tc_fence_after();
+      }
+      if (*abort_flag) { ok = false; break; }
+      // --- A: 64 elements (two 32-blocks) of row arow
+      {
+        const unsigned char* src = smem + OFF_ACODES + cs * A_CODES + arow * KB + ahalf * 32;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(src);
+        const uint4 c1 = *reinterpret_cast<const uint4*>(src + 16);
+        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        unsigned char* dst = smem + OFF_AOPS + os * A_OPS;
+        uint32_t sfw = 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {  // block i of this half
+          const uint32_t sh = a_sh[i];
+          const int emax = (int)(sh & 0xFu) + p.a_ebias;
+          sfw |= (a_in[i] ? (uint32_t)clampi(emax + 126, 1, 254) : 127u) << (8 * i);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {  // 8-element sub-block q: one code word
+            const uint32_t m3 = p.a_type == 1 ? ((sh >> 4) & 7u) : ((sh >> (4 + 3 * q)) & 7u);
+            const uint32_t w = cw[4 * i + q];
+            const uint32_t lo = mix_to_e4m3_x4(w, m3), hi = mix_to_e4m3_x4(w >> 16, m3);
+            const int chunk = ahalf * 4 + i * 2 + (q >> 1);
+            uint2* d = reinterpret_cast<uint2*>(dst + sw128_off(arow, chunk) + (q & 1) * 8);
+            *d = make_uint2(lo, hi);
+          }
+        }
+        reinterpret_cast<uint16_t*>(sfa_s + os * BM + arow)[ahalf] = (uint16_t)sfw;
+      }
+      // --- B: 128 elements of row brow
+      {
+        const unsigned char* src = smem + OFF_BCODES + cs * B_CODES + brow * KB;
+        unsigned char* dst = smem + OFF_BOPS + os * B_OPS;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 cv = *reinterpret_cast<const uint4*>(src + 16 * c);
+          const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {  // two 16-element chunks per 16 code bytes
+            const uint32_t w0 = cw[2 * h], w1 = cw[2 * h + 1];
+            uint4 o;
+            if (p.b_fp4) {
+              o = make_uint4(fp4_to_e4m3_x4(w0), fp4_to_e4m3_x4(w0 >> 16), fp4_to_e4m3_x4(w1),
+                             fp4_to_e4m3_x4(w1 >> 16));
+            } else {
+              o = make_uint4(int4_to_e4m3_x4(w0), int4_to_e4m3_x4(w0 >> 16), int4_to_e4m3_x4(w1),
+                             int4_to_e4m3_x4(w1 >> 16));
+            }
+            *reinterpret_cast<uint4*>(dst + sw128_off(brow, 2 * c + h)) = o;
+          }
+        }
+        sfb_s[os * BN + brow] = bsw;
+      }
+      // codes slot free and this warp's scale words published
+      __syncwarp();
+      if (lane == 0) {
+        ptx::mbar_arrive(&codes_empty[cs]);
+        ptx::mbar_arrive(&sf_ready[os]);
+      }
+      // scale words -> TMEM (each lane quadrant holds a full replica)
+      if (warp < DEC_WARP0 + 4) {
+        if (!ptx::mbar_wait(&sf_ready[os], on & 1, WAIT_LIMIT, abort_flag)) { flag_error(32u, abort_flag); ok = false; break; }
+        const uint32_t q = (uint32_t)(warp & 3);
+        const uint32_t base = tmem + ((32u * q) << 16);
+        const uint32_t* sa = sfa_s + os * BM;
+        const uint32_t* sb = sfb_s + os * BN;
+        ptx::tmem_st_x4(base + SF_COL + 16u * os, sa[lane], sa[lane + 32], sa[lane + 64], sa[lane + 96]);
+        ptx::tmem_st_x4(base + SF_COL + 16u * os + 4u, sb[lane], sb[lane + 32], sb[lane + 64], sb[lane + 96]);
+        ptx::tmem_st_x4(base + SF_COL + 16u * os + 8u, sb[lane + 128], sb[lane + 160], sb[lane + 192],
+                        sb[lane + 224]);
+        ptx::tmem_wait_st();
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ops_full[os]);
+    }
+    // --------------------------------------------------------- epilogue
+    if (warp < DEC_WARP0 + 4) {
+      const bool got = ok && !*abort_flag && ptx::mbar_wait(acc_full, 0, WAIT_LIMIT, abort_flag);
+      if (!got) {
+        if (ok && !*abort_flag) flag_error(16u, abort_flag);
+      } else {
+        ptx::tc_fence_after();
+        const uint32_t q = (uint32_t)(warp & 3);
+        const int64_t row = m0 + 32 * q + lane;
+        for (int cc = 0; cc < BN / 32; ++cc) {
+          uint32_t u[32];
+          ptx::tmem_ld_x32(tmem + ((32u * q) << 16) + (uint32_t)(cc * 32), u);
+          ptx::tmem_wait_ld();
+          const int64_t col = n0 + cc * 32;
+          if (row >= p.M || col >= p.N) continue;
+          if (p.c != nullptr) {
+            float* cp = p.c + bt * p.cbs + row * p.ldc + col;
+            if (col + 32 <= p.N) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                reinterpret_cast<float4*>(cp)[i] =
+                    make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
+                                __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
+            } else {
+              for (int i = 0; i < 32 && col + i < p.N; ++i) cp[i] = __uint_as_float(u[i]);
+            }
+          }
+          if (p.epi != MIX_EPI_NONE) {
+            uint4 cw;
+            uint32_t sh;
+            epi_quant_block(u, p, cw, sh);
+            const int64_t e = bt * p.out_bs + row * p.out_ld + col;
+            *reinterpret_cast<uint4*>(p.out_codes + e / 2) = cw;
+            if (p.epi == MIX_EPI_MIX_T2) static_cast<uint16_t*>(p.out_shared)[e / 32] = (uint16_t)sh;
+            else static_cast<uint8_t*>(p.out_shared)[e / 32] = (uint8_t)sh;
+          }
+        }
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 3-D map over a packed code plane: x = code bytes along K, y = rows, z = batch.
+bool make_code_map(CUtensorMap* m, const void* base, int64_t k, int64_t rows, int64_t batch, int64_t ld_elems,
+                   int64_t bs_elems, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)(k / 2), (cuuint64_t)rows, (cuuint64_t)batch};
+  int64_t bs = bs_elems / 2;
+  if (batch <= 1 || bs <= 0) bs = (ld_elems / 2) * rows;  // unused stride, keep it valid
+  const cuuint64_t strides[2] = {(cuuint64_t)(ld_elems / 2), (cuuint64_t)bs};
+  const cuuint32_t box[3] = {(cuuint32_t)KB, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, cudaStream_t st, mix_status_t* why) {
-  (void)d; (void)st;
-  *why = MIX_ERR_UNSUPPORTED;
-  return cudaSuccess;
+  *why = MIX_OK;
+  if (d.K == 0 || d.M > (int64_t)INT32_MAX || d.N > (int64_t)INT32_MAX || d.batch > 65535) {
+    *why = MIX_ERR_UNSUPPORTED;
+    return cudaSuccess;
+  }
+  const int64_t bb = (d.batch + d.b_group - 1) / d.b_group;
+  CUtensorMap ma, mb;
+  if (!make_code_map(&ma, d.a_codes, d.K, d.M, d.batch, d.a_ld, d.a_batch_stride, BM) ||
+      !make_code_map(&mb, d.b_codes, d.K, d.N, bb, d.b_ld, d.b_batch_stride, BN)) {
+    *why = MIX_ERR_UNSUPPORTED;
+    return cudaSuccess;
+  }
+  TcParams p{};
+  p.M = d.M; p.N = d.N; p.K = d.K; p.batch = d.batch; p.b_group = d.b_group;
+  p.a_shared = d.a_shared; p.a_ld = d.a_ld; p.a_bs = d.a_batch_stride;
+  p.a_type = (int)d.a_type; p.a_ebias = d.a_ebias; p.b_fp4 = d.b_type == MX_FP4_E2M1;
+  p.b_scales = d.b_scales; p.b_ld = d.b_ld; p.b_bs = d.b_batch_stride;
+  p.c = d.c; p.ldc = d.ldc; p.cbs = d.c_batch_stride;
+  p.epi = (int)d.epi; p.epi_ebias = d.epi_ebias; p.epi_flags = d.epi_flags;
+  p.out_codes = d.out_codes; p.out_shared = d.out_shared; p.out_ld = d.out_ld; p.out_bs = d.out_batch_stride;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const dim3 grid((unsigned)((d.M + BM - 1) / BM), (unsigned)((d.N + BN - 1) / BN), (unsigned)d.batch);
+  gemm_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, p);
+  return cudaGetLastError();
 }
 
 }  // namespace mixk

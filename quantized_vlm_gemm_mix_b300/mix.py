@@ -217,6 +217,8 @@ def gemm_desc(M, N, K, a_codes, a_shared, a_type, a_ebias, b_codes, b_scales, b_
               batch=1, b_group=1, a_ld=None, a_batch_stride=None, b_ld=None, b_batch_stride=None,
               ldc=None, c_batch_stride=None, out_ld=None, out_batch_stride=None, algo=MIX_GEMM_AUTO) -> GemmDesc:
     d = GemmDesc()
+    # the descriptor holds raw device pointers: keep the tensors alive with it
+    d._keep = [t for t in (a_codes, a_shared, b_codes, b_scales, c, out_codes, out_shared) if t is not None]
     d.M, d.N, d.K, d.batch, d.b_group = M, N, K, batch, b_group
     d.a_codes, d.a_shared, d.a_type, d.a_ebias = _ptr(a_codes), _ptr(a_shared), a_type, a_ebias
     d.a_ld = K if a_ld is None else a_ld

@@ -1,0 +1,195 @@
+"""GPU parity of the tcgen05 A-MiX x W-MX matmul and its fused output
+quantiser against the CPU oracle (Eq. (6): int64 shift-add per block, fp64
+across blocks).  Floating-point results: max error relative to each output
+row's largest reference magnitude <= 1e-3.  Quantised outputs: bit-exact
+against the oracle quantiser applied to the GPU's own fp32 C."""
+import numpy as np
+import pytest
+
+from quantized_vlm_gemm_mix_b300 import synth
+from helpers import GEMM_REL_TOL, row_rel_err, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mix():
+    import torch
+    assert torch.cuda.is_available()
+    from quantized_vlm_gemm_mix_b300 import mix as m
+    return m
+
+
+def operands(orc, seed, M, N, K, at, bt, a_dtype="bf16", batch=1, bb=1):
+    a = synth.vlm_activations(seed, 0, batch * M, K, visual_rows=(batch * M * 3) // 4)
+    a = synth.to_bf16_bits(a) if a_dtype == "bf16" else synth.to_f32(a)
+    w = synth.to_bf16_bits(synth.normal(seed, 1, bb * N * K, 0, 0.02).reshape(bb * N, K))
+    ac, ash = orc.mix_quantize(a, at)
+    bc, bs = orc.mx_quantize(w, 1, bt)
+    return ac, ash, bc, bs
+
+
+def run_tc(mix, ac, ash, at, bc, bs, bt, M, N, K, epi=0, epi_ebias=-8, epi_flags=1, batch=1, b_group=1,
+           want_c=True, **kw):
+    import torch
+    c = torch.empty((batch, M, N), dtype=torch.float32, device="cuda") if want_c else None
+    oc = osh = None
+    if epi:
+        oc = torch.empty((batch, M, N // 2), dtype=torch.uint8, device="cuda")
+        osh = torch.empty((batch, M, N // 32), dtype=torch.int16 if epi == 2 else torch.uint8, device="cuda")
+    d = mix.gemm_desc(M, N, K, to_dev(ac), to_dev(ash), at, -8, to_dev(bc), to_dev(bs), bt, c=c, epi=epi,
+                      epi_ebias=epi_ebias, epi_flags=epi_flags, out_codes=oc, out_shared=osh, batch=batch,
+                      b_group=b_group, algo=mix.MIX_GEMM_TCGEN05, **kw)
+    mix.gemm(d)
+    torch.cuda.synchronize()
+    assert mix.mix_device_error() == 0
+    return (to_host(c) if want_c else None), (to_host(oc) if epi else None), (to_host(osh) if epi else None)
+
+
+@pytest.mark.parametrize("at,bt", [(2, 1), (1, 0), (2, 0), (1, 1)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 128), (300, 520, 416), (1, 32, 32), (17, 288, 3584)])
+def test_tc_matches_eq6(mix, orc, M, N, K, at, bt):
+    ac, ash, bc, bs = operands(orc, M * 7 + N + K, M, N, K, at, bt)
+    ref = orc.gemm(ac, ash, at, -8, bc, bs, bt)
+    c, _, _ = run_tc(mix, ac, ash, at, bc, bs, bt, M, N, K)
+    err = row_rel_err(c[0], ref)
+    assert err <= GEMM_REL_TOL, err
+
+
+def test_tc_agrees_with_shiftadd_path(mix, orc):
+    import torch
+    M, N, K = 16, 512, 1024
+    ac, ash, bc, bs = operands(orc, 3, M, N, K, 2, 1)
+    c_tc, _, _ = run_tc(mix, ac, ash, 2, bc, bs, 1, M, N, K)
+    c2 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    d = mix.gemm_desc(M, N, K, to_dev(ac), to_dev(ash), 2, -8, to_dev(bc), to_dev(bs), 1, c=c2,
+                      algo=mix.MIX_GEMM_SHIFTADD)
+    mix.gemm(d)
+    torch.cuda.synchronize()
+    assert row_rel_err(c_tc[0], to_host(c2).astype(np.float64)) <= GEMM_REL_TOL
+
+
+def test_tiny_end_to_end_config(mix, orc):
+    """fp32 A [128 x 512] -> MiX-4.5b; W [512 x 256] N(0, 0.02) -> MXFP4 along K;
+    C = A W in fp32 plus the fused MiX-4.5b output quantiser; seed 0."""
+    import torch
+    a = synth.to_f32(synth.vlm_activations(0, 0, 128, 512, visual_rows=96, n_outlier=4))
+    w = synth.to_f32(synth.gaussian_weights(0, 2, 512, 256))
+    ac_g, ash_g = mix.quantize_mix(to_dev(a), mix.MIX_T2_4P5)
+    bc_g, bs_g = mix.quantize_mx(to_dev(w), 0, mix.MX_FP4_E2M1)
+    ac, ash = orc.mix_quantize(a, 2)
+    bc, bs = orc.mx_quantize(w, 0, 1)
+    assert np.array_equal(to_host(ac_g), ac) and np.array_equal(to_host(ash_g), ash)
+    assert np.array_equal(to_host(bc_g), bc) and np.array_equal(to_host(bs_g), bs)
+    c, oc, osh = run_tc(mix, ac, ash, 2, bc, bs, 1, 128, 256, 512, epi=2)
+    ref = orc.gemm(ac, ash, 2, -8, bc, bs, 1)
+    assert row_rel_err(c[0], ref) <= GEMM_REL_TOL
+    rc, rs = orc.mix_quantize(c[0], 2, -8, 1)
+    assert np.array_equal(oc[0], rc) and np.array_equal(osh[0], rs)
+    # against the oracle's own C the codes may differ only at rounding ties
+    rc2, _ = orc.mix_quantize(ref.astype(np.float32), 2, -8, 1)
+    assert np.mean(oc[0] != rc2) < 1e-3
+
+
+@pytest.mark.parametrize("epi", [1, 2, 3, 4])
+def test_tc_epilogue_formats(mix, orc, epi):
+    M, N, K = 200, 512, 640
+    ac, ash, bc, bs = operands(orc, 11 + epi, M, N, K, 1, 0)
+    c, oc, osh = run_tc(mix, ac, ash, 1, bc, bs, 0, M, N, K, epi=epi, epi_ebias=-6,
+                        epi_flags=1 if epi <= 2 else 0)
+    if epi <= 2:
+        rc, rs = orc.mix_quantize(c[0], epi, -6, 1)
+    else:
+        rc, rs = orc.mx_quantize(c[0], 1, 0 if epi == 3 else 1, 0)
+    assert np.array_equal(oc[0], rc) and np.array_equal(osh[0].astype(rs.dtype), rs)
+
+
+def test_tc_epilogue_only_no_c(mix, orc):
+    M, N, K = 130, 256, 256
+    ac, ash, bc, bs = operands(orc, 19, M, N, K, 2, 1)
+    c, _, _ = run_tc(mix, ac, ash, 2, bc, bs, 1, M, N, K)
+    _, oc, osh = run_tc(mix, ac, ash, 2, bc, bs, 1, M, N, K, epi=2, want_c=False)
+    rc, rs = orc.mix_quantize(c[0], 2, -8, 1)
+    assert np.array_equal(oc[0], rc) and np.array_equal(osh[0], rs)
+
+
+def test_tc_batched_gqa_and_strides(mix, orc):
+    """Batch 6 in groups of 3 sharing B; A read through an interleaved row
+    stride (the (token, head) layout of a QKV projection)."""
+    B, G, M, N, K = 6, 3, 160, 288, 128
+    ac, ash, bc, bs = operands(orc, 23, M, N, K, 2, 0, batch=B, bb=B // G)
+    # interleave: row m of batch b at element offset m * (B*K) + b * K
+    acb = ac.reshape(B, M, K // 2).transpose(1, 0, 2).copy()      # [M, B, K/2]
+    ashb = ash.reshape(B, M, K // 32).transpose(1, 0, 2).copy()
+    c, _, _ = run_tc(mix, acb, ashb, 2, bc, bs, 0, M, N, K, batch=B, b_group=G, a_ld=B * K, a_batch_stride=K)
+    ref = orc.gemm(ac.reshape(B, M, -1), ash.reshape(B, M, -1), 2, -8, bc.reshape(B // G, N, -1),
+                   bs.reshape(B // G, N, -1), 0, b_group=G)
+    assert row_rel_err(c, ref) <= GEMM_REL_TOL
+
+
+def sampled_check(orc, c, ac, ash, at, bc, bs, bt, rows, cols, ebias=-8):
+    ref = orc.gemm(ac[rows], ash[rows], at, ebias, bc[cols], bs[cols], bt)
+    return row_rel_err(c[np.ix_(rows, cols)], ref)
+
+
+@pytest.mark.parametrize("name,K,N", [("qkv", 3584, 4608), ("o", 3584, 3584), ("gate_up", 3584, 37888),
+                                      ("down", 18944, 3584)])
+def test_qwen2vl_prefill_linears_sampled(mix, orc, name, K, N):
+    """M = 4096 tokens, A-MiX-4.5b x W-MXFP4, fused MiX-4.5b epilogue, at full
+    size; the oracle checks 96 sampled rows x 256 sampled columns of C, and the
+    epilogue planes of the sampled rows bit for bit."""
+    import torch
+    M = 4096
+    x = synth.to_bf16_bits(synth.vlm_activations(1, 10 + K, M, K, visual_rows=3072))
+    w = synth.to_bf16_bits(synth.gaussian_weights(1, 20 + N, K, N))
+    ac_g, ash_g = mix.quantize_mix(to_dev(x), mix.MIX_T2_4P5)
+    bc_g, bs_g = mix.quantize_mx(to_dev(w), 0, mix.MX_FP4_E2M1)
+    del w
+    c = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    oc = torch.empty((M, N // 2), dtype=torch.uint8, device="cuda")
+    osh = torch.empty((M, N // 32), dtype=torch.int16, device="cuda")
+    d = mix.gemm_desc(M, N, K, ac_g, ash_g, 2, -8, bc_g, bs_g, 1, c=c, epi=2, out_codes=oc, out_shared=osh,
+                      algo=mix.MIX_GEMM_TCGEN05)
+    mix.gemm(d)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(K + N)
+    rows = np.sort(rng.choice(M, 96, replace=False))
+    cols = np.sort(rng.choice(N, 256, replace=False))
+    ac, ash = to_host(ac_g), to_host(ash_g)
+    bc, bs = to_host(bc_g), to_host(bs_g)
+    ch = to_host(c)
+    assert sampled_check(orc, ch, ac, ash, 2, bc, bs, 1, rows, cols) <= GEMM_REL_TOL
+    rc, rs = orc.mix_quantize(np.ascontiguousarray(ch[rows]), 2, -8, 1)
+    assert np.array_equal(to_host(oc)[rows], rc) and np.array_equal(to_host(osh)[rows], rs)
+
+
+def test_vit_mlp_chain_sampled(mix, orc):
+    """M = 16384 patch tokens, A-MiX-4.25b x W-MXINT4: fc1 1280 -> 5120 with the
+    fused MiX-4.25b epilogue feeding fc2 5120 -> 1280 directly."""
+    import torch
+    M, D, H = 16384, 1280, 5120
+    x = synth.to_bf16_bits(synth.vlm_activations(2, 0, M, D, visual_rows=M, outlier_frac=0.02,
+                                                 outlier_scale=20.0))
+    w1 = synth.to_bf16_bits(synth.gaussian_weights(2, 1, D, H))
+    w2 = synth.to_bf16_bits(synth.gaussian_weights(2, 2, H, D))
+    ac_g, ash_g = mix.quantize_mix(to_dev(x), mix.MIX_T1_4P25)
+    b1c, b1s = mix.quantize_mx(to_dev(w1), 0, mix.MX_INT4)
+    b2c, b2s = mix.quantize_mx(to_dev(w2), 0, mix.MX_INT4)
+    c1 = torch.empty((M, H), dtype=torch.float32, device="cuda")
+    hc = torch.empty((M, H // 2), dtype=torch.uint8, device="cuda")
+    hs = torch.empty((M, H // 32), dtype=torch.uint8, device="cuda")
+    mix.gemm(mix.gemm_desc(M, H, D, ac_g, ash_g, 1, -8, b1c, b1s, 0, c=c1, epi=1, out_codes=hc, out_shared=hs,
+                           algo=mix.MIX_GEMM_TCGEN05))
+    c2 = torch.empty((M, D), dtype=torch.float32, device="cuda")
+    mix.gemm(mix.gemm_desc(M, D, H, hc, hs, 1, -8, b2c, b2s, 0, c=c2, algo=mix.MIX_GEMM_TCGEN05))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(4)
+    rows = np.sort(rng.choice(M, 64, replace=False))
+    ac, ash = to_host(ac_g), to_host(ash_g)
+    c1h = to_host(c1)
+    assert sampled_check(orc, c1h, ac, ash, 1, to_host(b1c), to_host(b1s), 0, rows,
+                         np.sort(rng.choice(H, 256, replace=False))) <= GEMM_REL_TOL
+    rc, rs = orc.mix_quantize(np.ascontiguousarray(c1h[rows]), 1, -8, 1)
+    assert np.array_equal(to_host(hc)[rows], rc) and np.array_equal(to_host(hs)[rows], rs)
+    assert sampled_check(orc, to_host(c2), to_host(hc), to_host(hs), 1, to_host(b2c), to_host(b2s), 0, rows,
+                         np.sort(rng.choice(D, 256, replace=False))) <= GEMM_REL_TOL
