@@ -1,0 +1,595 @@
+"""Benchmark of the MiX hot path on one B300 (or N replicas).
+
+One step runs every stage of the path once, at the paper-shaped sizes:
+  * quantiser sweep: 4096 x 3584 bf16 activations -> MiX-4.25b and MiX-4.5b;
+    3584 x 18944 bf16 weights -> MXINT4 and MXFP4 (down the columns, as stored);
+  * Qwen2-VL-7B-shaped prefill linears (M = 4096): activations -> MiX-4.5b,
+    QKV / O / gate+up / down as A-MiX-4.5b x W-MXFP4 with the fused MiX-4.5b
+    output quantiser (the down projection's 18944-wide input is quantised too);
+  * ViT MLP (M = 16384): activations -> MiX-4.25b, fc1 (fused MiX-4.25b
+    output) feeding fc2 directly, A-MiX-4.25b x W-MXINT4;
+  * GQA attention (28 / 4 heads, d 128), prefill 4096: K-smoothing (mean +
+    subtraction), Q -> MiX-4.5b, K' -> MXINT4, S = Q K'^T (fp32), P (a fixed
+    softmax output) -> MiX-4.5b, V -> MXINT4 along tokens, O = P V;
+  * decode over an 8192-token MX cache: frozen-mean smoothing of the new key,
+    its MX codes, q -> MiX-4.5b, S = q K'^T and O = P V on the shift-add path.
+Weights and caches are quantised once at set-up; everything above is timed.
+
+value = 100 * (sum over the step's launches of max(bytes / HBM peak, flops /
+tensor peak)) / measured step time, i.e. the step's throughput as a percentage
+of the B300 roofline; absolute GB/s and TOPS of every call are in "parts".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MiX quantize GB/s + MiX×MX GEMM eff. TOPS, % of B300 roofline"
+UNIT = "% of B300 roofline"
+WORKLOAD = "qwen2vl7b_vit_attention_hot_path"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d["bf16_tflops_sustained"], "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+PEAKS = load_peaks()
+# kind::mxf8f6f4 (FP8-rate) dense peak: the measured bf16 peak x the nominal 2x ratio
+MX8_TFLOPS = PEAKS["bf16_tflops_sustained"] * 2.0
+MX8_TFLOPS_BURST = PEAKS["bf16_tflops"] * 2.0
+HBM = PEAKS["hbm_gbs"]
+
+
+class Call:
+    """One library call of the step with its algorithmic bytes and flops."""
+
+    def __init__(self, name, fn, nbytes, flops=0.0, launches=1, kind="hbm"):
+        self.name, self.fn, self.bytes, self.flops, self.launches, self.kind = name, fn, nbytes, flops, launches, kind
+
+    def roof_s(self):
+        t_mem = self.bytes / (HBM * 1e9)
+        t_mma = self.flops / (MX8_TFLOPS * 1e12) if self.flops else 0.0
+        return max(t_mem, t_mma)
+
+
+def mix_bytes(rows, k, t, in_bytes=2):
+    return rows * k * in_bytes + rows * k // 2 + rows * (k // 32) * (1 if t == 1 else 2)
+
+
+def mx_bytes(n, k, in_bytes=2):
+    return n * k * in_bytes + n * k // 2 + n * (k // 32)
+
+
+def plane_bytes(rows, k, t):
+    """Packed MiX planes (t = 1 / 2) or MX planes (t = 0)."""
+    return rows * k // 2 + rows * (k // 32) * (2 if t == 2 else 1)
+
+
+# ---------------------------------------------------------------------------
+# The step: every call with its algorithmic bytes and flops (shapes only)
+# ---------------------------------------------------------------------------
+
+def dims(small=False):
+    s = 8 if small else 1
+    return dict(M=4096 // s, DM=3584, DF=18944, QKV=4608, MV=16384 // s, T=4096 // s, TC=8192 // s,
+                HQ=28, HK=4, D=128)
+
+
+def step_table(small=False):
+    """[(name, bytes, flops, launches, cpu work)] in launch order.  The cpu work
+    (kind, count) lets the CPU baseline extrapolate the oracle's sampled cost:
+    elements for quantisers and smoothing, outputs x 32-blocks for matmuls."""
+    g = dims(small)
+    M, DM, DF, QKV, MV, T, TC, HQ, HK, D = (g[k] for k in ("M", "DM", "DF", "QKV", "MV", "T", "TC", "HQ", "HK", "D"))
+    rows = []
+
+    def add(name, nbytes, flops=0.0, launches=1, cpu=None):
+        rows.append((name, float(nbytes), float(flops), launches, cpu))
+
+    add(f"mix_quantize_t1_{M}x{DM}", mix_bytes(M, DM, 1), cpu=("mix1", M * DM))
+    add(f"mix_quantize_t2_{M}x{DM}", mix_bytes(M, DM, 2), cpu=("mix2", M * DM))
+    add(f"mx_quantize_int4_{DM}x{DF}", mx_bytes(DF, DM), cpu=("mx", DF * DM))
+    add(f"mx_quantize_fp4_{DM}x{DF}", mx_bytes(DF, DM), cpu=("mx", DF * DM))
+    add(f"mix_quantize_t2_{M}x{DF}", mix_bytes(M, DF, 2), cpu=("mix2", M * DF))
+    for name, k, n in (("qkv", DM, QKV), ("o", DM, DM), ("gate_up", DM, 2 * DF), ("down", DF, DM)):
+        add(f"gemm_{name}_{M}x{k}x{n}", plane_bytes(M, k, 2) + plane_bytes(n, k, 0) + plane_bytes(M, n, 2),
+            2.0 * M * n * k, cpu=("gemm", M * n * (k // 32)))
+    add(f"mix_quantize_t1_{MV}x1280", mix_bytes(MV, 1280, 1), cpu=("mix1", MV * 1280))
+    add(f"gemm_vit_fc1_{MV}x1280x5120", plane_bytes(MV, 1280, 1) + plane_bytes(5120, 1280, 0) +
+        plane_bytes(MV, 5120, 1), 2.0 * MV * 5120 * 1280, cpu=("gemm", MV * 5120 * 40))
+    add(f"gemm_vit_fc2_{MV}x5120x1280", plane_bytes(MV, 5120, 1) + plane_bytes(1280, 5120, 0) +
+        plane_bytes(MV, 1280, 1), 2.0 * MV * 1280 * 5120, cpu=("gemm", MV * 1280 * 160))
+    add(f"ksmooth_compute_{T}x{HK}x{D}", T * HK * D * (2 + 2 + 4), launches=3, cpu=("ks", 2 * T * HK * D))
+    add(f"mix_quantize_t2_q_{T * HQ}x{D}", mix_bytes(T * HQ, D, 2), cpu=("mix2", T * HQ * D))
+    add(f"mx_quantize_int4_kprime_{T * HK}x{D}", mx_bytes(T * HK, D, 4), cpu=("mx", T * HK * D))
+    add(f"bmm_qk_{HQ}x{T}x{T}x{D}", plane_bytes(T * HQ, D, 2) + plane_bytes(T * HK, D, 0) + HQ * T * T * 4,
+        2.0 * HQ * T * T * D, cpu=("gemm", HQ * T * T * (D // 32)))
+    add(f"mix_quantize_t2_p_{HQ * T}x{T}", mix_bytes(HQ * T, T, 2), cpu=("mix2", HQ * T * T))
+    for h in range(HK):
+        add(f"mx_quantize_int4_v_head{h}_{T}x{D}", mx_bytes(D, T), cpu=("mx", D * T))
+    add(f"bmm_pv_{HQ}x{T}x{D}x{T}", plane_bytes(HQ * T, T, 2) + plane_bytes(HK * D, T, 0) + HQ * T * D * 4,
+        2.0 * HQ * T * D * T, cpu=("gemm", HQ * T * D * (T // 32)))
+    add(f"ksmooth_apply_frozen_1x{HK}x{D}", HK * D * (2 + 4 + 4), cpu=("ks", HK * D))
+    add(f"mx_quantize_int4_knew_{HK}x{D}", mx_bytes(HK, D, 4), cpu=("mx", HK * D))
+    add(f"mix_quantize_t2_qdec_{HQ}x{D}", mix_bytes(HQ, D, 2), cpu=("mix2", HQ * D))
+    add(f"gemv_qk_decode_{HK}x7x{TC}x{D}", plane_bytes(HQ, D, 2) + plane_bytes(TC * HK, D, 0) + HK * 7 * TC * 4,
+        2.0 * HQ * TC * D, cpu=("gemm", HQ * TC * (D // 32)))
+    add(f"mix_quantize_t2_pdec_{HQ}x{TC}", mix_bytes(HQ, TC, 2), cpu=("mix2", HQ * TC))
+    add(f"gemv_pv_decode_{HK}x7x{D}x{TC}", plane_bytes(HQ, TC, 2) + plane_bytes(HK * D, TC, 0) + HK * 7 * D * 4,
+        2.0 * HQ * D * TC, launches=2, cpu=("gemm", HQ * D * (TC // 32)))
+    return rows
+
+
+def roof_seconds(nbytes, flops):
+    return max(nbytes / (HBM * 1e9), flops / (MX8_TFLOPS * 1e12) if flops else 0.0)
+
+
+# ---------------------------------------------------------------------------
+# Workload
+# ---------------------------------------------------------------------------
+
+def build_workload(torch, mix, synth, dev, seed=0, small=False):
+    """Inputs on the device, weights and caches quantised once, and one closure
+    per call of the step.  Returns (calls, h2d pairs, d2h tensors, host arrays,
+    tensors to keep alive)."""
+    bf16 = torch.bfloat16
+    T2, T1 = mix.MIX_T2_4P5, mix.MIX_T1_4P25
+    FP4, INT4 = mix.MX_FP4_E2M1, mix.MX_INT4
+    g = dims(small)
+    M, DM, DF, QKV, MV, T, TC, HQ, HK, D = (g[k] for k in ("M", "DM", "DF", "QKV", "MV", "T", "TC", "HQ", "HK", "D"))
+    fns, h2d, d2h, host, keep = {}, [], [], {}, []
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(bf16)
+
+    def new(shape, dtype):
+        t = torch.empty(shape, dtype=dtype, device=dev)
+        keep.append(t)
+        return t
+
+    # ----- per-step activations
+    x_np = synth.to_bf16_bits(synth.vlm_activations(seed, 1, M, DM, visual_rows=(3 * M) // 4))
+    xd_np = synth.to_bf16_bits(synth.vlm_activations(seed, 2, M, DF, visual_rows=(3 * M) // 4))
+    xv_np = synth.to_bf16_bits(synth.vlm_activations(seed, 3, MV, 1280, visual_rows=MV, outlier_frac=0.02,
+                                                     outlier_scale=20.0))
+    host.update(x=x_np, xd=xd_np, xv=xv_np)
+    x, xd, xv = dev_bf16(x_np), dev_bf16(xd_np), dev_bf16(xv_np)
+    h2d += [(x, x_np), (xd, xd_np), (xv, xv_np)]
+
+    # ----- resident weights, quantised at set-up (down the columns, as stored)
+    def weight(tid, k, n):
+        return dev_bf16(synth.to_bf16_bits(synth.gaussian_weights(seed, tid, k, n)))
+
+    w_gu = weight(30, DM, 2 * DF)        # gate+up 3584 x 37888; its first 18944 columns are the sweep weight
+    keep.append(w_gu)
+    wq = {"gate_up": mix.quantize_mx(w_gu, 0, FP4)}
+    for name, tid, k, n in (("qkv", 31, DM, QKV), ("o", 32, DM, DM), ("down", 33, DF, DM)):
+        w = weight(tid, k, n)
+        wq[name] = mix.quantize_mx(w, 0, FP4)
+        del w
+    w1, w2 = weight(34, 1280, 5120), weight(35, 5120, 1280)
+    wv1, wv2 = mix.quantize_mx(w1, 0, INT4), mix.quantize_mx(w2, 0, INT4)
+    del w1, w2
+    keep += [wq, wv1, wv2]
+
+    # ----- 1. quantiser sweep
+    a1c, a1s = new((M, DM // 2), torch.uint8), new((M, DM // 32), torch.uint8)
+    a2c, a2s = new((M, DM // 2), torch.uint8), new((M, DM // 32), torch.int16)
+    wic, wis = new((DF, DM // 2), torch.uint8), new((DF, DM // 32), torch.uint8)
+    wfc, wfs = new((DF, DM // 2), torch.uint8), new((DF, DM // 32), torch.uint8)
+    fns[f"mix_quantize_t1_{M}x{DM}"] = lambda: mix.mix_quantize(x, M, DM, DM, T1, -8, 1, a1c, a1s)
+    fns[f"mix_quantize_t2_{M}x{DM}"] = lambda: mix.mix_quantize(x, M, DM, DM, T2, -8, 1, a2c, a2s)
+    fns[f"mx_quantize_int4_{DM}x{DF}"] = lambda: mix.mx_quantize(w_gu, DM, DF, 2 * DF, 0, INT4, 0, wic, wis)
+    fns[f"mx_quantize_fp4_{DM}x{DF}"] = lambda: mix.mx_quantize(w_gu, DM, DF, 2 * DF, 0, FP4, 0, wfc, wfs)
+
+    # ----- 2. prefill linears: A = the MiX-4.5b activations; epilogue-only outputs
+    adc, ads = new((M, DF // 2), torch.uint8), new((M, DF // 32), torch.int16)
+    fns[f"mix_quantize_t2_{M}x{DF}"] = lambda: mix.mix_quantize(xd, M, DF, DF, T2, -8, 1, adc, ads)
+    outs = {}
+    for name, k, n, (ac_, as_) in (("qkv", DM, QKV, (a2c, a2s)), ("o", DM, DM, (a2c, a2s)),
+                                   ("gate_up", DM, 2 * DF, (a2c, a2s)), ("down", DF, DM, (adc, ads))):
+        oc, os_ = new((M, n // 2), torch.uint8), new((M, n // 32), torch.int16)
+        outs[name] = oc
+        bc, bs = wq[name]
+        d = mix.gemm_desc(M, n, k, ac_, as_, T2, -8, bc, bs, FP4, c=None, epi=mix.MIX_EPI_MIX_T2, out_codes=oc,
+                          out_shared=os_, algo=mix.MIX_GEMM_TCGEN05)
+        fns[f"gemm_{name}_{M}x{k}x{n}"] = (lambda d=d: mix.mix_mx_gemm(d))
+    d2h.append(outs["down"])
+
+    # ----- 3. ViT MLP: fc1's fused MiX-4.25b output is fc2's input
+    vc, vs = new((MV, 640), torch.uint8), new((MV, 40), torch.uint8)
+    hc, hs = new((MV, 2560), torch.uint8), new((MV, 160), torch.uint8)
+    yc, ys = new((MV, 640), torch.uint8), new((MV, 40), torch.uint8)
+    fns[f"mix_quantize_t1_{MV}x1280"] = lambda: mix.mix_quantize(xv, MV, 1280, 1280, T1, -8, 1, vc, vs)
+    d1 = mix.gemm_desc(MV, 5120, 1280, vc, vs, T1, -8, wv1[0], wv1[1], INT4, epi=mix.MIX_EPI_MIX_T1, out_codes=hc,
+                       out_shared=hs, algo=mix.MIX_GEMM_TCGEN05)
+    d2 = mix.gemm_desc(MV, 1280, 5120, hc, hs, T1, -8, wv2[0], wv2[1], INT4, epi=mix.MIX_EPI_MIX_T1, out_codes=yc,
+                       out_shared=ys, algo=mix.MIX_GEMM_TCGEN05)
+    fns[f"gemm_vit_fc1_{MV}x1280x5120"] = lambda: mix.mix_mx_gemm(d1)
+    fns[f"gemm_vit_fc2_{MV}x5120x1280"] = lambda: mix.mix_mx_gemm(d2)
+    d2h.append(yc)
+
+    # ----- 4. attention prefill (28 query / 4 KV heads, d 128)
+    q_np, k_np, v_np = synth.attention_qkv(seed, TC, HQ, HK, D)
+    qb = np.ascontiguousarray(synth.to_bf16_bits(q_np[:T]).reshape(T, HQ * D))
+    kb = synth.to_bf16_bits(k_np).reshape(TC, HK * D)
+    vb = synth.to_bf16_bits(v_np).reshape(TC, HK * D)
+    q_last = synth.to_bf16_bits(q_np[TC - 1]).reshape(HQ, D)
+    del q_np, k_np, v_np
+    host.update(q=qb, k=kb, v=vb)
+    q_d, k_d, v_d = dev_bf16(qb), dev_bf16(kb), dev_bf16(vb)
+    h2d += [(q_d, qb), (k_d, kb), (v_d, vb)]
+    k_pre = k_d[:T]
+    mean = new((HK, D), torch.float32)
+    kprime = new((T, HK, D), torch.float32)
+    ws_k = new(mix.ksmooth_workspace_bytes(T, HK, D), torch.uint8)
+    fns[f"ksmooth_compute_{T}x{HK}x{D}"] = lambda: mix.ksmooth_kv(k_pre, T, HK, D, HK * D, mean,
+                                                                  mix.KSMOOTH_COMPUTE, kprime, ws_k)
+    qc, qs = new((T * HQ, 64), torch.uint8), new((T * HQ, 4), torch.int16)         # rows (token, head)
+    fns[f"mix_quantize_t2_q_{T * HQ}x{D}"] = lambda: mix.mix_quantize(q_d, T * HQ, D, D, T2, -8, 1, qc, qs)
+    kc, ks = new((T * HK, 64), torch.uint8), new((T * HK, 4), torch.uint8)         # rows (token, head)
+    fns[f"mx_quantize_int4_kprime_{T * HK}x{D}"] = lambda: mix.mx_quantize(kprime, T * HK, D, D, 1, INT4, 0, kc, ks)
+    S = new((HQ, T, T), torch.float32)
+    dqk = mix.gemm_desc(T, T, D, qc, qs, T2, -8, kc, ks, INT4, c=S, batch=HQ, b_group=HQ // HK, a_ld=HQ * D,
+                        a_batch_stride=D, b_ld=HK * D, b_batch_stride=D, algo=mix.MIX_GEMM_TCGEN05)
+    fns[f"bmm_qk_{HQ}x{T}x{T}x{D}"] = lambda: mix.mix_mx_gemm(dqk)
+    # P: a fixed causal softmax of S, made once here (softmax is not on the path)
+    for f in (f"ksmooth_compute_{T}x{HK}x{D}", f"mix_quantize_t2_q_{T * HQ}x{D}",
+              f"mx_quantize_int4_kprime_{T * HK}x{D}", f"bmm_qk_{HQ}x{T}x{T}x{D}"):
+        fns[f]()
+    P = new((HQ, T, T), bf16)
+    causal = torch.ones((T, T), dtype=torch.bool, device=dev).tril()
+    for h in range(HQ):
+        P[h] = torch.softmax((S[h] / math.sqrt(D)).masked_fill(~causal, float("-inf")), dim=-1).to(bf16)
+    del causal
+    pc, ps = new((HQ * T, T // 2), torch.uint8), new((HQ * T, T // 32), torch.int16)
+    fns[f"mix_quantize_t2_p_{HQ * T}x{T}"] = lambda: mix.mix_quantize(P, HQ * T, T, T, T2, -15, 1, pc, ps)
+    vqc, vqs = new((HK, D, T // 2), torch.uint8), new((HK, D, T // 32), torch.uint8)
+    for h in range(HK):
+        vh = v_d[:T, h * D:(h + 1) * D]
+        fns[f"mx_quantize_int4_v_head{h}_{T}x{D}"] = (lambda vh=vh, h=h: mix.mx_quantize(
+            vh, T, D, HK * D, 0, INT4, 0, vqc[h], vqs[h]))
+    O = new((HQ, T, D), torch.float32)
+    dpv = mix.gemm_desc(T, D, T, pc, ps, T2, -15, vqc, vqs, INT4, c=O, batch=HQ, b_group=HQ // HK,
+                        algo=mix.MIX_GEMM_TCGEN05)
+    fns[f"bmm_pv_{HQ}x{T}x{D}x{T}"] = lambda: mix.mix_mx_gemm(dpv)
+    d2h.append(O)
+
+    # ----- 5. decode over a TC-token cache smoothed with the frozen prefill mean
+    mean_f = new((HK, D), torch.float32)
+    mean_f.copy_(mean)
+    kp_all = new((TC, HK, D), torch.float32)
+    mix.ksmooth_kv(k_d, TC, HK, D, HK * D, mean_f, mix.KSMOOTH_APPLY_FROZEN, kp_all)
+    kcc, kcs = new((TC * HK, 64), torch.uint8), new((TC * HK, 4), torch.uint8)
+    mix.mx_quantize(kp_all, TC * HK, D, D, 1, INT4, 0, kcc, kcs)
+    vcc, vcs = new((HK, D, TC // 2), torch.uint8), new((HK, D, TC // 32), torch.uint8)
+    for h in range(HK):
+        mix.mx_quantize(v_d[:, h * D:(h + 1) * D], TC, D, HK * D, 0, INT4, 0, vcc[h], vcs[h])
+    q_new = dev_bf16(q_last)
+    keep.append(q_new)
+    k_new = k_d[TC - 1:TC]
+    kp_new = new((1, HK, D), torch.float32)
+    fns[f"ksmooth_apply_frozen_1x{HK}x{D}"] = lambda: mix.ksmooth_kv(k_new, 1, HK, D, HK * D, mean_f,
+                                                                     mix.KSMOOTH_APPLY_FROZEN, kp_new)
+    knc, kns = kcc[(TC - 1) * HK:], kcs[(TC - 1) * HK:]      # the newest token's rows of the cache
+    fns[f"mx_quantize_int4_knew_{HK}x{D}"] = lambda: mix.mx_quantize(kp_new, HK, D, D, 1, INT4, 0, knc, kns)
+    qdc, qds = new((HQ, 64), torch.uint8), new((HQ, 4), torch.int16)
+    fns[f"mix_quantize_t2_qdec_{HQ}x{D}"] = lambda: mix.mix_quantize(q_new, HQ, D, D, T2, -8, 1, qdc, qds)
+    s_dec = new((HK, 7, TC), torch.float32)
+    dd1 = mix.gemm_desc(7, TC, D, qdc, qds, T2, -8, kcc, kcs, INT4, c=s_dec, batch=HK, b_ld=HK * D,
+                        b_batch_stride=D, algo=mix.MIX_GEMM_SHIFTADD)
+    ws1 = new(max(16, mix.mix_mx_gemm_workspace_bytes(dd1)), torch.uint8)
+    fns[f"gemv_qk_decode_{HK}x7x{TC}x{D}"] = lambda: mix.mix_mx_gemm(dd1, ws1)
+    p_dec = new((HQ, TC), bf16)
+    p_dec.copy_(torch.softmax(torch.randn((HQ, TC), device=dev, generator=torch.Generator(dev).manual_seed(seed))
+                              * 3.0, dim=-1))
+    pdc, pds = new((HQ, TC // 2), torch.uint8), new((HQ, TC // 32), torch.int16)
+    fns[f"mix_quantize_t2_pdec_{HQ}x{TC}"] = lambda: mix.mix_quantize(p_dec, HQ, TC, TC, T2, -15, 1, pdc, pds)
+    o_dec = new((HK, 7, D), torch.float32)
+    dd2 = mix.gemm_desc(7, D, TC, pdc, pds, T2, -15, vcc, vcs, INT4, c=o_dec, batch=HK, algo=mix.MIX_GEMM_SHIFTADD)
+    ws2 = new(max(16, mix.mix_mx_gemm_workspace_bytes(dd2)), torch.uint8)
+    fns[f"gemv_pv_decode_{HK}x7x{D}x{TC}"] = lambda: mix.mix_mx_gemm(dd2, ws2)
+    d2h.append(o_dec)
+
+    calls = []
+    for name, nbytes, flops, launches, _ in step_table(small):
+        calls.append(Call(name, fns.pop(name), nbytes, flops, launches))
+    assert not fns, f"closures without a table entry: {list(fns)}"
+    keep += [P, S, O, kprime, kp_all]
+    return calls, h2d, d2h, host, keep
+
+
+# ---------------------------------------------------------------------------
+# Clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index, self.rows, self.proc = index, [], None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm = [float(r[1]) for r in self.rows if len(r) >= 9 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) >= 9 and r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            if len(r) >= 9:
+                for n, v in zip(names, r[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample of the step
+# ---------------------------------------------------------------------------
+
+def oracle_unit_costs(budget_s=10.0):
+    """Seconds per unit of work of the oracle (one host thread), measured on
+    seeded samples of the step's tensors sized to take about budget_s: per
+    element for the quantisers and smoothing, per output x 32-block for the
+    matmul."""
+    import oracle as orc
+    from quantized_vlm_gemm_mix_b300 import synth
+    r = max(16, int(64 * math.sqrt(budget_s / 0.11)) // 16 * 16)
+    x = synth.to_bf16_bits(synth.vlm_activations(0, 1, r, 3584, visual_rows=(3 * r) // 4))
+    w = synth.to_bf16_bits(synth.gaussian_weights(0, 30, 3584, r))
+    _, k_np, _ = synth.attention_qkv(0, 4 * r, 2, 4, 128)
+    kb = synth.to_bf16_bits(k_np)
+    cost = {}
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        out = fn()
+        return time.perf_counter() - t0, out
+
+    t, _ = timed(lambda: orc.mix_quantize(x, orc.T1))
+    cost["mix1"] = t / x.size
+    t, (ac, ash) = timed(lambda: orc.mix_quantize(x, orc.T2))
+    cost["mix2"] = t / x.size
+    t, (bc, bs) = timed(lambda: orc.mx_quantize(w, 0, orc.MXFP4))
+    cost["mx"] = t / w.size
+    t, _ = timed(lambda: orc.ksmooth_mean(kb))
+    cost["ks"] = t / kb.size
+    rr = max(1, r // 4)
+    t, _ = timed(lambda: orc.gemm(ac[:rr], ash[:rr], orc.T2, -8, bc, bs, orc.MXFP4))
+    cost["gemm"] = t / (rr * bc.shape[0] * (3584 // 32))
+    sample = (f"oracle on {r} x 3584 activations (MiX T1, T2), 3584 x {r} weights (MXFP4), "
+              f"{4 * r} x 4 x 128 keys (mean), {rr} x {r} outputs of K 3584 (Eq. (6) matmul); "
+              f"per-unit costs extrapolated to every call of one full step")
+    return cost, sample
+
+
+def cpu_step_seconds(cost, small=False):
+    return sum(cost[c[0]] * c[1] for *_, c in step_table(small))
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle as it stands, on the host cores, each
+    step a bounded sample of the workload extrapolated to the full step."""
+    if rank != 0:
+        return
+    roof = sum(roof_seconds(b, f) for _, b, f, _, _ in step_table())
+    est = []
+    sample = ""
+    budget = min(10.0, 150.0 / max(1, args.warmup + args.steps))   # whole run within a few minutes
+    for i in range(args.warmup + args.steps):
+        cost, sample = oracle_unit_costs(budget)
+        if i >= args.warmup:
+            est.append(cpu_step_seconds(cost))
+    sec = float(np.mean(est))
+    val = 100.0 * roof / sec
+    out = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64 / int64 (scalar C oracle)",
+           "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "sample": sample},
+           "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+           "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--small", action="store_true", help="1/8-size workload (for profiler captures)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    from quantized_vlm_gemm_mix_b300 import _build
+    _build.build()
+    from quantized_vlm_gemm_mix_b300 import mix, synth
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    calls, h2d, d2h, host, keep = build_workload(torch, mix, synth, dev, small=args.small)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        for i, c in enumerate(calls):
+            if events is not None:
+                events[i][0].record(stream)
+            c.fn()
+            if events is not None:
+                events[i][1].record(stream)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(v):
+        if not dist:
+            return v
+        t = torch.tensor([v], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    barrier()
+    assert mix.mix_device_error() == 0, "a kernel reported a timed-out wait"
+
+    # headline: K back-to-back steps, no per-call events
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    ms_step = max_over_ranks(t0.elapsed_time(t1)) / args.steps
+
+    # per-call durations (second timed pass, CUDA events on the launching stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+    per_call = np.zeros(len(calls))
+    for _ in range(args.steps):
+        step(ev)
+        torch.cuda.synchronize()
+        per_call += np.array([a.elapsed_time(b) for a, b in ev])
+    per_call /= args.steps
+
+    roof_s = sum(c.roof_s() for c in calls)
+    value = 100.0 * roof_s * world / (ms_step * 1e-3)
+
+    e2e = None
+    if not args.no_e2e:
+        pin_in = [(d, torch.from_numpy(h.view(np.int16) if h.dtype == np.uint16 else h).pin_memory())
+                  for d, h in h2d]
+        pin_out = [(d, torch.empty(d.shape, dtype=d.dtype).pin_memory()) for d in d2h]
+        bi = sum(p.numel() * p.element_size() for _, p in pin_in)
+        bo = sum(p.numel() * p.element_size() for _, p in pin_out)
+
+        def e2e_step():
+            for d, p in pin_in:
+                d.view(p.dtype).copy_(p, non_blocking=True)
+            step()
+            for d, p in pin_out:
+                p.copy_(d, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1)) / args.steps
+        e2e = {"value": round(100.0 * roof_s * world / (ms_e2e * 1e-3), 3), "unit": UNIT,
+               "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+    parts = {}
+    for c, ms in zip(calls, per_call):
+        e = {"ms": round(float(ms), 5), "GB/s": round(c.bytes / (ms * 1e-3) / 1e9, 1),
+             "frac_hbm": round(c.bytes / (ms * 1e-3) / 1e9 / HBM, 3), "roofline_ms": round(c.roof_s() * 1e3, 5)}
+        if c.flops:
+            e["TFLOP/s"] = round(c.flops / (ms * 1e-3) / 1e12, 1)
+            e["frac_mma"] = round(c.flops / (ms * 1e-3) / 1e12 / MX8_TFLOPS, 3)
+        parts[c.name] = e
+    dom = max(range(len(calls)), key=lambda i: calls[i].roof_s())
+    dc = calls[dom]
+    ach = dc.flops / (per_call[dom] * 1e-3) / 1e12
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "dominant_kernel_traffic.json")
+    if os.path.exists(tp) and not args.small:
+        tj = json.load(open(tp))
+        if tj.get("call") == dc.name and tj.get("kernel_version") == mix.mix_version():
+            traffic = tj.get("dram_bytes_per_launch")
+    roofline = {"bound": "tensor", "kernel": dc.name, "achieved": round(ach, 1), "peak": round(MX8_TFLOPS, 1),
+                "unit": "TFLOP/s", "frac": round(ach / MX8_TFLOPS, 4), "traffic": traffic,
+                "algorithmic_bytes": dc.bytes, "algorithmic_flops": dc.flops,
+                "peak_source": f"2 x measured bf16 sustained ({PEAKS['source']}); "
+                               f"burst {MX8_TFLOPS_BURST:.0f} TFLOP/s"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cost, sample = oracle_unit_costs(10.0)
+        sec = cpu_step_seconds(cost, args.small)
+        cpu = {"value": 100.0 * roof_s / sec, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+               "seconds_per_step": round(sec, 2)}
+    out = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None,
+           "dtype": "e4m3 x e4m3 -> fp32 (tcgen05 kind::mxf8f6f4); int32 shift-add; u8 codes",
+           "data": "synthetic (seeded; Qwen2-VL-7B / ViT / GQA-attention shapes, paper activation statistics)",
+           "config": {"workload": WORKLOAD + ("_small" if args.small else ""),
+                      "l2": "inputs larger than L2 (several GB per step; each tensor is evicted before reuse)",
+                      "parallelism": f"replicas x{world}", "roofline_ms_per_step": round(roof_s * 1e3, 4),
+                      "hbm_peak_gbs": HBM, "mma_peak_tflops": round(MX8_TFLOPS, 1)},
+           "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+           "gpu_launches": int(sum(c.launches for c in calls) * args.steps), "clocks": clk, "parts": parts}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    del keep
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
