@@ -210,6 +210,29 @@ MIX_API mix_status_t ksmooth_kv(const void* k, mix_dtype_t dtype, int64_t tokens
                         int64_t ld, float* mean, int mode, float* k_out, void* workspace,
                         size_t workspace_bytes, mix_stream_t stream);
 
+/* No-allocation variant of ksmooth_kv.  The paper has no counterpart for
+ * this entry point; it exists for callers that cannot give the library device
+ * memory: code that runs while a CUDA graph is being captured, hosts whose
+ * device memory belongs to their own allocator, and loops that must not call
+ * cudaMalloc (which can synchronise the device).  Arguments and results are
+ * those of ksmooth_kv; the caller still passes k, mean and k_out.  COMPUTE
+ * keeps its fp64 partial sums in a fixed array built into the library
+ * (KSMOOTH_NOALLOC_SCRATCH_BYTES, held on every GPU that loads the library
+ * until the process exits) and allocates nothing.
+ *  - Size limit: a COMPUTE call whose ksmooth_workspace_bytes(tokens, heads,
+ *    head_dim) exceeds KSMOOTH_NOALLOC_SCRATCH_BYTES is rejected with
+ *    MIX_ERR_WORKSPACE before any launch.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls share the array.  Calls ordered on one stream are safe; calls
+ *    whose kernels overlap on the GPU (other streams, other threads) race.
+ *    Nothing has to be cleared between calls: each call writes every partial
+ *    sum it later reads. */
+#define KSMOOTH_NOALLOC_SCRATCH_BYTES ((size_t)2 << 20)
+MIX_API mix_status_t ksmooth_kv_noalloc(const void* k, mix_dtype_t dtype, int64_t tokens, int heads,
+                                        int head_dim, int64_t ld, float* mean, int mode, float* k_out,
+                                        mix_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* Status and device error word.                                           */
 /* ---------------------------------------------------------------------- */

@@ -221,4 +221,23 @@ mix_status_t ksmooth_kv(const void* k, mix_dtype_t dtype, int64_t tokens, int he
                                   workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+mix_status_t ksmooth_kv_noalloc(const void* k, mix_dtype_t dtype, int64_t tokens, int heads, int head_dim,
+                                int64_t ld, float* mean, int mode, float* k_out, mix_stream_t stream) {
+  if (!valid_dtype(dtype) || tokens < 0 || heads <= 0 || head_dim <= 0) return MIX_ERR_INVALID_ARG;
+  if (mode != KSMOOTH_COMPUTE && mode != KSMOOTH_APPLY_FROZEN) return MIX_ERR_INVALID_ARG;
+  const int64_t C = (int64_t)heads * head_dim;
+  if (ld < C) return MIX_ERR_INVALID_ARG;
+  if (C % 8 != 0) return MIX_ERR_SHAPE;
+  if (mean == nullptr) return MIX_ERR_INVALID_ARG;
+  if (mode == KSMOOTH_COMPUTE && tokens == 0) return MIX_ERR_INVALID_ARG;
+  if (tokens > 0 && k == nullptr) return MIX_ERR_INVALID_ARG;
+  // the built-in scratch holds at most KSMOOTH_NOALLOC_SCRATCH_BYTES of partial sums
+  if (mode == KSMOOTH_COMPUTE && ksmooth_ws_bytes(tokens, heads, head_dim) > ksmooth_noalloc_scratch_bytes())
+    return MIX_ERR_WORKSPACE;
+  if (!aligned(k, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(mean, 16) || (k_out && !aligned(k_out, 16)))
+    return MIX_ERR_ALIGN;
+  return from_cuda(launch_ksmooth_noalloc(k, dtype == MIX_DT_BF16, tokens, heads, head_dim, ld, mean, mode,
+                                          k_out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

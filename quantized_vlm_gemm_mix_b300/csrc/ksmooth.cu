@@ -138,3 +138,56 @@ cudaError_t launch_ksmooth(const void* k, bool bf16, int64_t tokens, int heads, 
 }
 
 }  // namespace mixk
+
+// ---------------------------------------------------------------------------
+// No-allocation variant.  Some callers cannot hand the library device memory:
+// code running while a CUDA graph is being captured, hosts whose device memory
+// is owned by their own allocator, loops that must never call cudaMalloc (it
+// can synchronise the device).  For them the fp64 partial sums of COMPUTE live
+// in a fixed array compiled into the library instead of a caller workspace.
+// Every GPU that loads the library keeps this array until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace mixk {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)2 << 20;  // 2 MiB
+static __device__ __align__(256) double g_ksmooth_scratch[kNoAllocScratchBytes / sizeof(double)];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {nullptr};
+
+// Device address of g_ksmooth_scratch on the current device, looked up once
+// per device (in host code the symbol is only a host-side stand-in).
+cudaError_t scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_ksmooth_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+size_t ksmooth_noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+cudaError_t launch_ksmooth_noalloc(const void* k, bool bf16, int64_t tokens, int heads, int head_dim,
+                                   int64_t ld, float* mean, int mode, float* k_out, cudaStream_t st) {
+  void* ws = nullptr;
+  if (mode == KSMOOTH_COMPUTE) {
+    cudaError_t e = scratch_address(&ws);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_ksmooth(k, bf16, tokens, heads, head_dim, ld, mean, mode, k_out, ws, st);
+}
+
+}  // namespace mixk

@@ -35,6 +35,11 @@ cudaError_t launch_ksmooth(const void* k, bool bf16, int64_t tokens, int heads, 
                            int64_t ld, float* mean, int mode, float* k_out, void* ws,
                            cudaStream_t st);
 
+// K-smoothing with the library's built-in scratch (no caller workspace).
+size_t ksmooth_noalloc_scratch_bytes();
+cudaError_t launch_ksmooth_noalloc(const void* k, bool bf16, int64_t tokens, int heads, int head_dim,
+                                   int64_t ld, float* mean, int mode, float* k_out, cudaStream_t st);
+
 // Device error word (bounded waits).
 cudaError_t read_device_error(unsigned* word, bool clear);
 

@@ -29,7 +29,9 @@ KSMOOTH_COMPUTE, KSMOOTH_APPLY_FROZEN = 0, 1
 
 EXPORTS = ["mix_codes_bytes", "mix_shared_bytes", "mx_scales_bytes", "mix_quantize", "mx_quantize",
            "mix_dequantize", "mx_dequantize", "mix_mx_gemm_workspace_bytes", "mix_mx_gemm",
-           "ksmooth_workspace_bytes", "ksmooth_kv", "mix_status_str", "mix_device_error", "mix_version"]
+           "ksmooth_workspace_bytes", "ksmooth_kv", "ksmooth_kv_noalloc", "mix_status_str", "mix_device_error",
+           "mix_version"]
+KSMOOTH_NOALLOC_SCRATCH_BYTES = 2 << 20
 
 
 class MixError(RuntimeError):
@@ -73,6 +75,7 @@ def _load():
         "mix_mx_gemm": (I, [ctypes.POINTER(GemmDesc), P, S, P]),
         "ksmooth_workspace_bytes": (S, [I64, I, I]),
         "ksmooth_kv": (I, [P, I, I64, I, I, I64, P, I, P, P, S, P]),
+        "ksmooth_kv_noalloc": (I, [P, I, I64, I, I, I64, P, I, P, P]),
         "mix_status_str": (ctypes.c_char_p, [I]),
         "mix_device_error": (I, [ctypes.POINTER(ctypes.c_uint), I]),
         "mix_version": (I, []),
@@ -173,6 +176,14 @@ def ksmooth_kv(k, tokens, heads, head_dim, ld, mean, mode, k_out, workspace=None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib.ksmooth_kv(_ptr(k), _dtype(k), tokens, heads, head_dim, ld, _ptr(mean), mode, _ptr(k_out),
                           _ptr(workspace), ws_bytes, _stream(stream)), "ksmooth_kv")
+
+
+def ksmooth_kv_noalloc(k, tokens, heads, head_dim, ld, mean, mode, k_out, stream=None) -> None:
+    """ksmooth_kv without a workspace: for callers that cannot allocate device
+    memory (graph capture, externally owned allocators).  COMPUTE is limited to
+    KSMOOTH_NOALLOC_SCRATCH_BYTES of partial sums; see include/mix.h."""
+    _check(lib.ksmooth_kv_noalloc(_ptr(k), _dtype(k), tokens, heads, head_dim, ld, _ptr(mean), mode,
+                                  _ptr(k_out), _stream(stream)), "ksmooth_kv_noalloc")
 
 
 def mix_device_error(clear: bool = True) -> int:
