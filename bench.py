@@ -492,6 +492,21 @@ def main():
     barrier()
     assert mix.mix_device_error() == 0, "a kernel reported a timed-out wait"
 
+    # One step captured as a CUDA graph: the ~30 launches replay without host
+    # gaps (every library call is asynchronous and allocation-free).
+    run, timing_mode = step, "eager"
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        run, timing_mode = graph.replay, "cuda graph"
+        for _ in range(2):
+            run()
+        barrier()
+    except Exception as exc:  # keep measuring eagerly, and say so
+        timing_mode = f"eager (graph capture failed: {type(exc).__name__})"
+        barrier()
+
     # headline: K back-to-back steps, no per-call events
     clocks = ClockSampler(local)
     clocks.start()
@@ -499,17 +514,26 @@ def main():
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(args.steps):
-        step()
+        run()
     t1.record(stream)
     barrier()
     clk = clocks.stop()
     ms_step = max_over_ranks(t0.elapsed_time(t1)) / args.steps
+    assert mix.mix_device_error() == 0, "a kernel reported a timed-out wait"
 
-    # per-call durations (second timed pass, CUDA events on the launching stream)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+    # Per-call durations: a second timed pass, CUDA events on the launching
+    # stream around each call.  A short spin kernel before every call keeps
+    # the GPU busy while the host enqueues it, so the events bracket device
+    # time only, not host launch gaps.
     per_call = np.zeros(len(calls))
+    percall_mode = "events per call, spin kernel ahead of each launch"
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
     for _ in range(args.steps):
-        step(ev)
+        for i, c in enumerate(calls):
+            torch.cuda._sleep(400000)
+            ev[i][0].record(stream)
+            c.fn()
+            ev[i][1].record(stream)
         torch.cuda.synchronize()
         per_call += np.array([a.elapsed_time(b) for a, b in ev])
     per_call /= args.steps
@@ -528,7 +552,7 @@ def main():
         def e2e_step():
             for d, p in pin_in:
                 d.view(p.dtype).copy_(p, non_blocking=True)
-            step()
+            run()
             for d, p in pin_out:
                 p.copy_(d, non_blocking=True)
 
@@ -581,7 +605,8 @@ def main():
            "config": {"workload": WORKLOAD + ("_small" if args.small else ""),
                       "l2": "inputs larger than L2 (several GB per step; each tensor is evicted before reuse)",
                       "parallelism": f"replicas x{world}", "roofline_ms_per_step": round(roof_s * 1e3, 4),
-                      "hbm_peak_gbs": HBM, "mma_peak_tflops": round(MX8_TFLOPS, 1)},
+                      "hbm_peak_gbs": HBM, "mma_peak_tflops": round(MX8_TFLOPS, 1), "timing": timing_mode,
+                      "per_call_timing": percall_mode},
            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
            "gpu_launches": int(sum(c.launches for c in calls) * args.steps), "clocks": clk, "parts": parts}
     if rank == 0:

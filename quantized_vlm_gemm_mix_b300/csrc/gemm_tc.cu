@@ -51,26 +51,33 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int KB = BK / 2;  // code bytes per row per stage
-constexpr int S_CODES = 4, S_OPS = 2;
+constexpr int S_CODES = 4;
 constexpr int A_CODES = BM * KB, B_CODES = BN * KB;  // 8 KB, 16 KB
-constexpr int A_OPS = BM * BK, B_OPS = BN * BK;      // 16 KB, 32 KB
-constexpr int NUM_THREADS = 384;
-constexpr int DEC_WARP0 = 4, NUM_DEC_WARPS = 8;
+constexpr int A_OPS = BM * BK, B_OPS = BN * BK;      // 16 KB, 32 KB (also the padded E2M1 tile)
+constexpr int DEC_WARP0 = 4, NUM_DEC_WARPS = 16;
+constexpr int NUM_THREADS = (DEC_WARP0 + NUM_DEC_WARPS) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL = 256;  // stage s: A scales at SF_COL + 16 s (4 cols), B at + 4 (8 cols)
 constexpr long long WAIT_LIMIT = 1LL << 31;  // SM clocks, about one second
 
-// Shared memory plan (offsets from a 1024-byte aligned base).
-constexpr int OFF_AOPS = 0;
-constexpr int OFF_BOPS = OFF_AOPS + S_OPS * A_OPS;
-constexpr int OFF_ACODES = OFF_BOPS + S_OPS * B_OPS;
-constexpr int OFF_BCODES = OFF_ACODES + S_CODES * A_CODES;
-constexpr int OFF_SFA = OFF_BCODES + S_CODES * B_CODES;  // [S_OPS][BM] scale words
-constexpr int OFF_SFB = OFF_SFA + S_OPS * BM * 4;        // [S_OPS][BN]
-constexpr int OFF_BAR = OFF_SFB + S_OPS * BN * 4;
-constexpr int NUM_BARS = 2 * S_CODES + 3 * S_OPS + 2;
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for the 1024-byte alignment
+// Shared memory plan (offsets from a 1024-byte aligned base).  B_NATIVE: the
+// MXFP4 weight tile goes straight from HBM into the MMA operand buffer (TMA
+// unpacks 16 x E2M1 into 16-byte slots), so there is no B code ring and the
+// operand ring is one stage deeper.
+template <bool B_NATIVE>
+struct Plan {
+  static constexpr int S_OPS = B_NATIVE ? 3 : 2;
+  static constexpr int OFF_AOPS = 0;
+  static constexpr int OFF_BOPS = OFF_AOPS + S_OPS * A_OPS;
+  static constexpr int OFF_ACODES = OFF_BOPS + S_OPS * B_OPS;
+  static constexpr int OFF_BCODES = OFF_ACODES + S_CODES * A_CODES;
+  static constexpr int OFF_SFA = OFF_BCODES + (B_NATIVE ? 0 : S_CODES * B_CODES);  // [S_OPS][BM] words
+  static constexpr int OFF_SFB = OFF_SFA + S_OPS * BM * 4;                           // [S_OPS][BN] words
+  static constexpr int OFF_BAR = OFF_SFB + S_OPS * BN * 4;
+  static constexpr int NUM_BARS = 2 * S_CODES + 4 * S_OPS + 2;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for the 1024-byte alignment
+};
 
 struct TcParams {
   int64_t M, N, K, batch, b_group;
@@ -89,31 +96,35 @@ struct TcParams {
 };
 
 // ------------------------------------------------------------------ decode
-// Four MiX nibbles (low 16 bits of v) -> four e4m3 bytes +-(1.m3) 2^(1-de);
-// 0x7 -> 0, 0xF (recycled -0) -> +(1.m3) 2^-6.
-__device__ __forceinline__ uint32_t mix_to_e4m3_x4(uint32_t v, uint32_t m3) {
+// Nibble -> e4m3 byte through two 8-entry tables (by the low three bits) and
+// a byte select by the sign bit: one prmt per table half and one to pick
+// between the positive and the negative candidate of every byte.
+struct DecTab {
+  uint32_t plo, phi, nlo, nhi;
+};
+// MiX element (s, de) with shared mantissa m3: +-(1.m3) 2^(1-de); code 0x7
+// is zero and 0xF the recycled -0, +(1.m3) 2^-6.
+__device__ __forceinline__ DecTab mix_tab(uint32_t m3) {
   const uint32_t m3x = m3 * 0x01010101u;
-  const uint32_t mag = ptx::prmt(0x28303840u | m3x, 0x00101820u | (m3 * 0x00010101u), v & 0x7777u);
-  const uint32_t z = ptx::prmt(0u, 0x80000000u, v & 0xFFFFu);  // 0xFF at 0xF, 0x80 at 0x7
-  const uint32_t t = ptx::prmt(v, 0u, 0x1100u);
-  const uint32_t sgn = (t & 0x80008000u) | ((t << 4) & 0x00800080u);
-  const uint32_t asym = z & 0x7F7F7F7Fu & (0x08080808u | m3x);
-  return mag | asym | (sgn & ~z & 0x80808080u);
+  DecTab t;
+  t.plo = 0x28303840u | m3x;
+  t.phi = 0x00101820u | (m3x & 0x00FFFFFFu);
+  t.nlo = t.plo | 0x80808080u;
+  t.nhi = 0x089098A0u | m3x;
+  return t;
 }
-// Four E2M1 nibbles -> e4m3.
-__device__ __forceinline__ uint32_t fp4_to_e4m3_x4(uint32_t v) {
-  const uint32_t mag = ptx::prmt(0x3C383000u, 0x4C484440u, v & 0x7777u);
-  const uint32_t t = ptx::prmt(v, 0u, 0x1100u);
-  return mag | (t & 0x80008000u) | ((t << 4) & 0x00800080u);
-}
-// Four INT4 nibbles (two's complement q) -> e4m3 of q / 4.
-__device__ __forceinline__ uint32_t int4_to_e4m3_x4(uint32_t v) {
-  const uint32_t sel = v & 0x7777u;
-  const uint32_t pos = ptx::prmt(0x34302800u, 0x3E3C3A38u, sel);
-  const uint32_t neg = ptx::prmt(0xBABCBEC0u, 0xA8B0B4B8u, sel);
-  uint32_t m = ptx::prmt(0x80808080u, 0x80808080u, v & 0xFFFFu) ^ 0x80808080u;  // 0x7F where negative
-  m |= (m << 1) & 0x80808080u;
-  return (pos & ~m) | (neg & m);
+// INT4 two's complement q -> q / 4; E2M1 -> its value.
+__device__ __forceinline__ DecTab int4_tab() { return DecTab{0x34302800u, 0x3E3C3A38u, 0xBABCBEC0u, 0xA8B0B4B8u}; }
+__device__ __forceinline__ DecTab fp4_tab() { return DecTab{0x3C383000u, 0x4C484440u, 0xBCB8B080u, 0xCCC8C4C0u}; }
+
+// Eight nibbles (element i in bits 4i..4i+3) -> eight e4m3 bytes.
+__device__ __forceinline__ uint2 dec8(uint32_t v, const DecTab& t) {
+  const uint32_t s7 = v & 0x77777777u, s2 = (v >> 1) & 0x44444444u;
+  const uint32_t s7h = s7 >> 16, s2h = s2 >> 16;
+  uint2 r;
+  r.x = ptx::prmt(ptx::prmt(t.plo, t.phi, s7), ptx::prmt(t.nlo, t.nhi, s7), s2 | 0x3210u);
+  r.y = ptx::prmt(ptx::prmt(t.plo, t.phi, s7h), ptx::prmt(t.nlo, t.nhi, s7h), s2h | 0x3210u);
+  return r;
 }
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a K-major operand tile
@@ -177,34 +188,42 @@ __device__ __forceinline__ void epi_quant_block(const uint32_t* u, const TcParam
   codes = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+template <bool B_NATIVE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const TcParams p) {
+  using L = Plan<B_NATIVE>;
+  constexpr int S_OPS = L::S_OPS;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* codes_full = bars;
   uint64_t* codes_empty = bars + S_CODES;
-  uint64_t* ops_full = bars + 2 * S_CODES;
-  uint64_t* ops_empty = bars + 2 * S_CODES + S_OPS;
-  uint64_t* sf_ready = bars + 2 * S_CODES + 2 * S_OPS;
-  uint64_t* acc_full = bars + 2 * S_CODES + 3 * S_OPS;
+  uint64_t* ops_full = bars + 2 * S_CODES;             // decoders: A operand + scale columns
+  uint64_t* ops_empty = ops_full + S_OPS;              // MMA commit
+  uint64_t* sf_ready = ops_empty + S_OPS;              // decoders: scale words in smem
+  uint64_t* b_full = sf_ready + S_OPS;                 // TMA: native B operand
+  uint64_t* acc_full = b_full + S_OPS;
   uint64_t* drain = acc_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
-  volatile int* never = reinterpret_cast<volatile int*>(smem + OFF_MISC + 8);  // drains ignore aborts
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  volatile int* never = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);  // drains ignore aborts
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m0 = (int64_t)blockIdx.x * BM, n0 = (int64_t)blockIdx.y * BN, bt = blockIdx.z;
   const int num_k = (int)((p.K + BK - 1) / BK);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S_CODES; ++i) { ptx::mbar_init(&codes_full[i], 1); ptx::mbar_init(&codes_empty[i], NUM_DEC_WARPS); }
+    for (int i = 0; i < S_CODES; ++i) {
+      ptx::mbar_init(&codes_full[i], 1);
+      ptx::mbar_init(&codes_empty[i], NUM_DEC_WARPS);
+    }
     for (int i = 0; i < S_OPS; ++i) {
       ptx::mbar_init(&ops_full[i], NUM_DEC_WARPS);
       ptx::mbar_init(&ops_empty[i], 1);
       ptx::mbar_init(&sf_ready[i], NUM_DEC_WARPS);
+      ptx::mbar_init(&b_full[i], 1);
     }
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(drain, 1);
@@ -226,32 +245,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int issued = 0;
+      int issued = 0, issued_b = 0;
       for (int kt = 0; kt < num_k; ++kt) {
         const int s = kt % S_CODES, n = kt / S_CODES;
-        if (n > 0 && !ptx::mbar_wait(&codes_empty[s], (n - 1) & 1, WAIT_LIMIT, abort_flag)) { flag_error(1u, abort_flag); break; }
+        if (n > 0 && !ptx::mbar_wait(&codes_empty[s], (n - 1) & 1, WAIT_LIMIT, abort_flag)) {
+          flag_error(1u, abort_flag);
+          break;
+        }
         if (*abort_flag) break;
-        ptx::mbar_arrive_expect_tx(&codes_full[s], A_CODES + B_CODES);
-        ptx::tma_load_3d(smem + OFF_ACODES + s * A_CODES, &tmap_a, &codes_full[s], kt * KB, (int)m0, (int)bt);
-        ptx::tma_load_3d(smem + OFF_BCODES + s * B_CODES, &tmap_b, &codes_full[s], kt * KB, (int)n0,
-                         (int)(bt / p.b_group));
+        ptx::mbar_arrive_expect_tx(&codes_full[s], B_NATIVE ? A_CODES : A_CODES + B_CODES);
+        ptx::tma_load_3d(smem + L::OFF_ACODES + s * A_CODES, &tmap_a, &codes_full[s], kt * KB, (int)m0, (int)bt);
+        if (!B_NATIVE)
+          ptx::tma_load_3d(smem + L::OFF_BCODES + s * B_CODES, &tmap_b, &codes_full[s], kt * KB, (int)n0,
+                           (int)(bt / p.b_group));
         ++issued;
+        if (B_NATIVE) {
+          const int os = kt % S_OPS, on = kt / S_OPS;
+          if (on > 0 && !ptx::mbar_wait(&ops_empty[os], (on - 1) & 1, WAIT_LIMIT, abort_flag)) {
+            flag_error(64u, abort_flag);
+            break;
+          }
+          if (*abort_flag) break;
+          // the transaction count of the unpacking load is the packed size
+          ptx::mbar_arrive_expect_tx(&b_full[os], B_OPS / 2);
+          ptx::tma_load_3d(smem + L::OFF_BOPS + os * B_OPS, &tmap_b, &b_full[os], kt * BK, (int)n0,
+                           (int)(bt / p.b_group));
+          ++issued_b;
+        }
       }
       // drain: every issued copy lands before the CTA may exit
       for (int kt = (issued > S_CODES ? issued - S_CODES : 0); kt < issued; ++kt)
         ptx::mbar_wait(&codes_full[kt % S_CODES], (kt / S_CODES) & 1, WAIT_LIMIT, never);
+      for (int kt = (issued_b > S_OPS ? issued_b - S_OPS : 0); kt < issued_b; ++kt)
+        ptx::mbar_wait(&b_full[kt % S_OPS], (kt / S_OPS) & 1, WAIT_LIMIT, never);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      const uint32_t b_fmt = 0;  // B decoded to E4M3
+      const uint32_t b_fmt = B_NATIVE ? 5u : 0u;  // E2M1 or E4M3
       for (int kt = 0; kt < num_k; ++kt) {
         const int s = kt % S_OPS, n = kt / S_OPS;
         if (!ptx::mbar_wait(&ops_full[s], n & 1, WAIT_LIMIT, abort_flag)) { flag_error(2u, abort_flag); break; }
+        if (B_NATIVE && !ptx::mbar_wait(&b_full[s], n & 1, WAIT_LIMIT, abort_flag)) {
+          flag_error(128u, abort_flag);
+          break;
+        }
         if (*abort_flag) break;
         ptx::tc_fence_after();
-        const uint32_t a_addr = ptx::smem_u32(smem + OFF_AOPS + s * A_OPS);
-        const uint32_t b_addr = ptx::smem_u32(smem + OFF_BOPS + s * B_OPS);
+        const uint32_t a_addr = ptx::smem_u32(smem + L::OFF_AOPS + s * A_OPS);
+        const uint32_t b_addr = ptx::smem_u32(smem + L::OFF_BOPS + s * B_OPS);
         const uint32_t sfa = tmem + SF_COL + 16u * s, sfb = sfa + 4u;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -266,94 +308,97 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp >= DEC_WARP0) {
     // ------------------------------------------------------------ decoders
-    const int dt = threadIdx.x - DEC_WARP0 * 32;
-    const int arow = dt >> 1, ahalf = dt & 1;  // A: two threads per row, 64 elements each
+    const int dt = threadIdx.x - DEC_WARP0 * 32;  // 0 .. 511
+    const int arow = dt >> 2, ablk = dt & 3;       // A: one 32-block per thread
     const int64_t am = m0 + arow;
-    const int brow = dt;  // B: one thread per row, 128 elements
-    const int64_t bn = n0 + brow;
     const int64_t a_row_elem = bt * p.a_bs + am * p.a_ld;
-    const int64_t b_row_elem = (bt / p.b_group) * p.b_bs + bn * p.b_ld;
-    uint32_t* sfa_s = reinterpret_cast<uint32_t*>(smem + OFF_SFA);
-    uint32_t* sfb_s = reinterpret_cast<uint32_t*>(smem + OFF_SFB);
+    const int brow = dt >> 1, bhalf = dt & 1;      // B decode: 64 elements per thread
+    const bool b_scale_thread = dt < BN;           // B scale words: one row per thread
+    const int64_t bsn = n0 + dt;
+    const int64_t b_row_elem = (bt / p.b_group) * p.b_bs + bsn * p.b_ld;
+    uint32_t* sfa_s = reinterpret_cast<uint32_t*>(smem + L::OFF_SFA);
+    uint32_t* sfb_s = reinterpret_cast<uint32_t*>(smem + L::OFF_SFB);
+    const DecTab btab = p.b_fp4 ? fp4_tab() : int4_tab();
+    // The A shared field and the four B scale bytes of a k-step come from L2;
+    // they are fetched two k-steps ahead so their latency stays hidden.
+    const bool b_words = (b_row_elem % 128) == 0;  // four scale bytes of a k-step form one aligned word
+    auto fetch_a = [&](int kt) -> uint32_t {
+      const int64_t ka = (int64_t)kt * BK + 32 * ablk;
+      if (kt >= num_k || am >= p.M || ka >= p.K) return 0u;
+      const int64_t idx = (a_row_elem + ka) / 32;
+      return p.a_type == 1 ? (uint32_t)__ldg(static_cast<const uint8_t*>(p.a_shared) + idx)
+                           : (uint32_t)__ldg(static_cast<const uint16_t*>(p.a_shared) + idx);
+    };
+    auto fetch_b = [&](int kt) -> uint32_t {
+      if (!b_scale_thread || kt >= num_k) return 0x7F7F7F7Fu;
+      const int64_t k0 = (int64_t)kt * BK;
+      if (bsn < p.N && b_words && k0 + BK <= p.K)
+        return __ldg(reinterpret_cast<const uint32_t*>(p.b_scales + (b_row_elem + k0) / 32));
+      uint32_t w = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t k = k0 + 32 * i;
+        const uint32_t sc = (bsn < p.N && k < p.K) ? (uint32_t)__ldg(p.b_scales + (b_row_elem + k) / 32) : 127u;
+        w |= sc << (8 * i);
+      }
+      return w;
+    };
+    uint32_t a_pf0 = fetch_a(0), a_pf1 = fetch_a(1);
+    uint32_t b_pf0 = fetch_b(0), b_pf1 = fetch_b(1);
     bool ok = true;
     for (int kt = 0; kt < num_k && ok; ++kt) {
       const int cs = kt % S_CODES, cn = kt / S_CODES;
       const int os = kt % S_OPS, on = kt / S_OPS;
-      // shared fields of A (two blocks) and B scales (four blocks), from L2
-      uint32_t a_sh[2] = {0, 0};
-      bool a_in[2];
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int64_t k = (int64_t)kt * BK + ahalf * 64 + 32 * i;
-        a_in[i] = am < p.M && k < p.K;
-        if (a_in[i]) {
-          const int64_t idx = (a_row_elem + k) / 32;
-          a_sh[i] = p.a_type == 1 ? (uint32_t)static_cast<const uint8_t*>(p.a_shared)[idx]
-                                  : (uint32_t)static_cast<const uint16_t*>(p.a_shared)[idx];
-        }
-      }
-      uint32_t bsw = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int64_t k = (int64_t)kt * BK + 32 * i;
-        const uint32_t sc = (bn < p.N && k < p.K) ? (uint32_t)p.b_scales[(b_row_elem + k) / 32] : 127u;
-        bsw |= sc << (8 * i);
-      }
+      const int64_t ka = (int64_t)kt * BK + 32 * ablk;
+      const bool a_in = am < p.M && ka < p.K;
+      const uint32_t a_sh = a_pf0, bsw = b_pf0;
+      a_pf0 = a_pf1;
+      b_pf0 = b_pf1;
+      a_pf1 = fetch_a(kt + 2);
+      b_pf1 = fetch_b(kt + 2);
       if (!ptx::mbar_wait(&codes_full[cs], cn & 1, WAIT_LIMIT, abort_flag)) { flag_error(4u, abort_flag); ok = false; break; }
       if (on > 0) {
-        if (!ptx::mbar_wait(&ops_empty[os], (on - 1) & 1, WAIT_LIMIT, abort_flag)) { flag_error(8u, abort_flag); ok = false; break; }
+        if (!ptx::mbar_wait(&ops_empty[os], (on - 1) & 1, WAIT_LIMIT, abort_flag)) {
+          flag_error(8u, abort_flag);
+          ok = false;
+          break;
+        }
         ptx::tc_fence_after();
       }
       if (*abort_flag) { ok = false; break; }
-      // --- A: 64 elements (two 32-blocks) of row arow
+      // --- A: one 32-block (two 16-element chunks) of row arow
       {
-        const unsigned char* src = smem + OFF_ACODES + cs * A_CODES + arow * KB + ahalf * 32;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(src);
-        const uint4 c1 = *reinterpret_cast<const uint4*>(src + 16);
-        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        unsigned char* dst = smem + OFF_AOPS + os * A_OPS;
-        uint32_t sfw = 0;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {  // block i of this half
-          const uint32_t sh = a_sh[i];
-          const int emax = (int)(sh & 0xFu) + p.a_ebias;
-          sfw |= (a_in[i] ? (uint32_t)clampi(emax + 126, 1, 254) : 127u) << (8 * i);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {  // 8-element sub-block q: one code word
-            const uint32_t m3 = p.a_type == 1 ? ((sh >> 4) & 7u) : ((sh >> (4 + 3 * q)) & 7u);
-            const uint32_t w = cw[4 * i + q];
-            const uint32_t lo = mix_to_e4m3_x4(w, m3), hi = mix_to_e4m3_x4(w >> 16, m3);
-            const int chunk = ahalf * 4 + i * 2 + (q >> 1);
-            uint2* d = reinterpret_cast<uint2*>(dst + sw128_off(arow, chunk) + (q & 1) * 8);
-            *d = make_uint2(lo, hi);
-          }
+        const uint4 cv = *reinterpret_cast<const uint4*>(smem + L::OFF_ACODES + cs * A_CODES + arow * KB + ablk * 16);
+        unsigned char* dst = smem + L::OFF_AOPS + os * A_OPS;
+        uint2 e[4];
+        if (p.a_type == 1) {
+          const DecTab t = mix_tab((a_sh >> 4) & 7u);
+          e[0] = dec8(cv.x, t); e[1] = dec8(cv.y, t); e[2] = dec8(cv.z, t); e[3] = dec8(cv.w, t);
+        } else {
+          e[0] = dec8(cv.x, mix_tab((a_sh >> 4) & 7u));
+          e[1] = dec8(cv.y, mix_tab((a_sh >> 7) & 7u));
+          e[2] = dec8(cv.z, mix_tab((a_sh >> 10) & 7u));
+          e[3] = dec8(cv.w, mix_tab((a_sh >> 13) & 7u));
         }
-        reinterpret_cast<uint16_t*>(sfa_s + os * BM + arow)[ahalf] = (uint16_t)sfw;
+        *reinterpret_cast<uint4*>(dst + sw128_off(arow, 2 * ablk)) = make_uint4(e[0].x, e[0].y, e[1].x, e[1].y);
+        *reinterpret_cast<uint4*>(dst + sw128_off(arow, 2 * ablk + 1)) = make_uint4(e[2].x, e[2].y, e[3].x, e[3].y);
+        const int emax = (int)(a_sh & 0xFu) + p.a_ebias;
+        reinterpret_cast<uint8_t*>(sfa_s + os * BM + arow)[ablk] =
+            (uint8_t)(a_in ? (uint32_t)clampi(emax + 126, 1, 254) : 127u);
       }
-      // --- B: 128 elements of row brow
-      {
-        const unsigned char* src = smem + OFF_BCODES + cs * B_CODES + brow * KB;
-        unsigned char* dst = smem + OFF_BOPS + os * B_OPS;
+      // --- B (decoded mode): 64 elements (4 chunks) of row brow
+      if (!B_NATIVE) {
+        const unsigned char* src = smem + L::OFF_BCODES + cs * B_CODES + brow * KB + bhalf * 32;
+        unsigned char* dst = smem + L::OFF_BOPS + os * B_OPS;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           const uint4 cv = *reinterpret_cast<const uint4*>(src + 16 * c);
-          const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {  // two 16-element chunks per 16 code bytes
-            const uint32_t w0 = cw[2 * h], w1 = cw[2 * h + 1];
-            uint4 o;
-            if (p.b_fp4) {
-              o = make_uint4(fp4_to_e4m3_x4(w0), fp4_to_e4m3_x4(w0 >> 16), fp4_to_e4m3_x4(w1),
-                             fp4_to_e4m3_x4(w1 >> 16));
-            } else {
-              o = make_uint4(int4_to_e4m3_x4(w0), int4_to_e4m3_x4(w0 >> 16), int4_to_e4m3_x4(w1),
-                             int4_to_e4m3_x4(w1 >> 16));
-            }
-            *reinterpret_cast<uint4*>(dst + sw128_off(brow, 2 * c + h)) = o;
-          }
+          const uint2 e0 = dec8(cv.x, btab), e1 = dec8(cv.y, btab), e2 = dec8(cv.z, btab), e3 = dec8(cv.w, btab);
+          *reinterpret_cast<uint4*>(dst + sw128_off(brow, bhalf * 4 + 2 * c)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
+          *reinterpret_cast<uint4*>(dst + sw128_off(brow, bhalf * 4 + 2 * c + 1)) = make_uint4(e2.x, e2.y, e3.x, e3.y);
         }
-        sfb_s[os * BN + brow] = bsw;
       }
+      if (b_scale_thread) sfb_s[os * BN + dt] = bsw;
       // codes slot free and this warp's scale words published
       __syncwarp();
       if (lane == 0) {
@@ -378,16 +423,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&ops_full[os]);
     }
+    (void)btab; (void)brow; (void)bhalf;
     // --------------------------------------------------------- epilogue
-    if (warp < DEC_WARP0 + 4) {
+    // All sixteen decoder warps: warp w reads TMEM lane quadrant w % 4 (the
+    // only one it may access) and a quarter of the tile's columns.
+    {
       const bool got = ok && !*abort_flag && ptx::mbar_wait(acc_full, 0, WAIT_LIMIT, abort_flag);
       if (!got) {
         if (ok && !*abort_flag) flag_error(16u, abort_flag);
       } else {
         ptx::tc_fence_after();
         const uint32_t q = (uint32_t)(warp & 3);
+        const int cg = (warp - DEC_WARP0) >> 2;  // column quarter 0..3
         const int64_t row = m0 + 32 * q + lane;
-        for (int cc = 0; cc < BN / 32; ++cc) {
+        for (int cc = cg * (BN / 128); cc < (cg + 1) * (BN / 128); ++cc) {
           uint32_t u[32];
           ptx::tmem_ld_x32(tmem + ((32u * q) << 16) + (uint32_t)(cc * 32), u);
           ptx::tmem_wait_ld();
@@ -459,6 +508,42 @@ bool make_code_map(CUtensorMap* m, const void* base, int64_t k, int64_t rows, in
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over a packed E2M1 plane read straight into the MMA operand layout:
+// TMA unpacks every 16 x 4-bit group into a 16-byte slot (8 bytes of data, 8
+// of padding) and applies the 128-byte swizzle, giving 128-byte K-major rows
+// of 128 elements.  Needs K % 128 == 0, 32-byte aligned base and strides.
+bool make_fp4_operand_map(CUtensorMap* m, const void* base, int64_t k, int64_t rows, int64_t batch,
+                          int64_t ld_elems, int64_t bs_elems) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  if (k % 128 != 0 || (reinterpret_cast<uintptr_t>(base) & 31) != 0 || (ld_elems / 2) % 32 != 0) return false;
+  int64_t bs = bs_elems / 2;
+  if (batch <= 1 || bs <= 0) bs = (ld_elems / 2) * rows;
+  if (bs % 32 != 0) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)k, (cuuint64_t)rows, (cuuint64_t)batch};
+  const cuuint64_t strides[2] = {(cuuint64_t)(ld_elems / 2), (cuuint64_t)bs};
+  const cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)BN, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool B_NATIVE>
+cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, dim3 grid, cudaStream_t st) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<B_NATIVE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Plan<B_NATIVE>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  gemm_tc_kernel<B_NATIVE><<<grid, NUM_THREADS, Plan<B_NATIVE>::SMEM_BYTES, st>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, cudaStream_t st, mix_status_t* why) {
@@ -469,8 +554,15 @@ cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, cudaStream_t st, mix_status
   }
   const int64_t bb = (d.batch + d.b_group - 1) / d.b_group;
   CUtensorMap ma, mb;
-  if (!make_code_map(&ma, d.a_codes, d.K, d.M, d.batch, d.a_ld, d.a_batch_stride, BM) ||
-      !make_code_map(&mb, d.b_codes, d.K, d.N, bb, d.b_ld, d.b_batch_stride, BN)) {
+  if (!make_code_map(&ma, d.a_codes, d.K, d.M, d.batch, d.a_ld, d.a_batch_stride, BM)) {
+    *why = MIX_ERR_UNSUPPORTED;
+    return cudaSuccess;
+  }
+  // MXFP4 weights feed the MMA directly when the plane meets the unpacking
+  // TMA's rules; otherwise (and for MXINT4) the decoders convert them.
+  const bool native = d.b_type == MX_FP4_E2M1 &&
+                      make_fp4_operand_map(&mb, d.b_codes, d.K, d.N, bb, d.b_ld, d.b_batch_stride);
+  if (!native && !make_code_map(&mb, d.b_codes, d.K, d.N, bb, d.b_ld, d.b_batch_stride, BN)) {
     *why = MIX_ERR_UNSUPPORTED;
     return cudaSuccess;
   }
@@ -482,15 +574,8 @@ cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, cudaStream_t st, mix_status
   p.c = d.c; p.ldc = d.ldc; p.cbs = d.c_batch_stride;
   p.epi = (int)d.epi; p.epi_ebias = d.epi_ebias; p.epi_flags = d.epi_flags;
   p.out_codes = d.out_codes; p.out_shared = d.out_shared; p.out_ld = d.out_ld; p.out_bs = d.out_batch_stride;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   const dim3 grid((unsigned)((d.M + BM - 1) / BM), (unsigned)((d.N + BN - 1) / BN), (unsigned)d.batch);
-  gemm_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, p);
-  return cudaGetLastError();
+  return native ? launch_tc<true>(ma, mb, p, grid, st) : launch_tc<false>(ma, mb, p, grid, st);
 }
 
 }  // namespace mixk
