@@ -150,22 +150,24 @@ __device__ __forceinline__ void epi_quant_block(const uint32_t* u, const TcParam
   shared = 0;
   if (p.epi == MIX_EPI_MIX_T1 || p.epi == MIX_EPI_MIX_T2) {
     const bool asym = (p.epi_flags & MIX_ASYM_ZERO) != 0;
-    if (kb == 0u) {
+    int f, m3;
+    if (!max_exp_mant(kb, &f, &m3)) {
       w[0] = w[1] = w[2] = w[3] = 0x77777777u;
     } else {
-      int f, m3;
-      max_exp_mant(kb, &f, &m3);
       const int emax = clampi(f, p.epi_ebias, p.epi_ebias + 15);
       uint32_t m3bits = 0;
       bool all_zero = true;
+      const MixBlk b1 = mix_blk(emax, 8 + m3, asym);
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         int ms = m3;
         if (p.epi == MIX_EPI_MIX_T2) {
-          ms = 0;
-          if (ks[s] != 0u) { int fs; max_exp_mant(ks[s], &fs, &ms); }
+          int fs;
+          if (!max_exp_mant(ks[s], &fs, &ms)) ms = 0;
+          w[s] = mix_codes8(u + 8 * s, mix_blk(emax, 8 + ms, asym));
+        } else {
+          w[s] = mix_codes8(u + 8 * s, b1);
         }
-        w[s] = mix_codes8(u + 8 * s, emax, 8 + ms, asym);
         const bool z = w[s] == 0x77777777u;
         all_zero &= z;
         if (z) ms = 0;
@@ -191,7 +193,7 @@ __device__ __forceinline__ void epi_quant_block(const uint32_t* u, const TcParam
 template <bool B_NATIVE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmap_c, const TcParams p) {
   using L = Plan<B_NATIVE>;
   constexpr int S_OPS = L::S_OPS;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -436,24 +438,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t q = (uint32_t)(warp & 3);
         const int cg = (warp - DEC_WARP0) >> 2;  // column quarter 0..3
         const int64_t row = m0 + 32 * q + lane;
+        // fp32 C leaves through a per-warp 32 x 32 staging tile (128-byte
+        // swizzled, in the drained B operand ring) and a TMA store, which
+        // writes whole lines and clips the ragged edges of the matrix.
+        unsigned char* stage = smem + L::OFF_BOPS + (warp - DEC_WARP0) * 4096;
+        bool staged = false;
         for (int cc = cg * (BN / 128); cc < (cg + 1) * (BN / 128); ++cc) {
           uint32_t u[32];
           ptx::tmem_ld_x32(tmem + ((32u * q) << 16) + (uint32_t)(cc * 32), u);
           ptx::tmem_wait_ld();
           const int64_t col = n0 + cc * 32;
-          if (row >= p.M || col >= p.N) continue;
-          if (p.c != nullptr) {
-            float* cp = p.c + bt * p.cbs + row * p.ldc + col;
-            if (col + 32 <= p.N) {
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                reinterpret_cast<float4*>(cp)[i] =
-                    make_float4(__uint_as_float(u[4 * i]), __uint_as_float(u[4 * i + 1]),
-                                __uint_as_float(u[4 * i + 2]), __uint_as_float(u[4 * i + 3]));
-            } else {
-              for (int i = 0; i < 32 && col + i < p.N; ++i) cp[i] = __uint_as_float(u[i]);
+          if (p.c != nullptr && col < p.N && m0 + 32 * q < p.M) {
+            if (staged) {
+              if (lane == 0) ptx::bulk_wait_read0();
+              __syncwarp();
             }
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(stage + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                  make_uint4(u[4 * j], u[4 * j + 1], u[4 * j + 2], u[4 * j + 3]);
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_3d(&tmap_c, stage, (int)col, (int)(m0 + 32 * q), (int)bt);
+              ptx::bulk_commit();
+            }
+            staged = true;
           }
+          if (row >= p.M || col >= p.N) continue;
           if (p.epi != MIX_EPI_NONE) {
             uint4 cw;
             uint32_t sh;
@@ -464,6 +476,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             else static_cast<uint8_t*>(p.out_shared)[e / 32] = (uint8_t)sh;
           }
         }
+        if (staged && lane == 0) ptx::bulk_wait_read0();  // staging read before the CTA exits
       }
     }
   }
@@ -529,8 +542,24 @@ bool make_fp4_operand_map(CUtensorMap* m, const void* base, int64_t k, int64_t r
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D fp32 map over C for the epilogue's TMA stores: 32 x 32 boxes, 128-byte swizzle.
+bool make_c_map(CUtensorMap* m, float* c, int64_t rows, int64_t cols, int64_t batch, int64_t ldc, int64_t cbs) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  int64_t bs = cbs * 4;
+  if (batch <= 1 || bs <= 0) bs = ldc * 4 * rows;
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
+  const cuuint64_t strides[2] = {(cuuint64_t)(ldc * 4), (cuuint64_t)bs};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, c, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 template <bool B_NATIVE>
-cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, dim3 grid, cudaStream_t st) {
+cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const TcParams& p,
+                      dim3 grid, cudaStream_t st) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -540,7 +569,7 @@ cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const TcPara
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  gemm_tc_kernel<B_NATIVE><<<grid, NUM_THREADS, Plan<B_NATIVE>::SMEM_BYTES, st>>>(ma, mb, p);
+  gemm_tc_kernel<B_NATIVE><<<grid, NUM_THREADS, Plan<B_NATIVE>::SMEM_BYTES, st>>>(ma, mb, mc, p);
   return cudaGetLastError();
 }
 
@@ -574,8 +603,13 @@ cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, cudaStream_t st, mix_status
   p.c = d.c; p.ldc = d.ldc; p.cbs = d.c_batch_stride;
   p.epi = (int)d.epi; p.epi_ebias = d.epi_ebias; p.epi_flags = d.epi_flags;
   p.out_codes = d.out_codes; p.out_shared = d.out_shared; p.out_ld = d.out_ld; p.out_bs = d.out_batch_stride;
+  CUtensorMap mc = ma;  // placeholder when there is no fp32 output
+  if (d.c != nullptr && !make_c_map(&mc, d.c, d.M, d.N, d.batch, d.ldc, d.c_batch_stride)) {
+    *why = MIX_ERR_UNSUPPORTED;
+    return cudaSuccess;
+  }
   const dim3 grid((unsigned)((d.M + BM - 1) / BM), (unsigned)((d.N + BN - 1) / BN), (unsigned)d.batch);
-  return native ? launch_tc<true>(ma, mb, p, grid, st) : launch_tc<false>(ma, mb, p, grid, st);
+  return native ? launch_tc<true>(ma, mb, mc, p, grid, st) : launch_tc<false>(ma, mb, mc, p, grid, st);
 }
 
 }  // namespace mixk

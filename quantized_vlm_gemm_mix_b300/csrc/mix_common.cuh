@@ -60,46 +60,65 @@ __device__ __forceinline__ uint32_t bf16_to_f32_bits(uint32_t h) { return h << 1
 // Algorithm 1, first two steps, on the maximum magnitude (key != 0): its
 // exponent and its mantissa rounded to 3 bits nearest-even; a carry out of the
 // 3 bits gives mantissa 0 and exponent + 1.  Inf: mantissa 0, huge exponent.
-__device__ __forceinline__ void max_exp_mant(uint32_t key, int* f, int* m3) {
-  if (key >= 0x7F800000u) { *f = 1 << 20; *m3 = 0; return; }
-  Elem e = split_f32(key);
-  uint32_t q = (e.sig >> 20) & 7u, r = e.sig & 0xFFFFFu;
-  if (r > 0x80000u || (r == 0x80000u && (q & 1u))) ++q;
-  int ff = e.f;
-  if (q == 8u) { q = 0; ++ff; }
-  *f = ff;
-  *m3 = (int)q;
+// Returns false for a zero or subnormal maximum: with Emax >= ebias >= -100
+// every element of such a (sub-)block quantises to the zero code, which is the
+// canonical all-zero block.
+__device__ __forceinline__ bool max_exp_mant(uint32_t key, int* f, int* m3) {
+  if (key < 0x00800000u) { *f = 0; *m3 = 0; return false; }
+  if (key >= 0x7F800000u) { *f = 1 << 20; *m3 = 0; return true; }
+  uint32_t q = (key >> 20) & 7u;
+  const uint32_t r = key & 0xFFFFFu;
+  q += (r > 0x80000u || (r == 0x80000u && (q & 1u))) ? 1u : 0u;
+  *f = (int)(key >> 23) - 127 + (int)(q >> 3);
+  *m3 = (int)(q & 7u);
+  return true;
 }
 
 __device__ __forceinline__ int clampi(int v, int lo, int hi) { return v < lo ? lo : (v > hi ? hi : v); }
 
-// Algorithm 1, element step: the code of least |x - xhat| among the refinement
-// candidates, ties to the larger magnitude.  M = 8 + mshared (the shared
-// significand in eighths).  The nearest level M/8 * 2^j has j in {f-1, f,
-// f+1}; the two midpoints 1.5 * M/8 * 2^(f-1) and 1.5 * M/8 * 2^f become the
-// integer compares sig >= 12M * 2^16 and sig >= 24M * 2^16 (the hardware's
-// 4-bit residual against 0.5).  Below the smallest level the choice is zero
-// versus that level, an exact compare against half of it.
-__device__ __forceinline__ uint32_t mix_code(const Elem& x, int emax, int M, bool asym) {
-  if (x.cls == 0) return 7u;
-  if (x.cls == 2) return (uint32_t)x.s << 3;
-  const uint32_t t_lo = (uint32_t)(12 * M) << 16, t_hi = (uint32_t)(24 * M) << 16;
-  int j = x.f + (x.sig >= t_hi ? 1 : 0) - (x.sig < t_lo ? 1 : 0);
-  int d = emax - j;
-  if (d < 0) d = 0;  // above the top level: saturate at de = 0
-  const int dmax = (asym && x.s == 0) ? 7 : 6;
-  if (d <= dmax) return d == 7 ? 0xFu : (((uint32_t)x.s << 3) | (uint32_t)d);
-  const int sh = emax - dmax - x.f + 19;  // x >= half the smallest level?
-  const bool up = sh < 21 && x.sig >= ((uint32_t)M << sh);
-  if (!up) return 7u;
-  return dmax == 7 ? 0xFu : (((uint32_t)x.s << 3) | 6u);
+// Algorithm 1, element step, for one (sub-)block with shared exponent emax and
+// shared significand M = 8 + mshared.  The levels M/8 * 2^(emax - de) form a
+// geometric sequence, so do the midpoints between neighbouring levels:
+// t_de = 3M * 2^(emax - 5 - de), whose fp32 bit patterns differ by exactly
+// 2^23 per step.  The level nearest to |x| (ties to the larger) is therefore
+// de = ceil((bits(t_0) - bits(|x|)) / 2^23) clamped at 0, an integer
+// subtract and shift; below the smallest level the choice is zero versus that
+// level, one compare against half of it.  This is the page's single-cycle
+// "4-bit residual against 0.5" test, evaluated on bit patterns.
+struct MixBlk {
+  uint32_t t0;   // bits of the midpoint between the two largest levels
+  uint32_t zp;   // bits of half the smallest positive level (de 7 with the recycled -0, else 6)
+  uint32_t zn;   // bits of half the smallest negative level (de 6)
+  int dmaxp;     // largest positive de: 7 with the recycled -0, else 6
+};
+
+__device__ __forceinline__ MixBlk mix_blk(int emax, int M, bool asym) {
+  MixBlk b;
+  const uint32_t m3M = 3u * (uint32_t)M;  // 24 .. 45
+  const int p = m3M >= 32u ? 5 : 4;
+  b.t0 = ((uint32_t)(emax - 5 + p + 127) << 23) | ((m3M - (1u << p)) << (23 - p));
+  b.zn = ((uint32_t)(emax - 7 + 127) << 23) | ((uint32_t)(M - 8) << 20);  // (M/8) 2^(emax-6) / 2
+  b.zp = asym ? b.zn - (1u << 23) : b.zn;
+  b.dmaxp = asym ? 7 : 6;
+  return b;
+}
+
+__device__ __forceinline__ uint32_t mix_code(uint32_t u, const MixBlk& b) {
+  const uint32_t a = u & 0x7FFFFFFFu;
+  int d = ((int)(b.t0 - a) + 0x7FFFFF) >> 23;
+  d = max(d, 0);
+  const bool neg = (int)u < 0;
+  const int dd = min(d, neg ? 6 : b.dmaxp);
+  const uint32_t code = (uint32_t)dd | (neg ? 8u : 0u) | ((uint32_t)(dd + 1) & 8u);
+  const uint32_t z = neg ? b.zn : b.zp;
+  return (a < z || a > 0x7F800000u) ? 7u : code;  // zero (or NaN) -> the zero code
 }
 
 // Eight elements -> eight nibbles (element i in bits 4i..4i+3).
-__device__ __forceinline__ uint32_t mix_codes8(const uint32_t* u, int emax, int M, bool asym) {
+__device__ __forceinline__ uint32_t mix_codes8(const uint32_t* u, const MixBlk& b) {
   uint32_t w = 0;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) w |= mix_code(split_f32(u[i]), emax, M, asym) << (4 * i);
+  for (int i = 0; i < 8; ++i) w |= mix_code(u[i], b) << (4 * i);
   return w;
 }
 
@@ -130,58 +149,51 @@ __device__ __forceinline__ int mx_shared_exp(uint32_t key, bool fp4, bool floor_
   return clampi(X, -127, 127);
 }
 
-__device__ __forceinline__ uint32_t rne_shift(uint32_t sig, int sh) {
-  // round-half-even of sig / 2^sh for 1 <= sh <= 31
-  uint32_t q = sig >> sh, r = sig & ((1u << sh) - 1u), half = 1u << (sh - 1);
-  if (r > half || (r == half && (q & 1u))) ++q;
-  return q;
+// 2^k as an fp32 factor, k in [-126, 127].
+__device__ __forceinline__ float pow2f(int k) { return __int_as_float((uint32_t)(k + 127) << 23); }
+
+// NaN -> +0 (NaN is coded as zero); everything else unchanged.
+__device__ __forceinline__ float clean_f(uint32_t u) {
+  return __uint_as_float(((u & 0x7FFFFFFFu) > 0x7F800000u) ? 0u : u);
 }
 
-// E2M1 code of x / 2^X: nearest, ties to the even code, saturating at 6, -0
-// written as +0.
-__device__ __forceinline__ uint32_t mx_fp4_code(const Elem& x, int X) {
-  if (x.cls == 0) return 0u;
-  if (x.cls == 2) return ((uint32_t)x.s << 3) | 7u;
-  int ey = x.f - X;
-  uint32_t code;
-  if (ey >= 3) {
-    code = 7u;
-  } else if (ey >= 0) {
-    uint32_t q = rne_shift(x.sig, 22);  // 2 .. 4 in units of 2^(ey-1)
-    if (q == 4u) { q = 2u; ++ey; }
-    code = (ey >= 3) ? 7u : ((uint32_t)((ey + 1) << 1) | (q - 2u));
-  } else {
-    const int sh = 22 - ey;  // >= 23: units of 0.5
-    code = (sh >= 25) ? 0u : rne_shift(x.sig, sh);  // 0, 1 (0.5) or 2 (1.0)
-  }
-  return code ? (((uint32_t)x.s << 3) | code) : 0u;
+// Two elements -> one byte of E2M1 codes (first element in the low nibble):
+// x / 2^X rounded to nearest-even on the E2M1 grid with saturation at 6 is the
+// hardware conversion cvt.rn.satfinite.e2m1x2.f32.
+__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(hi), "f"(lo));
+  return r;
 }
 
-// INT4 code of x / 2^(X-2): nearest-even, clamped to [-7, 7], two's complement.
-__device__ __forceinline__ uint32_t mx_int4_code(const Elem& x, int X) {
-  if (x.cls == 0) return 0u;
-  int q;
-  if (x.cls == 2) {
-    q = 7;
-  } else {
-    const int d = x.f - X;
-    if (d >= 1) {
-      q = 7;
-    } else {
-      const int sh = 21 - d;
-      q = (sh >= 25) ? 0 : (int)rne_shift(x.sig, sh);
-      if (q > 7) q = 7;
-    }
-  }
-  return (uint32_t)(x.s ? -q : q) & 0xFu;
-}
-
+// Eight elements of an MX block with shared exponent X -> eight nibbles.
+// MXFP4: E2M1 codes of x / 2^X, -0 written as +0.  MXINT4: q = round-half-even
+// of x / 2^(X-2) (an fp32 add of 1.5 * 2^23 rounds to an integer exactly),
+// clamped to [-7, 7], two's complement.  The 2^-X factor is applied as two
+// exact power-of-two multiplies so that it never overflows.
 __device__ __forceinline__ uint32_t mx_codes8(const uint32_t* u, int X, bool fp4) {
+  const int k = fp4 ? -X : 2 - X;
+  const int k1 = k / 2, k2 = k - k1;
+  const float s1 = pow2f(k1), s2 = pow2f(k2);
   uint32_t w = 0;
+  if (fp4) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    Elem e = split_f32(u[i]);
-    w |= (fp4 ? mx_fp4_code(e, X) : mx_int4_code(e, X)) << (4 * i);
+    for (int i = 0; i < 4; ++i)
+      w |= e2m1x2(clean_f(u[2 * i]) * s1 * s2, clean_f(u[2 * i + 1]) * s1 * s2) << (8 * i);
+    // -0 (nibble 0x8) -> +0
+    const uint32_t t = w ^ 0x88888888u;
+    const uint32_t nz = (t | (t >> 1) | (t >> 2) | (t >> 3)) & 0x11111111u;
+    w &= ~((~nz & 0x11111111u) << 3);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float y = clean_f(u[i]) * s1 * s2;
+      int q = __float_as_int(y + 12582912.0f) - 0x4B400000;
+      q = clampi(q, -7, 7);
+      w |= ((uint32_t)q & 0xFu) << (4 * i);
+    }
   }
   return w;
 }

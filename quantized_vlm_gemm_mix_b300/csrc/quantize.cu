@@ -36,6 +36,23 @@ constexpr int kThreads = 256;
 constexpr int kQuadsPerCta = kThreads / 4;
 constexpr int kUnroll = 2;
 
+// n / d for 32-bit n and a divisor fixed per launch, by multiply-high with a
+// precomputed magic number (q = (umulhi(n, m) + n) >> l, l = ceil(log2 d)).
+struct FastDiv {
+  uint32_t d, m, l;
+};
+FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  f.l = 0;
+  while ((1ull << f.l) < d) ++f.l;
+  f.m = (uint32_t)((((1ull << 32) * ((1ull << f.l) - d)) / d) + 1);
+  return f;
+}
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  return (uint32_t)(((uint64_t)__umulhi(n, f.m) + n) >> f.l);
+}
+
 // Eight consecutive elements as fp32 bit patterns.
 template <bool BF16>
 __device__ __forceinline__ void load8(const void* base, int64_t elem, uint32_t* u) {
@@ -69,21 +86,23 @@ __device__ __forceinline__ uint32_t quad_and(uint32_t v) {
 }
 
 template <bool BF16, int TYPE>
-__global__ void __launch_bounds__(kThreads) mix_quantize_kernel(
+__global__ void __launch_bounds__(kThreads, 4) mix_quantize_kernel(
     const void* __restrict__ x, int64_t rows, int64_t nb, int64_t ld, int ebias, int asym,
-    uint8_t* __restrict__ codes, void* __restrict__ shared) {
+    uint8_t* __restrict__ codes, void* __restrict__ shared, FastDiv fnb) {
   const int q = threadIdx.x & 3;
   const int64_t total = rows * nb;
   const int64_t stride = (int64_t)gridDim.x * kQuadsPerCta;
   for (int64_t base = (int64_t)blockIdx.x * kQuadsPerCta; base < total; base += stride * kUnroll) {
     uint32_t u[kUnroll][8];
     int64_t g[kUnroll];
+    uint32_t row[kUnroll] = {0u};
 #pragma unroll
     for (int r = 0; r < kUnroll; ++r) {
       g[r] = base + r * stride + (threadIdx.x >> 2);
       if (g[r] < total) {
-        const int64_t row = g[r] / nb, b = g[r] - row * nb;
-        load8<BF16>(x, row * ld + b * 32 + q * 8, u[r]);
+        row[r] = fdiv((uint32_t)g[r], fnb);
+        const int64_t b = g[r] - (int64_t)row[r] * nb;
+        load8<BF16>(x, (int64_t)row[r] * ld + b * 32 + q * 8, u[r]);
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) u[r][i] = 0;
@@ -95,24 +114,24 @@ __global__ void __launch_bounds__(kThreads) mix_quantize_kernel(
       const uint32_t kb = quad_max(kl);
       uint32_t word = 0x77777777u;
       int emax = ebias, m3 = 0, m3l = 0;
-      if (kb != 0u) {
-        int f;
-        max_exp_mant(kb, &f, &m3);
+      int f;
+      if (max_exp_mant(kb, &f, &m3)) {
         emax = clampi(f, ebias, ebias + 15);
         m3l = m3;
         if (TYPE == 2) {
-          m3l = 0;
-          if (kl != 0u) { int fl; max_exp_mant(kl, &fl, &m3l); }
+          int fl;
+          if (!max_exp_mant(kl, &fl, &m3l)) m3l = 0;
         }
-        word = mix_codes8(u[r], emax, 8 + m3l, asym != 0);
+        word = mix_codes8(u[r], mix_blk(emax, 8 + m3l, asym != 0));
+      } else {
+        m3 = 0;
       }
       const uint32_t lane_zero = (word == 0x77777777u) ? 1u : 0u;
       if (TYPE == 2 && lane_zero) m3l = 0;
       const uint32_t all_zero = quad_and(lane_zero);
       const uint32_t m3_bits = quad_or((uint32_t)m3l << (4 + 3 * q));
       if (g[r] < total) {
-        const int64_t row = g[r] / nb, b = g[r] - row * nb;
-        __stcs(reinterpret_cast<uint32_t*>(codes + row * nb * 16 + b * 16 + q * 4), word);
+        __stcs(reinterpret_cast<uint32_t*>(codes + g[r] * 16 + q * 4), word);
         if (q == 0) {
           const uint32_t ec = all_zero ? 0u : (uint32_t)(emax - ebias);
           if (TYPE == 1) {
@@ -127,21 +146,23 @@ __global__ void __launch_bounds__(kThreads) mix_quantize_kernel(
 }
 
 template <bool BF16, bool FP4>
-__global__ void __launch_bounds__(kThreads) mx_quantize_rows_kernel(
+__global__ void __launch_bounds__(kThreads, 4) mx_quantize_rows_kernel(
     const void* __restrict__ x, int64_t rows, int64_t nb, int64_t ld, int floor_rule,
-    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, FastDiv fnb) {
   const int q = threadIdx.x & 3;
   const int64_t total = rows * nb;
   const int64_t stride = (int64_t)gridDim.x * kQuadsPerCta;
   for (int64_t base = (int64_t)blockIdx.x * kQuadsPerCta; base < total; base += stride * kUnroll) {
     uint32_t u[kUnroll][8];
     int64_t g[kUnroll];
+    uint32_t row[kUnroll] = {0u};
 #pragma unroll
     for (int r = 0; r < kUnroll; ++r) {
       g[r] = base + r * stride + (threadIdx.x >> 2);
       if (g[r] < total) {
-        const int64_t row = g[r] / nb, b = g[r] - row * nb;
-        load8<BF16>(x, row * ld + b * 32 + q * 8, u[r]);
+        row[r] = fdiv((uint32_t)g[r], fnb);
+        const int64_t b = g[r] - (int64_t)row[r] * nb;
+        load8<BF16>(x, (int64_t)row[r] * ld + b * 32 + q * 8, u[r]);
       } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) u[r][i] = 0;
@@ -157,8 +178,7 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_rows_kernel(
         sc = (uint32_t)(X + 127);
       }
       if (g[r] < total) {
-        const int64_t row = g[r] / nb, b = g[r] - row * nb;
-        __stcs(reinterpret_cast<uint32_t*>(codes + row * nb * 16 + b * 16 + q * 4), word);
+        __stcs(reinterpret_cast<uint32_t*>(codes + g[r] * 16 + q * 4), word);
         if (q == 0) scales[g[r]] = (uint8_t)sc;
       }
     }
@@ -302,13 +322,15 @@ cudaError_t launch_mix_quantize(const void* x, bool bf16, int64_t rows, int64_t 
                                 int type, int ebias, bool asym, uint8_t* codes, void* shared,
                                 cudaStream_t st) {
   const int64_t nb = k / 32;
+  if (rows * nb >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;  // 32-bit block index
   const int grid = grid_for(rows * nb);
+  const FastDiv f = make_fastdiv((uint32_t)nb);
   if (bf16) {
-    if (type == 1) mix_quantize_kernel<true, 1><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared);
-    else mix_quantize_kernel<true, 2><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared);
+    if (type == 1) mix_quantize_kernel<true, 1><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared, f);
+    else mix_quantize_kernel<true, 2><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared, f);
   } else {
-    if (type == 1) mix_quantize_kernel<false, 1><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared);
-    else mix_quantize_kernel<false, 2><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared);
+    if (type == 1) mix_quantize_kernel<false, 1><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared, f);
+    else mix_quantize_kernel<false, 2><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared, f);
   }
   return cudaGetLastError();
 }
@@ -317,14 +339,16 @@ cudaError_t launch_mx_quantize_rows(const void* x, bool bf16, int64_t rows, int6
                                     bool fp4, bool floor_rule, uint8_t* codes, uint8_t* scales,
                                     cudaStream_t st) {
   const int64_t nb = k / 32;
+  if (rows * nb >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;  // 32-bit block index
   const int grid = grid_for(rows * nb);
   const int fr = floor_rule ? 1 : 0;
+  const FastDiv f = make_fastdiv((uint32_t)nb);
   if (bf16) {
-    if (fp4) mx_quantize_rows_kernel<true, true><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales);
-    else mx_quantize_rows_kernel<true, false><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales);
+    if (fp4) mx_quantize_rows_kernel<true, true><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales, f);
+    else mx_quantize_rows_kernel<true, false><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales, f);
   } else {
-    if (fp4) mx_quantize_rows_kernel<false, true><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales);
-    else mx_quantize_rows_kernel<false, false><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales);
+    if (fp4) mx_quantize_rows_kernel<false, true><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales, f);
+    else mx_quantize_rows_kernel<false, false><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales, f);
   }
   return cudaGetLastError();
 }
