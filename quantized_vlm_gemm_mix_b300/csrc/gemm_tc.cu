@@ -51,7 +51,7 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int KB = BK / 2;  // code bytes per row per stage
-constexpr int S_CODES = 4;
+constexpr int S_CODES = 3;
 constexpr int A_CODES = BM * KB, B_CODES = BN * KB;  // 8 KB, 16 KB
 constexpr int A_OPS = BM * BK, B_OPS = BN * BK;      // 16 KB, 32 KB (also the padded E2M1 tile)
 constexpr int DEC_WARP0 = 4, NUM_DEC_WARPS = 16;
@@ -66,7 +66,7 @@ constexpr long long WAIT_LIMIT = 1LL << 31;  // SM clocks, about one second
 // operand ring is one stage deeper.
 template <bool B_NATIVE>
 struct Plan {
-  static constexpr int S_OPS = B_NATIVE ? 3 : 2;
+  static constexpr int S_OPS = B_NATIVE ? 4 : 3;
   static constexpr int OFF_AOPS = 0;
   static constexpr int OFF_BOPS = OFF_AOPS + S_OPS * A_OPS;
   static constexpr int OFF_ACODES = OFF_BOPS + S_OPS * B_OPS;
@@ -311,26 +311,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp >= DEC_WARP0) {
     // ------------------------------------------------------------ decoders
     const int dt = threadIdx.x - DEC_WARP0 * 32;  // 0 .. 511
-    const int arow = dt >> 2, ablk = dt & 3;       // A: one 32-block per thread
+    const int arow = dt >> 2, ablk = dt & 3;       // A: one 32-block per thread per k-step
     const int64_t am = m0 + arow;
-    const int64_t a_row_elem = bt * p.a_bs + am * p.a_ld;
     const int brow = dt >> 1, bhalf = dt & 1;      // B decode: 64 elements per thread
-    const bool b_scale_thread = dt < BN;           // B scale words: one row per thread
+    const DecTab btab = p.b_fp4 ? fp4_tab() : int4_tab();
+    // Per-thread pointers and ranges, hoisted: the shared field of this
+    // thread's block at k-step kt is a_sh_ptr[4 kt] (valid while kt < a_kend).
+    const int64_t a_row_elem = bt * p.a_bs + am * p.a_ld;
+    const int a_kend = am < p.M ? (int)((p.K - 32 * ablk + BK - 1) / BK) : 0;
+    const uint8_t* a_sh8 = static_cast<const uint8_t*>(p.a_shared) + (a_row_elem + 32 * ablk) / 32;
+    const uint16_t* a_sh16 = static_cast<const uint16_t*>(p.a_shared) + (a_row_elem + 32 * ablk) / 32;
+    auto fetch_a = [&](int kt) -> uint32_t {
+      if (kt >= a_kend) return 0u;
+      return p.a_type == 1 ? (uint32_t)__ldg(a_sh8 + 4 * kt) : (uint32_t)__ldg(a_sh16 + 4 * kt);
+    };
+    // B scale words: one row per thread (dt < 256), one aligned word per k-step
+    const bool b_scale_thread = dt < BN;
     const int64_t bsn = n0 + dt;
     const int64_t b_row_elem = (bt / p.b_group) * p.b_bs + bsn * p.b_ld;
-    uint32_t* sfa_s = reinterpret_cast<uint32_t*>(smem + L::OFF_SFA);
-    uint32_t* sfb_s = reinterpret_cast<uint32_t*>(smem + L::OFF_SFB);
-    const DecTab btab = p.b_fp4 ? fp4_tab() : int4_tab();
-    // The A shared field and the four B scale bytes of a k-step come from L2;
-    // they are fetched two k-steps ahead so their latency stays hidden.
-    const bool b_words = (b_row_elem % 128) == 0;  // four scale bytes of a k-step form one aligned word
-    auto fetch_a = [&](int kt) -> uint32_t {
-      const int64_t ka = (int64_t)kt * BK + 32 * ablk;
-      if (kt >= num_k || am >= p.M || ka >= p.K) return 0u;
-      const int64_t idx = (a_row_elem + ka) / 32;
-      return p.a_type == 1 ? (uint32_t)__ldg(static_cast<const uint8_t*>(p.a_shared) + idx)
-                           : (uint32_t)__ldg(static_cast<const uint16_t*>(p.a_shared) + idx);
-    };
+    const bool b_words = (b_row_elem % 128) == 0;
     auto fetch_b = [&](int kt) -> uint32_t {
       if (!b_scale_thread || kt >= num_k) return 0x7F7F7F7Fu;
       const int64_t k0 = (int64_t)kt * BK;
@@ -345,18 +344,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       return w;
     };
+    uint32_t* sfa_s = reinterpret_cast<uint32_t*>(smem + L::OFF_SFA);
+    uint32_t* sfb_s = reinterpret_cast<uint32_t*>(smem + L::OFF_SFB);
     uint32_t a_pf0 = fetch_a(0), a_pf1 = fetch_a(1);
     uint32_t b_pf0 = fetch_b(0), b_pf1 = fetch_b(1);
     bool ok = true;
     for (int kt = 0; kt < num_k && ok; ++kt) {
       const int cs = kt % S_CODES, cn = kt / S_CODES;
       const int os = kt % S_OPS, on = kt / S_OPS;
-      const int64_t ka = (int64_t)kt * BK + 32 * ablk;
-      const bool a_in = am < p.M && ka < p.K;
       const uint32_t a_sh = a_pf0, bsw = b_pf0;
       a_pf0 = a_pf1;
-      b_pf0 = b_pf1;
       a_pf1 = fetch_a(kt + 2);
+      b_pf0 = b_pf1;
       b_pf1 = fetch_b(kt + 2);
       if (!ptx::mbar_wait(&codes_full[cs], cn & 1, WAIT_LIMIT, abort_flag)) { flag_error(4u, abort_flag); ok = false; break; }
       if (on > 0) {
@@ -368,6 +367,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::tc_fence_after();
       }
       if (*abort_flag) { ok = false; break; }
+      // --- this thread's scale words of the stage, to shared memory
+      {
+        const int emax = (int)(a_sh & 0xFu) + p.a_ebias;
+        const bool a_in = kt < a_kend;
+        reinterpret_cast<uint8_t*>(sfa_s + os * BM + arow)[ablk] =
+            (uint8_t)(a_in ? (uint32_t)clampi(emax + 126, 1, 254) : 127u);  // 2^(Emax - 1)
+        if (b_scale_thread) sfb_s[os * BN + dt] = bsw;
+      }
       // --- A: one 32-block (two 16-element chunks) of row arow
       {
         const uint4 cv = *reinterpret_cast<const uint4*>(smem + L::OFF_ACODES + cs * A_CODES + arow * KB + ablk * 16);
@@ -384,9 +391,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         *reinterpret_cast<uint4*>(dst + sw128_off(arow, 2 * ablk)) = make_uint4(e[0].x, e[0].y, e[1].x, e[1].y);
         *reinterpret_cast<uint4*>(dst + sw128_off(arow, 2 * ablk + 1)) = make_uint4(e[2].x, e[2].y, e[3].x, e[3].y);
-        const int emax = (int)(a_sh & 0xFu) + p.a_ebias;
-        reinterpret_cast<uint8_t*>(sfa_s + os * BM + arow)[ablk] =
-            (uint8_t)(a_in ? (uint32_t)clampi(emax + 126, 1, 254) : 127u);
       }
       // --- B (decoded mode): 64 elements (4 chunks) of row brow
       if (!B_NATIVE) {
@@ -400,8 +404,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           *reinterpret_cast<uint4*>(dst + sw128_off(brow, bhalf * 4 + 2 * c + 1)) = make_uint4(e2.x, e2.y, e3.x, e3.y);
         }
       }
-      if (b_scale_thread) sfb_s[os * BN + dt] = bsw;
-      // codes slot free and this warp's scale words published
       __syncwarp();
       if (lane == 0) {
         ptx::mbar_arrive(&codes_empty[cs]);
@@ -410,14 +412,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // scale words -> TMEM (each lane quadrant holds a full replica)
       if (warp < DEC_WARP0 + 4) {
         if (!ptx::mbar_wait(&sf_ready[os], on & 1, WAIT_LIMIT, abort_flag)) { flag_error(32u, abort_flag); ok = false; break; }
-        const uint32_t q = (uint32_t)(warp & 3);
-        const uint32_t base = tmem + ((32u * q) << 16);
+        const uint32_t base = tmem + ((32u * (uint32_t)(warp & 3)) << 16) + SF_COL + 16u * os;
         const uint32_t* sa = sfa_s + os * BM;
         const uint32_t* sb = sfb_s + os * BN;
-        ptx::tmem_st_x4(base + SF_COL + 16u * os, sa[lane], sa[lane + 32], sa[lane + 64], sa[lane + 96]);
-        ptx::tmem_st_x4(base + SF_COL + 16u * os + 4u, sb[lane], sb[lane + 32], sb[lane + 64], sb[lane + 96]);
-        ptx::tmem_st_x4(base + SF_COL + 16u * os + 8u, sb[lane + 128], sb[lane + 160], sb[lane + 192],
-                        sb[lane + 224]);
+        ptx::tmem_st_x4(base, sa[lane], sa[lane + 32], sa[lane + 64], sa[lane + 96]);
+        ptx::tmem_st_x4(base + 4u, sb[lane], sb[lane + 32], sb[lane + 64], sb[lane + 96]);
+        ptx::tmem_st_x4(base + 8u, sb[lane + 128], sb[lane + 160], sb[lane + 192], sb[lane + 224]);
         ptx::tmem_wait_st();
       }
       ptx::fence_proxy_async_smem();
