@@ -121,8 +121,7 @@ def step_table(small=False):
     add(f"bmm_qk_{HQ}x{T}x{T}x{D}", plane_bytes(T * HQ, D, 2) + plane_bytes(T * HK, D, 0) + HQ * T * T * 4,
         2.0 * HQ * T * T * D, cpu=("gemm", HQ * T * T * (D // 32)))
     add(f"mix_quantize_t2_p_{HQ * T}x{T}", mix_bytes(HQ * T, T, 2), cpu=("mix2", HQ * T * T))
-    for h in range(HK):
-        add(f"mx_quantize_int4_v_head{h}_{T}x{D}", mx_bytes(D, T), cpu=("mx", D * T))
+    add(f"mx_quantize_int4_v_{T}x{HK * D}", mx_bytes(HK * D, T), cpu=("mx", HK * D * T))
     add(f"bmm_pv_{HQ}x{T}x{D}x{T}", plane_bytes(HQ * T, T, 2) + plane_bytes(HK * D, T, 0) + HQ * T * D * 4,
         2.0 * HQ * T * D * T, cpu=("gemm", HQ * T * D * (T // 32)))
     add(f"ksmooth_apply_frozen_1x{HK}x{D}", HK * D * (2 + 4 + 4), cpu=("ks", HK * D))
@@ -260,11 +259,11 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
     del causal
     pc, ps = new((HQ * T, T // 2), torch.uint8), new((HQ * T, T // 32), torch.int16)
     fns[f"mix_quantize_t2_p_{HQ * T}x{T}"] = lambda: mix.mix_quantize(P, HQ * T, T, T, T2, -15, 1, pc, ps)
+    # V [T, HK*D] quantised down its columns in one call: column h*D + d is
+    # row (h, d) of the [HK][D][T/2] planes the PV matmul reads
     vqc, vqs = new((HK, D, T // 2), torch.uint8), new((HK, D, T // 32), torch.uint8)
-    for h in range(HK):
-        vh = v_d[:T, h * D:(h + 1) * D]
-        fns[f"mx_quantize_int4_v_head{h}_{T}x{D}"] = (lambda vh=vh, h=h: mix.mx_quantize(
-            vh, T, D, HK * D, 0, INT4, 0, vqc[h], vqs[h]))
+    v_pre = v_d[:T]
+    fns[f"mx_quantize_int4_v_{T}x{HK * D}"] = lambda: mix.mx_quantize(v_pre, T, HK * D, HK * D, 0, INT4, 0, vqc, vqs)
     O = new((HQ, T, D), torch.float32)
     dpv = mix.gemm_desc(T, D, T, pc, ps, T2, -15, vqc, vqs, INT4, c=O, batch=HQ, b_group=HQ // HK,
                         algo=mix.MIX_GEMM_TCGEN05)

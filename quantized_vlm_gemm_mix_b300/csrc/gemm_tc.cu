@@ -73,7 +73,8 @@ struct Plan {
   static constexpr int OFF_BCODES = OFF_ACODES + S_CODES * A_CODES;
   static constexpr int OFF_SFA = OFF_BCODES + (B_NATIVE ? 0 : S_CODES * B_CODES);  // [S_OPS][BM] words
   static constexpr int OFF_SFB = OFF_SFA + S_OPS * BM * 4;                           // [S_OPS][BN] words
-  static constexpr int OFF_BAR = OFF_SFB + S_OPS * BN * 4;
+  static constexpr int OFF_TAB = OFF_SFB + S_OPS * BN * 4;  // 8 decode tables (one per mshared), 16 B each
+  static constexpr int OFF_BAR = OFF_TAB + 8 * 16;
   static constexpr int NUM_BARS = 2 * S_CODES + 4 * S_OPS + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for the 1024-byte alignment
@@ -235,6 +236,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::prefetch_tmap(&tmap_a);
     ptx::prefetch_tmap(&tmap_b);
   }
+  if (threadIdx.x >= 32 * DEC_WARP0 && threadIdx.x < 32 * DEC_WARP0 + 8) {
+    const DecTab t = mix_tab((uint32_t)(threadIdx.x - 32 * DEC_WARP0));
+    *reinterpret_cast<uint4*>(smem + L::OFF_TAB + 16 * (threadIdx.x - 32 * DEC_WARP0)) =
+        make_uint4(t.plo, t.phi, t.nlo, t.nhi);
+  }
   if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, TMEM_COLS);
     ptx::tmem_relinquish();
@@ -315,8 +321,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int64_t am = m0 + arow;
     const int brow = dt >> 1, bhalf = dt & 1;      // B decode: 64 elements per thread
     const DecTab btab = p.b_fp4 ? fp4_tab() : int4_tab();
+    const unsigned char* tabs = smem + L::OFF_TAB;
     // Per-thread pointers and ranges, hoisted: the shared field of this
-    // thread's block at k-step kt is a_sh_ptr[4 kt] (valid while kt < a_kend).
+    // thread's block at k-step kt is at [4 kt], valid while kt < a_kend.
     const int64_t a_row_elem = bt * p.a_bs + am * p.a_ld;
     const int a_kend = am < p.M ? (int)((p.K - 32 * ablk + BK - 1) / BK) : 0;
     const uint8_t* a_sh8 = static_cast<const uint8_t*>(p.a_shared) + (a_row_elem + 32 * ablk) / 32;
@@ -370,27 +377,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // --- this thread's scale words of the stage, to shared memory
       {
         const int emax = (int)(a_sh & 0xFu) + p.a_ebias;
-        const bool a_in = kt < a_kend;
         reinterpret_cast<uint8_t*>(sfa_s + os * BM + arow)[ablk] =
-            (uint8_t)(a_in ? (uint32_t)clampi(emax + 126, 1, 254) : 127u);  // 2^(Emax - 1)
+            (uint8_t)(kt < a_kend ? (uint32_t)clampi(emax + 126, 1, 254) : 127u);  // 2^(Emax - 1)
         if (b_scale_thread) sfb_s[os * BN + dt] = bsw;
       }
-      // --- A: one 32-block (two 16-element chunks) of row arow
+      // --- A: two 32-blocks (four 16-element chunks) of row arow
       {
-        const uint4 cv = *reinterpret_cast<const uint4*>(smem + L::OFF_ACODES + cs * A_CODES + arow * KB + ablk * 16);
+        const unsigned char* src = smem + L::OFF_ACODES + cs * A_CODES + arow * KB + ablk * 16;
         unsigned char* dst = smem + L::OFF_AOPS + os * A_OPS;
-        uint2 e[4];
-        if (p.a_type == 1) {
-          const DecTab t = mix_tab((a_sh >> 4) & 7u);
-          e[0] = dec8(cv.x, t); e[1] = dec8(cv.y, t); e[2] = dec8(cv.z, t); e[3] = dec8(cv.w, t);
-        } else {
-          e[0] = dec8(cv.x, mix_tab((a_sh >> 4) & 7u));
-          e[1] = dec8(cv.y, mix_tab((a_sh >> 7) & 7u));
-          e[2] = dec8(cv.z, mix_tab((a_sh >> 10) & 7u));
-          e[3] = dec8(cv.w, mix_tab((a_sh >> 13) & 7u));
+        {
+          const uint4 cv = *reinterpret_cast<const uint4*>(src);
+          const uint32_t sh = a_sh;
+          auto tab = [&](uint32_t m3) {
+            const uint4 t = *reinterpret_cast<const uint4*>(tabs + 16 * m3);
+            return DecTab{t.x, t.y, t.z, t.w};
+          };
+          uint2 e[4];
+          if (p.a_type == 1) {
+            const DecTab t = tab((sh >> 4) & 7u);
+            e[0] = dec8(cv.x, t); e[1] = dec8(cv.y, t); e[2] = dec8(cv.z, t); e[3] = dec8(cv.w, t);
+          } else {
+            e[0] = dec8(cv.x, tab((sh >> 4) & 7u));
+            e[1] = dec8(cv.y, tab((sh >> 7) & 7u));
+            e[2] = dec8(cv.z, tab((sh >> 10) & 7u));
+            e[3] = dec8(cv.w, tab((sh >> 13) & 7u));
+          }
+          const int c0 = 2 * ablk;
+          *reinterpret_cast<uint4*>(dst + sw128_off(arow, c0)) = make_uint4(e[0].x, e[0].y, e[1].x, e[1].y);
+          *reinterpret_cast<uint4*>(dst + sw128_off(arow, c0 + 1)) = make_uint4(e[2].x, e[2].y, e[3].x, e[3].y);
         }
-        *reinterpret_cast<uint4*>(dst + sw128_off(arow, 2 * ablk)) = make_uint4(e[0].x, e[0].y, e[1].x, e[1].y);
-        *reinterpret_cast<uint4*>(dst + sw128_off(arow, 2 * ablk + 1)) = make_uint4(e[2].x, e[2].y, e[3].x, e[3].y);
       }
       // --- B (decoded mode): 64 elements (4 chunks) of row brow
       if (!B_NATIVE) {
@@ -438,19 +453,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t q = (uint32_t)(warp & 3);
         const int cg = (warp - DEC_WARP0) >> 2;  // column quarter 0..3
         const int64_t row = m0 + 32 * q + lane;
-        // fp32 C leaves through a per-warp 32 x 32 staging tile (128-byte
-        // swizzled, in the drained B operand ring) and a TMA store, which
-        // writes whole lines and clips the ragged edges of the matrix.
-        unsigned char* stage = smem + L::OFF_BOPS + (warp - DEC_WARP0) * 4096;
-        bool staged = false;
+        // fp32 C leaves through per-warp 32 x 32 staging tiles (128-byte
+        // swizzled, double-buffered, in the drained B operand ring) and TMA
+        // stores, which write whole lines and clip the ragged matrix edges.
+        unsigned char* stage0 = smem + L::OFF_BOPS + (warp - DEC_WARP0) * 8192;  // 16 x 8 KB = 128 KB
+        int staged = 0;
         for (int cc = cg * (BN / 128); cc < (cg + 1) * (BN / 128); ++cc) {
           uint32_t u[32];
           ptx::tmem_ld_x32(tmem + ((32u * q) << 16) + (uint32_t)(cc * 32), u);
           ptx::tmem_wait_ld();
           const int64_t col = n0 + cc * 32;
           if (p.c != nullptr && col < p.N && m0 + 32 * q < p.M) {
-            if (staged) {
-              if (lane == 0) ptx::bulk_wait_read0();
+            unsigned char* stage = stage0 + (staged & 1) * 4096;
+            if (staged >= 2) {
+              if (lane == 0) ptx::bulk_wait_read1();  // the store that last used this buffer
               __syncwarp();
             }
 #pragma unroll
@@ -463,7 +479,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ptx::tma_store_3d(&tmap_c, stage, (int)col, (int)(m0 + 32 * q), (int)bt);
               ptx::bulk_commit();
             }
-            staged = true;
+            ++staged;
           }
           if (row >= p.M || col >= p.N) continue;
           if (p.epi != MIX_EPI_NONE) {

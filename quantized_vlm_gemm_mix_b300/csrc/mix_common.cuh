@@ -103,6 +103,15 @@ __device__ __forceinline__ MixBlk mix_blk(int emax, int M, bool asym) {
   return b;
 }
 
+// Element step for a block known to hold no NaN (|x| bit pattern a given).
+__device__ __forceinline__ uint32_t mix_code_nonan(uint32_t u, uint32_t a, const MixBlk& b) {
+  int d = ((int)(b.t0 - a) + 0x7FFFFF) >> 23;
+  const bool neg = (int)u < 0;
+  const int dd = min(max(d, 0), neg ? 6 : b.dmaxp);
+  const uint32_t code = (uint32_t)dd | ((u >> 28) & 8u) | ((uint32_t)(dd + 1) & 8u);
+  return a < (neg ? b.zn : b.zp) ? 7u : code;
+}
+
 __device__ __forceinline__ uint32_t mix_code(uint32_t u, const MixBlk& b) {
   const uint32_t a = u & 0x7FFFFFFFu;
   int d = ((int)(b.t0 - a) + 0x7FFFFF) >> 23;

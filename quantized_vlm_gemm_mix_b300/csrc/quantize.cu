@@ -1,11 +1,12 @@
 // MiX and MX quantiser kernels (sm_103a).
 //
 // MiX (Algorithm 1, Method section of the pchao.org digest of "MiX:
-// Micro-Inverted-Scaling ..."): four lanes own one 32-element block, eight
-// elements each (one 16-byte load of bf16, two of fp32).  The block maximum
-// is two butterfly shuffles; for MiX-4.5b each lane's eight elements are
-// exactly one sub-block, so a lane computes its own mshared.  Codes leave as
-// one 32-bit store per lane (a warp stores 128 contiguous bytes).
+// Micro-Inverted-Scaling ..."): one thread owns one 32-element block (four
+// 16-byte loads of bf16, eight of fp32), computes the block's Emax and
+// mshared once, codes the 32 elements with integer compares on their fp32
+// bit patterns and stores 16 code bytes; a warp's stores are 512 contiguous
+// bytes.  MX along rows: four lanes per block, eight elements each, the block
+// maximum by two butterfly shuffles.
 //
 // The kernels are HBM-bound: a bf16 element costs 2 bytes in and 0.53125
 // (T1) / 0.5625 (T2) bytes out.  Each thread keeps two blocks in flight and
@@ -76,72 +77,106 @@ __device__ __forceinline__ uint32_t quad_max(uint32_t v) {
   v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
   return max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
 }
-__device__ __forceinline__ uint32_t quad_or(uint32_t v) {
-  v |= __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-  return v | __shfl_xor_sync(0xFFFFFFFFu, v, 2);
-}
-__device__ __forceinline__ uint32_t quad_and(uint32_t v) {
-  v &= __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-  return v & __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+
+// One thread per 32-element block: the block's parameters are computed once
+// and no lane exchange is needed.  |x| is formed once per element and feeds
+// both the block maximum and the element decision; a block holding a NaN
+// (rare) takes a slow path that codes the NaNs as zero first.
+template <bool BF16>
+__device__ __forceinline__ void load32(const void* base, int64_t elem, uint32_t* u) {
+  if (BF16) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + elem);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 v = p[j];
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        u[8 * j + 2 * i] = w[i] << 16;
+        u[8 * j + 2 * i + 1] = w[i] & 0xFFFF0000u;
+      }
+    }
+  } else {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const float*>(base) + elem);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint4 v = p[j];
+      u[4 * j] = v.x; u[4 * j + 1] = v.y; u[4 * j + 2] = v.z; u[4 * j + 3] = v.w;
+    }
+  }
 }
 
 template <bool BF16, int TYPE>
-__global__ void __launch_bounds__(kThreads, 4) mix_quantize_kernel(
+__global__ void __launch_bounds__(kThreads, 3) mix_quantize_kernel(
     const void* __restrict__ x, int64_t rows, int64_t nb, int64_t ld, int ebias, int asym,
     uint8_t* __restrict__ codes, void* __restrict__ shared, FastDiv fnb) {
-  const int q = threadIdx.x & 3;
   const int64_t total = rows * nb;
-  const int64_t stride = (int64_t)gridDim.x * kQuadsPerCta;
-  for (int64_t base = (int64_t)blockIdx.x * kQuadsPerCta; base < total; base += stride * kUnroll) {
-    uint32_t u[kUnroll][8];
-    int64_t g[kUnroll];
-    uint32_t row[kUnroll] = {0u};
+  for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < total; g += (int64_t)gridDim.x * kThreads) {
+    const uint32_t row = fdiv((uint32_t)g, fnb);
+    const int64_t b = g - (int64_t)row * nb;
+    uint32_t u[32];
+    load32<BF16>(x, (int64_t)row * ld + b * 32, u);
+    uint32_t ks[4];
 #pragma unroll
-    for (int r = 0; r < kUnroll; ++r) {
-      g[r] = base + r * stride + (threadIdx.x >> 2);
-      if (g[r] < total) {
-        row[r] = fdiv((uint32_t)g[r], fnb);
-        const int64_t b = g[r] - (int64_t)row[r] * nb;
-        load8<BF16>(x, (int64_t)row[r] * ld + b * 32 + q * 8, u[r]);
-      } else {
+    for (int s = 0; s < 4; ++s) {
+      uint32_t k = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) u[r][i] = 0;
-      }
+      for (int i = 0; i < 8; ++i) k = max(k, u[8 * s + i] & 0x7FFFFFFFu);
+      ks[s] = k;
     }
+    uint32_t kb = max(max(ks[0], ks[1]), max(ks[2], ks[3]));
+    if (kb > 0x7F800000u) {  // a NaN in the block: code it as zero
 #pragma unroll
-    for (int r = 0; r < kUnroll; ++r) {
-      const uint32_t kl = max_key8(u[r]);
-      const uint32_t kb = quad_max(kl);
-      uint32_t word = 0x77777777u;
-      int emax = ebias, m3 = 0, m3l = 0;
-      int f;
-      if (max_exp_mant(kb, &f, &m3)) {
-        emax = clampi(f, ebias, ebias + 15);
-        m3l = m3;
+      for (int i = 0; i < 32; ++i)
+        if ((u[i] & 0x7FFFFFFFu) > 0x7F800000u) u[i] = 0u;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        uint32_t k = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) k = max(k, u[8 * s + i] & 0x7FFFFFFFu);
+        ks[s] = k;
+      }
+      kb = max(max(ks[0], ks[1]), max(ks[2], ks[3]));
+    }
+    uint4 cw = make_uint4(0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);
+    uint32_t sh = 0;
+    int f, m3;
+    if (max_exp_mant(kb, &f, &m3)) {
+      const int emax = clampi(f, ebias, ebias + 15);
+      uint32_t w[4];
+      uint32_t m3bits = 0;
+      bool all_zero = true;
+      const MixBlk b1 = mix_blk(emax, 8 + m3, asym != 0);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        int ms = m3;
+        MixBlk bb = b1;
         if (TYPE == 2) {
-          int fl;
-          if (!max_exp_mant(kl, &fl, &m3l)) m3l = 0;
+          int fs;
+          if (!max_exp_mant(ks[s], &fs, &ms)) ms = 0;
+          bb = mix_blk(emax, 8 + ms, asym != 0);
         }
-        word = mix_codes8(u[r], mix_blk(emax, 8 + m3l, asym != 0));
-      } else {
-        m3 = 0;
+        uint32_t word = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t v = u[8 * s + i];
+          word |= mix_code_nonan(v, v & 0x7FFFFFFFu, bb) << (4 * i);
+        }
+        w[s] = word;
+        const bool z = word == 0x77777777u;
+        all_zero &= z;
+        if (z) ms = 0;
+        m3bits |= (uint32_t)ms << (4 + 3 * s);
       }
-      const uint32_t lane_zero = (word == 0x77777777u) ? 1u : 0u;
-      if (TYPE == 2 && lane_zero) m3l = 0;
-      const uint32_t all_zero = quad_and(lane_zero);
-      const uint32_t m3_bits = quad_or((uint32_t)m3l << (4 + 3 * q));
-      if (g[r] < total) {
-        __stcs(reinterpret_cast<uint32_t*>(codes + g[r] * 16 + q * 4), word);
-        if (q == 0) {
-          const uint32_t ec = all_zero ? 0u : (uint32_t)(emax - ebias);
-          if (TYPE == 1) {
-            static_cast<uint8_t*>(shared)[g[r]] = (uint8_t)(all_zero ? 0u : (ec | ((uint32_t)m3 << 4)));
-          } else {
-            static_cast<uint16_t*>(shared)[g[r]] = (uint16_t)(all_zero ? 0u : (ec | m3_bits));
-          }
-        }
+      cw = make_uint4(w[0], w[1], w[2], w[3]);
+      if (!all_zero) {
+        const uint32_t ec = (uint32_t)(emax - ebias);
+        sh = TYPE == 1 ? (ec | ((uint32_t)m3 << 4)) : (ec | m3bits);
       }
     }
+    __stcs(reinterpret_cast<uint4*>(codes + g * 16), cw);
+    if (TYPE == 1) static_cast<uint8_t*>(shared)[g] = (uint8_t)sh;
+    else static_cast<uint16_t*>(shared)[g] = (uint16_t)sh;
   }
 }
 
@@ -323,7 +358,9 @@ cudaError_t launch_mix_quantize(const void* x, bool bf16, int64_t rows, int64_t 
                                 cudaStream_t st) {
   const int64_t nb = k / 32;
   if (rows * nb >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;  // 32-bit block index
-  const int grid = grid_for(rows * nb);
+  int64_t gb = (rows * nb + kThreads - 1) / kThreads;
+  if (gb > (int64_t)num_sms() * 3) gb = (int64_t)num_sms() * 3;  // one wave of 3 resident CTAs per SM
+  const int grid = (int)(gb > 0 ? gb : 1);
   const FastDiv f = make_fastdiv((uint32_t)nb);
   if (bf16) {
     if (type == 1) mix_quantize_kernel<true, 1><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared, f);
