@@ -26,6 +26,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 
 #include "mix_common.cuh"
 #include "mix_internal.h"
@@ -586,7 +588,10 @@ cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtens
     attr_set[dev] = true;
   }
   gemm_tc_kernel<B_NATIVE><<<grid, NUM_THREADS, Plan<B_NATIVE>::SMEM_BYTES, st>>>(ma, mb, mc, p);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess && std::getenv("MIX_DEBUG") != nullptr)
+    std::fprintf(stderr, "gemm_tc launch: %s\n", cudaGetErrorString(e));
+  return e;
 }
 
 }  // namespace

@@ -107,7 +107,7 @@ __device__ __forceinline__ void load32(const void* base, int64_t elem, uint32_t*
 }
 
 template <bool BF16, int TYPE>
-__global__ void __launch_bounds__(kThreads, 3) mix_quantize_kernel(
+__global__ void __launch_bounds__(kThreads, 4) mix_quantize_kernel(
     const void* __restrict__ x, int64_t rows, int64_t nb, int64_t ld, int ebias, int asym,
     uint8_t* __restrict__ codes, void* __restrict__ shared, FastDiv fnb) {
   const int64_t total = rows * nb;
@@ -359,7 +359,7 @@ cudaError_t launch_mix_quantize(const void* x, bool bf16, int64_t rows, int64_t 
   const int64_t nb = k / 32;
   if (rows * nb >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;  // 32-bit block index
   int64_t gb = (rows * nb + kThreads - 1) / kThreads;
-  if (gb > (int64_t)num_sms() * 3) gb = (int64_t)num_sms() * 3;  // one wave of 3 resident CTAs per SM
+  if (gb > (int64_t)num_sms() * 4) gb = (int64_t)num_sms() * 4;  // one wave of 4 resident CTAs per SM
   const int grid = (int)(gb > 0 ? gb : 1);
   const FastDiv f = make_fastdiv((uint32_t)nb);
   if (bf16) {
