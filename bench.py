@@ -91,6 +91,12 @@ def dims(small=False):
                 HQ=28, HK=4, D=128)
 
 
+def tc_launches(n):
+    """Launches of one tensor-core matmul call: outputs wider than one 256-column
+    tile take the staged variant (expand A, expand B or its scales, matmul)."""
+    return 3 if n > 256 else 1
+
+
 def step_table(small=False):
     """[(name, bytes, flops, launches, cpu work)] in launch order.  The cpu work
     (kind, count) lets the CPU baseline extrapolate the oracle's sampled cost:
@@ -109,21 +115,21 @@ def step_table(small=False):
     add(f"mix_quantize_t2_{M}x{DF}", mix_bytes(M, DF, 2), cpu=("mix2", M * DF))
     for name, k, n in (("qkv", DM, QKV), ("o", DM, DM), ("gate_up", DM, 2 * DF), ("down", DF, DM)):
         add(f"gemm_{name}_{M}x{k}x{n}", plane_bytes(M, k, 2) + plane_bytes(n, k, 0) + plane_bytes(M, n, 2),
-            2.0 * M * n * k, cpu=("gemm", M * n * (k // 32)))
+            2.0 * M * n * k, launches=tc_launches(n), cpu=("gemm", M * n * (k // 32)))
     add(f"mix_quantize_t1_{MV}x1280", mix_bytes(MV, 1280, 1), cpu=("mix1", MV * 1280))
     add(f"gemm_vit_fc1_{MV}x1280x5120", plane_bytes(MV, 1280, 1) + plane_bytes(5120, 1280, 0) +
-        plane_bytes(MV, 5120, 1), 2.0 * MV * 5120 * 1280, cpu=("gemm", MV * 5120 * 40))
+        plane_bytes(MV, 5120, 1), 2.0 * MV * 5120 * 1280, launches=tc_launches(5120), cpu=("gemm", MV * 5120 * 40))
     add(f"gemm_vit_fc2_{MV}x5120x1280", plane_bytes(MV, 5120, 1) + plane_bytes(1280, 5120, 0) +
-        plane_bytes(MV, 1280, 1), 2.0 * MV * 1280 * 5120, cpu=("gemm", MV * 1280 * 160))
+        plane_bytes(MV, 1280, 1), 2.0 * MV * 1280 * 5120, launches=tc_launches(1280), cpu=("gemm", MV * 1280 * 160))
     add(f"ksmooth_compute_{T}x{HK}x{D}", T * HK * D * (2 + 2 + 4), launches=3, cpu=("ks", 2 * T * HK * D))
     add(f"mix_quantize_t2_q_{T * HQ}x{D}", mix_bytes(T * HQ, D, 2), cpu=("mix2", T * HQ * D))
     add(f"mx_quantize_int4_kprime_{T * HK}x{D}", mx_bytes(T * HK, D, 4), cpu=("mx", T * HK * D))
     add(f"bmm_qk_{HQ}x{T}x{T}x{D}", plane_bytes(T * HQ, D, 2) + plane_bytes(T * HK, D, 0) + HQ * T * T * 4,
-        2.0 * HQ * T * T * D, cpu=("gemm", HQ * T * T * (D // 32)))
+        2.0 * HQ * T * T * D, launches=tc_launches(T), cpu=("gemm", HQ * T * T * (D // 32)))
     add(f"mix_quantize_t2_p_{HQ * T}x{T}", mix_bytes(HQ * T, T, 2), cpu=("mix2", HQ * T * T))
     add(f"mx_quantize_int4_v_{T}x{HK * D}", mx_bytes(HK * D, T), cpu=("mx", HK * D * T))
     add(f"bmm_pv_{HQ}x{T}x{D}x{T}", plane_bytes(HQ * T, T, 2) + plane_bytes(HK * D, T, 0) + HQ * T * D * 4,
-        2.0 * HQ * T * D * T, cpu=("gemm", HQ * T * D * (T // 32)))
+        2.0 * HQ * T * D * T, launches=tc_launches(D), cpu=("gemm", HQ * T * D * (T // 32)))
     add(f"ksmooth_apply_frozen_1x{HK}x{D}", HK * D * (2 + 4 + 4), cpu=("ks", HK * D))
     add(f"mx_quantize_int4_knew_{HK}x{D}", mx_bytes(HK, D, 4), cpu=("mx", HK * D))
     add(f"mix_quantize_t2_qdec_{HQ}x{D}", mix_bytes(HQ, D, 2), cpu=("mix2", HQ * D))
@@ -161,6 +167,16 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
         t = torch.empty(shape, dtype=dtype, device=dev)
         keep.append(t)
         return t
+
+    # one workspace serves every tensor-core matmul of the step (they run in
+    # sequence on one stream); sized by the largest request
+    tc_descs = []
+
+    def tc_call(d):
+        tc_descs.append(d)
+        return lambda: mix.mix_mx_gemm(d, ws_tc[0])
+
+    ws_tc = [None]
 
     # ----- per-step activations
     x_np = synth.to_bf16_bits(synth.vlm_activations(seed, 1, M, DM, visual_rows=(3 * M) // 4))
@@ -208,7 +224,7 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
         bc, bs = wq[name]
         d = mix.gemm_desc(M, n, k, ac_, as_, T2, -8, bc, bs, FP4, c=None, epi=mix.MIX_EPI_MIX_T2, out_codes=oc,
                           out_shared=os_, algo=mix.MIX_GEMM_TCGEN05)
-        fns[f"gemm_{name}_{M}x{k}x{n}"] = (lambda d=d: mix.mix_mx_gemm(d))
+        fns[f"gemm_{name}_{M}x{k}x{n}"] = tc_call(d)
     d2h.append(outs["down"])
 
     # ----- 3. ViT MLP: fc1's fused MiX-4.25b output is fc2's input
@@ -220,8 +236,8 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
                        out_shared=hs, algo=mix.MIX_GEMM_TCGEN05)
     d2 = mix.gemm_desc(MV, 1280, 5120, hc, hs, T1, -8, wv2[0], wv2[1], INT4, epi=mix.MIX_EPI_MIX_T1, out_codes=yc,
                        out_shared=ys, algo=mix.MIX_GEMM_TCGEN05)
-    fns[f"gemm_vit_fc1_{MV}x1280x5120"] = lambda: mix.mix_mx_gemm(d1)
-    fns[f"gemm_vit_fc2_{MV}x5120x1280"] = lambda: mix.mix_mx_gemm(d2)
+    fns[f"gemm_vit_fc1_{MV}x1280x5120"] = tc_call(d1)
+    fns[f"gemm_vit_fc2_{MV}x5120x1280"] = tc_call(d2)
     d2h.append(yc)
 
     # ----- 4. attention prefill (28 query / 4 KV heads, d 128)
@@ -247,7 +263,8 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
     S = new((HQ, T, T), torch.float32)
     dqk = mix.gemm_desc(T, T, D, qc, qs, T2, -8, kc, ks, INT4, c=S, batch=HQ, b_group=HQ // HK, a_ld=HQ * D,
                         a_batch_stride=D, b_ld=HK * D, b_batch_stride=D, algo=mix.MIX_GEMM_TCGEN05)
-    fns[f"bmm_qk_{HQ}x{T}x{T}x{D}"] = lambda: mix.mix_mx_gemm(dqk)
+    fns[f"bmm_qk_{HQ}x{T}x{T}x{D}"] = tc_call(dqk)
+    ws_tc[0] = new(max(16, max(mix.mix_mx_gemm_workspace_bytes(d) for d in tc_descs)), torch.uint8)
     # P: a fixed causal softmax of S, made once here (softmax is not on the path)
     for f in (f"ksmooth_compute_{T}x{HK}x{D}", f"mix_quantize_t2_q_{T * HQ}x{D}",
               f"mx_quantize_int4_kprime_{T * HK}x{D}", f"bmm_qk_{HQ}x{T}x{T}x{D}"):
@@ -267,7 +284,8 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
     O = new((HQ, T, D), torch.float32)
     dpv = mix.gemm_desc(T, D, T, pc, ps, T2, -15, vqc, vqs, INT4, c=O, batch=HQ, b_group=HQ // HK,
                         algo=mix.MIX_GEMM_TCGEN05)
-    fns[f"bmm_pv_{HQ}x{T}x{D}x{T}"] = lambda: mix.mix_mx_gemm(dpv)
+    assert mix.mix_mx_gemm_workspace_bytes(dpv) <= ws_tc[0].numel()
+    fns[f"bmm_pv_{HQ}x{T}x{D}x{T}"] = tc_call(dpv)
     d2h.append(O)
 
     # ----- 5. decode over a TC-token cache smoothed with the frozen prefill mean

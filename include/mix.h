@@ -156,10 +156,25 @@ MIX_API mix_status_t mx_dequantize(const uint8_t* codes, const uint8_t* scales, 
  * multiply by the shared mantissa, one exponent add) and splits K across
  * CTAs when there are few outputs, summing the partials in a fixed order in
  * the caller's workspace (see mix_mx_gemm_workspace_bytes).
+ *
+ * The tensor-core path has two variants with identical results (every
+ * product is exact; only the fp32 accumulation order is fixed by the K
+ * loop, the same in both):
+ *  - staged (MIX_GEMM_TCGEN05_STAGED; chosen by AUTO / TCGEN05 when N > 256):
+ *    A, and B unless it is MXFP4 that the unpacking TMA reads in place, are
+ *    first expanded into exact e4m3 planes and UE8M0 scale words in the
+ *    caller's workspace, then a TMA-fed tcgen05 kernel multiplies them.  The
+ *    workspace holds batch*M*Kp + bB*N*Kp bytes (Kp = K rounded up to 128,
+ *    bB = ceil(batch / b_group); the B plane only when B is expanded) plus
+ *    the scale words and alignment; mix_mx_gemm_workspace_bytes gives the
+ *    exact size and a smaller workspace returns MIX_ERR_WORKSPACE.
+ *  - fused decode (MIX_GEMM_TCGEN05_FUSED; chosen when N <= 256): decoder
+ *    warps expand each tile inside the matmul.  No workspace.
  */
 typedef enum { MIX_EPI_NONE = 0, MIX_EPI_MIX_T1 = 1, MIX_EPI_MIX_T2 = 2,
                MIX_EPI_MXINT4 = 3, MIX_EPI_MXFP4 = 4 } mix_epilogue_t;
-typedef enum { MIX_GEMM_AUTO = 0, MIX_GEMM_TCGEN05 = 1, MIX_GEMM_SHIFTADD = 2 } mix_gemm_algo_t;
+typedef enum { MIX_GEMM_AUTO = 0, MIX_GEMM_TCGEN05 = 1, MIX_GEMM_SHIFTADD = 2,
+               MIX_GEMM_TCGEN05_STAGED = 3, MIX_GEMM_TCGEN05_FUSED = 4 } mix_gemm_algo_t;
 
 typedef struct {
   int64_t M, N, K;

@@ -132,7 +132,7 @@ static mix_status_t validate_gemm(const mix_gemm_desc_t* d) {
   if (d->a_ebias < -100 || d->a_ebias > 100 || d->epi_ebias < -100 || d->epi_ebias > 100)
     return MIX_ERR_INVALID_ARG;
   if (d->epi < MIX_EPI_NONE || d->epi > MIX_EPI_MXFP4) return MIX_ERR_INVALID_ARG;
-  if (d->algo < MIX_GEMM_AUTO || d->algo > MIX_GEMM_SHIFTADD) return MIX_ERR_INVALID_ARG;
+  if (d->algo < MIX_GEMM_AUTO || d->algo > MIX_GEMM_TCGEN05_FUSED) return MIX_ERR_INVALID_ARG;
   if (d->K % 32 != 0) return MIX_ERR_SHAPE;
   if (d->epi != MIX_EPI_NONE && d->N % 32 != 0) return MIX_ERR_SHAPE;
   if (d->epi == MIX_EPI_NONE && d->c == nullptr) return MIX_ERR_INVALID_ARG;
@@ -161,14 +161,14 @@ static mix_status_t validate_gemm(const mix_gemm_desc_t* d) {
 
 static bool use_shiftadd(const mix_gemm_desc_t* d) {
   if (d->algo == MIX_GEMM_SHIFTADD) return true;
-  if (d->algo == MIX_GEMM_TCGEN05) return false;
+  if (d->algo != MIX_GEMM_AUTO) return false;
   return d->M <= 16;
 }
 
 size_t mix_mx_gemm_workspace_bytes(const mix_gemm_desc_t* d) {
   if (validate_gemm(d) != MIX_OK || d->M == 0 || d->N == 0) return 0;
   if (use_shiftadd(d)) return gemv_workspace_bytes(*d);
-  return 0;
+  return gemm_tc_workspace_bytes(*d);
 }
 
 mix_status_t mix_mx_gemm(const mix_gemm_desc_t* d, void* workspace, size_t workspace_bytes,
@@ -189,7 +189,8 @@ mix_status_t mix_mx_gemm(const mix_gemm_desc_t* d, void* workspace, size_t works
     return from_cuda(launch_gemv_shiftadd(*d, workspace, st));
   }
   mix_status_t why = MIX_OK;
-  cudaError_t e = launch_gemm_tc(*d, st, &why);
+  if (workspace != nullptr && !aligned(workspace, 16)) return MIX_ERR_ALIGN;
+  cudaError_t e = launch_gemm_tc(*d, workspace, workspace_bytes, st, &why);
   if (why != MIX_OK) return why;
   return from_cuda(e);
 }

@@ -1,0 +1,229 @@
+// Staging pass of the tensor-core matmul: each operand is expanded ONCE per
+// call into exact e4m3 bytes plus UE8M0 block-scale words in the caller's
+// workspace, so that the matmul's main loop is TMA -> tcgen05.cp -> MMA with
+// no per-tile decode.  Without it every CTA of a row panel re-decodes the same
+// A tile (N / 256 times for a wide layer).
+//
+// The arithmetic is the decode of "MiX: Micro-Inverted-Scaling for End-to-End
+// Low-Bit Vision-Language Model Acceleration" (pchao.org digest, section
+// "Method", dual-format matmul bullet): MiX element -> +-(1.m3) 2^(1 - de)
+// with block scale 2^(Emax - 1); MX element -> (q / 4) or its E2M1 value with
+// block scale 2^X.  Every value is exact in e4m3 and every scale exact in
+// UE8M0, so the expanded operands multiply to the same products as Eq. (6).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "decode.cuh"
+#include "mix_common.cuh"
+#include "mix_internal.h"
+
+namespace mixk {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ uint32_t quad_or(uint32_t v) {
+  v |= __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+  v |= __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+  return v;
+}
+
+// One thread per 32-element block of a (padded) row of A.  Rows run to the
+// last full 128-row tile so every scale word of the tile is written; only
+// rows < M get e4m3 bytes (the matmul's TMA zero-fills rows >= M).  Warps
+// iterate in lockstep (the trip count is rounded to the warp) so the quad
+// shuffles that assemble a scale word always see all 32 lanes.
+template <int TYPE>
+__global__ void __launch_bounds__(kThreads) expand_a_kernel(const uint8_t* __restrict__ codes,
+                                                            const void* __restrict__ shared, int64_t M,
+                                                            int64_t K, int64_t a_ld, int64_t a_bs, int ebias,
+                                                            int64_t batch, int64_t k_pad, int64_t mt, int64_t kt_n,
+                                                            FastDiv f_kbp, FastDiv f_rows,
+                                                            uint8_t* __restrict__ a_e4m3, uint32_t* __restrict__ sfa) {
+  const int64_t kbv = K / 32;
+  const uint32_t total = (uint32_t)(batch * (int64_t)f_rows.d * f_kbp.d);
+  const uint32_t total_w = (total + 31u) & ~31u;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  const unsigned char* tabs;
+  __shared__ uint4 tab_s[8];
+  if (threadIdx.x < 8) {
+    const DecTab t = mix_tab(threadIdx.x);
+    tab_s[threadIdx.x] = make_uint4(t.plo, t.phi, t.nlo, t.nhi);
+  }
+  __syncthreads();
+  tabs = reinterpret_cast<const unsigned char*>(tab_s);
+  auto tab = [&](uint32_t m3) {
+    const uint4 t = *reinterpret_cast<const uint4*>(tabs + 16 * m3);
+    return DecTab{t.x, t.y, t.z, t.w};
+  };
+  for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < total_w; t += stride) {
+    const bool valid = t < total;
+    const uint32_t rr = fdiv(t, f_kbp), kb = t - rr * f_kbp.d;
+    const uint32_t b = fdiv(rr, f_rows), r = rr - b * f_rows.d;
+    uint32_t sbyte = 127u;
+    if (valid && r < M) {
+      uint4 out0 = make_uint4(0, 0, 0, 0), out1 = make_uint4(0, 0, 0, 0);
+      if (kb < kbv) {
+        const int64_t e = (int64_t)b * a_bs + (int64_t)r * a_ld + 32 * (int64_t)kb;
+        const uint4 cv = __ldg(reinterpret_cast<const uint4*>(codes + e / 2));
+        const uint32_t sh = TYPE == 1 ? (uint32_t)__ldg(static_cast<const uint8_t*>(shared) + e / 32)
+                                      : (uint32_t)__ldg(static_cast<const uint16_t*>(shared) + e / 32);
+        uint2 d0, d1, d2, d3;
+        if (TYPE == 1) {
+          const DecTab tt = tab((sh >> 4) & 7u);
+          d0 = dec8(cv.x, tt); d1 = dec8(cv.y, tt); d2 = dec8(cv.z, tt); d3 = dec8(cv.w, tt);
+        } else {
+          d0 = dec8(cv.x, tab((sh >> 4) & 7u));
+          d1 = dec8(cv.y, tab((sh >> 7) & 7u));
+          d2 = dec8(cv.z, tab((sh >> 10) & 7u));
+          d3 = dec8(cv.w, tab((sh >> 13) & 7u));
+        }
+        out0 = make_uint4(d0.x, d0.y, d1.x, d1.y);
+        out1 = make_uint4(d2.x, d2.y, d3.x, d3.y);
+        const int emax = (int)(sh & 0xFu) + ebias;
+        sbyte = (uint32_t)clampi(emax + 126, 1, 254);  // 2^(Emax - 1)
+      }
+      uint4* dst = reinterpret_cast<uint4*>(a_e4m3 + ((int64_t)b * M + r) * k_pad + 32 * (int64_t)kb);
+      dst[0] = out0;
+      dst[1] = out1;
+    }
+    // scale word of (row r, k-step kb / 4): byte kb % 4, assembled across the quad
+    const uint32_t word = quad_or(sbyte << (8 * (kb & 3u)));
+    if (valid && (kb & 3u) == 0) {
+      const int64_t tile = r >> 7, rin = r & 127;
+      const int64_t idx = (((int64_t)b * mt + tile) * kt_n + (kb >> 2)) * 128 + (rin & 31) * 4 + (rin >> 5);
+      sfa[idx] = word;
+    }
+  }
+}
+
+// B: MX plane -> e4m3 of q / 4 (MXINT4) or the E2M1 value, and the MX scale
+// bytes regrouped into 256-row tiles.  WRITE_OPS false: scales only (MXFP4
+// weights the matmul reads in place).
+template <bool FP4, bool WRITE_OPS>
+__global__ void __launch_bounds__(kThreads) expand_b_kernel(const uint8_t* __restrict__ codes,
+                                                            const uint8_t* __restrict__ scales, int64_t N,
+                                                            int64_t K, int64_t b_ld, int64_t b_bs, int64_t bb,
+                                                            int64_t k_pad, int64_t nt, int64_t kt_n,
+                                                            FastDiv f_kbp, FastDiv f_rows,
+                                                            uint8_t* __restrict__ b_e4m3, uint32_t* __restrict__ sfb) {
+  const int64_t kbv = K / 32;
+  const uint32_t total = (uint32_t)(bb * (int64_t)f_rows.d * f_kbp.d);
+  const uint32_t total_w = (total + 31u) & ~31u;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  const DecTab tt = FP4 ? fp4_tab() : int4_tab();
+  for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < total_w; t += stride) {
+    const bool valid = t < total;
+    const uint32_t rr = fdiv(t, f_kbp), kb = t - rr * f_kbp.d;
+    const uint32_t b = fdiv(rr, f_rows), r = rr - b * f_rows.d;
+    uint32_t sbyte = 127u;
+    if (valid && r < N) {
+      uint4 out0 = make_uint4(0, 0, 0, 0), out1 = make_uint4(0, 0, 0, 0);
+      if (kb < kbv) {
+        const int64_t e = (int64_t)b * b_bs + (int64_t)r * b_ld + 32 * (int64_t)kb;
+        sbyte = (uint32_t)__ldg(scales + e / 32);
+        if (WRITE_OPS) {
+          const uint4 cv = __ldg(reinterpret_cast<const uint4*>(codes + e / 2));
+          const uint2 d0 = dec8(cv.x, tt), d1 = dec8(cv.y, tt), d2 = dec8(cv.z, tt), d3 = dec8(cv.w, tt);
+          out0 = make_uint4(d0.x, d0.y, d1.x, d1.y);
+          out1 = make_uint4(d2.x, d2.y, d3.x, d3.y);
+        }
+      }
+      if (WRITE_OPS) {
+        uint4* dst = reinterpret_cast<uint4*>(b_e4m3 + ((int64_t)b * N + r) * k_pad + 32 * (int64_t)kb);
+        dst[0] = out0;
+        dst[1] = out1;
+      }
+    }
+    const uint32_t word = quad_or(sbyte << (8 * (kb & 3u)));
+    if (valid && (kb & 3u) == 0) {
+      const int64_t tile = r >> 8, rin = r & 255, h = rin >> 7, rq = rin & 127;
+      const int64_t idx = ((((int64_t)b * nt + tile) * kt_n + (kb >> 2)) * 2 + h) * 128 + (rq & 31) * 4 + (rq >> 5);
+      sfb[idx] = word;
+    }
+  }
+}
+
+int grid_for(int64_t threads) {
+  const int64_t cap = (int64_t)num_sms() * 8;
+  int64_t g = (threads + kThreads - 1) / kThreads;
+  if (g > cap) g = cap;
+  return (int)(g < 1 ? 1 : g);
+}
+
+size_t align_up(size_t v) { return (v + kStagedAlign - 1) / kStagedAlign * kStagedAlign; }
+
+}  // namespace
+
+bool staged_fp4_native_ok(const mix_gemm_desc_t& d) {
+  if (d.b_type != MX_FP4_E2M1 || d.K % 128 != 0) return false;
+  if ((reinterpret_cast<uintptr_t>(d.b_codes) & 31) != 0 || (d.b_ld / 2) % 32 != 0) return false;
+  const int64_t bb = (d.batch + d.b_group - 1) / d.b_group;
+  if (bb > 1 && (d.b_batch_stride / 2) % 32 != 0) return false;
+  return true;
+}
+
+StagedPlan staged_plan(const mix_gemm_desc_t& d) {
+  StagedPlan sp{};
+  sp.b_native = staged_fp4_native_ok(d);
+  sp.k_pad = (d.K + 127) / 128 * 128;
+  sp.kt = sp.k_pad / 128;
+  sp.mt = (d.M + 127) / 128;
+  sp.nt = (d.N + 255) / 256;
+  sp.bb = (d.batch + d.b_group - 1) / d.b_group;
+  size_t off = 0;
+  sp.off_a = off;
+  off = align_up(off + (size_t)d.batch * d.M * sp.k_pad);
+  sp.off_sfa = off;
+  off = align_up(off + (size_t)d.batch * sp.mt * sp.kt * 512);
+  sp.off_b = off;
+  if (!sp.b_native) off = align_up(off + (size_t)sp.bb * d.N * sp.k_pad);
+  sp.off_sfb = off;
+  off = align_up(off + (size_t)sp.bb * sp.nt * sp.kt * 1024);
+  sp.bytes = off;
+  return sp;
+}
+
+// Thread counts of the two passes; the staged path is taken only when both
+// index spaces fit 32 bits.
+int64_t expand_a_threads(const mix_gemm_desc_t& d, const StagedPlan& sp) { return d.batch * sp.mt * 128 * (sp.k_pad / 32); }
+int64_t expand_b_threads(const StagedPlan& sp) { return sp.bb * sp.nt * 256 * (sp.k_pad / 32); }
+
+cudaError_t launch_expand_a(const mix_gemm_desc_t& d, const StagedPlan& sp, unsigned char* base, cudaStream_t st) {
+  const int64_t threads = expand_a_threads(d, sp);
+  const FastDiv fk = make_fastdiv((uint32_t)(sp.k_pad / 32)), fr = make_fastdiv((uint32_t)(sp.mt * 128));
+  uint8_t* a = base + sp.off_a;
+  uint32_t* sfa = reinterpret_cast<uint32_t*>(base + sp.off_sfa);
+  if (d.a_type == MIX_T1_4P25)
+    expand_a_kernel<1><<<grid_for(threads), kThreads, 0, st>>>(d.a_codes, d.a_shared, d.M, d.K, d.a_ld,
+                                                               d.a_batch_stride, d.a_ebias, d.batch, sp.k_pad,
+                                                               sp.mt, sp.kt, fk, fr, a, sfa);
+  else
+    expand_a_kernel<2><<<grid_for(threads), kThreads, 0, st>>>(d.a_codes, d.a_shared, d.M, d.K, d.a_ld,
+                                                               d.a_batch_stride, d.a_ebias, d.batch, sp.k_pad,
+                                                               sp.mt, sp.kt, fk, fr, a, sfa);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_expand_b(const mix_gemm_desc_t& d, const StagedPlan& sp, unsigned char* base, cudaStream_t st) {
+  const int64_t threads = expand_b_threads(sp);
+  const FastDiv fk = make_fastdiv((uint32_t)(sp.k_pad / 32)), fr = make_fastdiv((uint32_t)(sp.nt * 256));
+  uint8_t* b = base + sp.off_b;
+  uint32_t* sfb = reinterpret_cast<uint32_t*>(base + sp.off_sfb);
+  const int g = grid_for(threads);
+  const int64_t bs = sp.bb > 1 ? d.b_batch_stride : 0;
+  if (sp.b_native)
+    expand_b_kernel<true, false><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
+                                                         sp.k_pad, sp.nt, sp.kt, fk, fr, nullptr, sfb);
+  else if (d.b_type == MX_FP4_E2M1)
+    expand_b_kernel<true, true><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
+                                                        sp.k_pad, sp.nt, sp.kt, fk, fr, b, sfb);
+  else
+    expand_b_kernel<false, true><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
+                                                         sp.k_pad, sp.nt, sp.kt, fk, fr, b, sfb);
+  return cudaGetLastError();
+}
+
+}  // namespace mixk

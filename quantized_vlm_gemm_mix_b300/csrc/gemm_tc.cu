@@ -30,6 +30,7 @@
 #include <cstdlib>
 
 #include "mix_common.cuh"
+#include "decode.cuh"
 #include "mix_internal.h"
 #include "tc_ptx.cuh"
 
@@ -96,39 +97,11 @@ struct TcParams {
   uint8_t* out_codes;
   void* out_shared;
   int64_t out_ld, out_bs;
+  // staged path: regrouped scale words in the workspace, tile and k-step counts
+  const uint8_t* sfa_g;
+  const uint8_t* sfb_g;
+  int64_t mt, nt, kt;
 };
-
-// ------------------------------------------------------------------ decode
-// Nibble -> e4m3 byte through two 8-entry tables (by the low three bits) and
-// a byte select by the sign bit: one prmt per table half and one to pick
-// between the positive and the negative candidate of every byte.
-struct DecTab {
-  uint32_t plo, phi, nlo, nhi;
-};
-// MiX element (s, de) with shared mantissa m3: +-(1.m3) 2^(1-de); code 0x7
-// is zero and 0xF the recycled -0, +(1.m3) 2^-6.
-__device__ __forceinline__ DecTab mix_tab(uint32_t m3) {
-  const uint32_t m3x = m3 * 0x01010101u;
-  DecTab t;
-  t.plo = 0x28303840u | m3x;
-  t.phi = 0x00101820u | (m3x & 0x00FFFFFFu);
-  t.nlo = t.plo | 0x80808080u;
-  t.nhi = 0x089098A0u | m3x;
-  return t;
-}
-// INT4 two's complement q -> q / 4; E2M1 -> its value.
-__device__ __forceinline__ DecTab int4_tab() { return DecTab{0x34302800u, 0x3E3C3A38u, 0xBABCBEC0u, 0xA8B0B4B8u}; }
-__device__ __forceinline__ DecTab fp4_tab() { return DecTab{0x3C383000u, 0x4C484440u, 0xBCB8B080u, 0xCCC8C4C0u}; }
-
-// Eight nibbles (element i in bits 4i..4i+3) -> eight e4m3 bytes.
-__device__ __forceinline__ uint2 dec8(uint32_t v, const DecTab& t) {
-  const uint32_t s7 = v & 0x77777777u, s2 = (v >> 1) & 0x44444444u;
-  const uint32_t s7h = s7 >> 16, s2h = s2 >> 16;
-  uint2 r;
-  r.x = ptx::prmt(ptx::prmt(t.plo, t.phi, s7), ptx::prmt(t.nlo, t.nhi, s7), s2 | 0x3210u);
-  r.y = ptx::prmt(ptx::prmt(t.plo, t.phi, s7h), ptx::prmt(t.nlo, t.nhi, s7h), s2h | 0x3210u);
-  return r;
-}
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a K-major operand tile
 // with 128-byte rows and the 128-byte swizzle (chunk index XOR row mod 8).
@@ -191,6 +164,59 @@ __device__ __forceinline__ void epi_quant_block(const uint32_t* u, const TcParam
     }
   }
   codes = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Epilogue of one 128 x 256 tile by sixteen warps (DEC_WARP0 ..): warp w
+// reads TMEM lane quadrant w % 4 (the only one it may access) and a quarter
+// of the columns.  fp32 C leaves through per-warp 32 x 32 staging tiles
+// (128-byte swizzled, double-buffered, 8 KB per warp in the drained operand
+// ring at `stage_base`) and TMA stores, which write whole lines and clip the
+// ragged matrix edges; the fused quantiser writes each 32-column block's codes
+// and shared field straight from registers.
+__device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorMap* tmap_c, uint32_t tmem,
+                                              unsigned char* stage_base, int64_t m0, int64_t n0, int64_t bt,
+                                              int warp, int lane) {
+  ptx::tc_fence_after();
+  const uint32_t q = (uint32_t)(warp & 3);
+  const int cg = (warp - DEC_WARP0) >> 2;  // column quarter 0..3
+  const int64_t row = m0 + 32 * q + lane;
+  unsigned char* stage0 = stage_base + (warp - DEC_WARP0) * 8192;  // 16 x 8 KB = 128 KB
+  int staged = 0;
+  for (int cc = cg * (BN / 128); cc < (cg + 1) * (BN / 128); ++cc) {
+    uint32_t u[32];
+    ptx::tmem_ld_x32(tmem + ((32u * q) << 16) + (uint32_t)(cc * 32), u);
+    ptx::tmem_wait_ld();
+    const int64_t col = n0 + cc * 32;
+    if (p.c != nullptr && col < p.N && m0 + 32 * q < p.M) {
+      unsigned char* stage = stage0 + (staged & 1) * 4096;
+      if (staged >= 2) {
+        if (lane == 0) ptx::bulk_wait_read1();  // the store that last used this buffer
+        __syncwarp();
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(stage + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+            make_uint4(u[4 * j], u[4 * j + 1], u[4 * j + 2], u[4 * j + 3]);
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        ptx::tma_store_3d(tmap_c, stage, (int)col, (int)(m0 + 32 * q), (int)bt);
+        ptx::bulk_commit();
+      }
+      ++staged;
+    }
+    if (row >= p.M || col >= p.N) continue;
+    if (p.epi != MIX_EPI_NONE) {
+      uint4 cw;
+      uint32_t sh;
+      epi_quant_block(u, p, cw, sh);
+      const int64_t e = bt * p.out_bs + row * p.out_ld + col;
+      *reinterpret_cast<uint4*>(p.out_codes + e / 2) = cw;
+      if (p.epi == MIX_EPI_MIX_T2) static_cast<uint16_t*>(p.out_shared)[e / 32] = (uint16_t)sh;
+      else static_cast<uint8_t*>(p.out_shared)[e / 32] = (uint8_t)sh;
+    }
+  }
+  if (staged && lane == 0) ptx::bulk_wait_read0();  // staging read before the CTA exits
 }
 
 template <bool B_NATIVE>
@@ -451,51 +477,148 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!got) {
         if (ok && !*abort_flag) flag_error(16u, abort_flag);
       } else {
-        ptx::tc_fence_after();
-        const uint32_t q = (uint32_t)(warp & 3);
-        const int cg = (warp - DEC_WARP0) >> 2;  // column quarter 0..3
-        const int64_t row = m0 + 32 * q + lane;
-        // fp32 C leaves through per-warp 32 x 32 staging tiles (128-byte
-        // swizzled, double-buffered, in the drained B operand ring) and TMA
-        // stores, which write whole lines and clip the ragged matrix edges.
-        unsigned char* stage0 = smem + L::OFF_BOPS + (warp - DEC_WARP0) * 8192;  // 16 x 8 KB = 128 KB
-        int staged = 0;
-        for (int cc = cg * (BN / 128); cc < (cg + 1) * (BN / 128); ++cc) {
-          uint32_t u[32];
-          ptx::tmem_ld_x32(tmem + ((32u * q) << 16) + (uint32_t)(cc * 32), u);
-          ptx::tmem_wait_ld();
-          const int64_t col = n0 + cc * 32;
-          if (p.c != nullptr && col < p.N && m0 + 32 * q < p.M) {
-            unsigned char* stage = stage0 + (staged & 1) * 4096;
-            if (staged >= 2) {
-              if (lane == 0) ptx::bulk_wait_read1();  // the store that last used this buffer
-              __syncwarp();
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              *reinterpret_cast<uint4*>(stage + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                  make_uint4(u[4 * j], u[4 * j + 1], u[4 * j + 2], u[4 * j + 3]);
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              ptx::tma_store_3d(&tmap_c, stage, (int)col, (int)(m0 + 32 * q), (int)bt);
-              ptx::bulk_commit();
-            }
-            ++staged;
-          }
-          if (row >= p.M || col >= p.N) continue;
-          if (p.epi != MIX_EPI_NONE) {
-            uint4 cw;
-            uint32_t sh;
-            epi_quant_block(u, p, cw, sh);
-            const int64_t e = bt * p.out_bs + row * p.out_ld + col;
-            *reinterpret_cast<uint4*>(p.out_codes + e / 2) = cw;
-            if (p.epi == MIX_EPI_MIX_T2) static_cast<uint16_t*>(p.out_shared)[e / 32] = (uint16_t)sh;
-            else static_cast<uint8_t*>(p.out_shared)[e / 32] = (uint8_t)sh;
-          }
-        }
-        if (staged && lane == 0) ptx::bulk_wait_read0();  // staging read before the CTA exits
+        epilogue_tile(p, &tmap_c, tmem, smem + L::OFF_BOPS, m0, n0, bt, warp, lane);
       }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------- staged kernel
+// Operands expanded beforehand (e4m3 planes and regrouped scale words in the
+// workspace; MXFP4 weights read in place by the unpacking TMA).  The main
+// loop has no decode: per 128-deep k-step the producer issues two tiled TMA
+// loads and two bulk copies of scale words onto one barrier, and the MMA
+// thread moves the scale words into TMEM with tcgen05.cp (which executes in
+// order before its MMAs) and issues four MMAs.  The sixteen epilogue warps
+// are idle until the accumulator is complete.
+struct PlanS {
+  static constexpr int S = 4;
+  static constexpr int SFA_BYTES = 512, SFB_BYTES = 1024;
+  static constexpr int OFF_AOPS = 0;
+  static constexpr int OFF_BOPS = OFF_AOPS + S * A_OPS;
+  static constexpr int OFF_SFA = OFF_BOPS + S * B_OPS;
+  static constexpr int OFF_SFB = OFF_SFA + S * SFA_BYTES;
+  static constexpr int OFF_BAR = OFF_SFB + S * SFB_BYTES;
+  static constexpr int NUM_BARS = 2 * S + 2;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+};
+
+template <bool B_NATIVE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_staged_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                       const __grid_constant__ CUtensorMap tmap_c, const TcParams p) {
+  using L = PlanS;
+  constexpr int S = L::S;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* full = bars;            // TMA + bulk copies of one stage
+  uint64_t* empty = bars + S;       // MMA commit
+  uint64_t* acc_full = bars + 2 * S;
+  uint64_t* drain = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
+  volatile int* never = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);  // drains ignore aborts
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t mtile = blockIdx.x, ntile = blockIdx.y, bt = blockIdx.z;
+  const int64_t m0 = mtile * BM, n0 = ntile * BN, bbt = bt / p.b_group;
+  const int num_k = (int)p.kt;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      ptx::mbar_init(&full[i], 1);
+      ptx::mbar_init(&empty[i], 1);
+    }
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(drain, 1);
+    *abort_flag = 0;
+    *never = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmap_a);
+    ptx::prefetch_tmap(&tmap_b);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      constexpr uint32_t kStageBytes = A_OPS + (B_NATIVE ? B_OPS / 2 : B_OPS) + L::SFA_BYTES + L::SFB_BYTES;
+      const uint8_t* sfa = p.sfa_g + ((bt * p.mt + mtile) * p.kt) * L::SFA_BYTES;
+      const uint8_t* sfb = p.sfb_g + ((bbt * p.nt + ntile) * p.kt) * L::SFB_BYTES;
+      int issued = 0;
+      for (int kt = 0; kt < num_k; ++kt) {
+        const int s = kt % S, n = kt / S;
+        if (n > 0 && !ptx::mbar_wait(&empty[s], (n - 1) & 1, WAIT_LIMIT, abort_flag)) {
+          flag_error(1u, abort_flag);
+          break;
+        }
+        if (*abort_flag) break;
+        ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
+        ptx::tma_load_3d(smem + L::OFF_AOPS + s * A_OPS, &tmap_a, &full[s], kt * BK, (int)m0, (int)bt);
+        ptx::tma_load_3d(smem + L::OFF_BOPS + s * B_OPS, &tmap_b, &full[s], kt * BK, (int)n0, (int)bbt);
+        ptx::bulk_load(smem + L::OFF_SFA + s * L::SFA_BYTES, sfa + (int64_t)kt * L::SFA_BYTES, L::SFA_BYTES,
+                       &full[s]);
+        ptx::bulk_load(smem + L::OFF_SFB + s * L::SFB_BYTES, sfb + (int64_t)kt * L::SFB_BYTES, L::SFB_BYTES,
+                       &full[s]);
+        ++issued;
+      }
+      // drain: every issued copy lands before the CTA may exit
+      for (int kt = (issued > S ? issued - S : 0); kt < issued; ++kt)
+        ptx::mbar_wait(&full[kt % S], (kt / S) & 1, WAIT_LIMIT, never);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t b_fmt = B_NATIVE ? 5u : 0u;  // E2M1 or E4M3
+      for (int kt = 0; kt < num_k; ++kt) {
+        const int s = kt % S, n = kt / S;
+        if (!ptx::mbar_wait(&full[s], n & 1, WAIT_LIMIT, abort_flag)) { flag_error(2u, abort_flag); break; }
+        if (*abort_flag) break;
+        ptx::tc_fence_after();
+        const uint32_t a_addr = ptx::smem_u32(smem + L::OFF_AOPS + s * A_OPS);
+        const uint32_t b_addr = ptx::smem_u32(smem + L::OFF_BOPS + s * B_OPS);
+        const uint32_t sfa_addr = ptx::smem_u32(smem + L::OFF_SFA + s * L::SFA_BYTES);
+        const uint32_t sfb_addr = ptx::smem_u32(smem + L::OFF_SFB + s * L::SFB_BYTES);
+        const uint32_t tsf = tmem + SF_COL + 16u * s;
+        // 32 rows x 16 bytes each, core matrices 128 bytes apart
+        ptx::tc_cp_32x128b_x4(tsf, ptx::sdesc_noswz(sfa_addr, 128u, 128u));
+        ptx::tc_cp_32x128b_x4(tsf + 4u, ptx::sdesc_noswz(sfb_addr, 128u, 128u));
+        ptx::tc_cp_32x128b_x4(tsf + 8u, ptx::sdesc_noswz(sfb_addr + 512u, 128u, 128u));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          ptx::mma_mxf8f6f4(tmem, ptx::sdesc_sw128(a_addr + 32u * j), ptx::sdesc_sw128(b_addr + 32u * j),
+                            ptx::idesc_mxf8(BM, BN, 0u, b_fmt, (uint32_t)j), tsf, tsf + 4u,
+                            (kt > 0 || j > 0) ? 1u : 0u);
+        }
+        ptx::tc_commit(&empty[s]);
+      }
+      ptx::tc_commit(acc_full);
+      ptx::tc_commit(drain);
+      ptx::mbar_wait(drain, 0, WAIT_LIMIT, never);
+    }
+  } else if (warp >= DEC_WARP0) {
+    // --------------------------------------------------------- epilogue
+    const bool got = !*abort_flag && ptx::mbar_wait(acc_full, 0, WAIT_LIMIT, abort_flag);
+    if (!got) {
+      if (!*abort_flag) flag_error(16u, abort_flag);
+    } else {
+      epilogue_tile(p, &tmap_c, tmem, smem + L::OFF_BOPS, m0, n0, bt, warp, lane);
     }
   }
   ptx::tc_fence_before();
@@ -575,6 +698,40 @@ bool make_c_map(CUtensorMap* m, float* c, int64_t rows, int64_t cols, int64_t ba
          CUDA_SUCCESS;
 }
 
+// 3-D map over an expanded e4m3 plane [batch][rows][k_pad] read straight into
+// the 128-byte-swizzled K-major operand layout: boxes of 128 bytes x box_rows.
+bool make_e4m3_map(CUtensorMap* m, const void* base, int64_t k_pad, int64_t rows, int64_t batch,
+                   uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)k_pad, (cuuint64_t)rows, (cuuint64_t)batch};
+  const cuuint64_t strides[2] = {(cuuint64_t)k_pad, (cuuint64_t)(k_pad * rows)};
+  const cuuint32_t box[3] = {(cuuint32_t)BK, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool B_NATIVE>
+cudaError_t launch_staged(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const TcParams& p,
+                          dim3 grid, cudaStream_t st) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_staged_kernel<B_NATIVE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         PlanS::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  gemm_staged_kernel<B_NATIVE><<<grid, NUM_THREADS, PlanS::SMEM_BYTES, st>>>(ma, mb, mc, p);
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess && std::getenv("MIX_DEBUG") != nullptr)
+    std::fprintf(stderr, "gemm_staged launch: %s\n", cudaGetErrorString(e));
+  return e;
+}
+
 template <bool B_NATIVE>
 cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const TcParams& p,
                       dim3 grid, cudaStream_t st) {
@@ -596,12 +753,37 @@ cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtens
 
 }  // namespace
 
-cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, cudaStream_t st, mix_status_t* why) {
-  *why = MIX_OK;
-  if (d.K == 0 || d.M > (int64_t)INT32_MAX || d.N > (int64_t)INT32_MAX || d.batch > 65535) {
-    *why = MIX_ERR_UNSUPPORTED;
-    return cudaSuccess;
-  }
+namespace {
+
+TcParams make_params(const mix_gemm_desc_t& d) {
+  TcParams p{};
+  p.M = d.M; p.N = d.N; p.K = d.K; p.batch = d.batch; p.b_group = d.b_group;
+  p.a_shared = d.a_shared; p.a_ld = d.a_ld; p.a_bs = d.a_batch_stride;
+  p.a_type = (int)d.a_type; p.a_ebias = d.a_ebias; p.b_fp4 = d.b_type == MX_FP4_E2M1;
+  p.b_scales = d.b_scales; p.b_ld = d.b_ld; p.b_bs = d.b_batch_stride;
+  p.c = d.c; p.ldc = d.ldc; p.cbs = d.c_batch_stride;
+  p.epi = (int)d.epi; p.epi_ebias = d.epi_ebias; p.epi_flags = d.epi_flags;
+  p.out_codes = d.out_codes; p.out_shared = d.out_shared; p.out_ld = d.out_ld; p.out_bs = d.out_batch_stride;
+  return p;
+}
+
+bool shape_ok(const mix_gemm_desc_t& d) {
+  return d.K > 0 && d.M <= (int64_t)INT32_MAX && d.N <= (int64_t)INT32_MAX && d.batch <= 65535 &&
+         (d.N + BN - 1) / BN <= 65535;
+}
+
+// The staged path: wide outputs (two or more 256-column tiles re-use each A
+// tile) and index spaces of the expansion passes within 32 bits.
+bool want_staged(const mix_gemm_desc_t& d) {
+  if (d.algo == MIX_GEMM_TCGEN05_FUSED) return false;
+  const StagedPlan sp = staged_plan(d);
+  const int64_t lim = (int64_t)1 << 31;
+  if (expand_a_threads(d, sp) >= lim || expand_b_threads(sp) >= lim) return false;
+  if (d.algo == MIX_GEMM_TCGEN05_STAGED) return true;
+  return d.N > BN;
+}
+
+cudaError_t launch_fused(const mix_gemm_desc_t& d, cudaStream_t st, mix_status_t* why) {
   const int64_t bb = (d.batch + d.b_group - 1) / d.b_group;
   CUtensorMap ma, mb;
   if (!make_code_map(&ma, d.a_codes, d.K, d.M, d.batch, d.a_ld, d.a_batch_stride, BM)) {
@@ -616,14 +798,7 @@ cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, cudaStream_t st, mix_status
     *why = MIX_ERR_UNSUPPORTED;
     return cudaSuccess;
   }
-  TcParams p{};
-  p.M = d.M; p.N = d.N; p.K = d.K; p.batch = d.batch; p.b_group = d.b_group;
-  p.a_shared = d.a_shared; p.a_ld = d.a_ld; p.a_bs = d.a_batch_stride;
-  p.a_type = (int)d.a_type; p.a_ebias = d.a_ebias; p.b_fp4 = d.b_type == MX_FP4_E2M1;
-  p.b_scales = d.b_scales; p.b_ld = d.b_ld; p.b_bs = d.b_batch_stride;
-  p.c = d.c; p.ldc = d.ldc; p.cbs = d.c_batch_stride;
-  p.epi = (int)d.epi; p.epi_ebias = d.epi_ebias; p.epi_flags = d.epi_flags;
-  p.out_codes = d.out_codes; p.out_shared = d.out_shared; p.out_ld = d.out_ld; p.out_bs = d.out_batch_stride;
+  const TcParams p = make_params(d);
   CUtensorMap mc = ma;  // placeholder when there is no fp32 output
   if (d.c != nullptr && !make_c_map(&mc, d.c, d.M, d.N, d.batch, d.ldc, d.c_batch_stride)) {
     *why = MIX_ERR_UNSUPPORTED;
@@ -631,6 +806,63 @@ cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, cudaStream_t st, mix_status
   }
   const dim3 grid((unsigned)((d.M + BM - 1) / BM), (unsigned)((d.N + BN - 1) / BN), (unsigned)d.batch);
   return native ? launch_tc<true>(ma, mb, mc, p, grid, st) : launch_tc<false>(ma, mb, mc, p, grid, st);
+}
+
+
+cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t st, mix_status_t* why) {
+  const StagedPlan sp = staged_plan(d);
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(ws) + kStagedAlign - 1) & ~static_cast<uintptr_t>(kStagedAlign - 1));
+  CUtensorMap ma, mb;
+  if (!make_e4m3_map(&ma, base + sp.off_a, sp.k_pad, d.M, d.batch, BM)) {
+    *why = MIX_ERR_UNSUPPORTED;
+    return cudaSuccess;
+  }
+  const bool ok_b = sp.b_native ? make_fp4_operand_map(&mb, d.b_codes, d.K, d.N, sp.bb, d.b_ld, d.b_batch_stride)
+                                : make_e4m3_map(&mb, base + sp.off_b, sp.k_pad, d.N, sp.bb, BN);
+  if (!ok_b) {
+    *why = MIX_ERR_UNSUPPORTED;
+    return cudaSuccess;
+  }
+  CUtensorMap mc = ma;  // placeholder when there is no fp32 output
+  if (d.c != nullptr && !make_c_map(&mc, d.c, d.M, d.N, d.batch, d.ldc, d.c_batch_stride)) {
+    *why = MIX_ERR_UNSUPPORTED;
+    return cudaSuccess;
+  }
+  TcParams p = make_params(d);
+  p.sfa_g = base + sp.off_sfa;
+  p.sfb_g = base + sp.off_sfb;
+  p.mt = sp.mt; p.nt = sp.nt; p.kt = sp.kt;
+  cudaError_t e = launch_expand_a(d, sp, base, st);
+  if (e != cudaSuccess) return e;
+  e = launch_expand_b(d, sp, base, st);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)sp.mt, (unsigned)sp.nt, (unsigned)d.batch);
+  return sp.b_native ? launch_staged<true>(ma, mb, mc, p, grid, st) : launch_staged<false>(ma, mb, mc, p, grid, st);
+}
+
+}  // namespace
+
+size_t gemm_tc_workspace_bytes(const mix_gemm_desc_t& d) {
+  if (!shape_ok(d) || !want_staged(d)) return 0;
+  return staged_plan(d).bytes + kStagedAlign;
+}
+
+cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, void* ws, size_t ws_bytes, cudaStream_t st,
+                           mix_status_t* why) {
+  *why = MIX_OK;
+  if (!shape_ok(d)) {
+    *why = MIX_ERR_UNSUPPORTED;
+    return cudaSuccess;
+  }
+  if (want_staged(d)) {
+    if (ws == nullptr || ws_bytes < gemm_tc_workspace_bytes(d)) {
+      *why = MIX_ERR_WORKSPACE;
+      return cudaSuccess;
+    }
+    return launch_staged_path(d, ws, st, why);
+  }
+  return launch_fused(d, st, why);
 }
 
 }  // namespace mixk

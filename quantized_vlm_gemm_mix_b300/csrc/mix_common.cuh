@@ -138,6 +138,25 @@ __device__ __forceinline__ uint32_t max_key8(const uint32_t* u) {
   return k;
 }
 
+// Division by a runtime constant d (1 <= d < 2^31) of 32-bit numerators with
+// a multiply-high and a shift (Granlund and Montgomery, "Division by invariant
+// integers using multiplication", 1994): m = floor(2^32 (2^l - d) / d) + 1
+// with l = ceil(log2 d), q = (mulhi(n, m) + n) >> l.
+struct FastDiv {
+  uint32_t d, m, l;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  FastDiv f;
+  f.d = d;
+  f.l = 0;
+  while ((1ull << f.l) < d) ++f.l;
+  f.m = (uint32_t)((((1ull << 32) * ((1ull << f.l) - d)) / d) + 1);
+  return f;
+}
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+  return (uint32_t)(((uint64_t)__umulhi(n, f.m) + n) >> f.l);
+}
+
 // ---------------------------------------------------------------------------
 // MX (MXINT4 / MXFP4)
 // ---------------------------------------------------------------------------

@@ -27,7 +27,32 @@ cudaError_t launch_mx_dequantize(const uint8_t* codes, const uint8_t* scales, in
 // GEMM paths.  Descriptor already validated.
 size_t gemv_workspace_bytes(const mix_gemm_desc_t& d);
 cudaError_t launch_gemv_shiftadd(const mix_gemm_desc_t& d, void* ws, cudaStream_t st);
-cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, cudaStream_t st, mix_status_t* why);
+cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, void* ws, size_t ws_bytes, cudaStream_t st,
+                           mix_status_t* why);
+size_t gemm_tc_workspace_bytes(const mix_gemm_desc_t& d);
+
+// Staged tensor-core matmul: the operands are expanded once per call into the
+// caller's workspace -- e4m3 planes [batch][rows][k_pad] (k_pad = K rounded up
+// to 128, zero padded) and UE8M0 block-scale words grouped per (row tile,
+// 128-deep k-step): 128-row tiles for A (512 bytes), 256-row tiles for B
+// (1024 bytes, two 128-row halves).  Inside a 128-row group, 32-bit word
+// 4 l + i holds the four k-block scales (byte j = k-block 4 kt + j) of row
+// 32 i + l, so one tcgen05.cp of 32 rows x 128 bits puts row 32 i + l at TMEM
+// lane l (of every lane quadrant), column i.  MXFP4 weights that the
+// unpacking TMA can read in place are not expanded: only their scales are
+// regrouped.
+struct StagedPlan {
+  bool b_native;
+  int64_t k_pad, kt, mt, nt, bb;
+  size_t off_a, off_sfa, off_b, off_sfb, bytes;  // offsets from the 1024-aligned workspace base
+};
+constexpr int kStagedAlign = 1024;
+StagedPlan staged_plan(const mix_gemm_desc_t& d);
+bool staged_fp4_native_ok(const mix_gemm_desc_t& d);
+int64_t expand_a_threads(const mix_gemm_desc_t& d, const StagedPlan& sp);
+int64_t expand_b_threads(const StagedPlan& sp);
+cudaError_t launch_expand_a(const mix_gemm_desc_t& d, const StagedPlan& sp, unsigned char* base, cudaStream_t st);
+cudaError_t launch_expand_b(const mix_gemm_desc_t& d, const StagedPlan& sp, unsigned char* base, cudaStream_t st);
 
 // K-smoothing.
 size_t ksmooth_ws_bytes(int64_t tokens, int heads, int head_dim);

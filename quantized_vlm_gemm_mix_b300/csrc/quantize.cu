@@ -37,23 +37,6 @@ constexpr int kThreads = 256;
 constexpr int kQuadsPerCta = kThreads / 4;
 constexpr int kUnroll = 2;
 
-// n / d for 32-bit n and a divisor fixed per launch, by multiply-high with a
-// precomputed magic number (q = (umulhi(n, m) + n) >> l, l = ceil(log2 d)).
-struct FastDiv {
-  uint32_t d, m, l;
-};
-FastDiv make_fastdiv(uint32_t d) {
-  FastDiv f;
-  f.d = d;
-  f.l = 0;
-  while ((1ull << f.l) < d) ++f.l;
-  f.m = (uint32_t)((((1ull << 32) * ((1ull << f.l) - d)) / d) + 1);
-  return f;
-}
-__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
-  return (uint32_t)(((uint64_t)__umulhi(n, f.m) + n) >> f.l);
-}
-
 // Eight consecutive elements as fp32 bit patterns.
 template <bool BF16>
 __device__ __forceinline__ void load8(const void* base, int64_t elem, uint32_t* u) {

@@ -162,6 +162,30 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr) {
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
 
+// Shared memory matrix descriptor without swizzle: canonical core matrices of
+// 8 rows x 16 bytes (128 contiguous bytes each); lbo / sbo are the byte
+// distances between core matrices along K and along M/N.
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((smem_addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46);
+}
+
+// tcgen05.cp of a 32-row x 128-bit shared memory matrix into 32 TMEM lanes x
+// 4 columns, written to all four lane quadrants (row r -> lane 32 q + r).
+// Executes in issue order before a following tcgen05.mma of the same thread.
+__device__ __forceinline__ void tc_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// 1-D bulk copy global -> shared memory whose completion is counted, in
+// bytes, on an mbarrier.  Both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
 // Instruction descriptor of kind::mxf8f6f4 with block scaling: A and B E4M3
 // (format 0), K-major, fp32 accumulation, UE8M0 scales, M x N; a_sf_id /
 // b_sf_id pick the byte of each 32-bit scale cell (the 32-element K block).

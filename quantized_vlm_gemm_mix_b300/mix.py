@@ -24,7 +24,7 @@ MX_INT4, MX_FP4_E2M1 = 0, 1
 MIX_DT_F32, MIX_DT_BF16 = 0, 1
 MIX_ASYM_ZERO, MX_SCALE_FLOOR = 1, 2
 MIX_EPI_NONE, MIX_EPI_MIX_T1, MIX_EPI_MIX_T2, MIX_EPI_MXINT4, MIX_EPI_MXFP4 = 0, 1, 2, 3, 4
-MIX_GEMM_AUTO, MIX_GEMM_TCGEN05, MIX_GEMM_SHIFTADD = 0, 1, 2
+MIX_GEMM_AUTO, MIX_GEMM_TCGEN05, MIX_GEMM_SHIFTADD, MIX_GEMM_TCGEN05_STAGED, MIX_GEMM_TCGEN05_FUSED = 0, 1, 2, 3, 4
 KSMOOTH_COMPUTE, KSMOOTH_APPLY_FROZEN = 0, 1
 
 EXPORTS = ["mix_codes_bytes", "mix_shared_bytes", "mx_scales_bytes", "mix_quantize", "mx_quantize",

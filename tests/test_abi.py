@@ -72,3 +72,46 @@ def test_status_strings(mix):
     for s in range(8):
         assert isinstance(mix.status_str(s), str) and mix.status_str(s)
     assert mix.mix_version() >= 10000
+
+
+def _staged_desc(mix, M, N, K, b_type, batch=1, b_group=1, algo=None):
+    # fake, suitably aligned device addresses: nothing is launched
+    d = mix.GemmDesc()
+    d.M, d.N, d.K, d.batch, d.b_group = M, N, K, batch, b_group
+    d.a_type, d.a_ebias, d.b_type = mix.MIX_T2_4P5, -8, b_type
+    d.a_codes, d.a_shared, d.b_codes, d.b_scales, d.c = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000
+    d.a_ld, d.a_batch_stride, d.b_ld, d.b_batch_stride = K, M * K, K, N * K
+    d.ldc, d.c_batch_stride = N, M * N
+    d.algo = mix.MIX_GEMM_TCGEN05 if algo is None else algo
+    return d
+
+
+def test_staged_gemm_workspace_size_and_check(mix):
+    """The staged tensor-core path needs batch*M*Kp bytes of e4m3 A, 512 bytes
+    of A scale words per (128-row tile, 128-deep k-step), the same for an
+    expanded B (bB*N*Kp bytes, 1024 bytes per 256-row tile and k-step), each
+    part rounded up to 1 KiB, plus 1 KiB of alignment slack; a call without
+    that workspace is refused before anything is launched."""
+    L = mix.lib
+    kib = lambda v: (v + 1023) // 1024 * 1024
+    M, N, K = 300, 520, 416                      # MXINT4 weights: B expanded
+    kp, kt, mt, nt = 512, 4, 3, 3
+    want = kib(M * kp) + kib(mt * kt * 512) + kib(N * kp) + kib(nt * kt * 1024) + 1024
+    d = _staged_desc(mix, M, N, K, mix.MX_INT4)
+    assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == want
+    assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_WORKSPACE
+    assert L.mix_mx_gemm(ctypes.byref(d), ctypes.c_void_p(0x600000), want - 1, None) == mix.MIX_ERR_WORKSPACE
+    # MXFP4 with K % 128 == 0 is read in place: only its scale words are staged
+    M, N, K, B, G = 160, 4096, 512, 6, 3
+    d = _staged_desc(mix, M, N, K, mix.MX_FP4_E2M1, batch=B, b_group=G)
+    want = kib(B * M * K) + kib(B * 2 * 4 * 512) + kib((B // G) * 16 * 4 * 1024) + 1024
+    assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == want
+    # one 256-column tile: the fused-decode variant, no workspace
+    d = _staged_desc(mix, 300, 256, 416, mix.MX_INT4)
+    assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == 0
+    d = _staged_desc(mix, 300, 520, 416, mix.MX_INT4, algo=mix.MIX_GEMM_TCGEN05_FUSED)
+    assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == 0
+    d = _staged_desc(mix, 300, 256, 416, mix.MX_INT4, algo=mix.MIX_GEMM_TCGEN05_STAGED)
+    assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) > 0
+    d.algo = 5
+    assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_INVALID_ARG

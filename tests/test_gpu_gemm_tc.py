@@ -29,8 +29,16 @@ def operands(orc, seed, M, N, K, at, bt, a_dtype="bf16", batch=1, bb=1):
     return ac, ash, bc, bs
 
 
+ALGOS = ["staged", "fused"]
+
+
+def algo_id(mix, algo):
+    return {"auto": mix.MIX_GEMM_TCGEN05, "staged": mix.MIX_GEMM_TCGEN05_STAGED,
+            "fused": mix.MIX_GEMM_TCGEN05_FUSED}[algo]
+
+
 def run_tc(mix, ac, ash, at, bc, bs, bt, M, N, K, epi=0, epi_ebias=-8, epi_flags=1, batch=1, b_group=1,
-           want_c=True, **kw):
+           want_c=True, algo="auto", **kw):
     import torch
     c = torch.empty((batch, M, N), dtype=torch.float32, device="cuda") if want_c else None
     oc = osh = None
@@ -39,21 +47,40 @@ def run_tc(mix, ac, ash, at, bc, bs, bt, M, N, K, epi=0, epi_ebias=-8, epi_flags
         osh = torch.empty((batch, M, N // 32), dtype=torch.int16 if epi == 2 else torch.uint8, device="cuda")
     d = mix.gemm_desc(M, N, K, to_dev(ac), to_dev(ash), at, -8, to_dev(bc), to_dev(bs), bt, c=c, epi=epi,
                       epi_ebias=epi_ebias, epi_flags=epi_flags, out_codes=oc, out_shared=osh, batch=batch,
-                      b_group=b_group, algo=mix.MIX_GEMM_TCGEN05, **kw)
+                      b_group=b_group, algo=algo_id(mix, algo), **kw)
     mix.gemm(d)
     torch.cuda.synchronize()
     assert mix.mix_device_error() == 0
     return (to_host(c) if want_c else None), (to_host(oc) if epi else None), (to_host(osh) if epi else None)
 
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("at,bt", [(2, 1), (1, 0), (2, 0), (1, 1)])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 128), (300, 520, 416), (1, 32, 32), (17, 288, 3584)])
-def test_tc_matches_eq6(mix, orc, M, N, K, at, bt):
+def test_tc_matches_eq6(mix, orc, M, N, K, at, bt, algo):
     ac, ash, bc, bs = operands(orc, M * 7 + N + K, M, N, K, at, bt)
     ref = orc.gemm(ac, ash, at, -8, bc, bs, bt)
-    c, _, _ = run_tc(mix, ac, ash, at, bc, bs, bt, M, N, K)
+    c, _, _ = run_tc(mix, ac, ash, at, bc, bs, bt, M, N, K, algo=algo)
     err = row_rel_err(c[0], ref)
     assert err <= GEMM_REL_TOL, err
+
+
+@pytest.mark.parametrize("at,bt", [(2, 1), (1, 0)])
+@pytest.mark.parametrize("M,N,K,batch,b_group", [(300, 544, 416, 1, 1), (130, 768, 1024, 1, 1),
+                                                 (160, 288, 128, 6, 3), (257, 1024, 96, 1, 1)])
+def test_staged_equals_fused_bitwise(mix, orc, M, N, K, batch, b_group, at, bt):
+    """The staged variant (operands expanded once into the workspace, scales
+    moved by tcgen05.cp) and the fused-decode variant feed the MMA the same
+    exact operand values in the same K order, so their fp32 outputs agree bit
+    for bit; the fused MiX epilogue planes then agree too."""
+    ac, ash, bc, bs = operands(orc, 31 + M + N + K, M, N, K, at, bt, batch=batch, bb=batch // b_group)
+    c1, o1, s1 = run_tc(mix, ac, ash, at, bc, bs, bt, M, N, K, epi=2, batch=batch, b_group=b_group, algo="staged")
+    c2, o2, s2 = run_tc(mix, ac, ash, at, bc, bs, bt, M, N, K, epi=2, batch=batch, b_group=b_group, algo="fused")
+    assert np.array_equal(c1.view(np.uint32), c2.view(np.uint32))
+    assert np.array_equal(o1, o2) and np.array_equal(s1, s2)
+    ref = orc.gemm(ac.reshape(batch, M, -1), ash.reshape(batch, M, -1), at, -8,
+                   bc.reshape(batch // b_group, N, -1), bs.reshape(batch // b_group, N, -1), bt, b_group=b_group)
+    assert row_rel_err(c1, ref) <= GEMM_REL_TOL
 
 
 def test_tc_agrees_with_shiftadd_path(mix, orc):
@@ -91,12 +118,13 @@ def test_tiny_end_to_end_config(mix, orc):
     assert np.mean(oc[0] != rc2) < 1e-3
 
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("epi", [1, 2, 3, 4])
-def test_tc_epilogue_formats(mix, orc, epi):
+def test_tc_epilogue_formats(mix, orc, epi, algo):
     M, N, K = 200, 512, 640
     ac, ash, bc, bs = operands(orc, 11 + epi, M, N, K, 1, 0)
     c, oc, osh = run_tc(mix, ac, ash, 1, bc, bs, 0, M, N, K, epi=epi, epi_ebias=-6,
-                        epi_flags=1 if epi <= 2 else 0)
+                        epi_flags=1 if epi <= 2 else 0, algo=algo)
     if epi <= 2:
         rc, rs = orc.mix_quantize(c[0], epi, -6, 1)
     else:
@@ -113,7 +141,8 @@ def test_tc_epilogue_only_no_c(mix, orc):
     assert np.array_equal(oc[0], rc) and np.array_equal(osh[0], rs)
 
 
-def test_tc_batched_gqa_and_strides(mix, orc):
+@pytest.mark.parametrize("algo", ALGOS)
+def test_tc_batched_gqa_and_strides(mix, orc, algo):
     """Batch 6 in groups of 3 sharing B; A read through an interleaved row
     stride (the (token, head) layout of a QKV projection)."""
     B, G, M, N, K = 6, 3, 160, 288, 128
@@ -121,7 +150,8 @@ def test_tc_batched_gqa_and_strides(mix, orc):
     # interleave: row m of batch b at element offset m * (B*K) + b * K
     acb = ac.reshape(B, M, K // 2).transpose(1, 0, 2).copy()      # [M, B, K/2]
     ashb = ash.reshape(B, M, K // 32).transpose(1, 0, 2).copy()
-    c, _, _ = run_tc(mix, acb, ashb, 2, bc, bs, 0, M, N, K, batch=B, b_group=G, a_ld=B * K, a_batch_stride=K)
+    c, _, _ = run_tc(mix, acb, ashb, 2, bc, bs, 0, M, N, K, batch=B, b_group=G, a_ld=B * K, a_batch_stride=K,
+                     algo=algo)
     ref = orc.gemm(ac.reshape(B, M, -1), ash.reshape(B, M, -1), 2, -8, bc.reshape(B // G, N, -1),
                    bs.reshape(B // G, N, -1), 0, b_group=G)
     assert row_rel_err(c, ref) <= GEMM_REL_TOL
