@@ -100,29 +100,34 @@ __global__ void __launch_bounds__(kThreads) expand_a_kernel(const uint8_t* __res
 }
 
 // B: MX plane -> e4m3 of q / 4 (MXINT4) or the E2M1 value, and the MX scale
-// bytes regrouped into 256-row tiles.  WRITE_OPS false: scales only (MXFP4
-// weights the matmul reads in place).
+// bytes regrouped into tiles of `tile_rows` (<= 256) rows, each stored as a
+// 256-row group (two 128-row halves; the words of rows tile_rows .. 255 are
+// padding and hold scale 1).  Threads walk the padded 256-row index space.
+// WRITE_OPS false: scales only (MXFP4 weights the matmul reads in place).
 template <bool FP4, bool WRITE_OPS>
 __global__ void __launch_bounds__(kThreads) expand_b_kernel(const uint8_t* __restrict__ codes,
                                                             const uint8_t* __restrict__ scales, int64_t N,
                                                             int64_t K, int64_t b_ld, int64_t b_bs, int64_t bb,
-                                                            int64_t k_pad, int64_t nt, int64_t kt_n,
+                                                            int64_t k_pad, int tile_rows, int64_t kt_n,
                                                             FastDiv f_kbp, FastDiv f_rows,
                                                             uint8_t* __restrict__ b_e4m3, uint32_t* __restrict__ sfb) {
   const int64_t kbv = K / 32;
   const uint32_t total = (uint32_t)(bb * (int64_t)f_rows.d * f_kbp.d);
   const uint32_t total_w = (total + 31u) & ~31u;
   const uint32_t stride = gridDim.x * blockDim.x;
+  const int64_t nt = f_rows.d / 256;
   const DecTab tt = FP4 ? fp4_tab() : int4_tab();
   for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < total_w; t += stride) {
     const bool valid = t < total;
     const uint32_t rr = fdiv(t, f_kbp), kb = t - rr * f_kbp.d;
-    const uint32_t b = fdiv(rr, f_rows), r = rr - b * f_rows.d;
+    const uint32_t b = fdiv(rr, f_rows), vr = rr - b * f_rows.d;   // padded row
+    const uint32_t tile = vr >> 8, rin = vr & 255u;
+    const int64_t r = (int64_t)tile * tile_rows + rin;              // matrix row
     uint32_t sbyte = 127u;
-    if (valid && r < N) {
+    if (valid && (int)rin < tile_rows && r < N) {
       uint4 out0 = make_uint4(0, 0, 0, 0), out1 = make_uint4(0, 0, 0, 0);
       if (kb < kbv) {
-        const int64_t e = (int64_t)b * b_bs + (int64_t)r * b_ld + 32 * (int64_t)kb;
+        const int64_t e = (int64_t)b * b_bs + r * b_ld + 32 * (int64_t)kb;
         sbyte = (uint32_t)__ldg(scales + e / 32);
         if (WRITE_OPS) {
           const uint4 cv = __ldg(reinterpret_cast<const uint4*>(codes + e / 2));
@@ -139,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) expand_b_kernel(const uint8_t* __res
     }
     const uint32_t word = quad_or(sbyte << (8 * (kb & 3u)));
     if (valid && (kb & 3u) == 0) {
-      const int64_t tile = r >> 8, rin = r & 255, h = rin >> 7, rq = rin & 127;
+      const uint32_t h = rin >> 7, rq = rin & 127u;
       const int64_t idx = ((((int64_t)b * nt + tile) * kt_n + (kb >> 2)) * 2 + h) * 128 + (rq & 31) * 4 + (rq >> 5);
       sfb[idx] = word;
     }
@@ -171,7 +176,7 @@ StagedPlan staged_plan(const mix_gemm_desc_t& d) {
   sp.k_pad = (d.K + 127) / 128 * 128;
   sp.kt = sp.k_pad / 128;
   sp.mt = (d.M + 127) / 128;
-  sp.nt = (d.N + 255) / 256;
+  sp.nt = (d.N + kStagedBN - 1) / kStagedBN;
   sp.bb = (d.batch + d.b_group - 1) / d.b_group;
   size_t off = 0;
   sp.off_a = off;
@@ -210,19 +215,20 @@ cudaError_t launch_expand_a(const mix_gemm_desc_t& d, const StagedPlan& sp, unsi
 cudaError_t launch_expand_b(const mix_gemm_desc_t& d, const StagedPlan& sp, unsigned char* base, cudaStream_t st) {
   const int64_t threads = expand_b_threads(sp);
   const FastDiv fk = make_fastdiv((uint32_t)(sp.k_pad / 32)), fr = make_fastdiv((uint32_t)(sp.nt * 256));
+  const int tr = kStagedBN;
   uint8_t* b = base + sp.off_b;
   uint32_t* sfb = reinterpret_cast<uint32_t*>(base + sp.off_sfb);
   const int g = grid_for(threads);
   const int64_t bs = sp.bb > 1 ? d.b_batch_stride : 0;
   if (sp.b_native)
     expand_b_kernel<true, false><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
-                                                         sp.k_pad, sp.nt, sp.kt, fk, fr, nullptr, sfb);
+                                                         sp.k_pad, tr, sp.kt, fk, fr, nullptr, sfb);
   else if (d.b_type == MX_FP4_E2M1)
     expand_b_kernel<true, true><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
-                                                        sp.k_pad, sp.nt, sp.kt, fk, fr, b, sfb);
+                                                        sp.k_pad, tr, sp.kt, fk, fr, b, sfb);
   else
     expand_b_kernel<false, true><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
-                                                         sp.k_pad, sp.nt, sp.kt, fk, fr, b, sfb);
+                                                         sp.k_pad, tr, sp.kt, fk, fr, b, sfb);
   return cudaGetLastError();
 }
 

@@ -491,27 +491,98 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ---------------------------------------------------------- staged kernel
 // Operands expanded beforehand (e4m3 planes and regrouped scale words in the
-// workspace; MXFP4 weights read in place by the unpacking TMA).  The main
+// workspace; MXFP4 weights read in place by the unpacking TMA), so the main
 // loop has no decode: per 128-deep k-step the producer issues two tiled TMA
-// loads and two bulk copies of scale words onto one barrier, and the MMA
-// thread moves the scale words into TMEM with tcgen05.cp (which executes in
-// order before its MMAs) and issues four MMAs.  The sixteen epilogue warps
-// are idle until the accumulator is complete.
+// loads and two bulk copies of scale words onto one barrier; four scale
+// warps (one per TMEM lane quadrant) store the scale words into TMEM with
+// tcgen05.st, off the tensor pipe (a tcgen05.cp there would serialise with
+// the MMAs), and the MMA thread issues four MMAs once they are in place.
+//
+// Persistent: one CTA per SM walks the 128 x 224 output tiles (M fastest, so
+// the CTAs in flight share B tiles and the whole of A stays in L2).  Two
+// TMEM accumulators let the twelve epilogue warps drain tile i while the
+// MMAs of tile i + 1 run.  224 columns make room in the 512 TMEM columns:
+// accumulators at columns 0 and 256, the four 12-column scale slots of the
+// operand ring in the gaps (224, 240, 480, 496).
+//
+// Warps: 0 TMA producer, 1 TMEM allocator and MMA issuer, 2-5 scale
+// writers, 6-17 epilogue.  Eighteen warps at 96 registers fit the register
+// file of each SM sub-partition (five warps on the fullest).
+constexpr int BNS = kStagedBN;      // 224
+constexpr int B_OPS_S = BNS * BK;   // 28 KB
+constexpr int SF_WARP0 = 2, EPI_WARP0 = 6, NUM_EPI_WARPS = 12;
+constexpr int NUM_THREADS_S = (EPI_WARP0 + NUM_EPI_WARPS) * 32;  // 576
 struct PlanS {
   static constexpr int S = 4;
   static constexpr int SFA_BYTES = 512, SFB_BYTES = 1024;
+  static constexpr int CST_BYTES = 2048;  // per epilogue warp: 32 rows x 16 fp32, 64-byte swizzle
   static constexpr int OFF_AOPS = 0;
   static constexpr int OFF_BOPS = OFF_AOPS + S * A_OPS;
-  static constexpr int OFF_SFA = OFF_BOPS + S * B_OPS;
+  static constexpr int OFF_SFA = OFF_BOPS + S * B_OPS_S;
   static constexpr int OFF_SFB = OFF_SFA + S * SFA_BYTES;
-  static constexpr int OFF_BAR = OFF_SFB + S * SFB_BYTES;
-  static constexpr int NUM_BARS = 2 * S + 2;
+  static constexpr int OFF_CST = OFF_SFB + S * SFB_BYTES;
+  static constexpr int OFF_BAR = OFF_CST + NUM_EPI_WARPS * CST_BYTES;
+  static constexpr int NUM_BARS = 3 * S + 4 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
 };
+static_assert(PlanS::SMEM_BYTES <= 227 * 1024, "staged plan exceeds shared memory");
+static_assert(B_OPS_S % 1024 == 0, "operand stages must keep the 1024-byte swizzle alignment");
+
+__device__ __forceinline__ uint32_t acc_col(int b) { return b ? 256u : 0u; }
+__device__ __forceinline__ uint32_t sf_col(int s) { return (s & 2 ? 480u : 224u) + 16u * (uint32_t)(s & 1); }
+
+// Epilogue of one 128 x 224 tile held in TMEM columns acc..acc+223: warp w
+// (EPI_WARP0 ..) reads lane quadrant w % 4 and the 32-column chunks cg,
+// cg + 3, cg + 6 (cg = its column group 0..2).  fp32 C leaves through one 2 KB
+// staging tile per warp (32 rows x 16 columns, 64-byte swizzle) and TMA
+// stores; the fused quantiser writes codes and shared fields from registers.
+__device__ __forceinline__ void epilogue_tile_s(const TcParams& p, const CUtensorMap* tmap_c, uint32_t tmem_acc,
+                                                unsigned char* cst, int64_t m0, int64_t n0, int64_t bt, int warp,
+                                                int lane, bool& c_pending) {
+  const uint32_t q = (uint32_t)(warp & 3);
+  const int cg = (warp - EPI_WARP0) >> 2;
+  const int64_t row = m0 + 32 * q + lane;
+  for (int cc = cg; cc < BNS / 32; cc += NUM_EPI_WARPS / 4) {
+    uint32_t u[32];
+    ptx::tmem_ld_x32(tmem_acc + ((32u * q) << 16) + (uint32_t)(cc * 32), u);
+    ptx::tmem_wait_ld();
+    const int64_t col = n0 + cc * 32;
+    if (p.c != nullptr && col < p.N && m0 + 32 * q < p.M) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        if (c_pending) {
+          if (lane == 0) ptx::bulk_wait_read0();  // the previous store has read the buffer
+          __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(cst + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+              make_uint4(u[16 * hh + 4 * j], u[16 * hh + 4 * j + 1], u[16 * hh + 4 * j + 2], u[16 * hh + 4 * j + 3]);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_3d(tmap_c, cst, (int)(col + 16 * hh), (int)(m0 + 32 * q), (int)bt);
+          ptx::bulk_commit();
+        }
+        c_pending = true;
+      }
+    }
+    if (row >= p.M || col >= p.N) continue;
+    if (p.epi != MIX_EPI_NONE) {
+      uint4 cw;
+      uint32_t sh;
+      epi_quant_block(u, p, cw, sh);
+      const int64_t e = bt * p.out_bs + row * p.out_ld + col;
+      *reinterpret_cast<uint4*>(p.out_codes + e / 2) = cw;
+      if (p.epi == MIX_EPI_MIX_T2) static_cast<uint16_t*>(p.out_shared)[e / 32] = (uint16_t)sh;
+      else static_cast<uint8_t*>(p.out_shared)[e / 32] = (uint8_t)sh;
+    }
+  }
+}
 
 template <bool B_NATIVE>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __maxnreg__(96)
     gemm_staged_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_c, const TcParams p) {
   using L = PlanS;
@@ -520,25 +591,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
-  uint64_t* full = bars;            // TMA + bulk copies of one stage
-  uint64_t* empty = bars + S;       // MMA commit
-  uint64_t* acc_full = bars + 2 * S;
-  uint64_t* drain = acc_full + 1;
+  uint64_t* full = bars;               // TMA + bulk copies of one stage
+  uint64_t* empty = bars + S;          // MMA commit
+  uint64_t* sf_ready = bars + 2 * S;   // four scale warps: the stage's scales are in TMEM
+  uint64_t* acc_full = bars + 3 * S;   // [2] MMA commit after a tile's last k-step
+  uint64_t* acc_empty = acc_full + 2;  // [2] twelve epilogue warps
+  uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);  // drains ignore aborts
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t mtile = blockIdx.x, ntile = blockIdx.y, bt = blockIdx.z;
-  const int64_t m0 = mtile * BM, n0 = ntile * BN, bbt = bt / p.b_group;
   const int num_k = (int)p.kt;
+  const int mt = (int)p.mt, nt = (int)p.nt;
+  const int tiles = (int)(p.batch * p.nt * p.mt);  // < 2^31: checked on the host
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       ptx::mbar_init(&full[i], 1);
       ptx::mbar_init(&empty[i], 1);
+      ptx::mbar_init(&sf_ready[i], 4);
     }
-    ptx::mbar_init(acc_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&acc_full[i], 1);
+      ptx::mbar_init(&acc_empty[i], NUM_EPI_WARPS);
+    }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
     *never = 0;
@@ -558,68 +635,132 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      constexpr uint32_t kStageBytes = A_OPS + (B_NATIVE ? B_OPS / 2 : B_OPS) + L::SFA_BYTES + L::SFB_BYTES;
-      const uint8_t* sfa = p.sfa_g + ((bt * p.mt + mtile) * p.kt) * L::SFA_BYTES;
-      const uint8_t* sfb = p.sfb_g + ((bbt * p.nt + ntile) * p.kt) * L::SFB_BYTES;
-      int issued = 0;
-      for (int kt = 0; kt < num_k; ++kt) {
-        const int s = kt % S, n = kt / S;
-        if (n > 0 && !ptx::mbar_wait(&empty[s], (n - 1) & 1, WAIT_LIMIT, abort_flag)) {
-          flag_error(1u, abort_flag);
-          break;
+      constexpr uint32_t kStageBytes = A_OPS + (B_NATIVE ? B_OPS_S / 2 : B_OPS_S) + L::SFA_BYTES + L::SFB_BYTES;
+      int64_t g = 0;  // k-steps issued by this CTA
+      bool stop = false;
+      for (int t = blockIdx.x; t < tiles && !stop; t += gridDim.x) {
+        const int mtile = t % mt, rest = t / mt, ntile = rest % nt, bt = rest / nt, bbt = bt / (int)p.b_group;
+        const uint8_t* sfa = p.sfa_g + (((int64_t)bt * mt + mtile) * p.kt) * L::SFA_BYTES;
+        const uint8_t* sfb = p.sfb_g + (((int64_t)bbt * nt + ntile) * p.kt) * L::SFB_BYTES;
+        for (int kt = 0; kt < num_k; ++kt, ++g) {
+          const int s = (int)(g % S);
+          const uint32_t n = (uint32_t)(g / S);
+          if (n > 0 && !ptx::mbar_wait_spin(&empty[s], (n - 1) & 1, WAIT_LIMIT, abort_flag)) {
+            flag_error(1u, abort_flag);
+            stop = true;
+            break;
+          }
+          if (*abort_flag) { stop = true; break; }
+          ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
+          ptx::tma_load_3d(smem + L::OFF_AOPS + s * A_OPS, &tmap_a, &full[s], kt * BK, mtile * BM, bt);
+          ptx::tma_load_3d(smem + L::OFF_BOPS + s * B_OPS_S, &tmap_b, &full[s], kt * BK, ntile * BNS, bbt);
+          ptx::bulk_load(smem + L::OFF_SFA + s * L::SFA_BYTES, sfa + (int64_t)kt * L::SFA_BYTES, L::SFA_BYTES,
+                         &full[s]);
+          ptx::bulk_load(smem + L::OFF_SFB + s * L::SFB_BYTES, sfb + (int64_t)kt * L::SFB_BYTES, L::SFB_BYTES,
+                         &full[s]);
         }
-        if (*abort_flag) break;
-        ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
-        ptx::tma_load_3d(smem + L::OFF_AOPS + s * A_OPS, &tmap_a, &full[s], kt * BK, (int)m0, (int)bt);
-        ptx::tma_load_3d(smem + L::OFF_BOPS + s * B_OPS, &tmap_b, &full[s], kt * BK, (int)n0, (int)bbt);
-        ptx::bulk_load(smem + L::OFF_SFA + s * L::SFA_BYTES, sfa + (int64_t)kt * L::SFA_BYTES, L::SFA_BYTES,
-                       &full[s]);
-        ptx::bulk_load(smem + L::OFF_SFB + s * L::SFB_BYTES, sfb + (int64_t)kt * L::SFB_BYTES, L::SFB_BYTES,
-                       &full[s]);
-        ++issued;
       }
       // drain: every issued copy lands before the CTA may exit
-      for (int kt = (issued > S ? issued - S : 0); kt < issued; ++kt)
-        ptx::mbar_wait(&full[kt % S], (kt / S) & 1, WAIT_LIMIT, never);
+      for (int64_t h = (g > S ? g - S : 0); h < g; ++h)
+        ptx::mbar_wait(&full[h % S], (uint32_t)(h / S) & 1, WAIT_LIMIT, never);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       const uint32_t b_fmt = B_NATIVE ? 5u : 0u;  // E2M1 or E4M3
-      for (int kt = 0; kt < num_k; ++kt) {
-        const int s = kt % S, n = kt / S;
-        if (!ptx::mbar_wait(&full[s], n & 1, WAIT_LIMIT, abort_flag)) { flag_error(2u, abort_flag); break; }
-        if (*abort_flag) break;
-        ptx::tc_fence_after();
-        const uint32_t a_addr = ptx::smem_u32(smem + L::OFF_AOPS + s * A_OPS);
-        const uint32_t b_addr = ptx::smem_u32(smem + L::OFF_BOPS + s * B_OPS);
-        const uint32_t sfa_addr = ptx::smem_u32(smem + L::OFF_SFA + s * L::SFA_BYTES);
-        const uint32_t sfb_addr = ptx::smem_u32(smem + L::OFF_SFB + s * L::SFB_BYTES);
-        const uint32_t tsf = tmem + SF_COL + 16u * s;
-        // 32 rows x 16 bytes each, core matrices 128 bytes apart
-        ptx::tc_cp_32x128b_x4(tsf, ptx::sdesc_noswz(sfa_addr, 128u, 128u));
-        ptx::tc_cp_32x128b_x4(tsf + 4u, ptx::sdesc_noswz(sfb_addr, 128u, 128u));
-        ptx::tc_cp_32x128b_x4(tsf + 8u, ptx::sdesc_noswz(sfb_addr + 512u, 128u, 128u));
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          ptx::mma_mxf8f6f4(tmem, ptx::sdesc_sw128(a_addr + 32u * j), ptx::sdesc_sw128(b_addr + 32u * j),
-                            ptx::idesc_mxf8(BM, BN, 0u, b_fmt, (uint32_t)j), tsf, tsf + 4u,
-                            (kt > 0 || j > 0) ? 1u : 0u);
+      int64_t g = 0;
+      int i = 0;  // local tile index
+      bool stop = false;
+      for (int t = blockIdx.x; t < tiles && !stop; t += gridDim.x, ++i) {
+        const int b = i & 1;
+        if (i >= 2 && !ptx::mbar_wait_spin(&acc_empty[b], (uint32_t)((i >> 1) - 1) & 1, WAIT_LIMIT, abort_flag)) {
+          flag_error(256u, abort_flag);
+          break;
         }
-        ptx::tc_commit(&empty[s]);
+        ptx::tc_fence_after();
+        const uint32_t dacc = tmem + acc_col(b);
+        for (int kt = 0; kt < num_k; ++kt, ++g) {
+          const int s = (int)(g % S);
+          const uint32_t n = (uint32_t)(g / S);
+          // the scale warps arrive only after the stage's copies landed
+          if (!ptx::mbar_wait_spin(&sf_ready[s], n & 1, WAIT_LIMIT, abort_flag)) {
+            flag_error(2u, abort_flag);
+            stop = true;
+            break;
+          }
+          if (*abort_flag) { stop = true; break; }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ptx::smem_u32(smem + L::OFF_AOPS + s * A_OPS);
+          const uint32_t b_addr = ptx::smem_u32(smem + L::OFF_BOPS + s * B_OPS_S);
+          const uint32_t tsf = tmem + sf_col(s);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            ptx::mma_mxf8f6f4(dacc, ptx::sdesc_sw128(a_addr + 32u * j), ptx::sdesc_sw128(b_addr + 32u * j),
+                              ptx::idesc_mxf8(BM, BNS, 0u, b_fmt, (uint32_t)j), tsf, tsf + 4u,
+                              (kt > 0 || j > 0) ? 1u : 0u);
+          }
+          ptx::tc_commit(&empty[s]);
+        }
+        if (stop) break;
+        ptx::tc_commit(&acc_full[b]);
       }
-      ptx::tc_commit(acc_full);
       ptx::tc_commit(drain);
       ptx::mbar_wait(drain, 0, WAIT_LIMIT, never);
     }
-  } else if (warp >= DEC_WARP0) {
-    // --------------------------------------------------------- epilogue
-    const bool got = !*abort_flag && ptx::mbar_wait(acc_full, 0, WAIT_LIMIT, abort_flag);
-    if (!got) {
-      if (!*abort_flag) flag_error(16u, abort_flag);
-    } else {
-      epilogue_tile(p, &tmap_c, tmem, smem + L::OFF_BOPS, m0, n0, bt, warp, lane);
+  } else if (warp < EPI_WARP0) {
+    // -------------------------------------------------------- scale warps
+    // Lane l of the warp for lane quadrant q stores, per k-step, the 32-bit
+    // scale words of rows 32 i + l (i = 0..3) of A and of both 128-row
+    // halves of B -- one 16-byte shared load each, laid out that way by the
+    // staging pass -- into TMEM lane 32 q + l: every quadrant holds a replica.
+    const uint32_t q = (uint32_t)(warp & 3);
+    const uint32_t tq = tmem + ((32u * q) << 16);
+    int64_t g = 0;
+    bool stop = false;
+    for (int t = blockIdx.x; t < tiles && !stop; t += gridDim.x) {
+      for (int kt = 0; kt < num_k; ++kt, ++g) {
+        const int s = (int)(g % S);
+        const uint32_t n = (uint32_t)(g / S);
+        if (!ptx::mbar_wait(&full[s], n & 1, WAIT_LIMIT, abort_flag)) {
+          flag_error(32u, abort_flag);
+          stop = true;
+          break;
+        }
+        if (*abort_flag) { stop = true; break; }
+        ptx::tc_fence_after();
+        const uint4 wa = *reinterpret_cast<const uint4*>(smem + L::OFF_SFA + s * L::SFA_BYTES + 16 * lane);
+        const uint4 wb0 = *reinterpret_cast<const uint4*>(smem + L::OFF_SFB + s * L::SFB_BYTES + 16 * lane);
+        const uint4 wb1 = *reinterpret_cast<const uint4*>(smem + L::OFF_SFB + s * L::SFB_BYTES + 512 + 16 * lane);
+        const uint32_t col = tq + sf_col(s);
+        ptx::tmem_st_x4(col, wa.x, wa.y, wa.z, wa.w);
+        ptx::tmem_st_x4(col + 4u, wb0.x, wb0.y, wb0.z, wb0.w);
+        ptx::tmem_st_x4(col + 8u, wb1.x, wb1.y, wb1.z, wb1.w);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sf_ready[s]);
+      }
     }
+  } else {
+    // --------------------------------------------------------- epilogue
+    unsigned char* cst = smem + L::OFF_CST + (warp - EPI_WARP0) * L::CST_BYTES;
+    bool c_pending = false;
+    int i = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      if (*abort_flag || !ptx::mbar_wait(&acc_full[b], (uint32_t)(i >> 1) & 1, WAIT_LIMIT, abort_flag)) {
+        if (!*abort_flag) flag_error(16u, abort_flag);
+        break;
+      }
+      ptx::tc_fence_after();
+      const int mtile = t % mt, rest = t / mt, ntile = rest % nt, bt = rest / nt;
+      epilogue_tile_s(p, &tmap_c, tmem + acc_col(b), cst, (int64_t)mtile * BM, (int64_t)ntile * BNS, bt, warp, lane,
+                      c_pending);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&acc_empty[b]);
+    }
+    if (c_pending && lane == 0) ptx::bulk_wait_read0();  // staging read before the CTA exits
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -667,7 +808,7 @@ bool make_code_map(CUtensorMap* m, const void* base, int64_t k, int64_t rows, in
 // of padding) and applies the 128-byte swizzle, giving 128-byte K-major rows
 // of 128 elements.  Needs K % 128 == 0, 32-byte aligned base and strides.
 bool make_fp4_operand_map(CUtensorMap* m, const void* base, int64_t k, int64_t rows, int64_t batch,
-                          int64_t ld_elems, int64_t bs_elems) {
+                          int64_t ld_elems, int64_t bs_elems, uint32_t box_rows = BN) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   if (k % 128 != 0 || (reinterpret_cast<uintptr_t>(base) & 31) != 0 || (ld_elems / 2) % 32 != 0) return false;
@@ -676,26 +817,28 @@ bool make_fp4_operand_map(CUtensorMap* m, const void* base, int64_t k, int64_t r
   if (bs % 32 != 0) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)k, (cuuint64_t)rows, (cuuint64_t)batch};
   const cuuint64_t strides[2] = {(cuuint64_t)(ld_elems / 2), (cuuint64_t)bs};
-  const cuuint32_t box[3] = {(cuuint32_t)BK, (cuuint32_t)BN, 1};
+  const cuuint32_t box[3] = {(cuuint32_t)BK, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D fp32 map over C for the epilogue's TMA stores: 32 x 32 boxes, 128-byte swizzle.
-bool make_c_map(CUtensorMap* m, float* c, int64_t rows, int64_t cols, int64_t batch, int64_t ldc, int64_t cbs) {
+// 3-D fp32 map over C for the epilogue's TMA stores: 32-row boxes of 32
+// columns with the 128-byte swizzle, or of 16 columns with the 64-byte one.
+bool make_c_map(CUtensorMap* m, float* c, int64_t rows, int64_t cols, int64_t batch, int64_t ldc, int64_t cbs,
+                uint32_t box_cols = 32) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   int64_t bs = cbs * 4;
   if (batch <= 1 || bs <= 0) bs = ldc * 4 * rows;
   const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)batch};
   const cuuint64_t strides[2] = {(cuuint64_t)(ldc * 4), (cuuint64_t)bs};
-  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t box[3] = {box_cols, 32, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, c, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
+            box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // 3-D map over an expanded e4m3 plane [batch][rows][k_pad] read straight into
@@ -725,7 +868,7 @@ cudaError_t launch_staged(const CUtensorMap& ma, const CUtensorMap& mb, const CU
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  gemm_staged_kernel<B_NATIVE><<<grid, NUM_THREADS, PlanS::SMEM_BYTES, st>>>(ma, mb, mc, p);
+  gemm_staged_kernel<B_NATIVE><<<grid, NUM_THREADS_S, PlanS::SMEM_BYTES, st>>>(ma, mb, mc, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess && std::getenv("MIX_DEBUG") != nullptr)
     std::fprintf(stderr, "gemm_staged launch: %s\n", cudaGetErrorString(e));
@@ -778,7 +921,7 @@ bool want_staged(const mix_gemm_desc_t& d) {
   if (d.algo == MIX_GEMM_TCGEN05_FUSED) return false;
   const StagedPlan sp = staged_plan(d);
   const int64_t lim = (int64_t)1 << 31;
-  if (expand_a_threads(d, sp) >= lim || expand_b_threads(sp) >= lim) return false;
+  if (expand_a_threads(d, sp) >= lim || expand_b_threads(sp) >= lim || d.batch * sp.mt * sp.nt >= lim) return false;
   if (d.algo == MIX_GEMM_TCGEN05_STAGED) return true;
   return d.N > BN;
 }
@@ -818,14 +961,14 @@ cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t 
     *why = MIX_ERR_UNSUPPORTED;
     return cudaSuccess;
   }
-  const bool ok_b = sp.b_native ? make_fp4_operand_map(&mb, d.b_codes, d.K, d.N, sp.bb, d.b_ld, d.b_batch_stride)
-                                : make_e4m3_map(&mb, base + sp.off_b, sp.k_pad, d.N, sp.bb, BN);
+  const bool ok_b = sp.b_native ? make_fp4_operand_map(&mb, d.b_codes, d.K, d.N, sp.bb, d.b_ld, d.b_batch_stride, BNS)
+                                : make_e4m3_map(&mb, base + sp.off_b, sp.k_pad, d.N, sp.bb, BNS);
   if (!ok_b) {
     *why = MIX_ERR_UNSUPPORTED;
     return cudaSuccess;
   }
   CUtensorMap mc = ma;  // placeholder when there is no fp32 output
-  if (d.c != nullptr && !make_c_map(&mc, d.c, d.M, d.N, d.batch, d.ldc, d.c_batch_stride)) {
+  if (d.c != nullptr && !make_c_map(&mc, d.c, d.M, d.N, d.batch, d.ldc, d.c_batch_stride, 16)) {
     *why = MIX_ERR_UNSUPPORTED;
     return cudaSuccess;
   }
@@ -837,7 +980,8 @@ cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t 
   if (e != cudaSuccess) return e;
   e = launch_expand_b(d, sp, base, st);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)sp.mt, (unsigned)sp.nt, (unsigned)d.batch);
+  const int64_t tiles = d.batch * sp.nt * sp.mt;
+  const dim3 grid((unsigned)(tiles < num_sms() ? tiles : num_sms()));
   return sp.b_native ? launch_staged<true>(ma, mb, mc, p, grid, st) : launch_staged<false>(ma, mb, mc, p, grid, st);
 }
 

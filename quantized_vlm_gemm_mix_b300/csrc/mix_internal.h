@@ -34,8 +34,9 @@ size_t gemm_tc_workspace_bytes(const mix_gemm_desc_t& d);
 // Staged tensor-core matmul: the operands are expanded once per call into the
 // caller's workspace -- e4m3 planes [batch][rows][k_pad] (k_pad = K rounded up
 // to 128, zero padded) and UE8M0 block-scale words grouped per (row tile,
-// 128-deep k-step): 128-row tiles for A (512 bytes), 256-row tiles for B
-// (1024 bytes, two 128-row halves).  Inside a 128-row group, 32-bit word
+// 128-deep k-step): 128-row tiles for A (512 bytes), kStagedBN-row tiles for
+// B stored as 256-row groups (1024 bytes, two 128-row halves, the rows past
+// kStagedBN padding).  Inside a 128-row group, 32-bit word
 // 4 l + i holds the four k-block scales (byte j = k-block 4 kt + j) of row
 // 32 i + l, so one tcgen05.cp of 32 rows x 128 bits puts row 32 i + l at TMEM
 // lane l (of every lane quadrant), column i.  MXFP4 weights that the
@@ -47,6 +48,7 @@ struct StagedPlan {
   size_t off_a, off_sfa, off_b, off_sfb, bytes;  // offsets from the 1024-aligned workspace base
 };
 constexpr int kStagedAlign = 1024;
+constexpr int kStagedBN = 224;  // output columns per tile of the staged matmul
 StagedPlan staged_plan(const mix_gemm_desc_t& d);
 bool staged_fp4_native_ok(const mix_gemm_desc_t& d);
 int64_t expand_a_threads(const mix_gemm_desc_t& d, const StagedPlan& sp);

@@ -54,6 +54,19 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
       : "memory");
   return ok != 0;
 }
+// Bounded spin wait for the single-thread roles on the critical path (TMA
+// producer, MMA issuer): polls without a suspend hint so it resumes the
+// moment the phase completes.  Same limit and abort rules as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, long long limit_cycles,
+                                               volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > limit_cycles) return false;
+  }
+}
 // Bounded wait: returns false once `limit_cycles` SM clocks have passed or
 // another thread of the CTA has raised *abort (a failed wait elsewhere).
 // Waiting threads stay suspended instead of polling, so they do not take

@@ -89,7 +89,7 @@ def _staged_desc(mix, M, N, K, b_type, batch=1, b_group=1, algo=None):
 def test_staged_gemm_workspace_size_and_check(mix):
     """The staged tensor-core path needs batch*M*Kp bytes of e4m3 A, 512 bytes
     of A scale words per (128-row tile, 128-deep k-step), the same for an
-    expanded B (bB*N*Kp bytes, 1024 bytes per 256-row tile and k-step), each
+    expanded B (bB*N*Kp bytes, 1024 bytes per 224-row tile and k-step), each
     part rounded up to 1 KiB, plus 1 KiB of alignment slack; a call without
     that workspace is refused before anything is launched."""
     L = mix.lib
@@ -104,7 +104,7 @@ def test_staged_gemm_workspace_size_and_check(mix):
     # MXFP4 with K % 128 == 0 is read in place: only its scale words are staged
     M, N, K, B, G = 160, 4096, 512, 6, 3
     d = _staged_desc(mix, M, N, K, mix.MX_FP4_E2M1, batch=B, b_group=G)
-    want = kib(B * M * K) + kib(B * 2 * 4 * 512) + kib((B // G) * 16 * 4 * 1024) + 1024
+    want = kib(B * M * K) + kib(B * 2 * 4 * 512) + kib((B // G) * 19 * 4 * 1024) + 1024   # 19 = ceil(4096 / 224)
     assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == want
     # one 256-column tile: the fused-decode variant, no workspace
     d = _staged_desc(mix, 300, 256, 416, mix.MX_INT4)
