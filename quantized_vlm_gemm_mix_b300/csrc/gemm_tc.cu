@@ -115,46 +115,26 @@ __device__ __forceinline__ void flag_error(unsigned bit, volatile int* abort_fla
 }
 
 // ----------------------------------------------------------- fused epilogue
-// Quantise one 32-column block of one output row held by one thread.
-__device__ __forceinline__ void epi_quant_block(const uint32_t* u, const TcParams& p, uint4& codes,
+// Quantise one 32-column block of one output row held by one thread (the
+// bit patterns in u may be overwritten).
+__device__ __forceinline__ void epi_quant_block(uint32_t* u, const TcParams& p, uint4& codes,
                                                 uint32_t& shared) {
+  const bool asym = (p.epi_flags & MIX_ASYM_ZERO) != 0;
+  if (p.epi == MIX_EPI_MIX_T1) {
+    mix_block32<1>(u, p.epi_ebias, asym, codes, shared);
+    return;
+  }
+  if (p.epi == MIX_EPI_MIX_T2) {
+    mix_block32<2>(u, p.epi_ebias, asym, codes, shared);
+    return;
+  }
   uint32_t ks[4];
 #pragma unroll
   for (int s = 0; s < 4; ++s) ks[s] = max_key8(u + 8 * s);
   const uint32_t kb = max(max(ks[0], ks[1]), max(ks[2], ks[3]));
   uint32_t w[4] = {0, 0, 0, 0};
   shared = 0;
-  if (p.epi == MIX_EPI_MIX_T1 || p.epi == MIX_EPI_MIX_T2) {
-    const bool asym = (p.epi_flags & MIX_ASYM_ZERO) != 0;
-    int f, m3;
-    if (!max_exp_mant(kb, &f, &m3)) {
-      w[0] = w[1] = w[2] = w[3] = 0x77777777u;
-    } else {
-      const int emax = clampi(f, p.epi_ebias, p.epi_ebias + 15);
-      uint32_t m3bits = 0;
-      bool all_zero = true;
-      const MixBlk b1 = mix_blk(emax, 8 + m3, asym);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        int ms = m3;
-        if (p.epi == MIX_EPI_MIX_T2) {
-          int fs;
-          if (!max_exp_mant(ks[s], &fs, &ms)) ms = 0;
-          w[s] = mix_codes8(u + 8 * s, mix_blk(emax, 8 + ms, asym));
-        } else {
-          w[s] = mix_codes8(u + 8 * s, b1);
-        }
-        const bool z = w[s] == 0x77777777u;
-        all_zero &= z;
-        if (z) ms = 0;
-        m3bits |= (uint32_t)ms << (4 + 3 * s);
-      }
-      if (!all_zero) {
-        const uint32_t ec = (uint32_t)(emax - p.epi_ebias);
-        shared = (p.epi == MIX_EPI_MIX_T1) ? (ec | ((uint32_t)m3 << 4)) : (ec | m3bits);
-      }
-    }
-  } else {
+  {
     const bool fp4 = p.epi == MIX_EPI_MXFP4;
     if (kb != 0u) {
       const int X = mx_shared_exp(kb, fp4, (p.epi_flags & MX_SCALE_FLOOR) != 0);

@@ -112,23 +112,71 @@ __device__ __forceinline__ uint32_t mix_code_nonan(uint32_t u, uint32_t a, const
   return a < (neg ? b.zn : b.zp) ? 7u : code;
 }
 
-__device__ __forceinline__ uint32_t mix_code(uint32_t u, const MixBlk& b) {
-  const uint32_t a = u & 0x7FFFFFFFu;
-  int d = ((int)(b.t0 - a) + 0x7FFFFF) >> 23;
-  d = max(d, 0);
-  const bool neg = (int)u < 0;
-  const int dd = min(d, neg ? 6 : b.dmaxp);
-  const uint32_t code = (uint32_t)dd | (neg ? 8u : 0u) | ((uint32_t)(dd + 1) & 8u);
-  const uint32_t z = neg ? b.zn : b.zp;
-  return (a < z || a > 0x7F800000u) ? 7u : code;  // zero (or NaN) -> the zero code
-}
-
-// Eight elements -> eight nibbles (element i in bits 4i..4i+3).
-__device__ __forceinline__ uint32_t mix_codes8(const uint32_t* u, const MixBlk& b) {
-  uint32_t w = 0;
+// Algorithm 1 on one 32-element block held as fp32 bit patterns (TYPE 1:
+// MiX-4.25b, one shared mantissa; TYPE 2: MiX-4.5b, one per 8-element
+// sub-block).  NaNs are coded as zero: the rare block holding one has them
+// replaced by +0 first, so the element step never sees a NaN.  Writes the
+// 16 code bytes and the shared field (zero for an all-zero block).
+template <int TYPE>
+__device__ __forceinline__ void mix_block32(uint32_t* u, int ebias, bool asym, uint4& cw, uint32_t& sh) {
+  uint32_t ks[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) w |= mix_code(u[i], b) << (4 * i);
-  return w;
+  for (int s = 0; s < 4; ++s) {
+    uint32_t k = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) k = max(k, u[8 * s + i] & 0x7FFFFFFFu);
+    ks[s] = k;
+  }
+  uint32_t kb = max(max(ks[0], ks[1]), max(ks[2], ks[3]));
+  if (kb > 0x7F800000u) {  // a NaN in the block: code it as zero
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if ((u[i] & 0x7FFFFFFFu) > 0x7F800000u) u[i] = 0u;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      uint32_t k = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) k = max(k, u[8 * s + i] & 0x7FFFFFFFu);
+      ks[s] = k;
+    }
+    kb = max(max(ks[0], ks[1]), max(ks[2], ks[3]));
+  }
+  cw = make_uint4(0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);
+  sh = 0;
+  int f, m3;
+  if (max_exp_mant(kb, &f, &m3)) {
+    const int emax = clampi(f, ebias, ebias + 15);
+    uint32_t w[4];
+    uint32_t m3bits = 0;
+    bool all_zero = true;
+    const MixBlk b1 = mix_blk(emax, 8 + m3, asym);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      int ms = m3;
+      MixBlk bb = b1;
+      if (TYPE == 2) {
+        int fs;
+        if (!max_exp_mant(ks[s], &fs, &ms)) ms = 0;
+        bb = mix_blk(emax, 8 + ms, asym);
+      }
+      uint32_t word = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t v = u[8 * s + i];
+        word |= mix_code_nonan(v, v & 0x7FFFFFFFu, bb) << (4 * i);
+      }
+      w[s] = word;
+      const bool z = word == 0x77777777u;
+      all_zero &= z;
+      if (z) ms = 0;
+      m3bits |= (uint32_t)ms << (4 + 3 * s);
+    }
+    cw = make_uint4(w[0], w[1], w[2], w[3]);
+    if (!all_zero) {
+      const uint32_t ec = (uint32_t)(emax - ebias);
+      sh = TYPE == 1 ? (ec | ((uint32_t)m3 << 4)) : (ec | m3bits);
+    }
+  }
 }
 
 __device__ __forceinline__ uint32_t max_key8(const uint32_t* u) {

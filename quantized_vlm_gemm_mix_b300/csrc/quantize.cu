@@ -99,64 +99,9 @@ __global__ void __launch_bounds__(kThreads, 4) mix_quantize_kernel(
     const int64_t b = g - (int64_t)row * nb;
     uint32_t u[32];
     load32<BF16>(x, (int64_t)row * ld + b * 32, u);
-    uint32_t ks[4];
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-      uint32_t k = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) k = max(k, u[8 * s + i] & 0x7FFFFFFFu);
-      ks[s] = k;
-    }
-    uint32_t kb = max(max(ks[0], ks[1]), max(ks[2], ks[3]));
-    if (kb > 0x7F800000u) {  // a NaN in the block: code it as zero
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if ((u[i] & 0x7FFFFFFFu) > 0x7F800000u) u[i] = 0u;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        uint32_t k = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) k = max(k, u[8 * s + i] & 0x7FFFFFFFu);
-        ks[s] = k;
-      }
-      kb = max(max(ks[0], ks[1]), max(ks[2], ks[3]));
-    }
-    uint4 cw = make_uint4(0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);
-    uint32_t sh = 0;
-    int f, m3;
-    if (max_exp_mant(kb, &f, &m3)) {
-      const int emax = clampi(f, ebias, ebias + 15);
-      uint32_t w[4];
-      uint32_t m3bits = 0;
-      bool all_zero = true;
-      const MixBlk b1 = mix_blk(emax, 8 + m3, asym != 0);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        int ms = m3;
-        MixBlk bb = b1;
-        if (TYPE == 2) {
-          int fs;
-          if (!max_exp_mant(ks[s], &fs, &ms)) ms = 0;
-          bb = mix_blk(emax, 8 + ms, asym != 0);
-        }
-        uint32_t word = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t v = u[8 * s + i];
-          word |= mix_code_nonan(v, v & 0x7FFFFFFFu, bb) << (4 * i);
-        }
-        w[s] = word;
-        const bool z = word == 0x77777777u;
-        all_zero &= z;
-        if (z) ms = 0;
-        m3bits |= (uint32_t)ms << (4 + 3 * s);
-      }
-      cw = make_uint4(w[0], w[1], w[2], w[3]);
-      if (!all_zero) {
-        const uint32_t ec = (uint32_t)(emax - ebias);
-        sh = TYPE == 1 ? (ec | ((uint32_t)m3 << 4)) : (ec | m3bits);
-      }
-    }
+    uint4 cw;
+    uint32_t sh;
+    mix_block32<TYPE>(u, ebias, asym != 0, cw, sh);
     __stcs(reinterpret_cast<uint4*>(codes + g * 16), cw);
     if (TYPE == 1) static_cast<uint8_t*>(shared)[g] = (uint8_t)sh;
     else static_cast<uint16_t*>(shared)[g] = (uint16_t)sh;
