@@ -141,6 +141,20 @@ def step_table(small=False):
     return rows
 
 
+MATMUL_SOURCES = ("gemm_tc.cu", "expand.cu", "decode.cuh", "mix_common.cuh", "tc_ptx.cuh")
+
+
+def matmul_source_sha():
+    """sha256 over the matmul's kernel sources: a recorded DRAM-traffic figure
+    counts only for the kernel it was measured on."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in MATMUL_SOURCES:
+        with open(os.path.join(ROOT, "quantized_vlm_gemm_mix_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def roof_seconds(nbytes, flops):
     return max(nbytes / (HBM * 1e9), flops / (MX8_TFLOPS * 1e12) if flops else 0.0)
 
@@ -601,7 +615,7 @@ def main():
     tp = os.path.join(ROOT, "profiles", "dominant_kernel_traffic.json")
     if os.path.exists(tp) and not args.small:
         tj = json.load(open(tp))
-        if tj.get("call") == dc.name and tj.get("kernel_version") == mix.mix_version():
+        if tj.get("call") == dc.name and tj.get("source_sha256") == matmul_source_sha():
             traffic = tj.get("dram_bytes_per_launch")
     roofline = {"bound": "tensor", "kernel": dc.name, "achieved": round(ach, 1), "peak": round(MX8_TFLOPS, 1),
                 "unit": "TFLOP/s", "frac": round(ach / MX8_TFLOPS, 4), "traffic": traffic,
