@@ -169,7 +169,9 @@ MIX_API mix_status_t mx_dequantize(const uint8_t* codes, const uint8_t* scales, 
  *    the scale words and alignment; mix_mx_gemm_workspace_bytes gives the
  *    exact size and a smaller workspace returns MIX_ERR_WORKSPACE.
  *  - fused decode (MIX_GEMM_TCGEN05_FUSED; chosen when N <= 256): decoder
- *    warps expand each tile inside the matmul.  No workspace.
+ *    warps expand each A tile inside the matmul; B enters by TMA, MXFP4 in
+ *    place (no workspace) or else expanded once into e4m3 in the workspace
+ *    (bB*N*Kp bytes plus its scale words and alignment).
  */
 typedef enum { MIX_EPI_NONE = 0, MIX_EPI_MIX_T1 = 1, MIX_EPI_MIX_T2 = 2,
                MIX_EPI_MXINT4 = 3, MIX_EPI_MXFP4 = 4 } mix_epilogue_t;

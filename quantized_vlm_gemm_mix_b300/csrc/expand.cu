@@ -191,6 +191,19 @@ StagedPlan staged_plan(const mix_gemm_desc_t& d) {
   return sp;
 }
 
+StagedPlan staged_plan_b_only(const mix_gemm_desc_t& d) {
+  StagedPlan sp = staged_plan(d);
+  sp.b_native = false;
+  size_t off = 0;
+  sp.off_a = sp.off_sfa = 0;
+  sp.off_b = off;
+  off = align_up(off + (size_t)sp.bb * d.N * sp.k_pad);
+  sp.off_sfb = off;
+  off = align_up(off + (size_t)sp.bb * sp.nt * sp.kt * 1024);
+  sp.bytes = off;
+  return sp;
+}
+
 // Thread counts of the two passes; the staged path is taken only when both
 // index spaces fit 32 bits.
 int64_t expand_a_threads(const mix_gemm_desc_t& d, const StagedPlan& sp) { return d.batch * sp.mt * 128 * (sp.k_pad / 32); }

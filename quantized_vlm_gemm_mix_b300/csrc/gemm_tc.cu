@@ -55,7 +55,7 @@ namespace {
 constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int KB = BK / 2;  // code bytes per row per stage
 constexpr int S_CODES = 3;
-constexpr int A_CODES = BM * KB, B_CODES = BN * KB;  // 8 KB, 16 KB
+constexpr int A_CODES = BM * KB;                     // 8 KB
 constexpr int A_OPS = BM * BK, B_OPS = BN * BK;      // 16 KB, 32 KB (also the padded E2M1 tile)
 constexpr int DEC_WARP0 = 4, NUM_DEC_WARPS = 16;
 constexpr int NUM_THREADS = (DEC_WARP0 + NUM_DEC_WARPS) * 32;
@@ -63,18 +63,16 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL = 256;  // stage s: A scales at SF_COL + 16 s (4 cols), B at + 4 (8 cols)
 constexpr long long WAIT_LIMIT = 1LL << 31;  // SM clocks, about one second
 
-// Shared memory plan (offsets from a 1024-byte aligned base).  B_NATIVE: the
-// MXFP4 weight tile goes straight from HBM into the MMA operand buffer (TMA
-// unpacks 16 x E2M1 into 16-byte slots), so there is no B code ring and the
-// operand ring is one stage deeper.
-template <bool B_NATIVE>
+// Shared memory plan of the fused-decode kernel (offsets from a 1024-byte
+// aligned base).  The B tile goes straight into the MMA operand buffer by TMA:
+// MXFP4 weights through the unpacking load (16 x E2M1 into 16-byte slots),
+// anything else from its e4m3 expansion in the workspace.
 struct Plan {
-  static constexpr int S_OPS = B_NATIVE ? 4 : 3;
+  static constexpr int S_OPS = 4;
   static constexpr int OFF_AOPS = 0;
   static constexpr int OFF_BOPS = OFF_AOPS + S_OPS * A_OPS;
   static constexpr int OFF_ACODES = OFF_BOPS + S_OPS * B_OPS;
-  static constexpr int OFF_BCODES = OFF_ACODES + S_CODES * A_CODES;
-  static constexpr int OFF_SFA = OFF_BCODES + (B_NATIVE ? 0 : S_CODES * B_CODES);  // [S_OPS][BM] words
+  static constexpr int OFF_SFA = OFF_ACODES + S_CODES * A_CODES;  // [S_OPS][BM] words
   static constexpr int OFF_SFB = OFF_SFA + S_OPS * BM * 4;                           // [S_OPS][BN] words
   static constexpr int OFF_TAB = OFF_SFB + S_OPS * BN * 4;  // 8 decode tables (one per mshared), 16 B each
   static constexpr int OFF_BAR = OFF_TAB + 8 * 16;
@@ -88,6 +86,7 @@ struct TcParams {
   const void* a_shared;
   int64_t a_ld, a_bs;
   int a_type, a_ebias, b_fp4;
+  uint32_t b_tma_fmt, b_tma_bytes;  // fused-decode kernel: B operand format (E2M1 5 / E4M3 0) and TMA bytes
   const uint8_t* b_scales;
   int64_t b_ld, b_bs;
   float* c;
@@ -199,11 +198,10 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
   if (staged && lane == 0) ptx::bulk_wait_read0();  // staging read before the CTA exits
 }
 
-template <bool B_NATIVE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const TcParams p) {
-  using L = Plan<B_NATIVE>;
+  using L = Plan;
   constexpr int S_OPS = L::S_OPS;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -269,21 +267,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         if (*abort_flag) break;
-        ptx::mbar_arrive_expect_tx(&codes_full[s], B_NATIVE ? A_CODES : A_CODES + B_CODES);
+        ptx::mbar_arrive_expect_tx(&codes_full[s], A_CODES);
         ptx::tma_load_3d(smem + L::OFF_ACODES + s * A_CODES, &tmap_a, &codes_full[s], kt * KB, (int)m0, (int)bt);
-        if (!B_NATIVE)
-          ptx::tma_load_3d(smem + L::OFF_BCODES + s * B_CODES, &tmap_b, &codes_full[s], kt * KB, (int)n0,
-                           (int)(bt / p.b_group));
         ++issued;
-        if (B_NATIVE) {
+        {
           const int os = kt % S_OPS, on = kt / S_OPS;
           if (on > 0 && !ptx::mbar_wait(&ops_empty[os], (on - 1) & 1, WAIT_LIMIT, abort_flag)) {
             flag_error(64u, abort_flag);
             break;
           }
           if (*abort_flag) break;
-          // the transaction count of the unpacking load is the packed size
-          ptx::mbar_arrive_expect_tx(&b_full[os], B_OPS / 2);
+          // the transaction count of the unpacking E2M1 load is the packed size
+          ptx::mbar_arrive_expect_tx(&b_full[os], p.b_tma_bytes);
           ptx::tma_load_3d(smem + L::OFF_BOPS + os * B_OPS, &tmap_b, &b_full[os], kt * BK, (int)n0,
                            (int)(bt / p.b_group));
           ++issued_b;
@@ -298,11 +293,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      const uint32_t b_fmt = B_NATIVE ? 5u : 0u;  // E2M1 or E4M3
+      const uint32_t b_fmt = p.b_tma_fmt;  // E2M1 or E4M3
       for (int kt = 0; kt < num_k; ++kt) {
         const int s = kt % S_OPS, n = kt / S_OPS;
         if (!ptx::mbar_wait(&ops_full[s], n & 1, WAIT_LIMIT, abort_flag)) { flag_error(2u, abort_flag); break; }
-        if (B_NATIVE && !ptx::mbar_wait(&b_full[s], n & 1, WAIT_LIMIT, abort_flag)) {
+        if (!ptx::mbar_wait(&b_full[s], n & 1, WAIT_LIMIT, abort_flag)) {
           flag_error(128u, abort_flag);
           break;
         }
@@ -327,8 +322,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int dt = threadIdx.x - DEC_WARP0 * 32;  // 0 .. 511
     const int arow = dt >> 2, ablk = dt & 3;       // A: one 32-block per thread per k-step
     const int64_t am = m0 + arow;
-    const int brow = dt >> 1, bhalf = dt & 1;      // B decode: 64 elements per thread
-    const DecTab btab = p.b_fp4 ? fp4_tab() : int4_tab();
     const unsigned char* tabs = smem + L::OFF_TAB;
     // Per-thread pointers and ranges, hoisted: the shared field of this
     // thread's block at k-step kt is at [4 kt], valid while kt < a_kend.
@@ -415,18 +408,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           *reinterpret_cast<uint4*>(dst + sw128_off(arow, c0 + 1)) = make_uint4(e[2].x, e[2].y, e[3].x, e[3].y);
         }
       }
-      // --- B (decoded mode): 64 elements (4 chunks) of row brow
-      if (!B_NATIVE) {
-        const unsigned char* src = smem + L::OFF_BCODES + cs * B_CODES + brow * KB + bhalf * 32;
-        unsigned char* dst = smem + L::OFF_BOPS + os * B_OPS;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint4 cv = *reinterpret_cast<const uint4*>(src + 16 * c);
-          const uint2 e0 = dec8(cv.x, btab), e1 = dec8(cv.y, btab), e2 = dec8(cv.z, btab), e3 = dec8(cv.w, btab);
-          *reinterpret_cast<uint4*>(dst + sw128_off(brow, bhalf * 4 + 2 * c)) = make_uint4(e0.x, e0.y, e1.x, e1.y);
-          *reinterpret_cast<uint4*>(dst + sw128_off(brow, bhalf * 4 + 2 * c + 1)) = make_uint4(e2.x, e2.y, e3.x, e3.y);
-        }
-      }
       __syncwarp();
       if (lane == 0) {
         ptx::mbar_arrive(&codes_empty[cs]);
@@ -448,7 +429,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&ops_full[os]);
     }
-    (void)btab; (void)brow; (void)bhalf;
     // --------------------------------------------------------- epilogue
     // All sixteen decoder warps: warp w reads TMEM lane quadrant w % 4 (the
     // only one it may access) and a quarter of the tile's columns.
@@ -855,19 +835,18 @@ cudaError_t launch_staged(const CUtensorMap& ma, const CUtensorMap& mb, const CU
   return e;
 }
 
-template <bool B_NATIVE>
 cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const TcParams& p,
                       dim3 grid, cudaStream_t st) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<B_NATIVE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Plan<B_NATIVE>::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Plan::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  gemm_tc_kernel<B_NATIVE><<<grid, NUM_THREADS, Plan<B_NATIVE>::SMEM_BYTES, st>>>(ma, mb, mc, p);
+  gemm_tc_kernel<<<grid, NUM_THREADS, Plan::SMEM_BYTES, st>>>(ma, mb, mc, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess && std::getenv("MIX_DEBUG") != nullptr)
     std::fprintf(stderr, "gemm_tc launch: %s\n", cudaGetErrorString(e));
@@ -906,31 +885,51 @@ bool want_staged(const mix_gemm_desc_t& d) {
   return d.N > BN;
 }
 
-cudaError_t launch_fused(const mix_gemm_desc_t& d, cudaStream_t st, mix_status_t* why) {
+// The fused-decode path: MXFP4 weights that the unpacking TMA reads in place
+// need no workspace; any other B is expanded once into e4m3 in the workspace.
+bool fused_b_native(const mix_gemm_desc_t& d) { return staged_fp4_native_ok(d); }
+
+cudaError_t launch_fused(const mix_gemm_desc_t& d, void* ws, cudaStream_t st, mix_status_t* why) {
   const int64_t bb = (d.batch + d.b_group - 1) / d.b_group;
   CUtensorMap ma, mb;
   if (!make_code_map(&ma, d.a_codes, d.K, d.M, d.batch, d.a_ld, d.a_batch_stride, BM)) {
     *why = MIX_ERR_UNSUPPORTED;
     return cudaSuccess;
   }
-  // MXFP4 weights feed the MMA directly when the plane meets the unpacking
-  // TMA's rules; otherwise (and for MXINT4) the decoders convert them.
-  const bool native = d.b_type == MX_FP4_E2M1 &&
-                      make_fp4_operand_map(&mb, d.b_codes, d.K, d.N, bb, d.b_ld, d.b_batch_stride);
-  if (!native && !make_code_map(&mb, d.b_codes, d.K, d.N, bb, d.b_ld, d.b_batch_stride, BN)) {
-    *why = MIX_ERR_UNSUPPORTED;
-    return cudaSuccess;
+  TcParams p = make_params(d);
+  const bool native = fused_b_native(d);
+  StagedPlan sp{};
+  unsigned char* base = nullptr;
+  if (native) {
+    if (!make_fp4_operand_map(&mb, d.b_codes, d.K, d.N, bb, d.b_ld, d.b_batch_stride)) {
+      *why = MIX_ERR_UNSUPPORTED;
+      return cudaSuccess;
+    }
+    p.b_tma_fmt = 5u;
+    p.b_tma_bytes = B_OPS / 2;
+  } else {
+    sp = staged_plan_b_only(d);
+    base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(ws) + kStagedAlign - 1) &
+                                            ~static_cast<uintptr_t>(kStagedAlign - 1));
+    if (!make_e4m3_map(&mb, base + sp.off_b, sp.k_pad, d.N, sp.bb, BN)) {
+      *why = MIX_ERR_UNSUPPORTED;
+      return cudaSuccess;
+    }
+    p.b_tma_fmt = 0u;
+    p.b_tma_bytes = B_OPS;
   }
-  const TcParams p = make_params(d);
   CUtensorMap mc = ma;  // placeholder when there is no fp32 output
   if (d.c != nullptr && !make_c_map(&mc, d.c, d.M, d.N, d.batch, d.ldc, d.c_batch_stride)) {
     *why = MIX_ERR_UNSUPPORTED;
     return cudaSuccess;
   }
+  if (!native) {
+    const cudaError_t e = launch_expand_b(d, sp, base, st);
+    if (e != cudaSuccess) return e;
+  }
   const dim3 grid((unsigned)((d.M + BM - 1) / BM), (unsigned)((d.N + BN - 1) / BN), (unsigned)d.batch);
-  return native ? launch_tc<true>(ma, mb, mc, p, grid, st) : launch_tc<false>(ma, mb, mc, p, grid, st);
+  return launch_tc(ma, mb, mc, p, grid, st);
 }
-
 
 cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t st, mix_status_t* why) {
   const StagedPlan sp = staged_plan(d);
@@ -968,8 +967,10 @@ cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t 
 }  // namespace
 
 size_t gemm_tc_workspace_bytes(const mix_gemm_desc_t& d) {
-  if (!shape_ok(d) || !want_staged(d)) return 0;
-  return staged_plan(d).bytes + kStagedAlign;
+  if (!shape_ok(d)) return 0;
+  if (want_staged(d)) return staged_plan(d).bytes + kStagedAlign;
+  if (fused_b_native(d)) return 0;
+  return staged_plan_b_only(d).bytes + kStagedAlign;
 }
 
 cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, void* ws, size_t ws_bytes, cudaStream_t st,
@@ -979,14 +980,12 @@ cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, void* ws, size_t ws_bytes, 
     *why = MIX_ERR_UNSUPPORTED;
     return cudaSuccess;
   }
-  if (want_staged(d)) {
-    if (ws == nullptr || ws_bytes < gemm_tc_workspace_bytes(d)) {
-      *why = MIX_ERR_WORKSPACE;
-      return cudaSuccess;
-    }
-    return launch_staged_path(d, ws, st, why);
+  if (ws_bytes < gemm_tc_workspace_bytes(d) || (ws == nullptr && gemm_tc_workspace_bytes(d) > 0)) {
+    *why = MIX_ERR_WORKSPACE;
+    return cudaSuccess;
   }
-  return launch_fused(d, st, why);
+  if (want_staged(d)) return launch_staged_path(d, ws, st, why);
+  return launch_fused(d, ws, st, why);
 }
 
 }  // namespace mixk

@@ -50,6 +50,7 @@ struct StagedPlan {
 constexpr int kStagedAlign = 1024;
 constexpr int kStagedBN = 224;  // output columns per tile of the staged matmul
 StagedPlan staged_plan(const mix_gemm_desc_t& d);
+StagedPlan staged_plan_b_only(const mix_gemm_desc_t& d);  // B expansion alone (fused-decode path)
 bool staged_fp4_native_ok(const mix_gemm_desc_t& d);
 int64_t expand_a_threads(const mix_gemm_desc_t& d, const StagedPlan& sp);
 int64_t expand_b_threads(const StagedPlan& sp);

@@ -106,10 +106,13 @@ def test_staged_gemm_workspace_size_and_check(mix):
     d = _staged_desc(mix, M, N, K, mix.MX_FP4_E2M1, batch=B, b_group=G)
     want = kib(B * M * K) + kib(B * 2 * 4 * 512) + kib((B // G) * 19 * 4 * 1024) + 1024   # 19 = ceil(4096 / 224)
     assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == want
-    # one 256-column tile: the fused-decode variant, no workspace
+    # one 256-column tile: the fused-decode variant; it stages only B, and
+    # MXFP4 read in place needs no workspace at all
     d = _staged_desc(mix, 300, 256, 416, mix.MX_INT4)
-    assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == 0
+    assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == kib(256 * 512) + kib(2 * 4 * 1024) + 1024
     d = _staged_desc(mix, 300, 520, 416, mix.MX_INT4, algo=mix.MIX_GEMM_TCGEN05_FUSED)
+    assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == kib(520 * 512) + kib(3 * 4 * 1024) + 1024
+    d = _staged_desc(mix, 300, 256, 512, mix.MX_FP4_E2M1)
     assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == 0
     d = _staged_desc(mix, 300, 256, 416, mix.MX_INT4, algo=mix.MIX_GEMM_TCGEN05_STAGED)
     assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) > 0
