@@ -5,9 +5,12 @@
 //
 // COMPUTE: the tokens are split into chunks across CTAs (the whole tensor has
 // to be in flight to reach HBM bandwidth); each CTA sums its chunk per
-// channel in fp64 and writes one fp64 partial row to the caller's workspace.
-// A second kernel adds the partial rows in chunk order and divides by the
-// token count, so the result does not depend on scheduling.  APPLY (both
+// channel and writes one fp64 partial row to the caller's workspace.  A
+// thread's own run of tokens is summed in double-float (an fp32 pair kept
+// exact by Knuth's two-sum, ~48-bit precision) because fp64 arithmetic is
+// slow on this part; the cross-warp and cross-chunk sums are fp64.  A second
+// kernel adds the partial rows in a fixed order and divides by the token
+// count, so the result does not depend on scheduling.  APPLY (both
 // modes): k_out = fp32(k) - mean, one fp32 subtraction per element.
 #include <cuda_runtime.h>
 
@@ -45,17 +48,24 @@ __global__ void __launch_bounds__(kThreads) ksmooth_partial_kernel(
   const int64_t c = (int64_t)blockIdx.x * 256 + lane * 8;
   const int64_t t0 = (int64_t)blockIdx.y * chunk;
   const int64_t t1 = min(tokens, t0 + chunk);
-  double s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float hi[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lo[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (c < C) {
     for (int64_t t = t0 + warp; t < t1; t += 8) {
       float v[8];
       load8f(k, bf16 != 0, t * ld + c, v);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s[i] += (double)v[i];
+      for (int i = 0; i < 8; ++i) {
+        // two-sum: hi + v = s + e exactly
+        const float sum = __fadd_rn(hi[i], v[i]);
+        const float bv = __fsub_rn(sum, hi[i]);
+        const float e = __fadd_rn(__fsub_rn(hi[i], __fsub_rn(sum, bv)), __fsub_rn(v[i], bv));
+        hi[i] = sum;
+        lo[i] = __fadd_rn(lo[i], e);
+      }
     }
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) red[warp][lane * 8 + i] = s[i];
+  for (int i = 0; i < 8; ++i) red[warp][lane * 8 + i] = (double)hi[i] + (double)lo[i];
   __syncthreads();
   const int64_t cc = (int64_t)blockIdx.x * 256 + threadIdx.x;
   if (cc < C) {
@@ -66,12 +76,22 @@ __global__ void __launch_bounds__(kThreads) ksmooth_partial_kernel(
   }
 }
 
+// One thread per channel adds the chunk partials in a fixed order: four
+// interleaved chains (chunk j goes to chain j % 4), then (c0 + c1) + (c2 + c3).
+// The unrolled loop keeps sixteen loads in flight instead of one.
 __global__ void ksmooth_finalize_kernel(const double* __restrict__ partial, int64_t nchunks, int64_t C,
                                         int64_t tokens, float* __restrict__ mean) {
   const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= C) return;
-  double acc = 0.0;
-  for (int64_t j = 0; j < nchunks; ++j) acc += partial[j * C + c];
+  double a[4] = {0.0, 0.0, 0.0, 0.0};
+  int64_t j = 0;
+#pragma unroll 4
+  for (; j + 4 <= nchunks; j += 4) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] += __ldg(partial + (j + i) * C + c);
+  }
+  for (int i = 0; j < nchunks; ++j, ++i) a[i] += __ldg(partial + j * C + c);
+  const double acc = (a[0] + a[1]) + (a[2] + a[3]);
   mean[c] = (float)(acc / (double)tokens);
 }
 
@@ -98,6 +118,7 @@ int64_t ksmooth_chunks(int64_t tokens, int64_t C) {
   int64_t want = (4 * (int64_t)num_sms() + tiles - 1) / tiles;  // about four CTAs per SM
   const int64_t by_len = (tokens + 31) / 32;                    // at least 32 tokens per chunk
   if (want > by_len) want = by_len;
+  if (want > 32) want = 32;  // keeps the fp64 chain of the finalize short
   return want > 0 ? want : 1;
 }
 
