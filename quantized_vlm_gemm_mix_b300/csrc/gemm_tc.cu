@@ -127,22 +127,8 @@ __device__ __forceinline__ void epi_quant_block(uint32_t* u, const TcParams& p, 
     mix_block32<2>(u, p.epi_ebias, asym, codes, shared);
     return;
   }
-  uint32_t ks[4];
-#pragma unroll
-  for (int s = 0; s < 4; ++s) ks[s] = max_key8(u + 8 * s);
-  const uint32_t kb = max(max(ks[0], ks[1]), max(ks[2], ks[3]));
-  uint32_t w[4] = {0, 0, 0, 0};
-  shared = 0;
-  {
-    const bool fp4 = p.epi == MIX_EPI_MXFP4;
-    if (kb != 0u) {
-      const int X = mx_shared_exp(kb, fp4, (p.epi_flags & MX_SCALE_FLOOR) != 0);
-#pragma unroll
-      for (int s = 0; s < 4; ++s) w[s] = mx_codes8(u + 8 * s, X, fp4);
-      shared = (uint32_t)(X + 127);
-    }
-  }
-  codes = make_uint4(w[0], w[1], w[2], w[3]);
+  if (p.epi == MIX_EPI_MXFP4) mx_block32<true>(u, (p.epi_flags & MX_SCALE_FLOOR) != 0, codes, shared);
+  else mx_block32<false>(u, (p.epi_flags & MX_SCALE_FLOOR) != 0, codes, shared);
 }
 
 // Epilogue of one 128 x 256 tile by sixteen warps (DEC_WARP0 ..): warp w

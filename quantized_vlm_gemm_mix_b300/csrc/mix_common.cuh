@@ -48,13 +48,6 @@ __device__ __forceinline__ Elem split_f32(uint32_t u) {
   return e;
 }
 
-// Magnitude key of an fp32 bit pattern for block maxima: NaN maps to 0, so a
-// NaN is never a maximum; +-Inf is the largest key.
-__device__ __forceinline__ uint32_t mag_key(uint32_t u) {
-  uint32_t a = u & 0x7FFFFFFFu;
-  return a > 0x7F800000u ? 0u : a;
-}
-
 __device__ __forceinline__ uint32_t bf16_to_f32_bits(uint32_t h) { return h << 16; }
 
 // Algorithm 1, first two steps, on the maximum magnitude (key != 0): its
@@ -179,13 +172,6 @@ __device__ __forceinline__ void mix_block32(uint32_t* u, int ebias, bool asym, u
   }
 }
 
-__device__ __forceinline__ uint32_t max_key8(const uint32_t* u) {
-  uint32_t k = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) k = max(k, mag_key(u[i]));
-  return k;
-}
-
 // Division by a runtime constant d (1 <= d < 2^31) of 32-bit numerators with
 // a multiply-high and a shift (Granlund and Montgomery, "Division by invariant
 // integers using multiplication", 1994): m = floor(2^32 (2^l - d) / d) + 1
@@ -228,11 +214,6 @@ __device__ __forceinline__ int mx_shared_exp(uint32_t key, bool fp4, bool floor_
 // 2^k as an fp32 factor, k in [-126, 127].
 __device__ __forceinline__ float pow2f(int k) { return __int_as_float((uint32_t)(k + 127) << 23); }
 
-// NaN -> +0 (NaN is coded as zero); everything else unchanged.
-__device__ __forceinline__ float clean_f(uint32_t u) {
-  return __uint_as_float(((u & 0x7FFFFFFFu) > 0x7F800000u) ? 0u : u);
-}
-
 // Two elements -> one byte of E2M1 codes (first element in the low nibble):
 // x / 2^X rounded to nearest-even on the E2M1 grid with saturation at 6 is the
 // hardware conversion cvt.rn.satfinite.e2m1x2.f32.
@@ -248,7 +229,8 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
 // MXFP4: E2M1 codes of x / 2^X, -0 written as +0.  MXINT4: q = round-half-even
 // of x / 2^(X-2) (an fp32 add of 1.5 * 2^23 rounds to an integer exactly),
 // clamped to [-7, 7], two's complement.  The 2^-X factor is applied as two
-// exact power-of-two multiplies so that it never overflows.
+// exact power-of-two multiplies so that it never overflows.  The elements
+// hold no NaN (mx_block32 / the callers replace NaNs by +0 first).
 __device__ __forceinline__ uint32_t mx_codes8(const uint32_t* u, int X, bool fp4) {
   const int k = fp4 ? -X : 2 - X;
   const int k1 = k / 2, k2 = k - k1;
@@ -257,7 +239,7 @@ __device__ __forceinline__ uint32_t mx_codes8(const uint32_t* u, int X, bool fp4
   if (fp4) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      w |= e2m1x2(clean_f(u[2 * i]) * s1 * s2, clean_f(u[2 * i + 1]) * s1 * s2) << (8 * i);
+      w |= e2m1x2(__uint_as_float(u[2 * i]) * s1 * s2, __uint_as_float(u[2 * i + 1]) * s1 * s2) << (8 * i);
     // -0 (nibble 0x8) -> +0
     const uint32_t t = w ^ 0x88888888u;
     const uint32_t nz = (t | (t >> 1) | (t >> 2) | (t >> 3)) & 0x11111111u;
@@ -265,13 +247,50 @@ __device__ __forceinline__ uint32_t mx_codes8(const uint32_t* u, int X, bool fp4
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float y = clean_f(u[i]) * s1 * s2;
+      const float y = __uint_as_float(u[i]) * s1 * s2;
       int q = __float_as_int(y + 12582912.0f) - 0x4B400000;
       q = clampi(q, -7, 7);
       w |= ((uint32_t)q & 0xFu) << (4 * i);
     }
   }
   return w;
+}
+
+// Largest |x| bit pattern of n elements (NaN patterns are larger than Inf's).
+template <int N>
+__device__ __forceinline__ uint32_t max_abs_bits(const uint32_t* u) {
+  uint32_t k = 0;
+#pragma unroll
+  for (int i = 0; i < N; ++i) k = max(k, u[i] & 0x7FFFFFFFu);
+  return k;
+}
+
+// NaN -> +0 in place (NaN is coded as zero and is never a block maximum).
+template <int N>
+__device__ __forceinline__ void zero_nans(uint32_t* u) {
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    if ((u[i] & 0x7FFFFFFFu) > 0x7F800000u) u[i] = 0u;
+}
+
+// One MX block of 32 elements (in place: NaNs become +0): the shared
+// exponent X, the 16 code bytes and the E8M0 scale byte X + 127 (zero codes
+// and scale for an all-zero block).
+template <bool FP4>
+__device__ __forceinline__ void mx_block32(uint32_t* u, bool floor_rule, uint4& w, uint32_t& sc) {
+  uint32_t kb = max_abs_bits<32>(u);
+  if (kb > 0x7F800000u) {
+    zero_nans<32>(u);
+    kb = max_abs_bits<32>(u);
+  }
+  w = make_uint4(0, 0, 0, 0);
+  sc = 0;
+  if (kb != 0u) {
+    const int X = mx_shared_exp(kb, FP4, floor_rule);
+    w = make_uint4(mx_codes8(u, X, FP4), mx_codes8(u + 8, X, FP4), mx_codes8(u + 16, X, FP4),
+                   mx_codes8(u + 24, X, FP4));
+    sc = (uint32_t)(X + 127);
+  }
 }
 
 }  // namespace mixk

@@ -133,7 +133,11 @@ __global__ void __launch_bounds__(kThreads, 4) mx_quantize_rows_kernel(
     }
 #pragma unroll
     for (int r = 0; r < kUnroll; ++r) {
-      const uint32_t kb = quad_max(max_key8(u[r]));
+      uint32_t kb = quad_max(max_abs_bits<8>(u[r]));
+      if (__any_sync(0xFFFFFFFFu, kb > 0x7F800000u)) {  // a NaN in some block of the warp
+        zero_nans<8>(u[r]);
+        kb = quad_max(max_abs_bits<8>(u[r]));
+      }
       uint32_t word = 0u, sc = 0u;
       if (kb != 0u) {
         const int X = mx_shared_exp(kb, FP4, floor_rule != 0);
@@ -192,20 +196,10 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_cols_kernel(
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
     if (c == 1 && !two) break;
-    const uint32_t* u = c ? u1 : u0;
-    uint32_t key = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) key = max(key, mag_key(u[i]));
-    uint4 w = make_uint4(0, 0, 0, 0);
-    uint32_t sc = 0;
-    if (key != 0u) {
-      const int X = mx_shared_exp(key, FP4, floor_rule != 0);
-      w.x = mx_codes8(u, X, FP4);
-      w.y = mx_codes8(u + 8, X, FP4);
-      w.z = mx_codes8(u + 16, X, FP4);
-      w.w = mx_codes8(u + 24, X, FP4);
-      sc = (uint32_t)(X + 127);
-    }
+    uint32_t* u = c ? u1 : u0;
+    uint4 w;
+    uint32_t sc;
+    mx_block32<FP4>(u, floor_rule != 0, w, sc);
     const int64_t col = n0 + c;
     *reinterpret_cast<uint4*>(codes + col * (kdim / 2) + kb * 16) = w;
     scales[col * nbk + kb] = (uint8_t)sc;
