@@ -172,6 +172,120 @@ __device__ __forceinline__ void mix_block32(uint32_t* u, int ebias, bool asym, u
   }
 }
 
+// ---------------------------------------------------------------------------
+// Packed element step for bf16 inputs: two elements per 32-bit word (element
+// 2j in the low half of word j), one integer operation for both.  Exact
+// because every threshold of the element step (t0, zn, zp above) has zero low
+// 16 bits, so comparing the bf16 bits (the top half of the fp32 pattern) gives
+// the same decisions:
+//   d   = ceil((t0 - |x|) / 2^23) = floor((T - a + 127) / 128), T = t0 >> 16,
+//         a = the bf16 magnitude; computed per 16-bit lane as
+//         ((0x807F + T - a) >> 7) - 256, the 0x8000 guard keeping every lane
+//         non-negative so no borrow crosses lanes,
+//   clamp to [0, 6] (negative) or [0, dmaxp] (positive) with max/min.u16x2,
+//   code = d | sign << 3 | ((d + 1) & 8), and the zero code 7 where a < z,
+//         the lane compare read from bit 15 of (a | 0x8000) - z.
+__device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t vmin_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+struct MixBlk2 {
+  uint32_t c1;   // (0x807F + T) in both lanes
+  uint32_t zp2;  // ZP in both lanes (ZN = ZP + 128 with the recycled -0, else ZP)
+  bool asym;
+};
+
+__device__ __forceinline__ MixBlk2 mix_blk2(const MixBlk& b, bool asym) {
+  MixBlk2 q;
+  q.c1 = (0x807Fu + (b.t0 >> 16)) * 0x00010001u;
+  q.zp2 = (b.zp >> 16) * 0x00010001u;
+  q.asym = asym;
+  return q;
+}
+
+// Codes of the two elements of word w (its magnitudes a = w & 0x7FFF7FFF),
+// as one byte: the low element's code in the low nibble.
+__device__ __forceinline__ uint32_t mix_code_pair(uint32_t w, uint32_t a, const MixBlk2& q) {
+  uint32_t v = ((q.c1 - a) >> 7) & 0x01FF01FFu;
+  v = vmax_u16x2(v, 0x01000100u);
+  const uint32_t neg01 = (w >> 15) & 0x00010001u;
+  v = vmin_u16x2(v, q.asym ? 0x01070107u - neg01 : 0x01060106u);
+  uint32_t code = (v & 0x00070007u) | ((v + 0x00010001u) & 0x00080008u) | (neg01 << 3);
+  const uint32_t z2 = q.zp2 + (q.asym ? (neg01 << 7) : 0u);
+  const uint32_t ge = (((a | 0x80008000u) - z2) >> 15) & 0x00010001u;
+  const uint32_t m = ge * 0xFu;
+  code = (code & m) | (0x00070007u & ~m);
+  return (code & 0xFu) | ((code >> 12) & 0xF0u);
+}
+
+// Algorithm 1 on one block of 32 bf16 elements held as 16 packed words;
+// same results as mix_block32 on the widened elements (a block holding a NaN
+// goes through mix_block32, which codes NaN as zero).
+template <int TYPE>
+__device__ __forceinline__ void mix_block32_bf16(const uint32_t* w, int ebias, bool asym, uint4& cw, uint32_t& sh) {
+  uint32_t a[16], ks[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      a[4 * s + j] = w[4 * s + j] & 0x7FFF7FFFu;
+      m = vmax_u16x2(m, a[4 * s + j]);
+    }
+    ks[s] = max(m >> 16, m & 0xFFFFu) << 16;
+  }
+  const uint32_t kb = max(max(ks[0], ks[1]), max(ks[2], ks[3]));
+  if (kb > 0x7F800000u) {  // a NaN in the block
+    uint32_t u[32];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      u[2 * j] = w[j] << 16;
+      u[2 * j + 1] = w[j] & 0xFFFF0000u;
+    }
+    mix_block32<TYPE>(u, ebias, asym, cw, sh);
+    return;
+  }
+  cw = make_uint4(0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);
+  sh = 0;
+  int f, m3;
+  if (!max_exp_mant(kb, &f, &m3)) return;
+  const int emax = clampi(f, ebias, ebias + 15);
+  uint32_t wd[4];
+  uint32_t m3bits = 0;
+  bool all_zero = true;
+  const MixBlk2 q1 = mix_blk2(mix_blk(emax, 8 + m3, asym), asym);
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    int ms = m3;
+    MixBlk2 q = q1;
+    if (TYPE == 2) {
+      int fs;
+      if (!max_exp_mant(ks[s], &fs, &ms)) ms = 0;
+      q = mix_blk2(mix_blk(emax, 8 + ms, asym), asym);
+    }
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) word |= mix_code_pair(w[4 * s + j], a[4 * s + j], q) << (8 * j);
+    wd[s] = word;
+    const bool z = word == 0x77777777u;
+    all_zero &= z;
+    if (z) ms = 0;
+    m3bits |= (uint32_t)ms << (4 + 3 * s);
+  }
+  cw = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+  if (!all_zero) {
+    const uint32_t ec = (uint32_t)(emax - ebias);
+    sh = TYPE == 1 ? (ec | ((uint32_t)m3 << 4)) : (ec | m3bits);
+  }
+}
+
 // Division by a runtime constant d (1 <= d < 2^31) of 32-bit numerators with
 // a multiply-high and a shift (Granlund and Montgomery, "Division by invariant
 // integers using multiplication", 1994): m = floor(2^32 (2^l - d) / d) + 1

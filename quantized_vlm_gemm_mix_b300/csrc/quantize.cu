@@ -97,11 +97,22 @@ __global__ void __launch_bounds__(kThreads, 4) mix_quantize_kernel(
   for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < total; g += (int64_t)gridDim.x * kThreads) {
     const uint32_t row = fdiv((uint32_t)g, fnb);
     const int64_t b = g - (int64_t)row * nb;
-    uint32_t u[32];
-    load32<BF16>(x, (int64_t)row * ld + b * 32, u);
     uint4 cw;
     uint32_t sh;
-    mix_block32<TYPE>(u, ebias, asym != 0, cw, sh);
+    if (BF16) {  // packed step: two elements per integer operation
+      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + (int64_t)row * ld + b * 32);
+      uint32_t w[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 v = p[j];
+        w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
+      }
+      mix_block32_bf16<TYPE>(w, ebias, asym != 0, cw, sh);
+    } else {
+      uint32_t u[32];
+      load32<BF16>(x, (int64_t)row * ld + b * 32, u);
+      mix_block32<TYPE>(u, ebias, asym != 0, cw, sh);
+    }
     __stcs(reinterpret_cast<uint4*>(codes + g * 16), cw);
     if (TYPE == 1) static_cast<uint8_t*>(shared)[g] = (uint8_t)sh;
     else static_cast<uint16_t*>(shared)[g] = (uint16_t)sh;
