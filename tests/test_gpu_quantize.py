@@ -88,6 +88,29 @@ def test_mix_edge_values(mix, orc):
             check_mix(mix, orc, xb, t)
 
 
+def test_mix_every_bf16_pattern(mix, orc):
+    """All 65536 bf16 bit patterns (NaNs, +-Inf, +-0, subnormals, every
+    magnitude) through the bf16 quantiser, bit-exact against the oracle: once
+    shuffled together (most blocks then hold a NaN: the scalar path), once
+    without NaNs (every block on the packed two-elements-per-word path); both
+    types, both zero modes, ebias at both ends of its range and in between."""
+    rng = np.random.default_rng(11)
+    every = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    no_nan = every[(every & 0x7FFF) <= 0x7F80]
+    mixed = rng.permutation(every).reshape(256, 256)
+    clean = rng.permutation(no_nan)
+    clean = clean[: (clean.size // 256) * 256].reshape(-1, 256)
+    # blocks of one binade band each, so many blocks neither saturate nor flush
+    banded = np.sort(clean.reshape(-1) & 0x7FFF).astype(np.uint16)
+    banded = (banded[: (banded.size // 256) * 256] | (rng.integers(0, 2, banded.size // 256 * 256) << 15)
+              ).astype(np.uint16).reshape(-1, 256)
+    for x in (mixed, clean, banded):
+        for t in (1, 2):
+            for flags in (0, 1):
+                for ebias in (-100, -8, 30, 100):
+                    check_mix(mix, orc, x, t, ebias=ebias, flags=flags)
+
+
 def test_mix_strided_input(mix, orc):
     import torch
     a = synth.to_bf16_bits(synth.vlm_activations(8, 0, 64, 512, visual_rows=48))
