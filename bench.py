@@ -91,10 +91,12 @@ def dims(small=False):
                 HQ=28, HK=4, D=128)
 
 
-def tc_launches(n):
+def tc_launches(n, b_in_place=False):
     """Launches of one tensor-core matmul call: outputs wider than one 256-column
-    tile take the staged variant (expand A, expand B or its scales, matmul)."""
-    return 3 if n > 256 else 1
+    tile take the staged variant (expand A, expand B or its scales, matmul);
+    narrower ones the fused-decode variant (expand B unless it is MXFP4 read
+    in place, matmul)."""
+    return 3 if n > 256 else (1 if b_in_place else 2)
 
 
 def step_table(small=False):
