@@ -103,8 +103,7 @@ __global__ void __launch_bounds__(kThreads) expand_a_kernel(const uint8_t* __res
 // bytes regrouped into tiles of `tile_rows` (<= 256) rows, each stored as a
 // 256-row group (two 128-row halves; the words of rows tile_rows .. 255 are
 // padding and hold scale 1).  Threads walk the padded 256-row index space.
-// WRITE_OPS false: scales only (MXFP4 weights the matmul reads in place).
-template <bool FP4, bool WRITE_OPS>
+template <bool FP4>
 __global__ void __launch_bounds__(kThreads) expand_b_kernel(const uint8_t* __restrict__ codes,
                                                             const uint8_t* __restrict__ scales, int64_t N,
                                                             int64_t K, int64_t b_ld, int64_t b_bs, int64_t bb,
@@ -129,18 +128,14 @@ __global__ void __launch_bounds__(kThreads) expand_b_kernel(const uint8_t* __res
       if (kb < kbv) {
         const int64_t e = (int64_t)b * b_bs + r * b_ld + 32 * (int64_t)kb;
         sbyte = (uint32_t)__ldg(scales + e / 32);
-        if (WRITE_OPS) {
-          const uint4 cv = __ldg(reinterpret_cast<const uint4*>(codes + e / 2));
-          const uint2 d0 = dec8(cv.x, tt), d1 = dec8(cv.y, tt), d2 = dec8(cv.z, tt), d3 = dec8(cv.w, tt);
-          out0 = make_uint4(d0.x, d0.y, d1.x, d1.y);
-          out1 = make_uint4(d2.x, d2.y, d3.x, d3.y);
-        }
+        const uint4 cv = __ldg(reinterpret_cast<const uint4*>(codes + e / 2));
+        const uint2 d0 = dec8(cv.x, tt), d1 = dec8(cv.y, tt), d2 = dec8(cv.z, tt), d3 = dec8(cv.w, tt);
+        out0 = make_uint4(d0.x, d0.y, d1.x, d1.y);
+        out1 = make_uint4(d2.x, d2.y, d3.x, d3.y);
       }
-      if (WRITE_OPS) {
-        uint4* dst = reinterpret_cast<uint4*>(b_e4m3 + ((int64_t)b * N + r) * k_pad + 32 * (int64_t)kb);
-        dst[0] = out0;
-        dst[1] = out1;
-      }
+      uint4* dst = reinterpret_cast<uint4*>(b_e4m3 + ((int64_t)b * N + r) * k_pad + 32 * (int64_t)kb);
+      dst[0] = out0;
+      dst[1] = out1;
     }
     const uint32_t word = quad_or(sbyte << (8 * (kb & 3u)));
     if (valid && (kb & 3u) == 0) {
@@ -148,6 +143,35 @@ __global__ void __launch_bounds__(kThreads) expand_b_kernel(const uint8_t* __res
       const int64_t idx = ((((int64_t)b * nt + tile) * kt_n + (kb >> 2)) * 2 + h) * 128 + (rq & 31) * 4 + (rq >> 5);
       sfb[idx] = word;
     }
+  }
+}
+
+// Scales only (MXFP4 weights read in place): one thread per 32-bit scale
+// word, i.e. per (row, 128-deep k-step) of the padded 256-row groups; the
+// k-step runs fastest so the four scale bytes are read contiguously.
+__global__ void __launch_bounds__(kThreads) b_scales_kernel(const uint8_t* __restrict__ scales, int64_t N,
+                                                            int64_t K, int64_t b_ld, int64_t b_bs, int64_t bb,
+                                                            int tile_rows, int64_t kt_n, FastDiv f_kt,
+                                                            FastDiv f_rows, uint32_t* __restrict__ sfb) {
+  const int64_t kbv = K / 32;
+  const uint32_t total = (uint32_t)(bb * (int64_t)f_rows.d * f_kt.d);
+  const int64_t nt = f_rows.d / 256;
+  for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
+    const uint32_t rr = fdiv(t, f_kt), kt = t - rr * f_kt.d;
+    const uint32_t b = fdiv(rr, f_rows), vr = rr - b * f_rows.d;
+    const uint32_t tile = vr >> 8, rin = vr & 255u;
+    const int64_t r = (int64_t)tile * tile_rows + rin;
+    uint32_t word = 0x7F7F7F7Fu;
+    if ((int)rin < tile_rows && r < N) {
+      const uint8_t* src = scales + ((int64_t)b * b_bs + r * b_ld) / 32;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t kb = 4 * (int64_t)kt + j;
+        if (kb < kbv) word = (word & ~(0xFFu << (8 * j))) | ((uint32_t)__ldg(src + kb) << (8 * j));
+      }
+    }
+    const uint32_t h = rin >> 7, rq = rin & 127u;
+    sfb[((((int64_t)b * nt + tile) * kt_n + kt) * 2 + h) * 128 + (rq & 31) * 4 + (rq >> 5)] = word;
   }
 }
 
@@ -233,14 +257,15 @@ cudaError_t launch_expand_b(const mix_gemm_desc_t& d, const StagedPlan& sp, unsi
   uint32_t* sfb = reinterpret_cast<uint32_t*>(base + sp.off_sfb);
   const int g = grid_for(threads);
   const int64_t bs = sp.bb > 1 ? d.b_batch_stride : 0;
-  if (sp.b_native)
-    expand_b_kernel<true, false><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
-                                                         sp.k_pad, tr, sp.kt, fk, fr, nullptr, sfb);
-  else if (d.b_type == MX_FP4_E2M1)
-    expand_b_kernel<true, true><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
+  if (sp.b_native) {
+    const int64_t words = sp.bb * sp.nt * 256 * sp.kt;
+    b_scales_kernel<<<grid_for(words), kThreads, 0, st>>>(d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb, tr, sp.kt,
+                                                          make_fastdiv((uint32_t)sp.kt), fr, sfb);
+  } else if (d.b_type == MX_FP4_E2M1)
+    expand_b_kernel<true><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
                                                         sp.k_pad, tr, sp.kt, fk, fr, b, sfb);
   else
-    expand_b_kernel<false, true><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
+    expand_b_kernel<false><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
                                                          sp.k_pad, tr, sp.kt, fk, fr, b, sfb);
   return cudaGetLastError();
 }
