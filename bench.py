@@ -468,6 +468,56 @@ def run_reference(args, rank, world):
 # Our arm
 # ---------------------------------------------------------------------------
 
+def measure_fp8_peak(local):
+    """Dense FP8 e4m3 x e4m3 -> fp32 tensor rate on this GPU, measured the way
+    the bf16 peak in MEASURED_PEAKS.json was: an 8192^3 cuBLASLt matmul, best
+    of 10 (burst) and back to back for 4 s (sustained), with the SM clock
+    sampled.  kind::mxf8f6f4 runs on the same FP8 tensor rate."""
+    import torch
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    n = 8192
+    g = torch.Generator(device=dev).manual_seed(0)
+    a = torch.randn((n, n), device=dev, generator=g).to(torch.float8_e4m3fn)
+    b = torch.randn((n, n), device=dev, generator=g).to(torch.float8_e4m3fn).t()
+    one = torch.ones((), device=dev)
+
+    def mm():
+        return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.float32)
+
+    for _ in range(5):
+        mm()
+    torch.cuda.synchronize()
+    flops = 2.0 * n ** 3
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mm()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    clocks = ClockSampler(local)
+    clocks.start()
+    reps, t_start = 0, time.time()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    while time.time() - t_start < 4.0:
+        for _ in range(20):
+            mm()
+        reps += 20
+        torch.cuda.synchronize()
+    e1.record()
+    torch.cuda.synchronize()
+    ck = clocks.stop()
+    line = {"what": "dense FP8 e4m3 tensor rate, cuBLASLt 8192^3, fp32 out",
+            "fp8_tflops_burst": round(flops / (best * 1e-3) / 1e12, 1),
+            "fp8_tflops_sustained": round(flops * reps / (e0.elapsed_time(e1) * 1e-3) / 1e12, 1),
+            "bf16_tflops_measured": PEAKS["bf16_tflops"], "bf16_tflops_sustained_measured": PEAKS["bf16_tflops_sustained"],
+            "clocks": ck}
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,12 +527,16 @@ def main():
     ap.add_argument("--small", action="store_true", help="1/8-size workload (for profiler captures)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--mma-peak", action="store_true",
+                    help="measure the dense FP8 (e4m3) tensor rate instead: cuBLASLt 8192^3, burst and sustained")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.mma_peak:
+        return measure_fp8_peak(local)
 
     import torch
     from quantized_vlm_gemm_mix_b300 import _build
@@ -658,8 +712,14 @@ def main():
         tj = json.load(open(tp))
         if tj.get("call") == dc.name and tj.get("source_sha256") == matmul_source_sha():
             traffic = tj.get("dram_bytes_per_launch")
+    fp8 = None
+    fp = os.path.join(ROOT, "profiles", "fp8_peak.json")
+    if os.path.exists(fp):
+        fj = json.load(open(fp))
+        fp8 = {"fp8_tflops_sustained_direct": fj["fp8_tflops_sustained"],
+               "frac_of_direct": round(ach / fj["fp8_tflops_sustained"], 4), "how": fj["command"]}
     roofline = {"bound": "tensor", "kernel": dc.name, "achieved": round(ach, 1), "peak": round(MX8_TFLOPS, 1),
-                "unit": "TFLOP/s", "frac": round(ach / MX8_TFLOPS, 4), "traffic": traffic,
+                "unit": "TFLOP/s", "frac": round(ach / MX8_TFLOPS, 4), "traffic": traffic, "fp8_measured": fp8,
                 "algorithmic_bytes": dc.bytes, "algorithmic_flops": dc.flops,
                 "peak_source": f"2 x measured bf16 sustained ({PEAKS['source']}); "
                                f"burst {MX8_TFLOPS_BURST:.0f} TFLOP/s"}
