@@ -21,7 +21,7 @@ _LIB = os.path.join(_HERE, "liborcmix.so")
 F32, BF16 = 0, 1
 T1, T2 = 1, 2
 MXINT4, MXFP4 = 0, 1
-ASYM_ZERO, MX_FLOOR = 1, 2
+ASYM_ZERO, MX_FLOOR, MX_TIGHT = 1, 2, 4
 
 _lib = None
 
@@ -50,8 +50,10 @@ def lib():
         L.orc_ksmooth_mean.argtypes = [P, I, I64, I, I, I64, P]
         L.orc_ksmooth_apply.argtypes = [P, I, I64, I, I, I64, P, P]
         L.orc_set_mutation.argtypes = [I]
+        L.orc_mix_auto_ebias.argtypes = [P, I, I64, I64, I64]
         for f in ("orc_mix_quantize", "orc_mix_dequantize", "orc_mx_quantize",
-                  "orc_mx_dequantize", "orc_gemm", "orc_ksmooth_mean", "orc_ksmooth_apply"):
+                  "orc_mx_dequantize", "orc_gemm", "orc_ksmooth_mean", "orc_ksmooth_apply",
+                  "orc_mix_auto_ebias"):
             getattr(L, f).restype = ctypes.c_int
         L.orc_set_mutation.restype = None
         _lib = L
@@ -89,6 +91,16 @@ def mix_quantize(x: np.ndarray, mix_type: int, ebias: int = -8, flags: int = ASY
     _check(lib().orc_mix_quantize(_ptr(x), _dtype_of(x), rows, k, k, mix_type, ebias,
                                   flags, _ptr(codes), _ptr(shared)))
     return codes, shared
+
+
+def mix_auto_ebias(x: np.ndarray) -> int:
+    """The automatic ebias of x [rows, k] (float32 or bf16 bits)."""
+    x = np.ascontiguousarray(x)
+    rows, k = x.shape
+    e = lib().orc_mix_auto_ebias(_ptr(x), _dtype_of(x), rows, k, k)
+    if e == -1000:
+        raise ValueError("k must be a multiple of 32")
+    return e
 
 
 def mix_dequantize(codes: np.ndarray, shared: np.ndarray, mix_type: int, ebias: int = -8):

@@ -19,6 +19,11 @@
  * errors resolved toward the larger magnitude; an all-zero (sub-)block stores
  * zero shared fields; NaN counts as zero, +-Inf saturates; MXFP4 scale
  * ceil(log2 amax) - 2, MXINT4 scale floor(log2 amax) with q in [-7, 7].
+ * Optional rules beyond the page: the OCP floor for MXFP4, and the "tight"
+ * shared exponent (the smallest one at which no element saturates: the
+ * ceil(log2(amax / 6)) alternative the page's ceil rule is contrasted with);
+ * the automatic ebias puts the largest block's Emax at the top of the 4-bit
+ * range.
  */
 #include <math.h>
 #include <stdint.h>
@@ -28,7 +33,7 @@
 enum { ORC_F32 = 0, ORC_BF16 = 1 };
 enum { ORC_T1 = 1, ORC_T2 = 2 };
 enum { ORC_MXINT4 = 0, ORC_MXFP4 = 1 };
-enum { ORC_ASYM_ZERO = 1, ORC_MX_FLOOR = 2 };
+enum { ORC_ASYM_ZERO = 1, ORC_MX_FLOOR = 2, ORC_MX_TIGHT = 4 };
 
 /* A test may plant one deliberate mistake here to prove the pins catch it. */
 static int g_mutation = 0;
@@ -236,6 +241,37 @@ int orc_mix_dequantize(const uint8_t* codes, const void* shared, int64_t rows, i
   return 0;
 }
 
+/* Automatic ebias (a two-pass mode; the page fixes only the 4-bit width of
+ * Emax): the largest block exponent f over the tensor -- floor(log2) of the
+ * block maximum after its mantissa is rounded to three bits, carry included,
+ * i.e. the Emax that block would take unclamped -- less 15, so that block
+ * sits at the top of the range; clamped to [-100, 100].  Infinite elements
+ * saturate under any ebias and are left out of the scan, as NaN is; a tensor
+ * without a nonzero finite element gets -8. */
+int orc_mix_auto_ebias(const void* x, int dtype, int64_t rows, int64_t k, int64_t ld) {
+  if (k % 32 != 0) return -1000;
+  int have = 0, fmax = 0;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < k / 32; ++b) {
+      double amax = 0.0;
+      for (int i = 0; i < 32; ++i) {
+        double a = mag(load_elem(x, dtype, r * ld + b * 32 + i));
+        if (!isinf(a) && a > amax) amax = a;
+      }
+      if (amax == 0.0) continue;
+      int f, m3;
+      max_exp_mant(amax, &f, &m3);   /* Algorithm 1's first two steps, carry included */
+      if (g_mutation == 9) f = floor_log2(amax);   /* planted: carry dropped */
+      if (!have || f > fmax) fmax = f;
+      have = 1;
+    }
+  if (!have) return -8;
+  int e = fmax - 15;
+  if (e < -100) e = -100;
+  if (e > 100) e = 100;
+  return e;
+}
+
 /* ----------------------------------------------------------------------- */
 /* MX: MXINT4 / MXFP4, block 32, E8M0 shared scale                          */
 /* ----------------------------------------------------------------------- */
@@ -249,7 +285,13 @@ static int mx_shared_exp(double amax, int type, unsigned flags) {
   int X;
   if (isinf(amax)) return 127;
   int fl = floor_log2(amax);
-  if (type == ORC_MXFP4) {
+  if (flags & ORC_MX_TIGHT) {
+    /* smallest X with amax <= cap * 2^X: cap 6 (the largest E2M1 value) for
+     * MXFP4, 7 * 2^-2 for MXINT4 (elements q * 2^(X-2), |q| <= 7) */
+    const double cap = (type == ORC_MXFP4) ? 6.0 : 1.75;
+    X = fl - 4;
+    while (amax > ldexp(cap, X) || (g_mutation == 8 && amax == ldexp(cap, X))) ++X;
+  } else if (type == ORC_MXFP4) {
     int is_pow2 = ldexp(amax, -fl) == 1.0;
     int ce = is_pow2 ? fl : fl + 1;
     X = (flags & ORC_MX_FLOOR) ? fl - 2 : ce - 2;
@@ -320,6 +362,7 @@ int orc_mx_quantize(const void* x, int dtype, int64_t rows, int64_t cols, int64_
                     int axis, int type, unsigned flags, uint8_t* codes, uint8_t* scales) {
   int64_t N = axis ? rows : cols, K = axis ? cols : rows;
   if (K % 32 != 0) return 1;
+  if ((flags & ORC_MX_FLOOR) && (flags & ORC_MX_TIGHT)) return 1;   /* two exponent rules */
   int64_t nb = K / 32;
   double v[32];
   int c[32], sc;

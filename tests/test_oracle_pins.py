@@ -475,11 +475,117 @@ def pin_ksmooth(orc):
     assert np.max(np.abs(ks_f - want)) <= np.max(np.abs(want)) * 2.0 ** -23
 
 
+def brute_mx_code(y: Fraction, mx_type: int) -> int:
+    """Element code of y = x / 2^X (MXFP4) or x / 2^(X-2) (MXINT4), by search."""
+    if mx_type == 1:
+        grid = e2m1_magnitudes()
+        if abs(y) >= 6:
+            c = 7
+        else:
+            c = min(range(8), key=lambda j: (abs(abs(y) - grid[j]), j % 2))
+        return c | (8 if (y < 0 and c != 0) else 0)
+    q = max(-7, min(7, round(y)))                       # half to even
+    return q & 0xF
+
+
+def exact_f_m(a: Fraction):
+    """a = m * 2^f with m in [1, 2), exactly."""
+    f = 0
+    while Fraction(2) ** f > a:
+        f -= 1
+    while Fraction(2) ** (f + 1) <= a:
+        f += 1
+    return f, a / Fraction(2) ** f
+
+
+def pin_mx_tight_rule(orc):
+    """The tight MX exponent, the ceil(log2(amax / 6)) alternative to the ceil
+    rule (Key results section): the smallest X at which no element of the
+    block saturates.  With amax = m 2^f, m in [1, 2), it has the closed forms
+    MXFP4 X = f - 2 + [m > 1.5] and MXINT4 X = f + [m > 1.75] (elements
+    q 2^(X-2), |q| <= 7); it is never above the ceil rule and at most one
+    below it."""
+    rng = np.random.default_rng(21)
+    maxima = [m * 2.0 ** f for f in (-30, -3, 0, 7)
+              for m in (1.0, 1.25, 1.5, 1.5 + 2 ** -7, 1.75, 1.75 + 2 ** -7, 2 - 2 ** -7)]
+    x = (rng.uniform(-0.99, 0.99, (len(maxima), 32)) * np.array(maxima)[:, None]).astype(np.float32)
+    for b, a in enumerate(maxima):
+        x[b, rng.integers(32)] = a if b % 2 else -a
+    w = synth.bf16_bits_to_f32(synth.to_bf16_bits(synth.gaussian_weights(5, 3, 256, 64)))
+    for xx, brute in ((x, True), (w, False)):
+        for mx_type, cap in ((1, Fraction(6)), (0, Fraction(7, 4))):
+            codes, scales = orc.mx_quantize(xx, 1, mx_type, orc.MX_TIGHT)
+            _, ceil_scales = orc.mx_quantize(xx, 1, mx_type, 0)
+            nib = unpack_nibbles(codes)
+            X_all = scales.astype(np.int64) - 127
+            for r in range(xx.shape[0]):
+                for b in range(xx.shape[1] // 32):
+                    blk = [Fraction(float(v)) for v in xx[r, 32 * b: 32 * b + 32]]
+                    amax = max(abs(v) for v in blk)
+                    X = int(X_all[r, b])
+                    f, m = exact_f_m(amax)
+                    want = f - 2 + (m > Fraction(3, 2)) if mx_type == 1 else f + (m > Fraction(7, 4))
+                    assert X == want, (mx_type, float(amax), X, want)
+                    assert amax <= cap * Fraction(2) ** X < 2 * amax   # fits; X - 1 would not
+                    dx = int(ceil_scales[r, b]) - 127 - X
+                    assert dx in ((0, 1) if mx_type == 1 else (0, -1)), (mx_type, float(amax), dx)
+                    if brute:
+                        step = Fraction(2) ** (X if mx_type == 1 else X - 2)
+                        for i in range(32):
+                            assert int(nib[r, 32 * b + i]) == brute_mx_code(blk[i] / step, mx_type)
+    # about log2(1.5) of gaussian block maxima move down one binade under MXFP4
+    _, s_t = orc.mx_quantize(w, 1, 1, orc.MX_TIGHT)
+    _, s_c = orc.mx_quantize(w, 1, 1, 0)
+    frac = float(np.mean(s_t != s_c))
+    assert 0.45 < frac < 0.72, frac
+    with pytest.raises(ValueError):
+        orc.mx_quantize(w, 1, 1, orc.MX_TIGHT | orc.MX_FLOOR)
+
+
+def pin_auto_ebias(orc):
+    """Automatic ebias: the largest block exponent (the block maximum rounded
+    to a 3-bit mantissa, carry included, as in Algorithm 1) lands on the top
+    4-bit code, so no block clamps from above and the range below it is the
+    widest the 4-bit Emax field allows (Format section)."""
+    x = np.zeros((3, 96), np.float32)
+    x[0, 5] = 3.0                       # f = 1
+    x[1, 40] = -2.0 ** -7
+    x[2, 70] = 15.0                     # 1.875 * 2^3: f = 3, no carry
+    assert orc.mix_auto_ebias(x) == 3 - 15
+    x[2, 70] = 15.5                     # rounds to 16: the carry makes f = 4
+    assert orc.mix_auto_ebias(x) == 4 - 15
+    x[2, 70] = np.inf                   # saturates under any ebias; left out
+    x[2, 71] = np.nan
+    assert orc.mix_auto_ebias(x) == 1 - 15
+    assert orc.mix_auto_ebias(np.zeros((2, 64), np.float32)) == -8
+    x = np.zeros((1, 32), np.float32)
+    x[0, 3] = -np.inf
+    assert orc.mix_auto_ebias(x) == -8
+    big = np.full((1, 32), 2.0 ** 120, np.float32)
+    assert orc.mix_auto_ebias(big) == 100                  # clamped
+    # brute force on a wide-range tensor, f32 and bf16 alike
+    xa = synth.vlm_activations(4, 1, 64, 256, visual_rows=48, outlier_frac=0.01)
+    xb = synth.to_bf16_bits(xa)
+    for xx, vals in ((xa.astype(np.float32), xa.astype(np.float32)), (xb, synth.bf16_bits_to_f32(xb))):
+        fs = []
+        for r in range(vals.shape[0]):
+            for b in range(vals.shape[1] // 32):
+                amax = max(abs(Fraction(float(v))) for v in vals[r, 32 * b: 32 * b + 32])
+                if amax:
+                    fs.append(nearest_mantissa(amax)[0])
+        eb = orc.mix_auto_ebias(xx)
+        assert eb == max(fs) - 15
+        for t in (1, 2):
+            _, sh = orc.mix_quantize(xx, t, eb)
+            assert int(np.max(sh.astype(np.int64) & 0xF)) == 15
+
+
 ALL_PINS = [pin_bit_accounting, pin_dequant_special_values, pin_refinement_brute_force,
             pin_exhaustive_sweep, pin_asymmetric_zero, pin_round_trip,
             pin_nonfinite_and_zero_blocks, pin_e2m1_and_int4_brute_force, pin_mx_scale_rule,
             pin_mx_axis_consistency, pin_gemm_eq6_exact, pin_gemm_against_dequant_matmul,
-            pin_gemm_reduces_to_mx_dot, pin_gemm_batch_gqa_indexing, pin_ksmooth]
+            pin_gemm_reduces_to_mx_dot, pin_gemm_batch_gqa_indexing, pin_ksmooth,
+            pin_mx_tight_rule, pin_auto_ebias]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -491,14 +597,17 @@ def test_pin(orc, pin):
 # Mutations planted in the oracle (see orc_set_mutation): 1 mshared truncated
 # instead of rounded, 2 implicit leading one dropped, 3 naive de off by one,
 # 4 refinement search removed, 5 MXFP4 floor instead of ceil, 6 FP4 exponent
-# dropped from the Eq. (6) shift, 7 smoothing adds the mean.
+# dropped from the Eq. (6) shift, 7 smoothing adds the mean, 8 the tight MX
+# exponent steps past a block maximum on the boundary, 9 the automatic ebias
+# drops the rounding carry.
 FAST_PINS = [pin_dequant_special_values, pin_round_trip, pin_asymmetric_zero,
              pin_e2m1_and_int4_brute_force, pin_mx_scale_rule, pin_gemm_eq6_exact,
              pin_gemm_against_dequant_matmul, pin_ksmooth, pin_nonfinite_and_zero_blocks,
+             pin_mx_tight_rule, pin_auto_ebias,
              lambda o: pin_refinement_brute_force(o, n_blocks=40)]
 
 
-@pytest.mark.parametrize("mutation", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("mutation", [1, 2, 3, 4, 5, 6, 7, 8, 9])
 def test_planted_mistakes_are_caught(orc, mutation):
     failed = []
     try:
