@@ -56,6 +56,9 @@ MX8_TFLOPS_BURST = PEAKS["bf16_tflops"] * 2.0
 HBM = PEAKS["hbm_gbs"]
 
 
+EXT_INPUTS = {}   # step tensors the extension measurements reuse
+
+
 class Call:
     """One library call of the step with its algorithmic bytes and flops."""
 
@@ -209,6 +212,7 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
 
     w_gu = weight(30, DM, 2 * DF)        # gate+up 3584 x 37888; its first 18944 columns are the sweep weight
     keep.append(w_gu)
+    EXT_INPUTS.update(w_gu=w_gu, xd=xd, g=g)
     wq = {"gate_up": mix.quantize_mx(w_gu, 0, FP4)}
     for name, tid, k, n in (("qkv", 31, DM, QKV), ("o", 32, DM, DM), ("down", 33, DF, DM)):
         w = weight(tid, k, n)
@@ -518,6 +522,51 @@ def measure_fp8_peak(local):
     print(json.dumps(line))
 
 
+def measure_extensions(torch, mix, stream, iters=10):
+    """Kernels beyond the step (the tight MX exponent, the automatic ebias),
+    timed like the step's calls: CUDA events on the launching stream around
+    each launch, a spin kernel ahead of it, inputs larger than L2.  Each
+    entry gives its algorithmic bytes and the fraction of measured HBM copy
+    bandwidth reached."""
+    g, w_gu, xd = EXT_INPUTS["g"], EXT_INPUTS["w_gu"], EXT_INPUTS["xd"]
+    M, DM, DF = g["M"], g["DM"], g["DF"]
+    dev = xd.device
+    FP4, T2 = mix.MX_FP4_E2M1, mix.MIX_T2_4P5
+    wc = torch.empty((DF, DM // 2), dtype=torch.uint8, device=dev)
+    ws = torch.empty((DF, DM // 32), dtype=torch.uint8, device=dev)
+    ac = torch.empty((M, DF // 2), dtype=torch.uint8, device=dev)
+    ash = torch.empty((M, DF // 32), dtype=torch.int16, device=dev)
+    eb = torch.empty((1,), dtype=torch.int32, device=dev)
+    table = [
+        (f"mx_quantize_fp4_tight_{DM}x{DF}", "tight MX shared exponent", mx_bytes(DF, DM), 1,
+         lambda: mix.mx_quantize(w_gu, DM, DF, 2 * DF, 0, FP4, mix.MX_SCALE_TIGHT, wc, ws)),
+        (f"mx_quantize_fp4_ceil_{DM}x{DF}", "the ceil rule, same call (for comparison)", mx_bytes(DF, DM), 1,
+         lambda: mix.mx_quantize(w_gu, DM, DF, 2 * DF, 0, FP4, 0, wc, ws)),
+        (f"mix_auto_ebias_{M}x{DF}", "automatic ebias, pass 1 (clear, max-reduction, finish)", M * DF * 2 + 4, 3,
+         lambda: mix.mix_auto_ebias(xd, M, DF, DF, eb)),
+        (f"mix_quantize_auto_t2_{M}x{DF}", "automatic ebias + MiX-4.5b quantiser (x read twice)",
+         mix_bytes(M, DF, 2) + M * DF * 2, 4,
+         lambda: mix.mix_quantize_auto(xd, M, DF, DF, T2, 1, ac, ash, eb)),
+    ]
+    out = {}
+    for name, what, nbytes, launches, fn in table:
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for a, b in ev:
+            torch.cuda._sleep(400000)
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"what": what, "ms": round(ms, 5), "bytes": int(nbytes), "GB/s": round(gbs, 1),
+                     "frac_hbm": round(gbs / HBM, 3), "launches": launches}
+    assert mix.mix_device_error() == 0, "a kernel reported a timed-out wait"
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -527,6 +576,7 @@ def main():
     ap.add_argument("--small", action="store_true", help="1/8-size workload (for profiler captures)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--no-ext", action="store_true", help="skip the kernels measured beside the step")
     ap.add_argument("--mma-peak", action="store_true",
                     help="measure the dense FP8 (e4m3) tensor rate instead: cuBLASLt 8192^3, burst and sustained")
     args = ap.parse_args()
@@ -627,6 +677,7 @@ def main():
 
     roof_s = sum(c.roof_s() for c in calls)
     value = 100.0 * roof_s * world / (ms_step * 1e-3)
+    ext = None if args.no_ext else measure_extensions(torch, mix, stream)
 
     e2e = None
     if not args.no_e2e:
@@ -740,7 +791,8 @@ def main():
                       "hbm_peak_gbs": HBM, "mma_peak_tflops": round(MX8_TFLOPS, 1), "timing": timing_mode,
                       "per_call_timing": percall_mode},
            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-           "gpu_launches": int(sum(c.launches for c in calls) * args.steps), "clocks": clk, "parts": parts}
+           "gpu_launches": int(sum(c.launches for c in calls) * args.steps), "clocks": clk, "parts": parts,
+           "extensions": ext}
     if rank == 0:
         print(json.dumps(out), flush=True)
     del keep

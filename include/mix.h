@@ -69,8 +69,13 @@ typedef enum { MIX_DT_F32 = 0, MIX_DT_BF16 = 1 } mix_dtype_t;
 enum {
   MIX_ASYM_ZERO = 1,  /* MiX: recycle the -0 code for one more positive binade
                          (Method section, accelerator bullet).  Default on.   */
-  MX_SCALE_FLOOR = 2  /* MXFP4: OCP floor shared exponent instead of the ceil
+  MX_SCALE_FLOOR = 2, /* MXFP4: OCP floor shared exponent instead of the ceil
                          rule the paper uses for every MXFP4 (Key results).   */
+  MX_SCALE_TIGHT = 4  /* MX: the smallest shared exponent at which no element
+                         of the block saturates -- ceil(log2(amax / 6)) for
+                         MXFP4 (the alternative to the ceil rule named beside
+                         it in Key results), ceil(log2(amax / 1.75)) for
+                         MXINT4.  Not combinable with MX_SCALE_FLOOR.         */
 };
 
 /* ---------------------------------------------------------------------- */
@@ -105,6 +110,26 @@ MIX_API mix_status_t mix_quantize(const void* x, mix_dtype_t dtype, int64_t rows
                           mix_type_t type, int ebias, unsigned flags, uint8_t* codes,
                           void* shared, mix_stream_t stream);
 
+/* Data-dependent ebias (a two-pass mode; the Method section fixes only the
+ * 4-bit width of Emax).  Pass 1 finds the largest block exponent f over the
+ * tensor -- floor(log2) of a block maximum after Algorithm 1 rounds its
+ * mantissa to three bits, carry included -- and sets ebias = f - 15, so that
+ * block takes the top code and no block clamps from above; clamped to
+ * [-100, 100].  +-Inf and NaN elements are left out (they saturate / code zero
+ * under any ebias); a tensor with no nonzero finite element gets -8.
+ *   x, dtype, rows, k, ld   as for mix_quantize (same alignment rules).
+ *   ebias   one int in DEVICE memory (4-byte aligned), written on `stream`;
+ *           the host reads it only after synchronising.
+ * Three launches: a clear, a max-reduction over x, a one-warp finish. */
+MIX_API mix_status_t mix_auto_ebias(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,
+                                    int* ebias, mix_stream_t stream);
+/* mix_auto_ebias followed by mix_quantize with that ebias, all on `stream`
+ * with no host round trip (the quantiser reads *ebias on the device).  The
+ * ebias stays in *ebias for dequantisation and the matmul's a_ebias. */
+MIX_API mix_status_t mix_quantize_auto(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,
+                                       mix_type_t type, unsigned flags, uint8_t* codes, void* shared,
+                                       int* ebias, mix_stream_t stream);
+
 /* ---------------------------------------------------------------------- */
 /* W-MX quantiser (MXINT4 / MXFP4, block 32, E8M0 scale).                  */
 /* ---------------------------------------------------------------------- */
@@ -114,7 +139,8 @@ MIX_API mix_status_t mix_quantize(const void* x, mix_dtype_t dtype, int64_t rows
  *             weight stored for x @ W; it is read down its columns and the
  *             planes are written transposed (N x K).
  * MXFP4 shared exponent: ceil(log2 amax) - 2 (the paper's ceil rule, Key
- * results section), or the OCP floor with MX_SCALE_FLOOR; elements E2M1,
+ * results section), the OCP floor with MX_SCALE_FLOOR, or the tight rule with
+ * MX_SCALE_TIGHT (both flags together: MIX_ERR_INVALID_ARG); elements E2M1,
  * nearest-even, saturating at 6.  MXINT4: X = floor(log2 amax), elements
  * q * 2^(X-2), q in [-7, 7] two's complement, nearest-even.
  *   codes  N x K/2 bytes; scales N x K/32 bytes (X + 127). */
@@ -195,7 +221,7 @@ typedef struct {
   int64_t ldc, c_batch_stride;
   mix_epilogue_t epi;
   int epi_ebias;       /* MiX epilogues */
-  unsigned epi_flags;  /* MIX_ASYM_ZERO / MX_SCALE_FLOOR */
+  unsigned epi_flags;  /* MIX_ASYM_ZERO / MX_SCALE_FLOOR / MX_SCALE_TIGHT */
   uint8_t* out_codes;  /* batch x M x N/2 codes of the quantised output */
   void* out_shared;    /* MiX shared entries or MX scale bytes */
   int64_t out_ld, out_batch_stride;

@@ -51,9 +51,12 @@ def lib():
         L.orc_ksmooth_apply.argtypes = [P, I, I64, I, I, I64, P, P]
         L.orc_set_mutation.argtypes = [I]
         L.orc_mix_auto_ebias.argtypes = [P, I, I64, I64, I64]
+        L.orc_mx_quantize_blk.argtypes = [P, I, I64, I64, I64, I, I, U, I, P, P]
+        L.orc_mx_dequantize_blk.argtypes = [P, P, I64, I64, I, I, P]
+        L.orc_gemm_blk.argtypes = [P, P, I, I, P, P, I, I, I64, I64, I64, I64, I64, P]
         for f in ("orc_mix_quantize", "orc_mix_dequantize", "orc_mx_quantize",
                   "orc_mx_dequantize", "orc_gemm", "orc_ksmooth_mean", "orc_ksmooth_apply",
-                  "orc_mix_auto_ebias"):
+                  "orc_mix_auto_ebias", "orc_mx_quantize_blk", "orc_mx_dequantize_blk", "orc_gemm_blk"):
             getattr(L, f).restype = ctypes.c_int
         L.orc_set_mutation.restype = None
         _lib = L
@@ -113,28 +116,28 @@ def mix_dequantize(codes: np.ndarray, shared: np.ndarray, mix_type: int, ebias: 
     return out
 
 
-def mx_quantize(x: np.ndarray, axis: int, mx_type: int, flags: int = 0):
-    """axis=1: x is [N, K]; axis=0: x is [K, N].  -> (codes [N, K/2], scales [N, K/32])."""
+def mx_quantize(x: np.ndarray, axis: int, mx_type: int, flags: int = 0, block: int = 32):
+    """axis=1: x is [N, K]; axis=0: x is [K, N].  -> (codes [N, K/2], scales [N, K/block])."""
     x = np.ascontiguousarray(x)
     rows, cols = x.shape
     N, K = (rows, cols) if axis == 1 else (cols, rows)
     codes = np.zeros((N, K // 2), dtype=np.uint8)
-    scales = np.zeros((N, K // 32), dtype=np.uint8)
-    _check(lib().orc_mx_quantize(_ptr(x), _dtype_of(x), rows, cols, cols, axis, mx_type,
-                                 flags, _ptr(codes), _ptr(scales)))
+    scales = np.zeros((N, K // block), dtype=np.uint8)
+    _check(lib().orc_mx_quantize_blk(_ptr(x), _dtype_of(x), rows, cols, cols, axis, mx_type,
+                                     flags, block, _ptr(codes), _ptr(scales)))
     return codes, scales
 
 
-def mx_dequantize(codes: np.ndarray, scales: np.ndarray, mx_type: int):
+def mx_dequantize(codes: np.ndarray, scales: np.ndarray, mx_type: int, block: int = 32):
     codes = np.ascontiguousarray(codes)
     scales = np.ascontiguousarray(scales)
     n, kh = codes.shape
     out = np.zeros((n, kh * 2), dtype=np.float64)
-    _check(lib().orc_mx_dequantize(_ptr(codes), _ptr(scales), n, kh * 2, mx_type, _ptr(out)))
+    _check(lib().orc_mx_dequantize_blk(_ptr(codes), _ptr(scales), n, kh * 2, mx_type, block, _ptr(out)))
     return out
 
 
-def gemm(a_codes, a_shared, a_type, a_ebias, b_codes, b_scales, b_type, b_group: int = 1):
+def gemm(a_codes, a_shared, a_type, a_ebias, b_codes, b_scales, b_type, b_group: int = 1, b_block: int = 32):
     """Eq. (6) reference.  a_*: [batch, M, ...] or [M, ...]; b_*: [batch_b, N, ...] or [N, ...].
 
     Returns C fp64 [batch, M, N] (or [M, N] for 2-D inputs).
@@ -147,8 +150,8 @@ def gemm(a_codes, a_shared, a_type, a_ebias, b_codes, b_scales, b_type, b_group:
     batch, M, kh = ac.shape
     N = bc.shape[1]
     c = np.zeros((batch, M, N), dtype=np.float64)
-    _check(lib().orc_gemm(_ptr(ac), _ptr(ash), a_type, a_ebias, _ptr(bc), _ptr(bs), b_type,
-                          batch, b_group, M, N, kh * 2, _ptr(c)))
+    _check(lib().orc_gemm_blk(_ptr(ac), _ptr(ash), a_type, a_ebias, _ptr(bc), _ptr(bs), b_type, b_block,
+                              batch, b_group, M, N, kh * 2, _ptr(c)))
     return c[0] if squeeze else c
 
 

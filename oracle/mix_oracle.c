@@ -333,17 +333,18 @@ static int int4_code(double y) {
   return qi & 0xF;
 }
 
-static void mx_block(const double* v, int type, unsigned flags, int* codes, int* scale) {
+/* One MX block of n (32, or 16 for the g16 variants) elements. */
+static void mx_block(const double* v, int n, int type, unsigned flags, int* codes, int* scale) {
   double amax = 0.0;
-  for (int i = 0; i < 32; ++i) { double a = mag(v[i]); if (a > amax) amax = a; }
+  for (int i = 0; i < n; ++i) { double a = mag(v[i]); if (a > amax) amax = a; }
   if (amax == 0.0) {
     *scale = 0;
-    for (int i = 0; i < 32; ++i) codes[i] = 0;
+    for (int i = 0; i < n; ++i) codes[i] = 0;
     return;
   }
   int X = mx_shared_exp(amax, type, flags);
   *scale = X + 127;
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < n; ++i) {
     double x = isnan(v[i]) ? 0.0 : v[i];
     if (type == ORC_MXFP4) {
       codes[i] = isinf(x) ? ((x < 0) << 3 | 7) : e2m1_code(ldexp(x, -X));
@@ -353,31 +354,38 @@ static void mx_block(const double* v, int type, unsigned flags, int* codes, int*
   }
 }
 
-/* Quantise a matrix to MX with blocks along the reduction dimension K.
+/* Quantise a matrix to MX with blocks of `block` (32; 16 for MXINT4g16 /
+ * MXFP4g16) elements along the reduction dimension K.
  * axis = 1: x is N x K (row-major, ld >= K), blocks along its rows.
  * axis = 0: x is K x N (row-major, ld >= N), blocks down its columns; the
  *           output is written transposed, i.e. as N x K.
- * codes: N x K/2 bytes; scales: N x K/32 E8M0 bytes (X + 127). */
-int orc_mx_quantize(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
-                    int axis, int type, unsigned flags, uint8_t* codes, uint8_t* scales) {
+ * codes: N x K/2 bytes; scales: N x K/block E8M0 bytes (X + 127). */
+int orc_mx_quantize_blk(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                        int axis, int type, unsigned flags, int block, uint8_t* codes, uint8_t* scales) {
   int64_t N = axis ? rows : cols, K = axis ? cols : rows;
+  if (block != 32 && block != 16) return 1;
   if (K % 32 != 0) return 1;
   if ((flags & ORC_MX_FLOOR) && (flags & ORC_MX_TIGHT)) return 1;   /* two exponent rules */
-  int64_t nb = K / 32;
+  int64_t nb = K / block;
   double v[32];
   int c[32], sc;
   for (int64_t n = 0; n < N; ++n)
     for (int64_t b = 0; b < nb; ++b) {
-      for (int i = 0; i < 32; ++i) {
-        int64_t kk = b * 32 + i;
+      for (int i = 0; i < block; ++i) {
+        int64_t kk = b * block + i;
         v[i] = load_elem(x, dtype, axis ? n * ld + kk : kk * ld + n);
       }
-      mx_block(v, type, flags, c, &sc);
-      uint8_t* out = codes + n * (K / 2) + b * 16;
-      for (int j = 0; j < 16; ++j) out[j] = (uint8_t)(c[2 * j] | (c[2 * j + 1] << 4));
+      mx_block(v, block, type, flags, c, &sc);
+      uint8_t* out = codes + n * (K / 2) + b * (block / 2);
+      for (int j = 0; j < block / 2; ++j) out[j] = (uint8_t)(c[2 * j] | (c[2 * j + 1] << 4));
       scales[n * nb + b] = (uint8_t)sc;
     }
   return 0;
+}
+
+int orc_mx_quantize(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld,
+                    int axis, int type, unsigned flags, uint8_t* codes, uint8_t* scales) {
+  return orc_mx_quantize_blk(x, dtype, rows, cols, ld, axis, type, flags, 32, codes, scales);
 }
 
 static double mx_value(int code, int X, int type) {
@@ -389,16 +397,21 @@ static double mx_value(int code, int X, int type) {
   return ldexp((double)q, X - 2);
 }
 
-int orc_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t n_rows, int64_t k,
-                      int type, double* out) {
-  if (k % 32 != 0) return 1;
-  int64_t nb = k / 32;
+int orc_mx_dequantize_blk(const uint8_t* codes, const uint8_t* scales, int64_t n_rows, int64_t k,
+                          int type, int block, double* out) {
+  if (k % 32 != 0 || (block != 32 && block != 16)) return 1;
+  int64_t nb = k / block;
   for (int64_t n = 0; n < n_rows; ++n)
     for (int64_t kk = 0; kk < k; ++kk) {
-      int X = (int)scales[n * nb + kk / 32] - 127;
+      int X = (int)scales[n * nb + kk / block] - 127;
       out[n * k + kk] = mx_value(nibble(codes + n * (k / 2), kk), X, type);
     }
   return 0;
+}
+
+int orc_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t n_rows, int64_t k,
+                      int type, double* out) {
+  return orc_mx_dequantize_blk(codes, scales, n_rows, k, type, 32, out);
 }
 
 /* ----------------------------------------------------------------------- */
@@ -422,20 +435,22 @@ static void mx_int_parts(int code, int type, int* mant, int* shift) {
  *    (1.mshared) * 2^(Emax + X) * sum_i sign_i * w_i * 2^(-de_i)      (Eq. 6)
  * evaluated as an exact int64 shift-add per block (per 8-sub-block for T2,
  * each multiplied by its own 8 + m3), one multiply by the shared mantissa,
- * one exponent add, and an fp64 sum across blocks in K order.
+ * one exponent add, and an fp64 sum across blocks in K order.  With g16
+ * weights (b_block 16) the block splits into its two 16-element halves, each
+ * scaled by its own X: two exponent adds per 32-block, in K order.
  * A: batch x M x K MiX; B: (batch / b_group) x N x K MX.  Planes dense. */
-int orc_gemm(const uint8_t* a_codes, const void* a_shared, int a_type, int a_ebias,
-             const uint8_t* b_codes, const uint8_t* b_scales, int b_type,
-             int64_t batch, int64_t b_group, int64_t M, int64_t N, int64_t K, double* c) {
-  if (K % 32 != 0 || b_group < 1) return 1;
-  int64_t nb = K / 32;
+int orc_gemm_blk(const uint8_t* a_codes, const void* a_shared, int a_type, int a_ebias,
+                 const uint8_t* b_codes, const uint8_t* b_scales, int b_type, int b_block,
+                 int64_t batch, int64_t b_group, int64_t M, int64_t N, int64_t K, double* c) {
+  if (K % 32 != 0 || b_group < 1 || (b_block != 32 && b_block != 16)) return 1;
+  int64_t nb = K / 32, nbb = K / b_block;
   int cB = (b_type == ORC_MXFP4) ? 1 : 2;
   size_t ssz = (a_type == ORC_T1) ? 1 : 2;
   for (int64_t bt = 0; bt < batch; ++bt) {
     const uint8_t* ac = a_codes + bt * M * (K / 2);
     const char* as = (const char*)a_shared + bt * M * nb * ssz;
     const uint8_t* bc = b_codes + (bt / b_group) * N * (K / 2);
-    const uint8_t* bs = b_scales + (bt / b_group) * N * nb;
+    const uint8_t* bs = b_scales + (bt / b_group) * N * nbb;
     for (int64_t m = 0; m < M; ++m)
       for (int64_t n = 0; n < N; ++n) {
         double acc = 0.0;
@@ -443,7 +458,6 @@ int orc_gemm(const uint8_t* a_codes, const void* a_shared, int a_type, int a_ebi
           int ec, m3s[4];
           mix_shared_fields(as, a_type, m * nb + b, &ec, m3s);
           int emax = ec + a_ebias;
-          int X = (int)bs[n * nb + b] - 127;
           int64_t block = 0;
           for (int sb = 0; sb < 4; ++sb) {
             int64_t S = 0;                  /* shift-add tree of one sub-block */
@@ -460,15 +474,27 @@ int orc_gemm(const uint8_t* a_codes, const void* a_shared, int a_type, int a_ebi
               S += s ? -t : t;
             }
             block += S * (8 + m3s[sb]);     /* x (1.mshared) in eighths */
+            if (b_block == 16 && (sb & 1)) {  /* end of a 16-element half */
+              int X = (int)bs[n * nbb + 2 * b + (sb >> 1)] - 127;
+              acc += ldexp((double)block, emax + X - 10 - cB);
+              block = 0;
+            }
           }
           /* A = s (8+m3) 2^(Emax-3-de), B = w 2^ws 2^(X-cB): the block is
            * block * 2^(Emax + X - 10 - cB). */
-          acc += ldexp((double)block, emax + X - 10 - cB);
+          if (b_block == 32) acc += ldexp((double)block, emax + (int)bs[n * nbb + b] - 127 - 10 - cB);
         }
         c[(bt * M + m) * N + n] = acc;
       }
   }
   return 0;
+}
+
+int orc_gemm(const uint8_t* a_codes, const void* a_shared, int a_type, int a_ebias,
+             const uint8_t* b_codes, const uint8_t* b_scales, int b_type,
+             int64_t batch, int64_t b_group, int64_t M, int64_t N, int64_t K, double* c) {
+  return orc_gemm_blk(a_codes, a_shared, a_type, a_ebias, b_codes, b_scales, b_type, 32, batch, b_group,
+                      M, N, K, c);
 }
 
 /* ----------------------------------------------------------------------- */

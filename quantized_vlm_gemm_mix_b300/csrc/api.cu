@@ -10,7 +10,7 @@ using namespace mixk;
 
 namespace {
 
-constexpr int kVersion = 10200;  // 1.2.0
+constexpr int kVersion = 10300;  // 1.3.0
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -82,18 +82,53 @@ mix_status_t mix_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_
                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
+mix_status_t mix_auto_ebias(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld, int* ebias,
+                            mix_stream_t stream) {
+  if (!valid_dtype(dtype) || rows < 0 || k < 0 || ld < k || ebias == nullptr) return MIX_ERR_INVALID_ARG;
+  if (k % 32 != 0) return MIX_ERR_SHAPE;
+  if (!aligned(ebias, 4)) return MIX_ERR_ALIGN;
+  if (rows > 0 && k > 0) {
+    if (x == nullptr) return MIX_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0) return MIX_ERR_ALIGN;
+  }
+  return from_cuda(launch_auto_ebias(x, dtype == MIX_DT_BF16, rows, k, ld, ebias,
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mix_status_t mix_quantize_auto(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,
+                               mix_type_t type, unsigned flags, uint8_t* codes, void* shared, int* ebias,
+                               mix_stream_t stream) {
+  if (!valid_dtype(dtype) || (type != MIX_T1_4P25 && type != MIX_T2_4P5)) return MIX_ERR_INVALID_ARG;
+  if (rows < 0 || k < 0 || ld < k || (flags & ~1u) || ebias == nullptr) return MIX_ERR_INVALID_ARG;
+  if (k % 32 != 0) return MIX_ERR_SHAPE;
+  if (!aligned(ebias, 4)) return MIX_ERR_ALIGN;
+  const bool empty = rows == 0 || k == 0;
+  if (!empty) {
+    if (x == nullptr || codes == nullptr || shared == nullptr) return MIX_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(codes, 16) ||
+        !aligned(shared, type == MIX_T1_4P25 ? 1 : 2))
+      return MIX_ERR_ALIGN;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_auto_ebias(x, dtype == MIX_DT_BF16, rows, k, ld, ebias, st);
+  if (e != cudaSuccess || empty) return from_cuda(e);
+  return from_cuda(launch_mix_quantize(x, dtype == MIX_DT_BF16, rows, k, ld, (int)type, 0,
+                                       (flags & MIX_ASYM_ZERO) != 0, codes, shared, st, ebias));
+}
+
 mix_status_t mx_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t cols, int64_t ld,
                          int axis, mx_type_t type, unsigned flags, uint8_t* codes, uint8_t* scales,
                          mix_stream_t stream) {
   if (!valid_dtype(dtype) || (type != MX_INT4 && type != MX_FP4_E2M1) || (axis != 0 && axis != 1))
     return MIX_ERR_INVALID_ARG;
-  if (rows < 0 || cols < 0 || ld < cols || (flags & ~2u)) return MIX_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ld < cols || (flags & ~6u) || flags == 6u) return MIX_ERR_INVALID_ARG;
   const int64_t K = axis ? cols : rows, N = axis ? rows : cols;
   if (K % 32 != 0) return MIX_ERR_SHAPE;
   if (N == 0 || K == 0) return MIX_OK;
   if (x == nullptr || codes == nullptr || scales == nullptr) return MIX_ERR_INVALID_ARG;
   if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(codes, 16)) return MIX_ERR_ALIGN;
-  const bool fp4 = type == MX_FP4_E2M1, fl = (flags & MX_SCALE_FLOOR) != 0;
+  const bool fp4 = type == MX_FP4_E2M1;
+  const int fl = mx_rule_of(flags);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (axis == 1)
     return from_cuda(launch_mx_quantize_rows(x, dtype == MIX_DT_BF16, N, K, ld, fp4, fl, codes, scales, st));
@@ -132,6 +167,7 @@ static mix_status_t validate_gemm(const mix_gemm_desc_t* d) {
   if (d->a_ebias < -100 || d->a_ebias > 100 || d->epi_ebias < -100 || d->epi_ebias > 100)
     return MIX_ERR_INVALID_ARG;
   if (d->epi < MIX_EPI_NONE || d->epi > MIX_EPI_MXFP4) return MIX_ERR_INVALID_ARG;
+  if ((d->epi_flags & ~7u) || (d->epi_flags & 6u) == 6u) return MIX_ERR_INVALID_ARG;
   if (d->algo < MIX_GEMM_AUTO || d->algo > MIX_GEMM_TCGEN05_FUSED) return MIX_ERR_INVALID_ARG;
   if (d->K % 32 != 0) return MIX_ERR_SHAPE;
   if (d->epi != MIX_EPI_NONE && d->N % 32 != 0) return MIX_ERR_SHAPE;

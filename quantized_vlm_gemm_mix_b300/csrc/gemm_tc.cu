@@ -127,8 +127,8 @@ __device__ __forceinline__ void epi_quant_block(uint32_t* u, const TcParams& p, 
     mix_block32<2>(u, p.epi_ebias, asym, codes, shared);
     return;
   }
-  if (p.epi == MIX_EPI_MXFP4) mx_block32<true>(u, (p.epi_flags & MX_SCALE_FLOOR) != 0, codes, shared);
-  else mx_block32<false>(u, (p.epi_flags & MX_SCALE_FLOOR) != 0, codes, shared);
+  if (p.epi == MIX_EPI_MXFP4) mx_block32<true>(u, mx_rule_of(p.epi_flags), codes, shared);
+  else mx_block32<false>(u, mx_rule_of(p.epi_flags), codes, shared);
 }
 
 // Epilogue of one 128 x 256 tile by sixteen warps (DEC_WARP0 ..): warp w

@@ -256,7 +256,7 @@ cudaError_t launch_gemv_shiftadd(const mix_gemm_desc_t& d, void* ws, cudaStream_
       } else {
         uint8_t* os = static_cast<uint8_t*>(d.out_shared) + bt * d.out_batch_stride / 32;
         e = launch_mx_quantize_rows(cb, false, d.M, d.N, ldc, d.epi == MIX_EPI_MXFP4,
-                                    (d.epi_flags & MX_SCALE_FLOOR) != 0, oc, os, st);
+                                    mx_rule_of(d.epi_flags), oc, os, st);
       }
       if (e != cudaSuccess) return e;
     }

@@ -10,6 +10,8 @@
 #pragma once
 #include <cstdint>
 
+#include "mix_internal.h"
+
 namespace mixk {
 
 // An fp32 value split for integer decisions.
@@ -309,18 +311,21 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
 // MX (MXINT4 / MXFP4)
 // ---------------------------------------------------------------------------
 
-// Shared exponent X from the block maximum key (key != 0).  MXFP4: the OCP
-// rule floor(log2 amax) - 2 with the floor replaced by a ceil (the paper's
-// MXFP4), or the OCP floor on request.  MXINT4: floor(log2 amax).
-__device__ __forceinline__ int mx_shared_exp(uint32_t key, bool fp4, bool floor_rule) {
+// Shared exponent X from the block maximum key (key != 0), amax = sig 2^f
+// with sig in [1, 2).  MXFP4: the OCP rule floor(log2 amax) - 2 with the
+// floor replaced by a ceil (the paper's MXFP4), the OCP floor, or the tight
+// ceil(log2(amax / 6)) = f - 2 + [sig > 1.5].  MXINT4 (elements q 2^(X-2),
+// |q| <= 7): floor(log2 amax), or the tight f + [sig > 1.75].
+__device__ __forceinline__ int mx_shared_exp(uint32_t key, bool fp4, int rule) {
   if (key >= 0x7F800000u) return 127;
   Elem e = split_f32(key);
   int X;
   if (fp4) {
-    int ce = (e.sig == 0x800000u) ? e.f : e.f + 1;
-    X = floor_rule ? e.f - 2 : ce - 2;
+    if (rule == MX_RULE_TIGHT) X = e.f - 2 + (e.sig > 0xC00000u ? 1 : 0);
+    else if (rule == MX_RULE_FLOOR) X = e.f - 2;
+    else X = (e.sig == 0x800000u) ? e.f - 2 : e.f - 1;
   } else {
-    X = e.f;
+    X = e.f + ((rule == MX_RULE_TIGHT && e.sig > 0xE00000u) ? 1 : 0);
   }
   return clampi(X, -127, 127);
 }
@@ -391,7 +396,7 @@ __device__ __forceinline__ void zero_nans(uint32_t* u) {
 // exponent X, the 16 code bytes and the E8M0 scale byte X + 127 (zero codes
 // and scale for an all-zero block).
 template <bool FP4>
-__device__ __forceinline__ void mx_block32(uint32_t* u, bool floor_rule, uint4& w, uint32_t& sc) {
+__device__ __forceinline__ void mx_block32(uint32_t* u, int rule, uint4& w, uint32_t& sc) {
   uint32_t kb = max_abs_bits<32>(u);
   if (kb > 0x7F800000u) {
     zero_nans<32>(u);
@@ -400,7 +405,7 @@ __device__ __forceinline__ void mx_block32(uint32_t* u, bool floor_rule, uint4& 
   w = make_uint4(0, 0, 0, 0);
   sc = 0;
   if (kb != 0u) {
-    const int X = mx_shared_exp(kb, FP4, floor_rule);
+    const int X = mx_shared_exp(kb, FP4, rule);
     w = make_uint4(mx_codes8(u, X, FP4), mx_codes8(u + 8, X, FP4), mx_codes8(u + 16, X, FP4),
                    mx_codes8(u + 24, X, FP4));
     sc = (uint32_t)(X + 127);

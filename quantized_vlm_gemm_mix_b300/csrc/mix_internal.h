@@ -10,14 +10,26 @@ namespace mixk {
 
 int num_sms();
 
+// MX shared-exponent rules: the paper's ceil (the default), the OCP floor, and
+// the tight rule (the smallest exponent at which no element saturates).
+enum { MX_RULE_CEIL = 0, MX_RULE_FLOOR = 1, MX_RULE_TIGHT = 2 };
+__host__ __device__ inline int mx_rule_of(unsigned flags) {
+  return (flags & MX_SCALE_FLOOR) ? MX_RULE_FLOOR : (flags & MX_SCALE_TIGHT) ? MX_RULE_TIGHT : MX_RULE_CEIL;
+}
+
+// ebias_dev, when given, overrides ebias with the int it points at (read on
+// the device: the automatic two-pass mode).
 cudaError_t launch_mix_quantize(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld,
                                 int type, int ebias, bool asym, uint8_t* codes, void* shared,
-                                cudaStream_t st);
+                                cudaStream_t st, const int* ebias_dev = nullptr);
+// Automatic ebias into one device int (clear, max-reduction, finish).
+cudaError_t launch_auto_ebias(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, int* ebias,
+                              cudaStream_t st);
 cudaError_t launch_mx_quantize_rows(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld,
-                                    bool fp4, bool floor_rule, uint8_t* codes, uint8_t* scales,
+                                    bool fp4, int rule, uint8_t* codes, uint8_t* scales,
                                     cudaStream_t st);
 cudaError_t launch_mx_quantize_cols(const void* x, bool bf16, int64_t kdim, int64_t n, int64_t ld,
-                                    bool fp4, bool floor_rule, uint8_t* codes, uint8_t* scales,
+                                    bool fp4, int rule, uint8_t* codes, uint8_t* scales,
                                     cudaStream_t st);
 cudaError_t launch_mix_dequantize(const uint8_t* codes, const void* shared, int64_t rows, int64_t k,
                                   int type, int ebias, float* out, cudaStream_t st);

@@ -89,10 +89,14 @@ __device__ __forceinline__ void load32(const void* base, int64_t elem, uint32_t*
   }
 }
 
-template <bool BF16, int TYPE>
+// DEV_EB: ebias is read from device memory (the automatic two-pass mode), in
+// its own instantiation so the fixed-ebias kernel keeps ebias in the
+// parameter bank rather than in a register.
+template <bool BF16, int TYPE, bool DEV_EB>
 __global__ void __launch_bounds__(kThreads, 4) mix_quantize_kernel(
     const void* __restrict__ x, int64_t rows, int64_t nb, int64_t ld, int ebias, int asym,
-    uint8_t* __restrict__ codes, void* __restrict__ shared, FastDiv fnb) {
+    uint8_t* __restrict__ codes, void* __restrict__ shared, FastDiv fnb, const int* __restrict__ ebias_dev) {
+  if (DEV_EB) ebias = *ebias_dev;
   const int64_t total = rows * nb;
   for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < total; g += (int64_t)gridDim.x * kThreads) {
     const uint32_t row = fdiv((uint32_t)g, fnb);
@@ -119,9 +123,73 @@ __global__ void __launch_bounds__(kThreads, 4) mix_quantize_kernel(
   }
 }
 
+// Automatic ebias, pass 1: the largest finite |x| of the tensor, as the
+// integer maximum of the magnitude bits (the order of non-negative floats).
+// Rounding a block maximum to three mantissa bits never lowers a larger one
+// below a smaller one, so the largest rounded block exponent is the rounded
+// exponent of the global maximum and the pass needs no block structure.
+// bf16 pairs are compared two at a time in 16-bit SIMD lanes.  One 16-byte
+// vector per load, four in flight per thread, one atomic per warp.
+constexpr int kAmaxUnroll = 4;
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) amax_bits_kernel(const void* __restrict__ x, int64_t rows,
+                                                             int64_t vpr, int64_t ld_bytes, FastDiv fv,
+                                                             unsigned* __restrict__ key) {
+  const int64_t total = rows * vpr;
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  uint32_t m = 0u;   // fp32 magnitude bits, or two bf16 magnitudes
+  for (int64_t g0 = (int64_t)blockIdx.x * kThreads + threadIdx.x; g0 < total; g0 += stride * kAmaxUnroll) {
+    uint4 v[kAmaxUnroll];
+#pragma unroll
+    for (int r = 0; r < kAmaxUnroll; ++r) {
+      const int64_t g = g0 + r * stride;
+      v[r] = make_uint4(0u, 0u, 0u, 0u);
+      if (g < total) {
+        const uint32_t row = fdiv((uint32_t)g, fv);
+        const int64_t c = g - (int64_t)row * vpr;
+        v[r] = __ldg(reinterpret_cast<const uint4*>(static_cast<const char*>(x) + (int64_t)row * ld_bytes + c * 16));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kAmaxUnroll; ++r) {
+      const uint32_t w[4] = {v[r].x, v[r].y, v[r].z, v[r].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (BF16) {
+          const uint32_t a = w[i] & 0x7FFF7FFFu;
+          m = __vmaxu2(m, a & __vcmpltu2(a, 0x7F807F80u));   // +-Inf and NaN drop out
+        } else {
+          const uint32_t a = w[i] & 0x7FFFFFFFu;
+          m = max(m, a < 0x7F800000u ? a : 0u);
+        }
+      }
+    }
+  }
+  if (BF16) m = max(m >> 16, m & 0xFFFFu) << 16;
+  m = __reduce_max_sync(0xFFFFFFFFu, m);
+  if ((threadIdx.x & 31) == 0 && m != 0u) atomicMax(key, m);
+}
+
+// Pass 1 finish: key (fp32 magnitude bits of the largest finite |x|, 0 if
+// none) -> ebias in place.  The exponent is Algorithm 1's: the significand
+// rounded to three fraction bits, nearest-even, a round-up to 2 carrying
+// into the exponent (fraction >= 15/16).
+__global__ void auto_ebias_finish_kernel(int* __restrict__ ebias) {
+  if (threadIdx.x != 0) return;
+  const uint32_t key = *reinterpret_cast<const unsigned*>(ebias);
+  int e = -8;
+  if (key != 0u) {
+    const Elem el = split_f32(key);
+    const int f = el.f + ((el.sig & 0x7FFFFFu) >= 0x780000u ? 1 : 0);
+    e = clampi(f - 15, -100, 100);
+  }
+  *ebias = e;
+}
+
 template <bool BF16, bool FP4>
 __global__ void __launch_bounds__(kThreads, 4) mx_quantize_rows_kernel(
-    const void* __restrict__ x, int64_t rows, int64_t nb, int64_t ld, int floor_rule,
+    const void* __restrict__ x, int64_t rows, int64_t nb, int64_t ld, int rule,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, FastDiv fnb) {
   const int q = threadIdx.x & 3;
   const int64_t total = rows * nb;
@@ -151,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 4) mx_quantize_rows_kernel(
       }
       uint32_t word = 0u, sc = 0u;
       if (kb != 0u) {
-        const int X = mx_shared_exp(kb, FP4, floor_rule != 0);
+        const int X = mx_shared_exp(kb, FP4, rule);
         word = mx_codes8(u[r], X, FP4);
         sc = (uint32_t)(X + 127);
       }
@@ -170,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 4) mx_quantize_rows_kernel(
 // written by one CTA.
 template <bool BF16, bool FP4>
 __global__ void __launch_bounds__(kThreads) mx_quantize_cols_kernel(
-    const void* __restrict__ x, int64_t kdim, int64_t n, int64_t ld, int floor_rule,
+    const void* __restrict__ x, int64_t kdim, int64_t n, int64_t ld, int rule,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nbk = kdim / 32;
@@ -210,7 +278,7 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_cols_kernel(
     uint32_t* u = c ? u1 : u0;
     uint4 w;
     uint32_t sc;
-    mx_block32<FP4>(u, floor_rule != 0, w, sc);
+    mx_block32<FP4>(u, rule, w, sc);
     const int64_t col = n0 + c;
     *reinterpret_cast<uint4*>(codes + col * (kdim / 2) + kb * 16) = w;
     scales[col * nbk + kb] = (uint8_t)sc;
@@ -288,30 +356,58 @@ int grid_for(int64_t quads) {
 
 cudaError_t launch_mix_quantize(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld,
                                 int type, int ebias, bool asym, uint8_t* codes, void* shared,
-                                cudaStream_t st) {
+                                cudaStream_t st, const int* ebias_dev) {
   const int64_t nb = k / 32;
   if (rows * nb >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;  // 32-bit block index
   int64_t gb = (rows * nb + kThreads - 1) / kThreads;
   if (gb > (int64_t)num_sms() * 4) gb = (int64_t)num_sms() * 4;  // one wave of 4 resident CTAs per SM
   const int grid = (int)(gb > 0 ? gb : 1);
   const FastDiv f = make_fastdiv((uint32_t)nb);
+  const bool dev = ebias_dev != nullptr;
+#define MIXQ_LAUNCH(BF, T)                                                                                   \
+  (dev ? mix_quantize_kernel<BF, T, true><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes,   \
+                                                                      shared, f, ebias_dev)                  \
+       : mix_quantize_kernel<BF, T, false><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes,  \
+                                                                       shared, f, ebias_dev))
   if (bf16) {
-    if (type == 1) mix_quantize_kernel<true, 1><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared, f);
-    else mix_quantize_kernel<true, 2><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared, f);
+    if (type == 1) MIXQ_LAUNCH(true, 1);
+    else MIXQ_LAUNCH(true, 2);
   } else {
-    if (type == 1) mix_quantize_kernel<false, 1><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared, f);
-    else mix_quantize_kernel<false, 2><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, ebias, asym, codes, shared, f);
+    if (type == 1) MIXQ_LAUNCH(false, 1);
+    else MIXQ_LAUNCH(false, 2);
   }
+#undef MIXQ_LAUNCH
+  return cudaGetLastError();
+}
+
+cudaError_t launch_auto_ebias(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, int* ebias,
+                              cudaStream_t st) {
+  const int es = bf16 ? 2 : 4;
+  const int64_t vpr = k * es / 16;   // 16-byte vectors per row (k % 32 == 0)
+  if (rows * vpr >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;  // 32-bit vector index
+  cudaError_t e = cudaMemsetAsync(ebias, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  if (rows > 0 && vpr > 0) {
+    int64_t gb = (rows * vpr + (int64_t)kThreads * kAmaxUnroll - 1) / ((int64_t)kThreads * kAmaxUnroll);
+    if (gb > (int64_t)num_sms() * 8) gb = (int64_t)num_sms() * 8;
+    const FastDiv f = make_fastdiv((uint32_t)vpr);
+    unsigned* key = reinterpret_cast<unsigned*>(ebias);
+    if (bf16) amax_bits_kernel<true><<<(int)gb, kThreads, 0, st>>>(x, rows, vpr, ld * es, f, key);
+    else amax_bits_kernel<false><<<(int)gb, kThreads, 0, st>>>(x, rows, vpr, ld * es, f, key);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  auto_ebias_finish_kernel<<<1, 32, 0, st>>>(ebias);
   return cudaGetLastError();
 }
 
 cudaError_t launch_mx_quantize_rows(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld,
-                                    bool fp4, bool floor_rule, uint8_t* codes, uint8_t* scales,
+                                    bool fp4, int rule, uint8_t* codes, uint8_t* scales,
                                     cudaStream_t st) {
   const int64_t nb = k / 32;
   if (rows * nb >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;  // 32-bit block index
   const int grid = grid_for(rows * nb);
-  const int fr = floor_rule ? 1 : 0;
+  const int fr = rule;
   const FastDiv f = make_fastdiv((uint32_t)nb);
   if (bf16) {
     if (fp4) mx_quantize_rows_kernel<true, true><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales, f);
@@ -324,10 +420,10 @@ cudaError_t launch_mx_quantize_rows(const void* x, bool bf16, int64_t rows, int6
 }
 
 cudaError_t launch_mx_quantize_cols(const void* x, bool bf16, int64_t kdim, int64_t n, int64_t ld,
-                                    bool fp4, bool floor_rule, uint8_t* codes, uint8_t* scales,
+                                    bool fp4, int rule, uint8_t* codes, uint8_t* scales,
                                     cudaStream_t st) {
   const dim3 grid((unsigned)((n + 63) / 64), (unsigned)((kdim / 32 + 7) / 8));
-  const int fr = floor_rule ? 1 : 0;
+  const int fr = rule;
   if (bf16) {
     if (fp4) mx_quantize_cols_kernel<true, true><<<grid, kThreads, 0, st>>>(x, kdim, n, ld, fr, codes, scales);
     else mx_quantize_cols_kernel<true, false><<<grid, kThreads, 0, st>>>(x, kdim, n, ld, fr, codes, scales);

@@ -22,12 +22,13 @@ MIX_ERR_UNSUPPORTED, MIX_ERR_CUDA, MIX_ERR_WORKSPACE, MIX_ERR_DEVICE = 4, 5, 6, 
 MIX_T1_4P25, MIX_T2_4P5 = 1, 2
 MX_INT4, MX_FP4_E2M1 = 0, 1
 MIX_DT_F32, MIX_DT_BF16 = 0, 1
-MIX_ASYM_ZERO, MX_SCALE_FLOOR = 1, 2
+MIX_ASYM_ZERO, MX_SCALE_FLOOR, MX_SCALE_TIGHT = 1, 2, 4
 MIX_EPI_NONE, MIX_EPI_MIX_T1, MIX_EPI_MIX_T2, MIX_EPI_MXINT4, MIX_EPI_MXFP4 = 0, 1, 2, 3, 4
 MIX_GEMM_AUTO, MIX_GEMM_TCGEN05, MIX_GEMM_SHIFTADD, MIX_GEMM_TCGEN05_STAGED, MIX_GEMM_TCGEN05_FUSED = 0, 1, 2, 3, 4
 KSMOOTH_COMPUTE, KSMOOTH_APPLY_FROZEN = 0, 1
 
-EXPORTS = ["mix_codes_bytes", "mix_shared_bytes", "mx_scales_bytes", "mix_quantize", "mx_quantize",
+EXPORTS = ["mix_codes_bytes", "mix_shared_bytes", "mx_scales_bytes", "mix_quantize", "mix_auto_ebias",
+           "mix_quantize_auto", "mx_quantize",
            "mix_dequantize", "mx_dequantize", "mix_mx_gemm_workspace_bytes", "mix_mx_gemm",
            "ksmooth_workspace_bytes", "ksmooth_kv", "ksmooth_kv_noalloc", "mix_status_str", "mix_device_error",
            "mix_version"]
@@ -68,6 +69,8 @@ def _load():
         "mix_shared_bytes": (S, [I, I64, I64]),
         "mx_scales_bytes": (S, [I64, I64]),
         "mix_quantize": (I, [P, I, I64, I64, I64, I, I, U, P, P, P]),
+        "mix_auto_ebias": (I, [P, I, I64, I64, I64, P, P]),
+        "mix_quantize_auto": (I, [P, I, I64, I64, I64, I, U, P, P, P, P]),
         "mx_quantize": (I, [P, I, I64, I64, I64, I, I, U, P, P, P]),
         "mix_dequantize": (I, [P, P, I64, I64, I, I, P, P]),
         "mx_dequantize": (I, [P, P, I64, I64, I, P, P]),
@@ -144,6 +147,15 @@ def mix_quantize(x, rows, k, ld, mix_type, ebias, flags, codes, shared, stream=N
                             _ptr(shared), _stream(stream)), "mix_quantize")
 
 
+def mix_auto_ebias(x, rows, k, ld, ebias, stream=None) -> None:
+    _check(lib.mix_auto_ebias(_ptr(x), _dtype(x), rows, k, ld, _ptr(ebias), _stream(stream)), "mix_auto_ebias")
+
+
+def mix_quantize_auto(x, rows, k, ld, mix_type, flags, codes, shared, ebias, stream=None) -> None:
+    _check(lib.mix_quantize_auto(_ptr(x), _dtype(x), rows, k, ld, mix_type, flags, _ptr(codes), _ptr(shared),
+                                 _ptr(ebias), _stream(stream)), "mix_quantize_auto")
+
+
 def mx_quantize(x, rows, cols, ld, axis, mx_type, flags, codes, scales, stream=None) -> None:
     _check(lib.mx_quantize(_ptr(x), _dtype(x), rows, cols, ld, axis, mx_type, flags, _ptr(codes),
                            _ptr(scales), _stream(stream)), "mx_quantize")
@@ -210,6 +222,18 @@ def quantize_mix(x: torch.Tensor, mix_type: int = MIX_T2_4P5, ebias: int = -8, f
                          device=x.device)
     mix_quantize(x, rows, k, x.stride(0), mix_type, ebias, flags, codes, shared, stream)
     return codes, shared
+
+
+def quantize_mix_auto(x: torch.Tensor, mix_type: int = MIX_T2_4P5, flags: int = MIX_ASYM_ZERO, stream=None):
+    """Two-pass MiX quantiser -> (codes, shared, ebias int32 [1] on the device)."""
+    rows, k = x.shape
+    assert x.stride(1) == 1
+    codes = torch.empty((rows, k // 2), dtype=torch.uint8, device=x.device)
+    shared = torch.empty((rows, k // 32), dtype=torch.uint8 if mix_type == MIX_T1_4P25 else torch.int16,
+                         device=x.device)
+    ebias = torch.empty((1,), dtype=torch.int32, device=x.device)
+    mix_quantize_auto(x, rows, k, x.stride(0), mix_type, flags, codes, shared, ebias, stream)
+    return codes, shared, ebias
 
 
 def quantize_mx(x: torch.Tensor, axis: int, mx_type: int, flags: int = 0, stream=None):

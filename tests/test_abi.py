@@ -56,6 +56,15 @@ def test_validation_rejects_before_launch(mix):
     assert L.mix_quantize(None, 1, 0, 64, 64, 2, -8, 1, None, None, None) == mix.MIX_OK  # empty: no-op
     assert L.mx_quantize(None, 1, 48, 64, 64, 0, 1, 0, None, None, None) == mix.MIX_ERR_SHAPE
     assert L.mx_quantize(None, 1, 64, 64, 64, 2, 1, 0, None, None, None) == mix.MIX_ERR_INVALID_ARG
+    # floor and tight rules together; an unknown flag bit
+    assert L.mx_quantize(None, 1, 64, 64, 64, 1, 1, 6, None, None, None) == mix.MIX_ERR_INVALID_ARG
+    assert L.mx_quantize(None, 1, 64, 64, 64, 1, 1, 8, None, None, None) == mix.MIX_ERR_INVALID_ARG
+    # automatic ebias: the result pointer is required, k % 32, alignment of the result int
+    assert L.mix_auto_ebias(None, 1, 4, 64, 64, None, None) == mix.MIX_ERR_INVALID_ARG
+    assert L.mix_auto_ebias(None, 1, 4, 40, 40, 16, None) == mix.MIX_ERR_SHAPE
+    assert L.mix_auto_ebias(None, 1, 4, 64, 64, 18, None) == mix.MIX_ERR_ALIGN
+    assert L.mix_quantize_auto(None, 1, 4, 64, 64, 2, 2, None, None, 16, None) == mix.MIX_ERR_INVALID_ARG
+    assert L.mix_quantize_auto(None, 1, 4, 64, 64, 3, 1, None, None, 16, None) == mix.MIX_ERR_INVALID_ARG
     d = mix.GemmDesc()
     d.M, d.N, d.K, d.batch, d.b_group = 8, 64, 48, 1, 1
     d.a_type, d.b_type = 2, 1
@@ -64,6 +73,9 @@ def test_validation_rejects_before_launch(mix):
     assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_INVALID_ARG
     d.batch, d.epi, d.N = 1, mix.MIX_EPI_MIX_T2, 48
     assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_SHAPE
+    d.N, d.epi, d.epi_flags = 64, mix.MIX_EPI_MXFP4, mix.MX_SCALE_FLOOR | mix.MX_SCALE_TIGHT
+    assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_INVALID_ARG
+    d.epi, d.epi_flags = mix.MIX_EPI_MIX_T2, 1
     assert L.ksmooth_kv(None, 1, 16, 4, 12, 48, None, 0, None, None, 0, None) in (mix.MIX_ERR_SHAPE,
                                                                                  mix.MIX_ERR_INVALID_ARG)
 

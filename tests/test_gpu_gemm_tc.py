@@ -119,16 +119,18 @@ def test_tiny_end_to_end_config(mix, orc):
 
 
 @pytest.mark.parametrize("algo", ALGOS)
-@pytest.mark.parametrize("epi", [1, 2, 3, 4])
-def test_tc_epilogue_formats(mix, orc, epi, algo):
+@pytest.mark.parametrize("epi,mx_flags", [(1, 0), (2, 0), (3, 0), (4, 0), (3, 4), (4, 4), (4, 2)])
+def test_tc_epilogue_formats(mix, orc, epi, mx_flags, algo):
+    """The fused output quantiser (MiX, MX with the ceil, tight or floor
+    exponent rule) equals the oracle quantiser applied to the GPU's own C."""
     M, N, K = 200, 512, 640
     ac, ash, bc, bs = operands(orc, 11 + epi, M, N, K, 1, 0)
     c, oc, osh = run_tc(mix, ac, ash, 1, bc, bs, 0, M, N, K, epi=epi, epi_ebias=-6,
-                        epi_flags=1 if epi <= 2 else 0, algo=algo)
+                        epi_flags=1 if epi <= 2 else mx_flags, algo=algo)
     if epi <= 2:
         rc, rs = orc.mix_quantize(c[0], epi, -6, 1)
     else:
-        rc, rs = orc.mx_quantize(c[0], 1, 0 if epi == 3 else 1, 0)
+        rc, rs = orc.mx_quantize(c[0], 1, 0 if epi == 3 else 1, mx_flags)
     assert np.array_equal(oc[0], rc) and np.array_equal(osh[0].astype(rs.dtype), rs)
 
 

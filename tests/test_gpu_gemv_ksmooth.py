@@ -55,8 +55,8 @@ def test_shiftadd_batched_gqa(mix, orc):
     assert row_rel_err(to_host(c), ref) < 1e-5
 
 
-@pytest.mark.parametrize("epi", [1, 2, 3, 4])
-def test_shiftadd_epilogue_codes_are_quantised_c(mix, orc, epi):
+@pytest.mark.parametrize("epi,mx_flags", [(1, 0), (2, 0), (3, 0), (4, 0), (3, 4), (4, 4)])
+def test_shiftadd_epilogue_codes_are_quantised_c(mix, orc, epi, mx_flags):
     """The fused output quantiser's planes equal the oracle quantiser applied
     to the GPU's own fp32 C, bit for bit."""
     import torch
@@ -66,7 +66,7 @@ def test_shiftadd_epilogue_codes_are_quantised_c(mix, orc, epi):
     oc = torch.empty((M, N // 2), dtype=torch.uint8, device="cuda")
     osh = torch.empty((M, N // 32), dtype=torch.int16 if epi == 2 else torch.uint8, device="cuda")
     d = mix.gemm_desc(M, N, K, to_dev(ac), to_dev(ash), 2, -8, to_dev(bc), to_dev(bs), 1, c=c, epi=epi,
-                      epi_ebias=-6, epi_flags=1 if epi <= 2 else 0, out_codes=oc, out_shared=osh,
+                      epi_ebias=-6, epi_flags=1 if epi <= 2 else mx_flags, out_codes=oc, out_shared=osh,
                       algo=mix.MIX_GEMM_SHIFTADD)
     mix.gemm(d)
     torch.cuda.synchronize()
@@ -74,7 +74,7 @@ def test_shiftadd_epilogue_codes_are_quantised_c(mix, orc, epi):
     if epi <= 2:
         rc, rs = orc.mix_quantize(ch, epi, -6, 1)
     else:
-        rc, rs = orc.mx_quantize(ch, 1, 0 if epi == 3 else 1, 0)
+        rc, rs = orc.mx_quantize(ch, 1, 0 if epi == 3 else 1, mx_flags)
     assert np.array_equal(to_host(oc), rc) and np.array_equal(to_host(osh).astype(rs.dtype), rs)
 
 

@@ -153,6 +153,7 @@ def test_mx_tiny_weights(mix, orc, axis, t):
     x = w if axis == 0 else np.ascontiguousarray(w.T)
     check_mx(mix, orc, x, axis, t)
     check_mx(mix, orc, x, axis, t, flags=2)
+    check_mx(mix, orc, x, axis, t, flags=4)
 
 
 @pytest.mark.parametrize("t", [0, 1])
@@ -194,7 +195,7 @@ def test_mx_edge_values(mix, orc):
     rows.append(np.linspace(-6.5, 0.25, 32).astype(np.float32))
     x = np.stack(rows)                      # 8 rows: the transposed copy has ld = 8
     for t in (0, 1):
-        for flags in (0, 2):
+        for flags in (0, 2, 4):
             check_mx(mix, orc, x, 1, t, flags)
             check_mx(mix, orc, np.ascontiguousarray(x.T), 0, t, flags)
 
@@ -207,3 +208,74 @@ def test_mx_dequantize_matches_oracle(mix, orc):
         out = torch.empty((96, 128), dtype=torch.float32, device="cuda")
         mix.mx_dequantize(to_dev(c), to_dev(s), 96, 128, t, out)
         assert np.array_equal(to_host(out).astype(np.float64), orc.mx_dequantize(c, s, t))
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_mx_tight_rule_boundaries(mix, orc, bf16):
+    """Tight shared exponent on blocks whose maximum sits on, just above and
+    just below the rule's switch points (significand 1.5 for MXFP4, 1.75 for
+    MXINT4), on powers of two and on subnormal and near-overflow maxima."""
+    rng = np.random.default_rng(31)
+    sig = [1.0, 1.0 + 2 ** -7, 1.25, 1.5 - 2 ** -7, 1.5, 1.5 + 2 ** -7, 1.75 - 2 ** -7, 1.75,
+           1.75 + 2 ** -7, 2 - 2 ** -7]
+    maxima = [s * 2.0 ** e for e in (-133, -126, -40, -1, 0, 3, 60, 127) for s in sig]
+    x = (rng.uniform(-1, 1, (len(maxima), 64)) * np.array(maxima)[:, None]).astype(np.float32)
+    for r, a in enumerate(maxima):
+        x[r, rng.integers(32)] = a if r % 2 else -a
+        x[r, 32 + rng.integers(32)] = a
+    x = synth.to_bf16_bits(x) if bf16 else x
+    for t in (0, 1):
+        check_mx(mix, orc, x, 1, t, 4)
+        check_mx(mix, orc, np.ascontiguousarray(x.T), 0, t, 4)
+
+
+def gpu_auto_ebias(mix, x_np, ld=None):
+    import torch
+    rows, k = x_np.shape
+    xd = to_dev(x_np)
+    if ld is not None:   # the same tensor read through a wider row stride
+        wide = torch.zeros((rows, ld), dtype=xd.dtype, device="cuda")
+        wide[:, :k] = xd
+        xd = wide
+    e = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    mix.mix_auto_ebias(xd, rows, k, xd.stride(0) if rows else k, e)
+    return int(to_host(e)[0])
+
+
+def auto_ebias_cases():
+    a = synth.vlm_activations(3, 1, 96, 512, visual_rows=64, n_outlier=4)
+    z = np.zeros((4, 64), np.float32)
+    special = np.zeros((3, 96), np.float32)
+    special[0, 5], special[1, 40], special[2, 70] = 3.0, -2.0 ** -7, 15.5   # 15.5 rounds up: carry
+    inf_nan = special.copy()
+    inf_nan[2, 70], inf_nan[2, 71], inf_nan[0, 1] = np.inf, np.nan, -np.inf
+    tiny = (np.random.default_rng(4).standard_normal((5, 32)) * 1e-42).astype(np.float32)
+    huge = np.full((2, 32), 3e38, np.float32)
+    return {"activations_f32": synth.to_f32(a), "activations_bf16": synth.to_bf16_bits(a),
+            "zeros": z, "carry": special, "inf_nan": inf_nan, "inf_nan_bf16": synth.to_bf16_bits(inf_nan),
+            "subnormal": tiny, "huge": huge, "empty": np.zeros((0, 64), np.float32)}
+
+
+@pytest.mark.parametrize("case", list(auto_ebias_cases()))
+def test_auto_ebias_matches_oracle(mix, orc, case):
+    x = auto_ebias_cases()[case]
+    want = orc.mix_auto_ebias(x) if x.shape[0] else -8
+    assert gpu_auto_ebias(mix, x) == want
+    if x.shape[0]:
+        assert gpu_auto_ebias(mix, x, ld=x.shape[1] + 32) == want
+
+
+@pytest.mark.parametrize("t", [1, 2])
+def test_quantize_auto_matches_oracle(mix, orc, t):
+    """Two passes on one stream, no host round trip: the codes are the oracle's
+    quantiser run with the oracle's automatic ebias; every block stays
+    unclamped from above and the largest lands on code 15."""
+    a = synth.vlm_activations(8, 2, 600, 1024, visual_rows=500, n_outlier=8) * 300.0
+    for x in (synth.to_bf16_bits(a), synth.to_f32(a)):
+        eb = orc.mix_auto_ebias(x)
+        c_ref, s_ref = orc.mix_quantize(x, t, eb, 1)
+        c, s, e = mix.quantize_mix_auto(to_dev(x), t)
+        assert int(to_host(e)[0]) == eb
+        assert np.array_equal(to_host(c), c_ref)
+        assert np.array_equal(to_host(s).astype(s_ref.dtype), s_ref)
+        assert int(np.max(s_ref.astype(np.int64) & 0xF)) == 15
