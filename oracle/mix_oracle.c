@@ -475,7 +475,7 @@ int orc_gemm_blk(const uint8_t* a_codes, const void* a_shared, int a_type, int a
             }
             block += S * (8 + m3s[sb]);     /* x (1.mshared) in eighths */
             if (b_block == 16 && (sb & 1)) {  /* end of a 16-element half */
-              int X = (int)bs[n * nbb + 2 * b + (sb >> 1)] - 127;
+              int X = (int)bs[n * nbb + 2 * b + (g_mutation == 10 ? 0 : (sb >> 1))] - 127;
               acc += ldexp((double)block, emax + X - 10 - cB);
               block = 0;
             }

@@ -580,12 +580,83 @@ def pin_auto_ebias(orc):
             assert int(np.max(sh.astype(np.int64) & 0xF)) == 15
 
 
+def pin_mx_g16(orc):
+    """MXINT4g16 / MXFP4g16 (Method and Key results sections: the weight
+    formats of MiX-INT4g16 and the g16 MX baselines): one E8M0 scale per 16
+    elements.  Every 16-element block obeys the 32-block rules (ceil for
+    MXFP4, floor for MXINT4; element codes by brute force), and equals the
+    32-block quantiser applied to that block padded with zeros."""
+    w = synth.to_bf16_bits(synth.gaussian_weights(9, 4, 96, 40))        # K = 96, N = 40
+    wf = synth.bf16_bits_to_f32(w)
+    for t in (0, 1):
+        for flags in (0, 4):
+            c16, s16 = orc.mx_quantize(w, 0, t, flags, block=16)
+            assert c16.shape == (40, 48) and s16.shape == (40, 6)
+            nib = unpack_nibbles(c16)
+            for n in range(40):
+                for b in range(6):
+                    blk = [Fraction(float(v)) for v in wf[16 * b: 16 * b + 16, n]]
+                    pad = np.zeros((32, 1), np.float32)
+                    pad[:16, 0] = wf[16 * b: 16 * b + 16, n]
+                    cp, sp = orc.mx_quantize(pad, 0, t, flags)
+                    assert s16[n, b] == sp[0, 0]
+                    assert np.array_equal(nib[n, 16 * b: 16 * b + 16], unpack_nibbles(cp)[0, :16])
+                    amax = max(abs(v) for v in blk)
+                    f, m = exact_f_m(amax)
+                    if flags == 0:
+                        want = (f - 2 + (m > 1)) if t == 1 else f
+                    else:
+                        want = (f - 2 + (m > Fraction(3, 2))) if t == 1 else f + (m > Fraction(7, 4))
+                    X = int(s16[n, b]) - 127
+                    assert X == want
+                    step = Fraction(2) ** (X if t == 1 else X - 2)
+                    for i in range(16):
+                        assert int(nib[n, 16 * b + i]) == brute_mx_code(blk[i] / step, t)
+            d = orc.mx_dequantize(c16, s16, t, block=16)
+            for n in range(0, 40, 7):
+                for kk in range(96):
+                    assert Fraction(d[n, kk]) == frac_mx_value(int(nib[n, kk]), s16[n, kk // 16], t)
+
+
+def pin_gemm_g16(orc):
+    """Eq. (6) with g16 weights: each 32-block of the MiX operand meets two
+    weight scales, one per 16-element half.  Exact against the sum of
+    products of dequantised values; equal to the 32-block matmul when both
+    halves carry the 32-block's scale."""
+    M, N, K = 3, 5, 96
+    a = synth.to_bf16_bits(synth.vlm_activations(7, 0, M, K, visual_rows=2))
+    w = synth.to_bf16_bits(synth.gaussian_weights(7, 1, K, N) * np.repeat(np.exp2(np.arange(6) % 4 - 1.5), 16)[:, None])
+    for at in (1, 2):
+        ac, ash = orc.mix_quantize(a, at, -8, 1)
+        an = unpack_nibbles(ac)
+        for bt in (0, 1):
+            bc, bs = orc.mx_quantize(w, 0, bt, 0, block=16)
+            assert np.any(bs[:, 0::2] != bs[:, 1::2])          # the halves' scales differ
+            bn = unpack_nibbles(bc)
+            c = orc.gemm(ac, ash, at, -8, bc, bs, bt, b_block=16)
+            for m in range(M):
+                for n in range(N):
+                    tot, mag_sum = Fraction(0), Fraction(0)
+                    for kk in range(K):
+                        ec, m3s = (t1_fields if at == 1 else t2_fields)(ash[m, kk // 32])
+                        av = mix_code_value(int(an[m, kk]), ec - 8, m3s[(kk % 32) // 8])
+                        p = av * frac_mx_value(int(bn[n, kk]), bs[n, kk // 16], bt)
+                        tot += p
+                        mag_sum += abs(p)
+                    # half-block sums are exact; only the fp64 additions across them round
+                    assert abs(Fraction(c[m, n]) - tot) <= mag_sum * Fraction(1, 2 ** 50), (at, bt, m, n)
+            bc32, bs32 = orc.mx_quantize(w, 0, bt)
+            c32 = orc.gemm(ac, ash, at, -8, bc32, bs32, bt)
+            c16 = orc.gemm(ac, ash, at, -8, bc32, np.repeat(bs32, 2, axis=1), bt, b_block=16)
+            assert np.max(np.abs(c16 - c32)) <= np.max(np.abs(c32)) * 2.0 ** -50
+
+
 ALL_PINS = [pin_bit_accounting, pin_dequant_special_values, pin_refinement_brute_force,
             pin_exhaustive_sweep, pin_asymmetric_zero, pin_round_trip,
             pin_nonfinite_and_zero_blocks, pin_e2m1_and_int4_brute_force, pin_mx_scale_rule,
             pin_mx_axis_consistency, pin_gemm_eq6_exact, pin_gemm_against_dequant_matmul,
             pin_gemm_reduces_to_mx_dot, pin_gemm_batch_gqa_indexing, pin_ksmooth,
-            pin_mx_tight_rule, pin_auto_ebias]
+            pin_mx_tight_rule, pin_auto_ebias, pin_mx_g16, pin_gemm_g16]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -599,15 +670,16 @@ def test_pin(orc, pin):
 # 4 refinement search removed, 5 MXFP4 floor instead of ceil, 6 FP4 exponent
 # dropped from the Eq. (6) shift, 7 smoothing adds the mean, 8 the tight MX
 # exponent steps past a block maximum on the boundary, 9 the automatic ebias
-# drops the rounding carry.
+# drops the rounding carry, 10 the g16 matmul reads the first half's scale
+# for both halves.
 FAST_PINS = [pin_dequant_special_values, pin_round_trip, pin_asymmetric_zero,
              pin_e2m1_and_int4_brute_force, pin_mx_scale_rule, pin_gemm_eq6_exact,
              pin_gemm_against_dequant_matmul, pin_ksmooth, pin_nonfinite_and_zero_blocks,
-             pin_mx_tight_rule, pin_auto_ebias,
+             pin_mx_tight_rule, pin_auto_ebias, pin_gemm_g16,
              lambda o: pin_refinement_brute_force(o, n_blocks=40)]
 
 
-@pytest.mark.parametrize("mutation", [1, 2, 3, 4, 5, 6, 7, 8, 9])
+@pytest.mark.parametrize("mutation", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
 def test_planted_mistakes_are_caught(orc, mutation):
     failed = []
     try:
