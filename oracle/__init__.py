@@ -54,9 +54,14 @@ def lib():
         L.orc_mx_quantize_blk.argtypes = [P, I, I64, I64, I64, I, I, U, I, P, P]
         L.orc_mx_dequantize_blk.argtypes = [P, P, I64, I64, I, I, P]
         L.orc_gemm_blk.argtypes = [P, P, I, I, P, P, I, I, I64, I64, I64, I64, I64, P]
+        L.orc_nvfp4_quantize.argtypes = [P, I, I64, I64, I64, P, P, P]
+        L.orc_nvfp4_dequantize.argtypes = [P, P, ctypes.c_float, I64, I64, P]
+        L.orc_underflow_count.argtypes = [P, I, I64, I64, I64, P, I]
+        L.orc_underflow_count.restype = I64
         for f in ("orc_mix_quantize", "orc_mix_dequantize", "orc_mx_quantize",
                   "orc_mx_dequantize", "orc_gemm", "orc_ksmooth_mean", "orc_ksmooth_apply",
-                  "orc_mix_auto_ebias", "orc_mx_quantize_blk", "orc_mx_dequantize_blk", "orc_gemm_blk"):
+                  "orc_mix_auto_ebias", "orc_mx_quantize_blk", "orc_mx_dequantize_blk", "orc_gemm_blk",
+                  "orc_nvfp4_quantize", "orc_nvfp4_dequantize"):
             getattr(L, f).restype = ctypes.c_int
         L.orc_set_mutation.restype = None
         _lib = L
@@ -135,6 +140,37 @@ def mx_dequantize(codes: np.ndarray, scales: np.ndarray, mx_type: int, block: in
     out = np.zeros((n, kh * 2), dtype=np.float64)
     _check(lib().orc_mx_dequantize_blk(_ptr(codes), _ptr(scales), n, kh * 2, mx_type, block, _ptr(out)))
     return out
+
+
+def nvfp4_quantize(x: np.ndarray):
+    """x [rows, k] float32 or bf16 bits -> (codes [rows, k/2], E4M3 scales [rows, k/16], fp32 tensor scale)."""
+    x = np.ascontiguousarray(x)
+    rows, k = x.shape
+    codes = np.zeros((rows, k // 2), dtype=np.uint8)
+    scales = np.zeros((rows, k // 16), dtype=np.uint8)
+    ts = np.zeros(1, dtype=np.float32)
+    _check(lib().orc_nvfp4_quantize(_ptr(x), _dtype_of(x), rows, k, k, _ptr(codes), _ptr(scales), _ptr(ts)))
+    return codes, scales, ts[0]
+
+
+def nvfp4_dequantize(codes: np.ndarray, scales: np.ndarray, tensor_scale):
+    codes = np.ascontiguousarray(codes)
+    scales = np.ascontiguousarray(scales)
+    rows, kh = codes.shape
+    out = np.zeros((rows, kh * 2), dtype=np.float64)
+    _check(lib().orc_nvfp4_dequantize(_ptr(codes), _ptr(scales), float(tensor_scale), rows, kh * 2, _ptr(out)))
+    return out
+
+
+UF_MIX, UF_MXINT4, UF_E2M1 = 0, 1, 2
+
+
+def underflow_count(x: np.ndarray, codes: np.ndarray, fmt: int) -> int:
+    """Finite nonzero elements of x [rows, k] whose code in codes [rows, k/2] is a zero code."""
+    x = np.ascontiguousarray(x)
+    codes = np.ascontiguousarray(codes)
+    rows, k = x.shape
+    return int(lib().orc_underflow_count(_ptr(x), _dtype_of(x), rows, k, k, _ptr(codes), fmt))
 
 
 def gemm(a_codes, a_shared, a_type, a_ebias, b_codes, b_scales, b_type, b_group: int = 1, b_block: int = 32):

@@ -415,6 +415,119 @@ int orc_mx_dequantize(const uint8_t* codes, const uint8_t* scales, int64_t n_row
 }
 
 /* ----------------------------------------------------------------------- */
+/* NVFP4 (a comparison format of the pages: blocks of 16 E2M1 elements, an  */
+/* E4M3 block scale and one FP32 tensor scale)                              */
+/* ----------------------------------------------------------------------- */
+
+/* Value of a non-negative E4M3 code (no NaN: codes up to 0x7E). */
+static double e4m3_value(int code) {
+  int e = (code >> 3) & 15, m = code & 7;
+  return e ? ldexp(1.0 + m / 8.0, e - 7) : ldexp(m / 8.0, -6);
+}
+
+/* E4M3 code nearest to t >= 0 (ties to the even code), saturating at 448. */
+static int e4m3_code_of(double t) {
+  if (!(t < 448.0)) return 0x7E;
+  int best = 0;
+  for (int c = 1; c <= 0x7E; ++c) {
+    if (g_mutation == 11 && e4m3_value(c) > t) break;   /* planted: truncation */
+    double e0 = fabs(t - e4m3_value(best)), e1 = fabs(t - e4m3_value(c));
+    if (e1 < e0 || (e1 == e0 && (c & 1) == 0)) best = c;
+  }
+  return best;
+}
+
+/* x: rows x k (ld elements), k % 16 == 0.  All arithmetic is fp32 with one
+ * rounding per operation, in this order:
+ *   amax_t = the largest finite |x| of the tensor (NaN and +-Inf left out);
+ *   amax_b = the block's largest |x| (NaN left out; +-Inf gives sb = 448);
+ *   s_t    = amax_t / 2688 (2688 = 6 * 448; 1 when amax_t is 0; the smallest
+ *            positive float if the quotient underflows), stored as fp32;
+ *   per 16-block: t = (amax_b / s_t) / 6, its E4M3 code sb (nearest, ties
+ *            even, saturating at 448);
+ *   d = e4m3(sb) * s_t, and each element's E2M1 code of x / d (nearest,
+ *            ties even, saturating at 6; NaN codes +0, +-Inf saturates).
+ * A block whose sb is 0 stores zero codes.  codes rows x k/2, scales rows x
+ * k/16 E4M3 bytes, *tensor_scale = s_t. */
+int orc_nvfp4_quantize(const void* x, int dtype, int64_t rows, int64_t k, int64_t ld,
+                       uint8_t* codes, uint8_t* scales, float* tensor_scale) {
+  if (k % 16 != 0) return 1;
+  float amax_t = 0.0f;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t i = 0; i < k; ++i) {
+      double a = mag(load_elem(x, dtype, r * ld + i));
+      if (!isinf(a) && (float)a > amax_t) amax_t = (float)a;
+    }
+  float s_t = 1.0f;
+  if (amax_t > 0.0f) {
+    volatile float q = amax_t / 2688.0f;
+    s_t = q > 0.0f ? q : 0x1p-149f;
+  }
+  *tensor_scale = s_t;
+  int64_t nb = k / 16;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t b = 0; b < nb; ++b) {
+      float amax_b = 0.0f, v[16];
+      for (int i = 0; i < 16; ++i) {
+        v[i] = (float)load_elem(x, dtype, r * ld + b * 16 + i);
+        double a = mag(v[i]);
+        if ((float)a > amax_b) amax_b = (float)a;     /* +-Inf included: its block saturates */
+      }
+      volatile float t1 = amax_b / s_t;
+      volatile float t = t1 / 6.0f;
+      int sb = e4m3_code_of((double)t);
+      scales[r * nb + b] = (uint8_t)sb;
+      volatile float d = (float)e4m3_value(sb) * s_t;
+      uint8_t* out = codes + r * (k / 2) + b * 8;
+      for (int j = 0; j < 8; ++j) {
+        int c[2];
+        for (int h = 0; h < 2; ++h) {
+          float xv = v[2 * j + h];
+          if (sb == 0 || isnan(xv)) { c[h] = 0; continue; }
+          if (isinf(xv)) { c[h] = (xv < 0 ? 8 : 0) | 7; continue; }
+          volatile float y = xv / d;
+          c[h] = e2m1_code((double)y);
+        }
+        out[j] = (uint8_t)(c[0] | (c[1] << 4));
+      }
+    }
+  return 0;
+}
+
+int orc_nvfp4_dequantize(const uint8_t* codes, const uint8_t* scales, float tensor_scale, int64_t rows,
+                         int64_t k, double* out) {
+  if (k % 16 != 0) return 1;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t i = 0; i < k; ++i) {
+      int c = nibble(codes + r * (k / 2), i);
+      double g = E2M1_GRID[c & 7] * e4m3_value(scales[r * (k / 16) + i / 16]) * (double)tensor_scale;
+      out[r * k + i] = (c & 8) ? -g : g;
+    }
+  return 0;
+}
+
+/* ----------------------------------------------------------------------- */
+/* Dead-zone count: nonzero inputs whose code is zero                       */
+/* ----------------------------------------------------------------------- */
+
+/* Counts elements of x (rows x k, ld) that are finite and nonzero but whose
+ * 4-bit code in `codes` (rows x k/2) is a zero code: MiX 0x7 (fmt 0), MXINT4
+ * 0 (fmt 1), E2M1 +-0 for MXFP4 and NVFP4 (fmt 2). */
+int64_t orc_underflow_count(const void* x, int dtype, int64_t rows, int64_t k, int64_t ld,
+                            const uint8_t* codes, int fmt) {
+  int64_t n = 0;
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t i = 0; i < k; ++i) {
+      double v = load_elem(x, dtype, r * ld + i);
+      if (isnan(v) || v == 0.0 || isinf(v)) continue;
+      int c = nibble(codes + r * (k / 2), i);
+      int zero = fmt == 0 ? c == 0x7 : fmt == 1 ? c == 0 : (c & 7) == 0;
+      n += zero;
+    }
+  return n;
+}
+
+/* ----------------------------------------------------------------------- */
 /* A-MiX x W-MX block matmul, Eq. (6)                                       */
 /* ----------------------------------------------------------------------- */
 

@@ -651,12 +651,119 @@ def pin_gemm_g16(orc):
             assert np.max(np.abs(c16 - c32)) <= np.max(np.abs(c32)) * 2.0 ** -50
 
 
+def e4m3_magnitudes():
+    """Every finite non-negative E4M3 value by code (0 .. 0x7E), exactly."""
+    out = []
+    for c in range(0x7F):
+        e, m = c >> 3, c & 7
+        out.append(Fraction(m, 8) * Fraction(2) ** -6 if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7))
+    return out
+
+
+def brute_e4m3(t: Fraction) -> int:
+    vals = e4m3_magnitudes()
+    if t >= 448:
+        return 0x7E
+    return min(range(0x7F), key=lambda c: (abs(t - vals[c]), c % 2))
+
+
+def pin_nvfp4(orc):
+    """NVFP4 (named by the pages as the 16-element, E4M3-block-scale,
+    FP32-tensor-scale comparison format): block scales are the nearest E4M3
+    (ties even, saturating) of (amax_b / s_t) / 6 with s_t = amax_t / 2688;
+    elements the nearest E2M1 of x / (e4m3(sb) s_t).  Checked by enumerating
+    both grids on exact rationals, by scale equivariance and by the
+    reconstruction bound."""
+    vals = e4m3_magnitudes()
+    # an anchor element 2688 makes s_t exactly 1, so t = amax_b / 6 exactly;
+    # targets: every E4M3 value, every midpoint between neighbours, and
+    # points just off the midpoints
+    targets = []
+    for c in range(0x7E):
+        lo, hi = vals[c], vals[c + 1]
+        mid = (lo + hi) / 2
+        targets += [lo, mid, mid + (hi - lo) / 64, mid - (hi - lo) / 64]
+    targets += [Fraction(448)]
+    nb = len(targets) + 1
+    x = np.zeros((1, 16 * nb), np.float32)
+    x[0, 0] = 2688.0
+    for i, t in enumerate(targets):
+        x[0, 16 * (i + 1) + 5] = np.float32(float(6 * t))
+        assert Fraction(float(x[0, 16 * (i + 1) + 5])) == 6 * t      # exactly representable
+    codes, scales, ts = orc.nvfp4_quantize(x)
+    assert ts == np.float32(1.0)
+    for i, t in enumerate(targets):
+        assert int(scales[0, i + 1]) == brute_e4m3(t), (float(t), int(scales[0, i + 1]), brute_e4m3(t))
+    # element codes on random blocks (general s_t), both grids by enumeration
+    rng = np.random.default_rng(41)
+    xr = (rng.standard_normal((6, 64)) * np.exp2(rng.integers(-8, 8, (6, 1)))).astype(np.float32)
+    xr[2, 5] = 0.0
+    codes, scales, ts = orc.nvfp4_quantize(xr)
+    amax_t = np.float32(np.max(np.abs(xr)))
+    assert ts == np.float32(amax_t / np.float32(2688.0))
+    grid = e2m1_magnitudes()
+    nib = unpack_nibbles(codes)
+    for r in range(6):
+        for b in range(4):
+            blk = xr[r, 16 * b: 16 * b + 16]
+            t = np.float32(np.float32(np.max(np.abs(blk)) / ts) / np.float32(6.0))
+            sb = brute_e4m3(Fraction(float(t)))
+            assert int(scales[r, b]) == sb
+            d = np.float32(np.float32(float(vals[sb])) * ts)
+            for i in range(16):
+                y = Fraction(float(np.float32(blk[i] / d)))
+                c = 7 if abs(y) >= 6 else min(range(8), key=lambda j: (abs(abs(y) - grid[j]), j % 2))
+                want = c | (8 if (y < 0 and c) else 0)
+                assert int(nib[r, 16 * b + i]) == want
+    # scale equivariance: x 2^j keeps codes and block scales, s_t scales exactly
+    for j in (-20, 3, 40):
+        c2, s2, t2 = orc.nvfp4_quantize((xr * np.float32(2.0 ** j)).astype(np.float32))
+        assert np.array_equal(c2, codes) and np.array_equal(s2, scales) and t2 == np.float32(ts * 2.0 ** j)
+    # reconstruction: within half an E2M1 step (at most 1 unit of d) plus saturation
+    deq = orc.nvfp4_dequantize(codes, scales, ts)
+    for r in range(6):
+        for b in range(4):
+            d = float(vals[int(scales[r, b])]) * float(ts)
+            err = np.abs(deq[r, 16 * b: 16 * b + 16] - xr[r, 16 * b: 16 * b + 16].astype(np.float64))
+            assert np.all(err <= d * 1.0 + 1e-30)
+    # +-Inf saturates its block, NaN codes zero, an all-zero tensor gives s_t = 1
+    xs = np.zeros((1, 32), np.float32)
+    xs[0, 3], xs[0, 4], xs[0, 20] = np.inf, np.nan, 1.0
+    c3, s3, t3 = orc.nvfp4_quantize(xs)
+    n3 = unpack_nibbles(c3)
+    assert t3 == np.float32(1.0 / 2688.0) and int(s3[0, 0]) == 0x7E and n3[0, 3] == 7 and n3[0, 4] == 0
+    assert orc.nvfp4_quantize(np.zeros((2, 32), np.float32))[2] == np.float32(1.0)
+
+
+def pin_underflow_count(orc):
+    """The dead-zone count (Key results section's key-underflow comparison,
+    made synthetic): finite nonzero inputs whose code is a zero code, equal to
+    the count of nonzero inputs that dequantise to exactly zero, per format;
+    and a hand-counted MXFP4 block."""
+    x = np.zeros((1, 32), np.float32)
+    x[0, :6] = [4.0, 0.2, 0.24, 0.26, -0.25, 0.0]          # X = 0: 0.2, 0.24 and -0.25 fall to zero
+    c, s = orc.mx_quantize(x, 1, 1)
+    assert orc.underflow_count(x, c, orc.UF_E2M1) == 3
+    a = synth.attention_qkv(3, 256, n_outlier=4)[1].reshape(-1, 128)           # K [tokens * heads, 128]
+    a = synth.to_bf16_bits(a)
+    af = synth.bf16_bits_to_f32(a).astype(np.float64)
+    nz = (af != 0)
+    for fmt, codes, deq in (
+            (orc.UF_MIX,) + (lambda cs: (cs[0], orc.mix_dequantize(cs[0], cs[1], 2, -8)))(orc.mix_quantize(a, 2)),
+            (orc.UF_MXINT4,) + (lambda cs: (cs[0], orc.mx_dequantize(cs[0], cs[1], 0)))(orc.mx_quantize(a, 1, 0)),
+            (orc.UF_E2M1,) + (lambda cs: (cs[0], orc.mx_dequantize(cs[0], cs[1], 1)))(orc.mx_quantize(a, 1, 1)),
+            (orc.UF_E2M1,) + (lambda cs: (cs[0], orc.nvfp4_dequantize(*cs)))(orc.nvfp4_quantize(a))):
+        n = orc.underflow_count(a, codes, fmt)
+        assert n == int(np.sum(nz & (deq == 0))), fmt
+        assert n > 0
+
+
 ALL_PINS = [pin_bit_accounting, pin_dequant_special_values, pin_refinement_brute_force,
             pin_exhaustive_sweep, pin_asymmetric_zero, pin_round_trip,
             pin_nonfinite_and_zero_blocks, pin_e2m1_and_int4_brute_force, pin_mx_scale_rule,
             pin_mx_axis_consistency, pin_gemm_eq6_exact, pin_gemm_against_dequant_matmul,
             pin_gemm_reduces_to_mx_dot, pin_gemm_batch_gqa_indexing, pin_ksmooth,
-            pin_mx_tight_rule, pin_auto_ebias, pin_mx_g16, pin_gemm_g16]
+            pin_mx_tight_rule, pin_auto_ebias, pin_mx_g16, pin_gemm_g16, pin_nvfp4, pin_underflow_count]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -671,15 +778,15 @@ def test_pin(orc, pin):
 # dropped from the Eq. (6) shift, 7 smoothing adds the mean, 8 the tight MX
 # exponent steps past a block maximum on the boundary, 9 the automatic ebias
 # drops the rounding carry, 10 the g16 matmul reads the first half's scale
-# for both halves.
+# for both halves, 11 the E4M3 rounding of the NVFP4 block scale truncates.
 FAST_PINS = [pin_dequant_special_values, pin_round_trip, pin_asymmetric_zero,
              pin_e2m1_and_int4_brute_force, pin_mx_scale_rule, pin_gemm_eq6_exact,
              pin_gemm_against_dequant_matmul, pin_ksmooth, pin_nonfinite_and_zero_blocks,
-             pin_mx_tight_rule, pin_auto_ebias, pin_gemm_g16,
+             pin_mx_tight_rule, pin_auto_ebias, pin_gemm_g16, pin_nvfp4,
              lambda o: pin_refinement_brute_force(o, n_blocks=40)]
 
 
-@pytest.mark.parametrize("mutation", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10])
+@pytest.mark.parametrize("mutation", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11])
 def test_planted_mistakes_are_caught(orc, mutation):
     failed = []
     try:
