@@ -208,3 +208,46 @@ def ksmooth_apply(k: np.ndarray, mu: np.ndarray):
     out = np.zeros((t, h, d), dtype=np.float32)
     _check(lib().orc_ksmooth_apply(_ptr(k), _dtype_of(k), t, h, d, h * d, _ptr(mu), _ptr(out)))
     return out
+
+
+def decode_attention(q, k_cache_codes, k_cache_scales, v_codes, v_scales, tokens, sm_scale,
+                     k_new=None, k_mean=None, q_ebias=-8, p_ebias=-15):
+    """One decode step of MiX attention over an MX KV cache, in the order the
+    pages give (Method section, accelerator bullet: K-smoothing with the
+    frozen prefill mean, Q-K^T on the dual-format matmul, the softmax of the
+    SFU, the MiX requantisation of P, P-V on the dual-format matmul).
+
+    q: [HQ, D] float32 or bf16 bits.  K' cache: codes [T, HK, D/2], scales
+    [T, HK, D/32] (MXINT4 along D).  k_new: [HK, D] (float32 or bf16 bits) or
+    None; when given, K' = fp32(k_new) - k_mean is quantised to MXINT4 and
+    written to cache row tokens - 1 (the arrays are updated in place).
+    V: codes [HK, D, Tv/2], scales [HK, D, Tv/32] (MXINT4 along tokens, Tv a
+    multiple of 32 >= tokens).  Returns (O fp64 [HQ, D], P fp32 [HQ, tokens],
+    the MiX-4.5b planes of P over Tv tokens, S fp64 [HQ, tokens]).
+    """
+    HQ, D = q.shape
+    HK = k_cache_codes.shape[1]
+    G = HQ // HK
+    Tv = v_codes.shape[2] * 2
+    if k_new is not None:
+        kp = ksmooth_apply(np.ascontiguousarray(k_new).reshape(1, HK, D), k_mean.astype(np.float32))
+        c, s = mx_quantize(kp.reshape(HK, D).astype(np.float32), 1, MXINT4)
+        k_cache_codes[tokens - 1] = c
+        k_cache_scales[tokens - 1] = s
+    qc, qs = mix_quantize(q, T2, q_ebias)
+    S = np.zeros((HQ, tokens))
+    for g in range(HK):
+        kc = np.ascontiguousarray(k_cache_codes[:tokens, g])
+        ks = np.ascontiguousarray(k_cache_scales[:tokens, g])
+        S[g * G:(g + 1) * G] = gemm(qc[g * G:(g + 1) * G], qs[g * G:(g + 1) * G], T2, q_ebias, kc, ks, MXINT4)
+    z = S * sm_scale
+    e = np.exp(z - z.max(axis=1, keepdims=True))
+    P = (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+    Pp = np.zeros((HQ, Tv), np.float32)
+    Pp[:, :tokens] = P
+    pc, ps = mix_quantize(Pp, T2, p_ebias)
+    O = np.zeros((HQ, D))
+    for g in range(HK):
+        O[g * G:(g + 1) * G] = gemm(pc[g * G:(g + 1) * G], ps[g * G:(g + 1) * G], T2, p_ebias,
+                                    np.ascontiguousarray(v_codes[g]), np.ascontiguousarray(v_scales[g]), MXINT4)
+    return O, P, (pc, ps), S

@@ -758,12 +758,61 @@ def pin_underflow_count(orc):
         assert n > 0
 
 
+def pin_decode_attention(orc):
+    """One decode step composed in the pages' order (frozen-mean K-smoothing
+    on append, Q-K^T, softmax, MiX requantisation of P, P-V): S and O equal
+    the fp64 products of the dequantised planes with head h reading KV head
+    h // G; P is a softmax (rows sum to 1, shift-invariant); the appended K'
+    row dequantises to fp32(k_new) - mean within half an MXINT4 step."""
+    HQ, HK, D, T = 6, 2, 128, 80
+    G = HQ // HK
+    q, k, v = synth.attention_qkv(9, T, q_heads=HQ, kv_heads=HK, head_dim=D)
+    mean = orc.ksmooth_mean(synth.to_bf16_bits(k[:48]))
+    kp = orc.ksmooth_apply(synth.to_bf16_bits(k[:T - 1]), mean.astype(np.float32))
+    kc = np.zeros((T, HK, D // 2), np.uint8)
+    ks = np.zeros((T, HK, D // 32), np.uint8)
+    c, s = orc.mx_quantize(kp.reshape(-1, D).astype(np.float32), 1, 0)
+    kc[:T - 1], ks[:T - 1] = c.reshape(T - 1, HK, -1), s.reshape(T - 1, HK, -1)
+    Tv = 96
+    vv = np.zeros((Tv, HK, D))
+    vv[:T] = v
+    vc, vs = orc.mx_quantize(synth.to_bf16_bits(vv.reshape(Tv, HK * D)), 0, 0)   # [HK*D, Tv/2]
+    vc, vs = vc.reshape(HK, D, -1), vs.reshape(HK, D, -1)
+    qb = synth.to_bf16_bits(q[T - 1])
+    kn = synth.to_bf16_bits(k[T - 1])
+    O, Pm, (pc, ps), S = orc.decode_attention(qb, kc, ks, vc, vs, T, 0.088, k_new=kn, k_mean=mean)
+    # the appended row
+    kd = orc.mx_dequantize(kc[T - 1], ks[T - 1], 0)
+    want = synth.bf16_bits_to_f32(kn).astype(np.float64) - mean.astype(np.float32).astype(np.float64)
+    step = np.exp2(ks[T - 1].astype(np.float64) - 127 - 2).repeat(32, axis=1)
+    sat = np.abs(want) > 7 * step                     # above the largest level 7 * 2^(X-2)
+    err = np.abs(kd - want)
+    assert np.all(err[~sat] <= step[~sat] / 2 + 1e-12) and np.all(err[sat] < step[sat])
+    # S and O against dequantised planes
+    qc, qs = orc.mix_quantize(qb, 2, -8)
+    qd = orc.mix_dequantize(qc, qs, 2, -8)
+    pd = orc.mix_dequantize(pc, ps, 2, -15)
+    for h in range(HQ):
+        g = h // G
+        kdq = orc.mx_dequantize(np.ascontiguousarray(kc[:T, g]), np.ascontiguousarray(ks[:T, g]), 0)
+        assert np.max(np.abs(S[h] - kdq @ qd[h])) <= 1e-12 * np.max(np.abs(S[h]))
+        vdq = orc.mx_dequantize(vc[g], vs[g], 0)                    # [D, Tv]
+        assert np.max(np.abs(O[h] - vdq @ pd[h])) <= 1e-12 * np.max(np.abs(O[h]))
+    # softmax properties
+    assert np.all(np.abs(Pm.astype(np.float64).sum(axis=1) - 1.0) < 1e-5)
+    assert np.all(pd[:, T:] == 0)
+    z = S * 0.088
+    e = np.exp(z + 7.0 - (z + 7.0).max(axis=1, keepdims=True))
+    assert np.allclose(e / e.sum(axis=1, keepdims=True), Pm, rtol=1e-6, atol=1e-12)
+
+
 ALL_PINS = [pin_bit_accounting, pin_dequant_special_values, pin_refinement_brute_force,
             pin_exhaustive_sweep, pin_asymmetric_zero, pin_round_trip,
             pin_nonfinite_and_zero_blocks, pin_e2m1_and_int4_brute_force, pin_mx_scale_rule,
             pin_mx_axis_consistency, pin_gemm_eq6_exact, pin_gemm_against_dequant_matmul,
             pin_gemm_reduces_to_mx_dot, pin_gemm_batch_gqa_indexing, pin_ksmooth,
-            pin_mx_tight_rule, pin_auto_ebias, pin_mx_g16, pin_gemm_g16, pin_nvfp4, pin_underflow_count]
+            pin_mx_tight_rule, pin_auto_ebias, pin_mx_g16, pin_gemm_g16, pin_nvfp4, pin_underflow_count,
+            pin_decode_attention]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
