@@ -212,7 +212,7 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
 
     w_gu = weight(30, DM, 2 * DF)        # gate+up 3584 x 37888; its first 18944 columns are the sweep weight
     keep.append(w_gu)
-    EXT_INPUTS.update(w_gu=w_gu, xd=xd, g=g)
+    EXT_INPUTS.update(w_gu=w_gu, xd=xd, x=x, g=g)
     wq = {"gate_up": mix.quantize_mx(w_gu, 0, FP4)}
     for name, tid, k, n in (("qkv", 31, DM, QKV), ("o", 32, DM, DM), ("down", 33, DF, DM)):
         w = weight(tid, k, n)
@@ -343,6 +343,8 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
     ws2 = new(max(16, mix.mix_mx_gemm_workspace_bytes(dd2)), torch.uint8)
     fns[f"gemv_pv_decode_{HK}x7x{D}x{TC}"] = lambda: mix.mix_mx_gemm(dd2, ws2)
     d2h.append(o_dec)
+    EXT_INPUTS.update(dec=dict(q=q_new, k_new=k_new[0], mean=mean_f, kc=kcc.view(TC, HK, 64), ks=kcs.view(TC, HK, 4),
+                               vc=vcc, vs=vcs, TC=TC, HQ=HQ, HK=HK))
 
     calls = []
     for name, nbytes, flops, launches, _ in step_table(small):
@@ -528,16 +530,47 @@ def measure_extensions(torch, mix, stream, iters=10):
     each launch, a spin kernel ahead of it, inputs larger than L2.  Each
     entry gives its algorithmic bytes and the fraction of measured HBM copy
     bandwidth reached."""
-    g, w_gu, xd = EXT_INPUTS["g"], EXT_INPUTS["w_gu"], EXT_INPUTS["xd"]
+    g, w_gu, xd, x = EXT_INPUTS["g"], EXT_INPUTS["w_gu"], EXT_INPUTS["xd"], EXT_INPUTS["x"]
     M, DM, DF = g["M"], g["DM"], g["DF"]
     dev = xd.device
-    FP4, T2 = mix.MX_FP4_E2M1, mix.MIX_T2_4P5
+    FP4, INT4, T2 = mix.MX_FP4_E2M1, mix.MX_INT4, mix.MIX_T2_4P5
+    # MiX-INT4g16: MiX-4.5b activations x MXINT4g16 weights, at the gate/up shape
+    a2c, a2s = mix.quantize_mix(x, T2)
+    g16c, g16s = mix.quantize_mx(w_gu, 0, INT4, mix.MX_BLOCK16)
+    g32c, g32s = mix.quantize_mx(w_gu, 0, INT4)
+    oc = torch.empty((M, DF), dtype=torch.uint8, device=dev)
+    osh = torch.empty((M, 2 * DF // 32), dtype=torch.int16, device=dev)
+    d16 = mix.gemm_desc(M, 2 * DF, DM, a2c, a2s, T2, -8, g16c, g16s, INT4, epi=mix.MIX_EPI_MIX_T2, out_codes=oc,
+                        out_shared=osh, algo=mix.MIX_GEMM_TCGEN05, b_block=16)
+    d32 = mix.gemm_desc(M, 2 * DF, DM, a2c, a2s, T2, -8, g32c, g32s, INT4, epi=mix.MIX_EPI_MIX_T2, out_codes=oc,
+                        out_shared=osh, algo=mix.MIX_GEMM_TCGEN05)
+    gws = torch.empty(max(mix.mix_mx_gemm_workspace_bytes(d16), mix.mix_mx_gemm_workspace_bytes(d32)),
+                      dtype=torch.uint8, device=dev)
+    g16_bytes = plane_bytes(M, DM, 2) + 2 * DF * DM // 2 + 2 * DF * DM // 16 + plane_bytes(M, 2 * DF, 2)
+    g32_bytes = plane_bytes(M, DM, 2) + plane_bytes(2 * DF, DM, 0) + plane_bytes(M, 2 * DF, 2)
+    gflops = 2.0 * M * 2 * DF * DM
+    nvc = torch.empty((M, DM // 2), dtype=torch.uint8, device=dev)
+    nvs = torch.empty((M, DM // 16), dtype=torch.uint8, device=dev)
+    nvt = torch.empty((1,), dtype=torch.float32, device=dev)
+    ufn = torch.empty((1,), dtype=torch.int64, device=dev)
     wc = torch.empty((DF, DM // 2), dtype=torch.uint8, device=dev)
     ws = torch.empty((DF, DM // 32), dtype=torch.uint8, device=dev)
     ac = torch.empty((M, DF // 2), dtype=torch.uint8, device=dev)
     ash = torch.empty((M, DF // 32), dtype=torch.int16, device=dev)
     eb = torch.empty((1,), dtype=torch.int32, device=dev)
     table = [
+        (f"gemm_gate_up_mix_int4g16_{M}x{DM}x{2 * DF}", "MiX-4.5b x MXINT4g16 (staged; the g16 scales folded "
+         "into the e4m3 expansion)", g16_bytes, 3, lambda: mix.mix_mx_gemm(d16, gws), gflops),
+        (f"gemm_gate_up_mix_int4_{M}x{DM}x{2 * DF}", "MiX-4.5b x MXINT4 (32-blocks), same call for comparison",
+         g32_bytes, 3, lambda: mix.mix_mx_gemm(d32, gws), gflops),
+        (f"mx_quantize_int4_g16_{DM}x{DF}", "MXINT4g16 weight quantiser (down the columns)",
+         DF * DM * 2 + DF * DM // 2 + DF * DM // 16, 1,
+         lambda: mix.mx_quantize(w_gu, DM, DF, 2 * DF, 0, INT4, mix.MX_BLOCK16, g16c, g16s)),
+        (f"nvfp4_quantize_{M}x{DM}", "NVFP4 comparison quantiser (tensor amax pass, then 16-blocks; x read twice)",
+         2 * M * DM * 2 + M * DM // 2 + M * DM // 16 + 4, 4,
+         lambda: mix.nvfp4_quantize(x, M, DM, DM, nvc, nvs, nvt)),
+        (f"mix_underflow_count_{M}x{DM}", "dead-zone count over the MiX-4.5b plane of x",
+         M * DM * 2 + M * DM // 2 + 8, 2, lambda: mix.mix_underflow_count(x, M, DM, DM, a2c, mix.MIX_UF_MIX, ufn)),
         (f"mx_quantize_fp4_tight_{DM}x{DF}", "tight MX shared exponent", mx_bytes(DF, DM), 1,
          lambda: mix.mx_quantize(w_gu, DM, DF, 2 * DF, 0, FP4, mix.MX_SCALE_TIGHT, wc, ws)),
         (f"mx_quantize_fp4_ceil_{DM}x{DF}", "the ceil rule, same call (for comparison)", mx_bytes(DF, DM), 1,
@@ -549,7 +582,9 @@ def measure_extensions(torch, mix, stream, iters=10):
          lambda: mix.mix_quantize_auto(xd, M, DF, DF, T2, 1, ac, ash, eb)),
     ]
     out = {}
-    for name, what, nbytes, launches, fn in table:
+    for row in table:
+        name, what, nbytes, launches, fn = row[:5]
+        flops = row[5] if len(row) > 5 else 0.0
         for _ in range(3):
             fn()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
@@ -563,8 +598,60 @@ def measure_extensions(torch, mix, stream, iters=10):
         gbs = nbytes / (ms * 1e-3) / 1e9
         out[name] = {"what": what, "ms": round(ms, 5), "bytes": int(nbytes), "GB/s": round(gbs, 1),
                      "frac_hbm": round(gbs / HBM, 3), "launches": launches}
+        if flops:
+            tf = flops / (ms * 1e-3) / 1e12
+            out[name].update({"TFLOP/s": round(tf, 1), "frac_mma": round(tf / MX8_TFLOPS, 3)})
     assert mix.mix_device_error() == 0, "a kernel reported a timed-out wait"
+    out.update(measure_decode_attention(torch, mix, stream, iters))
+    out["dead_zone"] = dead_zone_table(torch, mix, dev)
     return out
+
+
+def measure_decode_attention(torch, mix, stream, iters):
+    """The fused decode attention (K append, Q-K^T, softmax, P requantisation,
+    P-V: two launches) over the step's 8192-token cache; bytes = the K' and V
+    caches, q, the new key and the output, once each."""
+    e = EXT_INPUTS["dec"]
+    TC, HQ, HK = e["TC"], e["HQ"], e["HK"]
+    out = torch.empty((HQ, 128), dtype=torch.float32, device=e["q"].device)
+    d = mix.decode_attention_desc(e["q"], e["kc"], e["ks"], e["vc"], e["vs"], TC, 1.0 / math.sqrt(128.0), out,
+                                  k_new=e["k_new"], k_mean=e["mean"])
+    ws = mix.decode_attention(d)
+    nbytes = TC * HK * 68 + HK * 128 * (TC // 2 + TC // 32) + HQ * 128 * 2 + HK * 128 * (2 + 4) + HQ * 128 * 4
+    for _ in range(3):
+        mix.decode_attention(d, ws)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    for a, b in ev:
+        torch.cuda._sleep(400000)
+        a.record(stream)
+        mix.decode_attention(d, ws)
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    name = f"decode_attention_fused_{HK}x{HQ // HK}x{TC}x128"
+    return {name: {"what": "fused decode attention (append, QK, softmax, MiX P, PV; 2 launches)", "ms": round(ms, 5),
+                   "bytes": int(nbytes), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / HBM, 3), "launches": 2}}
+
+
+def dead_zone_table(torch, mix, dev, tokens=4096):
+    """Fraction of nonzero key elements that each 4-bit format codes as zero,
+    on the attention workload's synthetic keys (4 KV heads x 128, channel
+    outliers), raw and smoothed with the frozen prefill mean: a synthetic
+    analogue of the pages' key-underflow comparison."""
+    from quantized_vlm_gemm_mix_b300 import synth
+    q, k, v = synth.attention_qkv(0, tokens)
+    res = {}
+    for name, arr in (("K", k), ("K_smoothed", k - k[: tokens // 2].mean(axis=0, keepdims=True))):
+        xb = synth.to_bf16_bits(arr.reshape(-1, 128))
+        xd = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+        nz = int(np.count_nonzero(synth.bf16_bits_to_f32(xb)))
+        planes = {"MiX-4.5b": (mix.quantize_mix(xd, mix.MIX_T2_4P5)[0], mix.MIX_UF_MIX),
+                  "MXINT4": (mix.quantize_mx(xd, 1, mix.MX_INT4)[0], mix.MIX_UF_MXINT4),
+                  "MXFP4": (mix.quantize_mx(xd, 1, mix.MX_FP4_E2M1)[0], mix.MIX_UF_E2M1),
+                  "NVFP4": (mix.quantize_nvfp4(xd)[0], mix.MIX_UF_E2M1)}
+        res[name] = {f: round(int(mix.underflow_count(xd, c, fmt).item()) / nz, 4) for f, (c, fmt) in planes.items()}
+    return res
 
 
 def main():

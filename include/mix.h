@@ -71,11 +71,14 @@ enum {
                          (Method section, accelerator bullet).  Default on.   */
   MX_SCALE_FLOOR = 2, /* MXFP4: OCP floor shared exponent instead of the ceil
                          rule the paper uses for every MXFP4 (Key results).   */
-  MX_SCALE_TIGHT = 4  /* MX: the smallest shared exponent at which no element
+  MX_SCALE_TIGHT = 4, /* MX: the smallest shared exponent at which no element
                          of the block saturates -- ceil(log2(amax / 6)) for
                          MXFP4 (the alternative to the ceil rule named beside
                          it in Key results), ceil(log2(amax / 1.75)) for
                          MXINT4.  Not combinable with MX_SCALE_FLOOR.         */
+  MX_BLOCK16 = 8      /* mx_quantize: one scale per 16 elements (MXINT4g16 /
+                         MXFP4g16, the g16 weights of "MiX-INT4g16"); the
+                         scale plane is N x K/16.                             */
 };
 
 /* ---------------------------------------------------------------------- */
@@ -134,6 +137,8 @@ MIX_API mix_status_t mix_quantize_auto(const void* x, mix_dtype_t dtype, int64_t
 /* W-MX quantiser (MXINT4 / MXFP4, block 32, E8M0 scale).                  */
 /* ---------------------------------------------------------------------- */
 /* Blocks run along the reduction dimension K; outputs are N x K planes.
+ * With MX_BLOCK16 the blocks hold 16 elements (K still a multiple of 32) and
+ * the scales plane is N x K/16; the rules below apply per 16-block.
  *   axis = 1: x is N x K (rows = N, cols = K), row stride ld >= K.
  *   axis = 0: x is K x N (rows = K, cols = N), row stride ld >= N -- a
  *             weight stored for x @ W; it is read down its columns and the
@@ -147,6 +152,36 @@ MIX_API mix_status_t mix_quantize_auto(const void* x, mix_dtype_t dtype, int64_t
 MIX_API mix_status_t mx_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t cols, int64_t ld,
                          int axis, mx_type_t type, unsigned flags, uint8_t* codes,
                          uint8_t* scales, mix_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Comparison formats and the dead-zone count.                             */
+/* ---------------------------------------------------------------------- */
+/* NVFP4, the 16-element comparison format the pages set MiX against (blocks
+ * of 16 E2M1 elements, an E4M3 block scale, one FP32 tensor scale).  Every
+ * step is one IEEE fp32 operation, in this order: amax_t = the largest finite
+ * |x| of the tensor; s_t = amax_t / 2688 (1 if amax_t is 0, the smallest
+ * positive float if the quotient underflows); per 16-block t = (amax_b / s_t)
+ * / 6 (NaN left out of amax_b, +-Inf included) and its E4M3 code sb (nearest,
+ * ties even, saturating at 448); d = e4m3(sb) * s_t; each element the E2M1
+ * code of x / d (nearest, ties even, saturating at 6; NaN codes +0; -0 is
+ * written as +0); a block with sb = 0 stores zero codes.
+ *   x       rows x k, k % 16 == 0, row stride ld (alignment as mix_quantize).
+ *   codes   rows x k/2 bytes (8-byte aligned); scales rows x k/16 E4M3 bytes.
+ *   tensor_scale  one float in DEVICE memory, written on `stream`.
+ * Four launches: a clear, the amax reduction, a one-warp finish, the quantiser. */
+MIX_API mix_status_t nvfp4_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,
+                                    uint8_t* codes, uint8_t* scales, float* tensor_scale, mix_stream_t stream);
+
+/* Dead-zone count (the key-underflow comparison of the Key results section,
+ * made synthetic): how many finite nonzero elements of x have a zero code in
+ * `codes` -- 0x7 for MiX (the recycled -0 code 0xF is not zero), 0 for MXINT4,
+ * +-0 (nibble & 7 == 0) for E2M1 formats (MXFP4, NVFP4).
+ *   x       rows x k (k % 16 == 0), row stride ld; codes rows x k/2 (dense, 4-byte aligned).
+ *   count   one unsigned long long in DEVICE memory, written on `stream`. */
+typedef enum { MIX_UF_MIX = 0, MIX_UF_MXINT4 = 1, MIX_UF_E2M1 = 2 } mix_underflow_fmt_t;
+MIX_API mix_status_t mix_underflow_count(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,
+                                         const uint8_t* codes, mix_underflow_fmt_t fmt, unsigned long long* count,
+                                         mix_stream_t stream);
 
 /* Test aids: decode packed planes to fp32 (rows x k, dense).  MiX: the rule
  * (-1)^s (1.mshared)_2 2^(Emax - de) of the Method section, de = 7 zero, code
@@ -216,6 +251,7 @@ typedef struct {
   const uint8_t* b_codes;
   const uint8_t* b_scales;
   mx_type_t b_type;
+  int b_block;     /* elements per B scale: 32 (0 means 32) or 16 (g16) */
   int64_t b_ld, b_batch_stride;
   float* c; /* optional fp32 output (NULL: epilogue planes only) */
   int64_t ldc, c_batch_stride;
@@ -275,6 +311,47 @@ MIX_API mix_status_t ksmooth_kv(const void* k, mix_dtype_t dtype, int64_t tokens
 MIX_API mix_status_t ksmooth_kv_noalloc(const void* k, mix_dtype_t dtype, int64_t tokens, int heads,
                                         int head_dim, int64_t ld, float* mean, int mode, float* k_out,
                                         mix_stream_t stream);
+
+/* ---------------------------------------------------------------------- */
+/* Fused decode attention over an MX KV cache.                             */
+/* ---------------------------------------------------------------------- */
+/* One decode step for one sequence (one query token per head, GQA), in the
+ * dataflow of the Method section's accelerator bullet: the new key is
+ * smoothed with the frozen prefill mean and appended to the MXINT4 K' cache,
+ * S = q K'^T by Eq. (6) with q quantised to MiX-4.5b, P = softmax(sm_scale S)
+ * over the cache, P requantised to MiX-4.5b (32-token blocks, ebias p_ebias),
+ * O = P V by Eq. (6) against the MXINT4 V cache (blocks along tokens).  Two
+ * kernel launches, no host round trip; the last CTA of each KV head sums the
+ * per-chunk partial outputs in chunk order (an atomic ticket, no waiting).
+ * Products are exact integers per block; block terms, S and the softmax are
+ * fp32 (expf); O matches the oracle's fp64 composition within 1e-3 of each
+ * head's largest |O|. */
+typedef struct {
+  int64_t tokens;        /* cache length including the new token (>= 1)        */
+  int q_heads, kv_heads; /* q_heads % kv_heads == 0, q_heads / kv_heads <= 16   */
+  int head_dim;          /* 128                                                 */
+  mix_dtype_t dtype;     /* of q and k_new                                      */
+  const void* q;         /* [q_heads][head_dim]                                  */
+  const void* k_new;     /* [kv_heads][head_dim], or NULL: no append             */
+  const float* k_mean;   /* [kv_heads][head_dim] frozen prefill mean (with k_new) */
+  uint8_t* k_codes;      /* K' cache [tokens][kv_heads][head_dim/2], MXINT4 along
+                            head_dim; row tokens-1 is written when k_new is set */
+  uint8_t* k_scales;     /* [tokens][kv_heads][head_dim/32], 4-byte aligned rows  */
+  const uint8_t* v_codes;  /* V cache [kv_heads][head_dim][v_ld/2], MXINT4 along tokens */
+  const uint8_t* v_scales; /* [kv_heads][head_dim][v_ld/32]                         */
+  int64_t v_ld;          /* token capacity of the V planes: a multiple of 32 >= tokens */
+  float sm_scale;        /* softmax temperature (1/sqrt(head_dim) typically)     */
+  int q_ebias, p_ebias;  /* MiX ebias of q (-8) and of P (-15)                   */
+  float* out;            /* O [q_heads][head_dim] fp32                           */
+  uint8_t* p_codes;      /* optional P planes [q_heads][v_ld/2] (NULL: not kept); only
+                            the 32-token blocks that hold a token are written    */
+  void* p_shared;        /* [q_heads][v_ld/32] uint16 MiX-4.5b shared fields     */
+} mix_decode_attn_desc_t;
+
+/* Device workspace bytes (S, the per-chunk statistics and partial outputs). */
+MIX_API size_t mix_decode_attention_workspace_bytes(const mix_decode_attn_desc_t* desc);
+MIX_API mix_status_t mix_decode_attention(const mix_decode_attn_desc_t* desc, void* workspace, size_t workspace_bytes,
+                                          mix_stream_t stream);
 
 /* ---------------------------------------------------------------------- */
 /* Status and device error word.                                           */

@@ -121,18 +121,77 @@ mix_status_t mx_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t
                          mix_stream_t stream) {
   if (!valid_dtype(dtype) || (type != MX_INT4 && type != MX_FP4_E2M1) || (axis != 0 && axis != 1))
     return MIX_ERR_INVALID_ARG;
-  if (rows < 0 || cols < 0 || ld < cols || (flags & ~6u) || flags == 6u) return MIX_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || ld < cols || (flags & ~14u) || (flags & 6u) == 6u) return MIX_ERR_INVALID_ARG;
   const int64_t K = axis ? cols : rows, N = axis ? rows : cols;
   if (K % 32 != 0) return MIX_ERR_SHAPE;
   if (N == 0 || K == 0) return MIX_OK;
   if (x == nullptr || codes == nullptr || scales == nullptr) return MIX_ERR_INVALID_ARG;
   if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(codes, 16)) return MIX_ERR_ALIGN;
-  const bool fp4 = type == MX_FP4_E2M1;
+  const bool fp4 = type == MX_FP4_E2M1, g16 = (flags & MX_BLOCK16) != 0;
   const int fl = mx_rule_of(flags);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (axis == 1)
-    return from_cuda(launch_mx_quantize_rows(x, dtype == MIX_DT_BF16, N, K, ld, fp4, fl, codes, scales, st));
-  return from_cuda(launch_mx_quantize_cols(x, dtype == MIX_DT_BF16, K, N, ld, fp4, fl, codes, scales, st));
+    return from_cuda(launch_mx_quantize_rows(x, dtype == MIX_DT_BF16, N, K, ld, fp4, fl, g16, codes, scales, st));
+  return from_cuda(launch_mx_quantize_cols(x, dtype == MIX_DT_BF16, K, N, ld, fp4, fl, g16, codes, scales, st));
+}
+
+mix_status_t nvfp4_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,
+                            uint8_t* codes, uint8_t* scales, float* tensor_scale, mix_stream_t stream) {
+  if (!valid_dtype(dtype) || rows < 0 || k < 0 || ld < k || tensor_scale == nullptr) return MIX_ERR_INVALID_ARG;
+  if (k % 16 != 0) return MIX_ERR_SHAPE;
+  if (!aligned(tensor_scale, 4)) return MIX_ERR_ALIGN;
+  if (rows > 0 && k > 0) {
+    if (x == nullptr || codes == nullptr || scales == nullptr) return MIX_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(codes, 8)) return MIX_ERR_ALIGN;
+  }
+  return from_cuda(launch_nvfp4_quantize(x, dtype == MIX_DT_BF16, rows, k, ld, codes, scales, tensor_scale,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+mix_status_t mix_underflow_count(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,
+                                 const uint8_t* codes, mix_underflow_fmt_t fmt, unsigned long long* count,
+                                 mix_stream_t stream) {
+  if (!valid_dtype(dtype) || rows < 0 || k < 0 || ld < k || count == nullptr) return MIX_ERR_INVALID_ARG;
+  if (fmt != MIX_UF_MIX && fmt != MIX_UF_MXINT4 && fmt != MIX_UF_E2M1) return MIX_ERR_INVALID_ARG;
+  if (k % 16 != 0) return MIX_ERR_SHAPE;
+  if (!aligned(count, 8)) return MIX_ERR_ALIGN;
+  if (rows > 0 && k > 0) {
+    if (x == nullptr || codes == nullptr) return MIX_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(codes, 4)) return MIX_ERR_ALIGN;
+  }
+  return from_cuda(launch_underflow_count(x, dtype == MIX_DT_BF16, rows, k, ld, codes, (int)fmt, count,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static mix_status_t validate_attn(const mix_decode_attn_desc_t* d) {
+  if (d == nullptr) return MIX_ERR_INVALID_ARG;
+  if (d->tokens < 1 || d->q_heads < 1 || d->kv_heads < 1 || d->q_heads % d->kv_heads != 0 ||
+      d->q_heads / d->kv_heads > 16 || !valid_dtype(d->dtype))
+    return MIX_ERR_INVALID_ARG;
+  if (d->head_dim != 128 || d->v_ld % 32 != 0 || d->v_ld < d->tokens) return MIX_ERR_SHAPE;
+  if (d->q_ebias < -100 || d->q_ebias > 100 || d->p_ebias < -100 || d->p_ebias > 100) return MIX_ERR_INVALID_ARG;
+  if (d->q == nullptr || d->k_codes == nullptr || d->k_scales == nullptr || d->v_codes == nullptr ||
+      d->v_scales == nullptr || d->out == nullptr || (d->k_new != nullptr && d->k_mean == nullptr) ||
+      ((d->p_codes == nullptr) != (d->p_shared == nullptr)))
+    return MIX_ERR_INVALID_ARG;
+  if (!aligned(d->k_codes, 16) || !aligned(d->k_scales, 4) || !aligned(d->v_codes, 16) ||
+      (d->p_codes != nullptr && (!aligned(d->p_codes, 16) || !aligned(d->p_shared, 2))))
+    return MIX_ERR_ALIGN;
+  if (d->tokens >= (int64_t)1 << 40) return MIX_ERR_SHAPE;
+  return MIX_OK;
+}
+
+size_t mix_decode_attention_workspace_bytes(const mix_decode_attn_desc_t* d) {
+  if (validate_attn(d) != MIX_OK) return 0;
+  return decode_attention_ws_bytes(*d);
+}
+
+mix_status_t mix_decode_attention(const mix_decode_attn_desc_t* d, void* workspace, size_t workspace_bytes,
+                                  mix_stream_t stream) {
+  const mix_status_t s = validate_attn(d);
+  if (s != MIX_OK) return s;
+  if (workspace == nullptr || workspace_bytes < decode_attention_ws_bytes(*d)) return MIX_ERR_WORKSPACE;
+  return from_cuda(launch_decode_attention(*d, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mix_status_t mix_dequantize(const uint8_t* codes, const void* shared, int64_t rows, int64_t k,
@@ -164,6 +223,7 @@ static mix_status_t validate_gemm(const mix_gemm_desc_t* d) {
   if (d->M < 0 || d->N < 0 || d->K < 0 || d->batch < 1 || d->b_group < 1) return MIX_ERR_INVALID_ARG;
   if (d->a_type != MIX_T1_4P25 && d->a_type != MIX_T2_4P5) return MIX_ERR_INVALID_ARG;
   if (d->b_type != MX_INT4 && d->b_type != MX_FP4_E2M1) return MIX_ERR_INVALID_ARG;
+  if (d->b_block != 0 && d->b_block != 16 && d->b_block != 32) return MIX_ERR_INVALID_ARG;
   if (d->a_ebias < -100 || d->a_ebias > 100 || d->epi_ebias < -100 || d->epi_ebias > 100)
     return MIX_ERR_INVALID_ARG;
   if (d->epi < MIX_EPI_NONE || d->epi > MIX_EPI_MXFP4) return MIX_ERR_INVALID_ARG;

@@ -39,6 +39,46 @@ __device__ __forceinline__ DecTab mix_tab(uint32_t m3) {
 __device__ __forceinline__ DecTab int4_tab() { return DecTab{0x34302800u, 0x3E3C3A38u, 0xBABCBEC0u, 0xA8B0B4B8u}; }
 __device__ __forceinline__ DecTab fp4_tab() { return DecTab{0x3C383000u, 0x4C484440u, 0xBCB8B080u, 0xCCC8C4C0u}; }
 
+// e4m3 byte of +-mant 2^e (0 <= mant <= 15): exact when it fits, otherwise
+// rounded to the nearest (ties to even) subnormal, and clipped to 448 above.
+__device__ __forceinline__ uint32_t e4m3_of(int mant, int e, bool neg) {
+  uint32_t b = 0u;
+  if (mant != 0) {
+    const int p = 31 - __clz(mant);  // leading bit
+    const int E = p + e;
+    if (E > 8) {
+      b = 0x7Eu;
+    } else if (E >= -6) {
+      b = ((uint32_t)(E + 7) << 3) | ((uint32_t)((mant << 3) >> p) & 7u);
+    } else {  // subnormal: m 2^-9
+      const int s = e + 9;
+      if (s >= 0) {
+        b = (uint32_t)(mant << s);
+      } else {
+        const int r = -s;
+        if (r <= 5) {
+          const uint32_t q = (uint32_t)mant >> r, rem = (uint32_t)mant & ((1u << r) - 1u), half = 1u << (r - 1);
+          b = q + ((rem > half || (rem == half && (q & 1u))) ? 1u : 0u);  // 8 is the smallest normal
+        }
+      }
+    }
+  }
+  return (neg ? 0x80u : 0u) | b;
+}
+
+// The MX element tables (int4_tab / fp4_tab) with every value multiplied by
+// 2^sh, as 16 bytes in code order (codes 0..7 then 8..15): MXINT4 q / 4,
+// E2M1 in half units.
+__device__ __forceinline__ uint32_t mx_scaled_entry(int code, bool fp4, int sh) {
+  if (fp4) {
+    const int e = (code >> 1) & 3, m = code & 1;
+    const int half_units = e ? ((2 + m) << (e - 1)) : m;  // 0, 1, 2, 3, 4, 6, 8, 12
+    return e4m3_of(half_units, sh - 1, (code & 8) != 0);
+  }
+  const int q = (code & 8) ? code - 16 : code;
+  return e4m3_of(q < 0 ? -q : q, sh - 2, q < 0);
+}
+
 // Eight nibbles (element i in bits 4i..4i+3) -> eight e4m3 bytes.
 __device__ __forceinline__ uint2 dec8(uint32_t v, const DecTab& t) {
   const uint32_t s7 = v & 0x77777777u, s2 = (v >> 1) & 0x44444444u;

@@ -103,19 +103,37 @@ __global__ void __launch_bounds__(kThreads) expand_a_kernel(const uint8_t* __res
 // bytes regrouped into tiles of `tile_rows` (<= 256) rows, each stored as a
 // 256-row group (two 128-row halves; the words of rows tile_rows .. 255 are
 // padding and hold scale 1).  Threads walk the padded 256-row index space.
-template <bool FP4>
+//
+// G16 (MXINT4g16 / MXFP4g16, one scale per 16 elements): the matmul takes one
+// UE8M0 scale per 32-deep block, so each block gets S = max(X0, X1) - C and
+// each half's elements are stored multiplied by 2^(X_h - S) (C = 7 for
+// MXINT4, 6 for MXFP4: the larger half's largest element still fits e4m3).
+// A half whose exponent is within 14 binades of the other's stays exact; a
+// farther one is rounded to the nearest e4m3 subnormal.  The per-block S
+// bytes also go to `eff_scales` ([bb][N][k_pad / 32]) when it is given, for
+// the fused-decode matmul, which reads block scale bytes directly.
+constexpr int kG16ShiftMin = -24, kG16Shifts = 32;  // shifts -24 .. 7; -24 already zeroes every code
+
+template <bool FP4, bool G16>
 __global__ void __launch_bounds__(kThreads) expand_b_kernel(const uint8_t* __restrict__ codes,
                                                             const uint8_t* __restrict__ scales, int64_t N,
                                                             int64_t K, int64_t b_ld, int64_t b_bs, int64_t bb,
                                                             int64_t k_pad, int tile_rows, int64_t kt_n,
                                                             FastDiv f_kbp, FastDiv f_rows,
-                                                            uint8_t* __restrict__ b_e4m3, uint32_t* __restrict__ sfb) {
+                                                            uint8_t* __restrict__ b_e4m3, uint32_t* __restrict__ sfb,
+                                                            uint8_t* __restrict__ eff_scales) {
   const int64_t kbv = K / 32;
   const uint32_t total = (uint32_t)(bb * (int64_t)f_rows.d * f_kbp.d);
   const uint32_t total_w = (total + 31u) & ~31u;
   const uint32_t stride = gridDim.x * blockDim.x;
   const int64_t nt = f_rows.d / 256;
   const DecTab tt = FP4 ? fp4_tab() : int4_tab();
+  __shared__ __align__(16) uint8_t g16_tab[G16 ? kG16Shifts * 16 : 16];
+  if (G16) {
+    for (int i = threadIdx.x; i < kG16Shifts * 16; i += blockDim.x)
+      g16_tab[i] = (uint8_t)mx_scaled_entry(i & 15, FP4, kG16ShiftMin + (i >> 4));
+    __syncthreads();
+  }
   for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < total_w; t += stride) {
     const bool valid = t < total;
     const uint32_t rr = fdiv(t, f_kbp), kb = t - rr * f_kbp.d;
@@ -127,15 +145,28 @@ __global__ void __launch_bounds__(kThreads) expand_b_kernel(const uint8_t* __res
       uint4 out0 = make_uint4(0, 0, 0, 0), out1 = make_uint4(0, 0, 0, 0);
       if (kb < kbv) {
         const int64_t e = (int64_t)b * b_bs + r * b_ld + 32 * (int64_t)kb;
-        sbyte = (uint32_t)__ldg(scales + e / 32);
         const uint4 cv = __ldg(reinterpret_cast<const uint4*>(codes + e / 2));
-        const uint2 d0 = dec8(cv.x, tt), d1 = dec8(cv.y, tt), d2 = dec8(cv.z, tt), d3 = dec8(cv.w, tt);
-        out0 = make_uint4(d0.x, d0.y, d1.x, d1.y);
-        out1 = make_uint4(d2.x, d2.y, d3.x, d3.y);
+        if (G16) {
+          const int x0 = (int)__ldg(scales + e / 16), x1 = (int)__ldg(scales + e / 16 + 1);  // biased
+          const int s = max(max(x0, x1) - (FP4 ? 6 : 7), 0);
+          sbyte = (uint32_t)s;
+          const uint4 t0 = *reinterpret_cast<const uint4*>(g16_tab + 16 * (max(x0 - s, kG16ShiftMin) - kG16ShiftMin));
+          const uint4 t1 = *reinterpret_cast<const uint4*>(g16_tab + 16 * (max(x1 - s, kG16ShiftMin) - kG16ShiftMin));
+          const DecTab h0{t0.x, t0.y, t0.z, t0.w}, h1{t1.x, t1.y, t1.z, t1.w};
+          const uint2 d0 = dec8(cv.x, h0), d1 = dec8(cv.y, h0), d2 = dec8(cv.z, h1), d3 = dec8(cv.w, h1);
+          out0 = make_uint4(d0.x, d0.y, d1.x, d1.y);
+          out1 = make_uint4(d2.x, d2.y, d3.x, d3.y);
+        } else {
+          sbyte = (uint32_t)__ldg(scales + e / 32);
+          const uint2 d0 = dec8(cv.x, tt), d1 = dec8(cv.y, tt), d2 = dec8(cv.z, tt), d3 = dec8(cv.w, tt);
+          out0 = make_uint4(d0.x, d0.y, d1.x, d1.y);
+          out1 = make_uint4(d2.x, d2.y, d3.x, d3.y);
+        }
       }
       uint4* dst = reinterpret_cast<uint4*>(b_e4m3 + ((int64_t)b * N + r) * k_pad + 32 * (int64_t)kb);
       dst[0] = out0;
       dst[1] = out1;
+      if (G16 && eff_scales != nullptr) eff_scales[((int64_t)b * N + r) * (k_pad / 32) + kb] = (uint8_t)sbyte;
     }
     const uint32_t word = quad_or(sbyte << (8 * (kb & 3u)));
     if (valid && (kb & 3u) == 0) {
@@ -187,7 +218,7 @@ size_t align_up(size_t v) { return (v + kStagedAlign - 1) / kStagedAlign * kStag
 }  // namespace
 
 bool staged_fp4_native_ok(const mix_gemm_desc_t& d) {
-  if (d.b_type != MX_FP4_E2M1 || d.K % 128 != 0) return false;
+  if (d.b_type != MX_FP4_E2M1 || d.K % 128 != 0 || b_g16(d)) return false;
   if ((reinterpret_cast<uintptr_t>(d.b_codes) & 31) != 0 || (d.b_ld / 2) % 32 != 0) return false;
   const int64_t bb = (d.batch + d.b_group - 1) / d.b_group;
   if (bb > 1 && (d.b_batch_stride / 2) % 32 != 0) return false;
@@ -211,6 +242,7 @@ StagedPlan staged_plan(const mix_gemm_desc_t& d) {
   if (!sp.b_native) off = align_up(off + (size_t)sp.bb * d.N * sp.k_pad);
   sp.off_sfb = off;
   off = align_up(off + (size_t)sp.bb * sp.nt * sp.kt * 1024);
+  sp.off_sfe = off;
   sp.bytes = off;
   return sp;
 }
@@ -224,6 +256,8 @@ StagedPlan staged_plan_b_only(const mix_gemm_desc_t& d) {
   off = align_up(off + (size_t)sp.bb * d.N * sp.k_pad);
   sp.off_sfb = off;
   off = align_up(off + (size_t)sp.bb * sp.nt * sp.kt * 1024);
+  sp.off_sfe = off;
+  if (b_g16(d)) off = align_up(off + (size_t)sp.bb * d.N * (sp.k_pad / 32));  // per-block S bytes
   sp.bytes = off;
   return sp;
 }
@@ -261,12 +295,21 @@ cudaError_t launch_expand_b(const mix_gemm_desc_t& d, const StagedPlan& sp, unsi
     const int64_t words = sp.bb * sp.nt * 256 * sp.kt;
     b_scales_kernel<<<grid_for(words), kThreads, 0, st>>>(d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb, tr, sp.kt,
                                                           make_fastdiv((uint32_t)sp.kt), fr, sfb);
-  } else if (d.b_type == MX_FP4_E2M1)
-    expand_b_kernel<true><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
-                                                        sp.k_pad, tr, sp.kt, fk, fr, b, sfb);
-  else
-    expand_b_kernel<false><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb,
-                                                         sp.k_pad, tr, sp.kt, fk, fr, b, sfb);
+    return cudaGetLastError();
+  }
+  // the per-block scale bytes exist only in a B-only plan with g16 weights
+  uint8_t* sfe = (b_g16(d) && sp.bytes > sp.off_sfe) ? base + sp.off_sfe : nullptr;
+#define EXPAND_B(FP4, G16)                                                                                   \
+  expand_b_kernel<FP4, G16><<<g, kThreads, 0, st>>>(d.b_codes, d.b_scales, d.N, d.K, d.b_ld, bs, sp.bb, sp.k_pad, \
+                                                    tr, sp.kt, fk, fr, b, sfb, sfe)
+  if (d.b_type == MX_FP4_E2M1) {
+    if (b_g16(d)) EXPAND_B(true, true);
+    else EXPAND_B(true, false);
+  } else {
+    if (b_g16(d)) EXPAND_B(false, true);
+    else EXPAND_B(false, false);
+  }
+#undef EXPAND_B
   return cudaGetLastError();
 }
 

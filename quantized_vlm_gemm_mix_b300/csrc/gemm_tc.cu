@@ -903,6 +903,11 @@ cudaError_t launch_fused(const mix_gemm_desc_t& d, void* ws, cudaStream_t st, mi
     }
     p.b_tma_fmt = 0u;
     p.b_tma_bytes = B_OPS;
+    if (b_g16(d)) {  // the block scales the expansion chose, one byte per 32-deep block
+      p.b_scales = base + sp.off_sfe;
+      p.b_ld = sp.k_pad;
+      p.b_bs = d.N * sp.k_pad;
+    }
   }
   CUtensorMap mc = ma;  // placeholder when there is no fp32 output
   if (d.c != nullptr && !make_c_map(&mc, d.c, d.M, d.N, d.batch, d.ldc, d.c_batch_stride)) {

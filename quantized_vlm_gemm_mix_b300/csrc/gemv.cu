@@ -56,6 +56,9 @@ __device__ __forceinline__ int b_value(uint32_t c, int fp4) {
   return (c & 8u) ? (int)c - 16 : (int)c;  // INT4 two's complement
 }
 
+// G16: weights with one scale per 16 elements; each 32-block's two halves
+// (sub-trees 0-1 and 2-3) take their own exponent add.
+template <bool G16>
 __global__ void __launch_bounds__(kThreads) gemv_shiftadd_kernel(GemvArgs p) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int64_t bt = blockIdx.z;
@@ -107,10 +110,11 @@ __global__ void __launch_bounds__(kThreads) gemv_shiftadd_kernel(GemvArgs p) {
   if (n < p.N) {
     const int64_t gb = bt / p.b_group;
     const uint8_t* brow = p.b_codes + (gb * p.b_bs + n * p.b_ld + k0) / 2;
-    const uint8_t* bsc = p.b_scales + (gb * p.b_bs + n * p.b_ld + k0) / 32;
+    const uint8_t* bsc = p.b_scales + (gb * p.b_bs + n * p.b_ld + k0) / (G16 ? 16 : 32);
     for (int b = sub; b < nbc; b += tpn) {
       const uint4 cw = *reinterpret_cast<const uint4*>(brow + b * 16);
-      const int X = (int)bsc[b] - 127;
+      const int X = (int)bsc[G16 ? 2 * b : b] - 127;
+      const int X1 = G16 ? (int)bsc[2 * b + 1] - 127 : 0;
       int wv[32];
       const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) gemv_shiftadd_kernel(GemvArgs p) {
         if (m < p.M) {
           const int16_t* f = fa + (m * nbc_max + b) * 32;
           const int2 sh = ash[m * nbc_max + b];
-          int blockv = 0;
+          int blockv = 0, half0 = 0;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const int4 f0 = *reinterpret_cast<const int4*>(f + 8 * q);
@@ -134,8 +138,17 @@ __global__ void __launch_bounds__(kThreads) gemv_shiftadd_kernel(GemvArgs p) {
               S += wv[8 * q + 2 * i + 1] * (fw[i] >> 16);
             }
             blockv += S * (8 + ((sh.y >> (8 * q)) & 0xFF));  // x (1.mshared_k) in eighths
+            if (G16 && q == 1) {
+              half0 = blockv;
+              blockv = 0;
+            }
           }
-          acc[m] += ldexpf((float)blockv, sh.x + X - 10 - cB);  // one exponent add
+          if (G16) {
+            acc[m] += ldexpf((float)half0, sh.x + X - 10 - cB);
+            acc[m] += ldexpf((float)blockv, sh.x + X1 - 10 - cB);
+          } else {
+            acc[m] += ldexpf((float)blockv, sh.x + X - 10 - cB);  // one exponent add
+          }
         }
       }
     }
@@ -226,13 +239,18 @@ cudaError_t launch_gemv_shiftadd(const mix_gemm_desc_t& d, void* ws, cudaStream_
     p.out = cbuf; p.out_ld = ldc; p.out_bs = cbs; p.out_split_stride = 0;
   }
   const size_t smem = (size_t)d.M * (pl.kc / 32) * (32 * sizeof(int16_t) + sizeof(int2));
+  const bool g16 = b_g16(d);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_shiftadd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = g16 ? cudaFuncSetAttribute(gemv_shiftadd_kernel<true>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+                        : cudaFuncSetAttribute(gemv_shiftadd_kernel<false>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   const dim3 grid((unsigned)((d.N + (kThreads / pl.tpn) - 1) / (kThreads / pl.tpn)), (unsigned)pl.splits,
                   (unsigned)d.batch);
-  gemv_shiftadd_kernel<<<grid, kThreads, smem, st>>>(p);
+  if (g16) gemv_shiftadd_kernel<true><<<grid, kThreads, smem, st>>>(p);
+  else gemv_shiftadd_kernel<false><<<grid, kThreads, smem, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (pl.splits > 1) {
@@ -256,7 +274,7 @@ cudaError_t launch_gemv_shiftadd(const mix_gemm_desc_t& d, void* ws, cudaStream_
       } else {
         uint8_t* os = static_cast<uint8_t*>(d.out_shared) + bt * d.out_batch_stride / 32;
         e = launch_mx_quantize_rows(cb, false, d.M, d.N, ldc, d.epi == MIX_EPI_MXFP4,
-                                    mx_rule_of(d.epi_flags), oc, os, st);
+                                    mx_rule_of(d.epi_flags), false, oc, os, st);
       }
       if (e != cudaSuccess) return e;
     }

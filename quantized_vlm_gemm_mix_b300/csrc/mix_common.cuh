@@ -412,4 +412,21 @@ __device__ __forceinline__ void mx_block32(uint32_t* u, int rule, uint4& w, uint
   }
 }
 
+// One 16-element MX block (the g16 weight formats), as mx_block32.
+template <bool FP4>
+__device__ __forceinline__ void mx_block16(uint32_t* u, int rule, uint2& w, uint32_t& sc) {
+  uint32_t kb = max_abs_bits<16>(u);
+  if (kb > 0x7F800000u) {
+    zero_nans<16>(u);
+    kb = max_abs_bits<16>(u);
+  }
+  w = make_uint2(0, 0);
+  sc = 0;
+  if (kb != 0u) {
+    const int X = mx_shared_exp(kb, FP4, rule);
+    w = make_uint2(mx_codes8(u, X, FP4), mx_codes8(u + 8, X, FP4));
+    sc = (uint32_t)(X + 127);
+  }
+}
+
 }  // namespace mixk

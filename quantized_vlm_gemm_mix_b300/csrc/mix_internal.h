@@ -22,14 +22,20 @@ __host__ __device__ inline int mx_rule_of(unsigned flags) {
 cudaError_t launch_mix_quantize(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld,
                                 int type, int ebias, bool asym, uint8_t* codes, void* shared,
                                 cudaStream_t st, const int* ebias_dev = nullptr);
+// NVFP4 comparison quantiser (tensor scale written to *tensor_scale) and the
+// dead-zone count (fmt 0 MiX, 1 MXINT4, 2 E2M1).
+cudaError_t launch_nvfp4_quantize(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, uint8_t* codes,
+                                  uint8_t* scales, float* tensor_scale, cudaStream_t st);
+cudaError_t launch_underflow_count(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, const uint8_t* codes,
+                                   int fmt, unsigned long long* count, cudaStream_t st);
 // Automatic ebias into one device int (clear, max-reduction, finish).
 cudaError_t launch_auto_ebias(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, int* ebias,
                               cudaStream_t st);
 cudaError_t launch_mx_quantize_rows(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld,
-                                    bool fp4, int rule, uint8_t* codes, uint8_t* scales,
+                                    bool fp4, int rule, bool g16, uint8_t* codes, uint8_t* scales,
                                     cudaStream_t st);
 cudaError_t launch_mx_quantize_cols(const void* x, bool bf16, int64_t kdim, int64_t n, int64_t ld,
-                                    bool fp4, int rule, uint8_t* codes, uint8_t* scales,
+                                    bool fp4, int rule, bool g16, uint8_t* codes, uint8_t* scales,
                                     cudaStream_t st);
 cudaError_t launch_mix_dequantize(const uint8_t* codes, const void* shared, int64_t rows, int64_t k,
                                   int type, int ebias, float* out, cudaStream_t st);
@@ -57,8 +63,12 @@ size_t gemm_tc_workspace_bytes(const mix_gemm_desc_t& d);
 struct StagedPlan {
   bool b_native;
   int64_t k_pad, kt, mt, nt, bb;
-  size_t off_a, off_sfa, off_b, off_sfb, bytes;  // offsets from the 1024-aligned workspace base
+  // offsets from the 1024-aligned workspace base; off_sfe: per-32-block scale
+  // bytes of g16 weights ([bb][N][k_pad / 32]), in B-only plans
+  size_t off_a, off_sfa, off_b, off_sfb, off_sfe, bytes;
 };
+// Weights with one scale per 16 elements (MXINT4g16 / MXFP4g16).
+inline bool b_g16(const mix_gemm_desc_t& d) { return d.b_block == 16; }
 constexpr int kStagedAlign = 1024;
 constexpr int kStagedBN = 224;  // output columns per tile of the staged matmul
 StagedPlan staged_plan(const mix_gemm_desc_t& d);
@@ -68,6 +78,10 @@ int64_t expand_a_threads(const mix_gemm_desc_t& d, const StagedPlan& sp);
 int64_t expand_b_threads(const StagedPlan& sp);
 cudaError_t launch_expand_a(const mix_gemm_desc_t& d, const StagedPlan& sp, unsigned char* base, cudaStream_t st);
 cudaError_t launch_expand_b(const mix_gemm_desc_t& d, const StagedPlan& sp, unsigned char* base, cudaStream_t st);
+
+// Fused decode attention.
+size_t decode_attention_ws_bytes(const mix_decode_attn_desc_t& d);
+cudaError_t launch_decode_attention(const mix_decode_attn_desc_t& d, void* ws, cudaStream_t st);
 
 // K-smoothing.
 size_t ksmooth_ws_bytes(int64_t tokens, int heads, int head_dim);

@@ -56,6 +56,10 @@ __device__ __forceinline__ void load8(const void* base, int64_t elem, uint32_t* 
   }
 }
 
+__device__ __forceinline__ uint32_t pair_max(uint32_t v) {
+  return max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
+}
+
 __device__ __forceinline__ uint32_t quad_max(uint32_t v) {
   v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 1));
   return max(v, __shfl_xor_sync(0xFFFFFFFFu, v, 2));
@@ -123,6 +127,105 @@ __global__ void __launch_bounds__(kThreads, 4) mix_quantize_kernel(
   }
 }
 
+// NVFP4 (a comparison format: 16-element blocks of E2M1, an E4M3 block scale
+// and one fp32 tensor scale).  One thread per 16-element block; every
+// decision is an IEEE fp32 operation in the order the definition fixes:
+// t = (amax_b / s_t) / 6, its E4M3 code (nearest even, saturating), d =
+// e4m3(sb) * s_t, then E2M1 of x / d.  s_t comes from the tensor's largest
+// finite |x| (the automatic-ebias reduction), finished in place.
+__device__ __forceinline__ uint32_t e4m3_rn_satfinite(float t) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 h;\n\tcvt.rn.satfinite.e4m3x2.f32 h, %1, %2;\n\tcvt.u32.u16 %0, h;\n\t}"
+      : "=r"(r)
+      : "f"(0.0f), "f"(t));
+  return r & 0xFFu;
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t b) {  // b <= 0x7E
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0x1p-9f;
+}
+
+__global__ void nvfp4_scale_finish_kernel(float* __restrict__ ts) {
+  if (threadIdx.x != 0) return;
+  const uint32_t key = *reinterpret_cast<const unsigned*>(ts);
+  float s = 1.0f;
+  if (key != 0u) {
+    s = __fdiv_rn(__uint_as_float(key), 2688.0f);
+    if (s == 0.0f) s = 0x1p-149f;
+  }
+  *ts = s;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) nvfp4_quantize_kernel(const void* __restrict__ x, int64_t rows,
+                                                                  int64_t nb, int64_t ld, FastDiv fnb,
+                                                                  const float* __restrict__ ts,
+                                                                  uint8_t* __restrict__ codes,
+                                                                  uint8_t* __restrict__ scales) {
+  const float st = *ts;
+  const int64_t total = rows * nb;
+  for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < total; g += (int64_t)gridDim.x * kThreads) {
+    const uint32_t row = fdiv((uint32_t)g, fnb);
+    const int64_t e = (int64_t)row * ld + (g - (int64_t)row * nb) * 16;
+    uint32_t u[16];
+    load8<BF16>(x, e, u);
+    load8<BF16>(x, e + 8, u + 8);
+    uint32_t kb = max_abs_bits<16>(u);
+    if (kb > 0x7F800000u) {
+      zero_nans<16>(u);
+      kb = max_abs_bits<16>(u);
+    }
+    const float t = __fdiv_rn(__fdiv_rn(__uint_as_float(kb), st), 6.0f);
+    const uint32_t sb = e4m3_rn_satfinite(t);
+    uint2 w = make_uint2(0u, 0u);
+    if (sb != 0u) {
+      const float d = __fmul_rn(e4m3_to_f32(sb), st);
+      uint32_t c[2] = {0u, 0u};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        c[i >> 2] |= e2m1x2(__fdiv_rn(__uint_as_float(u[2 * i]), d), __fdiv_rn(__uint_as_float(u[2 * i + 1]), d))
+                     << (8 * (i & 3));
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {  // -0 (nibble 0x8) -> +0
+        const uint32_t tt = c[j] ^ 0x88888888u;
+        const uint32_t nz = (tt | (tt >> 1) | (tt >> 2) | (tt >> 3)) & 0x11111111u;
+        c[j] &= ~((~nz & 0x11111111u) << 3);
+      }
+      w = make_uint2(c[0], c[1]);
+    }
+    __stcs(reinterpret_cast<uint2*>(codes + g * 8), w);
+    scales[g] = (uint8_t)sb;
+  }
+}
+
+// Dead-zone count: finite nonzero inputs whose code is a zero code (MiX 0x7,
+// MXINT4 0, E2M1 +-0).  One thread per eight elements (one code word), one
+// atomic per warp.
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) underflow_count_kernel(const void* __restrict__ x, int64_t rows,
+                                                                   int64_t wpr, int64_t ld, FastDiv fw, int fmt,
+                                                                   const uint8_t* __restrict__ codes,
+                                                                   unsigned long long* __restrict__ count) {
+  const int64_t total = rows * wpr;
+  unsigned n = 0;
+  for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < total; g += (int64_t)gridDim.x * kThreads) {
+    const uint32_t row = fdiv((uint32_t)g, fw);
+    const int64_t j = g - (int64_t)row * wpr;
+    uint32_t u[8];
+    load8<BF16>(x, (int64_t)row * ld + j * 8, u);
+    const uint32_t cw = __ldcs(reinterpret_cast<const uint32_t*>(codes) + g);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t a = u[i] & 0x7FFFFFFFu, c = (cw >> (4 * i)) & 0xFu;
+      const bool zero = fmt == 0 ? c == 7u : (fmt == 1 ? c == 0u : (c & 7u) == 0u);
+      n += (a != 0u && a < 0x7F800000u && zero) ? 1u : 0u;
+    }
+  }
+  n = __reduce_add_sync(0xFFFFFFFFu, n);
+  if ((threadIdx.x & 31) == 0 && n != 0u) atomicAdd(count, (unsigned long long)n);
+}
+
 // Automatic ebias, pass 1: the largest finite |x| of the tensor, as the
 // integer maximum of the magnitude bits (the order of non-negative floats).
 // Rounding a block maximum to three mantissa bits never lowers a larger one
@@ -187,7 +290,8 @@ __global__ void auto_ebias_finish_kernel(int* __restrict__ ebias) {
   *ebias = e;
 }
 
-template <bool BF16, bool FP4>
+// G16: a pair of lanes per 16-element block (one scale per pair).
+template <bool BF16, bool FP4, bool G16>
 __global__ void __launch_bounds__(kThreads, 4) mx_quantize_rows_kernel(
     const void* __restrict__ x, int64_t rows, int64_t nb, int64_t ld, int rule,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales, FastDiv fnb) {
@@ -212,10 +316,10 @@ __global__ void __launch_bounds__(kThreads, 4) mx_quantize_rows_kernel(
     }
 #pragma unroll
     for (int r = 0; r < kUnroll; ++r) {
-      uint32_t kb = quad_max(max_abs_bits<8>(u[r]));
+      uint32_t kb = G16 ? pair_max(max_abs_bits<8>(u[r])) : quad_max(max_abs_bits<8>(u[r]));
       if (__any_sync(0xFFFFFFFFu, kb > 0x7F800000u)) {  // a NaN in some block of the warp
         zero_nans<8>(u[r]);
-        kb = quad_max(max_abs_bits<8>(u[r]));
+        kb = G16 ? pair_max(max_abs_bits<8>(u[r])) : quad_max(max_abs_bits<8>(u[r]));
       }
       uint32_t word = 0u, sc = 0u;
       if (kb != 0u) {
@@ -225,7 +329,11 @@ __global__ void __launch_bounds__(kThreads, 4) mx_quantize_rows_kernel(
       }
       if (g[r] < total) {
         __stcs(reinterpret_cast<uint32_t*>(codes + g[r] * 16 + q * 4), word);
-        if (q == 0) scales[g[r]] = (uint8_t)sc;
+        if (G16) {
+          if ((q & 1) == 0) scales[2 * g[r] + (q >> 1)] = (uint8_t)sc;
+        } else if (q == 0) {
+          scales[g[r]] = (uint8_t)sc;
+        }
       }
     }
   }
@@ -236,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 4) mx_quantize_rows_kernel(
 // contiguous 128-byte (bf16) or 256-byte (fp32) row segment.  The eight warps
 // of a CTA own eight consecutive k-blocks, so each column's 128 code bytes are
 // written by one CTA.
-template <bool BF16, bool FP4>
+template <bool BF16, bool FP4, bool G16>
 __global__ void __launch_bounds__(kThreads) mx_quantize_cols_kernel(
     const void* __restrict__ x, int64_t kdim, int64_t n, int64_t ld, int rule,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
@@ -276,12 +384,22 @@ __global__ void __launch_bounds__(kThreads) mx_quantize_cols_kernel(
   for (int c = 0; c < 2; ++c) {
     if (c == 1 && !two) break;
     uint32_t* u = c ? u1 : u0;
-    uint4 w;
-    uint32_t sc;
-    mx_block32<FP4>(u, rule, w, sc);
     const int64_t col = n0 + c;
-    *reinterpret_cast<uint4*>(codes + col * (kdim / 2) + kb * 16) = w;
-    scales[col * nbk + kb] = (uint8_t)sc;
+    if (G16) {
+      uint2 w0, w1;
+      uint32_t s0, s1;
+      mx_block16<FP4>(u, rule, w0, s0);
+      mx_block16<FP4>(u + 16, rule, w1, s1);
+      *reinterpret_cast<uint4*>(codes + col * (kdim / 2) + kb * 16) = make_uint4(w0.x, w0.y, w1.x, w1.y);
+      scales[col * 2 * nbk + 2 * kb] = (uint8_t)s0;
+      scales[col * 2 * nbk + 2 * kb + 1] = (uint8_t)s1;
+    } else {
+      uint4 w;
+      uint32_t sc;
+      mx_block32<FP4>(u, rule, w, sc);
+      *reinterpret_cast<uint4*>(codes + col * (kdim / 2) + kb * 16) = w;
+      scales[col * nbk + kb] = (uint8_t)sc;
+    }
   }
 }
 
@@ -380,57 +498,99 @@ cudaError_t launch_mix_quantize(const void* x, bool bf16, int64_t rows, int64_t 
   return cudaGetLastError();
 }
 
-cudaError_t launch_auto_ebias(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, int* ebias,
-                              cudaStream_t st) {
+// The largest finite |x| bit pattern into *key (cleared first).
+cudaError_t launch_auto_ebias_key(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, unsigned* key,
+                                  cudaStream_t st) {
   const int es = bf16 ? 2 : 4;
-  const int64_t vpr = k * es / 16;   // 16-byte vectors per row (k % 32 == 0)
+  const int64_t vpr = k * es / 16;   // 16-byte vectors per row (k % 16 == 0)
   if (rows * vpr >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;  // 32-bit vector index
-  cudaError_t e = cudaMemsetAsync(ebias, 0, sizeof(int), st);
+  cudaError_t e = cudaMemsetAsync(key, 0, sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
   if (rows > 0 && vpr > 0) {
     int64_t gb = (rows * vpr + (int64_t)kThreads * kAmaxUnroll - 1) / ((int64_t)kThreads * kAmaxUnroll);
     if (gb > (int64_t)num_sms() * 8) gb = (int64_t)num_sms() * 8;
     const FastDiv f = make_fastdiv((uint32_t)vpr);
-    unsigned* key = reinterpret_cast<unsigned*>(ebias);
     if (bf16) amax_bits_kernel<true><<<(int)gb, kThreads, 0, st>>>(x, rows, vpr, ld * es, f, key);
     else amax_bits_kernel<false><<<(int)gb, kThreads, 0, st>>>(x, rows, vpr, ld * es, f, key);
     e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
   }
+  return e;
+}
+
+cudaError_t launch_auto_ebias(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, int* ebias,
+                              cudaStream_t st) {
+  cudaError_t e = launch_auto_ebias_key(x, bf16, rows, k, ld, reinterpret_cast<unsigned*>(ebias), st);
+  if (e != cudaSuccess) return e;
   auto_ebias_finish_kernel<<<1, 32, 0, st>>>(ebias);
   return cudaGetLastError();
 }
 
+cudaError_t launch_nvfp4_quantize(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, uint8_t* codes,
+                                  uint8_t* scales, float* tensor_scale, cudaStream_t st) {
+  cudaError_t e = launch_auto_ebias_key(x, bf16, rows, k, ld, reinterpret_cast<unsigned*>(tensor_scale), st);
+  if (e != cudaSuccess) return e;
+  nvfp4_scale_finish_kernel<<<1, 32, 0, st>>>(tensor_scale);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || rows == 0 || k == 0) return e;
+  const int64_t nb = k / 16;
+  if (rows * nb >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;
+  int64_t gb = (rows * nb + kThreads - 1) / kThreads;
+  if (gb > (int64_t)num_sms() * 8) gb = (int64_t)num_sms() * 8;
+  const FastDiv f = make_fastdiv((uint32_t)nb);
+  if (bf16) nvfp4_quantize_kernel<true><<<(int)gb, kThreads, 0, st>>>(x, rows, nb, ld, f, tensor_scale, codes, scales);
+  else nvfp4_quantize_kernel<false><<<(int)gb, kThreads, 0, st>>>(x, rows, nb, ld, f, tensor_scale, codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_underflow_count(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, const uint8_t* codes,
+                                   int fmt, unsigned long long* count, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(count, 0, sizeof(unsigned long long), st);
+  if (e != cudaSuccess || rows == 0 || k == 0) return e;
+  const int64_t wpr = k / 8;
+  if (rows * wpr >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;
+  int64_t gb = (rows * wpr + kThreads - 1) / kThreads;
+  if (gb > (int64_t)num_sms() * 8) gb = (int64_t)num_sms() * 8;
+  const FastDiv f = make_fastdiv((uint32_t)wpr);
+  if (bf16) underflow_count_kernel<true><<<(int)gb, kThreads, 0, st>>>(x, rows, wpr, ld, f, fmt, codes, count);
+  else underflow_count_kernel<false><<<(int)gb, kThreads, 0, st>>>(x, rows, wpr, ld, f, fmt, codes, count);
+  return cudaGetLastError();
+}
+
+
 cudaError_t launch_mx_quantize_rows(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld,
-                                    bool fp4, int rule, uint8_t* codes, uint8_t* scales,
+                                    bool fp4, int rule, bool g16, uint8_t* codes, uint8_t* scales,
                                     cudaStream_t st) {
   const int64_t nb = k / 32;
   if (rows * nb >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;  // 32-bit block index
   const int grid = grid_for(rows * nb);
-  const int fr = rule;
   const FastDiv f = make_fastdiv((uint32_t)nb);
+#define MXR(BF, F4, G)                                                                                 \
+  mx_quantize_rows_kernel<BF, F4, G><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, rule, codes, scales, f)
   if (bf16) {
-    if (fp4) mx_quantize_rows_kernel<true, true><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales, f);
-    else mx_quantize_rows_kernel<true, false><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales, f);
+    if (fp4) { if (g16) MXR(true, true, true); else MXR(true, true, false); }
+    else { if (g16) MXR(true, false, true); else MXR(true, false, false); }
   } else {
-    if (fp4) mx_quantize_rows_kernel<false, true><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales, f);
-    else mx_quantize_rows_kernel<false, false><<<grid, kThreads, 0, st>>>(x, rows, nb, ld, fr, codes, scales, f);
+    if (fp4) { if (g16) MXR(false, true, true); else MXR(false, true, false); }
+    else { if (g16) MXR(false, false, true); else MXR(false, false, false); }
   }
+#undef MXR
   return cudaGetLastError();
 }
 
 cudaError_t launch_mx_quantize_cols(const void* x, bool bf16, int64_t kdim, int64_t n, int64_t ld,
-                                    bool fp4, int rule, uint8_t* codes, uint8_t* scales,
+                                    bool fp4, int rule, bool g16, uint8_t* codes, uint8_t* scales,
                                     cudaStream_t st) {
   const dim3 grid((unsigned)((n + 63) / 64), (unsigned)((kdim / 32 + 7) / 8));
-  const int fr = rule;
+#define MXC(BF, F4, G) \
+  mx_quantize_cols_kernel<BF, F4, G><<<grid, kThreads, 0, st>>>(x, kdim, n, ld, rule, codes, scales)
   if (bf16) {
-    if (fp4) mx_quantize_cols_kernel<true, true><<<grid, kThreads, 0, st>>>(x, kdim, n, ld, fr, codes, scales);
-    else mx_quantize_cols_kernel<true, false><<<grid, kThreads, 0, st>>>(x, kdim, n, ld, fr, codes, scales);
+    if (fp4) { if (g16) MXC(true, true, true); else MXC(true, true, false); }
+    else { if (g16) MXC(true, false, true); else MXC(true, false, false); }
   } else {
-    if (fp4) mx_quantize_cols_kernel<false, true><<<grid, kThreads, 0, st>>>(x, kdim, n, ld, fr, codes, scales);
-    else mx_quantize_cols_kernel<false, false><<<grid, kThreads, 0, st>>>(x, kdim, n, ld, fr, codes, scales);
+    if (fp4) { if (g16) MXC(false, true, true); else MXC(false, true, false); }
+    else { if (g16) MXC(false, false, true); else MXC(false, false, false); }
   }
+#undef MXC
   return cudaGetLastError();
 }
 

@@ -22,13 +22,15 @@ MIX_ERR_UNSUPPORTED, MIX_ERR_CUDA, MIX_ERR_WORKSPACE, MIX_ERR_DEVICE = 4, 5, 6, 
 MIX_T1_4P25, MIX_T2_4P5 = 1, 2
 MX_INT4, MX_FP4_E2M1 = 0, 1
 MIX_DT_F32, MIX_DT_BF16 = 0, 1
-MIX_ASYM_ZERO, MX_SCALE_FLOOR, MX_SCALE_TIGHT = 1, 2, 4
+MIX_ASYM_ZERO, MX_SCALE_FLOOR, MX_SCALE_TIGHT, MX_BLOCK16 = 1, 2, 4, 8
+MIX_UF_MIX, MIX_UF_MXINT4, MIX_UF_E2M1 = 0, 1, 2
 MIX_EPI_NONE, MIX_EPI_MIX_T1, MIX_EPI_MIX_T2, MIX_EPI_MXINT4, MIX_EPI_MXFP4 = 0, 1, 2, 3, 4
 MIX_GEMM_AUTO, MIX_GEMM_TCGEN05, MIX_GEMM_SHIFTADD, MIX_GEMM_TCGEN05_STAGED, MIX_GEMM_TCGEN05_FUSED = 0, 1, 2, 3, 4
 KSMOOTH_COMPUTE, KSMOOTH_APPLY_FROZEN = 0, 1
 
 EXPORTS = ["mix_codes_bytes", "mix_shared_bytes", "mx_scales_bytes", "mix_quantize", "mix_auto_ebias",
-           "mix_quantize_auto", "mx_quantize",
+           "mix_quantize_auto", "mx_quantize", "nvfp4_quantize", "mix_underflow_count",
+           "mix_decode_attention_workspace_bytes", "mix_decode_attention",
            "mix_dequantize", "mx_dequantize", "mix_mx_gemm_workspace_bytes", "mix_mx_gemm",
            "ksmooth_workspace_bytes", "ksmooth_kv", "ksmooth_kv_noalloc", "mix_status_str", "mix_device_error",
            "mix_version"]
@@ -50,12 +52,26 @@ class GemmDesc(ctypes.Structure):
         ("a_type", ctypes.c_int), ("a_ebias", ctypes.c_int),
         ("a_ld", ctypes.c_int64), ("a_batch_stride", ctypes.c_int64),
         ("b_codes", ctypes.c_void_p), ("b_scales", ctypes.c_void_p), ("b_type", ctypes.c_int),
+        ("b_block", ctypes.c_int),
         ("b_ld", ctypes.c_int64), ("b_batch_stride", ctypes.c_int64),
         ("c", ctypes.c_void_p), ("ldc", ctypes.c_int64), ("c_batch_stride", ctypes.c_int64),
         ("epi", ctypes.c_int), ("epi_ebias", ctypes.c_int), ("epi_flags", ctypes.c_uint),
         ("out_codes", ctypes.c_void_p), ("out_shared", ctypes.c_void_p),
         ("out_ld", ctypes.c_int64), ("out_batch_stride", ctypes.c_int64),
         ("algo", ctypes.c_int),
+    ]
+
+
+class DecodeAttnDesc(ctypes.Structure):
+    """mix_decode_attn_desc_t."""
+    _fields_ = [
+        ("tokens", ctypes.c_int64), ("q_heads", ctypes.c_int), ("kv_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int), ("dtype", ctypes.c_int),
+        ("q", ctypes.c_void_p), ("k_new", ctypes.c_void_p), ("k_mean", ctypes.c_void_p),
+        ("k_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p), ("v_scales", ctypes.c_void_p), ("v_ld", ctypes.c_int64),
+        ("sm_scale", ctypes.c_float), ("q_ebias", ctypes.c_int), ("p_ebias", ctypes.c_int),
+        ("out", ctypes.c_void_p), ("p_codes", ctypes.c_void_p), ("p_shared", ctypes.c_void_p),
     ]
 
 
@@ -70,6 +86,10 @@ def _load():
         "mx_scales_bytes": (S, [I64, I64]),
         "mix_quantize": (I, [P, I, I64, I64, I64, I, I, U, P, P, P]),
         "mix_auto_ebias": (I, [P, I, I64, I64, I64, P, P]),
+        "nvfp4_quantize": (I, [P, I, I64, I64, I64, P, P, P, P]),
+        "mix_decode_attention_workspace_bytes": (S, [P]),
+        "mix_decode_attention": (I, [P, P, S, P]),
+        "mix_underflow_count": (I, [P, I, I64, I64, I64, P, I, P, P]),
         "mix_quantize_auto": (I, [P, I, I64, I64, I64, I, U, P, P, P, P]),
         "mx_quantize": (I, [P, I, I64, I64, I64, I, I, U, P, P, P]),
         "mix_dequantize": (I, [P, P, I64, I64, I, I, P, P]),
@@ -156,6 +176,42 @@ def mix_quantize_auto(x, rows, k, ld, mix_type, flags, codes, shared, ebias, str
                                  _ptr(ebias), _stream(stream)), "mix_quantize_auto")
 
 
+def nvfp4_quantize(x, rows, k, ld, codes, scales, tensor_scale, stream=None) -> None:
+    _check(lib.nvfp4_quantize(_ptr(x), _dtype(x), rows, k, ld, _ptr(codes), _ptr(scales), _ptr(tensor_scale),
+                              _stream(stream)), "nvfp4_quantize")
+
+
+def mix_underflow_count(x, rows, k, ld, codes, fmt, count, stream=None) -> None:
+    _check(lib.mix_underflow_count(_ptr(x), _dtype(x), rows, k, ld, _ptr(codes), fmt, _ptr(count), _stream(stream)),
+           "mix_underflow_count")
+
+
+def decode_attention_desc(q, k_codes, k_scales, v_codes, v_scales, tokens, sm_scale, out, k_new=None, k_mean=None,
+                          q_ebias=-8, p_ebias=-15, p_codes=None, p_shared=None) -> DecodeAttnDesc:
+    """q [HQ, 128]; K' cache codes [T, HK, 64], scales [T, HK, 4]; V planes [HK, 128, Tv/2], [HK, 128, Tv/32]."""
+    d = DecodeAttnDesc()
+    d._keep = [t for t in (q, k_codes, k_scales, v_codes, v_scales, out, k_new, k_mean, p_codes, p_shared)
+               if t is not None]
+    d.tokens, d.q_heads, d.kv_heads, d.head_dim = tokens, q.shape[0], k_codes.shape[1], q.shape[1]
+    d.dtype = _dtype(q)
+    d.q, d.k_new, d.k_mean = _ptr(q), _ptr(k_new), _ptr(k_mean)
+    d.k_codes, d.k_scales, d.v_codes, d.v_scales = _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales)
+    d.v_ld = v_codes.shape[-1] * 2
+    d.sm_scale, d.q_ebias, d.p_ebias = sm_scale, q_ebias, p_ebias
+    d.out, d.p_codes, d.p_shared = _ptr(out), _ptr(p_codes), _ptr(p_shared)
+    return d
+
+
+def decode_attention(desc: DecodeAttnDesc, workspace=None, stream=None):
+    """mix_decode_attention; allocates the workspace with torch when none is given."""
+    need = lib.mix_decode_attention_workspace_bytes(ctypes.byref(desc))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    _check(lib.mix_decode_attention(ctypes.byref(desc), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mix_decode_attention")
+    return workspace
+
+
 def mx_quantize(x, rows, cols, ld, axis, mx_type, flags, codes, scales, stream=None) -> None:
     _check(lib.mx_quantize(_ptr(x), _dtype(x), rows, cols, ld, axis, mx_type, flags, _ptr(codes),
                            _ptr(scales), _stream(stream)), "mx_quantize")
@@ -236,13 +292,32 @@ def quantize_mix_auto(x: torch.Tensor, mix_type: int = MIX_T2_4P5, flags: int = 
     return codes, shared, ebias
 
 
+def quantize_nvfp4(x: torch.Tensor, stream=None):
+    """x [rows, k] -> (codes uint8 [rows, k/2], E4M3 scales uint8 [rows, k/16], tensor scale float32 [1])."""
+    rows, k = x.shape
+    assert x.stride(1) == 1
+    codes = torch.empty((rows, k // 2), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((rows, k // 16), dtype=torch.uint8, device=x.device)
+    ts = torch.empty((1,), dtype=torch.float32, device=x.device)
+    nvfp4_quantize(x, rows, k, x.stride(0), codes, scales, ts, stream)
+    return codes, scales, ts
+
+
+def underflow_count(x: torch.Tensor, codes: torch.Tensor, fmt: int, stream=None) -> torch.Tensor:
+    """Device count (int64 [1]) of finite nonzero x whose code is a zero code."""
+    rows, k = x.shape
+    n = torch.empty((1,), dtype=torch.int64, device=x.device)
+    mix_underflow_count(x, rows, k, x.stride(0), codes, fmt, n, stream)
+    return n
+
+
 def quantize_mx(x: torch.Tensor, axis: int, mx_type: int, flags: int = 0, stream=None):
-    """axis=1: x [N, K]; axis=0: x [K, N] -> (codes [N, K/2], scales [N, K/32])."""
+    """axis=1: x [N, K]; axis=0: x [K, N] -> (codes [N, K/2], scales [N, K/32], or K/16 with MX_BLOCK16)."""
     rows, cols = x.shape
     assert x.stride(1) == 1
     N, K = (rows, cols) if axis == 1 else (cols, rows)
     codes = torch.empty((N, K // 2), dtype=torch.uint8, device=x.device)
-    scales = torch.empty((N, K // 32), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((N, K // (16 if flags & MX_BLOCK16 else 32)), dtype=torch.uint8, device=x.device)
     mx_quantize(x, rows, cols, x.stride(0), axis, mx_type, flags, codes, scales, stream)
     return codes, scales
 
@@ -250,7 +325,7 @@ def quantize_mx(x: torch.Tensor, axis: int, mx_type: int, flags: int = 0, stream
 def gemm_desc(M, N, K, a_codes, a_shared, a_type, a_ebias, b_codes, b_scales, b_type, c=None,
               epi=MIX_EPI_NONE, epi_ebias=-8, epi_flags=MIX_ASYM_ZERO, out_codes=None, out_shared=None,
               batch=1, b_group=1, a_ld=None, a_batch_stride=None, b_ld=None, b_batch_stride=None,
-              ldc=None, c_batch_stride=None, out_ld=None, out_batch_stride=None, algo=MIX_GEMM_AUTO) -> GemmDesc:
+              ldc=None, c_batch_stride=None, out_ld=None, out_batch_stride=None, algo=MIX_GEMM_AUTO, b_block=32) -> GemmDesc:
     d = GemmDesc()
     # the descriptor holds raw device pointers: keep the tensors alive with it
     d._keep = [t for t in (a_codes, a_shared, b_codes, b_scales, c, out_codes, out_shared) if t is not None]
@@ -258,7 +333,7 @@ def gemm_desc(M, N, K, a_codes, a_shared, a_type, a_ebias, b_codes, b_scales, b_
     d.a_codes, d.a_shared, d.a_type, d.a_ebias = _ptr(a_codes), _ptr(a_shared), a_type, a_ebias
     d.a_ld = K if a_ld is None else a_ld
     d.a_batch_stride = M * d.a_ld if a_batch_stride is None else a_batch_stride
-    d.b_codes, d.b_scales, d.b_type = _ptr(b_codes), _ptr(b_scales), b_type
+    d.b_codes, d.b_scales, d.b_type, d.b_block = _ptr(b_codes), _ptr(b_scales), b_type, b_block
     d.b_ld = K if b_ld is None else b_ld
     d.b_batch_stride = N * d.b_ld if b_batch_stride is None else b_batch_stride
     d.c = _ptr(c)

@@ -76,6 +76,10 @@ def test_validation_rejects_before_launch(mix):
     d.N, d.epi, d.epi_flags = 64, mix.MIX_EPI_MXFP4, mix.MX_SCALE_FLOOR | mix.MX_SCALE_TIGHT
     assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_INVALID_ARG
     d.epi, d.epi_flags = mix.MIX_EPI_MIX_T2, 1
+    d.b_block = 8                                   # only 32 (or 0) and 16 exist
+    assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_INVALID_ARG
+    d.b_block = 0
+    assert L.mx_quantize(None, 1, 64, 64, 64, 1, 1, 16, None, None, None) == mix.MIX_ERR_INVALID_ARG
     assert L.ksmooth_kv(None, 1, 16, 4, 12, 48, None, 0, None, None, 0, None) in (mix.MIX_ERR_SHAPE,
                                                                                  mix.MIX_ERR_INVALID_ARG)
 
