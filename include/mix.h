@@ -328,7 +328,7 @@ MIX_API mix_status_t ksmooth_kv_noalloc(const void* k, mix_dtype_t dtype, int64_
  * head's largest |O|. */
 typedef struct {
   int64_t tokens;        /* cache length including the new token (>= 1)        */
-  int q_heads, kv_heads; /* q_heads % kv_heads == 0, q_heads / kv_heads <= 16   */
+  int q_heads, kv_heads; /* q_heads % kv_heads == 0, q_heads / kv_heads <= 8    */
   int head_dim;          /* 128                                                 */
   mix_dtype_t dtype;     /* of q and k_new                                      */
   const void* q;         /* [q_heads][head_dim]                                  */

@@ -166,7 +166,7 @@ mix_status_t mix_underflow_count(const void* x, mix_dtype_t dtype, int64_t rows,
 static mix_status_t validate_attn(const mix_decode_attn_desc_t* d) {
   if (d == nullptr) return MIX_ERR_INVALID_ARG;
   if (d->tokens < 1 || d->q_heads < 1 || d->kv_heads < 1 || d->q_heads % d->kv_heads != 0 ||
-      d->q_heads / d->kv_heads > 16 || !valid_dtype(d->dtype))
+      d->q_heads / d->kv_heads > 8 || !valid_dtype(d->dtype))
     return MIX_ERR_INVALID_ARG;
   if (d->head_dim != 128 || d->v_ld % 32 != 0 || d->v_ld < d->tokens) return MIX_ERR_SHAPE;
   if (d->q_ebias < -100 || d->q_ebias > 100 || d->p_ebias < -100 || d->p_ebias > 100) return MIX_ERR_INVALID_ARG;

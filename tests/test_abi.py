@@ -134,3 +134,30 @@ def test_staged_gemm_workspace_size_and_check(mix):
     assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) > 0
     d.algo = 5
     assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_INVALID_ARG
+
+
+def test_decode_attention_validation(mix):
+    """Host-side checks of the fused decode attention (no launch)."""
+    import ctypes
+    L = mix.lib
+    d = mix.DecodeAttnDesc()
+    d.tokens, d.q_heads, d.kv_heads, d.head_dim, d.dtype = 100, 28, 4, 128, mix.MIX_DT_BF16
+    d.q = d.k_codes = d.k_scales = d.v_codes = d.v_scales = d.out = 4096   # placeholders, never dereferenced
+    d.v_ld, d.sm_scale, d.q_ebias, d.p_ebias = 128, 0.088, -8, -15
+    need = L.mix_decode_attention_workspace_bytes(ctypes.byref(d))
+    # S [28][256] + statistics [2][28] + partial O [1][28][128] + tickets, each 256-aligned, + 256
+    assert need == 28 * 256 * 4 + 512 + 28 * 128 * 4 + 256 + 256
+    assert L.mix_decode_attention(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_WORKSPACE
+    for field, value, want in (("q_heads", 64, mix.MIX_ERR_INVALID_ARG),     # 16 query heads per KV head
+                               ("q_heads", 30, mix.MIX_ERR_INVALID_ARG),     # not a multiple of kv_heads
+                               ("head_dim", 64, mix.MIX_ERR_SHAPE),
+                               ("v_ld", 96, mix.MIX_ERR_SHAPE),              # below the token count
+                               ("v_ld", 120, mix.MIX_ERR_SHAPE),             # not a multiple of 32
+                               ("tokens", 0, mix.MIX_ERR_INVALID_ARG),
+                               ("k_new", 4096, mix.MIX_ERR_INVALID_ARG)):    # a new key without the mean
+        saved = getattr(d, field)
+        setattr(d, field, value)
+        assert L.mix_decode_attention(ctypes.byref(d), None, 0, None) == want, field
+        assert L.mix_decode_attention_workspace_bytes(ctypes.byref(d)) == 0
+        setattr(d, field, saved)
+

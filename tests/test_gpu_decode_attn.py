@@ -59,7 +59,7 @@ def run_both(mix, orc, q, kn, mean, kc, ks, vc, vs, T, sm, append=True):
 
 
 @pytest.mark.parametrize("T,HQ,HK", [(8192, 28, 4), (80, 28, 4), (1, 28, 4), (257, 28, 4), (300, 4, 4),
-                                     (1000, 32, 2)])
+                                     (1000, 16, 2)])
 def test_decode_attention_matches_oracle(mix, orc, T, HQ, HK):
     q, kn, mean, kc, ks, vc, vs = make_cache(orc, T + HQ, T, HQ, HK, prefill=max(1, T // 2))
     (o, kcg, ksg, pc, psh), (O, kco, kso, rpc, rps) = run_both(mix, orc, q, kn, mean, kc, ks, vc, vs, T,
