@@ -89,7 +89,8 @@ def plane_bytes(rows, k, t):
 # ---------------------------------------------------------------------------
 
 def dims(small=False):
-    s = 8 if small else 1
+    """Sizes of the step; small = a divisor of the token counts (True means 8)."""
+    s = (8 if small is True else int(small)) if small else 1
     return dict(M=4096 // s, DM=3584, DF=18944, QKV=4608, MV=16384 // s, T=4096 // s, TC=8192 // s,
                 HQ=28, HK=4, D=128)
 
@@ -661,6 +662,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--small", action="store_true", help="1/8-size workload (for profiler captures)")
+    ap.add_argument("--div", type=int, default=0,
+                    help="divide the token counts by this instead (2 or 4: profiler captures of steady-state tiles)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     ap.add_argument("--no-ext", action="store_true", help="skip the kernels measured beside the step")
@@ -686,6 +689,8 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
+    if args.div > 1:
+        args.small = args.div
     calls, h2d, d2h, host, keep = build_workload(torch, mix, synth, dev, small=args.small)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
@@ -872,7 +877,7 @@ def main():
            "scaling": "weak", "vs_baseline": None,
            "dtype": "e4m3 x e4m3 -> fp32 (tcgen05 kind::mxf8f6f4); int32 shift-add; u8 codes",
            "data": "synthetic (seeded; Qwen2-VL-7B / ViT / GQA-attention shapes, paper activation statistics)",
-           "config": {"workload": WORKLOAD + ("_small" if args.small else ""),
+           "config": {"workload": WORKLOAD + (f"_div{8 if args.small is True else args.small}" if args.small else ""),
                       "l2": "inputs larger than L2 (several GB per step; each tensor is evicted before reuse)",
                       "parallelism": f"replicas x{world}", "roofline_ms_per_step": round(roof_s * 1e3, 4),
                       "hbm_peak_gbs": HBM, "mma_peak_tflops": round(MX8_TFLOPS, 1), "timing": timing_mode,

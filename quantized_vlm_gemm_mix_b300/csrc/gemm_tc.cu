@@ -58,25 +58,33 @@ constexpr int S_CODES = 3;
 constexpr int A_CODES = BM * KB;                     // 8 KB
 constexpr int A_OPS = BM * BK, B_OPS = BN * BK;      // 16 KB, 32 KB (also the padded E2M1 tile)
 constexpr int DEC_WARP0 = 4, NUM_DEC_WARPS = 16;
-constexpr int NUM_THREADS = (DEC_WARP0 + NUM_DEC_WARPS) * 32;
+constexpr int SFW_WARP0 = DEC_WARP0 + NUM_DEC_WARPS;  // four scale warps, one per TMEM lane quadrant
+constexpr int NUM_THREADS = (SFW_WARP0 + 4) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL = 256;  // stage s: A scales at SF_COL + 16 s (4 cols), B at + 4 (8 cols)
 constexpr long long WAIT_LIMIT = 1LL << 31;  // SM clocks, about one second
 
 // Shared memory plan of the fused-decode kernel (offsets from a 1024-byte
-// aligned base).  The B tile goes straight into the MMA operand buffer by TMA:
-// MXFP4 weights through the unpacking load (16 x E2M1 into 16-byte slots),
-// anything else from its e4m3 expansion in the workspace.
+// aligned base) for output tiles TBN (256, or 128 for narrow outputs) columns
+// wide.  The B tile goes straight into the MMA operand buffer by TMA: MXFP4
+// weights through the unpacking load (16 x E2M1 into 16-byte slots), anything
+// else from its e4m3 expansion in the workspace.  The smaller B ring of the
+// 128-column tile leaves room for a deeper ring of A codes (8 stages instead
+// of 3): the codes stream from HBM and the ring depth sets how many loads are
+// in flight.
+template <int TBN>
 struct Plan {
   static constexpr int S_OPS = 4;
+  static constexpr int S_CODES_ = TBN == 256 ? 3 : 8;
+  static constexpr int B_OPS_ = TBN * BK;
   static constexpr int OFF_AOPS = 0;
   static constexpr int OFF_BOPS = OFF_AOPS + S_OPS * A_OPS;
-  static constexpr int OFF_ACODES = OFF_BOPS + S_OPS * B_OPS;
-  static constexpr int OFF_SFA = OFF_ACODES + S_CODES * A_CODES;  // [S_OPS][BM] words
-  static constexpr int OFF_SFB = OFF_SFA + S_OPS * BM * 4;                           // [S_OPS][BN] words
-  static constexpr int OFF_TAB = OFF_SFB + S_OPS * BN * 4;  // 8 decode tables (one per mshared), 16 B each
+  static constexpr int OFF_ACODES = OFF_BOPS + S_OPS * B_OPS_;
+  static constexpr int OFF_SFA = OFF_ACODES + S_CODES_ * A_CODES;  // [S_OPS][BM] words
+  static constexpr int OFF_SFB = OFF_SFA + S_OPS * BM * 4;         // [S_OPS][TBN] words
+  static constexpr int OFF_TAB = OFF_SFB + S_OPS * TBN * 4;  // 8 decode tables (one per mshared), 16 B each
   static constexpr int OFF_BAR = OFF_TAB + 8 * 16;
-  static constexpr int NUM_BARS = 2 * S_CODES + 4 * S_OPS + 2;
+  static constexpr int NUM_BARS = 2 * S_CODES_ + 4 * S_OPS + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for the 1024-byte alignment
 };
@@ -131,16 +139,18 @@ __device__ __forceinline__ void epi_quant_block(uint32_t* u, const TcParams& p, 
   else mx_block32<false>(u, mx_rule_of(p.epi_flags), codes, shared);
 }
 
-// Epilogue of one 128 x 256 tile by sixteen warps (DEC_WARP0 ..): warp w
+// Epilogue of one 128 x TBN tile by sixteen warps (DEC_WARP0 ..): warp w
 // reads TMEM lane quadrant w % 4 (the only one it may access) and a quarter
 // of the columns.  fp32 C leaves through per-warp 32 x 32 staging tiles
 // (128-byte swizzled, double-buffered, 8 KB per warp in the drained operand
 // ring at `stage_base`) and TMA stores, which write whole lines and clip the
 // ragged matrix edges; the fused quantiser writes each 32-column block's codes
 // and shared field straight from registers.
+template <int TBN>
 __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorMap* tmap_c, uint32_t tmem,
                                               unsigned char* stage_base, int64_t m0, int64_t n0, int64_t bt,
                                               int warp, int lane) {
+  constexpr int BN = TBN;
   ptx::tc_fence_after();
   const uint32_t q = (uint32_t)(warp & 3);
   const int cg = (warp - DEC_WARP0) >> 2;  // column quarter 0..3
@@ -184,11 +194,13 @@ __device__ __forceinline__ void epilogue_tile(const TcParams& p, const CUtensorM
   if (staged && lane == 0) ptx::bulk_wait_read0();  // staging read before the CTA exits
 }
 
+template <int TBN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const TcParams p) {
-  using L = Plan;
+  using L = Plan<TBN>;
   constexpr int S_OPS = L::S_OPS;
+  constexpr int S_CODES = L::S_CODES_, BN = TBN, B_OPS = L::B_OPS_;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -215,7 +227,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(&codes_empty[i], NUM_DEC_WARPS);
     }
     for (int i = 0; i < S_OPS; ++i) {
-      ptx::mbar_init(&ops_full[i], NUM_DEC_WARPS);
+      ptx::mbar_init(&ops_full[i], NUM_DEC_WARPS + 4);
       ptx::mbar_init(&ops_empty[i], 1);
       ptx::mbar_init(&sf_ready[i], NUM_DEC_WARPS);
       ptx::mbar_init(&b_full[i], 1);
@@ -243,9 +255,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------- producer of the A codes
+    // (its own thread, so that the codes ring runs as far ahead as its depth
+    // allows, independent of the operand ring)
     if (lane == 0) {
-      int issued = 0, issued_b = 0;
+      int issued = 0;
       for (int kt = 0; kt < num_k; ++kt) {
         const int s = kt % S_CODES, n = kt / S_CODES;
         if (n > 0 && !ptx::mbar_wait(&codes_empty[s], (n - 1) & 1, WAIT_LIMIT, abort_flag)) {
@@ -256,23 +270,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::mbar_arrive_expect_tx(&codes_full[s], A_CODES);
         ptx::tma_load_3d(smem + L::OFF_ACODES + s * A_CODES, &tmap_a, &codes_full[s], kt * KB, (int)m0, (int)bt);
         ++issued;
-        {
-          const int os = kt % S_OPS, on = kt / S_OPS;
-          if (on > 0 && !ptx::mbar_wait(&ops_empty[os], (on - 1) & 1, WAIT_LIMIT, abort_flag)) {
-            flag_error(64u, abort_flag);
-            break;
-          }
-          if (*abort_flag) break;
-          // the transaction count of the unpacking E2M1 load is the packed size
-          ptx::mbar_arrive_expect_tx(&b_full[os], p.b_tma_bytes);
-          ptx::tma_load_3d(smem + L::OFF_BOPS + os * B_OPS, &tmap_b, &b_full[os], kt * BK, (int)n0,
-                           (int)(bt / p.b_group));
-          ++issued_b;
-        }
       }
       // drain: every issued copy lands before the CTA may exit
       for (int kt = (issued > S_CODES ? issued - S_CODES : 0); kt < issued; ++kt)
         ptx::mbar_wait(&codes_full[kt % S_CODES], (kt / S_CODES) & 1, WAIT_LIMIT, never);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------- producer of B tiles
+    if (lane == 0) {
+      int issued_b = 0;
+      for (int kt = 0; kt < num_k; ++kt) {
+        const int os = kt % S_OPS, on = kt / S_OPS;
+        if (on > 0 && !ptx::mbar_wait(&ops_empty[os], (on - 1) & 1, WAIT_LIMIT, abort_flag)) {
+          flag_error(64u, abort_flag);
+          break;
+        }
+        if (*abort_flag) break;
+        // the transaction count of the unpacking E2M1 load is the packed size
+        ptx::mbar_arrive_expect_tx(&b_full[os], p.b_tma_bytes);
+        ptx::tma_load_3d(smem + L::OFF_BOPS + os * B_OPS, &tmap_b, &b_full[os], kt * BK, (int)n0,
+                         (int)(bt / p.b_group));
+        ++issued_b;
+      }
       for (int kt = (issued_b > S_OPS ? issued_b - S_OPS : 0); kt < issued_b; ++kt)
         ptx::mbar_wait(&b_full[kt % S_OPS], (kt / S_OPS) & 1, WAIT_LIMIT, never);
     }
@@ -302,6 +321,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tc_commit(acc_full);
       ptx::tc_commit(drain);
       ptx::mbar_wait(drain, 0, WAIT_LIMIT, never);
+    }
+  } else if (warp >= SFW_WARP0) {
+    // ------------------------------------------------------- scale warps
+    // Warp SFW_WARP0 + q stores the stage's scale words (written to shared
+    // memory by the decoders) into TMEM lane quadrant q: every quadrant holds
+    // a full replica (row 32 i + l at lane l, column i).
+    const uint32_t* sfa_s = reinterpret_cast<const uint32_t*>(smem + L::OFF_SFA);
+    const uint32_t* sfb_s = reinterpret_cast<const uint32_t*>(smem + L::OFF_SFB);
+    for (int kt = 0; kt < num_k; ++kt) {
+      const int os = kt % S_OPS, on = kt / S_OPS;
+      if (on > 0) {
+        if (!ptx::mbar_wait(&ops_empty[os], (on - 1) & 1, WAIT_LIMIT, abort_flag)) { flag_error(512u, abort_flag); break; }
+        ptx::tc_fence_after();
+      }
+      if (!ptx::mbar_wait(&sf_ready[os], on & 1, WAIT_LIMIT, abort_flag)) { flag_error(32u, abort_flag); break; }
+      if (*abort_flag) break;
+      const uint32_t base = tmem + ((32u * (uint32_t)(warp & 3)) << 16) + SF_COL + 16u * os;
+      const uint32_t* sa = sfa_s + os * BM;
+      const uint32_t* sb = sfb_s + os * BN;
+      ptx::tmem_st_x4(base, sa[lane], sa[lane + 32], sa[lane + 64], sa[lane + 96]);
+      ptx::tmem_st_x4(base + 4u, sb[lane], sb[lane + 32], sb[lane + 64], sb[lane + 96]);
+      if (BN == 256) ptx::tmem_st_x4(base + 8u, sb[lane + 128], sb[lane + 160], sb[lane + 192], sb[lane + 224]);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ops_full[os]);
     }
   } else if (warp >= DEC_WARP0) {
     // ------------------------------------------------------------ decoders
@@ -340,17 +385,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     uint32_t* sfa_s = reinterpret_cast<uint32_t*>(smem + L::OFF_SFA);
     uint32_t* sfb_s = reinterpret_cast<uint32_t*>(smem + L::OFF_SFB);
-    uint32_t a_pf0 = fetch_a(0), a_pf1 = fetch_a(1);
-    uint32_t b_pf0 = fetch_b(0), b_pf1 = fetch_b(1);
+    // shared fields and scale words four k-steps ahead: they come from HBM
+    // and the k-step is far shorter than a load's latency
+    uint32_t a_pf0 = fetch_a(0), a_pf1 = fetch_a(1), a_pf2 = fetch_a(2), a_pf3 = fetch_a(3);
+    uint32_t b_pf0 = fetch_b(0), b_pf1 = fetch_b(1), b_pf2 = fetch_b(2), b_pf3 = fetch_b(3);
     bool ok = true;
     for (int kt = 0; kt < num_k && ok; ++kt) {
       const int cs = kt % S_CODES, cn = kt / S_CODES;
       const int os = kt % S_OPS, on = kt / S_OPS;
       const uint32_t a_sh = a_pf0, bsw = b_pf0;
       a_pf0 = a_pf1;
-      a_pf1 = fetch_a(kt + 2);
+      a_pf1 = a_pf2;
+      a_pf2 = a_pf3;
+      a_pf3 = fetch_a(kt + 4);
       b_pf0 = b_pf1;
-      b_pf1 = fetch_b(kt + 2);
+      b_pf1 = b_pf2;
+      b_pf2 = b_pf3;
+      b_pf3 = fetch_b(kt + 4);
       if (!ptx::mbar_wait(&codes_full[cs], cn & 1, WAIT_LIMIT, abort_flag)) { flag_error(4u, abort_flag); ok = false; break; }
       if (on > 0) {
         if (!ptx::mbar_wait(&ops_empty[os], (on - 1) & 1, WAIT_LIMIT, abort_flag)) {
@@ -394,26 +445,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           *reinterpret_cast<uint4*>(dst + sw128_off(arow, c0 + 1)) = make_uint4(e[2].x, e[2].y, e[3].x, e[3].y);
         }
       }
+      // the scale words go to TMEM from the scale warps, so no decoder waits
+      // on another within a k-step
+      ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         ptx::mbar_arrive(&codes_empty[cs]);
         ptx::mbar_arrive(&sf_ready[os]);
+        ptx::mbar_arrive(&ops_full[os]);
       }
-      // scale words -> TMEM (each lane quadrant holds a full replica)
-      if (warp < DEC_WARP0 + 4) {
-        if (!ptx::mbar_wait(&sf_ready[os], on & 1, WAIT_LIMIT, abort_flag)) { flag_error(32u, abort_flag); ok = false; break; }
-        const uint32_t base = tmem + ((32u * (uint32_t)(warp & 3)) << 16) + SF_COL + 16u * os;
-        const uint32_t* sa = sfa_s + os * BM;
-        const uint32_t* sb = sfb_s + os * BN;
-        ptx::tmem_st_x4(base, sa[lane], sa[lane + 32], sa[lane + 64], sa[lane + 96]);
-        ptx::tmem_st_x4(base + 4u, sb[lane], sb[lane + 32], sb[lane + 64], sb[lane + 96]);
-        ptx::tmem_st_x4(base + 8u, sb[lane + 128], sb[lane + 160], sb[lane + 192], sb[lane + 224]);
-        ptx::tmem_wait_st();
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&ops_full[os]);
     }
     // --------------------------------------------------------- epilogue
     // All sixteen decoder warps: warp w reads TMEM lane quadrant w % 4 (the
@@ -423,7 +463,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!got) {
         if (ok && !*abort_flag) flag_error(16u, abort_flag);
       } else {
-        epilogue_tile(p, &tmap_c, tmem, smem + L::OFF_BOPS, m0, n0, bt, warp, lane);
+        // C staging (16 x 8 KB) in the drained operand rings
+        epilogue_tile<TBN>(p, &tmap_c, tmem, smem, m0, n0, bt, warp, lane);
       }
     }
   }
@@ -821,18 +862,19 @@ cudaError_t launch_staged(const CUtensorMap& ma, const CUtensorMap& mb, const CU
   return e;
 }
 
+template <int TBN>
 cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const TcParams& p,
                       dim3 grid, cudaStream_t st) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Plan::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<TBN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Plan<TBN>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  gemm_tc_kernel<<<grid, NUM_THREADS, Plan::SMEM_BYTES, st>>>(ma, mb, mc, p);
+  gemm_tc_kernel<TBN><<<grid, NUM_THREADS, Plan<TBN>::SMEM_BYTES, st>>>(ma, mb, mc, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess && std::getenv("MIX_DEBUG") != nullptr)
     std::fprintf(stderr, "gemm_tc launch: %s\n", cudaGetErrorString(e));
@@ -884,25 +926,26 @@ cudaError_t launch_fused(const mix_gemm_desc_t& d, void* ws, cudaStream_t st, mi
   }
   TcParams p = make_params(d);
   const bool native = fused_b_native(d);
+  const int tbn = d.N <= 128 ? 128 : BN;  // narrow outputs: 128-column tiles
   StagedPlan sp{};
   unsigned char* base = nullptr;
   if (native) {
-    if (!make_fp4_operand_map(&mb, d.b_codes, d.K, d.N, bb, d.b_ld, d.b_batch_stride)) {
+    if (!make_fp4_operand_map(&mb, d.b_codes, d.K, d.N, bb, d.b_ld, d.b_batch_stride, (uint32_t)tbn)) {
       *why = MIX_ERR_UNSUPPORTED;
       return cudaSuccess;
     }
     p.b_tma_fmt = 5u;
-    p.b_tma_bytes = B_OPS / 2;
+    p.b_tma_bytes = (uint32_t)(tbn * BK / 2);
   } else {
     sp = staged_plan_b_only(d);
     base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(ws) + kStagedAlign - 1) &
                                             ~static_cast<uintptr_t>(kStagedAlign - 1));
-    if (!make_e4m3_map(&mb, base + sp.off_b, sp.k_pad, d.N, sp.bb, BN)) {
+    if (!make_e4m3_map(&mb, base + sp.off_b, sp.k_pad, d.N, sp.bb, (uint32_t)tbn)) {
       *why = MIX_ERR_UNSUPPORTED;
       return cudaSuccess;
     }
     p.b_tma_fmt = 0u;
-    p.b_tma_bytes = B_OPS;
+    p.b_tma_bytes = (uint32_t)(tbn * BK);
     if (b_g16(d)) {  // the block scales the expansion chose, one byte per 32-deep block
       p.b_scales = base + sp.off_sfe;
       p.b_ld = sp.k_pad;
@@ -918,8 +961,8 @@ cudaError_t launch_fused(const mix_gemm_desc_t& d, void* ws, cudaStream_t st, mi
     const cudaError_t e = launch_expand_b(d, sp, base, st);
     if (e != cudaSuccess) return e;
   }
-  const dim3 grid((unsigned)((d.M + BM - 1) / BM), (unsigned)((d.N + BN - 1) / BN), (unsigned)d.batch);
-  return launch_tc(ma, mb, mc, p, grid, st);
+  const dim3 grid((unsigned)((d.M + BM - 1) / BM), (unsigned)((d.N + tbn - 1) / tbn), (unsigned)d.batch);
+  return tbn == 128 ? launch_tc<128>(ma, mb, mc, p, grid, st) : launch_tc<256>(ma, mb, mc, p, grid, st);
 }
 
 cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t st, mix_status_t* why) {
