@@ -86,7 +86,10 @@ struct Plan {
   static constexpr int OFF_BAR = OFF_TAB + 8 * 16;
   static constexpr int NUM_BARS = 2 * S_CODES_ + 4 * S_OPS + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for the 1024-byte alignment
+  // misc: TMEM address, abort flag, a never-set flag, and per operand stage
+  // the last k-step (+1) whose A tile held a nonzero block
+  static constexpr int OFF_NZ = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = OFF_MISC + 64 + 1024;  // + slack for the 1024-byte alignment
 };
 
 struct TcParams {
@@ -216,6 +219,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);  // drains ignore aborts
+  volatile int* stage_nz = reinterpret_cast<volatile int*>(smem + L::OFF_NZ);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m0 = (int64_t)blockIdx.x * BM, n0 = (int64_t)blockIdx.y * BN, bt = blockIdx.z;
@@ -236,6 +240,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
     *never = 0;
+    for (int i = 0; i < S_OPS; ++i) stage_nz[i] = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmap_a);
     ptx::prefetch_tmap(&tmap_b);
@@ -308,13 +313,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (*abort_flag) break;
         ptx::tc_fence_after();
-        const uint32_t a_addr = ptx::smem_u32(smem + L::OFF_AOPS + s * A_OPS);
-        const uint32_t b_addr = ptx::smem_u32(smem + L::OFF_BOPS + s * B_OPS);
-        const uint32_t sfa = tmem + SF_COL + 16u * s, sfb = sfa + 4u;
+        // A stage whose A tile is all zero codes contributes nothing: skip its
+        // MMAs (the causal half of attention P is such tiles).  Stage 0 always
+        // runs, so the accumulator is initialised.
+        // the decoders mark a stage by writing kt + 1 (never reset, so no
+        // store of this thread can race with theirs)
+        if (stage_nz[s] == kt + 1 || kt == 0) {
+          const uint32_t a_addr = ptx::smem_u32(smem + L::OFF_AOPS + s * A_OPS);
+          const uint32_t b_addr = ptx::smem_u32(smem + L::OFF_BOPS + s * B_OPS);
+          const uint32_t sfa = tmem + SF_COL + 16u * s, sfb = sfa + 4u;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          ptx::mma_mxf8f6f4(tmem, ptx::sdesc_sw128(a_addr + 32u * j), ptx::sdesc_sw128(b_addr + 32u * j),
-                            ptx::idesc_mxf8(BM, BN, 0u, b_fmt, (uint32_t)j), sfa, sfb, (kt > 0 || j > 0) ? 1u : 0u);
+          for (int j = 0; j < 4; ++j) {
+            ptx::mma_mxf8f6f4(tmem, ptx::sdesc_sw128(a_addr + 32u * j), ptx::sdesc_sw128(b_addr + 32u * j),
+                              ptx::idesc_mxf8(BM, BN, 0u, b_fmt, (uint32_t)j), sfa, sfb, (kt > 0 || j > 0) ? 1u : 0u);
+          }
         }
         ptx::tc_commit(&ops_empty[s]);
       }
@@ -430,16 +442,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint4 t = *reinterpret_cast<const uint4*>(tabs + 16 * m3);
             return DecTab{t.x, t.y, t.z, t.w};
           };
-          uint2 e[4];
-          if (p.a_type == 1) {
-            const DecTab t = tab((sh >> 4) & 7u);
-            e[0] = dec8(cv.x, t); e[1] = dec8(cv.y, t); e[2] = dec8(cv.z, t); e[3] = dec8(cv.w, t);
-          } else {
-            e[0] = dec8(cv.x, tab((sh >> 4) & 7u));
-            e[1] = dec8(cv.y, tab((sh >> 7) & 7u));
-            e[2] = dec8(cv.z, tab((sh >> 10) & 7u));
-            e[3] = dec8(cv.w, tab((sh >> 13) & 7u));
+          // an all-zero block (every nibble the zero code) is written as
+          // zeros without decoding
+          const bool zero_blk = cv.x == 0x77777777u && cv.y == 0x77777777u && cv.z == 0x77777777u &&
+                                cv.w == 0x77777777u;
+          uint2 e[4] = {};
+          if (!zero_blk) {
+            if (p.a_type == 1) {
+              const DecTab t = tab((sh >> 4) & 7u);
+              e[0] = dec8(cv.x, t); e[1] = dec8(cv.y, t); e[2] = dec8(cv.z, t); e[3] = dec8(cv.w, t);
+            } else {
+              e[0] = dec8(cv.x, tab((sh >> 4) & 7u));
+              e[1] = dec8(cv.y, tab((sh >> 7) & 7u));
+              e[2] = dec8(cv.z, tab((sh >> 10) & 7u));
+              e[3] = dec8(cv.w, tab((sh >> 13) & 7u));
+            }
           }
+          if (__any_sync(0xFFFFFFFFu, !zero_blk) && lane == 0) stage_nz[os] = kt + 1;
           const int c0 = 2 * ablk;
           *reinterpret_cast<uint4*>(dst + sw128_off(arow, c0)) = make_uint4(e[0].x, e[0].y, e[1].x, e[1].y);
           *reinterpret_cast<uint4*>(dst + sw128_off(arow, c0 + 1)) = make_uint4(e[2].x, e[2].y, e[3].x, e[3].y);

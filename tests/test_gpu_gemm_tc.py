@@ -225,3 +225,34 @@ def test_vit_mlp_chain_sampled(mix, orc):
     assert np.array_equal(to_host(hc)[rows], rc) and np.array_equal(to_host(hs)[rows], rs)
     assert sampled_check(orc, to_host(c2), to_host(hc), to_host(hs), 1, to_host(b2c), to_host(b2s), 0, rows,
                          np.sort(rng.choice(D, 256, replace=False))) <= GEMM_REL_TOL
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("N", [128, 256])
+def test_tc_zero_blocks_causal(mix, orc, algo, N):
+    """An A operand with all-zero 32-blocks and all-zero 128-deep tiles (a
+    causal attention P: row m is zero past column m), a tile whose first
+    k-step is zero but not its later ones, and an all-zero row tile: the
+    stages whose A tile is all zero are skipped on the fused path, and the
+    result still equals the oracle's."""
+    M, K = 384, 1024
+    rng = np.random.default_rng(5)
+    a = rng.random((M, K)).astype(np.float32)
+    a[np.arange(K)[None, :] > np.arange(M)[:, None] * 2] = 0.0      # causal-like: zero tiles to the right
+    a[128:256, :128] = 0.0                                          # first k-step zero, later ones not
+    a[256:384] = 0.0                                                # an all-zero row tile
+    a[260, 700] = 0.5                                               # ... but one nonzero block in it
+    w = synth.to_bf16_bits(synth.normal(9, 1, N * K, 0, 0.5).reshape(N, K))
+    ac, ash = orc.mix_quantize(a, 2, -15)
+    bc, bs = orc.mx_quantize(w, 1, 0)
+    import torch
+    c = torch.empty((1, M, N), dtype=torch.float32, device="cuda")
+    d = mix.gemm_desc(M, N, K, to_dev(ac), to_dev(ash), 2, -15, to_dev(bc), to_dev(bs), 0, c=c,
+                      algo=algo_id(mix, algo))
+    mix.gemm(d)
+    torch.cuda.synchronize()
+    assert mix.mix_device_error() == 0
+    ref = orc.gemm(ac, ash, 2, -15, bc, bs, 0)
+    got = to_host(c)[0]
+    assert row_rel_err(got, ref) <= GEMM_REL_TOL
+    assert np.all(got[256:260] == 0) and np.all(got[261:] == 0)
