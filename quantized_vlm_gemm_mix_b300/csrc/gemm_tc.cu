@@ -131,11 +131,11 @@ __device__ __forceinline__ void epi_quant_block(uint32_t* u, const TcParams& p, 
                                                 uint32_t& shared) {
   const bool asym = (p.epi_flags & MIX_ASYM_ZERO) != 0;
   if (p.epi == MIX_EPI_MIX_T1) {
-    mix_block32<1>(u, p.epi_ebias, asym, codes, shared);
+    mix_block32_f32<1>(u, p.epi_ebias, asym, codes, shared);
     return;
   }
   if (p.epi == MIX_EPI_MIX_T2) {
-    mix_block32<2>(u, p.epi_ebias, asym, codes, shared);
+    mix_block32_f32<2>(u, p.epi_ebias, asym, codes, shared);
     return;
   }
   if (p.epi == MIX_EPI_MXFP4) mx_block32<true>(u, mx_rule_of(p.epi_flags), codes, shared);

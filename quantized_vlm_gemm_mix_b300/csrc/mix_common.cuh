@@ -227,6 +227,48 @@ __device__ __forceinline__ uint32_t mix_code_pair(uint32_t w, uint32_t a, const 
   return (code & 0xFu) | ((code >> 12) & 0xF0u);
 }
 
+// The packed part of Algorithm 1 for one NaN-free block: w holds the top 16
+// bits of the 32 elements (element 2j in the low half of word j), ks the exact
+// fp32 magnitude bits of each 8-element sub-block's maximum and kb the
+// block's (they set Emax and mshared, whose rounding needs every mantissa
+// bit).
+template <int TYPE>
+__device__ __forceinline__ void mix_block32_packed(const uint32_t* w, const uint32_t* ks, uint32_t kb, int ebias,
+                                                   bool asym, uint4& cw, uint32_t& sh) {
+  cw = make_uint4(0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);
+  sh = 0;
+  int f, m3;
+  if (!max_exp_mant(kb, &f, &m3)) return;
+  const int emax = clampi(f, ebias, ebias + 15);
+  uint32_t wd[4];
+  uint32_t m3bits = 0;
+  bool all_zero = true;
+  const MixBlk2 q1 = mix_blk2(mix_blk(emax, 8 + m3, asym), asym);
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    int ms = m3;
+    MixBlk2 q = q1;
+    if (TYPE == 2) {
+      int fs;
+      if (!max_exp_mant(ks[s], &fs, &ms)) ms = 0;
+      q = mix_blk2(mix_blk(emax, 8 + ms, asym), asym);
+    }
+    uint32_t word = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) word |= mix_code_pair(w[4 * s + j], w[4 * s + j] & 0x7FFF7FFFu, q) << (8 * j);
+    wd[s] = word;
+    const bool z = word == 0x77777777u;
+    all_zero &= z;
+    if (z) ms = 0;
+    m3bits |= (uint32_t)ms << (4 + 3 * s);
+  }
+  cw = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+  if (!all_zero) {
+    const uint32_t ec = (uint32_t)(emax - ebias);
+    sh = TYPE == 1 ? (ec | ((uint32_t)m3 << 4)) : (ec | m3bits);
+  }
+}
+
 // Algorithm 1 on one block of 32 bf16 elements held as 16 packed words;
 // same results as mix_block32 on the widened elements (a block holding a NaN
 // goes through mix_block32, which codes NaN as zero).
@@ -254,38 +296,33 @@ __device__ __forceinline__ void mix_block32_bf16(const uint32_t* w, int ebias, b
     mix_block32<TYPE>(u, ebias, asym, cw, sh);
     return;
   }
-  cw = make_uint4(0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);
-  sh = 0;
-  int f, m3;
-  if (!max_exp_mant(kb, &f, &m3)) return;
-  const int emax = clampi(f, ebias, ebias + 15);
-  uint32_t wd[4];
-  uint32_t m3bits = 0;
-  bool all_zero = true;
-  const MixBlk2 q1 = mix_blk2(mix_blk(emax, 8 + m3, asym), asym);
+  mix_block32_packed<TYPE>(w, ks, kb, ebias, asym, cw, sh);
+}
+
+// Algorithm 1 on one block of 32 fp32 elements (bit patterns; u may be
+// overwritten).  Emax and mshared come from the exact fp32 maxima; the element
+// step runs packed on the top 16 bits of each element, which decides exactly
+// as on all 32: every threshold is a multiple of 2^16 in bit-pattern space,
+// and for such a t, |x| < t holds exactly when its top 16 bits are below t's.
+template <int TYPE>
+__device__ __forceinline__ void mix_block32_f32(uint32_t* u, int ebias, bool asym, uint4& cw, uint32_t& sh) {
+  uint32_t ks[4];
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
-    int ms = m3;
-    MixBlk2 q = q1;
-    if (TYPE == 2) {
-      int fs;
-      if (!max_exp_mant(ks[s], &fs, &ms)) ms = 0;
-      q = mix_blk2(mix_blk(emax, 8 + ms, asym), asym);
-    }
-    uint32_t word = 0;
+    uint32_t k = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) word |= mix_code_pair(w[4 * s + j], a[4 * s + j], q) << (8 * j);
-    wd[s] = word;
-    const bool z = word == 0x77777777u;
-    all_zero &= z;
-    if (z) ms = 0;
-    m3bits |= (uint32_t)ms << (4 + 3 * s);
+    for (int i = 0; i < 8; ++i) k = max(k, u[8 * s + i] & 0x7FFFFFFFu);
+    ks[s] = k;
   }
-  cw = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-  if (!all_zero) {
-    const uint32_t ec = (uint32_t)(emax - ebias);
-    sh = TYPE == 1 ? (ec | ((uint32_t)m3 << 4)) : (ec | m3bits);
+  const uint32_t kb = max(max(ks[0], ks[1]), max(ks[2], ks[3]));
+  if (kb > 0x7F800000u) {  // a NaN in the block: the scalar path codes it as zero
+    mix_block32<TYPE>(u, ebias, asym, cw, sh);
+    return;
   }
+  uint32_t w[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) w[j] = __byte_perm(u[2 * j], u[2 * j + 1], 0x7632);
+  mix_block32_packed<TYPE>(w, ks, kb, ebias, asym, cw, sh);
 }
 
 // Division by a runtime constant d (1 <= d < 2^31) of 32-bit numerators with
