@@ -175,18 +175,23 @@ __device__ __forceinline__ void mix_block32(uint32_t* u, int ebias, bool asym, u
 }
 
 // ---------------------------------------------------------------------------
-// Packed element step for bf16 inputs: two elements per 32-bit word (element
-// 2j in the low half of word j), one integer operation for both.  Exact
-// because every threshold of the element step (t0, zn, zp above) has zero low
-// 16 bits, so comparing the bf16 bits (the top half of the fp32 pattern) gives
-// the same decisions:
+// Packed element step: two elements per 32-bit word (element 2j in the low
+// half of word j), one integer operation for both.  The inputs are the top
+// 16 bits of the fp32 patterns (bf16 inputs as they are).  Exact because
+// every threshold of the element step (t0, zn, zp above) has zero low 16
+// bits, so comparing the top halves gives the same decisions:
 //   d   = ceil((t0 - |x|) / 2^23) = floor((T - a + 127) / 128), T = t0 >> 16,
-//         a = the bf16 magnitude; computed per 16-bit lane as
+//         a = the top-half magnitude; computed per 16-bit lane as
 //         ((0x807F + T - a) >> 7) - 256, the 0x8000 guard keeping every lane
 //         non-negative so no borrow crosses lanes,
 //   clamp to [0, 6] (negative) or [0, dmaxp] (positive) with max/min.u16x2,
 //   code = d | sign << 3 | ((d + 1) & 8), and the zero code 7 where a < z,
 //         the lane compare read from bit 15 of (a | 0x8000) - z.
+// Per-lane sign and compare masks come from one byte permute each (prmt
+// replicates the sign bit of a byte), and the caps and zero thresholds of
+// the two signs are chosen by those masks.  Checked against the scalar step
+// exhaustively (every top-half pattern in each lane, every Emax of seven
+// ebias values, every mshared, both zero modes) in an emulation before use.
 __device__ __forceinline__ uint32_t vmax_u16x2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
@@ -197,34 +202,53 @@ __device__ __forceinline__ uint32_t vmin_u16x2(uint32_t a, uint32_t b) {
   asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
   return d;
 }
+// Byte permute in its generic mode: a selector nibble with bit 3 set
+// replicates the sign bit of the selected byte.
+__device__ __forceinline__ uint32_t prmt_sel(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
 
 struct MixBlk2 {
   uint32_t c1;   // (0x807F + T) in both lanes
-  uint32_t zp2;  // ZP in both lanes (ZN = ZP + 128 with the recycled -0, else ZP)
-  bool asym;
+  uint32_t zp2;  // ZP in both lanes
+  uint32_t zn2;  // ZN in both lanes (ZP + 128 with the recycled -0, else ZP)
+  uint32_t capn; // low bit of the positive lanes' cap: 1 with the recycled -0 (cap 7), else 0 (cap 6)
 };
 
 __device__ __forceinline__ MixBlk2 mix_blk2(const MixBlk& b, bool asym) {
   MixBlk2 q;
   q.c1 = (0x807Fu + (b.t0 >> 16)) * 0x00010001u;
   q.zp2 = (b.zp >> 16) * 0x00010001u;
-  q.asym = asym;
+  q.zn2 = (b.zn >> 16) * 0x00010001u;
+  q.capn = asym ? 0x00010001u : 0u;
   return q;
 }
 
-// Codes of the two elements of word w (its magnitudes a = w & 0x7FFF7FFF),
-// as one byte: the low element's code in the low nibble.
-__device__ __forceinline__ uint32_t mix_code_pair(uint32_t w, uint32_t a, const MixBlk2& q) {
+// Codes of the two elements of word w, at bits 0..3 (low element) and
+// 16..19 (high element); every other bit zero.
+__device__ __forceinline__ uint32_t mix_code_pair(uint32_t w, const MixBlk2& q) {
+  const uint32_t a = w & 0x7FFF7FFFu;
   uint32_t v = ((q.c1 - a) >> 7) & 0x01FF01FFu;
   v = vmax_u16x2(v, 0x01000100u);
-  const uint32_t neg01 = (w >> 15) & 0x00010001u;
-  v = vmin_u16x2(v, q.asym ? 0x01070107u - neg01 : 0x01060106u);
-  uint32_t code = (v & 0x00070007u) | ((v + 0x00010001u) & 0x00080008u) | (neg01 << 3);
-  const uint32_t z2 = q.zp2 + (q.asym ? (neg01 << 7) : 0u);
-  const uint32_t ge = (((a | 0x80008000u) - z2) >> 15) & 0x00010001u;
-  const uint32_t m = ge * 0xFu;
-  code = (code & m) | (0x00070007u & ~m);
-  return (code & 0xFu) | ((code >> 12) & 0xF0u);
+  const uint32_t s = prmt_sel(w, w, 0xBB99u);              // 0xFFFF in negative lanes
+  v = vmin_u16x2(v, 0x01060106u | (~s & q.capn));
+  const uint32_t code = (v & 0x00070007u) | (((v + 0x00010001u) | s) & 0x00080008u);
+  const uint32_t y = (w | 0x80008000u) - ((s & q.zn2) | (~s & q.zp2));
+  const uint32_t m = prmt_sel(y, 0u, 0x4B49u);              // 0x00FF where |x| >= z
+  return (code & m) | (0x00070007u & ~m);
+}
+
+// Eight codes of words w[0..3] as one 32-bit word (element 2j in the low
+// nibble of byte j): two pairs meet in a half-word by a multiply-add and a
+// shift, two half-words in a word by a byte permute.
+__device__ __forceinline__ uint32_t mix_codes8_packed(const uint32_t* w, const MixBlk2& q) {
+  uint32_t p0 = mix_code_pair(w[0], q) + mix_code_pair(w[1], q) * 256u;
+  uint32_t p1 = mix_code_pair(w[2], q) + mix_code_pair(w[3], q) * 256u;
+  p0 |= p0 >> 12;
+  p1 |= p1 >> 12;
+  return prmt_sel(p0, p1, 0x5410u);
 }
 
 // The packed part of Algorithm 1 for one NaN-free block: w holds the top 16
@@ -253,9 +277,7 @@ __device__ __forceinline__ void mix_block32_packed(const uint32_t* w, const uint
       if (!max_exp_mant(ks[s], &fs, &ms)) ms = 0;
       q = mix_blk2(mix_blk(emax, 8 + ms, asym), asym);
     }
-    uint32_t word = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) word |= mix_code_pair(w[4 * s + j], w[4 * s + j] & 0x7FFF7FFFu, q) << (8 * j);
+    const uint32_t word = mix_codes8_packed(w + 4 * s, q);
     wd[s] = word;
     const bool z = word == 0x77777777u;
     all_zero &= z;
