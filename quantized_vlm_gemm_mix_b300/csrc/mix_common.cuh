@@ -182,11 +182,13 @@ __device__ __forceinline__ void mix_block32(uint32_t* u, int ebias, bool asym, u
 // bits, so comparing the top halves gives the same decisions:
 //   d   = ceil((t0 - |x|) / 2^23) = floor((T - a + 127) / 128), T = t0 >> 16,
 //         a = the top-half magnitude; computed per 16-bit lane as
-//         ((0x807F + T - a) >> 7) - 256, the 0x8000 guard keeping every lane
-//         non-negative so no borrow crosses lanes,
-//   clamp to [0, 6] (negative) or [0, dmaxp] (positive) with max/min.u16x2,
+//         X = 0x807F + T - a (the 0x8000 guard keeps every lane positive, so
+//         no borrow crosses lanes), clamped with max/min.u16x2 to
+//         [0x8000, 0x8000 + 128 cap + 127] (cap 6 for negative elements,
+//         dmaxp for positive ones), then shifted right by 7: the low three
+//         bits of each lane are d (clamping before the shift needs no mask),
 //   code = d | sign << 3 | ((d + 1) & 8), and the zero code 7 where a < z,
-//         the lane compare read from bit 15 of (a | 0x8000) - z.
+//         the lane compare read from bit 15 of a + (0x8000 - z).
 // Per-lane sign and compare masks come from one byte permute each (prmt
 // replicates the sign bit of a byte), and the caps and zero thresholds of
 // the two signs are chosen by those masks.  Checked against the scalar step
@@ -212,17 +214,17 @@ __device__ __forceinline__ uint32_t prmt_sel(uint32_t a, uint32_t b, uint32_t se
 
 struct MixBlk2 {
   uint32_t c1;   // (0x807F + T) in both lanes
-  uint32_t zp2;  // ZP in both lanes
-  uint32_t zn2;  // ZN in both lanes (ZP + 128 with the recycled -0, else ZP)
-  uint32_t capn; // low bit of the positive lanes' cap: 1 with the recycled -0 (cap 7), else 0 (cap 6)
+  uint32_t kp2;  // 0x8000 - ZP in both lanes (positive elements)
+  uint32_t kn2;  // 0x8000 - ZN in both lanes (ZN = ZP + 128 with the recycled -0, else ZP)
+  uint32_t capn; // what the positive lanes' clamp adds: 128 with the recycled -0 (cap 7), else 0 (cap 6)
 };
 
 __device__ __forceinline__ MixBlk2 mix_blk2(const MixBlk& b, bool asym) {
   MixBlk2 q;
   q.c1 = (0x807Fu + (b.t0 >> 16)) * 0x00010001u;
-  q.zp2 = (b.zp >> 16) * 0x00010001u;
-  q.zn2 = (b.zn >> 16) * 0x00010001u;
-  q.capn = asym ? 0x00010001u : 0u;
+  q.kp2 = (0x8000u - (b.zp >> 16)) * 0x00010001u;
+  q.kn2 = (0x8000u - (b.zn >> 16)) * 0x00010001u;
+  q.capn = asym ? 0x00800080u : 0u;
   return q;
 }
 
@@ -230,12 +232,12 @@ __device__ __forceinline__ MixBlk2 mix_blk2(const MixBlk& b, bool asym) {
 // 16..19 (high element); every other bit zero.
 __device__ __forceinline__ uint32_t mix_code_pair(uint32_t w, const MixBlk2& q) {
   const uint32_t a = w & 0x7FFF7FFFu;
-  uint32_t v = ((q.c1 - a) >> 7) & 0x01FF01FFu;
-  v = vmax_u16x2(v, 0x01000100u);
   const uint32_t s = prmt_sel(w, w, 0xBB99u);              // 0xFFFF in negative lanes
-  v = vmin_u16x2(v, 0x01060106u | (~s & q.capn));
-  const uint32_t code = (v & 0x00070007u) | (((v + 0x00010001u) | s) & 0x00080008u);
-  const uint32_t y = (w | 0x80008000u) - ((s & q.zn2) | (~s & q.zp2));
+  uint32_t x = vmax_u16x2(q.c1 - a, 0x80008000u);
+  x = vmin_u16x2(x, 0x837F837Fu | (~s & q.capn));
+  const uint32_t d = x >> 7;                                // d in bits 0..2 of each lane
+  const uint32_t code = (d & 0x00070007u) | (((d + 0x00010001u) | s) & 0x00080008u);
+  const uint32_t y = a + ((s & q.kn2) | (~s & q.kp2));
   const uint32_t m = prmt_sel(y, 0u, 0x4B49u);              // 0x00FF where |x| >= z
   return (code & m) | (0x00070007u & ~m);
 }
