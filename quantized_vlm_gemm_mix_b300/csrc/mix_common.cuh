@@ -219,11 +219,20 @@ struct MixBlk2 {
   uint32_t capn; // what the positive lanes' clamp adds: 128 with the recycled -0 (cap 7), else 0 (cap 6)
 };
 
-__device__ __forceinline__ MixBlk2 mix_blk2(const MixBlk& b, bool asym) {
+// The packed-step constants of a (sub-)block straight from (Emax, mshared):
+// they are the top halves of mix_blk's t0, zn, zp, that is, in units of the top
+// half, T = 128 Emax + 16192 + 24 m (m < 3, where 3 M < 32) or 16224 + 12 m,
+// ZN = 128 Emax + 15360 + 16 m, ZP = ZN - 128 with the recycled -0 (checked
+// against mix_blk for every Emax in [-100, 115] and every m).
+__device__ __forceinline__ MixBlk2 mix_blk2_direct(int emax, int ms, bool asym) {
+  const int e7 = emax * 128;
+  const int T = e7 + (ms < 3 ? 16192 + 24 * ms : 16224 + 12 * ms);
+  const int ZN = e7 + 15360 + 16 * ms;
+  const int ZP = asym ? ZN - 128 : ZN;
   MixBlk2 q;
-  q.c1 = (0x807Fu + (b.t0 >> 16)) * 0x00010001u;
-  q.kp2 = (0x8000u - (b.zp >> 16)) * 0x00010001u;
-  q.kn2 = (0x8000u - (b.zn >> 16)) * 0x00010001u;
+  q.c1 = (uint32_t)(0x807F + T) * 0x00010001u;
+  q.kp2 = (uint32_t)(0x8000 - ZP) * 0x00010001u;
+  q.kn2 = (uint32_t)(0x8000 - ZN) * 0x00010001u;
   q.capn = asym ? 0x00800080u : 0u;
   return q;
 }
@@ -269,7 +278,7 @@ __device__ __forceinline__ void mix_block32_packed(const uint32_t* w, const uint
   uint32_t wd[4];
   uint32_t m3bits = 0;
   bool all_zero = true;
-  const MixBlk2 q1 = mix_blk2(mix_blk(emax, 8 + m3, asym), asym);
+  const MixBlk2 q1 = mix_blk2_direct(emax, m3, asym);
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     int ms = m3;
@@ -277,7 +286,7 @@ __device__ __forceinline__ void mix_block32_packed(const uint32_t* w, const uint
     if (TYPE == 2) {
       int fs;
       if (!max_exp_mant(ks[s], &fs, &ms)) ms = 0;
-      q = mix_blk2(mix_blk(emax, 8 + ms, asym), asym);
+      q = mix_blk2_direct(emax, ms, asym);
     }
     const uint32_t word = mix_codes8_packed(w + 4 * s, q);
     wd[s] = word;
