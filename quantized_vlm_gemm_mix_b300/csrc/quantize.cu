@@ -344,6 +344,62 @@ __global__ void __launch_bounds__(kThreads, 4) mx_quantize_rows_kernel(
 // contiguous 128-byte (bf16) or 256-byte (fp32) row segment.  The eight warps
 // of a CTA own eight consecutive k-blocks, so each column's 128 code bytes are
 // written by one CTA.
+// bf16 input, 32-element blocks: the same work with the two columns of a
+// lane kept packed (one 32-bit word per row) until each column is coded, so
+// a thread holds 32 words rather than 64 and four CTAs fit on an SM.  NaNs
+// are cleared in the packed words (a 16-bit lane compare per word).
+template <bool FP4>
+__global__ void __launch_bounds__(kThreads, 4) mx_quantize_cols_bf16_kernel(
+    const uint16_t* __restrict__ x, int64_t kdim, int64_t n, int64_t ld, int rule,
+    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t nbk = kdim / 32;
+  const int64_t kb = (int64_t)blockIdx.y * 8 + warp;
+  const int64_t n0 = (int64_t)blockIdx.x * 64 + 2 * lane;
+  if (kb >= nbk || n0 >= n) return;
+  const bool two = n0 + 1 < n;
+  uint32_t v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint16_t* p = x + (kb * 32 + i) * ld + n0;
+    v[i] = two ? __ldcs(reinterpret_cast<const unsigned int*>(p)) : (uint32_t)__ldcs(p);
+  }
+  uint32_t m = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) m = vmax_u16x2(m, v[i] & 0x7FFF7FFFu);
+  if (((m & 0xFFFFu) > 0x7F80u) || ((m >> 16) > 0x7F80u)) {  // a NaN in one of the two blocks
+    m = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      v[i] &= ~__vcmpgtu2(v[i] & 0x7FFF7FFFu, 0x7F807F80u);
+      m = vmax_u16x2(m, v[i] & 0x7FFF7FFFu);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    if (c == 1 && !two) break;
+    const uint32_t kbits = c ? (m & 0xFFFF0000u) : (m << 16);
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    uint32_t sc = 0u;
+    if (kbits != 0u) {
+      const int X = mx_shared_exp(kbits, FP4, rule);
+      uint32_t wd[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = c ? (v[8 * j + i] & 0xFFFF0000u) : (v[8 * j + i] << 16);
+        wd[j] = mx_codes8(t, X, FP4);
+      }
+      w = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      sc = (uint32_t)(X + 127);
+    }
+    const int64_t col = n0 + c;
+    *reinterpret_cast<uint4*>(codes + col * (kdim / 2) + kb * 16) = w;
+    scales[col * nbk + kb] = (uint8_t)sc;
+  }
+}
+
 template <bool BF16, bool FP4, bool G16>
 __global__ void __launch_bounds__(kThreads) mx_quantize_cols_kernel(
     const void* __restrict__ x, int64_t kdim, int64_t n, int64_t ld, int rule,
@@ -583,9 +639,13 @@ cudaError_t launch_mx_quantize_cols(const void* x, bool bf16, int64_t kdim, int6
   const dim3 grid((unsigned)((n + 63) / 64), (unsigned)((kdim / 32 + 7) / 8));
 #define MXC(BF, F4, G) \
   mx_quantize_cols_kernel<BF, F4, G><<<grid, kThreads, 0, st>>>(x, kdim, n, ld, rule, codes, scales)
-  if (bf16) {
-    if (fp4) { if (g16) MXC(true, true, true); else MXC(true, true, false); }
-    else { if (g16) MXC(true, false, true); else MXC(true, false, false); }
+  if (bf16 && !g16) {
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    if (fp4) mx_quantize_cols_bf16_kernel<true><<<grid, kThreads, 0, st>>>(xb, kdim, n, ld, rule, codes, scales);
+    else mx_quantize_cols_bf16_kernel<false><<<grid, kThreads, 0, st>>>(xb, kdim, n, ld, rule, codes, scales);
+  } else if (bf16) {
+    if (fp4) MXC(true, true, true);
+    else MXC(true, false, true);
   } else {
     if (fp4) { if (g16) MXC(false, true, true); else MXC(false, true, false); }
     else { if (g16) MXC(false, false, true); else MXC(false, false, false); }
