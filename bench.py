@@ -151,13 +151,18 @@ MATMUL_SOURCES = ("gemm_tc.cu", "expand.cu", "decode.cuh", "mix_common.cuh", "tc
 
 
 def matmul_source_sha():
-    """sha256 over the matmul's kernel sources: a recorded DRAM-traffic figure
-    counts only for the kernel it was measured on."""
+    """sha256 over the matmul's kernel sources with comments and blank space
+    removed: a recorded DRAM-traffic figure counts only for the code it was
+    measured on, and an edit of a comment does not change that code."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in MATMUL_SOURCES:
-        with open(os.path.join(ROOT, "quantized_vlm_gemm_mix_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "quantized_vlm_gemm_mix_b300", "csrc", f), encoding="utf-8") as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)   # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                  # line comments
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()
 
 

@@ -1,7 +1,7 @@
 // Staging pass of the tensor-core matmul: each operand is expanded ONCE per
 // call into exact e4m3 bytes plus UE8M0 block-scale words in the caller's
-// workspace, so that the matmul's main loop is TMA -> tcgen05.cp -> MMA with
-// no per-tile decode.  Without it every CTA of a row panel re-decodes the same
+// workspace, so that the matmul's main loop is TMA -> tcgen05.st of the
+// scale words -> MMA with no per-tile decode.  Without it every CTA of a row panel re-decodes the same
 // A tile (N / 256 times for a wide layer).
 //
 // The arithmetic is the decode of "MiX: Micro-Inverted-Scaling for End-to-End

@@ -12,14 +12,20 @@
 // same products exactly and accumulates in fp32 in TMEM.  mshared must stay
 // inside the element: a block scale has to be a power of two.
 //
-// CTA tile 128 (M) x 256 (N) x 128 (K per stage = four 32-blocks = four MMAs
-// of K 32), one CTA per tile.  Warp roles:
-//   warp 0      TMA producer: packed A and B code tiles into a 4-deep ring.
+// Two kernels.  The fused-decode kernel (gemm_tc_kernel, for outputs at most
+// 256 wide) takes one CTA per 128 x TBN tile (TBN 256, or 128 for outputs at
+// most 128 wide) and 128-deep k-steps (four MMAs of K 32).  Warp roles:
+//   warp 0      TMA producer of the packed A code tiles (3- or 8-deep ring).
 //   warp 1      TMEM allocator and the single MMA-issuing thread.
-//   warps 4-11  decoders: nibbles -> e4m3 in the 128-byte-swizzled K-major
-//               operand layout (2-deep ring); block scales -> TMEM; then
-//               warps 4-7 run the epilogue (tcgen05.ld, optional fp32 store,
-//               optional fused MiX/MX quantiser of each 32-column block).
+//   warp 2      TMA producer of the B operand tiles (4-deep operand ring).
+//   warps 4-19  decoders: nibbles -> e4m3 in the 128-byte-swizzled K-major
+//               operand layout, the stage's scale words to shared memory;
+//               then the epilogue (tcgen05.ld, optional fp32 store through
+//               TMA, optional fused MiX/MX quantiser of each 32-column block).
+//   warps 20-23 scale warps: the stage's scale words into TMEM (tcgen05.st),
+//               one warp per TMEM lane quadrant.
+// A stage whose A tile holds only zero codes skips its MMAs.  The staged
+// kernel (gemm_staged_kernel, wider outputs) is described further down.
 // Every wait is bounded; a wait that runs out sets the device error word and
 // the CTA drains and exits.
 #include <cuda.h>
