@@ -18,6 +18,7 @@
 // order.
 #include <cuda_runtime.h>
 
+#include "decode.cuh"
 #include "mix_internal.h"
 
 namespace mixk {
@@ -47,14 +48,11 @@ __device__ __forceinline__ int a_factor(uint32_t c) {
   return (c & 8u) ? -v : v;
 }
 
-__device__ __forceinline__ int b_value(uint32_t c, int fp4) {
-  if (fp4) {
-    const int e = (int)((c >> 1) & 3u), m = (int)(c & 1u);
-    const int v = e ? ((2 + m) << (e - 1)) : m;  // E2M1 value in half units
-    return (c & 8u) ? -v : v;
-  }
-  return (c & 8u) ? (int)c - 16 : (int)c;  // INT4 two's complement
-}
+// W-MX element code -> int8 value through two 8-entry byte tables and a
+// byte select by the sign bit (dec8): E2M1 in half units (0, 1, 2, 3, 4, 6,
+// 8, 12 and their negatives), INT4 as its two's complement value.
+__device__ __forceinline__ DecTab fp4_int8_tab() { return DecTab{0x03020100u, 0x0C080604u, 0xFDFEFF00u, 0xF4F8FAFCu}; }
+__device__ __forceinline__ DecTab int4_int8_tab() { return DecTab{0x03020100u, 0x07060504u, 0xFBFAF9F8u, 0xFFFEFDFCu}; }
 
 // G16: weights with one scale per 16 elements; each 32-block's two halves
 // (sub-trees 0-1 and 2-3) take their own exponent add.
@@ -115,12 +113,9 @@ __global__ void __launch_bounds__(kThreads) gemv_shiftadd_kernel(GemvArgs p) {
       const uint4 cw = *reinterpret_cast<const uint4*>(brow + b * 16);
       const int X = (int)bsc[G16 ? 2 * b : b] - 127;
       const int X1 = G16 ? (int)bsc[2 * b + 1] - 127 : 0;
-      int wv[32];
-      const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) wv[8 * q + i] = b_value((cws[q] >> (4 * i)) & 0xFu, p.b_fp4);
+      // the block's 32 weights as int8, four per word (element order)
+      const DecTab tb = p.b_fp4 ? fp4_int8_tab() : int4_int8_tab();
+      const uint2 bw[4] = {dec8(cw.x, tb), dec8(cw.y, tb), dec8(cw.z, tb), dec8(cw.w, tb)};
 #pragma unroll
       for (int m = 0; m < kMaxM; ++m) {
         if (m < p.M) {
@@ -131,12 +126,11 @@ __global__ void __launch_bounds__(kThreads) gemv_shiftadd_kernel(GemvArgs p) {
           for (int q = 0; q < 4; ++q) {
             const int4 f0 = *reinterpret_cast<const int4*>(f + 8 * q);
             const int fw[4] = {f0.x, f0.y, f0.z, f0.w};
-            int S = 0;  // one 8-way shift-add sub-tree
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              S += wv[8 * q + 2 * i] * (int)(int16_t)(fw[i] & 0xFFFF);
-              S += wv[8 * q + 2 * i + 1] * (fw[i] >> 16);
-            }
+            // one 8-way shift-add sub-tree: four 2-way 16 x 8-bit dot products
+            int S = __dp2a_lo(fw[0], (int)bw[q].x, 0);
+            S = __dp2a_hi(fw[1], (int)bw[q].x, S);
+            S = __dp2a_lo(fw[2], (int)bw[q].y, S);
+            S = __dp2a_hi(fw[3], (int)bw[q].y, S);
             blockv += S * (8 + ((sh.y >> (8 * q)) & 0xFF));  // x (1.mshared_k) in eighths
             if (G16 && q == 1) {
               half0 = blockv;
