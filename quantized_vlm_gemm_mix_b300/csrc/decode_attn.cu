@@ -76,16 +76,50 @@ __device__ __forceinline__ int mix_factor(uint32_t c) {
   return (c & 8u) ? -v : v;
 }
 
-// Decode one quantised MiX-4.5b block into factors and (Emax, packed m3s).
-__device__ __forceinline__ void mix_unpack(const uint4& cw, uint32_t sh, int ebias, int16_t* f, int2* meta) {
-  const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+// Algorithm 1 (MiX-4.5b) on one 32-element block by four consecutive lanes
+// of a fully active warp: lane q holds sub-block q (eight fp32 patterns, no
+// NaN).  The same steps as mix_block32<2> -- block maximum (by shuffles),
+// Emax and this sub-block's mshared, the element step, canonical zeros --
+// with a quarter of the serial work per thread.  Returns this lane's code
+// word; sh, the block's shared field, is the same in all four lanes.
+__device__ __forceinline__ uint32_t mix_block32_quad(const uint32_t* u, int q, int ebias, bool asym, uint32_t& sh) {
+  uint32_t ks = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
+  for (int i = 0; i < 8; ++i) ks = max(ks, u[i] & 0x7FFFFFFFu);
+  uint32_t kb = max(ks, __shfl_xor_sync(0xFFFFFFFFu, ks, 1));
+  kb = max(kb, __shfl_xor_sync(0xFFFFFFFFu, kb, 2));
+  int f, m3;
+  const bool nz = max_exp_mant(kb, &f, &m3);
+  const int emax = clampi(f, ebias, ebias + 15);
+  uint32_t word = 0x77777777u, mine = 0u;
+  if (nz) {
+    int fs, ms;
+    if (!max_exp_mant(ks, &fs, &ms)) ms = 0;
+    const MixBlk bb = mix_blk(emax, 8 + ms, asym);
+    word = 0u;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) f[8 * j + i] = (int16_t)mix_factor((w[j] >> (4 * i)) & 0xFu);
-  const int mk = (int)(((sh >> 4) & 7u) | (((sh >> 7) & 7u) << 8) | (((sh >> 10) & 7u) << 16) |
-                       (((sh >> 13) & 7u) << 24));
-  *meta = make_int2((int)(sh & 0xFu) + ebias, mk);
+    for (int i = 0; i < 8; ++i) word |= mix_code_nonan(u[i], u[i] & 0x7FFFFFFFu, bb) << (4 * i);
+    if (word != 0x77777777u) mine = (uint32_t)ms << (4 + 3 * q);
+  }
+  uint32_t allz = word == 0x77777777u ? 1u : 0u;
+  allz &= __shfl_xor_sync(0xFFFFFFFFu, allz, 1);
+  allz &= __shfl_xor_sync(0xFFFFFFFFu, allz, 2);
+  uint32_t bits = mine | __shfl_xor_sync(0xFFFFFFFFu, mine, 1);
+  bits |= __shfl_xor_sync(0xFFFFFFFFu, bits, 2);
+  sh = (nz && !allz) ? ((uint32_t)(emax - ebias) | bits) : 0u;
+  return word;
+}
+
+// This lane's eight factors of a quad-quantised block, and (lane 0 of the
+// quad) the block's (Emax, packed mshared).
+__device__ __forceinline__ void mix_unpack_quad(uint32_t word, uint32_t sh, int q, int ebias, int16_t* f, int2* meta) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) f[8 * q + i] = (int16_t)mix_factor((word >> (4 * i)) & 0xFu);
+  if (q == 0) {
+    const int mk = (int)(((sh >> 4) & 7u) | (((sh >> 7) & 7u) << 8) | (((sh >> 10) & 7u) << 16) |
+                         (((sh >> 13) & 7u) << 24));
+    *meta = make_int2((int)(sh & 0xFu) + ebias, mk);
+  }
 }
 
 // v * 2^e for an integer-valued v (|v| < 2^24, exact in fp32): one exact
@@ -155,21 +189,27 @@ __global__ void __launch_bounds__(kChunkA * kMaxG, 2) attn_qk_kernel(AttnArgs a)
     for (int b = 0; b < 4; ++b) kw[b] = __ldg(reinterpret_cast<const uint4*>(a.k_codes + row * (kD / 2)) + b);
     scw = __ldg(reinterpret_cast<const uint32_t*>(a.k_scales + row * (kD / 32)));
   }
-  // the group's query heads -> MiX-4.5b, decoded into factors
-  if (tid < a.G * 4) {
-    const int hh = tid >> 2, b = tid & 3;
-    uint32_t u[32];
-    const int64_t base = (int64_t)(g * a.G + hh) * kD + 32 * b;
+  // the group's query heads -> MiX-4.5b, decoded into factors: four lanes per
+  // 32-element block (sixteen per head), whole warps
+  const int q_warps = (a.G + 1) / 2, warp_id = tid >> 5;
+  if (warp_id < q_warps) {
+    const int hh = tid >> 4, b = (tid >> 2) & 3, qq = tid & 3;
+    uint32_t u[8] = {};
+    if (hh < a.G) {
+      const int64_t base = (int64_t)(g * a.G + hh) * kD + 32 * b + 8 * qq;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) u[i] = load_bits(a.q, bf16, base + i);
-    uint4 cw;
+      for (int i = 0; i < 8; ++i) u[i] = load_bits(a.q, bf16, base + i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if ((u[i] & 0x7FFFFFFFu) > 0x7F800000u) u[i] = 0u;  // NaN codes as zero
+    }
     uint32_t sh;
-    mix_block32<2>(u, a.q_ebias, true, cw, sh);
-    mix_unpack(cw, sh, a.q_ebias, &qf[hh][32 * b], &qmeta[hh][b]);
-  } else if (a.k_new != nullptr && t_new / kChunkA == c && tid < a.G * 4 + 4) {
-    // append the new key: K' = fp32(k) - mean, MXINT4 along head_dim (the
-    // four threads after the query quantisers; 64 G >= 4 G + 4 for G >= 1)
-    const int b = tid - a.G * 4;
+    const uint32_t word = mix_block32_quad(u, qq, a.q_ebias, true, sh);
+    if (hh < a.G) mix_unpack_quad(word, sh, qq, a.q_ebias, &qf[hh][32 * b], &qmeta[hh][b]);
+  } else if (a.k_new != nullptr && t_new / kChunkA == c && warp_id == 2 * a.G - 1 && (tid & 31) < 4) {
+    // append the new key: K' = fp32(k) - mean, MXINT4 along head_dim (four
+    // lanes of the block's last warp, never one of the query warps)
+    const int b = tid & 31;
     uint32_t u[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
@@ -261,8 +301,8 @@ __global__ void __launch_bounds__(kD * kMaxG) attn_pv_kernel(AttnArgs a) {
   }
   __syncthreads();
 
-  // P for this chunk: every thread forms some, then one thread per (head,
-  // 32-token block) requantises them to MiX-4.5b
+  // P for this chunk: every thread forms some, then four lanes per (head,
+  // 32-token block) requantise them to MiX-4.5b
   for (int i = tid; i < a.G * kChunkB; i += nthr) {
     const int hh = i / kChunkB, j = i % kChunkB;
     const int64_t t = t0 + j;
@@ -272,20 +312,22 @@ __global__ void __launch_bounds__(kD * kMaxG) attn_pv_kernel(AttnArgs a) {
     pv[hh][j] = p;
   }
   __syncthreads();
-  if (tid < a.G * (kChunkB / 32)) {
-    const int hh = tid >> 3, b = tid & 7;
-    if (b < nblk) {
-      uint32_t u[32];
+  if (warp < a.G) {  // warp hh: its 8 blocks, four lanes per block
+    const int hh = warp, b = lane >> 2, qq = lane & 3;
+    uint32_t u[8];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(pv[hh][32 * b + i]);
-      uint4 cw;
-      uint32_t sh;
-      mix_block32<2>(u, a.p_ebias, true, cw, sh);
-      mix_unpack(cw, sh, a.p_ebias, &pf[hh][32 * b], &pmeta[hh][b]);
+    for (int i = 0; i < 8; ++i) {
+      u[i] = __float_as_uint(pv[hh][32 * b + 8 * qq + i]);
+      if ((u[i] & 0x7FFFFFFFu) > 0x7F800000u) u[i] = 0u;  // NaN codes as zero
+    }
+    uint32_t sh;
+    const uint32_t word = mix_block32_quad(u, qq, a.p_ebias, true, sh);
+    if (b < nblk) {
+      mix_unpack_quad(word, sh, qq, a.p_ebias, &pf[hh][32 * b], &pmeta[hh][b]);
       if (a.p_codes != nullptr) {
         const int64_t e = (int64_t)(g * a.G + hh) * a.v_ld + t0 + 32 * b;
-        *reinterpret_cast<uint4*>(a.p_codes + e / 2) = cw;
-        a.p_shared[e / 32] = (uint16_t)sh;
+        reinterpret_cast<uint32_t*>(a.p_codes + e / 2)[qq] = word;
+        if (qq == 0) a.p_shared[e / 32] = (uint16_t)sh;
       }
     }
   }
