@@ -171,6 +171,29 @@ def roof_seconds(nbytes, flops):
 
 
 # ---------------------------------------------------------------------------
+# Replicas (N > 1): every rank runs the whole step on its own GPU; the only
+# exchanges are the barriers around the timed region and the max of the
+# ranks' times.  No collective touches the data path.
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(torch, dist, v, device):
+    """The largest of the ranks' values v (every rank gets it); v itself with
+    no process group."""
+    if dist is None:
+        return v
+    t = torch.tensor([v], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(roof_s, world, ms_step):
+    """Whole-job throughput as a percentage of ONE B300's roofline: the work
+    of all `world` replicas (each one step's roofline time roof_s) over the
+    slowest rank's time per step."""
+    return 100.0 * roof_s * world / (ms_step * 1e-3)
+
+
+# ---------------------------------------------------------------------------
 # Workload
 # ---------------------------------------------------------------------------
 
@@ -714,13 +737,6 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(v):
-        if not dist:
-            return v
-        t = torch.tensor([v], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     for _ in range(max(3, args.warmup)):
         step()
     barrier()
@@ -752,7 +768,7 @@ def main():
     t1.record(stream)
     barrier()
     clk = clocks.stop()
-    ms_step = max_over_ranks(t0.elapsed_time(t1)) / args.steps
+    ms_step = max_over_ranks(torch, dist, t0.elapsed_time(t1), dev) / args.steps
     assert mix.mix_device_error() == 0, "a kernel reported a timed-out wait"
 
     # Per-call durations: a second timed pass, CUDA events on the launching
@@ -773,7 +789,7 @@ def main():
     per_call /= args.steps
 
     roof_s = sum(c.roof_s() for c in calls)
-    value = 100.0 * roof_s * world / (ms_step * 1e-3)
+    value = job_value(roof_s, world, ms_step)
     ext = None if args.no_ext else measure_extensions(torch, mix, stream)
 
     e2e = None
@@ -838,8 +854,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ms_e2e = max_over_ranks(e0.elapsed_time(e1)) / args.steps
-        e2e = {"value": round(100.0 * roof_s * world / (ms_e2e * 1e-3), 3), "unit": UNIT,
+        ms_e2e = max_over_ranks(torch, dist, e0.elapsed_time(e1), dev) / args.steps
+        e2e = {"value": round(job_value(roof_s, world, ms_e2e), 3), "unit": UNIT,
                "ms_per_step": round(ms_e2e, 4), "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
                "overlap": "2 steps in flight: upload, compute and download on separate streams"}
 

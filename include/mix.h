@@ -281,8 +281,9 @@ MIX_API mix_status_t mix_mx_gemm(const mix_gemm_desc_t* desc, void* workspace, s
  * mean).  KSMOOTH_APPLY_FROZEN: mean is an input (frozen at prefill; decode
  * does not re-read the cache).  Both modes write k_out = fp32(k) - mean (one
  * fp32 subtraction), tokens x heads x head_dim dense, when k_out != NULL.
- * COMPUTE splits the tokens across CTAs and keeps fp64 partial sums in the
- * caller's workspace (ksmooth_workspace_bytes); APPLY needs none. */
+ * COMPUTE splits the tokens across CTAs and keeps per-chunk partial sums
+ * (fp32 pairs, about 48 bits) in the caller's workspace
+ * (ksmooth_workspace_bytes); APPLY needs none. */
 enum { KSMOOTH_COMPUTE = 0, KSMOOTH_APPLY_FROZEN = 1 };
 MIX_API size_t ksmooth_workspace_bytes(int64_t tokens, int heads, int head_dim);
 MIX_API mix_status_t ksmooth_kv(const void* k, mix_dtype_t dtype, int64_t tokens, int heads, int head_dim,
@@ -295,7 +296,7 @@ MIX_API mix_status_t ksmooth_kv(const void* k, mix_dtype_t dtype, int64_t tokens
  * device memory belongs to their own allocator, and loops that must not call
  * cudaMalloc (which can synchronise the device).  Arguments and results are
  * those of ksmooth_kv; the caller still passes k, mean and k_out.  COMPUTE
- * keeps its fp64 partial sums in a fixed array built into the library
+ * keeps its partial sums in a fixed array built into the library
  * (KSMOOTH_NOALLOC_SCRATCH_BYTES, held on every GPU that loads the library
  * until the process exits) and allocates nothing.
  *  - Size limit: a COMPUTE call whose ksmooth_workspace_bytes(tokens, heads,

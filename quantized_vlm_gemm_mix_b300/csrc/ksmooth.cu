@@ -5,13 +5,14 @@
 //
 // COMPUTE: the tokens are split into chunks across CTAs (the whole tensor has
 // to be in flight to reach HBM bandwidth); each CTA sums its chunk per
-// channel and writes one fp64 partial row to the caller's workspace.  A
-// thread's own run of tokens is summed in double-float (an fp32 pair kept
-// exact by Knuth's two-sum, ~48-bit precision) because fp64 arithmetic is
-// slow on this part; the cross-warp and cross-chunk sums are fp64.  A second
-// kernel adds the partial rows in a fixed order and divides by the token
-// count, so the result does not depend on scheduling.  APPLY (both
-// modes): k_out = fp32(k) - mean, one fp32 subtraction per element.
+// channel and writes one partial row to the caller's workspace.  Every sum is
+// a double-float (an fp32 pair (hi, lo) kept exact by Knuth's two-sum, about
+// 48 bits of precision) because fp64 arithmetic is slow on this part: a
+// thread's own run of tokens, the cross-warp sum and the cross-chunk sum.  A
+// second kernel adds the partial rows in a fixed order and divides by the
+// token count (the one fp64 operation per channel), so the result does not
+// depend on scheduling.  APPLY (both modes): k_out = fp32(k) - mean, one fp32
+// subtraction per element.
 #include <cuda_runtime.h>
 
 #include "mix_internal.h"
@@ -38,61 +39,103 @@ __device__ __forceinline__ void load8f(const void* base, bool bf16, int64_t elem
   }
 }
 
+// Knuth's two-sum: a + b = s + e exactly.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float bv = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bv)), __fsub_rn(b, bv));
+}
+
+// (h, l) += (bh, bl) in double-float, renormalised with a second two-sum.
+__device__ __forceinline__ void df_add(float& h, float& l, float bh, float bl) {
+  float s, e;
+  two_sum(h, bh, s, e);
+  two_sum(s, __fadd_rn(e, __fadd_rn(l, bl)), h, l);
+}
+
+constexpr int kBatch = 8;  // tokens whose loads a thread has in flight at once
+
 // grid (channel tiles of 256, chunks).  Warp w sums tokens t0 + w, t0 + w + 8,
-// ... of the chunk; lane l owns channels c0 + 8l .. c0 + 8l + 7.
+// ... of the chunk, kBatch of them per round of loads; lane l owns channels
+// c0 + 8l .. c0 + 8l + 7.  partial[chunk][c] = (hi, lo).
 __global__ void __launch_bounds__(kThreads) ksmooth_partial_kernel(
     const void* __restrict__ k, int bf16, int64_t tokens, int64_t C, int64_t ld, int64_t chunk,
-    double* __restrict__ partial) {
-  __shared__ double red[8][256];
+    float2* __restrict__ partial) {
+  __shared__ float2 red[8][256];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t c = (int64_t)blockIdx.x * 256 + lane * 8;
   const int64_t t0 = (int64_t)blockIdx.y * chunk;
   const int64_t t1 = min(tokens, t0 + chunk);
   float hi[8] = {0, 0, 0, 0, 0, 0, 0, 0}, lo[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (c < C) {
-    for (int64_t t = t0 + warp; t < t1; t += 8) {
-      float v[8];
-      load8f(k, bf16 != 0, t * ld + c, v);
+    for (int64_t tb = t0 + warp; tb < t1; tb += 8 * kBatch) {
+      float v[kBatch][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        // two-sum: hi + v = s + e exactly
-        const float sum = __fadd_rn(hi[i], v[i]);
-        const float bv = __fsub_rn(sum, hi[i]);
-        const float e = __fadd_rn(__fsub_rn(hi[i], __fsub_rn(sum, bv)), __fsub_rn(v[i], bv));
-        hi[i] = sum;
-        lo[i] = __fadd_rn(lo[i], e);
+      for (int b = 0; b < kBatch; ++b) {
+        const int64_t t = tb + 8 * b;
+        if (t < t1) {
+          load8f(k, bf16 != 0, t * ld + c, v[b]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[b][i] = 0.0f;  // adding +0 leaves the pair unchanged
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float s, e;
+          two_sum(hi[i], v[b][i], s, e);
+          hi[i] = s;
+          lo[i] = __fadd_rn(lo[i], e);
+        }
       }
     }
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) red[warp][lane * 8 + i] = (double)hi[i] + (double)lo[i];
+  for (int i = 0; i < 8; ++i) red[warp][lane * 8 + i] = make_float2(hi[i], lo[i]);
   __syncthreads();
   const int64_t cc = (int64_t)blockIdx.x * 256 + threadIdx.x;
   if (cc < C) {
-    double acc = 0.0;
+    float h = 0.0f, l = 0.0f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) acc += red[w][threadIdx.x];
-    partial[(int64_t)blockIdx.y * C + cc] = acc;
+    for (int w = 0; w < 8; ++w) df_add(h, l, red[w][threadIdx.x].x, red[w][threadIdx.x].y);
+    partial[(int64_t)blockIdx.y * C + cc] = make_float2(h, l);
   }
 }
 
-// One thread per channel adds the chunk partials in a fixed order: four
-// interleaved chains (chunk j goes to chain j % 4), then (c0 + c1) + (c2 + c3).
-// The unrolled loop keeps sixteen loads in flight instead of one.
-__global__ void ksmooth_finalize_kernel(const double* __restrict__ partial, int64_t nchunks, int64_t C,
-                                        int64_t tokens, float* __restrict__ mean) {
-  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= C) return;
-  double a[4] = {0.0, 0.0, 0.0, 0.0};
-  int64_t j = 0;
-#pragma unroll 4
-  for (; j + 4 <= nchunks; j += 4) {
+// grid ceil(C / 32), 256 threads: lane x owns channel c0 + x and row y
+// (threadIdx.x / 32) adds chunks y, y + 8, ... (all of its loads in flight);
+// the eight rows are then added in order 0..7.  The one fp64 step is the
+// division of the pair's sum by the token count.
+__global__ void __launch_bounds__(256) ksmooth_finalize_kernel(const float2* __restrict__ partial,
+                                                               int64_t nchunks, int64_t C, int64_t tokens,
+                                                               float* __restrict__ mean) {
+  __shared__ float2 red[8][32];
+  const int x = threadIdx.x & 31, y = threadIdx.x >> 5;
+  const int64_t c = (int64_t)blockIdx.x * 32 + x;
+  float h = 0.0f, l = 0.0f;
+  if (c < C) {
+    int64_t j = y;
+    for (; j + 24 < nchunks; j += 32) {
+      float2 p[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) a[i] += __ldg(partial + (j + i) * C + c);
+      for (int i = 0; i < 4; ++i) p[i] = __ldg(partial + (j + 8 * i) * C + c);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) df_add(h, l, p[i].x, p[i].y);
+    }
+    for (; j < nchunks; j += 8) {
+      const float2 p = __ldg(partial + j * C + c);
+      df_add(h, l, p.x, p.y);
+    }
   }
-  for (int i = 0; j < nchunks; ++j, ++i) a[i] += __ldg(partial + j * C + c);
-  const double acc = (a[0] + a[1]) + (a[2] + a[3]);
-  mean[c] = (float)(acc / (double)tokens);
+  red[y][x] = make_float2(h, l);
+  __syncthreads();
+  if (y == 0 && c < C) {
+#pragma unroll
+    for (int w = 1; w < 8; ++w) df_add(h, l, red[w][x].x, red[w][x].y);
+    mean[c] = (float)(((double)h + (double)l) / (double)tokens);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads) ksmooth_apply_kernel(
@@ -118,7 +161,7 @@ int64_t ksmooth_chunks(int64_t tokens, int64_t C) {
   int64_t want = (4 * (int64_t)num_sms() + tiles - 1) / tiles;  // about four CTAs per SM
   const int64_t by_len = (tokens + 31) / 32;                    // at least 32 tokens per chunk
   if (want > by_len) want = by_len;
-  if (want > 32) want = 32;  // keeps the fp64 chain of the finalize short
+  if (want > 32) want = 32;  // keeps the finalize's chain short
   return want > 0 ? want : 1;
 }
 
@@ -127,7 +170,7 @@ int64_t ksmooth_chunks(int64_t tokens, int64_t C) {
 size_t ksmooth_ws_bytes(int64_t tokens, int heads, int head_dim) {
   const int64_t C = (int64_t)heads * head_dim;
   if (tokens <= 0 || C <= 0) return 0;
-  return (size_t)ksmooth_chunks(tokens, C) * (size_t)C * sizeof(double);
+  return (size_t)ksmooth_chunks(tokens, C) * (size_t)C * sizeof(float2);
 }
 
 cudaError_t launch_ksmooth(const void* k, bool bf16, int64_t tokens, int heads, int head_dim,
@@ -140,11 +183,11 @@ cudaError_t launch_ksmooth(const void* k, bool bf16, int64_t tokens, int heads, 
     const int64_t used = (tokens + chunk - 1) / chunk;
     const dim3 grid((unsigned)((C + 255) / 256), (unsigned)used);
     ksmooth_partial_kernel<<<grid, kThreads, 0, st>>>(k, bf16 ? 1 : 0, tokens, C, ld, chunk,
-                                                      static_cast<double*>(ws));
+                                                      static_cast<float2*>(ws));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    ksmooth_finalize_kernel<<<(unsigned)((C + 127) / 128), 128, 0, st>>>(
-        static_cast<const double*>(ws), used, C, tokens, mean);
+    ksmooth_finalize_kernel<<<(unsigned)((C + 31) / 32), 256, 0, st>>>(static_cast<const float2*>(ws), used,
+                                                                       C, tokens, mean);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -164,7 +207,7 @@ cudaError_t launch_ksmooth(const void* k, bool bf16, int64_t tokens, int heads, 
 // No-allocation variant.  Some callers cannot hand the library device memory:
 // code running while a CUDA graph is being captured, hosts whose device memory
 // is owned by their own allocator, loops that must never call cudaMalloc (it
-// can synchronise the device).  For them the fp64 partial sums of COMPUTE live
+// can synchronise the device).  For them the partial sums of COMPUTE live
 // in a fixed array compiled into the library instead of a caller workspace.
 // Every GPU that loads the library keeps this array until the process exits.
 // ---------------------------------------------------------------------------
@@ -174,7 +217,7 @@ namespace mixk {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = (size_t)2 << 20;  // 2 MiB
-static __device__ __align__(256) double g_ksmooth_scratch[kNoAllocScratchBytes / sizeof(double)];
+static __device__ __align__(256) float2 g_ksmooth_scratch[kNoAllocScratchBytes / sizeof(float2)];
 
 std::mutex g_scratch_mu;
 void* g_scratch_addr[64] = {nullptr};
