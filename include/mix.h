@@ -292,9 +292,10 @@ MIX_API mix_status_t ksmooth_kv(const void* k, mix_dtype_t dtype, int64_t tokens
 
 /* No-allocation variant of ksmooth_kv.  The paper has no counterpart for
  * this entry point; it exists for callers that cannot give the library device
- * memory: code that runs while a CUDA graph is being captured, hosts whose
- * device memory belongs to their own allocator, and loops that must not call
- * cudaMalloc (which can synchronise the device).  Arguments and results are
+ * memory: hosts whose device memory all belongs to their own allocator (a
+ * framework's pool that hands out no raw buffers), and serving or decode loops
+ * that must not call cudaMalloc, which can synchronise the whole device and
+ * stall every stream.  Arguments and results are
  * those of ksmooth_kv; the caller still passes k, mean and k_out.  COMPUTE
  * keeps its partial sums in a fixed array built into the library
  * (KSMOOTH_NOALLOC_SCRATCH_BYTES, held on every GPU that loads the library

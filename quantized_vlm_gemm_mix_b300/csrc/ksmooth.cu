@@ -205,9 +205,8 @@ cudaError_t launch_ksmooth(const void* k, bool bf16, int64_t tokens, int heads, 
 
 // ---------------------------------------------------------------------------
 // No-allocation variant.  Some callers cannot hand the library device memory:
-// code running while a CUDA graph is being captured, hosts whose device memory
-// is owned by their own allocator, loops that must never call cudaMalloc (it
-// can synchronise the device).  For them the partial sums of COMPUTE live
+// hosts whose device memory is all owned by their own allocator, and loops
+// that must never call cudaMalloc (it can synchronise the whole device).  For them the partial sums of COMPUTE live
 // in a fixed array compiled into the library instead of a caller workspace.
 // Every GPU that loads the library keeps this array until the process exits.
 // ---------------------------------------------------------------------------

@@ -248,7 +248,8 @@ def ksmooth_kv(k, tokens, heads, head_dim, ld, mean, mode, k_out, workspace=None
 
 def ksmooth_kv_noalloc(k, tokens, heads, head_dim, ld, mean, mode, k_out, stream=None) -> None:
     """ksmooth_kv without a workspace: for callers that cannot allocate device
-    memory (graph capture, externally owned allocators).  COMPUTE is limited to
+    memory (an allocator that owns all of it, loops that must not call
+    cudaMalloc).  COMPUTE is limited to
     KSMOOTH_NOALLOC_SCRATCH_BYTES of partial sums; see include/mix.h."""
     _check(lib.ksmooth_kv_noalloc(_ptr(k), _dtype(k), tokens, heads, head_dim, ld, _ptr(mean), mode,
                                   _ptr(k_out), _stream(stream)), "ksmooth_kv_noalloc")

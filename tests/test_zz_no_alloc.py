@@ -1,8 +1,8 @@
 """The no-allocation K-smoothing entry point (ksmooth_kv_noalloc).
 
-Some callers cannot give the library device memory: code running inside a
-CUDA graph capture, hosts whose allocator owns all device memory, loops that
-must never call cudaMalloc.  This entry point keeps its partial sums in a
+Some callers cannot give the library device memory: hosts whose allocator owns
+all device memory, and loops that must never call cudaMalloc because it can
+synchronise the whole device.  This entry point keeps its partial sums in a
 fixed array inside the library.  These tests call it through the C ABI twice
 in a row and check each result against the workspace-taking ksmooth_kv on the
 same input, within the tolerance the K-smoothing tests use; the file runs
