@@ -100,6 +100,7 @@ static void max_exp_mant(double amax, int* f_out, int* m3_out) {
 static double mix_value(int s, int d, int emax, int m3) {
   double M = 1.0 + m3 / 8.0;
   if (g_mutation == 2) M = m3 / 8.0;       /* planted: implicit leading 1 dropped */
+  if (d == 7 && s && g_mutation == 13) return -ldexp(M, emax - 7);   /* planted: recycled -0 negative */
   if (d == 7) return s ? ldexp(M, emax - 7) : 0.0;
   double v = ldexp(M, emax - d);
   return s ? -v : v;
@@ -163,6 +164,7 @@ static void mix_block(const double* v, int type, int ebias, unsigned flags,
       int fk = 0, mk = 0;
       if (sm > 0.0) max_exp_mant(sm, &fk, &mk);
       m3s[k] = mk;                         /* a carry only zeroes mk; Emax stays */
+      if (g_mutation == 12) m3s[k] = m3;   /* planted: sub-block mantissa from the block max */
     }
   }
   for (int i = 0; i < 32; ++i) codes[i] = mix_element(v[i], emax, m3s[i / 8], asym);
@@ -194,7 +196,9 @@ int orc_mix_quantize(const void* x, int dtype, int64_t rows, int64_t k, int64_t 
       for (int i = 0; i < 32; ++i) v[i] = load_elem(x, dtype, r * ld + b * 32 + i);
       mix_block(v, type, ebias, flags, c, &ec, m3s);
       uint8_t* out = codes + r * (k / 2) + b * 16;
-      for (int j = 0; j < 16; ++j) out[j] = (uint8_t)(c[2 * j] | (c[2 * j + 1] << 4));
+      for (int j = 0; j < 16; ++j)
+        out[j] = g_mutation == 18 ? (uint8_t)((c[2 * j] << 4) | c[2 * j + 1])   /* planted: nibble order */
+                                  : (uint8_t)(c[2 * j] | (c[2 * j + 1] << 4));
       if (type == ORC_T1) {
         ((uint8_t*)shared)[r * nb + b] = (uint8_t)(ec | (m3s[0] << 4));
       } else {
@@ -328,6 +332,7 @@ static int int4_code(double y) {
   double a = fabs(y);
   double q = isinf(a) ? 7.0 : rne(a);
   if (q > 7.0) q = 7.0;
+  if (g_mutation == 14 && isfinite(a) && rne(a) >= 8.0) q = 8.0;   /* planted: clamp at 8 */
   int qi = (int)q;
   if (y < 0.0) qi = -qi;
   return qi & 0xF;
@@ -394,6 +399,7 @@ static double mx_value(int code, int X, int type) {
     return (code & 8) ? -v : v;
   }
   int q = (code & 8) ? code - 16 : code;
+  if (g_mutation == 19) return ldexp((double)q, X - 1);   /* planted: INT4 step of 2^(X-1) */
   return ldexp((double)q, X - 2);
 }
 
@@ -519,7 +525,7 @@ int64_t orc_underflow_count(const void* x, int dtype, int64_t rows, int64_t k, i
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t i = 0; i < k; ++i) {
       double v = load_elem(x, dtype, r * ld + i);
-      if (isnan(v) || v == 0.0 || isinf(v)) continue;
+      if (isnan(v) || (v == 0.0 && g_mutation != 16) || isinf(v)) continue;   /* 16 planted: zeros counted */
       int c = nibble(codes + r * (k / 2), i);
       int zero = fmt == 0 ? c == 0x7 : fmt == 1 ? c == 0 : (c & 7) == 0;
       n += zero;
@@ -579,6 +585,7 @@ int orc_gemm_blk(const uint8_t* a_codes, const void* a_shared, int a_type, int a
               int cb = nibble(bc + n * (K / 2), b * 32 + i);
               int s = ca >> 3, d = ca & 7;
               if (d == 7 && s == 0) continue;          /* zero code */
+              if (d == 7 && g_mutation == 17) continue;   /* planted: recycled -0 dropped */
               if (d == 7) s = 0;                       /* recycled -0: positive */
               int wm, ws;
               mx_int_parts(cb, b_type, &wm, &ws);
@@ -586,7 +593,7 @@ int orc_gemm_blk(const uint8_t* a_codes, const void* a_shared, int a_type, int a
               if (g_mutation == 6) t = (int64_t)wm << (7 - d);   /* planted: FP4 exponent dropped */
               S += s ? -t : t;
             }
-            block += S * (8 + m3s[sb]);     /* x (1.mshared) in eighths */
+            block += S * (8 + m3s[g_mutation == 15 ? 0 : sb]);   /* x (1.mshared) in eighths */
             if (b_block == 16 && (sb & 1)) {  /* end of a 16-element half */
               int X = (int)bs[n * nbb + 2 * b + (g_mutation == 10 ? 0 : (sb >> 1))] - 127;
               acc += ldexp((double)block, emax + X - 10 - cB);

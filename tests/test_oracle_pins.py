@@ -827,15 +827,22 @@ def test_pin(orc, pin):
 # dropped from the Eq. (6) shift, 7 smoothing adds the mean, 8 the tight MX
 # exponent steps past a block maximum on the boundary, 9 the automatic ebias
 # drops the rounding carry, 10 the g16 matmul reads the first half's scale
-# for both halves, 11 the E4M3 rounding of the NVFP4 block scale truncates.
+# for both halves, 11 the E4M3 rounding of the NVFP4 block scale truncates,
+# 12 a Type 2 sub-block takes its mantissa from the whole block's maximum,
+# 13 the recycled -0 decodes as a negative value, 14 MXINT4 saturates at 8
+# (which wraps to the code of -8), 15 the Type 2 matmul scales every
+# sub-block by sub-block 0's mantissa, 16 the underflow count also counts
+# elements that were zero before quantisation, 17 the matmul drops the
+# recycled -0 as if it coded zero, 18 element nibbles are packed high nibble
+# first, 19 the MXINT4 element step is 2^(X-1) instead of 2^(X-2).
 FAST_PINS = [pin_dequant_special_values, pin_round_trip, pin_asymmetric_zero,
              pin_e2m1_and_int4_brute_force, pin_mx_scale_rule, pin_gemm_eq6_exact,
              pin_gemm_against_dequant_matmul, pin_ksmooth, pin_nonfinite_and_zero_blocks,
-             pin_mx_tight_rule, pin_auto_ebias, pin_gemm_g16, pin_nvfp4,
+             pin_mx_tight_rule, pin_auto_ebias, pin_gemm_g16, pin_nvfp4, pin_underflow_count,
              lambda o: pin_refinement_brute_force(o, n_blocks=40)]
 
 
-@pytest.mark.parametrize("mutation", [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11])
+@pytest.mark.parametrize("mutation", list(range(1, 20)))
 def test_planted_mistakes_are_caught(orc, mutation):
     failed = []
     try:
