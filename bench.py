@@ -127,7 +127,8 @@ def step_table(small=False):
         plane_bytes(MV, 5120, 1), 2.0 * MV * 5120 * 1280, launches=tc_launches(5120), cpu=("gemm", MV * 5120 * 40))
     add(f"gemm_vit_fc2_{MV}x5120x1280", plane_bytes(MV, 5120, 1) + plane_bytes(1280, 5120, 0) +
         plane_bytes(MV, 1280, 1), 2.0 * MV * 1280 * 5120, launches=tc_launches(1280), cpu=("gemm", MV * 1280 * 160))
-    add(f"ksmooth_compute_{T}x{HK}x{D}", T * HK * D * (2 + 2 + 4), launches=3, cpu=("ks", 2 * T * HK * D))
+    add(f"ksmooth_compute_{T}x{HK}x{D}", T * HK * D * (2 + 4) + HK * D * 4, launches=3,
+        cpu=("ks", 2 * T * HK * D))   # K read once, K' (fp32) and the mean written once
     add(f"mix_quantize_t2_q_{T * HQ}x{D}", mix_bytes(T * HQ, D, 2), cpu=("mix2", T * HQ * D))
     add(f"mx_quantize_int4_kprime_{T * HK}x{D}", mx_bytes(T * HK, D, 4), cpu=("mx", T * HK * D))
     add(f"bmm_qk_{HQ}x{T}x{T}x{D}", plane_bytes(T * HQ, D, 2) + plane_bytes(T * HK, D, 0) + HQ * T * T * 4,
