@@ -161,3 +161,46 @@ def test_decode_attention_validation(mix):
         assert L.mix_decode_attention_workspace_bytes(ctypes.byref(d)) == 0
         setattr(d, field, saved)
 
+
+
+# ---------------------------------------------------------------------------
+# The ctypes binding mirrors the header: every enum and define it repeats, and
+# the byte layout of both descriptor structs, read from a C program compiled
+# against include/mix.h.
+
+_MIRRORED = ["MIX_OK", "MIX_ERR_INVALID_ARG", "MIX_ERR_SHAPE", "MIX_ERR_ALIGN", "MIX_ERR_UNSUPPORTED",
+             "MIX_ERR_CUDA", "MIX_ERR_WORKSPACE", "MIX_ERR_DEVICE", "MIX_T1_4P25", "MIX_T2_4P5", "MX_INT4",
+             "MX_FP4_E2M1", "MIX_DT_F32", "MIX_DT_BF16", "MIX_ASYM_ZERO", "MX_SCALE_FLOOR", "MX_SCALE_TIGHT",
+             "MX_BLOCK16", "MIX_UF_MIX", "MIX_UF_MXINT4", "MIX_UF_E2M1", "MIX_EPI_NONE", "MIX_EPI_MIX_T1",
+             "MIX_EPI_MIX_T2", "MIX_EPI_MXINT4", "MIX_EPI_MXFP4", "MIX_GEMM_AUTO", "MIX_GEMM_TCGEN05",
+             "MIX_GEMM_SHIFTADD", "MIX_GEMM_TCGEN05_STAGED", "MIX_GEMM_TCGEN05_FUSED", "KSMOOTH_COMPUTE",
+             "KSMOOTH_APPLY_FROZEN", "KSMOOTH_NOALLOC_SCRATCH_BYTES"]
+
+
+def _header_layout(mix, tmp_path):
+    import subprocess
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "mix.h"', "int main(void) {"]
+    for name in _MIRRORED:
+        lines.append(f'  printf("{name} %lld\\n", (long long)({name}));')
+    for struct, cls in (("mix_gemm_desc_t", mix.GemmDesc), ("mix_decode_attn_desc_t", mix.DecodeAttnDesc)):
+        lines.append(f'  printf("sizeof.{struct} %zu\\n", sizeof({struct}));')
+        for field, _ in cls._fields_:
+            lines.append(f'  printf("{struct}.{field} %zu\\n", offsetof({struct}, {field}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                    str(exe)], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    return dict((k, int(v)) for k, v in (line.split() for line in out.splitlines()))
+
+
+def test_binding_mirrors_header_constants_and_struct_layouts(mix, tmp_path):
+    got = _header_layout(mix, tmp_path)
+    for name in _MIRRORED:
+        assert getattr(mix, name) == got[name], name
+    for struct, cls in (("mix_gemm_desc_t", mix.GemmDesc), ("mix_decode_attn_desc_t", mix.DecodeAttnDesc)):
+        assert ctypes.sizeof(cls) == got[f"sizeof.{struct}"], struct
+        for field, _ in cls._fields_:
+            assert getattr(cls, field).offset == got[f"{struct}.{field}"], f"{struct}.{field}"
