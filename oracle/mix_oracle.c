@@ -589,8 +589,9 @@ int orc_gemm_blk(const uint8_t* a_codes, const void* a_shared, int a_type, int a
               if (d == 7) s = 0;                       /* recycled -0: positive */
               int wm, ws;
               mx_int_parts(cb, b_type, &wm, &ws);
-              int64_t t = (int64_t)wm << (7 - d + ws);
-              if (g_mutation == 6) t = (int64_t)wm << (7 - d);   /* planted: FP4 exponent dropped */
+              /* w' 2^(7 - de + ws) as a product: a shift of a negative w' is not defined in C */
+              int64_t t = (int64_t)wm * ((int64_t)1 << (7 - d + ws));
+              if (g_mutation == 6) t = (int64_t)wm * ((int64_t)1 << (7 - d));   /* planted: FP4 exponent dropped */
               S += s ? -t : t;
             }
             block += S * (8 + m3s[g_mutation == 15 ? 0 : sb]);   /* x (1.mshared) in eighths */

@@ -177,8 +177,10 @@ _MIRRORED = ["MIX_OK", "MIX_ERR_INVALID_ARG", "MIX_ERR_SHAPE", "MIX_ERR_ALIGN", 
              "KSMOOTH_APPLY_FROZEN", "KSMOOTH_NOALLOC_SCRATCH_BYTES"]
 
 
-def _header_layout(mix, tmp_path):
+def _header_layout(mix):
     import subprocess
+    out = os.path.join(ROOT, "_build", "abi_layout")
+    os.makedirs(out, exist_ok=True)
     lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "mix.h"', "int main(void) {"]
     for name in _MIRRORED:
         lines.append(f'  printf("{name} %lld\\n", (long long)({name}));')
@@ -187,17 +189,23 @@ def _header_layout(mix, tmp_path):
         for field, _ in cls._fields_:
             lines.append(f'  printf("{struct}.{field} %zu\\n", offsetof({struct}, {field}));')
     lines += ["  return 0;", "}"]
-    src = tmp_path / "layout.c"
-    src.write_text("\n".join(lines) + "\n")
-    exe = tmp_path / "layout"
-    subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src), "-o",
-                    str(exe)], check=True, capture_output=True)
-    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout
+    src = os.path.join(out, f"layout.{os.getpid()}.c")
+    exe = os.path.join(out, f"layout.{os.getpid()}")
+    with open(src, "w") as f:
+        f.write("\n".join(lines) + "\n")
+    try:
+        subprocess.run(["gcc", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), src, "-o", exe],
+                       check=True, capture_output=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    finally:
+        for p in (src, exe):
+            if os.path.exists(p):
+                os.remove(p)
     return dict((k, int(v)) for k, v in (line.split() for line in out.splitlines()))
 
 
-def test_binding_mirrors_header_constants_and_struct_layouts(mix, tmp_path):
-    got = _header_layout(mix, tmp_path)
+def test_binding_mirrors_header_constants_and_struct_layouts(mix):
+    got = _header_layout(mix)
     for name in _MIRRORED:
         assert getattr(mix, name) == got[name], name
     for struct, cls in (("mix_gemm_desc_t", mix.GemmDesc), ("mix_decode_attn_desc_t", mix.DecodeAttnDesc)):
