@@ -25,6 +25,14 @@
  *    launches nothing and returns a MIX_ERR_* status.  A launch failure
  *    returns MIX_ERR_CUDA.
  *  - Non-finite inputs never fault: NaN is coded as zero and +-Inf saturates.
+ *  - The element-wise kernels number their work items with 32 bits.  A call
+ *    that would need 2^32 - 1 or more returns MIX_ERR_UNSUPPORTED before any
+ *    launch.  The items are 32-element blocks for mix_quantize and for
+ *    mx_quantize along rows; 16-element blocks for nvfp4_quantize; 8-element
+ *    groups for mix_underflow_count; and 16-byte vectors of x for the amax
+ *    pass of mix_auto_ebias, mix_quantize_auto and nvfp4_quantize.  The
+ *    tightest of these is the amax pass, at 64 GiB of input (2^35 bf16 or
+ *    2^34 fp32 elements).
  *  - Sizes are in elements unless a name ends in _bytes.  The packed planes
  *    of a matrix with R rows and K columns are: codes R x K/2 bytes (element
  *    2j in the low nibble of byte j, 16-byte aligned rows), shared R x K/32

@@ -10,7 +10,7 @@ using namespace mixk;
 
 namespace {
 
-constexpr int kVersion = 10300;  // 1.3.0
+constexpr int kVersion = 10301;  // 1.3.1
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -24,6 +24,12 @@ int esize(mix_dtype_t d) { return d == MIX_DT_F32 ? 4 : 2; }
 // 16-byte codes boundary.
 bool plane_strides_ok(int64_t ld, int64_t bs, int64_t k) {
   return ld >= k && ld % 32 == 0 && bs % 32 == 0 && bs >= 0;
+}
+
+// The element-wise kernels number their work items (blocks, 16-byte vectors,
+// 8-element groups) with 32 bits: rows * per_row must stay below 2^32 - 1.
+bool items_fit(int64_t rows, int64_t per_row) {
+  return per_row <= 0 || rows <= (int64_t)(UINT32_MAX - 1u) / per_row;
 }
 
 }  // namespace
@@ -77,6 +83,7 @@ mix_status_t mix_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_
   if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(codes, 16) ||
       !aligned(shared, type == MIX_T1_4P25 ? 1 : 2))
     return MIX_ERR_ALIGN;
+  if (!items_fit(rows, k / 32)) return MIX_ERR_UNSUPPORTED;
   return from_cuda(launch_mix_quantize(x, dtype == MIX_DT_BF16, rows, k, ld, (int)type, ebias,
                                        (flags & MIX_ASYM_ZERO) != 0, codes, shared,
                                        reinterpret_cast<cudaStream_t>(stream)));
@@ -90,6 +97,7 @@ mix_status_t mix_auto_ebias(const void* x, mix_dtype_t dtype, int64_t rows, int6
   if (rows > 0 && k > 0) {
     if (x == nullptr) return MIX_ERR_INVALID_ARG;
     if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0) return MIX_ERR_ALIGN;
+    if (!items_fit(rows, k * esize(dtype) / 16)) return MIX_ERR_UNSUPPORTED;
   }
   return from_cuda(launch_auto_ebias(x, dtype == MIX_DT_BF16, rows, k, ld, ebias,
                                      reinterpret_cast<cudaStream_t>(stream)));
@@ -108,6 +116,7 @@ mix_status_t mix_quantize_auto(const void* x, mix_dtype_t dtype, int64_t rows, i
     if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(codes, 16) ||
         !aligned(shared, type == MIX_T1_4P25 ? 1 : 2))
       return MIX_ERR_ALIGN;
+    if (!items_fit(rows, k / 32) || !items_fit(rows, k * esize(dtype) / 16)) return MIX_ERR_UNSUPPORTED;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = launch_auto_ebias(x, dtype == MIX_DT_BF16, rows, k, ld, ebias, st);
@@ -127,6 +136,7 @@ mix_status_t mx_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t
   if (N == 0 || K == 0) return MIX_OK;
   if (x == nullptr || codes == nullptr || scales == nullptr) return MIX_ERR_INVALID_ARG;
   if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(codes, 16)) return MIX_ERR_ALIGN;
+  if (axis == 1 && !items_fit(N, K / 32)) return MIX_ERR_UNSUPPORTED;
   const bool fp4 = type == MX_FP4_E2M1, g16 = (flags & MX_BLOCK16) != 0;
   const int fl = mx_rule_of(flags);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
@@ -143,6 +153,7 @@ mix_status_t nvfp4_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int6
   if (rows > 0 && k > 0) {
     if (x == nullptr || codes == nullptr || scales == nullptr) return MIX_ERR_INVALID_ARG;
     if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(codes, 8)) return MIX_ERR_ALIGN;
+    if (!items_fit(rows, k / 16) || !items_fit(rows, k * esize(dtype) / 16)) return MIX_ERR_UNSUPPORTED;
   }
   return from_cuda(launch_nvfp4_quantize(x, dtype == MIX_DT_BF16, rows, k, ld, codes, scales, tensor_scale,
                                          reinterpret_cast<cudaStream_t>(stream)));
@@ -158,6 +169,7 @@ mix_status_t mix_underflow_count(const void* x, mix_dtype_t dtype, int64_t rows,
   if (rows > 0 && k > 0) {
     if (x == nullptr || codes == nullptr) return MIX_ERR_INVALID_ARG;
     if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0 || !aligned(codes, 4)) return MIX_ERR_ALIGN;
+    if (!items_fit(rows, k / 8)) return MIX_ERR_UNSUPPORTED;
   }
   return from_cuda(launch_underflow_count(x, dtype == MIX_DT_BF16, rows, k, ld, codes, (int)fmt, count,
                                           reinterpret_cast<cudaStream_t>(stream)));

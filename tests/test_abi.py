@@ -212,3 +212,35 @@ def test_binding_mirrors_header_constants_and_struct_layouts(mix):
         assert ctypes.sizeof(cls) == got[f"sizeof.{struct}"], struct
         for field, _ in cls._fields_:
             assert getattr(cls, field).offset == got[f"{struct}.{field}"], f"{struct}.{field}"
+
+
+def test_work_item_limits_are_rejected_before_launch(mix):
+    """Calls past a kernel's 32-bit work-item count return MIX_ERR_UNSUPPORTED
+    from validation.  The device addresses are fake but aligned; nothing is
+    launched, on a GPU machine or not."""
+    L = mix.lib
+    X, C, S, R = 0x100000, 0x200000, 0x300000, 0x400000
+    BF, F32 = mix.MIX_DT_BF16, mix.MIX_DT_F32
+    UN = mix.MIX_ERR_UNSUPPORTED
+    # 32-element blocks: rows * k/32 reaches 2^32 - 1 at k = 64 from rows = 2^31
+    assert L.mix_quantize(X, BF, 2 ** 31, 64, 64, 2, -8, 1, C, S, None) == UN
+    assert L.mx_quantize(X, BF, 2 ** 31, 64, 64, 1, 1, 0, C, S, None) == UN
+    # 16-byte vectors of x: bf16 k = 64 is 8 per row, fp32 16 per row
+    assert L.mix_auto_ebias(X, BF, 2 ** 29, 64, 64, R, None) == UN
+    assert L.mix_auto_ebias(X, F32, 2 ** 28, 64, 64, R, None) == UN
+    assert L.mix_quantize_auto(X, BF, 2 ** 29, 64, 64, 2, 1, C, S, R, None) == UN
+    assert L.nvfp4_quantize(X, BF, 2 ** 29, 64, 64, C, S, R, None) == UN
+    # 8-element groups
+    assert L.mix_underflow_count(X, BF, 2 ** 29, 64, 64, C, mix.MIX_UF_MIX, R, None) == UN
+    # just below each limit the size check passes; a GPU-less machine then fails at the launch
+    if not mix_has_gpu():
+        assert L.mix_underflow_count(X, BF, 2 ** 29 - 1, 64, 64, C, mix.MIX_UF_MIX, R, None) == mix.MIX_ERR_CUDA
+        assert L.mix_quantize(X, BF, 2 ** 31 - 1, 64, 64, 2, -8, 1, C, S, None) == mix.MIX_ERR_CUDA
+
+
+def mix_has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return True      # when in doubt, skip the calls that would launch
