@@ -138,6 +138,14 @@ def _ptr(t) -> int:
     return t.data_ptr()
 
 
+def _rows_of(x, name: str = "x"):
+    """(rows, cols) of a 2-D tensor whose elements run contiguously along a row."""
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError(f"{name} must be 2-D with unit stride along its rows (got shape {tuple(x.shape)}, "
+                         f"strides {tuple(x.stride())})")
+    return x.shape
+
+
 def _dtype(t) -> int:
     if t.dtype == torch.float32:
         return MIX_DT_F32
@@ -272,8 +280,7 @@ def mix_version() -> int:
 def quantize_mix(x: torch.Tensor, mix_type: int = MIX_T2_4P5, ebias: int = -8, flags: int = MIX_ASYM_ZERO,
                  stream=None):
     """x [rows, k] (row stride x.stride(0)) -> (codes uint8 [rows, k/2], shared [rows, k/32])."""
-    rows, k = x.shape
-    assert x.stride(1) == 1
+    rows, k = _rows_of(x)
     codes = torch.empty((rows, k // 2), dtype=torch.uint8, device=x.device)
     shared = torch.empty((rows, k // 32), dtype=torch.uint8 if mix_type == MIX_T1_4P25 else torch.int16,
                          device=x.device)
@@ -283,8 +290,7 @@ def quantize_mix(x: torch.Tensor, mix_type: int = MIX_T2_4P5, ebias: int = -8, f
 
 def quantize_mix_auto(x: torch.Tensor, mix_type: int = MIX_T2_4P5, flags: int = MIX_ASYM_ZERO, stream=None):
     """Two-pass MiX quantiser -> (codes, shared, ebias int32 [1] on the device)."""
-    rows, k = x.shape
-    assert x.stride(1) == 1
+    rows, k = _rows_of(x)
     codes = torch.empty((rows, k // 2), dtype=torch.uint8, device=x.device)
     shared = torch.empty((rows, k // 32), dtype=torch.uint8 if mix_type == MIX_T1_4P25 else torch.int16,
                          device=x.device)
@@ -295,8 +301,7 @@ def quantize_mix_auto(x: torch.Tensor, mix_type: int = MIX_T2_4P5, flags: int = 
 
 def quantize_nvfp4(x: torch.Tensor, stream=None):
     """x [rows, k] -> (codes uint8 [rows, k/2], E4M3 scales uint8 [rows, k/16], tensor scale float32 [1])."""
-    rows, k = x.shape
-    assert x.stride(1) == 1
+    rows, k = _rows_of(x)
     codes = torch.empty((rows, k // 2), dtype=torch.uint8, device=x.device)
     scales = torch.empty((rows, k // 16), dtype=torch.uint8, device=x.device)
     ts = torch.empty((1,), dtype=torch.float32, device=x.device)
@@ -306,7 +311,7 @@ def quantize_nvfp4(x: torch.Tensor, stream=None):
 
 def underflow_count(x: torch.Tensor, codes: torch.Tensor, fmt: int, stream=None) -> torch.Tensor:
     """Device count (int64 [1]) of finite nonzero x whose code is a zero code."""
-    rows, k = x.shape
+    rows, k = _rows_of(x)
     n = torch.empty((1,), dtype=torch.int64, device=x.device)
     mix_underflow_count(x, rows, k, x.stride(0), codes, fmt, n, stream)
     return n
@@ -314,8 +319,7 @@ def underflow_count(x: torch.Tensor, codes: torch.Tensor, fmt: int, stream=None)
 
 def quantize_mx(x: torch.Tensor, axis: int, mx_type: int, flags: int = 0, stream=None):
     """axis=1: x [N, K]; axis=0: x [K, N] -> (codes [N, K/2], scales [N, K/32], or K/16 with MX_BLOCK16)."""
-    rows, cols = x.shape
-    assert x.stride(1) == 1
+    rows, cols = _rows_of(x)
     N, K = (rows, cols) if axis == 1 else (cols, rows)
     codes = torch.empty((N, K // 2), dtype=torch.uint8, device=x.device)
     scales = torch.empty((N, K // (16 if flags & MX_BLOCK16 else 32)), dtype=torch.uint8, device=x.device)

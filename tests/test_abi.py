@@ -244,3 +244,14 @@ def mix_has_gpu():
         return torch.cuda.is_available()
     except Exception:
         return True      # when in doubt, skip the calls that would launch
+
+
+def test_helpers_reject_tensors_without_unit_row_stride(mix):
+    import torch
+    x = torch.zeros((64, 8), dtype=torch.float32).t()          # [8, 64] with stride (1, 8)
+    for call in (lambda: mix.quantize_mix(x), lambda: mix.quantize_mx(x, 1, mix.MX_INT4),
+                 lambda: mix.quantize_nvfp4(x), lambda: mix.quantize_mix_auto(x)):
+        with pytest.raises(ValueError):
+            call()
+    with pytest.raises(ValueError):
+        mix.quantize_mix(torch.zeros(64))                       # not 2-D
