@@ -167,6 +167,12 @@ def matmul_source_sha():
     return h.hexdigest()
 
 
+def _require(ok, what: str) -> None:
+    """A check that holds under python -O too (unlike assert)."""
+    if not ok:
+        raise RuntimeError(what)
+
+
 def roof_seconds(nbytes, flops):
     return max(nbytes / (HBM * 1e9), flops / (MX8_TFLOPS * 1e12) if flops else 0.0)
 
@@ -334,7 +340,7 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
     O = new((HQ, T, D), torch.float32)
     dpv = mix.gemm_desc(T, D, T, pc, ps, T2, -15, vqc, vqs, INT4, c=O, batch=HQ, b_group=HQ // HK,
                         algo=mix.MIX_GEMM_TCGEN05)
-    assert mix.mix_mx_gemm_workspace_bytes(dpv) <= ws_tc[0].numel()
+    _require(mix.mix_mx_gemm_workspace_bytes(dpv) <= ws_tc[0].numel(), "P.V workspace exceeds the shared staging buffer")
     fns[f"bmm_pv_{HQ}x{T}x{D}x{T}"] = tc_call(dpv)
     d2h.append(O)
 
@@ -379,7 +385,7 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
     calls = []
     for name, nbytes, flops, launches, _ in step_table(small):
         calls.append(Call(name, fns.pop(name), nbytes, flops, launches))
-    assert not fns, f"closures without a table entry: {list(fns)}"
+    _require(not fns, f"closures without a table entry: {list(fns)}")
     keep += [P, S, O, kprime, kp_all]
     return calls, h2d, d2h, host, keep
 
@@ -631,7 +637,7 @@ def measure_extensions(torch, mix, stream, iters=10):
         if flops:
             tf = flops / (ms * 1e-3) / 1e12
             out[name].update({"TFLOP/s": round(tf, 1), "frac_mma": round(tf / MX8_TFLOPS, 3)})
-    assert mix.mix_device_error() == 0, "a kernel reported a timed-out wait"
+    _require(mix.mix_device_error() == 0, "a kernel reported a timed-out wait")
     out.update(measure_decode_attention(torch, mix, stream, iters))
     out["dead_zone"] = dead_zone_table(torch, mix, dev)
     return out
@@ -741,7 +747,7 @@ def main():
     for _ in range(max(3, args.warmup)):
         step()
     barrier()
-    assert mix.mix_device_error() == 0, "a kernel reported a timed-out wait"
+    _require(mix.mix_device_error() == 0, "a kernel reported a timed-out wait")
 
     # One step captured as a CUDA graph: the ~30 launches replay without host
     # gaps (every library call is asynchronous and allocation-free).
@@ -770,7 +776,7 @@ def main():
     barrier()
     clk = clocks.stop()
     ms_step = max_over_ranks(torch, dist, t0.elapsed_time(t1), dev) / args.steps
-    assert mix.mix_device_error() == 0, "a kernel reported a timed-out wait"
+    _require(mix.mix_device_error() == 0, "a kernel reported a timed-out wait")
 
     # Per-call durations: a second timed pass, CUDA events on the launching
     # stream around each call.  A short spin kernel before every call keeps
