@@ -13,22 +13,26 @@
 // the grid is a multiple of the SM count.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "mix_common.cuh"
 #include "mix_internal.h"
 
 namespace mixk {
 
+// SM count of the current device, looked up once per device.  Host threads
+// may call this concurrently: each entry is an atomic, and a race only makes
+// two threads store the same value.
 int num_sms() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (!cached[dev]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev] = n > 0 ? n : 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 namespace {
