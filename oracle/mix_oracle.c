@@ -203,6 +203,8 @@ int orc_mix_quantize(const void* x, int dtype, int64_t rows, int64_t k, int64_t 
         ((uint8_t*)shared)[r * nb + b] = (uint8_t)(ec | (m3s[0] << 4));
       } else {
         uint16_t w = (uint16_t)(ec | (m3s[0] << 4) | (m3s[1] << 7) | (m3s[2] << 10) | (m3s[3] << 13));
+        if (g_mutation == 20)   /* planted: sub-blocks packed in reverse order (unpacked the same way) */
+          w = (uint16_t)(ec | (m3s[3] << 4) | (m3s[2] << 7) | (m3s[1] << 10) | (m3s[0] << 13));
         ((uint16_t*)shared)[r * nb + b] = w;
       }
     }
@@ -219,7 +221,7 @@ static void mix_shared_fields(const void* shared, int type, int64_t idx, int* ec
   } else {
     uint16_t s = ((const uint16_t*)shared)[idx];
     *ec = s & 0xF;
-    for (int k = 0; k < 4; ++k) m3s[k] = (s >> (4 + 3 * k)) & 7;
+    for (int k = 0; k < 4; ++k) m3s[k] = (s >> (4 + 3 * (g_mutation == 20 ? 3 - k : k))) & 7;
   }
 }
 

@@ -239,6 +239,32 @@ def pin_exhaustive_sweep(orc):
                     assert int(nib[r, 0]) == 0                 # the maximum: de = 0
 
 
+def pin_t2_shared_layout(orc):
+    """The Type 2 shared half-word read by hand against the format's bit
+    positions (Method section, MiX-4.5b bullet, for the fields; their order is
+    the format's reading): Emax - ebias in bits 3..0, then the mshared of
+    sub-blocks 0..3 in bits 6..4, 9..7, 12..10, 15..13."""
+    ebias, ec = -8, 9
+    m3 = [5, 2, 7, 1]
+    word = ec | (m3[0] << 4) | (m3[1] << 7) | (m3[2] << 10) | (m3[3] << 13)
+    codes = np.full((1, 16), 0x77, dtype=np.uint8)
+    for k in range(4):
+        codes[0, 4 * k] = 0x70                       # element 8k: de = 0, element 8k + 1: zero
+    sh = np.array([[word]], dtype=np.uint16)
+    v = orc.mix_dequantize(codes, sh, orc.T2, ebias)[0]
+    for k in range(4):
+        assert v[8 * k] == (1.0 + m3[k] / 8.0) * 2.0 ** (ec + ebias)
+    # and the quantiser writes that layout: each sub-block's maximum is its own
+    # (1.m3) 2^Emax, so the word comes back bit for bit
+    x = np.zeros((1, 32), dtype=np.float32)
+    for k in range(4):
+        x[0, 8 * k] = (1.0 + m3[k] / 8.0) * 2.0 ** (ec + ebias)   # all in the binade of 2^(ec + ebias)
+    c, s = orc.mix_quantize(x, orc.T2, ebias, 1)
+    assert int(s[0, 0]) == word
+    for k in range(4):
+        assert c[0, 4 * k] == 0x70                  # de = 0 at element 8k, zero at 8k + 1
+
+
 def pin_asymmetric_zero(orc):
     """The recycled -0 code gives positive values one more binade (accelerator
     bullet of the Method section)."""
@@ -812,7 +838,7 @@ ALL_PINS = [pin_bit_accounting, pin_dequant_special_values, pin_refinement_brute
             pin_mx_axis_consistency, pin_gemm_eq6_exact, pin_gemm_against_dequant_matmul,
             pin_gemm_reduces_to_mx_dot, pin_gemm_batch_gqa_indexing, pin_ksmooth,
             pin_mx_tight_rule, pin_auto_ebias, pin_mx_g16, pin_gemm_g16, pin_nvfp4, pin_underflow_count,
-            pin_decode_attention]
+            pin_decode_attention, pin_t2_shared_layout]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -834,15 +860,17 @@ def test_pin(orc, pin):
 # sub-block by sub-block 0's mantissa, 16 the underflow count also counts
 # elements that were zero before quantisation, 17 the matmul drops the
 # recycled -0 as if it coded zero, 18 element nibbles are packed high nibble
-# first, 19 the MXINT4 element step is 2^(X-1) instead of 2^(X-2).
+# first, 19 the MXINT4 element step is 2^(X-1) instead of 2^(X-2), 20 the
+# Type 2 sub-block mantissas are packed and unpacked in reverse order.
 FAST_PINS = [pin_dequant_special_values, pin_round_trip, pin_asymmetric_zero,
              pin_e2m1_and_int4_brute_force, pin_mx_scale_rule, pin_gemm_eq6_exact,
              pin_gemm_against_dequant_matmul, pin_ksmooth, pin_nonfinite_and_zero_blocks,
              pin_mx_tight_rule, pin_auto_ebias, pin_gemm_g16, pin_nvfp4, pin_underflow_count,
+             pin_t2_shared_layout,
              lambda o: pin_refinement_brute_force(o, n_blocks=40)]
 
 
-@pytest.mark.parametrize("mutation", list(range(1, 20)))
+@pytest.mark.parametrize("mutation", list(range(1, 21)))
 def test_planted_mistakes_are_caught(orc, mutation):
     failed = []
     try:
