@@ -478,6 +478,20 @@ def oracle_unit_costs(budget_s=10.0):
     return cost, sample
 
 
+def host_cpu():
+    """The host's CPU model and logical core count, for the CPU-baseline record."""
+    model = None
+    try:
+        with open("/proc/cpuinfo", encoding="utf-8") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return {"cpu_model": model, "host_logical_cpus": os.cpu_count()}
+
+
 def cpu_step_seconds(cost, small=False):
     return sum(cost[c[0]] * c[1] for *_, c in step_table(small))
 
@@ -501,7 +515,8 @@ def run_reference(args, rank, world):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64 / int64 (scalar C oracle)",
            "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "sample": sample},
-           "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+           "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
+                            **host_cpu()},
            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
@@ -899,7 +914,7 @@ def main():
         cost, sample = oracle_unit_costs(10.0)
         sec = cpu_step_seconds(cost, args.small)
         cpu = {"value": 100.0 * roof_s / sec, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample,
-               "seconds_per_step": round(sec, 2)}
+               "seconds_per_step": round(sec, 2), **host_cpu()}
     out = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None,
