@@ -50,13 +50,53 @@ def load_peaks():
 
 
 PEAKS = load_peaks()
-# kind::mxf8f6f4 (FP8-rate) dense peak: the measured bf16 peak x the nominal 2x ratio
-MX8_TFLOPS = PEAKS["bf16_tflops_sustained"] * 2.0
+# kind::mxf8f6f4 (FP8-rate) dense peak: the measured bf16 peak x the nominal
+# 2x fp8/bf16 ratio.  A call timed on its own (a fraction of a millisecond,
+# at full clock) is graded against the burst figure; the sustained one was
+# measured seconds into a loop at the power cap's lower clock, and applies
+# only to a run whose own clock record shows that cap pulling the clock down.
 MX8_TFLOPS_BURST = PEAKS["bf16_tflops"] * 2.0
+MX8_TFLOPS_SUSTAINED = PEAKS["bf16_tflops_sustained"] * 2.0
+MX8_TFLOPS = MX8_TFLOPS_BURST
 HBM = PEAKS["hbm_gbs"]
 
 
+def step_mma_peak(clk):
+    """The MMA peak that matches the step's timed run: burst unless the SM
+    clock sampled during it had a median below 90 % of its maximum (the
+    power cap at work), then sustained."""
+    sm, mx = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    if sm and mx and sm < 0.9 * mx:
+        return MX8_TFLOPS_SUSTAINED, f"sustained (median SM clock {sm:.0f} of {mx:.0f} MHz)"
+    return MX8_TFLOPS_BURST, (f"burst (median SM clock {sm:.0f} of {mx:.0f} MHz)" if sm and mx
+                              else "burst (no clock record)")
+
+
 EXT_INPUTS = {}   # step tensors the extension measurements reuse
+CLAMP = {}        # what the clamped-block report reads (filled by build_workload)
+
+
+def clamp_report(torch, mix, ws):
+    """Clamped MiX blocks of every MiX quantisation in the step, at its ebias:
+    [blocks clamped down (exponent above ebias + 15), blocks clamped up
+    (nonzero, below ebias), blocks].  The matmul epilogues are counted on
+    their fp32 C, made once here by the same matmul with an fp32 output
+    (outside the timed region)."""
+    out = {}
+    for name, x, eb in CLAMP["inputs"]:
+        n = mix.clamp_count(x, eb)
+        out[name] = [int(v) for v in n.tolist()] + [x.shape[0] * (x.shape[1] // 32)]
+    big = max(m * n for _, _, m, n, _ in CLAMP["epi"])
+    cbuf = torch.empty(big, dtype=torch.float32, device=ws.device)
+    for name, make, m, n, eb in CLAMP["epi"]:
+        c = cbuf[:m * n].view(m, n)
+        d = make(c)
+        mix.mix_mx_gemm(d, ws)
+        cnt = mix.clamp_count(c, eb)
+        out[name + ":epilogue"] = [int(v) for v in cnt.tolist()] + [m * (n // 32)]
+    del cbuf
+    torch.cuda.synchronize()
+    return out
 
 
 class Call:
@@ -65,9 +105,9 @@ class Call:
     def __init__(self, name, fn, nbytes, flops=0.0, launches=1, kind="hbm"):
         self.name, self.fn, self.bytes, self.flops, self.launches, self.kind = name, fn, nbytes, flops, launches, kind
 
-    def roof_s(self):
+    def roof_s(self, mma_tflops=None):
         t_mem = self.bytes / (HBM * 1e9)
-        t_mma = self.flops / (MX8_TFLOPS * 1e12) if self.flops else 0.0
+        t_mma = self.flops / ((mma_tflops or MX8_TFLOPS) * 1e12) if self.flops else 0.0
         return max(t_mem, t_mma)
 
 
@@ -173,8 +213,8 @@ def _require(ok, what: str) -> None:
         raise RuntimeError(what)
 
 
-def roof_seconds(nbytes, flops):
-    return max(nbytes / (HBM * 1e9), flops / (MX8_TFLOPS * 1e12) if flops else 0.0)
+def roof_seconds(nbytes, flops, mma_tflops=None):
+    return max(nbytes / (HBM * 1e9), flops / ((mma_tflops or MX8_TFLOPS) * 1e12) if flops else 0.0)
 
 
 # ---------------------------------------------------------------------------
@@ -214,6 +254,10 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
     g = dims(small)
     M, DM, DF, QKV, MV, T, TC, HQ, HK, D = (g[k] for k in ("M", "DM", "DF", "QKV", "MV", "T", "TC", "HQ", "HK", "D"))
     fns, h2d, d2h, host, keep = {}, [], [], {}, []
+    # MiX quantiser inputs (tensor, ebias) and the matmuls with a fused MiX
+    # epilogue (a descriptor maker taking an fp32 C, its M x N, ebias), for
+    # the clamped-block report
+    CLAMP["inputs"], CLAMP["epi"] = [], []
 
     def dev_bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(bf16)
@@ -281,6 +325,9 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
         d = mix.gemm_desc(M, n, k, ac_, as_, T2, -8, bc, bs, FP4, c=None, epi=mix.MIX_EPI_MIX_T2, out_codes=oc,
                           out_shared=os_, algo=mix.MIX_GEMM_TCGEN05)
         fns[f"gemm_{name}_{M}x{k}x{n}"] = tc_call(d)
+        CLAMP["epi"].append((f"gemm_{name}_{M}x{k}x{n}", (lambda c, k=k, n=n, ac_=ac_, as_=as_, bc=bc, bs=bs:
+                             mix.gemm_desc(M, n, k, ac_, as_, T2, -8, bc, bs, FP4, c=c, algo=mix.MIX_GEMM_TCGEN05)),
+                             M, n, -8))
     d2h.append(outs["down"])
 
     # ----- 3. ViT MLP: fc1's fused MiX-4.25b output is fc2's input
@@ -294,6 +341,12 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
                        out_shared=ys, algo=mix.MIX_GEMM_TCGEN05)
     fns[f"gemm_vit_fc1_{MV}x1280x5120"] = tc_call(d1)
     fns[f"gemm_vit_fc2_{MV}x5120x1280"] = tc_call(d2)
+    CLAMP["epi"].append((f"gemm_vit_fc1_{MV}x1280x5120", lambda c: mix.gemm_desc(
+        MV, 5120, 1280, vc, vs, T1, -8, wv1[0], wv1[1], INT4, c=c, algo=mix.MIX_GEMM_TCGEN05), MV, 5120, -8))
+    CLAMP["epi"].append((f"gemm_vit_fc2_{MV}x5120x1280", lambda c: mix.gemm_desc(
+        MV, 1280, 5120, hc, hs, T1, -8, wv2[0], wv2[1], INT4, c=c, algo=mix.MIX_GEMM_TCGEN05), MV, 1280, -8))
+    CLAMP["inputs"] += [(f"mix_quantize_t1_{M}x{DM}", x, -8), (f"mix_quantize_t2_{M}x{DF}", xd, -8),
+                        (f"mix_quantize_t1_{MV}x1280", xv, -8)]
     d2h.append(yc)
 
     # ----- 4. attention prefill (28 query / 4 KV heads, d 128)
@@ -321,6 +374,7 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
                         a_batch_stride=D, b_ld=HK * D, b_batch_stride=D, algo=mix.MIX_GEMM_TCGEN05)
     fns[f"bmm_qk_{HQ}x{T}x{T}x{D}"] = tc_call(dqk)
     ws_tc[0] = new(max(16, max(mix.mix_mx_gemm_workspace_bytes(d) for d in tc_descs)), torch.uint8)
+    CLAMP["ws"] = ws_tc[0]
     # P: a fixed causal softmax of S, made once here (softmax is not on the path)
     for f in (f"ksmooth_compute_{T}x{HK}x{D}", f"mix_quantize_t2_q_{T * HQ}x{D}",
               f"mx_quantize_int4_kprime_{T * HK}x{D}", f"bmm_qk_{HQ}x{T}x{T}x{D}"):
@@ -330,6 +384,8 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
     for h in range(HQ):
         P[h] = torch.softmax((S[h] / math.sqrt(D)).masked_fill(~causal, float("-inf")), dim=-1).to(bf16)
     del causal
+    CLAMP["inputs"] += [(f"mix_quantize_t2_q_{T * HQ}x{D}", q_d.view(T * HQ, D), -8),
+                        (f"mix_quantize_t2_p_{HQ * T}x{T}", P.view(HQ * T, T), -15)]
     pc, ps = new((HQ * T, T // 2), torch.uint8), new((HQ * T, T // 32), torch.int16)
     fns[f"mix_quantize_t2_p_{HQ * T}x{T}"] = lambda: mix.mix_quantize(P, HQ * T, T, T, T2, -15, 1, pc, ps)
     # V [T, HK*D] quantised down its columns in one call: column h*D + d is
@@ -372,6 +428,7 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
     p_dec = new((HQ, TC), bf16)
     p_dec.copy_(torch.softmax(torch.randn((HQ, TC), device=dev, generator=torch.Generator(dev).manual_seed(seed))
                               * 3.0, dim=-1))
+    CLAMP["inputs"] += [(f"mix_quantize_t2_qdec_{HQ}x{D}", q_new, -8), (f"mix_quantize_t2_pdec_{HQ}x{TC}", p_dec, -15)]
     pdc, pds = new((HQ, TC // 2), torch.uint8), new((HQ, TC // 32), torch.int16)
     fns[f"mix_quantize_t2_pdec_{HQ}x{TC}"] = lambda: mix.mix_quantize(p_dec, HQ, TC, TC, T2, -15, 1, pdc, pds)
     o_dec = new((HK, 7, D), torch.float32)
@@ -763,6 +820,7 @@ def main():
         step()
     barrier()
     _require(mix.mix_device_error() == 0, "a kernel reported a timed-out wait")
+    clamped = clamp_report(torch, mix, CLAMP["ws"])
 
     # One step captured as a CUDA graph: the ~30 launches replay without host
     # gaps (every library call is asynchronous and allocation-free).
@@ -810,7 +868,8 @@ def main():
         per_call += np.array([a.elapsed_time(b) for a, b in ev])
     per_call /= args.steps
 
-    roof_s = sum(c.roof_s() for c in calls)
+    step_peak, step_peak_source = step_mma_peak(clk)
+    roof_s = sum(c.roof_s(step_peak) for c in calls)
     value = job_value(roof_s, world, ms_step)
     ext = None if args.no_ext else measure_extensions(torch, mix, stream)
 
@@ -902,13 +961,13 @@ def main():
     fp = os.path.join(ROOT, "profiles", "fp8_peak.json")
     if os.path.exists(fp):
         fj = json.load(open(fp))
-        fp8 = {"fp8_tflops_sustained_direct": fj["fp8_tflops_sustained"],
-               "frac_of_direct": round(ach / fj["fp8_tflops_sustained"], 4), "how": fj["command"]}
+        fp8 = {"fp8_tflops_burst_direct": fj["fp8_tflops_burst"],
+               "frac_of_direct": round(ach / fj["fp8_tflops_burst"], 4), "how": fj["command"]}
     roofline = {"bound": "tensor", "kernel": dc.name, "achieved": round(ach, 1), "peak": round(MX8_TFLOPS, 1),
                 "unit": "TFLOP/s", "frac": round(ach / MX8_TFLOPS, 4), "traffic": traffic, "fp8_measured": fp8,
                 "algorithmic_bytes": dc.bytes, "algorithmic_flops": dc.flops,
-                "peak_source": f"2 x measured bf16 sustained ({PEAKS['source']}); "
-                               f"burst {MX8_TFLOPS_BURST:.0f} TFLOP/s"}
+                "peak_source": f"2 x measured bf16 burst ({PEAKS['source']}; the call is timed on its own, "
+                               f"at full clock); sustained would be {MX8_TFLOPS_SUSTAINED:.0f} TFLOP/s"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cost, sample = oracle_unit_costs(10.0)
@@ -923,9 +982,11 @@ def main():
            "config": {"workload": WORKLOAD + (f"_div{8 if args.small is True else args.small}" if args.small else ""),
                       "l2": "inputs larger than L2 (several GB per step; each tensor is evicted before reuse)",
                       "parallelism": f"replicas x{world}", "roofline_ms_per_step": round(roof_s * 1e3, 4),
-                      "hbm_peak_gbs": HBM, "mma_peak_tflops": round(MX8_TFLOPS, 1), "timing": timing_mode,
+                      "hbm_peak_gbs": HBM, "mma_peak_tflops_per_call": round(MX8_TFLOPS, 1),
+                      "mma_peak_tflops_step": round(step_peak, 1), "mma_peak_step_source": step_peak_source,
+                      "timing": timing_mode,
                       "per_call_timing": percall_mode},
-           "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+           "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clamped_blocks": clamped,
            "gpu_launches": int(sum(c.launches for c in calls) * args.steps), "clocks": clk, "parts": parts,
            "extensions": ext}
     if rank == 0:

@@ -180,6 +180,20 @@ MIX_API mix_status_t mx_quantize(const void* x, mix_dtype_t dtype, int64_t rows,
 MIX_API mix_status_t nvfp4_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,
                                     uint8_t* codes, uint8_t* scales, float* tensor_scale, mix_stream_t stream);
 
+/* Clamped-block count of the MiX quantiser (Method section, MiX-4.25b
+ * bullet: Emax has 4 bits, so with Emax = field + ebias a block exponent
+ * outside [ebias, ebias + 15] is clamped).  For every 32-element block of x
+ * (rows x k, row stride ld elements, bf16 or fp32): f = the exponent that
+ * steps 1-2 of Algorithm 1 give the block maximum, its 3-bit mantissa
+ * rounding and carry included.  counts[0] = blocks with f > ebias + 15 (the
+ * elements saturate; +-Inf blocks count here); counts[1] = blocks with a
+ * nonzero maximum and f < ebias (small elements flush to zero).  NaN counts
+ * as zero.  counts: two uint64 in device memory, 8-byte aligned, overwritten
+ * (stream-ordered).  x 16-byte aligned, ld * element size a multiple of 16,
+ * k % 32 == 0, ebias in [-100, 100]. */
+MIX_API mix_status_t mix_clamp_count(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,
+                                     int ebias, unsigned long long* counts, mix_stream_t stream);
+
 /* Dead-zone count (the key-underflow comparison of the Key results section,
  * made synthetic): how many finite nonzero elements of x have a zero code in
  * `codes` -- 0x7 for MiX (the recycled -0 code 0xF is not zero), 0 for MXINT4,
@@ -285,7 +299,8 @@ MIX_API mix_status_t mix_mx_gemm(const mix_gemm_desc_t* desc, void* workspace, s
 /* ---------------------------------------------------------------------- */
 /* k: tokens x heads x head_dim keys (bf16 or fp32), token stride ld >= heads *
  * head_dim elements.  KSMOOTH_COMPUTE: mean[h][d] = mean over the tokens,
- * summed in fp64 in a fixed order and rounded once to fp32 (the prefill
+ * summed as fp32 pairs (about 48 bits, Knuth's two-sum) in a fixed order,
+ * divided by the token count in fp64 and rounded once to fp32 (the prefill
  * mean).  KSMOOTH_APPLY_FROZEN: mean is an input (frozen at prefill; decode
  * does not re-read the cache).  Both modes write k_out = fp32(k) - mean (one
  * fp32 subtraction), tokens x heads x head_dim dense, when k_out != NULL.
@@ -313,6 +328,8 @@ MIX_API mix_status_t ksmooth_kv(const void* k, mix_dtype_t dtype, int64_t tokens
  *    MIX_ERR_WORKSPACE before any launch.
  *  - The first call on a device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
+ *    The address is kept for the life of that device's CUDA context: a call
+ *    made under a new context (after cudaDeviceReset, say) looks it up again.
  *  - All calls share the array.  Calls ordered on one stream are safe; calls
  *    whose kernels overlap on the GPU (other streams, other threads) race.
  *    Nothing has to be cleared between calls: each call writes every partial
@@ -356,6 +373,11 @@ typedef struct {
   uint8_t* p_codes;      /* optional P planes [q_heads][v_ld/2] (NULL: not kept); only
                             the 32-token blocks that hold a token are written    */
   void* p_shared;        /* [q_heads][v_ld/32] uint16 MiX-4.5b shared fields     */
+  float* p_values;       /* optional [q_heads][v_ld] fp32 (NULL: not kept): the
+                            probabilities the kernel quantised into p_codes, for
+                            checking the quantiser on the kernel's own P; only the
+                            32-token blocks that hold a token are written, with 0
+                            past the last token                                   */
 } mix_decode_attn_desc_t;
 
 /* Device workspace bytes (S, the per-chunk statistics and partial outputs). */

@@ -57,11 +57,12 @@ def lib():
         L.orc_nvfp4_quantize.argtypes = [P, I, I64, I64, I64, P, P, P]
         L.orc_nvfp4_dequantize.argtypes = [P, P, ctypes.c_float, I64, I64, P]
         L.orc_underflow_count.argtypes = [P, I, I64, I64, I64, P, I]
+        L.orc_mix_clamp_count.argtypes = [P, I, I64, I64, I64, I, P]
         L.orc_underflow_count.restype = I64
         for f in ("orc_mix_quantize", "orc_mix_dequantize", "orc_mx_quantize",
                   "orc_mx_dequantize", "orc_gemm", "orc_ksmooth_mean", "orc_ksmooth_apply",
                   "orc_mix_auto_ebias", "orc_mx_quantize_blk", "orc_mx_dequantize_blk", "orc_gemm_blk",
-                  "orc_nvfp4_quantize", "orc_nvfp4_dequantize"):
+                  "orc_nvfp4_quantize", "orc_nvfp4_dequantize", "orc_mix_clamp_count"):
             getattr(L, f).restype = ctypes.c_int
         L.orc_set_mutation.restype = None
         _lib = L
@@ -109,6 +110,17 @@ def mix_auto_ebias(x: np.ndarray) -> int:
     if e == -1000:
         raise ValueError("k must be a multiple of 32")
     return e
+
+
+def mix_clamp_count(x: np.ndarray, ebias: int = -8):
+    """(blocks clamped down, blocks clamped up) of the MiX quantiser of x
+    [rows, k] at this ebias: the block exponent of Algorithm 1's steps 1-2
+    above ebias + 15, or (nonzero blocks) below ebias."""
+    x = np.ascontiguousarray(x)
+    rows, k = x.shape
+    out = np.zeros(2, dtype=np.int64)
+    _check(lib().orc_mix_clamp_count(_ptr(x), _dtype_of(x), rows, k, k, int(ebias), _ptr(out)))
+    return int(out[0]), int(out[1])
 
 
 def mix_dequantize(codes: np.ndarray, shared: np.ndarray, mix_type: int, ebias: int = -8):

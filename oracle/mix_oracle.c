@@ -247,6 +247,34 @@ int orc_mix_dequantize(const uint8_t* codes, const void* shared, int64_t rows, i
   return 0;
 }
 
+/* Clamped blocks of the MiX quantiser at a given ebias (the page gives Emax
+ * only its 4-bit width, so Emax = field + ebias and an exponent outside
+ * [ebias, ebias + 15] is clamped).  Per 32-element block: f = the exponent
+ * steps 1-2 of Algorithm 1 give the block maximum (mshared rounding and its
+ * carry included).  counts[0]: blocks with f > ebias + 15 (+-Inf included);
+ * counts[1]: blocks with a nonzero maximum and f < ebias.  NaN counts as 0. */
+int orc_mix_clamp_count(const void* x, int dtype, int64_t rows, int64_t k, int64_t ld, int ebias,
+                        int64_t* counts) {
+  if (k % 32 != 0) return 1;
+  counts[0] = counts[1] = 0;
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t b = 0; b < k / 32; ++b) {
+      double amax = 0.0;
+      for (int i = 0; i < 32; ++i) {
+        double a = mag(load_elem(x, dtype, r * ld + b * 32 + i));
+        if (a > amax) amax = a;
+      }
+      if (amax == 0.0) continue;
+      int f, m3;
+      max_exp_mant(amax, &f, &m3);
+      if (g_mutation == 21) { f = floor_log2(amax); }   /* planted: carry ignored */
+      if (f > ebias + 15) counts[0] += 1;
+      else if (f < ebias) counts[1] += 1;
+    }
+  }
+  return 0;
+}
+
 /* Automatic ebias (a two-pass mode; the page fixes only the 4-bit width of
  * Emax): the largest block exponent f over the tensor -- floor(log2) of the
  * block maximum after its mantissa is rounded to three bits, carry included,

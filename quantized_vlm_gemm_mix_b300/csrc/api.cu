@@ -175,6 +175,21 @@ mix_status_t mix_underflow_count(const void* x, mix_dtype_t dtype, int64_t rows,
                                           reinterpret_cast<cudaStream_t>(stream)));
 }
 
+mix_status_t mix_clamp_count(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld, int ebias,
+                             unsigned long long* counts, mix_stream_t stream) {
+  if (!valid_dtype(dtype) || rows < 0 || k < 0 || ld < k || counts == nullptr || ebias < -100 || ebias > 100)
+    return MIX_ERR_INVALID_ARG;
+  if (k % 32 != 0) return MIX_ERR_SHAPE;
+  if (!aligned(counts, 8)) return MIX_ERR_ALIGN;
+  if (rows > 0 && k > 0) {
+    if (x == nullptr) return MIX_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || (ld * esize(dtype)) % 16 != 0) return MIX_ERR_ALIGN;
+    if (!items_fit(rows, k / 32)) return MIX_ERR_UNSUPPORTED;
+  }
+  return from_cuda(launch_clamp_count(x, dtype == MIX_DT_BF16, rows, k, ld, ebias, counts,
+                                      reinterpret_cast<cudaStream_t>(stream)));
+}
+
 static mix_status_t validate_attn(const mix_decode_attn_desc_t* d) {
   if (d == nullptr) return MIX_ERR_INVALID_ARG;
   if (d->tokens < 1 || d->q_heads < 1 || d->kv_heads < 1 || d->q_heads % d->kv_heads != 0 ||
@@ -187,7 +202,8 @@ static mix_status_t validate_attn(const mix_decode_attn_desc_t* d) {
       ((d->p_codes == nullptr) != (d->p_shared == nullptr)))
     return MIX_ERR_INVALID_ARG;
   if (!aligned(d->k_codes, 16) || !aligned(d->k_scales, 4) || !aligned(d->v_codes, 16) ||
-      (d->p_codes != nullptr && (!aligned(d->p_codes, 16) || !aligned(d->p_shared, 2))))
+      (d->p_codes != nullptr && (!aligned(d->p_codes, 16) || !aligned(d->p_shared, 2))) ||
+      (d->p_values != nullptr && !aligned(d->p_values, 4)))
     return MIX_ERR_ALIGN;
   if (d->tokens >= (int64_t)1 << 40) return MIX_ERR_SHAPE;
   return MIX_OK;

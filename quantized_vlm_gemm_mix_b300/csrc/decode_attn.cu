@@ -61,6 +61,7 @@ struct AttnArgs {
   float* out;      // [HQ][D]
   uint8_t* p_codes;    // optional [HQ][v_ld / 2]
   uint16_t* p_shared;  // optional [HQ][v_ld / 32]
+  float* p_values;     // optional [HQ][v_ld]: the P that was quantised
 };
 
 __device__ __forceinline__ uint32_t load_bits(const void* p, bool bf16, int64_t i) {
@@ -310,6 +311,7 @@ __global__ void __launch_bounds__(kD * kMaxG) attn_pv_kernel(AttnArgs a) {
     if (t < a.T)
       p = __fdiv_rn(expf(__fmul_rn(a.S[(int64_t)(g * a.G + hh) * a.Tpad + t], a.sm_scale) - gm[hh]), gl[hh]);
     pv[hh][j] = p;
+    if (a.p_values != nullptr && j < 32 * nblk) a.p_values[(int64_t)(g * a.G + hh) * a.v_ld + t] = p;
   }
   __syncthreads();
   if (warp < a.G) {  // warp hh: its 8 blocks, four lanes per block
@@ -388,6 +390,7 @@ cudaError_t launch_decode_attention(const mix_decode_attn_desc_t& d, void* ws, c
   p += align256((size_t)CB * d.q_heads * kD * 4);
   a.tickets = reinterpret_cast<unsigned*>(p);
   a.out = d.out; a.p_codes = d.p_codes; a.p_shared = static_cast<uint16_t*>(d.p_shared);
+  a.p_values = d.p_values;
   attn_qk_kernel<<<dim3((unsigned)CA, (unsigned)d.kv_heads), kChunkA * a.G, 0, st>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

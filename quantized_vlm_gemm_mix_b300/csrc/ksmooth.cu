@@ -210,6 +210,8 @@ cudaError_t launch_ksmooth(const void* k, bool bf16, int64_t tokens, int heads, 
 // in a fixed array compiled into the library instead of a caller workspace.
 // Every GPU that loads the library keeps this array until the process exits.
 // ---------------------------------------------------------------------------
+#include <cuda.h>
+
 #include <mutex>
 
 namespace mixk {
@@ -219,23 +221,62 @@ constexpr size_t kNoAllocScratchBytes = (size_t)2 << 20;  // 2 MiB
 static __device__ __align__(256) float2 g_ksmooth_scratch[kNoAllocScratchBytes / sizeof(float2)];
 
 std::mutex g_scratch_mu;
-void* g_scratch_addr[64] = {nullptr};
+struct ScratchEntry {
+  unsigned long long ctx_id;  // the context the address belongs to
+  void* addr;
+};
+ScratchEntry g_scratch_addr[64] = {};
 
-// Device address of g_ksmooth_scratch on the current device, looked up once
-// per device (in host code the symbol is only a host-side stand-in).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current CUDA context (0 if it cannot be
+// read).  A context created after cudaDeviceReset gets a new id.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(a);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(b);
+    looked_up = true;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_cur == nullptr || get_id == nullptr || get_cur(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_ksmooth_scratch on the current device (in host code
+// the symbol is only a host-side stand-in).  Looked up once per device and
+// context: an address cached under a context that has since been destroyed
+// (cudaDeviceReset) is never handed out; with no readable context id the
+// address is looked up on every call.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const unsigned long long id = current_context_id();  // 0 before the context exists
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchEntry& ent = g_scratch_addr[dev];
+  if (ent.addr == nullptr || ent.ctx_id != id || id == 0) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_ksmooth_scratch);
+    e = cudaGetSymbolAddress(&p, g_ksmooth_scratch);  // creates the primary context if needed
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+    ent.addr = p;
+    ent.ctx_id = current_context_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = ent.addr;
   return cudaSuccess;
 }
 

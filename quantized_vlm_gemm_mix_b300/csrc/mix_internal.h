@@ -28,6 +28,9 @@ cudaError_t launch_nvfp4_quantize(const void* x, bool bf16, int64_t rows, int64_
                                   uint8_t* scales, float* tensor_scale, cudaStream_t st);
 cudaError_t launch_underflow_count(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, const uint8_t* codes,
                                    int fmt, unsigned long long* count, cudaStream_t st);
+// Clamped-block count of the MiX quantiser at ebias (counts[0] high, [1] low).
+cudaError_t launch_clamp_count(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, int ebias,
+                               unsigned long long* counts, cudaStream_t st);
 // Automatic ebias into one device int (clear, max-reduction, finish).
 cudaError_t launch_auto_ebias(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, int* ebias,
                               cudaStream_t st);

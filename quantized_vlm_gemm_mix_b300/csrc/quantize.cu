@@ -230,6 +230,45 @@ __global__ void __launch_bounds__(kThreads) underflow_count_kernel(const void* _
   if ((threadIdx.x & 31) == 0 && n != 0u) atomicAdd(count, (unsigned long long)n);
 }
 
+// Clamped blocks of the MiX quantiser at `ebias`: one thread per 32-element
+// block, the block exponent f of Algorithm 1's first two steps (mantissa
+// rounding and carry included); counts[0] += [f > ebias + 15] (+-Inf too),
+// counts[1] += [nonzero maximum and f < ebias].  A subnormal maximum is below
+// any allowed ebias (>= -100).  NaN counts as zero.  One atomic per warp.
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) clamp_count_kernel(const void* __restrict__ x, int64_t rows,
+                                                               int64_t nb, int64_t ld, FastDiv fb, int ebias,
+                                                               unsigned long long* __restrict__ counts) {
+  const int64_t total = rows * nb;
+  unsigned hi = 0, lo = 0;
+  for (int64_t g = (int64_t)blockIdx.x * kThreads + threadIdx.x; g < total; g += (int64_t)gridDim.x * kThreads) {
+    const uint32_t row = fdiv((uint32_t)g, fb);
+    const int64_t b = g - (int64_t)row * nb;
+    uint32_t u[32];
+    load32<BF16>(x, (int64_t)row * ld + b * 32, u);
+    uint32_t key = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t a = u[i] & 0x7FFFFFFFu;
+      key = max(key, a <= 0x7F800000u ? a : 0u);
+    }
+    if (key == 0u) continue;
+    int f = 0, m3 = 0;
+    if (!max_exp_mant(key, &f, &m3)) {  // subnormal maximum
+      ++lo;
+      continue;
+    }
+    hi += f > ebias + 15 ? 1u : 0u;
+    lo += f < ebias ? 1u : 0u;
+  }
+  hi = __reduce_add_sync(0xFFFFFFFFu, hi);
+  lo = __reduce_add_sync(0xFFFFFFFFu, lo);
+  if ((threadIdx.x & 31) == 0) {
+    if (hi != 0u) atomicAdd(counts, (unsigned long long)hi);
+    if (lo != 0u) atomicAdd(counts + 1, (unsigned long long)lo);
+  }
+}
+
 // Automatic ebias, pass 1: the largest finite |x| of the tensor, as the
 // integer maximum of the magnitude bits (the order of non-negative floats).
 // Rounding a block maximum to three mantissa bits never lowers a larger one
@@ -599,6 +638,20 @@ cudaError_t launch_nvfp4_quantize(const void* x, bool bf16, int64_t rows, int64_
   const FastDiv f = make_fastdiv((uint32_t)nb);
   if (bf16) nvfp4_quantize_kernel<true><<<(int)gb, kThreads, 0, st>>>(x, rows, nb, ld, f, tensor_scale, codes, scales);
   else nvfp4_quantize_kernel<false><<<(int)gb, kThreads, 0, st>>>(x, rows, nb, ld, f, tensor_scale, codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_clamp_count(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld, int ebias,
+                               unsigned long long* counts, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(counts, 0, 2 * sizeof(unsigned long long), st);
+  if (e != cudaSuccess || rows == 0 || k == 0) return e;
+  const int64_t nb = k / 32;
+  if (rows * nb >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;
+  int64_t gb = (rows * nb + kThreads - 1) / kThreads;
+  if (gb > (int64_t)num_sms() * 8) gb = (int64_t)num_sms() * 8;
+  const FastDiv f = make_fastdiv((uint32_t)nb);
+  if (bf16) clamp_count_kernel<true><<<(int)gb, kThreads, 0, st>>>(x, rows, nb, ld, f, ebias, counts);
+  else clamp_count_kernel<false><<<(int)gb, kThreads, 0, st>>>(x, rows, nb, ld, f, ebias, counts);
   return cudaGetLastError();
 }
 

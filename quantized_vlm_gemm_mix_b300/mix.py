@@ -29,7 +29,7 @@ MIX_GEMM_AUTO, MIX_GEMM_TCGEN05, MIX_GEMM_SHIFTADD, MIX_GEMM_TCGEN05_STAGED, MIX
 KSMOOTH_COMPUTE, KSMOOTH_APPLY_FROZEN = 0, 1
 
 EXPORTS = ["mix_codes_bytes", "mix_shared_bytes", "mx_scales_bytes", "mix_quantize", "mix_auto_ebias",
-           "mix_quantize_auto", "mx_quantize", "nvfp4_quantize", "mix_underflow_count",
+           "mix_quantize_auto", "mx_quantize", "nvfp4_quantize", "mix_underflow_count", "mix_clamp_count",
            "mix_decode_attention_workspace_bytes", "mix_decode_attention",
            "mix_dequantize", "mx_dequantize", "mix_mx_gemm_workspace_bytes", "mix_mx_gemm",
            "ksmooth_workspace_bytes", "ksmooth_kv", "ksmooth_kv_noalloc", "mix_status_str", "mix_device_error",
@@ -72,6 +72,7 @@ class DecodeAttnDesc(ctypes.Structure):
         ("v_codes", ctypes.c_void_p), ("v_scales", ctypes.c_void_p), ("v_ld", ctypes.c_int64),
         ("sm_scale", ctypes.c_float), ("q_ebias", ctypes.c_int), ("p_ebias", ctypes.c_int),
         ("out", ctypes.c_void_p), ("p_codes", ctypes.c_void_p), ("p_shared", ctypes.c_void_p),
+        ("p_values", ctypes.c_void_p),
     ]
 
 
@@ -90,6 +91,7 @@ def _load():
         "mix_decode_attention_workspace_bytes": (S, [P]),
         "mix_decode_attention": (I, [P, P, S, P]),
         "mix_underflow_count": (I, [P, I, I64, I64, I64, P, I, P, P]),
+        "mix_clamp_count": (I, [P, I, I64, I64, I64, I, P, P]),
         "mix_quantize_auto": (I, [P, I, I64, I64, I64, I, U, P, P, P, P]),
         "mx_quantize": (I, [P, I, I64, I64, I64, I, I, U, P, P, P]),
         "mix_dequantize": (I, [P, P, I64, I64, I, I, P, P]),
@@ -194,19 +196,24 @@ def mix_underflow_count(x, rows, k, ld, codes, fmt, count, stream=None) -> None:
            "mix_underflow_count")
 
 
+def mix_clamp_count(x, rows, k, ld, ebias, counts, stream=None) -> None:
+    _check(lib.mix_clamp_count(_ptr(x), _dtype(x), rows, k, ld, ebias, _ptr(counts), _stream(stream)),
+           "mix_clamp_count")
+
+
 def decode_attention_desc(q, k_codes, k_scales, v_codes, v_scales, tokens, sm_scale, out, k_new=None, k_mean=None,
-                          q_ebias=-8, p_ebias=-15, p_codes=None, p_shared=None) -> DecodeAttnDesc:
+                          q_ebias=-8, p_ebias=-15, p_codes=None, p_shared=None, p_values=None) -> DecodeAttnDesc:
     """q [HQ, 128]; K' cache codes [T, HK, 64], scales [T, HK, 4]; V planes [HK, 128, Tv/2], [HK, 128, Tv/32]."""
     d = DecodeAttnDesc()
-    d._keep = [t for t in (q, k_codes, k_scales, v_codes, v_scales, out, k_new, k_mean, p_codes, p_shared)
-               if t is not None]
+    d._keep = [t for t in (q, k_codes, k_scales, v_codes, v_scales, out, k_new, k_mean, p_codes, p_shared,
+                           p_values) if t is not None]
     d.tokens, d.q_heads, d.kv_heads, d.head_dim = tokens, q.shape[0], k_codes.shape[1], q.shape[1]
     d.dtype = _dtype(q)
     d.q, d.k_new, d.k_mean = _ptr(q), _ptr(k_new), _ptr(k_mean)
     d.k_codes, d.k_scales, d.v_codes, d.v_scales = _ptr(k_codes), _ptr(k_scales), _ptr(v_codes), _ptr(v_scales)
     d.v_ld = v_codes.shape[-1] * 2
     d.sm_scale, d.q_ebias, d.p_ebias = sm_scale, q_ebias, p_ebias
-    d.out, d.p_codes, d.p_shared = _ptr(out), _ptr(p_codes), _ptr(p_shared)
+    d.out, d.p_codes, d.p_shared, d.p_values = _ptr(out), _ptr(p_codes), _ptr(p_shared), _ptr(p_values)
     return d
 
 
@@ -314,6 +321,15 @@ def underflow_count(x: torch.Tensor, codes: torch.Tensor, fmt: int, stream=None)
     rows, k = _rows_of(x)
     n = torch.empty((1,), dtype=torch.int64, device=x.device)
     mix_underflow_count(x, rows, k, x.stride(0), codes, fmt, n, stream)
+    return n
+
+
+def clamp_count(x: torch.Tensor, ebias: int = -8, stream=None) -> torch.Tensor:
+    """Device counts (int64 [2]) of the MiX blocks of x clamped down (block
+    exponent above ebias + 15) and clamped up (nonzero, below ebias)."""
+    rows, k = _rows_of(x)
+    n = torch.empty((2,), dtype=torch.int64, device=x.device)
+    mix_clamp_count(x, rows, k, x.stride(0), ebias, n, stream)
     return n
 
 

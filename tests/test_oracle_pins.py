@@ -832,13 +832,60 @@ def pin_decode_attention(orc):
     assert np.allclose(e / e.sum(axis=1, keepdims=True), Pm, rtol=1e-6, atol=1e-12)
 
 
+def pin_clamp_count(orc):
+    """The clamped-block count against blocks built by hand and against an
+    independent restatement in Python: the block exponent is the floor of
+    log2 of the maximum, plus one when rounding its mantissa to three bits
+    (half to even, Python's round) carries out."""
+    import math
+    ebias = -8
+    # hand-built blocks: (block values, expected (high, low))
+    cases = [
+        ([1.875 * 2.0 ** 7], (0, 0)),          # f = 7 = ebias + 15: top code, not clamped
+        ([1.9375 * 2.0 ** 7], (1, 0)),         # rounds to 2^8: carried past the top
+        ([2.0 ** 8], (1, 0)),
+        ([2.0 ** -8], (0, 0)),                 # f = ebias: bottom code
+        ([1.9375 * 2.0 ** -9], (0, 0)),        # rounds up to 2^-8: carried into range
+        ([1.875 * 2.0 ** -9], (0, 1)),
+        ([2.0 ** -140], (0, 1)),               # fp32 subnormal
+        ([np.inf], (1, 0)),
+        ([-np.inf, 1.0], (1, 0)),
+        ([np.nan], (0, 0)),                    # NaN counts as zero
+        ([0.0], (0, 0)),
+        ([-3.0 * 2.0 ** 9, 1.0], (1, 0)),
+    ]
+    for vals, want in cases:
+        x = np.zeros((1, 32), np.float32)
+        x[0, :len(vals)] = vals
+        assert orc.mix_clamp_count(x, ebias) == want, (vals, want)
+    # random blocks over a wide exponent range, fp32 and bf16, several ebias
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((64, 256)) * np.exp2(rng.integers(-30, 30, (64, 256)))).astype(np.float32)
+    x[3, :32] = 0.0
+    for eb in (-15, -8, 0):
+        for arr in (x, synth.to_bf16_bits(x.astype(np.float64))):
+            vals = synth.bf16_bits_to_f32(arr) if arr.dtype == np.uint16 else arr
+            hi = lo = 0
+            for blk in vals.reshape(-1, 32).astype(np.float64):
+                amax = float(np.max(np.abs(blk)))
+                if amax == 0.0:
+                    continue
+                m, e = math.frexp(amax)           # amax = m 2^e, m in [0.5, 1)
+                f = e - 1
+                if round((2.0 * m - 1.0) * 8.0) == 8:
+                    f += 1
+                hi += f > eb + 15
+                lo += f < eb
+            assert orc.mix_clamp_count(arr, eb) == (hi, lo), eb
+
+
 ALL_PINS = [pin_bit_accounting, pin_dequant_special_values, pin_refinement_brute_force,
             pin_exhaustive_sweep, pin_asymmetric_zero, pin_round_trip,
             pin_nonfinite_and_zero_blocks, pin_e2m1_and_int4_brute_force, pin_mx_scale_rule,
             pin_mx_axis_consistency, pin_gemm_eq6_exact, pin_gemm_against_dequant_matmul,
             pin_gemm_reduces_to_mx_dot, pin_gemm_batch_gqa_indexing, pin_ksmooth,
             pin_mx_tight_rule, pin_auto_ebias, pin_mx_g16, pin_gemm_g16, pin_nvfp4, pin_underflow_count,
-            pin_decode_attention, pin_t2_shared_layout]
+            pin_decode_attention, pin_t2_shared_layout, pin_clamp_count]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda f: f.__name__)
@@ -861,16 +908,17 @@ def test_pin(orc, pin):
 # elements that were zero before quantisation, 17 the matmul drops the
 # recycled -0 as if it coded zero, 18 element nibbles are packed high nibble
 # first, 19 the MXINT4 element step is 2^(X-1) instead of 2^(X-2), 20 the
-# Type 2 sub-block mantissas are packed and unpacked in reverse order.
+# Type 2 sub-block mantissas are packed and unpacked in reverse order, 21 the
+# clamped-block count ignores the mantissa rounding's carry.
 FAST_PINS = [pin_dequant_special_values, pin_round_trip, pin_asymmetric_zero,
              pin_e2m1_and_int4_brute_force, pin_mx_scale_rule, pin_gemm_eq6_exact,
              pin_gemm_against_dequant_matmul, pin_ksmooth, pin_nonfinite_and_zero_blocks,
              pin_mx_tight_rule, pin_auto_ebias, pin_gemm_g16, pin_nvfp4, pin_underflow_count,
-             pin_t2_shared_layout,
+             pin_t2_shared_layout, pin_clamp_count,
              lambda o: pin_refinement_brute_force(o, n_blocks=40)]
 
 
-@pytest.mark.parametrize("mutation", list(range(1, 21)))
+@pytest.mark.parametrize("mutation", list(range(1, 22)))
 def test_planted_mistakes_are_caught(orc, mutation):
     failed = []
     try:
