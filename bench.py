@@ -76,6 +76,12 @@ EXT_INPUTS = {}   # step tensors the extension measurements reuse
 CLAMP = {}        # what the clamped-block report reads (filled by build_workload)
 
 
+def with_prepared(d, src):
+    """d with the prepared B of the descriptor src (same B and shapes)."""
+    d.b_prepared = src.b_prepared
+    return d
+
+
 def clamp_report(torch, mix, ws):
     """Clamped MiX blocks of every MiX quantisation in the step, at its ebias:
     [blocks clamped down (exponent above ebias + 15), blocks clamped up
@@ -135,12 +141,14 @@ def dims(small=False):
                 HQ=28, HK=4, D=128)
 
 
-def tc_launches(n, b_in_place=False):
+def tc_launches(n, b_in_place=False, prepared=False):
     """Launches of one tensor-core matmul call: outputs wider than one 256-column
-    tile take the staged variant (expand A, expand B or its scales, matmul);
-    narrower ones the fused-decode variant (expand B unless it is MXFP4 read
-    in place, matmul)."""
-    return 3 if n > 256 else (1 if b_in_place else 2)
+    tile take the staged variant (expand A, expand B or its scales unless B was
+    prepared once, matmul); narrower ones the fused-decode variant (expand B
+    unless it is MXFP4 read in place or prepared, matmul)."""
+    if n > 256:
+        return 2 if prepared else 3
+    return 1 if (b_in_place or prepared) else 2
 
 
 def step_table(small=False):
@@ -161,12 +169,14 @@ def step_table(small=False):
     add(f"mix_quantize_t2_{M}x{DF}", mix_bytes(M, DF, 2), cpu=("mix2", M * DF))
     for name, k, n in (("qkv", DM, QKV), ("o", DM, DM), ("gate_up", DM, 2 * DF), ("down", DF, DM)):
         add(f"gemm_{name}_{M}x{k}x{n}", plane_bytes(M, k, 2) + plane_bytes(n, k, 0) + plane_bytes(M, n, 2),
-            2.0 * M * n * k, launches=tc_launches(n), cpu=("gemm", M * n * (k // 32)))
+            2.0 * M * n * k, launches=tc_launches(n, prepared=True), cpu=("gemm", M * n * (k // 32)))
     add(f"mix_quantize_t1_{MV}x1280", mix_bytes(MV, 1280, 1), cpu=("mix1", MV * 1280))
     add(f"gemm_vit_fc1_{MV}x1280x5120", plane_bytes(MV, 1280, 1) + plane_bytes(5120, 1280, 0) +
-        plane_bytes(MV, 5120, 1), 2.0 * MV * 5120 * 1280, launches=tc_launches(5120), cpu=("gemm", MV * 5120 * 40))
+        plane_bytes(MV, 5120, 1), 2.0 * MV * 5120 * 1280, launches=tc_launches(5120, prepared=True),
+        cpu=("gemm", MV * 5120 * 40))
     add(f"gemm_vit_fc2_{MV}x5120x1280", plane_bytes(MV, 5120, 1) + plane_bytes(1280, 5120, 0) +
-        plane_bytes(MV, 1280, 1), 2.0 * MV * 1280 * 5120, launches=tc_launches(1280), cpu=("gemm", MV * 1280 * 160))
+        plane_bytes(MV, 1280, 1), 2.0 * MV * 1280 * 5120, launches=tc_launches(1280, prepared=True),
+        cpu=("gemm", MV * 1280 * 160))
     add(f"ksmooth_compute_{T}x{HK}x{D}", T * HK * D * (2 + 4) + HK * D * 4, launches=3,
         cpu=("ks", 2 * T * HK * D))   # K read once, K' (fp32) and the mean written once
     add(f"mix_quantize_t2_q_{T * HQ}x{D}", mix_bytes(T * HQ, D, 2), cpu=("mix2", T * HQ * D))
@@ -275,6 +285,14 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
         tc_descs.append(d)
         return lambda: mix.mix_mx_gemm(d, ws_tc[0])
 
+    # weights are fixed: their MMA-ready form (scale words regrouped, MXINT4
+    # expanded to e4m3) is made once here, when they are quantised
+    def weight_call(d):
+        buf = mix.prepare_b(d)
+        if buf is not None:
+            keep.append(buf)
+        return tc_call(d)
+
     ws_tc = [None]
 
     # ----- per-step activations
@@ -324,10 +342,10 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
         bc, bs = wq[name]
         d = mix.gemm_desc(M, n, k, ac_, as_, T2, -8, bc, bs, FP4, c=None, epi=mix.MIX_EPI_MIX_T2, out_codes=oc,
                           out_shared=os_, algo=mix.MIX_GEMM_TCGEN05)
-        fns[f"gemm_{name}_{M}x{k}x{n}"] = tc_call(d)
-        CLAMP["epi"].append((f"gemm_{name}_{M}x{k}x{n}", (lambda c, k=k, n=n, ac_=ac_, as_=as_, bc=bc, bs=bs:
-                             mix.gemm_desc(M, n, k, ac_, as_, T2, -8, bc, bs, FP4, c=c, algo=mix.MIX_GEMM_TCGEN05)),
-                             M, n, -8))
+        fns[f"gemm_{name}_{M}x{k}x{n}"] = weight_call(d)
+        CLAMP["epi"].append((f"gemm_{name}_{M}x{k}x{n}", (lambda c, k=k, n=n, ac_=ac_, as_=as_, bc=bc, bs=bs, d=d:
+                             with_prepared(mix.gemm_desc(M, n, k, ac_, as_, T2, -8, bc, bs, FP4, c=c,
+                                                         algo=mix.MIX_GEMM_TCGEN05), d)), M, n, -8))
     d2h.append(outs["down"])
 
     # ----- 3. ViT MLP: fc1's fused MiX-4.25b output is fc2's input
@@ -339,12 +357,12 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
                        out_shared=hs, algo=mix.MIX_GEMM_TCGEN05)
     d2 = mix.gemm_desc(MV, 1280, 5120, hc, hs, T1, -8, wv2[0], wv2[1], INT4, epi=mix.MIX_EPI_MIX_T1, out_codes=yc,
                        out_shared=ys, algo=mix.MIX_GEMM_TCGEN05)
-    fns[f"gemm_vit_fc1_{MV}x1280x5120"] = tc_call(d1)
-    fns[f"gemm_vit_fc2_{MV}x5120x1280"] = tc_call(d2)
-    CLAMP["epi"].append((f"gemm_vit_fc1_{MV}x1280x5120", lambda c: mix.gemm_desc(
-        MV, 5120, 1280, vc, vs, T1, -8, wv1[0], wv1[1], INT4, c=c, algo=mix.MIX_GEMM_TCGEN05), MV, 5120, -8))
-    CLAMP["epi"].append((f"gemm_vit_fc2_{MV}x5120x1280", lambda c: mix.gemm_desc(
-        MV, 1280, 5120, hc, hs, T1, -8, wv2[0], wv2[1], INT4, c=c, algo=mix.MIX_GEMM_TCGEN05), MV, 1280, -8))
+    fns[f"gemm_vit_fc1_{MV}x1280x5120"] = weight_call(d1)
+    fns[f"gemm_vit_fc2_{MV}x5120x1280"] = weight_call(d2)
+    CLAMP["epi"].append((f"gemm_vit_fc1_{MV}x1280x5120", lambda c: with_prepared(mix.gemm_desc(
+        MV, 5120, 1280, vc, vs, T1, -8, wv1[0], wv1[1], INT4, c=c, algo=mix.MIX_GEMM_TCGEN05), d1), MV, 5120, -8))
+    CLAMP["epi"].append((f"gemm_vit_fc2_{MV}x5120x1280", lambda c: with_prepared(mix.gemm_desc(
+        MV, 1280, 5120, hc, hs, T1, -8, wv2[0], wv2[1], INT4, c=c, algo=mix.MIX_GEMM_TCGEN05), d2), MV, 1280, -8))
     CLAMP["inputs"] += [(f"mix_quantize_t1_{M}x{DM}", x, -8), (f"mix_quantize_t2_{M}x{DF}", xd, -8),
                         (f"mix_quantize_t1_{MV}x1280", xv, -8)]
     d2h.append(yc)
@@ -652,6 +670,8 @@ def measure_extensions(torch, mix, stream, iters=10):
                         out_shared=osh, algo=mix.MIX_GEMM_TCGEN05, b_block=16)
     d32 = mix.gemm_desc(M, 2 * DF, DM, a2c, a2s, T2, -8, g32c, g32s, INT4, epi=mix.MIX_EPI_MIX_T2, out_codes=oc,
                         out_shared=osh, algo=mix.MIX_GEMM_TCGEN05)
+    mix.prepare_b(d16)   # weights: prepared once, as in the step
+    mix.prepare_b(d32)
     gws = torch.empty(max(mix.mix_mx_gemm_workspace_bytes(d16), mix.mix_mx_gemm_workspace_bytes(d32)),
                       dtype=torch.uint8, device=dev)
     g16_bytes = plane_bytes(M, DM, 2) + 2 * DF * DM // 2 + 2 * DF * DM // 16 + plane_bytes(M, 2 * DF, 2)
@@ -668,9 +688,9 @@ def measure_extensions(torch, mix, stream, iters=10):
     eb = torch.empty((1,), dtype=torch.int32, device=dev)
     table = [
         (f"gemm_gate_up_mix_int4g16_{M}x{DM}x{2 * DF}", "MiX-4.5b x MXINT4g16 (staged; the g16 scales folded "
-         "into the e4m3 expansion)", g16_bytes, 3, lambda: mix.mix_mx_gemm(d16, gws), gflops),
+         "into the e4m3 expansion, prepared once)", g16_bytes, 2, lambda: mix.mix_mx_gemm(d16, gws), gflops),
         (f"gemm_gate_up_mix_int4_{M}x{DM}x{2 * DF}", "MiX-4.5b x MXINT4 (32-blocks), same call for comparison",
-         g32_bytes, 3, lambda: mix.mix_mx_gemm(d32, gws), gflops),
+         g32_bytes, 2, lambda: mix.mix_mx_gemm(d32, gws), gflops),
         (f"mx_quantize_int4_g16_{DM}x{DF}", "MXINT4g16 weight quantiser (down the columns)",
          DF * DM * 2 + DF * DM // 2 + DF * DM // 16, 1,
          lambda: mix.mx_quantize(w_gu, DM, DF, 2 * DF, 0, INT4, mix.MX_BLOCK16, g16c, g16s)),
@@ -762,6 +782,79 @@ def dead_zone_table(torch, mix, dev, tokens=4096):
     return res
 
 
+def single_call(args):
+    """--call NAME: only that call of the step, its operands alone on the
+    device (a few hundred MB), run warm-up + steps times with CUDA events
+    around each launch; for profiler captures of one kernel and for quick
+    timing.  Prints one JSON line with the median time."""
+    import torch
+    from quantized_vlm_gemm_mix_b300 import _build
+    _build.build()
+    from quantized_vlm_gemm_mix_b300 import mix, synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = dims()
+    M, DM, DF, QKV, MV = g["M"], g["DM"], g["DF"], g["QKV"], g["MV"]
+    T1, T2, FP4, INT4 = mix.MIX_T1_4P25, mix.MIX_T2_4P5, mix.MX_FP4_E2M1, mix.MX_INT4
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    table = {r[0]: r for r in step_table()}
+    name = args.call
+    _require(name in table, f"--call takes one of: {', '.join(table)}")
+    _, nbytes, flops, _, _ = table[name]
+    gemms = {f"gemm_qkv_{M}x{DM}x{QKV}": (M, DM, QKV, 31, T2, FP4, 1), f"gemm_o_{M}x{DM}x{DM}": (M, DM, DM, 32, T2, FP4, 1),
+             f"gemm_gate_up_{M}x{DM}x{2 * DF}": (M, DM, 2 * DF, 30, T2, FP4, 1),
+             f"gemm_down_{M}x{DF}x{DM}": (M, DF, DM, 33, T2, FP4, 2),
+             f"gemm_vit_fc1_{MV}x1280x5120": (MV, 1280, 5120, 34, T1, INT4, 3),
+             f"gemm_vit_fc2_{MV}x5120x1280": (MV, 5120, 1280, 35, T1, INT4, 4)}
+    if name in gemms:
+        m, k, n, wid, at, bt, aid = gemms[name]
+        x = bf16(synth.to_bf16_bits(synth.vlm_activations(0, aid, m, k, visual_rows=(3 * m) // 4 if m == M else m)))
+        ac, ash = mix.quantize_mix(x, at)
+        del x
+        w = bf16(synth.to_bf16_bits(synth.gaussian_weights(0, wid, k, n)))
+        bc, bs = mix.quantize_mx(w, 0, bt)
+        del w
+        oc = torch.empty((m, n // 2), dtype=torch.uint8, device=dev)
+        os_ = torch.empty((m, n // 32), dtype=torch.uint8 if at == T1 else torch.int16, device=dev)
+        d = mix.gemm_desc(m, n, k, ac, ash, at, -8, bc, bs, bt, epi=at, out_codes=oc, out_shared=os_,
+                          algo=mix.MIX_GEMM_TCGEN05)
+        mix.prepare_b(d)
+        ws = torch.empty(max(16, mix.mix_mx_gemm_workspace_bytes(d)), dtype=torch.uint8, device=dev)
+        fn = lambda: mix.mix_mx_gemm(d, ws)
+    elif name.startswith("mix_quantize_t") and name.endswith(f"_{M}x{DM}"):
+        t = T1 if name.startswith("mix_quantize_t1") else T2
+        x = bf16(synth.to_bf16_bits(synth.vlm_activations(0, 1, M, DM, visual_rows=(3 * M) // 4)))
+        c = torch.empty((M, DM // 2), dtype=torch.uint8, device=dev)
+        sh = torch.empty((M, DM // 32), dtype=torch.uint8 if t == T1 else torch.int16, device=dev)
+        fn = lambda: mix.mix_quantize(x, M, DM, DM, t, -8, 1, c, sh)
+    else:
+        raise SystemExit(f"--call supports the prefill matmuls and the MiX quantisers of the sweep, not {name}")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # larger than L2
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(200000)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(a.elapsed_time(b))
+    _require(mix.mix_device_error() == 0, "a kernel reported a timed-out wait")
+    ms = float(np.median(times))
+    out = {"call": name, "ms": round(ms, 5), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+           "frac_hbm": round(nbytes / (ms * 1e-3) / 1e9 / HBM, 3), "steps": args.steps, "warmup": args.warmup,
+           "l2": "256 MB buffer written before every launch"}
+    if flops:
+        out.update({"TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1),
+                    "frac_mma": round(flops / (ms * 1e-3) / 1e12 / MX8_TFLOPS, 3)})
+    print(json.dumps(out), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -774,6 +867,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     ap.add_argument("--no-ext", action="store_true", help="skip the kernels measured beside the step")
+    ap.add_argument("--call", default=None, help="run one call of the step alone (see single_call)")
     ap.add_argument("--mma-peak", action="store_true",
                     help="measure the dense FP8 (e4m3) tensor rate instead: cuBLASLt 8192^3, burst and sustained")
     args = ap.parse_args()
@@ -784,6 +878,8 @@ def main():
         return run_reference(args, rank, world)
     if args.mma_peak:
         return measure_fp8_peak(local)
+    if args.call:
+        return single_call(args)
 
     import torch
     from quantized_vlm_gemm_mix_b300 import _build

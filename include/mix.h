@@ -284,14 +284,38 @@ typedef struct {
   void* out_shared;    /* MiX shared entries or MX scale bytes */
   int64_t out_ld, out_batch_stride;
   mix_gemm_algo_t algo;
+  /* Optional: B in the tensor-core path's prepared form, written by
+   * mix_mx_gemm_prepare_b for a descriptor with the same M, N, K, batch,
+   * b_group, B fields and algo (NULL: B is prepared inside every call). */
+  const void* b_prepared;
 } mix_gemm_desc_t;
 
 /* Bytes of device workspace mix_mx_gemm needs for this descriptor (0 if
  * none).  The workspace is scratch owned by the caller; its contents on entry
- * do not matter. */
+ * do not matter.  With b_prepared set it covers A's staging only. */
 MIX_API size_t mix_mx_gemm_workspace_bytes(const mix_gemm_desc_t* desc);
 MIX_API mix_status_t mix_mx_gemm(const mix_gemm_desc_t* desc, void* workspace, size_t workspace_bytes,
                          mix_stream_t stream);
+
+/* Prepared weights.  The tensor-core path feeds the MMA from B in a fixed
+ * form: the UE8M0 scale bytes regrouped into the words the MMA's scale
+ * columns take (one 32-bit word per row and 128-deep k-step, in tiles of
+ * rows), plus, unless B is MXFP4 that the unpacking TMA reads in place, the
+ * exact e4m3 expansion of every element (Kp = K rounded up to 128 bytes per
+ * row).  This is a layout transform of B alone: no arithmetic of the method
+ * moves out of the matmul, and the products are the same bits.  Weights are
+ * fixed, so a caller can prepare them once, when they are quantised, and
+ * pass the result in desc->b_prepared on every call; without it each call
+ * prepares B again in its workspace.
+ *   mix_mx_gemm_prepare_b_bytes: bytes of the prepared form (0: this
+ *     descriptor takes no prepared B -- the shift-add path, or MXFP4 on the
+ *     fused-decode variant, which reads B as it is).
+ *   mix_mx_gemm_prepare_b: writes it into `prepared` (device memory owned by
+ *     the caller, any alignment of 16 bytes or more; valid while B's planes
+ *     are unchanged).  desc->b_prepared is ignored here. */
+MIX_API size_t mix_mx_gemm_prepare_b_bytes(const mix_gemm_desc_t* desc);
+MIX_API mix_status_t mix_mx_gemm_prepare_b(const mix_gemm_desc_t* desc, void* prepared, size_t prepared_bytes,
+                                           mix_stream_t stream);
 
 /* ---------------------------------------------------------------------- */
 /* K-smoothing (SageAttention style; Method section, accelerator bullet,   */
@@ -392,7 +416,9 @@ MIX_API const char* mix_status_str(mix_status_t status);
 /* Kernels never spin without bound: a wait that runs out records a bit in a
  * per-device error word and the kernel returns early (its outputs are then
  * undefined).  This reads the word for the current device (synchronising the
- * device) and clears it when `clear` is nonzero.  MIX_OK if the read worked. */
+ * device) and clears it when `clear` is nonzero.  MIX_OK if the read worked.
+ * Bits 0..9: a wait of the matmul kernels (which one, by role); bit 20: a
+ * wait of the MiX quantiser's TMA pipeline. */
 MIX_API mix_status_t mix_device_error(unsigned* word, int clear);
 /* Library version, major * 10000 + minor * 100 + patch. */
 MIX_API int mix_version(void);

@@ -69,7 +69,11 @@ int mix_version(void) { return kVersion; }
 
 mix_status_t mix_device_error(unsigned* word, int clear) {
   if (word == nullptr) return MIX_ERR_INVALID_ARG;
-  return from_cuda(read_device_error(word, clear != 0));
+  unsigned q = 0;
+  cudaError_t e = read_device_error(word, clear != 0);
+  if (e == cudaSuccess) e = read_quant_error(&q, clear != 0);
+  if (e == cudaSuccess && q != 0) *word |= 1u << 20;  // the quantiser's TMA wait ran out
+  return from_cuda(e);
 }
 
 mix_status_t mix_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,
@@ -257,6 +261,7 @@ static mix_status_t validate_gemm(const mix_gemm_desc_t* d) {
   if (d->epi < MIX_EPI_NONE || d->epi > MIX_EPI_MXFP4) return MIX_ERR_INVALID_ARG;
   if ((d->epi_flags & ~7u) || (d->epi_flags & 6u) == 6u) return MIX_ERR_INVALID_ARG;
   if (d->algo < MIX_GEMM_AUTO || d->algo > MIX_GEMM_TCGEN05_FUSED) return MIX_ERR_INVALID_ARG;
+  if (d->b_prepared != nullptr && !aligned(d->b_prepared, 16)) return MIX_ERR_ALIGN;
   if (d->K % 32 != 0) return MIX_ERR_SHAPE;
   if (d->epi != MIX_EPI_NONE && d->N % 32 != 0) return MIX_ERR_SHAPE;
   if (d->epi == MIX_EPI_NONE && d->c == nullptr) return MIX_ERR_INVALID_ARG;
@@ -293,6 +298,22 @@ size_t mix_mx_gemm_workspace_bytes(const mix_gemm_desc_t* d) {
   if (validate_gemm(d) != MIX_OK || d->M == 0 || d->N == 0) return 0;
   if (use_shiftadd(d)) return gemv_workspace_bytes(*d);
   return gemm_tc_workspace_bytes(*d);
+}
+
+size_t mix_mx_gemm_prepare_b_bytes(const mix_gemm_desc_t* d) {
+  if (validate_gemm(d) != MIX_OK || d->M == 0 || d->N == 0 || d->K == 0 || use_shiftadd(d)) return 0;
+  return gemm_tc_prepare_b_bytes(*d);
+}
+
+mix_status_t mix_mx_gemm_prepare_b(const mix_gemm_desc_t* d, void* prepared, size_t prepared_bytes,
+                                   mix_stream_t stream) {
+  mix_status_t s = validate_gemm(d);
+  if (s != MIX_OK) return s;
+  const size_t need = mix_mx_gemm_prepare_b_bytes(d);
+  if (need == 0) return MIX_ERR_UNSUPPORTED;
+  if (prepared == nullptr || prepared_bytes < need) return MIX_ERR_WORKSPACE;
+  if (!aligned(prepared, 16)) return MIX_ERR_ALIGN;
+  return from_cuda(launch_gemm_tc_prepare_b(*d, prepared, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mix_status_t mix_mx_gemm(const mix_gemm_desc_t* d, void* workspace, size_t workspace_bytes,

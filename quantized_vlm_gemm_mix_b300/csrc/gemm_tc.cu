@@ -908,6 +908,18 @@ cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtens
 
 }  // namespace
 
+bool make_rows128_map(CUtensorMap* m, const void* base, int64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows < 1 || (reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
+  const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {128};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 
 TcParams make_params(const mix_gemm_desc_t& d) {
@@ -942,6 +954,22 @@ bool want_staged(const mix_gemm_desc_t& d) {
 // need no workspace; any other B is expanded once into e4m3 in the workspace.
 bool fused_b_native(const mix_gemm_desc_t& d) { return staged_fp4_native_ok(d); }
 
+unsigned char* align_ws(const void* p) {
+  return reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(p) + kStagedAlign - 1) &
+                                          ~static_cast<uintptr_t>(kStagedAlign - 1));
+}
+
+// A staged plan's B parts (the expanded B plane, when there is one, and the
+// scale words) moved to start at offset 0: the layout of a prepared B.
+StagedPlan rebase_b(StagedPlan sp) {
+  const size_t o = sp.off_b;
+  sp.off_b -= o;
+  sp.off_sfb -= o;
+  sp.off_sfe -= o;
+  sp.bytes -= o;
+  return sp;
+}
+
 cudaError_t launch_fused(const mix_gemm_desc_t& d, void* ws, cudaStream_t st, mix_status_t* why) {
   const int64_t bb = (d.batch + d.b_group - 1) / d.b_group;
   CUtensorMap ma, mb;
@@ -963,8 +991,7 @@ cudaError_t launch_fused(const mix_gemm_desc_t& d, void* ws, cudaStream_t st, mi
     p.b_tma_bytes = (uint32_t)(tbn * BK / 2);
   } else {
     sp = staged_plan_b_only(d);
-    base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(ws) + kStagedAlign - 1) &
-                                            ~static_cast<uintptr_t>(kStagedAlign - 1));
+    base = align_ws(d.b_prepared != nullptr ? d.b_prepared : ws);
     if (!make_e4m3_map(&mb, base + sp.off_b, sp.k_pad, d.N, sp.bb, (uint32_t)tbn)) {
       *why = MIX_ERR_UNSUPPORTED;
       return cudaSuccess;
@@ -982,7 +1009,7 @@ cudaError_t launch_fused(const mix_gemm_desc_t& d, void* ws, cudaStream_t st, mi
     *why = MIX_ERR_UNSUPPORTED;
     return cudaSuccess;
   }
-  if (!native) {
+  if (!native && d.b_prepared == nullptr) {
     const cudaError_t e = launch_expand_b(d, sp, base, st);
     if (e != cudaSuccess) return e;
   }
@@ -992,15 +1019,18 @@ cudaError_t launch_fused(const mix_gemm_desc_t& d, void* ws, cudaStream_t st, mi
 
 cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t st, mix_status_t* why) {
   const StagedPlan sp = staged_plan(d);
-  unsigned char* base = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(ws) + kStagedAlign - 1) & ~static_cast<uintptr_t>(kStagedAlign - 1));
+  unsigned char* base = align_ws(ws);
+  // B's staging: in the workspace, or prepared once by the caller
+  const bool prepared = d.b_prepared != nullptr;
+  const StagedPlan bp = prepared ? rebase_b(sp) : sp;
+  unsigned char* bbase = prepared ? align_ws(d.b_prepared) : base;
   CUtensorMap ma, mb;
   if (!make_e4m3_map(&ma, base + sp.off_a, sp.k_pad, d.M, d.batch, BM)) {
     *why = MIX_ERR_UNSUPPORTED;
     return cudaSuccess;
   }
   const bool ok_b = sp.b_native ? make_fp4_operand_map(&mb, d.b_codes, d.K, d.N, sp.bb, d.b_ld, d.b_batch_stride, BNS)
-                                : make_e4m3_map(&mb, base + sp.off_b, sp.k_pad, d.N, sp.bb, BNS);
+                                : make_e4m3_map(&mb, bbase + bp.off_b, sp.k_pad, d.N, sp.bb, BNS);
   if (!ok_b) {
     *why = MIX_ERR_UNSUPPORTED;
     return cudaSuccess;
@@ -1012,12 +1042,14 @@ cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t 
   }
   TcParams p = make_params(d);
   p.sfa_g = base + sp.off_sfa;
-  p.sfb_g = base + sp.off_sfb;
+  p.sfb_g = bbase + bp.off_sfb;
   p.mt = sp.mt; p.nt = sp.nt; p.kt = sp.kt;
   cudaError_t e = launch_expand_a(d, sp, base, st);
   if (e != cudaSuccess) return e;
-  e = launch_expand_b(d, sp, base, st);
-  if (e != cudaSuccess) return e;
+  if (!prepared) {
+    e = launch_expand_b(d, sp, base, st);
+    if (e != cudaSuccess) return e;
+  }
   const int64_t tiles = d.batch * sp.nt * sp.mt;
   const dim3 grid((unsigned)(tiles < num_sms() ? tiles : num_sms()));
   return sp.b_native ? launch_staged<true>(ma, mb, mc, p, grid, st) : launch_staged<false>(ma, mb, mc, p, grid, st);
@@ -1027,9 +1059,24 @@ cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t 
 
 size_t gemm_tc_workspace_bytes(const mix_gemm_desc_t& d) {
   if (!shape_ok(d)) return 0;
-  if (want_staged(d)) return staged_plan(d).bytes + kStagedAlign;
+  if (want_staged(d)) {
+    const StagedPlan sp = staged_plan(d);
+    return (d.b_prepared != nullptr ? sp.off_b : sp.bytes) + kStagedAlign;
+  }
+  if (fused_b_native(d) || d.b_prepared != nullptr) return 0;
+  return staged_plan_b_only(d).bytes + kStagedAlign;
+}
+
+size_t gemm_tc_prepare_b_bytes(const mix_gemm_desc_t& d) {
+  if (!shape_ok(d)) return 0;
+  if (want_staged(d)) return rebase_b(staged_plan(d)).bytes + kStagedAlign;
   if (fused_b_native(d)) return 0;
   return staged_plan_b_only(d).bytes + kStagedAlign;
+}
+
+cudaError_t launch_gemm_tc_prepare_b(const mix_gemm_desc_t& d, void* prepared, cudaStream_t st) {
+  if (want_staged(d)) return launch_expand_b(d, rebase_b(staged_plan(d)), align_ws(prepared), st);
+  return launch_expand_b(d, staged_plan_b_only(d), align_ws(prepared), st);
 }
 
 cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, void* ws, size_t ws_bytes, cudaStream_t st,

@@ -1,6 +1,7 @@
 // Host-side launchers shared between the library's translation units.  The
 // C ABI (include/mix.h) validates arguments and then calls these.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -51,6 +52,9 @@ cudaError_t launch_gemv_shiftadd(const mix_gemm_desc_t& d, void* ws, cudaStream_
 cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, void* ws, size_t ws_bytes, cudaStream_t st,
                            mix_status_t* why);
 size_t gemm_tc_workspace_bytes(const mix_gemm_desc_t& d);
+// Prepared B (the tensor-core path's B staging, written once for fixed weights).
+size_t gemm_tc_prepare_b_bytes(const mix_gemm_desc_t& d);
+cudaError_t launch_gemm_tc_prepare_b(const mix_gemm_desc_t& d, void* prepared, cudaStream_t st);
 
 // Staged tensor-core matmul: the operands are expanded once per call into the
 // caller's workspace -- e4m3 planes [batch][rows][k_pad] (k_pad = K rounded up
@@ -97,7 +101,14 @@ size_t ksmooth_noalloc_scratch_bytes();
 cudaError_t launch_ksmooth_noalloc(const void* k, bool bf16, int64_t tokens, int heads, int head_dim,
                                    int64_t ld, float* mean, int mode, float* k_out, cudaStream_t st);
 
-// Device error word (bounded waits).
+// A contiguous byte range viewed as rows of 128 bytes (`rows` of them), read
+// by 2-D TMA boxes of 128 bytes x box_rows with the 128-byte swizzle: 16-byte
+// unit u of box row r lands at unit u ^ (r % 8) of that row in shared memory.
+bool make_rows128_map(CUtensorMap* m, const void* base, int64_t rows, uint32_t box_rows);
+
+// Device error word (bounded waits): the matmul's, and the quantiser's (its
+// TMA waits), read (and cleared) separately.
 cudaError_t read_device_error(unsigned* word, bool clear);
+cudaError_t read_quant_error(unsigned* word, bool clear);
 
 }  // namespace mixk

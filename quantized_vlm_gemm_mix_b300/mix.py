@@ -32,6 +32,7 @@ EXPORTS = ["mix_codes_bytes", "mix_shared_bytes", "mx_scales_bytes", "mix_quanti
            "mix_quantize_auto", "mx_quantize", "nvfp4_quantize", "mix_underflow_count", "mix_clamp_count",
            "mix_decode_attention_workspace_bytes", "mix_decode_attention",
            "mix_dequantize", "mx_dequantize", "mix_mx_gemm_workspace_bytes", "mix_mx_gemm",
+           "mix_mx_gemm_prepare_b_bytes", "mix_mx_gemm_prepare_b",
            "ksmooth_workspace_bytes", "ksmooth_kv", "ksmooth_kv_noalloc", "mix_status_str", "mix_device_error",
            "mix_version"]
 KSMOOTH_NOALLOC_SCRATCH_BYTES = 2 << 20
@@ -58,7 +59,7 @@ class GemmDesc(ctypes.Structure):
         ("epi", ctypes.c_int), ("epi_ebias", ctypes.c_int), ("epi_flags", ctypes.c_uint),
         ("out_codes", ctypes.c_void_p), ("out_shared", ctypes.c_void_p),
         ("out_ld", ctypes.c_int64), ("out_batch_stride", ctypes.c_int64),
-        ("algo", ctypes.c_int),
+        ("algo", ctypes.c_int), ("b_prepared", ctypes.c_void_p),
     ]
 
 
@@ -98,6 +99,8 @@ def _load():
         "mx_dequantize": (I, [P, P, I64, I64, I, P, P]),
         "mix_mx_gemm_workspace_bytes": (S, [ctypes.POINTER(GemmDesc)]),
         "mix_mx_gemm": (I, [ctypes.POINTER(GemmDesc), P, S, P]),
+        "mix_mx_gemm_prepare_b_bytes": (S, [ctypes.POINTER(GemmDesc)]),
+        "mix_mx_gemm_prepare_b": (I, [ctypes.POINTER(GemmDesc), P, S, P]),
         "ksmooth_workspace_bytes": (S, [I64, I, I]),
         "ksmooth_kv": (I, [P, I, I64, I, I, I64, P, I, P, P, S, P]),
         "ksmooth_kv_noalloc": (I, [P, I, I64, I, I, I64, P, I, P, P]),
@@ -249,6 +252,30 @@ def mix_mx_gemm_workspace_bytes(desc: GemmDesc) -> int:
 def mix_mx_gemm(desc: GemmDesc, workspace=None, stream=None) -> None:
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib.mix_mx_gemm(ctypes.byref(desc), _ptr(workspace), ws_bytes, _stream(stream)), "mix_mx_gemm")
+
+
+def mix_mx_gemm_prepare_b_bytes(desc: GemmDesc) -> int:
+    return lib.mix_mx_gemm_prepare_b_bytes(ctypes.byref(desc))
+
+
+def mix_mx_gemm_prepare_b(desc: GemmDesc, prepared, stream=None) -> None:
+    nbytes = prepared.numel() * prepared.element_size()
+    _check(lib.mix_mx_gemm_prepare_b(ctypes.byref(desc), _ptr(prepared), nbytes, _stream(stream)),
+           "mix_mx_gemm_prepare_b")
+
+
+def prepare_b(desc: GemmDesc, stream=None):
+    """Prepare desc's B once (a device buffer allocated by torch) and set
+    desc.b_prepared to it; returns the buffer, or None when this descriptor
+    takes B as it is."""
+    need = mix_mx_gemm_prepare_b_bytes(desc)
+    if not need:
+        return None
+    buf = torch.empty(need, dtype=torch.uint8, device=torch.device("cuda"))
+    mix_mx_gemm_prepare_b(desc, buf, stream)
+    desc.b_prepared = _ptr(buf)
+    desc._keep.append(buf)
+    return buf
 
 
 def ksmooth_workspace_bytes(tokens: int, heads: int, head_dim: int) -> int:

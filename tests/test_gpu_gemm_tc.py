@@ -256,3 +256,56 @@ def test_tc_zero_blocks_causal(mix, orc, algo, N):
     got = to_host(c)[0]
     assert row_rel_err(got, ref) <= GEMM_REL_TOL
     assert np.all(got[256:260] == 0) and np.all(got[261:] == 0)
+
+
+PREP_CASES = [(algo, bt, blk) for algo in ALGOS for bt, blk in ((1, 32), (0, 32), (0, 16), (1, 16))
+              if not (algo == "fused" and bt == 1 and blk == 32)]   # MXFP4 on the fused path: read as it is
+
+
+@pytest.mark.parametrize("algo,bt,b_block", PREP_CASES)
+def test_prepared_b_equals_per_call(mix, orc, algo, bt, b_block):
+    """B prepared once (mix_mx_gemm_prepare_b) gives the same bits as B
+    prepared inside the call, with and without the fused epilogue, and a
+    second call on the same prepared B gives them again."""
+    import torch
+    M, K = 200, 640
+    N = 544 if algo == "staged" else 224
+    a = synth.to_bf16_bits(synth.vlm_activations(50, 0, M, K, visual_rows=150))
+    w = synth.to_bf16_bits(synth.normal(51, 1, K * N, 0, 0.02).reshape(K, N))
+    ac, ash = orc.mix_quantize(a, 2)
+    bc, bs = orc.mx_quantize(w, 0, bt, 0, block=b_block)
+    outs = []
+    for prep in (False, True, True):
+        c = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        oc = torch.empty((M, N // 2), dtype=torch.uint8, device="cuda")
+        osh = torch.empty((M, N // 32), dtype=torch.int16, device="cuda")
+        d = mix.gemm_desc(M, N, K, to_dev(ac), to_dev(ash), 2, -8, to_dev(bc), to_dev(bs), bt, c=c, epi=2,
+                          out_codes=oc, out_shared=osh, algo=algo_id(mix, algo), b_block=b_block)
+        ws_plain = mix.mix_mx_gemm_workspace_bytes(d)
+        if prep:
+            assert mix.prepare_b(d) is not None
+            assert mix.mix_mx_gemm_workspace_bytes(d) < ws_plain
+        mix.gemm(d)
+        torch.cuda.synchronize()
+        assert mix.mix_device_error() == 0
+        outs.append((to_host(c), to_host(oc), to_host(osh)))
+    for o in outs[1:]:
+        assert np.array_equal(o[0].view(np.uint32), outs[0][0].view(np.uint32))
+        assert np.array_equal(o[1], outs[0][1]) and np.array_equal(o[2], outs[0][2])
+    ref = orc.gemm(ac, ash, 2, -8, bc, bs, bt, b_block=b_block)
+    assert row_rel_err(outs[0][0], ref) <= GEMM_REL_TOL
+
+
+def test_prepare_b_not_taken(mix, orc):
+    """MXFP4 weights on the fused-decode variant are read as they are: no
+    prepared form (0 bytes) and prepare_b says so."""
+    import ctypes
+    import torch
+    M, N, K = 128, 128, 256
+    ac, ash, bc, bs = operands(orc, 52, M, N, K, 2, 1)
+    c = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    d = mix.gemm_desc(M, N, K, to_dev(ac), to_dev(ash), 2, -8, to_dev(bc), to_dev(bs), 1, c=c,
+                      algo=mix.MIX_GEMM_TCGEN05_FUSED)
+    assert mix.mix_mx_gemm_prepare_b_bytes(d) == 0
+    st = mix.lib.mix_mx_gemm_prepare_b(ctypes.byref(d), ctypes.c_void_p(c.data_ptr()), 1 << 20, None)
+    assert st == mix.MIX_ERR_UNSUPPORTED
