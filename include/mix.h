@@ -417,9 +417,20 @@ MIX_API const char* mix_status_str(mix_status_t status);
  * per-device error word and the kernel returns early (its outputs are then
  * undefined).  This reads the word for the current device (synchronising the
  * device) and clears it when `clear` is nonzero.  MIX_OK if the read worked.
- * Bits 0..9: a wait of the matmul kernels (which one, by role); bit 20: a
- * wait of the MiX quantiser's TMA pipeline. */
+ * Bits 0..9: a wait of the matmul kernels (which one, by role). */
 MIX_API mix_status_t mix_device_error(unsigned* word, int clear);
+/* Test aid for the bounded waits.  Launches the staged tensor-core matmul
+ * kernel once, on a single 128 x 224 tile, with its producer switched off
+ * and every wait limited to 2^20 SM clocks (about half a millisecond): the
+ * MMA thread's wait for the first stage runs out with no copy or MMA in
+ * flight, the kernel records it in the device error word (bit 1, or bit 5
+ * if a scale warp's wait runs out first), its other roles see the CTA's
+ * abort flag, and the CTA frees its TMEM and exits.  The device stays
+ * usable; read and clear the word with mix_device_error afterwards.
+ * workspace: device memory, 16-byte aligned, at least
+ * MIX_SELFTEST_WORKSPACE_BYTES (its contents are never read). */
+#define MIX_SELFTEST_WORKSPACE_BYTES ((size_t)64 << 10)
+MIX_API mix_status_t mix_selftest_wait_timeout(void* workspace, size_t workspace_bytes, mix_stream_t stream);
 /* Library version, major * 10000 + minor * 100 + patch. */
 MIX_API int mix_version(void);
 

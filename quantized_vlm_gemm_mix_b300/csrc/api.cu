@@ -67,13 +67,16 @@ const char* mix_status_str(mix_status_t s) {
 
 int mix_version(void) { return kVersion; }
 
+mix_status_t mix_selftest_wait_timeout(void* workspace, size_t workspace_bytes, mix_stream_t stream) {
+  if (workspace == nullptr || workspace_bytes < MIX_SELFTEST_WORKSPACE_BYTES) return MIX_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return MIX_ERR_ALIGN;
+  if (selftest_ws_bytes() > MIX_SELFTEST_WORKSPACE_BYTES) return MIX_ERR_UNSUPPORTED;
+  return from_cuda(launch_selftest_wait_timeout(workspace, 1LL << 20, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 mix_status_t mix_device_error(unsigned* word, int clear) {
   if (word == nullptr) return MIX_ERR_INVALID_ARG;
-  unsigned q = 0;
-  cudaError_t e = read_device_error(word, clear != 0);
-  if (e == cudaSuccess) e = read_quant_error(&q, clear != 0);
-  if (e == cudaSuccess && q != 0) *word |= 1u << 20;  // the quantiser's TMA wait ran out
-  return from_cuda(e);
+  return from_cuda(read_device_error(word, clear != 0));
 }
 
 mix_status_t mix_quantize(const void* x, mix_dtype_t dtype, int64_t rows, int64_t k, int64_t ld,

@@ -19,12 +19,14 @@
 //   warp 1      TMEM allocator and the single MMA-issuing thread.
 //   warp 2      TMA producer of the B operand tiles (4-deep operand ring).
 //   warps 4-19  decoders: nibbles -> e4m3 in the 128-byte-swizzled K-major
-//               operand layout, the stage's scale words to shared memory;
-//               then the epilogue (tcgen05.ld, optional fp32 store through
-//               TMA, optional fused MiX/MX quantiser of each 32-column block).
-//   warps 20-23 scale warps: the stage's scale words into TMEM (tcgen05.st),
-//               one warp per TMEM lane quadrant.
-// A stage whose A tile holds only zero codes skips its MMAs.  The staged
+//               operand layout, the stage's scale words to shared memory in
+//               the layout tcgen05.cp reads (row 32 i + l in word i of lane
+//               l's 16 bytes); then the epilogue (tcgen05.ld, optional fp32
+//               store through TMA, optional fused MiX/MX quantiser of each
+//               32-column block).
+// The MMA thread copies the stage's scale words into TMEM (tcgen05.cp, in
+// issue order with the MMAs) and issues the MMAs behind them.  A stage whose
+// A tile holds only zero codes skips its copies and MMAs.  The staged
 // kernel (gemm_staged_kernel, wider outputs) is described further down.
 // Every wait is bounded; a wait that runs out sets the device error word and
 // the CTA drains and exits.
@@ -64,8 +66,7 @@ constexpr int S_CODES = 3;
 constexpr int A_CODES = BM * KB;                     // 8 KB
 constexpr int A_OPS = BM * BK, B_OPS = BN * BK;      // 16 KB, 32 KB (also the padded E2M1 tile)
 constexpr int DEC_WARP0 = 4, NUM_DEC_WARPS = 16;
-constexpr int SFW_WARP0 = DEC_WARP0 + NUM_DEC_WARPS;  // four scale warps, one per TMEM lane quadrant
-constexpr int NUM_THREADS = (SFW_WARP0 + 4) * 32;
+constexpr int NUM_THREADS = (DEC_WARP0 + NUM_DEC_WARPS) * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SF_COL = 256;  // stage s: A scales at SF_COL + 16 s (4 cols), B at + 4 (8 cols)
 constexpr long long WAIT_LIMIT = 1LL << 31;  // SM clocks, about one second
@@ -90,7 +91,7 @@ struct Plan {
   static constexpr int OFF_SFB = OFF_SFA + S_OPS * BM * 4;         // [S_OPS][TBN] words
   static constexpr int OFF_TAB = OFF_SFB + S_OPS * TBN * 4;  // 8 decode tables (one per mshared), 16 B each
   static constexpr int OFF_BAR = OFF_TAB + 8 * 16;
-  static constexpr int NUM_BARS = 2 * S_CODES_ + 4 * S_OPS + 2;
+  static constexpr int NUM_BARS = 2 * S_CODES_ + 3 * S_OPS + 2;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   // misc: TMEM address, abort flag, a never-set flag, and per operand stage
   // the last k-step (+1) whose A tile held a nonzero block
@@ -117,6 +118,11 @@ struct TcParams {
   const uint8_t* sfa_g;
   const uint8_t* sfb_g;
   int64_t mt, nt, kt;
+  // staged kernel: the limit of every bounded wait (SM clocks), and a test
+  // mode in which the producer issues nothing, so that the first wait of the
+  // MMA thread runs out with no copy or MMA in flight
+  long long wait_limit;
+  int selftest_no_loads;
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a K-major operand tile
@@ -216,10 +222,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* codes_full = bars;
   uint64_t* codes_empty = bars + S_CODES;
-  uint64_t* ops_full = bars + 2 * S_CODES;             // decoders: A operand + scale columns
+  uint64_t* ops_full = bars + 2 * S_CODES;             // decoders: A operand + scale words
   uint64_t* ops_empty = ops_full + S_OPS;              // MMA commit
-  uint64_t* sf_ready = ops_empty + S_OPS;              // decoders: scale words in smem
-  uint64_t* b_full = sf_ready + S_OPS;                 // TMA: native B operand
+  uint64_t* b_full = ops_empty + S_OPS;                // TMA: native B operand
   uint64_t* acc_full = b_full + S_OPS;
   uint64_t* drain = acc_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
@@ -237,9 +242,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(&codes_empty[i], NUM_DEC_WARPS);
     }
     for (int i = 0; i < S_OPS; ++i) {
-      ptx::mbar_init(&ops_full[i], NUM_DEC_WARPS + 4);
+      ptx::mbar_init(&ops_full[i], NUM_DEC_WARPS);
       ptx::mbar_init(&ops_empty[i], 1);
-      ptx::mbar_init(&sf_ready[i], NUM_DEC_WARPS);
       ptx::mbar_init(&b_full[i], 1);
     }
     ptx::mbar_init(acc_full, 1);
@@ -328,6 +332,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t a_addr = ptx::smem_u32(smem + L::OFF_AOPS + s * A_OPS);
           const uint32_t b_addr = ptx::smem_u32(smem + L::OFF_BOPS + s * B_OPS);
           const uint32_t sfa = tmem + SF_COL + 16u * s, sfb = sfa + 4u;
+          const uint32_t sfa_s = ptx::smem_u32(smem + L::OFF_SFA + s * BM * 4);
+          const uint32_t sfb_s = ptx::smem_u32(smem + L::OFF_SFB + s * BN * 4);
+          ptx::tc_cp_32x128b_x4(sfa, ptx::sdesc_noswz(sfa_s, 128, 128));
+          ptx::tc_cp_32x128b_x4(sfb, ptx::sdesc_noswz(sfb_s, 128, 128));
+          if (BN == 256) ptx::tc_cp_32x128b_x4(sfb + 4u, ptx::sdesc_noswz(sfb_s + 512, 128, 128));
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             ptx::mma_mxf8f6f4(tmem, ptx::sdesc_sw128(a_addr + 32u * j), ptx::sdesc_sw128(b_addr + 32u * j),
@@ -339,32 +348,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::tc_commit(acc_full);
       ptx::tc_commit(drain);
       ptx::mbar_wait(drain, 0, WAIT_LIMIT, never);
-    }
-  } else if (warp >= SFW_WARP0) {
-    // ------------------------------------------------------- scale warps
-    // Warp SFW_WARP0 + q stores the stage's scale words (written to shared
-    // memory by the decoders) into TMEM lane quadrant q: every quadrant holds
-    // a full replica (row 32 i + l at lane l, column i).
-    const uint32_t* sfa_s = reinterpret_cast<const uint32_t*>(smem + L::OFF_SFA);
-    const uint32_t* sfb_s = reinterpret_cast<const uint32_t*>(smem + L::OFF_SFB);
-    for (int kt = 0; kt < num_k; ++kt) {
-      const int os = kt % S_OPS, on = kt / S_OPS;
-      if (on > 0) {
-        if (!ptx::mbar_wait(&ops_empty[os], (on - 1) & 1, WAIT_LIMIT, abort_flag)) { flag_error(512u, abort_flag); break; }
-        ptx::tc_fence_after();
-      }
-      if (!ptx::mbar_wait(&sf_ready[os], on & 1, WAIT_LIMIT, abort_flag)) { flag_error(32u, abort_flag); break; }
-      if (*abort_flag) break;
-      const uint32_t base = tmem + ((32u * (uint32_t)(warp & 3)) << 16) + SF_COL + 16u * os;
-      const uint32_t* sa = sfa_s + os * BM;
-      const uint32_t* sb = sfb_s + os * BN;
-      ptx::tmem_st_x4(base, sa[lane], sa[lane + 32], sa[lane + 64], sa[lane + 96]);
-      ptx::tmem_st_x4(base + 4u, sb[lane], sb[lane + 32], sb[lane + 64], sb[lane + 96]);
-      if (BN == 256) ptx::tmem_st_x4(base + 8u, sb[lane + 128], sb[lane + 160], sb[lane + 192], sb[lane + 224]);
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&ops_full[os]);
     }
   } else if (warp >= DEC_WARP0) {
     // ------------------------------------------------------------ decoders
@@ -430,12 +413,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::tc_fence_after();
       }
       if (*abort_flag) { ok = false; break; }
-      // --- this thread's scale words of the stage, to shared memory
+      // --- this thread's scale words of the stage, to shared memory, where
+      // tcgen05.cp takes them: the word of row r of a 128-row group at
+      // index 4 (r % 32) + r / 32
       {
         const int emax = (int)(a_sh & 0xFu) + p.a_ebias;
-        reinterpret_cast<uint8_t*>(sfa_s + os * BM + arow)[ablk] =
+        reinterpret_cast<uint8_t*>(sfa_s + os * BM + 4 * (arow & 31) + (arow >> 5))[ablk] =
             (uint8_t)(kt < a_kend ? (uint32_t)clampi(emax + 126, 1, 254) : 127u);  // 2^(Emax - 1)
-        if (b_scale_thread) sfb_s[os * BN + dt] = bsw;
+        if (b_scale_thread) sfb_s[os * BN + (dt & 128) + 4 * (dt & 31) + ((dt & 127) >> 5)] = bsw;
       }
       // --- A: two 32-blocks (four 16-element chunks) of row arow
       {
@@ -470,13 +455,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           *reinterpret_cast<uint4*>(dst + sw128_off(arow, c0 + 1)) = make_uint4(e[2].x, e[2].y, e[3].x, e[3].y);
         }
       }
-      // the scale words go to TMEM from the scale warps, so no decoder waits
-      // on another within a k-step
+      // operand bytes and scale words reach the async proxy (MMA, tcgen05.cp)
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
         ptx::mbar_arrive(&codes_empty[cs]);
-        ptx::mbar_arrive(&sf_ready[os]);
         ptx::mbar_arrive(&ops_full[os]);
       }
     }
@@ -507,8 +490,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // loop has no decode: per 128-deep k-step the producer issues two tiled TMA
 // loads and two bulk copies of scale words onto one barrier; four scale
 // warps (one per TMEM lane quadrant) store the scale words into TMEM with
-// tcgen05.st, off the tensor pipe (a tcgen05.cp there would serialise with
-// the MMAs), and the MMA thread issues four MMAs once they are in place.
+// tcgen05.st, off the tensor pipe, and the MMA thread issues four MMAs once
+// they are in place.  (Copying them with tcgen05.cp from the MMA thread made
+// this kernel about a fifth slower on every shape measured, although the
+// same copies cost nothing in the fused-decode kernel, which uses them.)
 //
 // Persistent: one CTA per SM walks the 128 x 224 output tiles (M fastest, so
 // the CTAs in flight share B tiles and the whole of A stays in L2).  Two
@@ -650,14 +635,14 @@ __global__ void __maxnreg__(96)
       constexpr uint32_t kStageBytes = A_OPS + (B_NATIVE ? B_OPS_S / 2 : B_OPS_S) + L::SFA_BYTES + L::SFB_BYTES;
       int64_t g = 0;  // k-steps issued by this CTA
       bool stop = false;
-      for (int t = blockIdx.x; t < tiles && !stop; t += gridDim.x) {
+      for (int t = blockIdx.x; t < tiles && !stop && !p.selftest_no_loads; t += gridDim.x) {
         const int mtile = t % mt, rest = t / mt, ntile = rest % nt, bt = rest / nt, bbt = bt / (int)p.b_group;
         const uint8_t* sfa = p.sfa_g + (((int64_t)bt * mt + mtile) * p.kt) * L::SFA_BYTES;
         const uint8_t* sfb = p.sfb_g + (((int64_t)bbt * nt + ntile) * p.kt) * L::SFB_BYTES;
         for (int kt = 0; kt < num_k; ++kt, ++g) {
           const int s = (int)(g % S);
           const uint32_t n = (uint32_t)(g / S);
-          if (n > 0 && !ptx::mbar_wait_spin(&empty[s], (n - 1) & 1, WAIT_LIMIT, abort_flag)) {
+          if (n > 0 && !ptx::mbar_wait_spin(&empty[s], (n - 1) & 1, p.wait_limit, abort_flag)) {
             flag_error(1u, abort_flag);
             stop = true;
             break;
@@ -674,7 +659,7 @@ __global__ void __maxnreg__(96)
       }
       // drain: every issued copy lands before the CTA may exit
       for (int64_t h = (g > S ? g - S : 0); h < g; ++h)
-        ptx::mbar_wait(&full[h % S], (uint32_t)(h / S) & 1, WAIT_LIMIT, never);
+        ptx::mbar_wait(&full[h % S], (uint32_t)(h / S) & 1, p.wait_limit, never);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
@@ -685,7 +670,7 @@ __global__ void __maxnreg__(96)
       bool stop = false;
       for (int t = blockIdx.x; t < tiles && !stop; t += gridDim.x, ++i) {
         const int b = i & 1;
-        if (i >= 2 && !ptx::mbar_wait_spin(&acc_empty[b], (uint32_t)((i >> 1) - 1) & 1, WAIT_LIMIT, abort_flag)) {
+        if (i >= 2 && !ptx::mbar_wait_spin(&acc_empty[b], (uint32_t)((i >> 1) - 1) & 1, p.wait_limit, abort_flag)) {
           flag_error(256u, abort_flag);
           break;
         }
@@ -695,7 +680,7 @@ __global__ void __maxnreg__(96)
           const int s = (int)(g % S);
           const uint32_t n = (uint32_t)(g / S);
           // the scale warps arrive only after the stage's copies landed
-          if (!ptx::mbar_wait_spin(&sf_ready[s], n & 1, WAIT_LIMIT, abort_flag)) {
+          if (!ptx::mbar_wait_spin(&sf_ready[s], n & 1, p.wait_limit, abort_flag)) {
             flag_error(2u, abort_flag);
             stop = true;
             break;
@@ -717,7 +702,7 @@ __global__ void __maxnreg__(96)
         ptx::tc_commit(&acc_full[b]);
       }
       ptx::tc_commit(drain);
-      ptx::mbar_wait(drain, 0, WAIT_LIMIT, never);
+      ptx::mbar_wait(drain, 0, p.wait_limit, never);
     }
   } else if (warp < EPI_WARP0) {
     // -------------------------------------------------------- scale warps
@@ -733,7 +718,7 @@ __global__ void __maxnreg__(96)
       for (int kt = 0; kt < num_k; ++kt, ++g) {
         const int s = (int)(g % S);
         const uint32_t n = (uint32_t)(g / S);
-        if (!ptx::mbar_wait(&full[s], n & 1, WAIT_LIMIT, abort_flag)) {
+        if (!ptx::mbar_wait(&full[s], n & 1, p.wait_limit, abort_flag)) {
           flag_error(32u, abort_flag);
           stop = true;
           break;
@@ -760,7 +745,7 @@ __global__ void __maxnreg__(96)
     int i = 0;
     for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
       const int b = i & 1;
-      if (*abort_flag || !ptx::mbar_wait(&acc_full[b], (uint32_t)(i >> 1) & 1, WAIT_LIMIT, abort_flag)) {
+      if (*abort_flag || !ptx::mbar_wait(&acc_full[b], (uint32_t)(i >> 1) & 1, p.wait_limit, abort_flag)) {
         if (!*abort_flag) flag_error(16u, abort_flag);
         break;
       }
@@ -908,18 +893,6 @@ cudaError_t launch_tc(const CUtensorMap& ma, const CUtensorMap& mb, const CUtens
 
 }  // namespace
 
-bool make_rows128_map(CUtensorMap* m, const void* base, int64_t rows, uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn || rows < 1 || (reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
-  const cuuint64_t dims[2] = {128, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {128};
-  const cuuint32_t box[2] = {128, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 namespace {
 
 TcParams make_params(const mix_gemm_desc_t& d) {
@@ -931,6 +904,8 @@ TcParams make_params(const mix_gemm_desc_t& d) {
   p.c = d.c; p.ldc = d.ldc; p.cbs = d.c_batch_stride;
   p.epi = (int)d.epi; p.epi_ebias = d.epi_ebias; p.epi_flags = d.epi_flags;
   p.out_codes = d.out_codes; p.out_shared = d.out_shared; p.out_ld = d.out_ld; p.out_bs = d.out_batch_stride;
+  p.wait_limit = WAIT_LIMIT;
+  p.selftest_no_loads = 0;
   return p;
 }
 
@@ -1077,6 +1052,29 @@ size_t gemm_tc_prepare_b_bytes(const mix_gemm_desc_t& d) {
 cudaError_t launch_gemm_tc_prepare_b(const mix_gemm_desc_t& d, void* prepared, cudaStream_t st) {
   if (want_staged(d)) return launch_expand_b(d, rebase_b(staged_plan(d)), align_ws(prepared), st);
   return launch_expand_b(d, staged_plan_b_only(d), align_ws(prepared), st);
+}
+
+size_t selftest_ws_bytes() { return (size_t)(A_OPS + B_OPS_S + 2048) + kStagedAlign; }
+
+// One staged-kernel launch on a single 128 x 224 tile whose producer issues
+// no copy: the MMA thread's wait for the first stage runs out after
+// `limit_cycles`, sets the device error word and raises the CTA's abort flag;
+// every other role sees the flag, the CTA frees its TMEM and exits.  The
+// tensor maps point into `ws` (never read: nothing is loaded).
+cudaError_t launch_selftest_wait_timeout(void* ws, long long limit_cycles, cudaStream_t st) {
+  unsigned char* base = align_ws(ws);
+  CUtensorMap ma, mb;
+  if (!make_e4m3_map(&ma, base, BK, BM, 1, BM) || !make_e4m3_map(&mb, base + A_OPS, BK, BNS, 1, BNS))
+    return cudaErrorInvalidValue;
+  TcParams p{};
+  p.M = BM; p.N = BNS; p.K = BK; p.batch = 1; p.b_group = 1;
+  p.epi = MIX_EPI_NONE;
+  p.sfa_g = base + A_OPS + B_OPS_S;
+  p.sfb_g = base + A_OPS + B_OPS_S + 512;
+  p.mt = 1; p.nt = 1; p.kt = 1;
+  p.wait_limit = limit_cycles;
+  p.selftest_no_loads = 1;
+  return launch_staged<false>(ma, mb, ma, p, dim3(1), st);
 }
 
 cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, void* ws, size_t ws_bytes, cudaStream_t st,

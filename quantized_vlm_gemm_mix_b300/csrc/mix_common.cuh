@@ -58,14 +58,15 @@ __device__ __forceinline__ uint32_t bf16_to_f32_bits(uint32_t h) { return h << 1
 // Returns false for a zero or subnormal maximum: with Emax >= ebias >= -100
 // every element of such a (sub-)block quantises to the zero code, which is the
 // canonical all-zero block.
+// The rounding adds 2^19 - 1 plus the kept lowest mantissa bit below bit 20
+// (ties to even), so a carry out of the mantissa raises the exponent field
+// by itself (checked against the compare form for every normal key).
 __device__ __forceinline__ bool max_exp_mant(uint32_t key, int* f, int* m3) {
   if (key < 0x00800000u) { *f = 0; *m3 = 0; return false; }
   if (key >= 0x7F800000u) { *f = 1 << 20; *m3 = 0; return true; }
-  uint32_t q = (key >> 20) & 7u;
-  const uint32_t r = key & 0xFFFFFu;
-  q += (r > 0x80000u || (r == 0x80000u && (q & 1u))) ? 1u : 0u;
-  *f = (int)(key >> 23) - 127 + (int)(q >> 3);
-  *m3 = (int)(q & 7u);
+  const uint32_t t = key + 0x7FFFFu + ((key >> 20) & 1u);
+  *f = (int)(t >> 23) - 127;
+  *m3 = (int)((t >> 20) & 7u);
   return true;
 }
 
@@ -219,28 +220,43 @@ struct MixBlk2 {
   uint32_t capn; // what the positive lanes' clamp adds: 128 with the recycled -0 (cap 7), else 0 (cap 6)
 };
 
-// The packed-step constants of a (sub-)block straight from (Emax, mshared):
-// they are the top halves of mix_blk's t0, zn, zp, that is, in units of the top
-// half, T = 128 Emax + 16192 + 24 m (m < 3, where 3 M < 32) or 16224 + 12 m,
-// ZN = 128 Emax + 15360 + 16 m, ZP = ZN - 128 with the recycled -0 (checked
-// against mix_blk for every Emax in [-100, 115] and every m).
-__device__ __forceinline__ MixBlk2 mix_blk2_direct(int emax, int ms, bool asym) {
+// The packed-step constants of a (sub-)block are the top halves of mix_blk's
+// t0, zn, zp: in units of the top half, T = 128 Emax + 16192 + 24 m (m < 3,
+// where 3 M < 32) or 16224 + 12 m, ZN = 128 Emax + 15360 + 16 m, ZP = ZN - 128
+// with the recycled -0 (checked against mix_blk for every Emax in [-100, 115]
+// and every m).  They split into a per-block part (Emax) and a per-sub-block
+// part (mshared), linear in both -- T's mshared offset is 24 m - max(12 m -
+// 32, 0) -- exact modulo 2^32 because every lane's final value lies in
+// [0, 2^16) (checked against the formulas above for every Emax, m and zero
+// mode).
+struct MixBlkBase {
+  uint32_t b1;    // (0x807F + 16192 + 128 Emax) in both lanes
+  uint32_t b2;    // (0x8000 - 15360 - 128 Emax) in both lanes
+  uint32_t ak;    // 128 in both lanes with the recycled -0, else 0
+  uint32_t capn;
+};
+__device__ __forceinline__ MixBlkBase mix_blk_base(int emax, bool asym) {
+  MixBlkBase b;
   const int e7 = emax * 128;
-  const int T = e7 + (ms < 3 ? 16192 + 24 * ms : 16224 + 12 * ms);
-  const int ZN = e7 + 15360 + 16 * ms;
-  const int ZP = asym ? ZN - 128 : ZN;
+  b.b1 = (uint32_t)(0x807F + 16192 + e7) * 0x00010001u;
+  b.b2 = (uint32_t)(0x8000 - 15360 - e7) * 0x00010001u;
+  b.ak = asym ? 0x00800080u : 0u;
+  b.capn = asym ? 0x00800080u : 0u;
+  return b;
+}
+__device__ __forceinline__ MixBlk2 mix_blk2_lin(const MixBlkBase& b, int ms) {
   MixBlk2 q;
-  q.c1 = (uint32_t)(0x807F + T) * 0x00010001u;
-  q.kp2 = (uint32_t)(0x8000 - ZP) * 0x00010001u;
-  q.kn2 = (uint32_t)(0x8000 - ZN) * 0x00010001u;
-  q.capn = asym ? 0x00800080u : 0u;
+  const uint32_t m12 = (uint32_t)max(12 * ms - 32, 0);
+  q.c1 = b.b1 + (uint32_t)ms * (24u * 0x00010001u) - m12 * 0x00010001u;
+  q.kn2 = b.b2 - (uint32_t)ms * (16u * 0x00010001u);
+  q.kp2 = q.kn2 + b.ak;
+  q.capn = b.capn;
   return q;
 }
 
-// Codes of the two elements of word w, at bits 0..3 (low element) and
-// 16..19 (high element); every other bit zero.
-__device__ __forceinline__ uint32_t mix_code_pair(uint32_t w, const MixBlk2& q) {
-  const uint32_t a = w & 0x7FFF7FFFu;
+// Codes of the two elements of word w (magnitudes a = w & 0x7FFF7FFF), at
+// bits 0..3 (low element) and 16..19 (high element); every other bit zero.
+__device__ __forceinline__ uint32_t mix_code_pair(uint32_t w, uint32_t a, const MixBlk2& q) {
   const uint32_t s = prmt_sel(w, w, 0xBB99u);              // 0xFFFF in negative lanes
   uint32_t x = vmax_u16x2(q.c1 - a, 0x80008000u);
   x = vmin_u16x2(x, 0x837F837Fu | (~s & q.capn));
@@ -251,12 +267,12 @@ __device__ __forceinline__ uint32_t mix_code_pair(uint32_t w, const MixBlk2& q) 
   return (code & m) | (0x00070007u & ~m);
 }
 
-// Eight codes of words w[0..3] as one 32-bit word (element 2j in the low
-// nibble of byte j): two pairs meet in a half-word by a multiply-add and a
-// shift, two half-words in a word by a byte permute.
-__device__ __forceinline__ uint32_t mix_codes8_packed(const uint32_t* w, const MixBlk2& q) {
-  uint32_t p0 = mix_code_pair(w[0], q) + mix_code_pair(w[1], q) * 256u;
-  uint32_t p1 = mix_code_pair(w[2], q) + mix_code_pair(w[3], q) * 256u;
+// Eight codes of words w[0..3] (magnitudes a[0..3]) as one 32-bit word
+// (element 2j in the low nibble of byte j): two pairs meet in a half-word by
+// a multiply-add and a shift, two half-words in a word by a byte permute.
+__device__ __forceinline__ uint32_t mix_codes8_packed(const uint32_t* w, const uint32_t* a, const MixBlk2& q) {
+  uint32_t p0 = mix_code_pair(w[0], a[0], q) + mix_code_pair(w[1], a[1], q) * 256u;
+  uint32_t p1 = mix_code_pair(w[2], a[2], q) + mix_code_pair(w[3], a[3], q) * 256u;
   p0 |= p0 >> 12;
   p1 |= p1 >> 12;
   return prmt_sel(p0, p1, 0x5410u);
@@ -268,8 +284,8 @@ __device__ __forceinline__ uint32_t mix_codes8_packed(const uint32_t* w, const M
 // block's (they set Emax and mshared, whose rounding needs every mantissa
 // bit).
 template <int TYPE>
-__device__ __forceinline__ void mix_block32_packed(const uint32_t* w, const uint32_t* ks, uint32_t kb, int ebias,
-                                                   bool asym, uint4& cw, uint32_t& sh) {
+__device__ __forceinline__ void mix_block32_packed(const uint32_t* w, const uint32_t* a, const uint32_t* ks,
+                                                   uint32_t kb, int ebias, bool asym, uint4& cw, uint32_t& sh) {
   cw = make_uint4(0x77777777u, 0x77777777u, 0x77777777u, 0x77777777u);
   sh = 0;
   int f, m3;
@@ -278,7 +294,8 @@ __device__ __forceinline__ void mix_block32_packed(const uint32_t* w, const uint
   uint32_t wd[4];
   uint32_t m3bits = 0;
   bool all_zero = true;
-  const MixBlk2 q1 = mix_blk2_direct(emax, m3, asym);
+  const MixBlkBase base = mix_blk_base(emax, asym);
+  const MixBlk2 q1 = mix_blk2_lin(base, m3);
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     int ms = m3;
@@ -286,9 +303,9 @@ __device__ __forceinline__ void mix_block32_packed(const uint32_t* w, const uint
     if (TYPE == 2) {
       int fs;
       if (!max_exp_mant(ks[s], &fs, &ms)) ms = 0;
-      q = mix_blk2_direct(emax, ms, asym);
+      q = mix_blk2_lin(base, ms);
     }
-    const uint32_t word = mix_codes8_packed(w + 4 * s, q);
+    const uint32_t word = mix_codes8_packed(w + 4 * s, a + 4 * s, q);
     wd[s] = word;
     const bool z = word == 0x77777777u;
     all_zero &= z;
@@ -329,7 +346,7 @@ __device__ __forceinline__ void mix_block32_bf16(const uint32_t* w, int ebias, b
     mix_block32<TYPE>(u, ebias, asym, cw, sh);
     return;
   }
-  mix_block32_packed<TYPE>(w, ks, kb, ebias, asym, cw, sh);
+  mix_block32_packed<TYPE>(w, a, ks, kb, ebias, asym, cw, sh);
 }
 
 // Algorithm 1 on one block of 32 fp32 elements (bit patterns; u may be
@@ -352,10 +369,13 @@ __device__ __forceinline__ void mix_block32_f32(uint32_t* u, int ebias, bool asy
     mix_block32<TYPE>(u, ebias, asym, cw, sh);
     return;
   }
-  uint32_t w[16];
+  uint32_t w[16], a[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) w[j] = __byte_perm(u[2 * j], u[2 * j + 1], 0x7632);
-  mix_block32_packed<TYPE>(w, ks, kb, ebias, asym, cw, sh);
+  for (int j = 0; j < 16; ++j) {
+    w[j] = __byte_perm(u[2 * j], u[2 * j + 1], 0x7632);
+    a[j] = w[j] & 0x7FFF7FFFu;
+  }
+  mix_block32_packed<TYPE>(w, a, ks, kb, ebias, asym, cw, sh);
 }
 
 // Division by a runtime constant d (1 <= d < 2^31) of 32-bit numerators with

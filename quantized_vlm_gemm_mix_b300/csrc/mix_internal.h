@@ -101,14 +101,9 @@ size_t ksmooth_noalloc_scratch_bytes();
 cudaError_t launch_ksmooth_noalloc(const void* k, bool bf16, int64_t tokens, int heads, int head_dim,
                                    int64_t ld, float* mean, int mode, float* k_out, cudaStream_t st);
 
-// A contiguous byte range viewed as rows of 128 bytes (`rows` of them), read
-// by 2-D TMA boxes of 128 bytes x box_rows with the 128-byte swizzle: 16-byte
-// unit u of box row r lands at unit u ^ (r % 8) of that row in shared memory.
-bool make_rows128_map(CUtensorMap* m, const void* base, int64_t rows, uint32_t box_rows);
-
-// Device error word (bounded waits): the matmul's, and the quantiser's (its
-// TMA waits), read (and cleared) separately.
+// Device error word (bounded waits), and the launch that makes one run out.
 cudaError_t read_device_error(unsigned* word, bool clear);
-cudaError_t read_quant_error(unsigned* word, bool clear);
+size_t selftest_ws_bytes();
+cudaError_t launch_selftest_wait_timeout(void* ws, long long limit_cycles, cudaStream_t st);
 
 }  // namespace mixk

@@ -17,7 +17,6 @@
 
 #include "mix_common.cuh"
 #include "mix_internal.h"
-#include "tc_ptx.cuh"
 
 namespace mixk {
 
@@ -130,122 +129,6 @@ __global__ void __launch_bounds__(kThreads, 4) mix_quantize_kernel(
     if (TYPE == 1) static_cast<uint8_t*>(shared)[g] = (uint8_t)sh;
     else static_cast<uint16_t*>(shared)[g] = (uint16_t)sh;
   }
-}
-
-// The same quantiser for a contiguous x (row stride == k), fed by TMA.
-// Each CTA walks chunks of 256 blocks (16 KB of bf16 / 32 KB of fp32) through
-// a ring of shared-memory stages: thread 0 keeps the next stages' 2-D TMA
-// loads in flight while the CTA codes the current one, so the loads run ahead
-// of the arithmetic at no register cost, and the 128-byte swizzle makes every
-// thread's 16-byte shared-memory reads of its own block conflict-free.  The
-// per-block arithmetic is the one above, so the codes are identical.  Blocks
-// past the last whole 128-byte row of x (at most one bf16 block) are read
-// from global memory directly.
-constexpr int kTmaChunk = 256;  // blocks per chunk: one per thread
-__device__ unsigned g_quant_error;  // bit 0: a TMA wait of the quantiser ran out
-
-template <bool BF16>
-struct TmaQ {
-  static constexpr int kRows = BF16 ? 128 : 256;  // 128-byte rows per chunk
-  static constexpr int kStageBytes = kRows * 128;
-  static constexpr int kStages = BF16 ? 4 : 3;
-  static constexpr int kMinCtas = BF16 ? 3 : 2;
-  static constexpr int kSmem = kStages * kStageBytes + 1024 + 64;
-};
-
-template <bool BF16, int TYPE, bool DEV_EB>
-__global__ void __launch_bounds__(kTmaChunk, TmaQ<BF16>::kMinCtas) mix_quantize_tma_kernel(
-    const __grid_constant__ CUtensorMap tmap, const void* __restrict__ x, int64_t total, int64_t tma_blocks,
-    int ebias, int asym, uint8_t* __restrict__ codes, void* __restrict__ shared,
-    const int* __restrict__ ebias_dev) {
-  using Q = TmaQ<BF16>;
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Q::kStages * Q::kStageBytes);
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + Q::kStages * Q::kStageBytes + 8 * Q::kStages);
-  if (DEV_EB) ebias = *ebias_dev;
-  const int tid = threadIdx.x;
-  const int64_t nchunks = (total + kTmaChunk - 1) / kTmaChunk;
-  const int64_t grid = gridDim.x;
-  int issued = 0;  // thread 0: chunks of this CTA whose loads were issued
-  if (tid == 0) {
-    for (int i = 0; i < Q::kStages; ++i) ptx::mbar_init(&full[i], 1);
-    flags[0] = 0;  // abort (never raised: waits here are the last ones)
-    flags[1] = 0;
-    ptx::fence_mbar_init();
-    ptx::prefetch_tmap(&tmap);
-    for (int i = 0; i < Q::kStages; ++i) {
-      const int64_t c = blockIdx.x + i * grid;
-      if (c >= nchunks) break;
-      ptx::mbar_arrive_expect_tx(&full[i], Q::kStageBytes);
-      ptx::tma_load_2d(smem + i * Q::kStageBytes, &tmap, &full[i], 0, (int)(c * Q::kRows));
-      ++issued;
-    }
-  }
-  __syncthreads();
-  int done = 0;  // chunks consumed
-  for (int64_t c = blockIdx.x; c < nchunks; c += grid, ++done) {
-    const int s = done % Q::kStages;
-    const bool ok = ptx::mbar_wait(&full[s], (uint32_t)(done / Q::kStages) & 1u, 1LL << 31, flags);
-    const int64_t g = c * kTmaChunk + tid;
-    const bool mine = g < total;
-    const unsigned char* st = smem + s * Q::kStageBytes;
-    uint32_t w[BF16 ? 16 : 32];
-    if (mine && g < tma_blocks) {
-      if (BF16) {
-        const int r = tid >> 1, h = (tid & 1) * 4;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 v = *reinterpret_cast<const uint4*>(st + r * 128 + (((h + j) ^ (r & 7)) << 4));
-          w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
-        }
-      } else {
-        const int r = tid;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 v = *reinterpret_cast<const uint4*>(st + r * 128 + ((j ^ (r & 7)) << 4));
-          w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
-        }
-      }
-    } else if (mine) {  // past the last whole 128-byte row
-      const uint4* p = reinterpret_cast<const uint4*>(static_cast<const char*>(x) + g * 32 * (BF16 ? 2 : 4));
-#pragma unroll
-      for (int j = 0; j < (BF16 ? 4 : 8); ++j) {
-        const uint4 v = p[j];
-        w[4 * j] = v.x; w[4 * j + 1] = v.y; w[4 * j + 2] = v.z; w[4 * j + 3] = v.w;
-      }
-    }
-    if (__syncthreads_or(!ok)) {  // every thread has read stage s (or a wait ran out)
-      if (tid == 0) atomicOr(&g_quant_error, 1u);
-      break;
-    }
-    if (tid == 0) {
-      const int64_t cn = c + (int64_t)Q::kStages * grid;
-      if (cn < nchunks) {
-        ptx::mbar_arrive_expect_tx(&full[s], Q::kStageBytes);
-        ptx::tma_load_2d(smem + s * Q::kStageBytes, &tmap, &full[s], 0, (int)(cn * Q::kRows));
-        ++issued;
-      }
-    }
-    if (mine) {
-      uint4 cw;
-      uint32_t sh;
-      if (BF16) {
-        mix_block32_bf16<TYPE>(w, ebias, asym != 0, cw, sh);
-      } else {
-        mix_block32<TYPE>(w, ebias, asym != 0, cw, sh);
-      }
-      __stcs(reinterpret_cast<uint4*>(codes + g * 16), cw);
-      if (TYPE == 1) static_cast<uint8_t*>(shared)[g] = (uint8_t)sh;
-      else static_cast<uint16_t*>(shared)[g] = (uint16_t)sh;
-    }
-  }
-  // every issued load has landed before the CTA exits (only an early exit
-  // leaves any outstanding)
-  if (tid == 0)
-    for (int i = done; i < issued; ++i)
-      ptx::mbar_wait(&full[i % Q::kStages], (uint32_t)(i / Q::kStages) & 1u, 1LL << 31, flags + 1);
 }
 
 // NVFP4 (a comparison format: 16-element blocks of E2M1, an E4M3 block scale
@@ -688,64 +571,11 @@ int grid_for(int64_t quads) {
 
 }  // namespace
 
-cudaError_t read_quant_error(unsigned* word, bool clear) {
-  cudaError_t e = cudaMemcpyFromSymbol(word, g_quant_error, sizeof(unsigned));
-  if (e != cudaSuccess || !clear) return e;
-  const unsigned z = 0;
-  return cudaMemcpyToSymbol(g_quant_error, &z, sizeof(unsigned));
-}
-
-namespace {
-
-template <bool BF16, int TYPE>
-cudaError_t launch_mix_tma(const CUtensorMap& m, const void* x, int64_t total, int64_t tma_blocks, int ebias,
-                           bool asym, uint8_t* codes, void* shared, const int* ebias_dev, cudaStream_t st) {
-  using Q = TmaQ<BF16>;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(mix_quantize_tma_kernel<BF16, TYPE, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(mix_quantize_tma_kernel<BF16, TYPE, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, Q::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
-  const int64_t nchunks = (total + kTmaChunk - 1) / kTmaChunk;
-  const int64_t cap = (int64_t)num_sms() * Q::kMinCtas;
-  const int grid = (int)(nchunks < cap ? nchunks : cap);
-  if (ebias_dev != nullptr)
-    mix_quantize_tma_kernel<BF16, TYPE, true><<<grid, kTmaChunk, Q::kSmem, st>>>(
-        m, x, total, tma_blocks, ebias, asym ? 1 : 0, codes, shared, ebias_dev);
-  else
-    mix_quantize_tma_kernel<BF16, TYPE, false><<<grid, kTmaChunk, Q::kSmem, st>>>(
-        m, x, total, tma_blocks, ebias, asym ? 1 : 0, codes, shared, ebias_dev);
-  return cudaGetLastError();
-}
-
-}  // namespace
-
 cudaError_t launch_mix_quantize(const void* x, bool bf16, int64_t rows, int64_t k, int64_t ld,
                                 int type, int ebias, bool asym, uint8_t* codes, void* shared,
                                 cudaStream_t st, const int* ebias_dev) {
   const int64_t nb = k / 32;
   if (rows * nb >= (int64_t)UINT32_MAX) return cudaErrorInvalidValue;  // 32-bit block index
-  // contiguous rows: the TMA-fed kernel
-  const int64_t total = rows * nb;
-  const int64_t rows128 = total * 32 * (bf16 ? 2 : 4) / 128;
-  if ((ld == k || rows == 1) && rows128 >= 1 && rows128 < (int64_t)INT32_MAX - 512) {
-    CUtensorMap m;
-    if (make_rows128_map(&m, x, rows128, bf16 ? TmaQ<true>::kRows : TmaQ<false>::kRows)) {
-      const int64_t tma_blocks = rows128 * 128 / (32 * (bf16 ? 2 : 4));
-      if (bf16)
-        return type == 1 ? launch_mix_tma<true, 1>(m, x, total, tma_blocks, ebias, asym, codes, shared, ebias_dev, st)
-                         : launch_mix_tma<true, 2>(m, x, total, tma_blocks, ebias, asym, codes, shared, ebias_dev, st);
-      return type == 1 ? launch_mix_tma<false, 1>(m, x, total, tma_blocks, ebias, asym, codes, shared, ebias_dev, st)
-                       : launch_mix_tma<false, 2>(m, x, total, tma_blocks, ebias, asym, codes, shared, ebias_dev, st);
-    }
-  }
   int64_t gb = (rows * nb + kThreads - 1) / kThreads;
   if (gb > (int64_t)num_sms() * 4) gb = (int64_t)num_sms() * 4;  // one wave of 4 resident CTAs per SM
   const int grid = (int)(gb > 0 ? gb : 1);

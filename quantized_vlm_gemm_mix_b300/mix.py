@@ -34,8 +34,9 @@ EXPORTS = ["mix_codes_bytes", "mix_shared_bytes", "mx_scales_bytes", "mix_quanti
            "mix_dequantize", "mx_dequantize", "mix_mx_gemm_workspace_bytes", "mix_mx_gemm",
            "mix_mx_gemm_prepare_b_bytes", "mix_mx_gemm_prepare_b",
            "ksmooth_workspace_bytes", "ksmooth_kv", "ksmooth_kv_noalloc", "mix_status_str", "mix_device_error",
-           "mix_version"]
+           "mix_selftest_wait_timeout", "mix_version"]
 KSMOOTH_NOALLOC_SCRATCH_BYTES = 2 << 20
+MIX_SELFTEST_WORKSPACE_BYTES = 64 << 10
 
 
 class MixError(RuntimeError):
@@ -106,6 +107,7 @@ def _load():
         "ksmooth_kv_noalloc": (I, [P, I, I64, I, I, I64, P, I, P, P]),
         "mix_status_str": (ctypes.c_char_p, [I]),
         "mix_device_error": (I, [ctypes.POINTER(ctypes.c_uint), I]),
+        "mix_selftest_wait_timeout": (I, [P, S, P]),
         "mix_version": (I, []),
     }
     for name, (res, args) in sig.items():

@@ -117,6 +117,14 @@ def test_staged_gemm_workspace_size_and_check(mix):
     assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == want
     assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_WORKSPACE
     assert L.mix_mx_gemm(ctypes.byref(d), ctypes.c_void_p(0x600000), want - 1, None) == mix.MIX_ERR_WORKSPACE
+    # prepared once, B's part (expanded plane and scale words) moves out of the workspace
+    assert L.mix_mx_gemm_prepare_b_bytes(ctypes.byref(d)) == kib(N * kp) + kib(nt * kt * 1024) + 1024
+    assert L.mix_mx_gemm_prepare_b(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_WORKSPACE
+    d.b_prepared = 0x700000
+    assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == kib(M * kp) + kib(mt * kt * 512) + 1024
+    d.b_prepared = 0x700008                      # not 16-byte aligned
+    assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) == 0
+    d.b_prepared = None
     # MXFP4 with K % 128 == 0 is read in place: only its scale words are staged
     M, N, K, B, G = 160, 4096, 512, 6, 3
     d = _staged_desc(mix, M, N, K, mix.MX_FP4_E2M1, batch=B, b_group=G)
@@ -134,6 +142,16 @@ def test_staged_gemm_workspace_size_and_check(mix):
     assert L.mix_mx_gemm_workspace_bytes(ctypes.byref(d)) > 0
     d.algo = 5
     assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_INVALID_ARG
+
+
+def test_selftest_validation(mix):
+    """The bounded-wait self-test refuses a missing, short or misaligned
+    workspace before launching anything."""
+    L = mix.lib
+    assert L.mix_selftest_wait_timeout(None, 0, None) == mix.MIX_ERR_WORKSPACE
+    assert L.mix_selftest_wait_timeout(ctypes.c_void_p(0x600000), 1024, None) == mix.MIX_ERR_WORKSPACE
+    assert L.mix_selftest_wait_timeout(ctypes.c_void_p(0x600004), mix.MIX_SELFTEST_WORKSPACE_BYTES,
+                                       None) == mix.MIX_ERR_ALIGN
 
 
 def test_decode_attention_validation(mix):

@@ -31,7 +31,7 @@ def test_plane_bytes_are_the_library_plane_sizes(mix, rows, k):
 def test_step_table_flops_and_shapes(small):
     rows = bench.step_table(small)
     names = [r[0] for r in rows]
-    assert len(names) == len(set(names)) == 25
+    assert len(names) == len(set(names)) == 20
     for name, nbytes, flops, launches, cpu in rows:
         assert nbytes > 0 and launches >= 1
         m = re.fullmatch(r"gemm_\w+?_(\d+)x(\d+)x(\d+)", name)
@@ -45,6 +45,20 @@ def test_step_table_flops_and_shapes(small):
             assert flops == 2.0 * H * M * N * K
         if name.startswith(("mix_quantize", "mx_quantize", "ksmooth")):
             assert flops == 0.0
+        m = re.fullmatch(r"decode_attention_(\d+)x(\d+)x(\d+)x(\d+)", name)
+        if m:                                        # kv heads x group x cache tokens x head_dim
+            HK, G, TC, D = map(int, m.groups())
+            assert flops == 2.0 * 2.0 * HK * G * TC * D          # q K'^T and P V
+            assert launches == 2
+
+
+def test_decode_attention_bytes():
+    """The fused decode step reads the MXINT4 K' cache (64 code and 4 scale
+    bytes per token and KV head) and the V planes along tokens once, plus q,
+    the new key and the mean, and writes the appended row and the output."""
+    TC, HQ, HK, D = 8192, 28, 4, 128
+    want = TC * HK * 68 + HK * D * (TC // 2 + TC // 32) + HQ * D * 2 + HK * D * 6 + HK * 68 + HQ * D * 4
+    assert bench.decode_attention_bytes(TC, HQ, HK, D) == want
 
 
 def test_ksmooth_reads_keys_once():
