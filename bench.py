@@ -858,6 +858,31 @@ def single_call(args):
         mix.prepare_b(d)
         ws = torch.empty(max(16, mix.mix_mx_gemm_workspace_bytes(d)), dtype=torch.uint8, device=dev)
         fn = lambda: mix.mix_mx_gemm(d, ws)
+    elif name.startswith("bmm_pv_"):
+        # a causal softmax P (made by torch: the softmax is outside the
+        # library) in MiX-4.5b at ebias -15, V in MXINT4 along tokens
+        T, HQ, HK, D = g["T"], g["HQ"], g["HK"], g["D"]
+        gen = torch.Generator(device=dev).manual_seed(0)
+        P = torch.empty((HQ, T, T), dtype=torch.bfloat16, device=dev)
+        causal = torch.ones((T, T), dtype=torch.bool, device=dev).tril()
+        for h in range(HQ):
+            sc = torch.randn((T, T), device=dev, generator=gen) * 3.0
+            P[h] = torch.softmax((sc / math.sqrt(D)).masked_fill(~causal, float("-inf")), dim=-1).to(torch.bfloat16)
+        del causal, sc
+        pc = torch.empty((HQ * T, T // 2), dtype=torch.uint8, device=dev)
+        ps = torch.empty((HQ * T, T // 32), dtype=torch.int16, device=dev)
+        mix.mix_quantize(P, HQ * T, T, T, T2, -15, 1, pc, ps)
+        del P
+        _, _, v = synth.attention_qkv(0, T, HQ, HK, D)
+        vb = bf16(synth.to_bf16_bits(v).reshape(T, HK * D))
+        vqc = torch.empty((HK, D, T // 2), dtype=torch.uint8, device=dev)
+        vqs = torch.empty((HK, D, T // 32), dtype=torch.uint8, device=dev)
+        mix.mx_quantize(vb, T, HK * D, HK * D, 0, INT4, 0, vqc, vqs)
+        O = torch.empty((HQ, T, D), dtype=torch.float32, device=dev)
+        d = mix.gemm_desc(T, D, T, pc, ps, T2, -15, vqc, vqs, INT4, c=O, batch=HQ, b_group=HQ // HK,
+                          algo=mix.MIX_GEMM_TCGEN05)
+        ws = torch.empty(max(16, mix.mix_mx_gemm_workspace_bytes(d)), dtype=torch.uint8, device=dev)
+        fn = lambda: mix.mix_mx_gemm(d, ws)
     elif name.startswith("mix_quantize_t") and name.endswith(f"_{M}x{DM}"):
         t = T1 if name.startswith("mix_quantize_t1") else T2
         x = bf16(synth.to_bf16_bits(synth.vlm_activations(0, 1, M, DM, visual_rows=(3 * M) // 4)))
@@ -865,7 +890,8 @@ def single_call(args):
         sh = torch.empty((M, DM // 32), dtype=torch.uint8 if t == T1 else torch.int16, device=dev)
         fn = lambda: mix.mix_quantize(x, M, DM, DM, t, -8, 1, c, sh)
     else:
-        raise SystemExit(f"--call supports the prefill matmuls and the MiX quantisers of the sweep, not {name}")
+        raise SystemExit(f"--call supports the prefill matmuls, the attention P.V and the MiX quantisers of the "
+                         f"sweep, not {name}")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # larger than L2
     times = []
     for i in range(args.warmup + args.steps):
