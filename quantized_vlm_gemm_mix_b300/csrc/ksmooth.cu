@@ -159,9 +159,9 @@ __global__ void __launch_bounds__(kThreads) ksmooth_apply_kernel(
 int64_t ksmooth_chunks(int64_t tokens, int64_t C) {
   const int64_t tiles = (C + 255) / 256;
   int64_t want = (4 * (int64_t)num_sms() + tiles - 1) / tiles;  // about four CTAs per SM
-  const int64_t by_len = (tokens + 31) / 32;                    // at least 32 tokens per chunk
+  const int64_t by_len = (tokens + 15) / 16;                    // at least 16 tokens per chunk
   if (want > by_len) want = by_len;
-  if (want > 32) want = 32;  // keeps the finalize's chain short
+  if (want > 128) want = 128;  // the finalize adds at most 16 rows per thread, four loads in flight
   return want > 0 ? want : 1;
 }
 
