@@ -883,6 +883,25 @@ def single_call(args):
                           algo=mix.MIX_GEMM_TCGEN05)
         ws = torch.empty(max(16, mix.mix_mx_gemm_workspace_bytes(d)), dtype=torch.uint8, device=dev)
         fn = lambda: mix.mix_mx_gemm(d, ws)
+    elif name.startswith("bmm_qk_"):
+        # Q (MiX-4.5b, rows (token, head)) x K' (MXINT4 along head_dim), GQA,
+        # both read in place with head strides; fp32 scores out
+        T, HQ, HK, D = g["T"], g["HQ"], g["HK"], g["D"]
+        q, k, _ = synth.attention_qkv(0, T, HQ, HK, D)
+        qd = bf16(synth.to_bf16_bits(q).reshape(T, HQ * D))
+        kd = bf16(synth.to_bf16_bits(k).reshape(T, HK * D))
+        del q, k
+        qc = torch.empty((T * HQ, D // 2), dtype=torch.uint8, device=dev)
+        qs = torch.empty((T * HQ, D // 32), dtype=torch.int16, device=dev)
+        mix.mix_quantize(qd, T * HQ, D, D, T2, -8, 1, qc, qs)
+        kc = torch.empty((T * HK, D // 2), dtype=torch.uint8, device=dev)
+        ks = torch.empty((T * HK, D // 32), dtype=torch.uint8, device=dev)
+        mix.mx_quantize(kd.float(), T * HK, D, D, 1, INT4, 0, kc, ks)
+        S = torch.empty((HQ, T, T), dtype=torch.float32, device=dev)
+        d = mix.gemm_desc(T, T, D, qc, qs, T2, -8, kc, ks, INT4, c=S, batch=HQ, b_group=HQ // HK, a_ld=HQ * D,
+                          a_batch_stride=D, b_ld=HK * D, b_batch_stride=D, algo=mix.MIX_GEMM_TCGEN05)
+        ws = torch.empty(max(16, mix.mix_mx_gemm_workspace_bytes(d)), dtype=torch.uint8, device=dev)
+        fn = lambda: mix.mix_mx_gemm(d, ws)
     elif name.startswith("mix_quantize_t") and name.endswith(f"_{M}x{DM}"):
         t = T1 if name.startswith("mix_quantize_t1") else T2
         x = bf16(synth.to_bf16_bits(synth.vlm_activations(0, 1, M, DM, visual_rows=(3 * M) // 4)))
@@ -890,8 +909,8 @@ def single_call(args):
         sh = torch.empty((M, DM // 32), dtype=torch.uint8 if t == T1 else torch.int16, device=dev)
         fn = lambda: mix.mix_quantize(x, M, DM, DM, t, -8, 1, c, sh)
     else:
-        raise SystemExit(f"--call supports the prefill matmuls, the attention P.V and the MiX quantisers of the "
-                         f"sweep, not {name}")
+        raise SystemExit(f"--call supports the prefill matmuls, the attention Q.K'^T and P.V and the MiX "
+                         f"quantisers of the sweep, not {name}")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # larger than L2
     times = []
     for i in range(args.warmup + args.steps):

@@ -240,9 +240,9 @@ MIX_API mix_status_t mx_dequantize(const uint8_t* codes, const uint8_t* scales, 
  * CTAs when there are few outputs, summing the partials in a fixed order in
  * the caller's workspace (see mix_mx_gemm_workspace_bytes).
  *
- * The tensor-core path has two variants with identical results (every
- * product is exact; only the fp32 accumulation order is fixed by the K
- * loop, the same in both):
+ * The tensor-core path has two variants.  Every product is exact and the
+ * fp32 sums run in K order in both, so their results are identical, except
+ * where the staged variant cuts a tile along K (below):
  *  - staged (MIX_GEMM_TCGEN05_STAGED; chosen by AUTO / TCGEN05 when N > 256):
  *    A, and B unless it is MXFP4 that the unpacking TMA reads in place, are
  *    first expanded into exact e4m3 planes and UE8M0 scale words in the
@@ -250,7 +250,16 @@ MIX_API mix_status_t mx_dequantize(const uint8_t* codes, const uint8_t* scales, 
  *    workspace holds batch*M*Kp + bB*N*Kp bytes (Kp = K rounded up to 128,
  *    bB = ceil(batch / b_group); the B plane only when B is expanded) plus
  *    the scale words and alignment; mix_mx_gemm_workspace_bytes gives the
- *    exact size and a smaller workspace returns MIX_ERR_WORKSPACE.
+ *    exact size and a smaller workspace returns MIX_ERR_WORKSPACE.  When
+ *    the output tiles (128 x 224) leave a last wave that would keep most SMs
+ *    idle, those tiles' K loops are shared out over all SMs: each part's fp32
+ *    sums go through the workspace (one 128 x 224 fp32 slot and 12 flag
+ *    words per SM) and the SM holding a tile's first k-steps adds the later
+ *    parts in K order before the epilogue.  Such tiles can differ from the
+ *    fused variant in the last bits of C; the result is deterministic for a
+ *    given device.  The kernel relies on all its CTAs (one per SM) being
+ *    resident together; a part that never arrives ends its wait with bit 9
+ *    of the device error word.
  *  - fused decode (MIX_GEMM_TCGEN05_FUSED; chosen when N <= 256): decoder
  *    warps expand each A tile inside the matmul; B enters by TMA, MXFP4 in
  *    place (no workspace) or else expanded once into e4m3 in the workspace

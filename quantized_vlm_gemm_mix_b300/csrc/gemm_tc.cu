@@ -123,6 +123,15 @@ struct TcParams {
   // MMA thread runs out with no copy or MMA in flight
   long long wait_limit;
   int selftest_no_loads;
+  // staged kernel: the split of the last partial wave along K (see the
+  // schedule in mix_internal.h): parts' fp32 sums and their flags
+  int sk_split, sk_nd;
+  int64_t sk_tile0, sk_len;
+  float* sk_part;
+  unsigned* sk_flags;
+  // staged kernel: how many of the three groups of four epilogue warps drain
+  // a tile (the others only pass the barriers)
+  int epi_groups;
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a K-major operand tile
@@ -492,8 +501,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // warps (one per TMEM lane quadrant) store the scale words into TMEM with
 // tcgen05.st, off the tensor pipe, and the MMA thread issues four MMAs once
 // they are in place.  (Copying them with tcgen05.cp from the MMA thread made
-// this kernel about a fifth slower on every shape measured, although the
-// same copies cost nothing in the fused-decode kernel, which uses them.)
+// this kernel about a fifth slower on every shape measured: the copies
+// occupy the tensor pipe.)
 //
 // Persistent: one CTA per SM walks the 128 x 224 output tiles (M fastest, so
 // the CTAs in flight share B tiles and the whole of A stays in L2).  Two
@@ -521,29 +530,160 @@ struct PlanS {
   static constexpr int OFF_BAR = OFF_CST + NUM_EPI_WARPS * CST_BYTES;
   static constexpr int NUM_BARS = 3 * S + 4 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int OFF_UNITS = OFF_MISC + 16;  // this CTA's units of split tiles (SkUnits)
+  static constexpr int SMEM_BYTES = OFF_UNITS + 48 + 1024;
 };
 static_assert(PlanS::SMEM_BYTES <= 227 * 1024, "staged plan exceeds shared memory");
 static_assert(B_OPS_S % 1024 == 0, "operand stages must keep the 1024-byte swizzle alignment");
 
 __device__ __forceinline__ uint32_t acc_col(int b) { return b ? 256u : 0u; }
 __device__ __forceinline__ uint32_t sf_col(int s) { return (s & 2 ? 480u : 224u) + 16u * (uint32_t)(s & 1); }
+static_assert(NUM_EPI_WARPS == kSkFlags, "one split-part flag per epilogue warp");
+static_assert(BNS == kStagedBN, "split-part slots hold one 128 x 224 tile");
+
+// Work unit i of this CTA under the staged schedule: tile t, k-steps
+// [k0, k1), and the unit's role in a tile cut along K.  Every role of the
+// CTA walks the same units in the same order.
+enum { UNIT_WHOLE = 0, UNIT_HEAD = 1, UNIT_PART = 2 };
+struct Unit {
+  int t, k0, k1, kind;
+};
+// The units of split tiles, worked out once per CTA (thread 0, at entry):
+// at most two -- the end of one tile and the start of the next, since a
+// CTA's share of the split k-steps is shorter than a tile -- and, for a head,
+// how many later parts it adds.
+struct SkUnits {
+  Unit u[2];
+  int n, nparts;
+};
+__device__ __noinline__ void make_sk_units(const TcParams& p, SkUnits* su) {
+  const int P = (int)gridDim.x, c = (int)blockIdx.x;
+  const int64_t kt = p.kt;
+  su->n = 0;
+  su->nparts = 0;
+  if (!p.sk_split) return;
+  // this CTA's share [s, e) of the split tiles' k-steps
+  const int64_t s = (int64_t)c * p.sk_len / P, e = (int64_t)(c + 1) * p.sk_len / P;
+  for (int j = 0; j < 2; ++j) {
+    const int64_t ti = s / kt + j, x = j == 0 ? s : ti * kt;
+    if (x >= e) break;
+    Unit& u = su->u[su->n++];
+    u.t = (int)(p.sk_tile0 + ti);
+    u.k0 = (int)(x - ti * kt);
+    u.k1 = (int)min(kt, e - ti * kt);
+    u.kind = (u.k0 == 0 && u.k1 == kt) ? UNIT_WHOLE : (u.k0 == 0 ? UNIT_HEAD : UNIT_PART);
+    if (u.kind == UNIT_HEAD) {  // later parts: CTAs whose shares start inside this tile
+      const int64_t tile_end = (ti + 1) * kt;
+      int n = 0;
+      while (c + n + 1 < P && (int64_t)(c + n + 1) * p.sk_len / P < tile_end) ++n;
+      su->nparts = n;
+    }
+  }
+}
+template <bool SPLIT>
+__device__ __forceinline__ bool staged_unit(const TcParams& p, int tiles, int i, Unit& u, const SkUnits* su) {
+  if (!SPLIT || i < p.sk_nd) {  // whole tiles c, c + P, ...
+    const int64_t t = (int64_t)blockIdx.x + (int64_t)i * gridDim.x;
+    if (t >= tiles) return false;
+    u.t = (int)t;
+    u.k0 = 0;
+    u.k1 = (int)p.kt;
+    u.kind = UNIT_WHOLE;
+    return true;
+  }
+  const int j = i - p.sk_nd;
+  if (j >= su->n) return false;
+  u = su->u[j];
+  return true;
+}
+
+// Split parts: CTA c's part sums of one tile live in slot c as float4
+// [chunk of 32 columns][4-column group][row], so that the lanes of a warp
+// (one row each) touch consecutive 16-byte words.
+__device__ __forceinline__ float4* sk_slot(const TcParams& p, int c) {
+  return reinterpret_cast<float4*>(p.sk_part) + (size_t)c * (kSkSlotBytes / 16);
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned* a, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* a) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+
+// A part that does not start the tile: its sums go to this CTA's slot, then
+// each epilogue warp raises its own flag (the head's warp of the same number
+// reads exactly the rows and columns this warp wrote).
+__device__ __forceinline__ void epilogue_part_s(const TcParams& p, uint32_t tmem_acc, int warp, int lane) {
+  const uint32_t q = (uint32_t)(warp & 3);
+  const int cg = (warp - EPI_WARP0) >> 2;
+  const int row = 32 * (int)q + lane;
+  float4* slot = sk_slot(p, (int)blockIdx.x);
+  for (int cc = cg; cc < BNS / 32 && cg < p.epi_groups; cc += p.epi_groups) {
+    uint32_t u[32];
+    ptx::tmem_ld_x32(tmem_acc + ((32u * q) << 16) + (uint32_t)(cc * 32), u);
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      slot[(cc * 8 + j) * 128 + row] = make_float4(__uint_as_float(u[4 * j]), __uint_as_float(u[4 * j + 1]),
+                                                   __uint_as_float(u[4 * j + 2]), __uint_as_float(u[4 * j + 3]));
+  }
+  __threadfence();
+  __syncwarp();
+  if (lane == 0) st_release_u32(p.sk_flags + (size_t)blockIdx.x * kSkFlags + (warp - EPI_WARP0), 1u);
+}
+
+// The head of a split tile: the CTAs holding its later parts are c + 1 ..
+// c + nparts.  Waits (bounded) for this warp's flag of each, so that the
+// fix-up below can add their sums.  Every lane acquires the flags itself; the
+// answer is the warp's.
+__device__ __forceinline__ bool wait_parts(const TcParams& p, int nparts, int warp, volatile int* abort_flag) {
+  bool ok = true;
+  for (int i = 1; i <= nparts && ok; ++i) {
+    const unsigned* f = p.sk_flags + (size_t)(blockIdx.x + i) * kSkFlags + (warp - EPI_WARP0);
+    const long long t0 = clock64();
+    while (ok && ld_acquire_u32(f) == 0u) {
+      if (*abort_flag || clock64() - t0 > p.wait_limit) ok = false;
+      else __nanosleep(64);
+    }
+  }
+  return __all_sync(0xFFFFFFFFu, ok);
+}
 
 // Epilogue of one 128 x 224 tile held in TMEM columns acc..acc+223: warp w
 // (EPI_WARP0 ..) reads lane quadrant w % 4 and the 32-column chunks cg,
 // cg + 3, cg + 6 (cg = its column group 0..2).  fp32 C leaves through one 2 KB
 // staging tile per warp (32 rows x 16 columns, 64-byte swizzle) and TMA
 // stores; the fused quantiser writes codes and shared fields from registers.
+//
+// The head of a split tile passes nparts > 0: the sums of the later parts
+// (slots blockIdx.x + 1 .. + nparts, already waited for) are added to the
+// accumulator in k order before anything is written.
+template <bool SPLIT>
 __device__ __forceinline__ void epilogue_tile_s(const TcParams& p, const CUtensorMap* tmap_c, uint32_t tmem_acc,
                                                 unsigned char* cst, int64_t m0, int64_t n0, int64_t bt, int warp,
-                                                int lane, bool& c_pending) {
+                                                int lane, bool& c_pending, int nparts) {
   const uint32_t q = (uint32_t)(warp & 3);
   const int cg = (warp - EPI_WARP0) >> 2;
   const int64_t row = m0 + 32 * q + lane;
-  for (int cc = cg; cc < BNS / 32; cc += NUM_EPI_WARPS / 4) {
+  for (int cc = cg; cc < BNS / 32 && cg < p.epi_groups; cc += p.epi_groups) {
     uint32_t u[32];
     ptx::tmem_ld_x32(tmem_acc + ((32u * q) << 16) + (uint32_t)(cc * 32), u);
     ptx::tmem_wait_ld();
+    for (int i = 1; SPLIT && i <= nparts; ++i) {
+      const float4* slot = sk_slot(p, (int)blockIdx.x + i);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j == 4) asm volatile("" ::: "memory");  // at most four loads in flight: the epilogue has 96 registers
+        const float4 v = __ldcg(slot + (cc * 8 + j) * 128 + 32 * (int)q + lane);
+        u[4 * j] = __float_as_uint(__fadd_rn(__uint_as_float(u[4 * j]), v.x));
+        u[4 * j + 1] = __float_as_uint(__fadd_rn(__uint_as_float(u[4 * j + 1]), v.y));
+        u[4 * j + 2] = __float_as_uint(__fadd_rn(__uint_as_float(u[4 * j + 2]), v.z));
+        u[4 * j + 3] = __float_as_uint(__fadd_rn(__uint_as_float(u[4 * j + 3]), v.w));
+      }
+    }
     const int64_t col = n0 + cc * 32;
     if (p.c != nullptr && col < p.N && m0 + 32 * q < p.M) {
 #pragma unroll
@@ -578,7 +718,7 @@ __device__ __forceinline__ void epilogue_tile_s(const TcParams& p, const CUtenso
   }
 }
 
-template <bool B_NATIVE>
+template <bool B_NATIVE, bool SPLIT>
 __global__ void __maxnreg__(96)
     gemm_staged_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_c, const TcParams p) {
@@ -597,9 +737,9 @@ __global__ void __maxnreg__(96)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + L::OFF_MISC + 8);  // drains ignore aborts
+  SkUnits* sku = reinterpret_cast<SkUnits*>(smem + L::OFF_UNITS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int num_k = (int)p.kt;
   const int mt = (int)p.mt, nt = (int)p.nt;
   const int tiles = (int)(p.batch * p.nt * p.mt);  // < 2^31: checked on the host
 
@@ -616,6 +756,7 @@ __global__ void __maxnreg__(96)
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
     *never = 0;
+    if (SPLIT) make_sk_units(p, sku);
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmap_a);
     ptx::prefetch_tmap(&tmap_b);
@@ -632,33 +773,36 @@ __global__ void __maxnreg__(96)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // Kept lean: this one thread's issue rate bounds the ring.  Per unit the
+      // tile coordinates and scale-word addresses are set up once; per k-step
+      // only counters and pointers advance.
       constexpr uint32_t kStageBytes = A_OPS + (B_NATIVE ? B_OPS_S / 2 : B_OPS_S) + L::SFA_BYTES + L::SFB_BYTES;
-      int64_t g = 0;  // k-steps issued by this CTA
-      bool stop = false;
-      for (int t = blockIdx.x; t < tiles && !stop && !p.selftest_no_loads; t += gridDim.x) {
+      int g = 0;  // k-steps issued by this CTA (fewer than 2^31)
+      bool stop = p.selftest_no_loads != 0;
+      Unit u;
+      for (int i = 0; !stop && staged_unit<SPLIT>(p, tiles, i, u, sku); ++i) {
+        const int t = u.t;
         const int mtile = t % mt, rest = t / mt, ntile = rest % nt, bt = rest / nt, bbt = bt / (int)p.b_group;
-        const uint8_t* sfa = p.sfa_g + (((int64_t)bt * mt + mtile) * p.kt) * L::SFA_BYTES;
-        const uint8_t* sfb = p.sfb_g + (((int64_t)bbt * nt + ntile) * p.kt) * L::SFB_BYTES;
-        for (int kt = 0; kt < num_k; ++kt, ++g) {
-          const int s = (int)(g % S);
-          const uint32_t n = (uint32_t)(g / S);
-          if (n > 0 && !ptx::mbar_wait_spin(&empty[s], (n - 1) & 1, p.wait_limit, abort_flag)) {
+        const uint8_t* sfa = p.sfa_g + (((int64_t)bt * mt + mtile) * p.kt + u.k0) * L::SFA_BYTES;
+        const uint8_t* sfb = p.sfb_g + (((int64_t)bbt * nt + ntile) * p.kt + u.k0) * L::SFB_BYTES;
+        const int ay = mtile * BM, by = ntile * BNS;
+        for (int kt = u.k0; kt < u.k1; ++kt, ++g, sfa += L::SFA_BYTES, sfb += L::SFB_BYTES) {
+          const int s = g & (S - 1);
+          if (g >= S && !ptx::mbar_wait_spin(&empty[s], (uint32_t)((g / S) - 1) & 1u, p.wait_limit, abort_flag)) {
             flag_error(1u, abort_flag);
             stop = true;
             break;
           }
           if (*abort_flag) { stop = true; break; }
           ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
-          ptx::tma_load_3d(smem + L::OFF_AOPS + s * A_OPS, &tmap_a, &full[s], kt * BK, mtile * BM, bt);
-          ptx::tma_load_3d(smem + L::OFF_BOPS + s * B_OPS_S, &tmap_b, &full[s], kt * BK, ntile * BNS, bbt);
-          ptx::bulk_load(smem + L::OFF_SFA + s * L::SFA_BYTES, sfa + (int64_t)kt * L::SFA_BYTES, L::SFA_BYTES,
-                         &full[s]);
-          ptx::bulk_load(smem + L::OFF_SFB + s * L::SFB_BYTES, sfb + (int64_t)kt * L::SFB_BYTES, L::SFB_BYTES,
-                         &full[s]);
+          ptx::tma_load_3d(smem + L::OFF_AOPS + s * A_OPS, &tmap_a, &full[s], kt * BK, ay, bt);
+          ptx::tma_load_3d(smem + L::OFF_BOPS + s * B_OPS_S, &tmap_b, &full[s], kt * BK, by, bbt);
+          ptx::bulk_load(smem + L::OFF_SFA + s * L::SFA_BYTES, sfa, L::SFA_BYTES, &full[s]);
+          ptx::bulk_load(smem + L::OFF_SFB + s * L::SFB_BYTES, sfb, L::SFB_BYTES, &full[s]);
         }
       }
       // drain: every issued copy lands before the CTA may exit
-      for (int64_t h = (g > S ? g - S : 0); h < g; ++h)
+      for (int h = (g > S ? g - S : 0); h < g; ++h)
         ptx::mbar_wait(&full[h % S], (uint32_t)(h / S) & 1, p.wait_limit, never);
     }
   } else if (warp == 1) {
@@ -666,9 +810,9 @@ __global__ void __maxnreg__(96)
     if (lane == 0) {
       const uint32_t b_fmt = B_NATIVE ? 5u : 0u;  // E2M1 or E4M3
       int64_t g = 0;
-      int i = 0;  // local tile index
       bool stop = false;
-      for (int t = blockIdx.x; t < tiles && !stop; t += gridDim.x, ++i) {
+      Unit u;
+      for (int i = 0; !stop && staged_unit<SPLIT>(p, tiles, i, u, sku); ++i) {  // i: this CTA's unit index
         const int b = i & 1;
         if (i >= 2 && !ptx::mbar_wait_spin(&acc_empty[b], (uint32_t)((i >> 1) - 1) & 1, p.wait_limit, abort_flag)) {
           flag_error(256u, abort_flag);
@@ -676,7 +820,7 @@ __global__ void __maxnreg__(96)
         }
         ptx::tc_fence_after();
         const uint32_t dacc = tmem + acc_col(b);
-        for (int kt = 0; kt < num_k; ++kt, ++g) {
+        for (int kt = u.k0; kt < u.k1; ++kt, ++g) {
           const int s = (int)(g % S);
           const uint32_t n = (uint32_t)(g / S);
           // the scale warps arrive only after the stage's copies landed
@@ -694,7 +838,7 @@ __global__ void __maxnreg__(96)
           for (int j = 0; j < 4; ++j) {
             ptx::mma_mxf8f6f4(dacc, ptx::sdesc_sw128(a_addr + 32u * j), ptx::sdesc_sw128(b_addr + 32u * j),
                               ptx::idesc_mxf8(BM, BNS, 0u, b_fmt, (uint32_t)j), tsf, tsf + 4u,
-                              (kt > 0 || j > 0) ? 1u : 0u);
+                              (kt > u.k0 || j > 0) ? 1u : 0u);
           }
           ptx::tc_commit(&empty[s]);
         }
@@ -714,8 +858,9 @@ __global__ void __maxnreg__(96)
     const uint32_t tq = tmem + ((32u * q) << 16);
     int64_t g = 0;
     bool stop = false;
-    for (int t = blockIdx.x; t < tiles && !stop; t += gridDim.x) {
-      for (int kt = 0; kt < num_k; ++kt, ++g) {
+    Unit u;
+    for (int i = 0; !stop && staged_unit<SPLIT>(p, tiles, i, u, sku); ++i) {
+      for (int kt = u.k0; kt < u.k1; ++kt, ++g) {
         const int s = (int)(g % S);
         const uint32_t n = (uint32_t)(g / S);
         if (!ptx::mbar_wait(&full[s], n & 1, p.wait_limit, abort_flag)) {
@@ -742,17 +887,27 @@ __global__ void __maxnreg__(96)
     // --------------------------------------------------------- epilogue
     unsigned char* cst = smem + L::OFF_CST + (warp - EPI_WARP0) * L::CST_BYTES;
     bool c_pending = false;
-    int i = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+    Unit u;
+    for (int i = 0; staged_unit<SPLIT>(p, tiles, i, u, sku); ++i) {
       const int b = i & 1;
       if (*abort_flag || !ptx::mbar_wait(&acc_full[b], (uint32_t)(i >> 1) & 1, p.wait_limit, abort_flag)) {
         if (!*abort_flag) flag_error(16u, abort_flag);
         break;
       }
       ptx::tc_fence_after();
+      const int t = u.t;
       const int mtile = t % mt, rest = t / mt, ntile = rest % nt, bt = rest / nt;
-      epilogue_tile_s(p, &tmap_c, tmem + acc_col(b), cst, (int64_t)mtile * BM, (int64_t)ntile * BNS, bt, warp, lane,
-                      c_pending);
+      if (SPLIT && u.kind == UNIT_PART) {
+        epilogue_part_s(p, tmem + acc_col(b), warp, lane);
+      } else {
+        const int nparts = SPLIT && u.kind == UNIT_HEAD ? sku->nparts : 0;
+        if (nparts > 0 && !wait_parts(p, nparts, warp, abort_flag)) {
+          if (!*abort_flag) flag_error(512u, abort_flag);
+          break;
+        }
+        epilogue_tile_s<SPLIT>(p, &tmap_c, tmem + acc_col(b), cst, (int64_t)mtile * BM, (int64_t)ntile * BNS, bt, warp,
+                        lane, c_pending, nparts);
+      }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&acc_empty[b]);
@@ -853,19 +1008,19 @@ bool make_e4m3_map(CUtensorMap* m, const void* base, int64_t k_pad, int64_t rows
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool B_NATIVE>
+template <bool B_NATIVE, bool SPLIT>
 cudaError_t launch_staged(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const TcParams& p,
                           dim3 grid, cudaStream_t st) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_staged_kernel<B_NATIVE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_staged_kernel<B_NATIVE, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          PlanS::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  gemm_staged_kernel<B_NATIVE><<<grid, NUM_THREADS_S, PlanS::SMEM_BYTES, st>>>(ma, mb, mc, p);
+  gemm_staged_kernel<B_NATIVE, SPLIT><<<grid, NUM_THREADS_S, PlanS::SMEM_BYTES, st>>>(ma, mb, mc, p);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess && std::getenv("MIX_DEBUG") != nullptr)
     std::fprintf(stderr, "gemm_staged launch: %s\n", cudaGetErrorString(e));
@@ -1019,15 +1174,31 @@ cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t 
   p.sfa_g = base + sp.off_sfa;
   p.sfb_g = bbase + bp.off_sfb;
   p.mt = sp.mt; p.nt = sp.nt; p.kt = sp.kt;
+  p.sk_split = sp.split;
+  p.sk_nd = sp.nd;
+  // The epilogue (and its quantiser above all) slows the MMAs of the next tile
+  // while it runs, less so when fewer warps spread it over a longer time; a
+  // tile of 16 or more k-steps leaves time for one group of four warps, a
+  // shorter one needs two, and a tile of a few k-steps whose fp32 C is
+  // stored (the epilogue is then the bound: e.g. attention scores, K = 128)
+  // all three.
+  p.epi_groups = sp.kt >= 16 ? 1 : (sp.kt >= 4 && d.c == nullptr) ? 2 : 3;
+  p.sk_tile0 = sp.sk_tile0;
+  p.sk_len = sp.sk_len;
+  p.sk_part = sp.split ? reinterpret_cast<float*>(base + sp.off_sk) : nullptr;
+  p.sk_flags = sp.split ? reinterpret_cast<unsigned*>(base + sp.off_sk + (size_t)sp.grid * kSkSlotBytes) : nullptr;
   cudaError_t e = launch_expand_a(d, sp, base, st);
   if (e != cudaSuccess) return e;
   if (!prepared) {
     e = launch_expand_b(d, sp, base, st);
     if (e != cudaSuccess) return e;
   }
-  const int64_t tiles = d.batch * sp.nt * sp.mt;
-  const dim3 grid((unsigned)(tiles < num_sms() ? tiles : num_sms()));
-  return sp.b_native ? launch_staged<true>(ma, mb, mc, p, grid, st) : launch_staged<false>(ma, mb, mc, p, grid, st);
+  const dim3 grid((unsigned)sp.grid);
+  if (sp.split)
+    return sp.b_native ? launch_staged<true, true>(ma, mb, mc, p, grid, st)
+                       : launch_staged<false, true>(ma, mb, mc, p, grid, st);
+  return sp.b_native ? launch_staged<true, false>(ma, mb, mc, p, grid, st)
+                     : launch_staged<false, false>(ma, mb, mc, p, grid, st);
 }
 
 }  // namespace
@@ -1074,7 +1245,8 @@ cudaError_t launch_selftest_wait_timeout(void* ws, long long limit_cycles, cudaS
   p.mt = 1; p.nt = 1; p.kt = 1;
   p.wait_limit = limit_cycles;
   p.selftest_no_loads = 1;
-  return launch_staged<false>(ma, mb, ma, p, dim3(1), st);
+  p.epi_groups = 3;
+  return launch_staged<false, false>(ma, mb, ma, p, dim3(1), st);
 }
 
 cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, void* ws, size_t ws_bytes, cudaStream_t st,

@@ -67,17 +67,34 @@ cudaError_t launch_gemm_tc_prepare_b(const mix_gemm_desc_t& d, void* prepared, c
 // lane l (of every lane quadrant), column i.  MXFP4 weights that the
 // unpacking TMA can read in place are not expanded: only their scales are
 // regrouped.
+//
+// Tile schedule of the persistent staged kernel (grid `grid`, one CTA per SM).
+// Without a split, CTA c takes tiles c, c + grid, ...  With one (`split`),
+// the first `nd` waves of whole tiles go that way and the last
+// R = tiles - nd * grid tiles, which would leave most SMs idle in a final
+// wave, are cut along K: their R * kt k-steps (sk_len) are divided evenly
+// over all CTAs, CTA c taking k-steps [c * sk_len / grid, (c + 1) * sk_len /
+// grid) of them, tile by tile.  A CTA whose share starts inside a tile writes
+// that part's fp32 sums to its slot of `off_sk` and raises per-warp flags;
+// the CTA holding the tile's first k-step adds the later parts in k order
+// and runs the epilogue.
 struct StagedPlan {
   bool b_native;
   int64_t k_pad, kt, mt, nt, bb;
   // offsets from the 1024-aligned workspace base; off_sfe: per-32-block scale
-  // bytes of g16 weights ([bb][N][k_pad / 32]), in B-only plans
-  size_t off_a, off_sfa, off_b, off_sfb, off_sfe, bytes;
+  // bytes of g16 weights ([bb][N][k_pad / 32]), in B-only plans; off_sk: the
+  // split parts' partial sums ([grid][128 x 224] fp32) and their flags
+  // ([grid][12] words), present when split
+  size_t off_a, off_sfa, off_sk, off_b, off_sfb, off_sfe, bytes;
+  int grid, split, nd;
+  int64_t sk_tile0, sk_len;
 };
 // Weights with one scale per 16 elements (MXINT4g16 / MXFP4g16).
 inline bool b_g16(const mix_gemm_desc_t& d) { return d.b_block == 16; }
 constexpr int kStagedAlign = 1024;
 constexpr int kStagedBN = 224;  // output columns per tile of the staged matmul
+constexpr int kSkSlotBytes = 128 * kStagedBN * 4;  // one split part's fp32 sums
+constexpr int kSkFlags = 12;                        // flags per part: one per epilogue warp
 StagedPlan staged_plan(const mix_gemm_desc_t& d);
 StagedPlan staged_plan_b_only(const mix_gemm_desc_t& d);  // B expansion alone (fused-decode path)
 bool staged_fp4_native_ok(const mix_gemm_desc_t& d);

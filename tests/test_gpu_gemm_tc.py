@@ -227,6 +227,50 @@ def test_vit_mlp_chain_sampled(mix, orc):
                          np.sort(rng.choice(D, 256, replace=False))) <= GEMM_REL_TOL
 
 
+def split_schedule(M, N, K, sms):
+    """The staged kernel's schedule rule, restated: 128 x 224 tiles; when the
+    last wave is partial and cutting it along K shortens it by more than
+    about four k-steps, its R tiles' k-steps are shared out over all SMs."""
+    mt, nt, kt = -(-M // 128), -(-N // 224), -(-K // 128)
+    tiles = mt * nt
+    nd, R = divmod(tiles, sms)
+    split = kt >= 64 and R > 0 and R * kt >= 2 * sms and R * kt + 4 * sms <= kt * sms
+    return split, mt, nd * sms
+
+
+@pytest.mark.parametrize("M,N,K,at,bt", [(1000, 2208, 8192, 2, 1), (1536, 3136, 8192, 1, 0),
+                                         (4096, 3584, 8192, 2, 1)])
+def test_staged_split_last_wave(mix, orc, M, N, K, at, bt):
+    """Tiles of a partial last wave cut along K across every SM: the CTA that
+    holds a tile's first k-steps adds the later parts' fp32 sums in k order
+    before its epilogue.  Shapes: fewer tiles than SMs with ragged edges (two
+    parts a tile), 20 tiles past a full wave (seven or eight parts a tile),
+    and 68 past three waves (two or three parts; the 18944-deep down
+    projection of the full-size test is cut the same way).  Whole rows of C (every column,
+    cut tiles and whole ones) match the oracle on rows sampled mostly from
+    the cut tiles; the fused MiX epilogue is bit-exact given C; two calls
+    agree bit for bit."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    split, mt, first = split_schedule(M, N, K, sms)
+    if sms == 148:
+        assert split  # the shapes are chosen to be cut on this part
+    ac, ash, bc, bs = operands(orc, 77 + M + N, M, N, K, at, bt)
+    outs = [run_tc(mix, ac, ash, at, bc, bs, bt, M, N, K, epi=2, algo="staged") for _ in range(2)]
+    assert np.array_equal(outs[0][0].view(np.uint32), outs[1][0].view(np.uint32))
+    assert np.array_equal(outs[0][1], outs[1][1]) and np.array_equal(outs[0][2], outs[1][2])
+    c, oc, osh = outs[0]
+    c = c[0]
+    rng = np.random.default_rng(M + N + K)
+    cut_rows = sorted({min(M - 1, 128 * (t % mt) + int(r)) for t in range(first, mt * (-(-N // 224)))
+                       for r in rng.choice(128, 2, replace=False)}) if split else []
+    rows = np.array(sorted(set(cut_rows[:48]) | set(rng.choice(M, 16, replace=False).tolist())))
+    ref = orc.gemm(ac[rows], ash[rows], at, -8, bc, bs, bt)
+    assert row_rel_err(c[rows], ref) <= GEMM_REL_TOL
+    rc, rs = orc.mix_quantize(np.ascontiguousarray(c[rows]), 2, -8, 1)
+    assert np.array_equal(oc[0][rows], rc) and np.array_equal(osh[0][rows], rs)
+
+
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("N", [128, 256])
 def test_tc_zero_blocks_causal(mix, orc, algo, N):
