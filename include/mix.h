@@ -339,7 +339,11 @@ MIX_API mix_status_t mix_mx_gemm_prepare_b(const mix_gemm_desc_t* desc, void* pr
  * fp32 subtraction), tokens x heads x head_dim dense, when k_out != NULL.
  * COMPUTE splits the tokens across CTAs and keeps per-chunk partial sums
  * (fp32 pairs, about 48 bits) in the caller's workspace
- * (ksmooth_workspace_bytes); APPLY needs none. */
+ * (ksmooth_workspace_bytes); APPLY needs none.  When every CTA's run of
+ * tokens fits in shared memory (a few MB of keys in all, e.g. one layer's
+ * prefill), COMPUTE is one cooperative launch whose CTAs meet at a barrier
+ * counter in the workspace; longer inputs take three kernels.  The two
+ * orders of summation can differ in the last bit of the mean. */
 enum { KSMOOTH_COMPUTE = 0, KSMOOTH_APPLY_FROZEN = 1 };
 MIX_API size_t ksmooth_workspace_bytes(int64_t tokens, int heads, int head_dim);
 MIX_API mix_status_t ksmooth_kv(const void* k, mix_dtype_t dtype, int64_t tokens, int heads, int head_dim,
@@ -426,7 +430,8 @@ MIX_API const char* mix_status_str(mix_status_t status);
  * per-device error word and the kernel returns early (its outputs are then
  * undefined).  This reads the word for the current device (synchronising the
  * device) and clears it when `clear` is nonzero.  MIX_OK if the read worked.
- * Bits 0..9: a wait of the matmul kernels (which one, by role). */
+ * Bits 0..9: a wait of the matmul kernels (which one, by role); bit 10:
+ * the grid barrier of the one-pass K-smoothing kernel. */
 MIX_API mix_status_t mix_device_error(unsigned* word, int clear);
 /* Test aid for the bounded waits.  Launches the staged tensor-core matmul
  * kernel once, on a single 128 x 224 tile, with its producer switched off

@@ -46,6 +46,10 @@ namespace mixk {
 
 __device__ unsigned g_mix_device_error;
 
+cudaError_t device_error_word(unsigned** word) {
+  return cudaGetSymbolAddress(reinterpret_cast<void**>(word), g_mix_device_error);
+}
+
 cudaError_t read_device_error(unsigned* word, bool clear) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return e;

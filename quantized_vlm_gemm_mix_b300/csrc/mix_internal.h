@@ -120,6 +120,7 @@ cudaError_t launch_ksmooth_noalloc(const void* k, bool bf16, int64_t tokens, int
 
 // Device error word (bounded waits), and the launch that makes one run out.
 cudaError_t read_device_error(unsigned* word, bool clear);
+cudaError_t device_error_word(unsigned** word);  // device address of the error word
 size_t selftest_ws_bytes();
 cudaError_t launch_selftest_wait_timeout(void* ws, long long limit_cycles, cudaStream_t st);
 
