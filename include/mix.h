@@ -257,8 +257,8 @@ MIX_API mix_status_t mx_dequantize(const uint8_t* codes, const uint8_t* scales, 
  *    words per SM) and the SM holding a tile's first k-steps adds the later
  *    parts in K order before the epilogue.  Such tiles can differ from the
  *    fused variant in the last bits of C; the result is deterministic for a
- *    given device.  The kernel relies on all its CTAs (one per SM) being
- *    resident together; a part that never arrives ends its wait with bit 9
+ *    given device.  Such a launch is cooperative (all its CTAs, one per SM,
+ *    resident together); a part that never arrives ends its wait with bit 9
  *    of the device error word.
  *  - fused decode (MIX_GEMM_TCGEN05_FUSED; chosen when N <= 256): decoder
  *    warps expand each A tile inside the matmul; B enters by TMA, MXFP4 in
@@ -384,9 +384,14 @@ MIX_API mix_status_t ksmooth_kv_noalloc(const void* k, mix_dtype_t dtype, int64_
  * smoothed with the frozen prefill mean and appended to the MXINT4 K' cache,
  * S = q K'^T by Eq. (6) with q quantised to MiX-4.5b, P = softmax(sm_scale S)
  * over the cache, P requantised to MiX-4.5b (32-token blocks, ebias p_ebias),
- * O = P V by Eq. (6) against the MXINT4 V cache (blocks along tokens).  Two
- * kernel launches, no host round trip; the last CTA of each KV head sums the
- * per-chunk partial outputs in chunk order (an atomic ticket, no waiting).
+ * O = P V by Eq. (6) against the MXINT4 V cache (blocks along tokens).  One
+ * cooperative launch (KV heads x token chunks, filling the SMs once) keeps
+ * each chunk's keys, values and scores in shared memory and meets at two
+ * bounded grid barriers (a counter in the workspace; bit 11 of the device
+ * error word on timeout): after the chunk statistics, and after the partial
+ * outputs, which are then summed in chunk order.  A cache too long for that
+ * (chunks over 200 KB of shared memory, tens of thousands of tokens) runs as
+ * two kernels, the last CTA of each KV head summing the partials.
  * Products are exact integers per block; block terms, S and the softmax are
  * fp32 (expf); O matches the oracle's fp64 composition within 1e-3 of each
  * head's largest |O|. */
@@ -417,7 +422,8 @@ typedef struct {
                             past the last token                                   */
 } mix_decode_attn_desc_t;
 
-/* Device workspace bytes (S, the per-chunk statistics and partial outputs). */
+/* Device workspace bytes (the per-chunk statistics and partial outputs, the
+ * barrier counter; S as well on the two-kernel path). */
 MIX_API size_t mix_decode_attention_workspace_bytes(const mix_decode_attn_desc_t* desc);
 MIX_API mix_status_t mix_decode_attention(const mix_decode_attn_desc_t* desc, void* workspace, size_t workspace_bytes,
                                           mix_stream_t stream);
@@ -431,7 +437,8 @@ MIX_API const char* mix_status_str(mix_status_t status);
  * undefined).  This reads the word for the current device (synchronising the
  * device) and clears it when `clear` is nonzero.  MIX_OK if the read worked.
  * Bits 0..9: a wait of the matmul kernels (which one, by role); bit 10:
- * the grid barrier of the one-pass K-smoothing kernel. */
+ * the grid barrier of the one-pass K-smoothing kernel; bit 11: a grid
+ * barrier of the one-kernel decode attention. */
 MIX_API mix_status_t mix_device_error(unsigned* word, int clear);
 /* Test aid for the bounded waits.  Launches the staged tensor-core matmul
  * kernel once, on a single 128 x 224 tile, with its producer switched off

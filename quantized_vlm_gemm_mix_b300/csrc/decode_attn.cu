@@ -3,30 +3,35 @@
 // Micro-Inverted-Scaling ..." (Method section, accelerator bullet: K-mean
 // subtraction with the frozen prefill mean, Q-K^T on the dual-format
 // matmul, the SFU softmax, MiX requantisation of P, P-V on the dual-format
-// matmul) as two kernels and no host round trip.
+// matmul) as ONE cooperative kernel and no host round trip.
 //
-//  attn_qk_kernel   grid (64-token chunks, KV heads), one thread per (query
-//                   head of the group, token): 64 G threads.  Quantises the group's
-//                   query heads to MiX-4.5b, appends the new key (K' =
-//                   fp32(k) - mean, MXINT4 along head_dim) when this chunk
-//                   holds the last token, then S = Eq. (6) shift-add for
-//                   every (head, token) of the chunk, and the chunk's softmax
-//                   statistics (max, sum of exp) per head.
-//  attn_pv_kernel   grid (256-token chunks, KV heads), one thread per (query
-//                   head, channel): 128 G threads.  Combines the statistics of
-//                   all chunks, forms P = exp(s - m) / l for its chunk,
-//                   requantises P to MiX-4.5b (32-token blocks), P-V by
-//                   Eq. (6) shift-add against the MXINT4 V plane (blocks
-//                   along tokens), writes a partial O; the last CTA of a KV
-//                   head (an atomic ticket, no waiting) sums the partials in
-//                   chunk order.
+// Grid: KV heads x NC token chunks of TB tokens (TB a multiple of 32, chosen
+// so that the grid fills the SMs once); 512 threads.  CTA (g, c):
+//   A. loads its chunk of the K' cache (MXINT4 rows along head_dim) and of
+//      the V planes (MXINT4 blocks along tokens) into shared memory,
+//      quantises the group's query heads to MiX-4.5b, appends the new key
+//      (K' = fp32(k) - mean, MXINT4) when the chunk holds the last token,
+//      forms S = Eq. (6) shift-add for every (head, token) of the chunk and
+//      the chunk's softmax statistics (max, sum of exp) per head;
+//   -- grid barrier --
+//   B. combines the statistics of every chunk of its KV head in chunk order,
+//      forms P = exp(s - m) / l for its tokens, requantises P to MiX-4.5b
+//      (32-token blocks) and computes the chunk's partial O by Eq. (6)
+//      against the V blocks;
+//   -- grid barrier --
+//   C. each CTA sums, in chunk order, the partial outputs of a slice of the
+//      (query head, channel) outputs.
+// The barriers are a counter in the workspace, zeroed by the host before the
+// launch; every wait is bounded (bit 11 of the device error word on
+// timeout, and the CTA writes nothing more).
 //
 // Every block product is an exact integer (as on the shift-add PE); block
 // terms are accumulated in fp32.  The work is tiny (the 8192-token cache of
-// four KV heads is 4.3 MB) and latency-bound, so the kernels spread it over
-// many short threads, and keep each thread to one head so that the code
-// stays small: a first version that unrolled every head of a thread spent
-// most of its time waiting on instruction fetch.
+// four KV heads is 4.3 MB) and latency-bound: one launch with the keys,
+// values and scores kept in shared memory replaces two kernels and the
+// global round trip of S.  Loops over heads stay rolled: a version that
+// unrolled every head of a thread spent most of its time waiting on
+// instruction fetch.
 #include <cuda_runtime.h>
 
 #include "mix_common.cuh"
@@ -36,9 +41,9 @@ namespace mixk {
 namespace {
 
 constexpr int kD = 128;          // head_dim
-constexpr int kChunkA = 64;      // tokens per CTA of the Q-K^T kernel
-constexpr int kChunkB = 256;     // tokens per CTA of the P-V kernel (8 blocks of 32)
-constexpr int kMaxG = 8;         // query heads per KV head (blocks of 64 G and 128 G threads)
+constexpr int kMaxG = 8;         // query heads per KV head
+constexpr int kThreadsD = 512;   // threads of the kernel
+constexpr int kDecMaxSmem = 200 * 1024;  // shared memory a CTA of the one-kernel path may use
 
 struct AttnArgs {
   const void* q;
@@ -50,19 +55,42 @@ struct AttnArgs {
   const uint8_t* v_codes;
   const uint8_t* v_scales;
   int64_t v_ld;
-  int64_t T, Tpad;
-  int CA, CB, HQ, HK, G;
+  int64_t T;
+  int NC, TB, HQ, HK, G;
   float sm_scale;
   int q_ebias, p_ebias;
-  float* S;        // [HQ][Tpad]
-  float2* stats;   // [CA][HQ] (chunk max, chunk sum of exp)
-  float* opart;    // [CB][HQ][D]
-  unsigned* tickets;  // [HK]
-  float* out;      // [HQ][D]
+  float2* stats;       // [HK][NC][G] (chunk max, chunk sum of exp)
+  float* opart;        // [HK][NC][G][D]
+  unsigned* counter;   // grid barrier
+  unsigned* err;       // device error word
+  long long limit;     // bounded waits, SM clocks
+  float* out;          // [HQ][D]
   uint8_t* p_codes;    // optional [HQ][v_ld / 2]
   uint16_t* p_shared;  // optional [HQ][v_ld / 32]
   float* p_values;     // optional [HQ][v_ld]: the P that was quantised
 };
+
+// Shared memory of one CTA for TB tokens (offsets in bytes, 16-aligned).
+struct DecPlan {
+  int kc, ksc, vsm, vxs, qf, qmeta, zs, pf, pmeta, stat, bytes;
+};
+__host__ __device__ inline DecPlan dec_plan(int TB) {
+  DecPlan p;
+  const int nb = TB / 32;
+  int o = 0;
+  p.kc = o;    o += TB * (kD / 2);                    // K' codes of the chunk
+  p.ksc = o;   o += TB * 4;                           // their four scale bytes per token
+  p.vsm = o;   o += nb * kD * 16;                     // V words [block][channel]
+  p.vxs = o;   o += nb * kD * 4;                      // V exponents [block][channel]
+  p.qf = o;    o += kMaxG * kD * 2;                   // MiX factors of the query heads
+  p.qmeta = o; o += kMaxG * (kD / 32) * 8;
+  p.zs = o;    o += kMaxG * TB * 4;                   // scaled scores, then P
+  p.pf = o;    o += kMaxG * TB * 2;                   // MiX factors of P
+  p.pmeta = o; o += kMaxG * nb * 8;
+  p.stat = o;  o += 2 * kMaxG * 4;                    // global max and sum per head
+  p.bytes = (o + 15) & ~15;
+  return p;
+}
 
 __device__ __forceinline__ uint32_t load_bits(const void* p, bool bf16, int64_t i) {
   return bf16 ? (uint32_t)static_cast<const uint16_t*>(p)[i] << 16 : __float_as_uint(static_cast<const float*>(p)[i]);
@@ -167,7 +195,261 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__global__ void __launch_bounds__(kChunkA * kMaxG, 2) attn_qk_kernel(AttnArgs a) {
+
+// Bounded grid barrier: every CTA of the cooperative grid arrives once; the
+// counter reaches `target` (the host zeroed it; gridDim.x per barrier).
+__device__ __forceinline__ bool dec_barrier(const AttnArgs& a, unsigned target, int* ok_s) {
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    atomicAdd(a.counter, 1u);
+    const long long s0 = clock64();
+    int ok = 1;
+    for (;;) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a.counter) : "memory");
+      if (v >= target) break;
+      if (clock64() - s0 > a.limit) {
+        atomicOr(a.err, 2048u);
+        ok = 0;
+        break;
+      }
+      __nanosleep(32);
+    }
+    *ok_s = ok;
+  }
+  __syncthreads();
+  return *ok_s != 0;
+}
+
+__global__ void __launch_bounds__(kThreadsD, 1) attn_decode_kernel(AttnArgs a) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  __shared__ int ok_s;
+  const int TB = a.TB, G = a.G, NC = a.NC;
+  const DecPlan L = dec_plan(TB);
+  uint8_t* kc = dsm + L.kc;
+  uint32_t* ksc = reinterpret_cast<uint32_t*>(dsm + L.ksc);
+  uint4* vsm = reinterpret_cast<uint4*>(dsm + L.vsm);
+  int* vxs = reinterpret_cast<int*>(dsm + L.vxs);
+  int16_t* qf = reinterpret_cast<int16_t*>(dsm + L.qf);
+  int2* qmeta = reinterpret_cast<int2*>(dsm + L.qmeta);
+  float* zs = reinterpret_cast<float*>(dsm + L.zs);
+  int16_t* pf = reinterpret_cast<int16_t*>(dsm + L.pf);
+  int2* pmeta = reinterpret_cast<int2*>(dsm + L.pmeta);
+  float* gm = reinterpret_cast<float*>(dsm + L.stat);
+  float* gl = gm + kMaxG;
+  const int g = (int)blockIdx.x / NC, c = (int)blockIdx.x % NC;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool bf16 = a.bf16 != 0;
+  const int64_t t0 = (int64_t)c * TB;
+  const int nt = (int)min((int64_t)TB, a.T - t0);  // tokens of this chunk (>= 1)
+  const int nblk = (nt + 31) / 32;                 // 32-token blocks holding a token
+  const int64_t t_new = a.T - 1;
+  const bool appends = a.k_new != nullptr && t_new >= t0 && t_new < t0 + TB;
+  const int nb = TB / 32;
+
+  // ---- A. the chunk's keys and values into shared memory
+  for (int i = tid; i < nt * 5; i += kThreadsD) {
+    const int tt = i / 5, part = i % 5;
+    if (appends && t0 + tt == t_new) continue;  // made below
+    const int64_t row = (t0 + tt) * a.HK + g;
+    if (part < 4)
+      reinterpret_cast<uint4*>(kc + tt * (kD / 2))[part] = __ldg(reinterpret_cast<const uint4*>(a.k_codes + row * (kD / 2)) + part);
+    else
+      ksc[tt] = __ldg(reinterpret_cast<const uint32_t*>(a.k_scales + row * (kD / 32)));
+  }
+  for (int i = tid; i < nblk * kD; i += kThreadsD) {
+    const int d = i / nblk, b = i % nblk;  // blocks of one channel are contiguous
+    const int64_t e = ((int64_t)g * kD + d) * a.v_ld + t0 + 32 * b;
+    vsm[b * kD + d] = __ldg(reinterpret_cast<const uint4*>(a.v_codes + e / 2));
+    vxs[b * kD + d] = (int)__ldg(a.v_scales + e / 32) - 127;
+  }
+  // the group's query heads -> MiX-4.5b factors: four lanes per 32-element
+  // block, sixteen per head, whole warps
+  const int q_warps = (G + 1) / 2;
+  if (warp < q_warps) {
+    const int hh = tid >> 4, b = (tid >> 2) & 3, qq = tid & 3;
+    uint32_t u[8] = {};
+    if (hh < G) {
+      const int64_t base = (int64_t)(g * G + hh) * kD + 32 * b + 8 * qq;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) u[i] = load_bits(a.q, bf16, base + i);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if ((u[i] & 0x7FFFFFFFu) > 0x7F800000u) u[i] = 0u;  // NaN codes as zero
+    }
+    uint32_t sh;
+    const uint32_t word = mix_block32_quad(u, qq, a.q_ebias, true, sh);
+    if (hh < G) mix_unpack_quad(word, sh, qq, a.q_ebias, &qf[hh * kD + 32 * b], &qmeta[hh * 4 + b]);
+  } else if (appends && warp == q_warps && lane < 4) {
+    // append the new key: K' = fp32(k) - mean, MXINT4 along head_dim
+    const int b = lane;
+    uint32_t u[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int64_t e = (int64_t)g * kD + 32 * b + i;
+      u[i] = __float_as_uint(__fsub_rn(__uint_as_float(load_bits(a.k_new, bf16, e)), a.k_mean[e]));
+    }
+    uint4 w;
+    uint32_t sc;
+    mx_block32<false>(u, MX_RULE_CEIL, w, sc);
+    const int64_t row = t_new * a.HK + g;
+    *reinterpret_cast<uint4*>(a.k_codes + row * (kD / 2) + 16 * b) = w;
+    a.k_scales[row * (kD / 32) + b] = (uint8_t)sc;
+    const int tt = (int)(t_new - t0);
+    reinterpret_cast<uint4*>(kc + tt * (kD / 2))[b] = w;
+    reinterpret_cast<uint8_t*>(ksc + tt)[b] = (uint8_t)sc;
+  }
+  __syncthreads();
+
+  // S of every (head, token) of the chunk, scaled for the softmax
+  for (int i = tid; i < G * nt; i += kThreadsD) {
+    const int h = i / nt, tt = i % nt;
+    const uint4* kr = reinterpret_cast<const uint4*>(kc + tt * (kD / 2));
+    const uint32_t scw = ksc[tt];
+    float s = 0.0f;
+#pragma unroll 1
+    for (int b = 0; b < 4; ++b)
+      s += eq6_block(kr[b], &qf[h * kD + 32 * b], qmeta[h * 4 + b], (int)((scw >> (8 * b)) & 0xFFu) - 127);
+    zs[h * TB + tt] = __fmul_rn(s, a.sm_scale);
+  }
+  __syncthreads();
+  // the chunk's statistics, one warp per head
+  if (warp < G) {
+    const int h = warp;
+    float m = -INFINITY;
+    for (int tt = lane; tt < nt; tt += 32) m = fmaxf(m, zs[h * TB + tt]);
+    m = warp_max(m);
+    float e = 0.0f;
+    for (int tt = lane; tt < nt; tt += 32) e += expf(zs[h * TB + tt] - m);
+    e = warp_sum(e);
+    if (lane == 0) a.stats[((int64_t)g * NC + c) * G + h] = make_float2(m, e);
+  }
+  if (!dec_barrier(a, gridDim.x, &ok_s)) return;
+
+  // ---- B. the softmax over every chunk of this KV head, P, P-V
+  if (warp < G) {
+    const int h = warp;
+    const float2* st = a.stats + (int64_t)g * NC * G + h;
+    float m = -INFINITY;
+    for (int j = lane; j < NC; j += 32) m = fmaxf(m, __ldcg(st + (int64_t)j * G).x);
+    m = warp_max(m);
+    float l = 0.0f;
+    for (int j = lane; j < NC; j += 32) {
+      const float2 v = __ldcg(st + (int64_t)j * G);
+      l += v.y * expf(v.x - m);
+    }
+    l = warp_sum(l);
+    if (lane == 0) {
+      gm[h] = m;
+      gl[h] = l;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < G * nblk * 32; i += kThreadsD) {
+    const int h = i / (nblk * 32), j = i % (nblk * 32);
+    const int64_t t = t0 + j;
+    const float p = j < nt ? __fdiv_rn(expf(zs[h * TB + j] - gm[h]), gl[h]) : 0.0f;
+    zs[h * TB + j] = p;
+    if (a.p_values != nullptr) a.p_values[(int64_t)(g * G + h) * a.v_ld + t] = p;
+  }
+  __syncthreads();
+  // P -> MiX-4.5b: four lanes per (head, 32-token block), whole warps
+  for (int w0 = warp * 8; w0 < G * nblk; w0 += (kThreadsD / 32) * 8) {
+    const int blk = w0 + (lane >> 2), qq = lane & 3;
+    const bool on = blk < G * nblk;
+    const int h = on ? blk / nblk : 0, b = on ? blk % nblk : 0;
+    uint32_t u[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      u[i] = on ? __float_as_uint(zs[h * TB + 32 * b + 8 * qq + i]) : 0u;
+      if ((u[i] & 0x7FFFFFFFu) > 0x7F800000u) u[i] = 0u;  // NaN codes as zero
+    }
+    uint32_t sh;
+    const uint32_t word = mix_block32_quad(u, qq, a.p_ebias, true, sh);
+    if (on) {
+      mix_unpack_quad(word, sh, qq, a.p_ebias, &pf[h * TB + 32 * b], &pmeta[h * nb + b]);
+      if (a.p_codes != nullptr) {
+        const int64_t e = (int64_t)(g * G + h) * a.v_ld + t0 + 32 * b;
+        reinterpret_cast<uint32_t*>(a.p_codes + e / 2)[qq] = word;
+        if (qq == 0) a.p_shared[e / 32] = (uint16_t)sh;
+      }
+    }
+  }
+  __syncthreads();
+  // the chunk's partial O of (head, channel)
+  for (int i = tid; i < G * kD; i += kThreadsD) {
+    const int h = i / kD, d = i % kD;
+    float acc = 0.0f;
+#pragma unroll 1
+    for (int b = 0; b < nblk; ++b) acc += eq6_block(vsm[b * kD + d], &pf[h * TB + 32 * b], pmeta[h * nb + b], vxs[b * kD + d]);
+    a.opart[(((int64_t)g * NC + c) * G + h) * kD + d] = acc;
+  }
+  if (!dec_barrier(a, 2u * gridDim.x, &ok_s)) return;
+
+  // ---- C. O = the partial outputs summed in chunk order, a slice per CTA
+  const int64_t total = (int64_t)a.HQ * kD;
+  const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+  const int64_t o0 = (int64_t)blockIdx.x * per, o1 = min(total, o0 + per);
+  for (int64_t o = o0 + tid; o < o1; o += kThreadsD) {
+    const int hq = (int)(o / kD), d = (int)(o % kD);
+    const int gg = hq / G, h = hq % G;
+    const float* src = a.opart + ((int64_t)gg * NC * G + h) * kD + d;
+    const int64_t step = (int64_t)G * kD;
+    float sum = 0.0f;
+    int j = 0;
+    for (; j + 8 <= NC; j += 8) {
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + (int64_t)(j + i) * step);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum += v[i];
+    }
+    for (; j < NC; ++j) sum += __ldcg(src + (int64_t)j * step);
+    a.out[o] = sum;
+  }
+}
+
+
+// ------------------------------------------------------ long caches
+// When a chunk of the one-kernel grid no longer fits in shared memory (tens
+// of thousands of tokens), the step runs as two kernels instead:
+//  attn_qk_kernel  grid (64-token chunks, KV heads), one thread per (query
+//                  head, token): quantises the query heads, appends the new
+//                  key, S by Eq. (6), the chunk's softmax statistics;
+//  attn_pv_kernel  grid (256-token chunks, KV heads), one thread per (query
+//                  head, channel): combines the statistics, P, MiX-4.5b
+//                  requantisation, P-V by Eq. (6) into a partial O; the last
+//                  CTA of a KV head (an atomic ticket, no waiting) sums the
+//                  partials in chunk order.
+constexpr int kChunkA = 64;      // tokens per CTA of the Q-K^T kernel
+constexpr int kChunkB = 256;     // tokens per CTA of the P-V kernel (8 blocks of 32)
+
+struct AttnArgs2 {  // the two-kernel path
+  const void* q;
+  const void* k_new;
+  const float* k_mean;
+  int bf16;
+  uint8_t* k_codes;
+  uint8_t* k_scales;
+  const uint8_t* v_codes;
+  const uint8_t* v_scales;
+  int64_t v_ld;
+  int64_t T, Tpad;
+  int CA, CB, HQ, HK, G;
+  float sm_scale;
+  int q_ebias, p_ebias;
+  float* S;        // [HQ][Tpad]
+  float2* stats;   // [CA][HQ] (chunk max, chunk sum of exp)
+  float* opart;    // [CB][HQ][D]
+  unsigned* tickets;  // [HK]
+  float* out;      // [HQ][D]
+  uint8_t* p_codes;    // optional [HQ][v_ld / 2]
+  uint16_t* p_shared;  // optional [HQ][v_ld / 32]
+  float* p_values;     // optional [HQ][v_ld]: the P that was quantised
+};
+
+__global__ void __launch_bounds__(kChunkA * kMaxG, 2) attn_qk_kernel(AttnArgs2 a) {
   __shared__ __align__(16) int16_t qf[kMaxG][kD];
   __shared__ int2 qmeta[kMaxG][kD / 32];
   __shared__ float red[2 * kMaxG];
@@ -261,7 +543,7 @@ __global__ void __launch_bounds__(kChunkA * kMaxG, 2) attn_qk_kernel(AttnArgs a)
     a.stats[(int64_t)c * a.HQ + g * a.G + tid] = make_float2(cmax[tid], red[2 * tid] + red[2 * tid + 1]);
 }
 
-__global__ void __launch_bounds__(kD * kMaxG) attn_pv_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kD * kMaxG) attn_pv_kernel(AttnArgs2 a) {
   __shared__ __align__(16) int16_t pf[kMaxG][kChunkB];
   __shared__ int2 pmeta[kMaxG][kChunkB / 32];
   __shared__ __align__(16) float pv[kMaxG][kChunkB];
@@ -365,17 +647,75 @@ __global__ void __launch_bounds__(kD * kMaxG) attn_pv_kernel(AttnArgs a) {
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
-}  // namespace
+// Chunk length: the smallest multiple of 32 that lets KV heads x chunks fit
+// the SMs once.
+int dec_chunk(int64_t T, int HK) {
+  int64_t per = num_sms() / HK;
+  if (per < 1) per = 1;
+  int64_t tb = (T + per - 1) / per;
+  tb = (tb + 31) / 32 * 32;
+  return (int)(tb < 32 ? 32 : tb);
+}
 
-size_t decode_attention_ws_bytes(const mix_decode_attn_desc_t& d) {
+size_t one_ws_bytes(const mix_decode_attn_desc_t& d) {
+  const int TB = dec_chunk(d.tokens, d.kv_heads);
+  const int64_t NC = (d.tokens + TB - 1) / TB, G = d.q_heads / d.kv_heads;
+  return align256((size_t)d.kv_heads * NC * G * 8) + align256((size_t)d.kv_heads * NC * G * kD * 4) + 256 + 256;
+}
+
+cudaError_t launch_one(const mix_decode_attn_desc_t& d, void* ws, cudaStream_t st) {
+  AttnArgs a{};
+  const int TB = dec_chunk(d.tokens, d.kv_heads);
+  const int64_t NC = (d.tokens + TB - 1) / TB;
+  a.q = d.q; a.k_new = d.k_new; a.k_mean = d.k_mean; a.bf16 = d.dtype == MIX_DT_BF16;
+  a.k_codes = d.k_codes; a.k_scales = d.k_scales; a.v_codes = d.v_codes; a.v_scales = d.v_scales; a.v_ld = d.v_ld;
+  a.T = d.tokens; a.NC = (int)NC; a.TB = TB; a.HQ = d.q_heads; a.HK = d.kv_heads;
+  a.G = d.q_heads / d.kv_heads; a.sm_scale = d.sm_scale; a.q_ebias = d.q_ebias; a.p_ebias = d.p_ebias;
+  char* p = reinterpret_cast<char*>((reinterpret_cast<uintptr_t>(ws) + 255) & ~static_cast<uintptr_t>(255));
+  a.stats = reinterpret_cast<float2*>(p);
+  p += align256((size_t)d.kv_heads * NC * a.G * 8);
+  a.opart = reinterpret_cast<float*>(p);
+  p += align256((size_t)d.kv_heads * NC * a.G * kD * 4);
+  a.counter = reinterpret_cast<unsigned*>(p);
+  a.limit = 1LL << 31;
+  a.out = d.out; a.p_codes = d.p_codes; a.p_shared = static_cast<uint16_t*>(d.p_shared);
+  a.p_values = d.p_values;
+  cudaError_t e = cudaMemsetAsync(a.counter, 0, sizeof(unsigned), st);
+  if (e != cudaSuccess) return e;
+  e = device_error_word(&a.err);
+  if (e != cudaSuccess) return e;
+  const DecPlan L = dec_plan(TB);
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecMaxSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(d.kv_heads * NC));
+  cfg.blockDim = dim3(kThreadsD);
+  cfg.dynamicSmemBytes = (size_t)L.bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // CTAs wait on one another: all resident at once
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel, a);
+}
+
+size_t two_ws_bytes(const mix_decode_attn_desc_t& d) {
   const int64_t CB = (d.tokens + kChunkB - 1) / kChunkB, CA = (d.tokens + kChunkA - 1) / kChunkA;
   const int64_t Tpad = CB * kChunkB;
   return align256((size_t)d.q_heads * Tpad * 4) + align256((size_t)CA * d.q_heads * 8) +
          align256((size_t)CB * d.q_heads * kD * 4) + align256((size_t)d.kv_heads * 4) + 256;
 }
 
-cudaError_t launch_decode_attention(const mix_decode_attn_desc_t& d, void* ws, cudaStream_t st) {
-  AttnArgs a{};
+cudaError_t launch_two(const mix_decode_attn_desc_t& d, void* ws, cudaStream_t st) {
+  AttnArgs2 a{};
   const int64_t CB = (d.tokens + kChunkB - 1) / kChunkB, CA = (d.tokens + kChunkA - 1) / kChunkA;
   a.q = d.q; a.k_new = d.k_new; a.k_mean = d.k_mean; a.bf16 = d.dtype == MIX_DT_BF16;
   a.k_codes = d.k_codes; a.k_scales = d.k_scales; a.v_codes = d.v_codes; a.v_scales = d.v_scales; a.v_ld = d.v_ld;
@@ -396,6 +736,21 @@ cudaError_t launch_decode_attention(const mix_decode_attn_desc_t& d, void* ws, c
   if (e != cudaSuccess) return e;
   attn_pv_kernel<<<dim3((unsigned)CB, (unsigned)d.kv_heads), kD * a.G, 0, st>>>(a);
   return cudaGetLastError();
+}
+
+// The one-kernel path when a chunk fits in shared memory.
+bool one_kernel_fits(const mix_decode_attn_desc_t& d) {
+  return dec_plan(dec_chunk(d.tokens, d.kv_heads)).bytes <= kDecMaxSmem;
+}
+
+}  // namespace
+
+size_t decode_attention_ws_bytes(const mix_decode_attn_desc_t& d) {
+  return one_kernel_fits(d) ? one_ws_bytes(d) : two_ws_bytes(d);
+}
+
+cudaError_t launch_decode_attention(const mix_decode_attn_desc_t& d, void* ws, cudaStream_t st) {
+  return one_kernel_fits(d) ? launch_one(d, ws, st) : launch_two(d, ws, st);
 }
 
 }  // namespace mixk

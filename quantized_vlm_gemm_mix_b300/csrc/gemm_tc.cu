@@ -1024,8 +1024,25 @@ cudaError_t launch_staged(const CUtensorMap& ma, const CUtensorMap& mb, const CU
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  gemm_staged_kernel<B_NATIVE, SPLIT><<<grid, NUM_THREADS_S, PlanS::SMEM_BYTES, st>>>(ma, mb, mc, p);
-  const cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (SPLIT) {
+    // the heads of cut tiles wait for other CTAs' parts: a cooperative launch,
+    // so that every CTA of the grid (one per SM) is resident at once
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NUM_THREADS_S);
+    cfg.dynamicSmemBytes = PlanS::SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemm_staged_kernel<B_NATIVE, SPLIT>, ma, mb, mc, p);
+  } else {
+    gemm_staged_kernel<B_NATIVE, SPLIT><<<grid, NUM_THREADS_S, PlanS::SMEM_BYTES, st>>>(ma, mb, mc, p);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess && std::getenv("MIX_DEBUG") != nullptr)
     std::fprintf(stderr, "gemm_staged launch: %s\n", cudaGetErrorString(e));
   return e;

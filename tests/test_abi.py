@@ -163,8 +163,13 @@ def test_decode_attention_validation(mix):
     d.q = d.k_codes = d.k_scales = d.v_codes = d.v_scales = d.out = 4096   # placeholders, never dereferenced
     d.v_ld, d.sm_scale, d.q_ebias, d.p_ebias = 128, 0.088, -8, -15
     need = L.mix_decode_attention_workspace_bytes(ctypes.byref(d))
-    # S [28][256] + statistics [2][28] + partial O [1][28][128] + tickets, each 256-aligned, + 256
-    assert need == 28 * 256 * 4 + 512 + 28 * 128 * 4 + 256 + 256
+    # one cooperative kernel over 4 KV heads x NC chunks of at least 32 tokens
+    # (the SMs shared out per KV head: 100 tokens -> 4 chunks of 32 here):
+    # statistics [4][NC][7] float2 + partial O [4][NC][7][128] + the barrier
+    # counter, each 256-aligned, + 256
+    nc = 4
+    al = lambda v: (v + 255) // 256 * 256
+    assert need == al(4 * nc * 7 * 8) + al(4 * nc * 7 * 128 * 4) + 256 + 256
     assert L.mix_decode_attention(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_WORKSPACE
     for field, value, want in (("q_heads", 64, mix.MIX_ERR_INVALID_ARG),     # 16 query heads per KV head
                                ("q_heads", 30, mix.MIX_ERR_INVALID_ARG),     # not a multiple of kv_heads

@@ -1,5 +1,6 @@
 """GPU parity of the fused MiX decode attention (frozen-mean K append, Q-K^T,
-softmax, MiX requantisation of P, P-V; two launches) against the oracle's
+softmax, MiX requantisation of P, P-V; one cooperative launch, or two for a
+cache too long for it) against the oracle's
 composition of the pinned steps.  The appended K' row is bit-exact; O is
 within 1e-3 of each head's largest |O|; the kernel's own fp32 P (a debug
 output) is within fp32 rounding of the oracle's softmax, and the P planes are
@@ -84,8 +85,11 @@ def check_p(T, sm, got, ref, orc):
 
 
 @pytest.mark.parametrize("T,HQ,HK", [(8192, 28, 4), (80, 28, 4), (1, 28, 4), (257, 28, 4), (300, 4, 4),
-                                     (1000, 16, 2)])
+                                     (1000, 16, 2), (40000, 8, 4)])
 def test_decode_attention_matches_oracle(mix, orc, T, HQ, HK):
+    """Up to a few tens of thousands of tokens the step is one kernel whose
+    chunks of keys, values and scores stay in shared memory; the 40000-token
+    cache (chunks of 1088 tokens) is too long for it and takes two kernels."""
     q, kn, mean, kc, ks, vc, vs = make_cache(orc, T + HQ, T, HQ, HK, prefill=max(1, T // 2))
     got, ref = run_both(mix, orc, q, kn, mean, kc, ks, vc, vs, T, 1 / np.sqrt(128.0))
     o, kcg, ksg = got[:3]
@@ -109,8 +113,8 @@ def test_decode_attention_no_append_f32(mix, orc):
 
 
 def test_decode_attention_repeat_is_identical(mix, orc):
-    """The ticket reset and the chunk-order reduction make repeated calls give
-    identical bits."""
+    """The barrier counter reset and the chunk-order reductions make repeated
+    calls give identical bits."""
     import torch
     T, HQ, HK = 2048, 28, 4
     q, kn, mean, kc, ks, vc, vs = make_cache(orc, 11, T, HQ, HK, prefill=1024)
