@@ -72,7 +72,7 @@ struct AttnArgs {
 
 // Shared memory of one CTA for TB tokens (offsets in bytes, 16-aligned).
 struct DecPlan {
-  int kc, ksc, vsm, vxs, qf, qmeta, zs, pf, pmeta, stat, bytes;
+  int kc, ksc, vsm, vxs, qf, qmeta, zs, pf, pmeta, stat, red, bytes;
 };
 __host__ __device__ inline DecPlan dec_plan(int TB) {
   DecPlan p;
@@ -88,6 +88,7 @@ __host__ __device__ inline DecPlan dec_plan(int TB) {
   p.pf = o;    o += kMaxG * TB * 2;                   // MiX factors of P
   p.pmeta = o; o += kMaxG * nb * 8;
   p.stat = o;  o += 2 * kMaxG * 4;                    // global max and sum per head
+  p.red = o;   o += 4 * kMaxG * kD * 4;               // P-V sums of four block groups
   p.bytes = (o + 15) & ~15;
   return p;
 }
@@ -184,6 +185,32 @@ __device__ __forceinline__ float eq6_block(const uint4& cw, const int16_t* f, in
   return scale_pow2((float)blockv, meta.x + X - 12);  // 2^(Emax + X - 10 - c_B), c_B = 2 for MXINT4
 }
 
+// The same block product with the 32 INT4 weights already widened to int8
+// (eight words of four lanes, nib4_to_s8 of each half-word in order), for a
+// weight block used by several heads.
+__device__ __forceinline__ void int4x32_to_s8(const uint4& cw, uint32_t* s8) {
+  const uint32_t w[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    s8[2 * q] = nib4_to_s8(w[q] & 0xFFFFu);
+    s8[2 * q + 1] = nib4_to_s8(w[q] >> 16);
+  }
+}
+__device__ __forceinline__ float eq6_block_s8(const uint32_t* s8, const int16_t* f, int2 meta, int X) {
+  int blockv = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int4 fv = *reinterpret_cast<const int4*>(f + 8 * q);
+    const int lo = (int)s8[2 * q], hi = (int)s8[2 * q + 1];
+    int sq = __dp2a_lo(fv.x, lo, 0);
+    sq = __dp2a_hi(fv.y, lo, sq);
+    sq = __dp2a_lo(fv.z, hi, sq);
+    sq = __dp2a_hi(fv.w, hi, sq);
+    blockv += sq * (8 + ((meta.y >> (8 * q)) & 0xFF));
+  }
+  return scale_pow2((float)blockv, meta.x + X - 12);
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
@@ -214,7 +241,6 @@ __device__ __forceinline__ bool dec_barrier(const AttnArgs& a, unsigned target, 
         ok = 0;
         break;
       }
-      __nanosleep(32);
     }
     *ok_s = ok;
   }
@@ -302,16 +328,26 @@ __global__ void __launch_bounds__(kThreadsD, 1) attn_decode_kernel(AttnArgs a) {
   }
   __syncthreads();
 
-  // S of every (head, token) of the chunk, scaled for the softmax
-  for (int i = tid; i < G * nt; i += kThreadsD) {
-    const int h = i / nt, tt = i % nt;
+  // S of every (head, token) of the chunk, scaled for the softmax: one
+  // thread per (token, group of up to four heads); the token's K' row is
+  // widened to int8 once and serves every head of the group
+  const int HG = (G + 3) / 4;
+  for (int i = tid; i < nt * HG; i += kThreadsD) {
+    const int tt = i % nt, hg = i / nt;
     const uint4* kr = reinterpret_cast<const uint4*>(kc + tt * (kD / 2));
     const uint32_t scw = ksc[tt];
-    float s = 0.0f;
+    uint32_t s8[4][8];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) int4x32_to_s8(kr[b], s8[b]);
+    const int h1 = min(G, 4 * hg + 4);
 #pragma unroll 1
-    for (int b = 0; b < 4; ++b)
-      s += eq6_block(kr[b], &qf[h * kD + 32 * b], qmeta[h * 4 + b], (int)((scw >> (8 * b)) & 0xFFu) - 127);
-    zs[h * TB + tt] = __fmul_rn(s, a.sm_scale);
+    for (int h = 4 * hg; h < h1; ++h) {
+      float s = 0.0f;
+#pragma unroll
+      for (int b = 0; b < 4; ++b)
+        s += eq6_block_s8(s8[b], &qf[h * kD + 32 * b], qmeta[h * 4 + b], (int)((scw >> (8 * b)) & 0xFFu) - 127);
+      zs[h * TB + tt] = __fmul_rn(s, a.sm_scale);
+    }
   }
   __syncthreads();
   // the chunk's statistics, one warp per head
@@ -329,27 +365,35 @@ __global__ void __launch_bounds__(kThreadsD, 1) attn_decode_kernel(AttnArgs a) {
 
   // ---- B. the softmax over every chunk of this KV head, P, P-V
   if (warp < G) {
+    // NC <= 160 chunks: each lane holds its (up to five) chunk statistics in
+    // registers, so the maximum and the sum need one round of loads
     const int h = warp;
     const float2* st = a.stats + (int64_t)g * NC * G + h;
+    float2 v[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+      const int j = lane + 32 * i;
+      v[i] = j < NC ? __ldcg(st + (int64_t)j * G) : make_float2(-INFINITY, 0.0f);
+    }
     float m = -INFINITY;
-    for (int j = lane; j < NC; j += 32) m = fmaxf(m, __ldcg(st + (int64_t)j * G).x);
+#pragma unroll
+    for (int i = 0; i < 5; ++i) m = fmaxf(m, v[i].x);
     m = warp_max(m);
     float l = 0.0f;
-    for (int j = lane; j < NC; j += 32) {
-      const float2 v = __ldcg(st + (int64_t)j * G);
-      l += v.y * expf(v.x - m);
-    }
+#pragma unroll
+    for (int i = 0; i < 5; ++i)
+      if (lane + 32 * i < NC) l += v[i].y * expf(v[i].x - m);
     l = warp_sum(l);
     if (lane == 0) {
       gm[h] = m;
-      gl[h] = l;
+      gl[h] = __frcp_rn(l);  // P = exp(z - m) * (1 / l)
     }
   }
   __syncthreads();
   for (int i = tid; i < G * nblk * 32; i += kThreadsD) {
     const int h = i / (nblk * 32), j = i % (nblk * 32);
     const int64_t t = t0 + j;
-    const float p = j < nt ? __fdiv_rn(expf(zs[h * TB + j] - gm[h]), gl[h]) : 0.0f;
+    const float p = j < nt ? __fmul_rn(expf(zs[h * TB + j] - gm[h]), gl[h]) : 0.0f;
     zs[h * TB + j] = p;
     if (a.p_values != nullptr) a.p_values[(int64_t)(g * G + h) * a.v_ld + t] = p;
   }
@@ -377,36 +421,64 @@ __global__ void __launch_bounds__(kThreadsD, 1) attn_decode_kernel(AttnArgs a) {
     }
   }
   __syncthreads();
-  // the chunk's partial O of (head, channel)
+  // the chunk's partial O of (head, channel): one thread per (channel, group
+  // of blocks) widens the group's V words to int8 once for every head, two
+  // blocks at a time; the four groups' sums are then added in group order
+  constexpr int BG = 4;
+  float* red = reinterpret_cast<float*>(dsm + L.red);  // [BG][kMaxG][kD]
+  const int bpg = (nblk + BG - 1) / BG;
+  for (int i = tid; i < BG * kD; i += kThreadsD) {
+    const int d = i % kD, bg = i / kD;
+    const int b0 = bg * bpg, b1 = min(nblk, b0 + bpg);
+    for (int h = 0; h < G; ++h) red[(bg * kMaxG + h) * kD + d] = 0.0f;
+    for (int bb = b0; bb < b1; bb += 2) {
+      const bool two = bb + 1 < b1;
+      uint32_t v8[2][8];
+      int4x32_to_s8(vsm[bb * kD + d], v8[0]);
+      int4x32_to_s8(two ? vsm[(bb + 1) * kD + d] : make_uint4(0, 0, 0, 0), v8[1]);
+      const int x0 = vxs[bb * kD + d], x1 = two ? vxs[(bb + 1) * kD + d] : 0;
+#pragma unroll 1
+      for (int h = 0; h < G; ++h) {
+        float acc = red[(bg * kMaxG + h) * kD + d];
+        acc += eq6_block_s8(v8[0], &pf[h * TB + 32 * bb], pmeta[h * nb + bb], x0);
+        if (two) acc += eq6_block_s8(v8[1], &pf[h * TB + 32 * (bb + 1)], pmeta[h * nb + bb + 1], x1);
+        red[(bg * kMaxG + h) * kD + d] = acc;
+      }
+    }
+  }
+  __syncthreads();
   for (int i = tid; i < G * kD; i += kThreadsD) {
     const int h = i / kD, d = i % kD;
     float acc = 0.0f;
-#pragma unroll 1
-    for (int b = 0; b < nblk; ++b) acc += eq6_block(vsm[b * kD + d], &pf[h * TB + 32 * b], pmeta[h * nb + b], vxs[b * kD + d]);
+#pragma unroll
+    for (int bg = 0; bg < BG; ++bg) acc += red[(bg * kMaxG + h) * kD + d];
     a.opart[(((int64_t)g * NC + c) * G + h) * kD + d] = acc;
   }
   if (!dec_barrier(a, 2u * gridDim.x, &ok_s)) return;
 
-  // ---- C. O = the partial outputs summed in chunk order, a slice per CTA
+  // ---- C. O = the partial outputs summed over the chunks, a slice of the
+  // outputs per CTA and one warp per output: lane l adds chunks l, l + 32, ...
+  // (up to five, loaded at once) and the warp's butterfly adds the lanes, the
+  // same fixed order for every output
   const int64_t total = (int64_t)a.HQ * kD;
   const int64_t per = (total + gridDim.x - 1) / gridDim.x;
   const int64_t o0 = (int64_t)blockIdx.x * per, o1 = min(total, o0 + per);
-  for (int64_t o = o0 + tid; o < o1; o += kThreadsD) {
+  for (int64_t o = o0 + warp; o < o1; o += kThreadsD / 32) {
     const int hq = (int)(o / kD), d = (int)(o % kD);
     const int gg = hq / G, h = hq % G;
     const float* src = a.opart + ((int64_t)gg * NC * G + h) * kD + d;
     const int64_t step = (int64_t)G * kD;
-    float sum = 0.0f;
-    int j = 0;
-    for (; j + 8 <= NC; j += 8) {
-      float v[8];
+    float v[5];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + (int64_t)(j + i) * step);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sum += v[i];
+    for (int i = 0; i < 5; ++i) {
+      const int j = lane + 32 * i;
+      v[i] = j < NC ? __ldcg(src + (int64_t)j * step) : 0.0f;
     }
-    for (; j < NC; ++j) sum += __ldcg(src + (int64_t)j * step);
-    a.out[o] = sum;
+    float sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 5; ++i) sum += v[i];
+    sum = warp_sum(sum);
+    if (lane == 0) a.out[o] = sum;
   }
 }
 
@@ -652,6 +724,7 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 int dec_chunk(int64_t T, int HK) {
   int64_t per = num_sms() / HK;
   if (per < 1) per = 1;
+  if (per > 160) per = 160;  // the kernel's per-lane registers hold at most 160 chunks
   int64_t tb = (T + per - 1) / per;
   tb = (tb + 31) / 32 * 32;
   return (int)(tb < 32 ? 32 : tb);
