@@ -49,7 +49,7 @@ def test_step_table_flops_and_shapes(small):
         if m:                                        # kv heads x group x cache tokens x head_dim
             HK, G, TC, D = map(int, m.groups())
             assert flops == 2.0 * 2.0 * HK * G * TC * D          # q K'^T and P V
-            assert launches == 2
+            assert launches == 1
 
 
 def test_decode_attention_bytes():
