@@ -395,51 +395,65 @@ template <bool FP4>
 __global__ void __launch_bounds__(kThreads, 4) mx_quantize_cols_bf16_kernel(
     const uint16_t* __restrict__ x, int64_t kdim, int64_t n, int64_t ld, int rule,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  // The CTA's 64 columns x 8 k-blocks of output are staged in shared memory
+  // ([column][k-block], one pad slot per column), then written out whole: a
+  // column's codes for the 8 k-blocks are 128 contiguous bytes, its scales 8.
+  __shared__ uint4 cs[64][9];
+  __shared__ uint8_t ss[64][8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nbk = kdim / 32;
   const int64_t kb = (int64_t)blockIdx.y * 8 + warp;
   const int64_t n0 = (int64_t)blockIdx.x * 64 + 2 * lane;
-  if (kb >= nbk || n0 >= n) return;
-  const bool two = n0 + 1 < n;
-  uint32_t v[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const uint16_t* p = x + (kb * 32 + i) * ld + n0;
-    v[i] = two ? __ldcs(reinterpret_cast<const unsigned int*>(p)) : (uint32_t)__ldcs(p);
-  }
-  uint32_t m = 0;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) m = vmax_u16x2(m, v[i] & 0x7FFF7FFFu);
-  if (((m & 0xFFFFu) > 0x7F80u) || ((m >> 16) > 0x7F80u)) {  // a NaN in one of the two blocks
-    m = 0;
+  if (kb < nbk && n0 < n) {
+    const bool two = n0 + 1 < n;
+    uint32_t v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      v[i] &= ~__vcmpgtu2(v[i] & 0x7FFF7FFFu, 0x7F807F80u);
-      m = vmax_u16x2(m, v[i] & 0x7FFF7FFFu);
+      const uint16_t* p = x + (kb * 32 + i) * ld + n0;
+      v[i] = two ? __ldcs(reinterpret_cast<const unsigned int*>(p)) : (uint32_t)__ldcs(p);
+    }
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = vmax_u16x2(m, v[i] & 0x7FFF7FFFu);
+    if (((m & 0xFFFFu) > 0x7F80u) || ((m >> 16) > 0x7F80u)) {  // a NaN in one of the two blocks
+      m = 0;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        v[i] &= ~__vcmpgtu2(v[i] & 0x7FFF7FFFu, 0x7F807F80u);
+        m = vmax_u16x2(m, v[i] & 0x7FFF7FFFu);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint32_t kbits = c ? (m & 0xFFFF0000u) : (m << 16);
+      uint4 w = make_uint4(0u, 0u, 0u, 0u);
+      uint32_t sc = 0u;
+      if (kbits != 0u) {
+        const int X = mx_shared_exp(kbits, FP4, rule);
+        uint32_t wd[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t t[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) t[i] = c ? (v[8 * j + i] & 0xFFFF0000u) : (v[8 * j + i] << 16);
+          wd[j] = mx_codes8(t, X, FP4);
+        }
+        w = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        sc = (uint32_t)(X + 127);
+      }
+      cs[2 * lane + c][warp] = w;
+      ss[2 * lane + c][warp] = (uint8_t)sc;
     }
   }
-#pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    if (c == 1 && !two) break;
-    const uint32_t kbits = c ? (m & 0xFFFF0000u) : (m << 16);
-    uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    uint32_t sc = 0u;
-    if (kbits != 0u) {
-      const int X = mx_shared_exp(kbits, FP4, rule);
-      uint32_t wd[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        uint32_t t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = c ? (v[8 * j + i] & 0xFFFF0000u) : (v[8 * j + i] << 16);
-        wd[j] = mx_codes8(t, X, FP4);
-      }
-      w = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-      sc = (uint32_t)(X + 127);
+  __syncthreads();
+  const int64_t c0 = (int64_t)blockIdx.x * 64, k0 = (int64_t)blockIdx.y * 8;
+  for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {
+    const int cl = i >> 3, kl = i & 7;
+    const int64_t col = c0 + cl, kbo = k0 + kl;
+    if (col < n && kbo < nbk) {
+      *reinterpret_cast<uint4*>(codes + col * (kdim / 2) + kbo * 16) = cs[cl][kl];
+      scales[col * nbk + kbo] = ss[cl][kl];
     }
-    const int64_t col = n0 + c;
-    *reinterpret_cast<uint4*>(codes + col * (kdim / 2) + kb * 16) = w;
-    scales[col * nbk + kb] = (uint8_t)sc;
   }
 }
 
