@@ -461,57 +461,73 @@ template <bool BF16, bool FP4, bool G16>
 __global__ void __launch_bounds__(kThreads) mx_quantize_cols_kernel(
     const void* __restrict__ x, int64_t kdim, int64_t n, int64_t ld, int rule,
     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  // outputs staged per CTA as in mx_quantize_cols_bf16_kernel: a column's 8
+  // k-blocks of codes (128 bytes) and of scales (8, or 16 for g16) contiguous
+  constexpr int SPB = G16 ? 2 : 1;  // scale bytes per 32-row block
+  __shared__ uint4 cs[64][9];
+  __shared__ uint8_t ss[64][8 * SPB];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t nbk = kdim / 32;
   const int64_t kb = (int64_t)blockIdx.y * 8 + warp;
   const int64_t n0 = (int64_t)blockIdx.x * 64 + 2 * lane;
-  if (kb >= nbk || n0 >= n) return;
-  const bool two = n0 + 1 < n;
-  uint32_t u0[32], u1[32];
+  if (kb < nbk && n0 < n) {
+    const bool two = n0 + 1 < n;
+    uint32_t u0[32], u1[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int64_t off = (kb * 32 + i) * ld + n0;
-    if (BF16) {
-      const uint16_t* p = static_cast<const uint16_t*>(x) + off;
-      if (two) {
-        const uint32_t v = __ldcs(reinterpret_cast<const unsigned int*>(p));
-        u0[i] = v << 16;
-        u1[i] = v & 0xFFFF0000u;
+    for (int i = 0; i < 32; ++i) {
+      const int64_t off = (kb * 32 + i) * ld + n0;
+      if (BF16) {
+        const uint16_t* p = static_cast<const uint16_t*>(x) + off;
+        if (two) {
+          const uint32_t v = __ldcs(reinterpret_cast<const unsigned int*>(p));
+          u0[i] = v << 16;
+          u1[i] = v & 0xFFFF0000u;
+        } else {
+          u0[i] = (uint32_t)__ldcs(p) << 16;
+          u1[i] = 0;
+        }
       } else {
-        u0[i] = (uint32_t)__ldcs(p) << 16;
-        u1[i] = 0;
+        const float* p = static_cast<const float*>(x) + off;
+        if (two) {
+          const float2 v = __ldcs(reinterpret_cast<const float2*>(p));
+          u0[i] = __float_as_uint(v.x);
+          u1[i] = __float_as_uint(v.y);
+        } else {
+          u0[i] = __float_as_uint(__ldcs(p));
+          u1[i] = 0;
+        }
       }
-    } else {
-      const float* p = static_cast<const float*>(x) + off;
-      if (two) {
-        const float2 v = __ldcs(reinterpret_cast<const float2*>(p));
-        u0[i] = __float_as_uint(v.x);
-        u1[i] = __float_as_uint(v.y);
+    }
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint32_t* u = c ? u1 : u0;
+      const int cl = 2 * lane + c;
+      if (G16) {
+        uint2 w0, w1;
+        uint32_t s0, s1;
+        mx_block16<FP4>(u, rule, w0, s0);
+        mx_block16<FP4>(u + 16, rule, w1, s1);
+        cs[cl][warp] = make_uint4(w0.x, w0.y, w1.x, w1.y);
+        ss[cl][2 * warp] = (uint8_t)s0;
+        ss[cl][2 * warp + 1] = (uint8_t)s1;
       } else {
-        u0[i] = __float_as_uint(__ldcs(p));
-        u1[i] = 0;
+        uint4 w;
+        uint32_t sc;
+        mx_block32<FP4>(u, rule, w, sc);
+        cs[cl][warp] = w;
+        ss[cl][warp] = (uint8_t)sc;
       }
     }
   }
+  __syncthreads();
+  const int64_t c0 = (int64_t)blockIdx.x * 64, k0 = (int64_t)blockIdx.y * 8;
+  for (int i = threadIdx.x; i < 64 * 8; i += blockDim.x) {
+    const int cl = i >> 3, kl = i & 7;
+    const int64_t col = c0 + cl, kbo = k0 + kl;
+    if (col < n && kbo < nbk) {
+      *reinterpret_cast<uint4*>(codes + col * (kdim / 2) + kbo * 16) = cs[cl][kl];
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    if (c == 1 && !two) break;
-    uint32_t* u = c ? u1 : u0;
-    const int64_t col = n0 + c;
-    if (G16) {
-      uint2 w0, w1;
-      uint32_t s0, s1;
-      mx_block16<FP4>(u, rule, w0, s0);
-      mx_block16<FP4>(u + 16, rule, w1, s1);
-      *reinterpret_cast<uint4*>(codes + col * (kdim / 2) + kb * 16) = make_uint4(w0.x, w0.y, w1.x, w1.y);
-      scales[col * 2 * nbk + 2 * kb] = (uint8_t)s0;
-      scales[col * 2 * nbk + 2 * kb + 1] = (uint8_t)s1;
-    } else {
-      uint4 w;
-      uint32_t sc;
-      mx_block32<FP4>(u, rule, w, sc);
-      *reinterpret_cast<uint4*>(codes + col * (kdim / 2) + kb * 16) = w;
-      scales[col * nbk + kb] = (uint8_t)sc;
+      for (int j = 0; j < SPB; ++j) scales[(col * nbk + kbo) * SPB + j] = ss[cl][SPB * kl + j];
     }
   }
 }
