@@ -905,6 +905,43 @@ def single_call(args):
                           a_batch_stride=D, b_ld=HK * D, b_batch_stride=D, algo=mix.MIX_GEMM_TCGEN05)
         ws = torch.empty(max(16, mix.mix_mx_gemm_workspace_bytes(d)), dtype=torch.uint8, device=dev)
         fn = lambda: mix.mix_mx_gemm(d, ws)
+    elif name.startswith("ksmooth_compute_"):
+        # the prefill keys of one layer: mean over the tokens and K' = K - mean
+        T, HK, D = g["T"], g["HK"], g["D"]
+        _, k, _ = synth.attention_qkv(0, T, g["HQ"], HK, D)
+        kd = bf16(synth.to_bf16_bits(k).reshape(T, HK * D))
+        del k
+        mean = torch.empty((HK, D), dtype=torch.float32, device=dev)
+        kout = torch.empty((T, HK, D), dtype=torch.float32, device=dev)
+        ws = torch.empty(mix.ksmooth_workspace_bytes(T, HK, D), dtype=torch.uint8, device=dev)
+        fn = lambda: mix.ksmooth_kv(kd, T, HK, D, HK * D, mean, mix.KSMOOTH_COMPUTE, kout, ws)
+    elif name.startswith("decode_attention_"):
+        # one decode step over the TC-token MX cache (K' smoothed with the mean
+        # of its first half, the new key appended each call)
+        TC, HQ, HK, D = g["TC"], g["HQ"], g["HK"], g["D"]
+        q, k, v = synth.attention_qkv(0, TC, HQ, HK, D)
+        kd = bf16(synth.to_bf16_bits(k).reshape(TC, HK * D))
+        vd = bf16(synth.to_bf16_bits(v).reshape(TC, HK * D))
+        qn = bf16(synth.to_bf16_bits(q[TC - 1]).reshape(HQ, D))
+        del q, k, v
+        mean = torch.empty((HK, D), dtype=torch.float32, device=dev)
+        kp = torch.empty((TC, HK, D), dtype=torch.float32, device=dev)
+        wsk = torch.empty(mix.ksmooth_workspace_bytes(TC // 2, HK, D), dtype=torch.uint8, device=dev)
+        mix.ksmooth_kv(kd, TC // 2, HK, D, HK * D, mean, mix.KSMOOTH_COMPUTE, kp[:TC // 2], wsk)
+        mix.ksmooth_kv(kd, TC, HK, D, HK * D, mean, mix.KSMOOTH_APPLY_FROZEN, kp)
+        kc = torch.empty((TC * HK, 64), dtype=torch.uint8, device=dev)
+        ks = torch.empty((TC * HK, 4), dtype=torch.uint8, device=dev)
+        mix.mx_quantize(kp, TC * HK, D, D, 1, INT4, 0, kc, ks)
+        vc = torch.empty((HK, D, TC // 2), dtype=torch.uint8, device=dev)
+        vs = torch.empty((HK, D, TC // 32), dtype=torch.uint8, device=dev)
+        for h in range(HK):
+            mix.mx_quantize(vd[:, h * D:(h + 1) * D], TC, D, HK * D, 0, INT4, 0, vc[h], vs[h])
+        out = torch.empty((HQ, D), dtype=torch.float32, device=dev)
+        dd = mix.decode_attention_desc(qn, kc.view(TC, HK, 64), ks.view(TC, HK, 4), vc, vs, TC, 1.0 / math.sqrt(D),
+                                       out, k_new=kd[TC - 1].view(HK, D), k_mean=mean)
+        ws = torch.empty(mix.lib.mix_decode_attention_workspace_bytes(ctypes.byref(dd)), dtype=torch.uint8,
+                         device=dev)
+        fn = lambda: mix.decode_attention(dd, ws)
     elif name.startswith("mix_quantize_t") and name.endswith(f"_{M}x{DM}"):
         t = T1 if name.startswith("mix_quantize_t1") else T2
         x = bf16(synth.to_bf16_bits(synth.vlm_activations(0, 1, M, DM, visual_rows=(3 * M) // 4)))
@@ -912,8 +949,8 @@ def single_call(args):
         sh = torch.empty((M, DM // 32), dtype=torch.uint8 if t == T1 else torch.int16, device=dev)
         fn = lambda: mix.mix_quantize(x, M, DM, DM, t, -8, 1, c, sh)
     else:
-        raise SystemExit(f"--call supports the prefill matmuls, the attention Q.K'^T and P.V and the MiX "
-                         f"quantisers of the sweep, not {name}")
+        raise SystemExit(f"--call supports the prefill matmuls, the attention Q.K'^T and P.V, K-smoothing, the "
+                         f"decode attention and the MiX quantisers of the sweep, not {name}")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # larger than L2
     times = []
     for i in range(args.warmup + args.steps):
