@@ -28,6 +28,7 @@ import ctypes
 import json
 import math
 import os
+import re
 import subprocess
 import sys
 import threading
@@ -190,8 +191,12 @@ def step_table(small=False):
         2.0 * HQ * T * T * D, launches=tc_launches(T), cpu=("gemm", HQ * T * T * (D // 32)))
     add(f"mix_quantize_t2_p_{HQ * T}x{T}", mix_bytes(HQ * T, T, 2), cpu=("mix2", HQ * T * T))
     add(f"mx_quantize_int4_v_{T}x{HK * D}", mx_bytes(HK * D, T), cpu=("mx", HK * D * T))
-    add(f"bmm_pv_{HQ}x{T}x{D}x{T}", plane_bytes(HQ * T, T, 2) + plane_bytes(HK * D, T, 0) + HQ * T * D * 4,
-        2.0 * HQ * T * D * T, launches=tc_launches(D), cpu=("gemm", HQ * T * D * (T // 32)))
+    # P is causal and the call says so: the work is P's 32-blocks that hold an
+    # unmasked entry (row r: blocks 0 .. r // 32; 16 code bytes and a 2-byte
+    # shared field each) and the products below the mask
+    pv_blocks = HQ * 32 * (T // 32) * (T // 32 + 1) // 2
+    add(f"bmm_pv_{HQ}x{T}x{D}x{T}", pv_blocks * 18 + plane_bytes(HK * D, T, 0) + HQ * T * D * 4,
+        2.0 * HQ * D * T * (T + 1) / 2, launches=tc_launches(D), cpu=("gemm", HQ * T * D * (T // 32)))
     # decode over the TC-token MX cache: one fused call (frozen-mean K append,
     # Q.K'^T, softmax, MiX requantisation of P, P.V; one cooperative kernel
     # after a counter reset)
@@ -423,8 +428,9 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
     v_pre = v_d[:T]
     fns[f"mx_quantize_int4_v_{T}x{HK * D}"] = lambda: mix.mx_quantize(v_pre, T, HK * D, HK * D, 0, INT4, 0, vqc, vqs)
     O = new((HQ, T, D), torch.float32)
+    # P is causal: the call states it, and the matmul skips the masked k-steps
     dpv = mix.gemm_desc(T, D, T, pc, ps, T2, -15, vqc, vqs, INT4, c=O, batch=HQ, b_group=HQ // HK,
-                        algo=mix.MIX_GEMM_TCGEN05)
+                        algo=mix.MIX_GEMM_TCGEN05, a_causal=1)
     _require(mix.mix_mx_gemm_workspace_bytes(dpv) <= ws_tc[0].numel(), "P.V workspace exceeds the shared staging buffer")
     fns[f"bmm_pv_{HQ}x{T}x{D}x{T}"] = tc_call(dpv)
     d2h.append(O)
@@ -883,7 +889,7 @@ def single_call(args):
         mix.mx_quantize(vb, T, HK * D, HK * D, 0, INT4, 0, vqc, vqs)
         O = torch.empty((HQ, T, D), dtype=torch.float32, device=dev)
         d = mix.gemm_desc(T, D, T, pc, ps, T2, -15, vqc, vqs, INT4, c=O, batch=HQ, b_group=HQ // HK,
-                          algo=mix.MIX_GEMM_TCGEN05)
+                          algo=mix.MIX_GEMM_TCGEN05, a_causal=1)
         ws = torch.empty(max(16, mix.mix_mx_gemm_workspace_bytes(d)), dtype=torch.uint8, device=dev)
         fn = lambda: mix.mix_mx_gemm(d, ws)
     elif name.startswith("bmm_qk_"):
@@ -942,15 +948,17 @@ def single_call(args):
         ws = torch.empty(mix.lib.mix_decode_attention_workspace_bytes(ctypes.byref(dd)), dtype=torch.uint8,
                          device=dev)
         fn = lambda: mix.decode_attention(dd, ws)
-    elif name.startswith("mix_quantize_t") and name.endswith(f"_{M}x{DM}"):
+    elif re.fullmatch(r"mix_quantize_t[12]_\d+x\d+", name):
+        # the activation quantisers (the sweep's, the MLP's and the ViT's)
         t = T1 if name.startswith("mix_quantize_t1") else T2
-        x = bf16(synth.to_bf16_bits(synth.vlm_activations(0, 1, M, DM, visual_rows=(3 * M) // 4)))
-        c = torch.empty((M, DM // 2), dtype=torch.uint8, device=dev)
-        sh = torch.empty((M, DM // 32), dtype=torch.uint8 if t == T1 else torch.int16, device=dev)
-        fn = lambda: mix.mix_quantize(x, M, DM, DM, t, -8, 1, c, sh)
+        rows, k = map(int, name.rsplit("_", 1)[1].split("x"))
+        x = bf16(synth.to_bf16_bits(synth.vlm_activations(0, 1, rows, k, visual_rows=(3 * rows) // 4)))
+        c = torch.empty((rows, k // 2), dtype=torch.uint8, device=dev)
+        sh = torch.empty((rows, k // 32), dtype=torch.uint8 if t == T1 else torch.int16, device=dev)
+        fn = lambda: mix.mix_quantize(x, rows, k, k, t, -8, 1, c, sh)
     else:
         raise SystemExit(f"--call supports the prefill matmuls, the attention Q.K'^T and P.V, K-smoothing, the "
-                         f"decode attention and the MiX quantisers of the sweep, not {name}")
+                         f"decode attention and the MiX activation quantisers, not {name}")
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # larger than L2
     times = []
     for i in range(args.warmup + args.steps):

@@ -297,6 +297,18 @@ typedef struct {
    * mix_mx_gemm_prepare_b for a descriptor with the same M, N, K, batch,
    * b_group, B fields and algo (NULL: B is prepared inside every call). */
   const void* b_prepared;
+  /* Optional causal bound of A (a_causal = 0: none).  a_causal = 1 asserts
+   * that in every batch A[m][k] is zero for every k > m + a_causal_shift:
+   * the masked part of a causal attention P (a_causal_shift = keys -
+   * queries, 0 for a square self-attention P; |a_causal_shift| < 2^31).
+   * The fused-decode variant then neither loads nor multiplies the 128-deep
+   * k-steps that lie wholly past the bound of a 128-row tile, and starts the
+   * tiles with the longest K loops first; the other variants ignore it.
+   * When the assertion holds the result is the same bits as without it (the
+   * skipped steps would only add exact zeros); when it does not, the entries
+   * of those steps are taken as zero. */
+  int a_causal;
+  int64_t a_causal_shift;
 } mix_gemm_desc_t;
 
 /* Bytes of device workspace mix_mx_gemm needs for this descriptor (0 if

@@ -265,6 +265,9 @@ static mix_status_t validate_gemm(const mix_gemm_desc_t* d) {
   if ((d->epi_flags & ~7u) || (d->epi_flags & 6u) == 6u) return MIX_ERR_INVALID_ARG;
   if (d->algo < MIX_GEMM_AUTO || d->algo > MIX_GEMM_TCGEN05_FUSED) return MIX_ERR_INVALID_ARG;
   if (d->b_prepared != nullptr && !aligned(d->b_prepared, 16)) return MIX_ERR_ALIGN;
+  if (d->a_causal != 0 && d->a_causal != 1) return MIX_ERR_INVALID_ARG;
+  if (d->a_causal && (d->a_causal_shift <= -(int64_t)INT32_MAX || d->a_causal_shift >= (int64_t)INT32_MAX))
+    return MIX_ERR_INVALID_ARG;
   if (d->K % 32 != 0) return MIX_ERR_SHAPE;
   if (d->epi != MIX_EPI_NONE && d->N % 32 != 0) return MIX_ERR_SHAPE;
   if (d->epi == MIX_EPI_NONE && d->c == nullptr) return MIX_ERR_INVALID_ARG;

@@ -136,6 +136,10 @@ struct TcParams {
   // staged kernel: how many of the three groups of four epilogue warps drain
   // a tile (the others only pass the barriers)
   int epi_groups;
+  // fused-decode kernel: A is zero past column m + a_causal_shift (a causal
+  // attention P), so a tile's K loop ends at the last k-step reaching below
+  int a_causal;
+  int64_t a_causal_shift;
 };
 
 // Byte offset of 16-byte chunk `chunk` of row `row` in a K-major operand tile
@@ -246,8 +250,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* stage_nz = reinterpret_cast<volatile int*>(smem + L::OFF_NZ);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t m0 = (int64_t)blockIdx.x * BM, n0 = (int64_t)blockIdx.y * BN, bt = blockIdx.z;
-  const int num_k = (int)((p.K + BK - 1) / BK);
+  // Under a causal bound of A (every entry past column m + shift is zero) a
+  // tile's K loop stops at the last k-step that reaches below the bound of
+  // its last row, and the tiles are taken last row tile first, so that the
+  // longest loops start in the first wave.  Step 0 always runs (it
+  // initialises the accumulator).
+  const int64_t mtile = p.a_causal ? (int64_t)(gridDim.x - 1 - blockIdx.x) : (int64_t)blockIdx.x;
+  const int64_t m0 = mtile * BM, n0 = (int64_t)blockIdx.y * BN, bt = blockIdx.z;
+  int num_k = (int)((p.K + BK - 1) / BK);
+  if (p.a_causal) {
+    const int64_t last_col = m0 + BM - 1 + p.a_causal_shift;
+    const int64_t kend = last_col < 0 ? 1 : last_col / BK + 1;
+    if (kend < num_k) num_k = (int)kend;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S_CODES; ++i) {
@@ -1082,6 +1097,8 @@ TcParams make_params(const mix_gemm_desc_t& d) {
   p.out_codes = d.out_codes; p.out_shared = d.out_shared; p.out_ld = d.out_ld; p.out_bs = d.out_batch_stride;
   p.wait_limit = WAIT_LIMIT;
   p.selftest_no_loads = 0;
+  p.a_causal = d.a_causal;
+  p.a_causal_shift = d.a_causal_shift;
   return p;
 }
 

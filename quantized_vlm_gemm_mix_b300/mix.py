@@ -61,6 +61,7 @@ class GemmDesc(ctypes.Structure):
         ("out_codes", ctypes.c_void_p), ("out_shared", ctypes.c_void_p),
         ("out_ld", ctypes.c_int64), ("out_batch_stride", ctypes.c_int64),
         ("algo", ctypes.c_int), ("b_prepared", ctypes.c_void_p),
+        ("a_causal", ctypes.c_int), ("a_causal_shift", ctypes.c_int64),
     ]
 
 
@@ -375,7 +376,8 @@ def quantize_mx(x: torch.Tensor, axis: int, mx_type: int, flags: int = 0, stream
 def gemm_desc(M, N, K, a_codes, a_shared, a_type, a_ebias, b_codes, b_scales, b_type, c=None,
               epi=MIX_EPI_NONE, epi_ebias=-8, epi_flags=MIX_ASYM_ZERO, out_codes=None, out_shared=None,
               batch=1, b_group=1, a_ld=None, a_batch_stride=None, b_ld=None, b_batch_stride=None,
-              ldc=None, c_batch_stride=None, out_ld=None, out_batch_stride=None, algo=MIX_GEMM_AUTO, b_block=32) -> GemmDesc:
+              ldc=None, c_batch_stride=None, out_ld=None, out_batch_stride=None, algo=MIX_GEMM_AUTO, b_block=32,
+              a_causal=0, a_causal_shift=0) -> GemmDesc:
     d = GemmDesc()
     # the descriptor holds raw device pointers: keep the tensors alive with it
     d._keep = [t for t in (a_codes, a_shared, b_codes, b_scales, c, out_codes, out_shared) if t is not None]
@@ -394,6 +396,7 @@ def gemm_desc(M, N, K, a_codes, a_shared, a_type, a_ebias, b_codes, b_scales, b_
     d.out_ld = N if out_ld is None else out_ld
     d.out_batch_stride = M * d.out_ld if out_batch_stride is None else out_batch_stride
     d.algo = algo
+    d.a_causal, d.a_causal_shift = a_causal, a_causal_shift
     return d
 
 

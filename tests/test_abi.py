@@ -79,6 +79,13 @@ def test_validation_rejects_before_launch(mix):
     d.b_block = 8                                   # only 32 (or 0) and 16 exist
     assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_INVALID_ARG
     d.b_block = 0
+    d.a_causal = 2                                  # the causal bound is off (0) or on (1)
+    assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_INVALID_ARG
+    d.a_causal, d.a_causal_shift = 1, 1 << 31       # |shift| < 2^31
+    assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_INVALID_ARG
+    d.a_causal_shift = -(1 << 31)
+    assert L.mix_mx_gemm(ctypes.byref(d), None, 0, None) == mix.MIX_ERR_INVALID_ARG
+    d.a_causal, d.a_causal_shift = 0, 0
     assert L.mx_quantize(None, 1, 64, 64, 64, 1, 1, 16, None, None, None) == mix.MIX_ERR_INVALID_ARG
     assert L.ksmooth_kv(None, 1, 16, 4, 12, 48, None, 0, None, None, 0, None) in (mix.MIX_ERR_SHAPE,
                                                                                  mix.MIX_ERR_INVALID_ARG)

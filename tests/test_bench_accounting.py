@@ -40,9 +40,14 @@ def test_step_table_flops_and_shapes(small):
             assert flops == 2.0 * M * N * K
             assert cpu == ("gemm", M * N * (K // 32))
         m = re.fullmatch(r"bmm_(qk|pv)_(\d+)x(\d+)x(\d+)x(\d+)", name)
-        if m:                                        # bmm_<qk|pv>_heads x M x N x K
+        if m and m.group(1) == "qk":                 # bmm_qk_heads x M x N x K
             H, M, N, K = map(int, m.groups()[1:])
             assert flops == 2.0 * H * M * N * K
+        if m and m.group(1) == "pv":                 # causal P (M = K tokens): products below the mask,
+            H, M, N, K = map(int, m.groups()[1:])    # P's blocks holding an unmasked entry
+            assert M == K and flops == 2.0 * H * N * M * (M + 1) / 2
+            blocks = H * sum(r // 32 + 1 for r in range(M))
+            assert nbytes == blocks * 18 + bench.plane_bytes(N * H // 7, K, 0) + H * M * N * 4
         if name.startswith(("mix_quantize", "mx_quantize", "ksmooth")):
             assert flops == 0.0
         m = re.fullmatch(r"decode_attention_(\d+)x(\d+)x(\d+)x(\d+)", name)

@@ -105,12 +105,19 @@ def test_pv_prefill_bench_form_and_full_size_p_quantiser(mix, orc):
     mix.mx_quantize(to_dev(vb), T, HK * D, HK * D, 0, mix.MX_INT4, 0, vqc_g, vqs_g)
     assert np.array_equal(to_host(vqc_g).reshape(HK * D, -1), vc)
     assert np.array_equal(to_host(vqs_g).reshape(HK * D, -1), vs)
-    O = torch.empty((HQ, T, D), dtype=torch.float32, device="cuda")
-    d = mix.gemm_desc(T, D, T, pc_g, ps_g, mix.MIX_T2_4P5, -15, vqc_g, vqs_g, mix.MX_INT4, c=O, batch=HQ,
-                      b_group=G, algo=mix.MIX_GEMM_TCGEN05)
-    mix.gemm(d)
-    torch.cuda.synchronize()
-    assert mix.mix_device_error() == 0
+    # the benchmark's form states P's causal bound (a_causal); the same call
+    # without it reads every k-step and must give the same bits
+    outs = []
+    for causal in (1, 0):
+        O = torch.empty((HQ, T, D), dtype=torch.float32, device="cuda")
+        d = mix.gemm_desc(T, D, T, pc_g, ps_g, mix.MIX_T2_4P5, -15, vqc_g, vqs_g, mix.MX_INT4, c=O, batch=HQ,
+                          b_group=G, algo=mix.MIX_GEMM_TCGEN05, a_causal=causal)
+        mix.gemm(d)
+        torch.cuda.synchronize()
+        assert mix.mix_device_error() == 0
+        outs.append(O)
+    assert torch.equal(outs[0], outs[1])
+    O = outs[0]
     vc3, vs3 = vc.reshape(HK, D, -1), vs.reshape(HK, D, -1)
     rng = np.random.default_rng(15)
     for h in HEADS:

@@ -302,6 +302,40 @@ def test_tc_zero_blocks_causal(mix, orc, algo, N):
     assert np.all(got[256:260] == 0) and np.all(got[261:] == 0)
 
 
+@pytest.mark.parametrize("shift,M,K,batch,N", [(0, 384, 1024, 2, 128), (200, 300, 640, 1, 128),
+                                               (-300, 520, 896, 2, 128), (0, 1000, 1024, 1, 256)])
+def test_tc_causal_bound(mix, orc, shift, M, K, batch, N):
+    """A stated causal bound (a_causal): A is zero past column m + shift in
+    every batch, and the fused-decode kernel skips the k-steps past each row
+    tile's bound and takes the row tiles last first.  The result is the same
+    bits as the same call without the bound, and the oracle's within the
+    matmul tolerance.  A negative shift leaves whole row tiles zero (their
+    loop keeps step 0), a positive one (more keys than queries) moves the
+    bound right, M is ragged in two cases, and the 256-column tile runs too."""
+    import torch
+    rng = np.random.default_rng(17 + M)
+    a = rng.random((batch, M, K)).astype(np.float32)
+    a[:, np.arange(K)[None, :] > np.arange(M)[:, None] + shift] = 0.0
+    ac, ash = orc.mix_quantize(a.reshape(batch * M, K), 2, -15)
+    w = synth.to_bf16_bits(synth.normal(18, 1, N * K, 0, 0.5).reshape(N, K))
+    bc, bs = orc.mx_quantize(w, 1, 0)
+    outs = []
+    for causal in (0, 1):
+        c = torch.empty((batch, M, N), dtype=torch.float32, device="cuda")
+        d = mix.gemm_desc(M, N, K, to_dev(ac), to_dev(ash), 2, -15, to_dev(bc), to_dev(bs), 0, c=c, batch=batch,
+                          b_group=batch, algo=mix.MIX_GEMM_TCGEN05_FUSED, a_causal=causal, a_causal_shift=shift)
+        mix.gemm(d)
+        torch.cuda.synchronize()
+        assert mix.mix_device_error() == 0
+        outs.append(to_host(c))
+    assert np.array_equal(outs[0], outs[1])
+    for b in range(batch):
+        ref = orc.gemm(ac[b * M:(b + 1) * M], ash[b * M:(b + 1) * M], 2, -15, bc, bs, 0)
+        assert row_rel_err(outs[1][b], ref) <= GEMM_REL_TOL, b
+    if shift < 0:
+        assert np.all(outs[1][:, :-shift] == 0)
+
+
 PREP_CASES = [(algo, bt, blk) for algo in ALGOS for bt, blk in ((1, 32), (0, 32), (0, 16), (1, 16))
               if not (algo == "fused" and bt == 1 and blk == 32)]   # MXFP4 on the fused path: read as it is
 
