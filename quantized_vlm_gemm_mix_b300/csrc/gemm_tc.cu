@@ -66,9 +66,8 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 128;
 constexpr int KB = BK / 2;  // code bytes per row per stage
-constexpr int S_CODES = 3;
 constexpr int A_CODES = BM * KB;                     // 8 KB
-constexpr int A_OPS = BM * BK, B_OPS = BN * BK;      // 16 KB, 32 KB (also the padded E2M1 tile)
+constexpr int A_OPS = BM * BK;                       // 16 KB
 constexpr int DEC_WARP0 = 4, NUM_DEC_WARPS = 16;
 constexpr int NUM_THREADS = (DEC_WARP0 + NUM_DEC_WARPS) * 32;
 constexpr uint32_t TMEM_COLS = 512;
@@ -252,11 +251,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // Under a causal bound of A (every entry past column m + shift is zero) a
   // tile's K loop stops at the last k-step that reaches below the bound of
-  // its last row, and the tiles are taken last row tile first, so that the
-  // longest loops start in the first wave.  Step 0 always runs (it
-  // initialises the accumulator).
-  const int64_t mtile = p.a_causal ? (int64_t)(gridDim.x - 1 - blockIdx.x) : (int64_t)blockIdx.x;
-  const int64_t m0 = mtile * BM, n0 = (int64_t)blockIdx.y * BN, bt = blockIdx.z;
+  // its last row, and the CTAs take the tiles in order of decreasing loop
+  // length (the last row tile of every column tile and batch first), so the
+  // short loops fill in the tail.  Step 0 always runs (it initialises the
+  // accumulator).
+  int64_t mtile = blockIdx.x, ntile = blockIdx.y, bt = blockIdx.z;
+  if (p.a_causal) {
+    const int64_t lin = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+    const int64_t per = (int64_t)gridDim.y * gridDim.z;
+    mtile = (int64_t)gridDim.x - 1 - lin / per;
+    ntile = (lin % per) % gridDim.y;
+    bt = (lin % per) / gridDim.y;
+  }
+  const int64_t m0 = mtile * BM, n0 = ntile * BN;
   int num_k = (int)((p.K + BK - 1) / BK);
   if (p.a_causal) {
     const int64_t last_col = m0 + BM - 1 + p.a_causal_shift;
@@ -867,7 +874,7 @@ __global__ void __maxnreg__(96)
       ptx::tc_commit(drain);
       ptx::mbar_wait(drain, 0, p.wait_limit, never);
     }
-  } else if (warp < EPI_WARP0) {
+  } else if (warp >= SF_WARP0 && warp < EPI_WARP0) {
     // -------------------------------------------------------- scale warps
     // Lane l of the warp for lane quadrant q stores, per k-step, the 32-bit
     // scale words of rows 32 i + l (i = 0..3) of A and of both 128-row
