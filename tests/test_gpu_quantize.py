@@ -207,6 +207,31 @@ def test_mx_cols_ragged(mix, orc, shape, t):
     assert np.array_equal(to_host(codes), c_ref) and np.array_equal(to_host(scales), s_ref)
 
 
+@pytest.mark.parametrize("shape", [(32, 8), (96, 200), (4128, 72), (288, 1024)])
+def test_mx_cols_bf16_aligned_edges(mix, orc, shape):
+    """bf16 weights quantised down their columns (n and the row stride
+    multiples of 8), partial column groups and k-block groups, and edge
+    values planted in some blocks: NaN
+    (coded as zero, never the maximum), +-Inf, an all-zero block, bf16
+    subnormals and values near the bf16 maximum; both formats and all three
+    scale rules, bit for bit against the oracle."""
+    kdim, n = shape
+    rng = np.random.default_rng(kdim + n)
+    w = rng.standard_normal((kdim, n)).astype(np.float32) * 0.02
+    w[3, 1] = np.nan
+    w[5, n - 1] = np.inf
+    w[40 % kdim, n // 2] = -np.inf
+    w[:32, min(3, n - 1)] = 0.0
+    w[:32, n - 2] = (rng.standard_normal(32) * 1e-40).astype(np.float32)
+    if n > 8:
+        w[kdim - 32:, 8] = (rng.uniform(-1.1, 1.1, 32) * 3e38).astype(np.float32)
+        w[kdim - 1, 9] = np.nan
+    wb = synth.to_bf16_bits(w)
+    for t in (0, 1):
+        for flags in (0, 2, 4):
+            check_mx(mix, orc, wb, 0, t, flags)
+
+
 def test_mx_edge_values(mix, orc):
     rng = np.random.default_rng(6)
     rows = [np.zeros(32, np.float32)]
