@@ -26,7 +26,9 @@
 //               32-column block).
 // The MMA thread copies the stage's scale words into TMEM (tcgen05.cp, in
 // issue order with the MMAs) and issues the MMAs behind them.  A stage whose
-// A tile holds only zero codes skips its copies and MMAs.  The staged
+// A tile holds only zero codes skips its copies and MMAs; under a stated
+// causal bound of A the k-steps past a tile's bound are not run at all, and
+// the tiles are taken longest K loop first.  The staged
 // kernel (gemm_staged_kernel, wider outputs) is described further down.
 // Every wait is bounded; a wait that runs out sets the device error word and
 // the CTA drains and exits.
