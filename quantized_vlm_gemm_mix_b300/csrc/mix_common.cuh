@@ -354,15 +354,30 @@ __device__ __forceinline__ void mix_block32_bf16(const uint32_t* w, int ebias, b
 // step runs packed on the top 16 bits of each element, which decides exactly
 // as on all 32: every threshold is a multiple of 2^16 in bit-pattern space,
 // and for such a t, |x| < t holds exactly when its top 16 bits are below t's.
+// max(|a|, |b|, |c|) in one instruction, NaN if any input is NaN.  For
+// values that are not NaN the result is the largest magnitude with its sign
+// clear, and non-negative floats order as their bit patterns do, so its bits
+// are the integer maximum of the magnitude bit patterns (checked on the GPU
+// for every fp32 pattern as an input).
+__device__ __forceinline__ float absmax3(float a, float b, float c) {
+  float d;
+  asm("max.NaN.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <int TYPE>
 __device__ __forceinline__ void mix_block32_f32(uint32_t* u, int ebias, bool asym, uint4& cw, uint32_t& sh) {
+  // the sub-block maxima of |x|, eight elements in four 3-input steps; a NaN
+  // makes the maximum a NaN pattern, above every finite and infinite one
   uint32_t ks[4];
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
-    uint32_t k = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) k = max(k, u[8 * s + i] & 0x7FFFFFFFu);
-    ks[s] = k;
+    const uint32_t* v = u + 8 * s;
+    float m = absmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+    m = absmax3(m, __uint_as_float(v[3]), __uint_as_float(v[4]));
+    m = absmax3(m, __uint_as_float(v[5]), __uint_as_float(v[6]));
+    m = absmax3(m, __uint_as_float(v[7]), __uint_as_float(v[7]));
+    ks[s] = __float_as_uint(m);
   }
   const uint32_t kb = max(max(ks[0], ks[1]), max(ks[2], ks[3]));
   if (kb > 0x7F800000u) {  // a NaN in the block: the scalar path codes it as zero
