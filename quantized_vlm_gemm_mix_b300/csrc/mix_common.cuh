@@ -480,13 +480,15 @@ __device__ __forceinline__ uint32_t mx_codes8(const uint32_t* u, int X, bool fp4
   return w;
 }
 
-// Largest |x| bit pattern of n elements (NaN patterns are larger than Inf's).
+// Largest |x| bit pattern of n >= 3 elements, or a NaN pattern (above every
+// other) when one of them is NaN: two elements per 3-input abs max.
 template <int N>
 __device__ __forceinline__ uint32_t max_abs_bits(const uint32_t* u) {
-  uint32_t k = 0;
+  float m = absmax3(__uint_as_float(u[0]), __uint_as_float(u[1]), __uint_as_float(u[2]));
 #pragma unroll
-  for (int i = 0; i < N; ++i) k = max(k, u[i] & 0x7FFFFFFFu);
-  return k;
+  for (int i = 3; i < N; i += 2)
+    m = absmax3(m, __uint_as_float(u[i]), __uint_as_float(u[i + 1 < N ? i + 1 : i]));
+  return __float_as_uint(m);
 }
 
 // NaN -> +0 in place (NaN is coded as zero and is never a block maximum).
