@@ -428,6 +428,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t a_pf0 = fetch_a(0), a_pf1 = fetch_a(1), a_pf2 = fetch_a(2), a_pf3 = fetch_a(3);
     uint32_t b_pf0 = fetch_b(0), b_pf1 = fetch_b(1), b_pf2 = fetch_b(2), b_pf3 = fetch_b(3);
     bool ok = true;
+    // unrolled by four: the prefetched shared fields and scale words then
+    // rotate through registers by renaming instead of moves (P.V 2 % faster)
+#pragma unroll 4
     for (int kt = 0; kt < num_k && ok; ++kt) {
       const int cs = kt % S_CODES, cn = kt / S_CODES;
       const int os = kt % S_OPS, on = kt / S_OPS;
