@@ -472,7 +472,8 @@ def build_workload(torch, mix, synth, dev, seed=0, small=False):
     dd2 = mix.gemm_desc(7, D, TC, pdc, pds, T2, -15, vcc, vcs, INT4, c=o_dec, batch=HK, algo=mix.MIX_GEMM_SHIFTADD)
     EXT_INPUTS.update(gemv=dict(dd1=dd1, ws1=new(max(16, mix.mix_mx_gemm_workspace_bytes(dd1)), torch.uint8),
                                 dd2=dd2, ws2=new(max(16, mix.mix_mx_gemm_workspace_bytes(dd2)), torch.uint8),
-                                TC=TC, HQ=HQ, HK=HK, D=D))
+                                TC=TC, HQ=HQ, HK=HK, D=D,
+                                dec=lambda: mix.decode_attention(dda, ws_dec)))
 
     calls = []
     for name, nbytes, flops, launches, _ in step_table(small):
@@ -774,6 +775,36 @@ def measure_extensions(torch, mix, stream, iters=10):
     return out
 
 
+def decode_l2_states(torch, stream, iters, name, nbytes, fn):
+    """The fused decode attention with its caches cold in L2 (a 256 MB buffer
+    written before every launch) and warm (launched back to back, so the 4.5
+    MB of caches stay in L2 from the previous call), each against HBM."""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    res = {}
+    for state in ("cold_l2", "warm_l2"):
+        for _ in range(3):
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+        for a, b in ev:
+            if state == "cold_l2":
+                flush.zero_()
+            torch.cuda._sleep(400000)
+            if state == "warm_l2":
+                fn()                                  # the caches the timed call reads, just read
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[f"{name}_{state}"] = {"what": "the fused decode attention, one call, caches " +
+                                  ("evicted from L2 first" if state == "cold_l2" else "resident in L2"),
+                                  "ms": round(ms, 5), "bytes": int(nbytes), "GB/s": round(gbs, 1),
+                                  "frac_hbm": round(gbs / HBM, 3), "launches": 1}
+    del flush
+    return res
+
+
 def measure_unfused_decode(torch, mix, stream, iters):
     """The decode step's two matmuls on the integer shift-add path alone (the
     fused call of the step does the same arithmetic): S = q K'^T over the
@@ -787,6 +818,8 @@ def measure_unfused_decode(torch, mix, stream, iters):
              plane_bytes(HQ, TC, 2) + plane_bytes(HK * D, TC, 0) + HQ * D * 4, 2.0 * HQ * D * TC, 2,
              lambda: mix.mix_mx_gemm(e["dd2"], e["ws2"]))]
     out = {}
+    out.update(decode_l2_states(torch, stream, iters, f"decode_attention_{HK}x{HQ // HK}x{TC}x{D}",
+                                decode_attention_bytes(TC, HQ, HK, D), e["dec"]))
     for name, what, nbytes, flops, launches, fn in rows:
         for _ in range(3):
             fn()
