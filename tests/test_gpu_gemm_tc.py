@@ -303,7 +303,8 @@ def test_tc_zero_blocks_causal(mix, orc, algo, N):
 
 
 @pytest.mark.parametrize("shift,M,K,batch,N", [(0, 384, 1024, 2, 128), (200, 300, 640, 1, 128),
-                                               (-300, 520, 896, 2, 128), (0, 1000, 1024, 1, 256)])
+                                               (-300, 520, 896, 2, 128), (0, 1000, 1024, 1, 256),
+                                               (64, 300, 640, 3, 544)])
 def test_tc_causal_bound(mix, orc, shift, M, K, batch, N):
     """A stated causal bound (a_causal): A is zero past column m + shift in
     every batch, and the fused-decode kernel skips the k-steps past each row
@@ -311,7 +312,9 @@ def test_tc_causal_bound(mix, orc, shift, M, K, batch, N):
     bits as the same call without the bound, and the oracle's within the
     matmul tolerance.  A negative shift leaves whole row tiles zero (their
     loop keeps step 0), a positive one (more keys than queries) moves the
-    bound right, M is ragged in two cases, and the 256-column tile runs too."""
+    bound right, M is ragged in three cases, the 256-column tile runs too,
+    and N = 544 gives three column tiles, which the reordering walks with
+    the row tiles and the batches."""
     import torch
     rng = np.random.default_rng(17 + M)
     a = rng.random((batch, M, K)).astype(np.float32)
