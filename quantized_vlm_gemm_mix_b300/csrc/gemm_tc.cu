@@ -568,6 +568,25 @@ static_assert(PlanS::SMEM_BYTES <= 227 * 1024, "staged plan exceeds shared memor
 static_assert(B_OPS_S % 1024 == 0, "operand stages must keep the 1024-byte swizzle alignment");
 
 __device__ __forceinline__ uint32_t acc_col(int b) { return b ? 256u : 0u; }
+
+// Output tile t of the staged walk.  M fastest: the CTAs in flight share one
+// B tile and sweep A, which is then re-read once per column of tiles; N
+// fastest (NFAST): they share A tiles and sweep B.  The host picks N fastest
+// when A is the larger operand and too large to stay in L2 between sweeps.
+template <bool NFAST>
+__device__ __forceinline__ void staged_tile(int mt, int nt, int t, int& mtile, int& ntile, int& bt) {
+  if (NFAST) {
+    ntile = t % nt;
+    const int rest = t / nt;
+    mtile = rest % mt;
+    bt = rest / mt;
+  } else {
+    mtile = t % mt;
+    const int rest = t / mt;
+    ntile = rest % nt;
+    bt = rest / nt;
+  }
+}
 __device__ __forceinline__ uint32_t sf_col(int s) { return (s & 2 ? 480u : 224u) + 16u * (uint32_t)(s & 1); }
 static_assert(NUM_EPI_WARPS == kSkFlags, "one split-part flag per epilogue warp");
 static_assert(BNS == kStagedBN, "split-part slots hold one 128 x 224 tile");
@@ -749,7 +768,7 @@ __device__ __forceinline__ void epilogue_tile_s(const TcParams& p, const CUtenso
   }
 }
 
-template <bool B_NATIVE, bool SPLIT>
+template <bool B_NATIVE, bool SPLIT, bool NFAST>
 __global__ void __maxnreg__(96)
     gemm_staged_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                        const __grid_constant__ CUtensorMap tmap_c, const TcParams p) {
@@ -812,8 +831,9 @@ __global__ void __maxnreg__(96)
       bool stop = p.selftest_no_loads != 0;
       Unit u;
       for (int i = 0; !stop && staged_unit<SPLIT>(p, tiles, i, u, sku); ++i) {
-        const int t = u.t;
-        const int mtile = t % mt, rest = t / mt, ntile = rest % nt, bt = rest / nt, bbt = bt / (int)p.b_group;
+        int mtile, ntile, bt;
+        staged_tile<NFAST>(mt, nt, u.t, mtile, ntile, bt);
+        const int bbt = bt / (int)p.b_group;
         const uint8_t* sfa = p.sfa_g + (((int64_t)bt * mt + mtile) * p.kt + u.k0) * L::SFA_BYTES;
         const uint8_t* sfb = p.sfb_g + (((int64_t)bbt * nt + ntile) * p.kt + u.k0) * L::SFB_BYTES;
         const int ay = mtile * BM, by = ntile * BNS;
@@ -926,8 +946,8 @@ __global__ void __maxnreg__(96)
         break;
       }
       ptx::tc_fence_after();
-      const int t = u.t;
-      const int mtile = t % mt, rest = t / mt, ntile = rest % nt, bt = rest / nt;
+      int mtile, ntile, bt;
+      staged_tile<NFAST>(mt, nt, u.t, mtile, ntile, bt);
       if (SPLIT && u.kind == UNIT_PART) {
         epilogue_part_s(p, tmem + acc_col(b), warp, lane);
       } else {
@@ -1039,14 +1059,14 @@ bool make_e4m3_map(CUtensorMap* m, const void* base, int64_t k_pad, int64_t rows
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool B_NATIVE, bool SPLIT>
+template <bool B_NATIVE, bool SPLIT, bool NFAST>
 cudaError_t launch_staged(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc, const TcParams& p,
                           dim3 grid, cudaStream_t st) {
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_staged_kernel<B_NATIVE, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_staged_kernel<B_NATIVE, SPLIT, NFAST>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          PlanS::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
@@ -1065,9 +1085,9 @@ cudaError_t launch_staged(const CUtensorMap& ma, const CUtensorMap& mb, const CU
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemm_staged_kernel<B_NATIVE, SPLIT>, ma, mb, mc, p);
+    e = cudaLaunchKernelEx(&cfg, gemm_staged_kernel<B_NATIVE, SPLIT, NFAST>, ma, mb, mc, p);
   } else {
-    gemm_staged_kernel<B_NATIVE, SPLIT><<<grid, NUM_THREADS_S, PlanS::SMEM_BYTES, st>>>(ma, mb, mc, p);
+    gemm_staged_kernel<B_NATIVE, SPLIT, NFAST><<<grid, NUM_THREADS_S, PlanS::SMEM_BYTES, st>>>(ma, mb, mc, p);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess && std::getenv("MIX_DEBUG") != nullptr)
@@ -1233,6 +1253,14 @@ cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t 
   // stored (the epilogue is then the bound: e.g. attention scores, K = 128)
   // all three.
   p.epi_groups = sp.kt >= 16 ? 1 : (sp.kt >= 4 && d.c == nullptr) ? 2 : 3;
+  // The tile walk re-reads one operand per sweep: A (M fastest) or B (N
+  // fastest).  N fastest when A (e4m3 in HBM) is larger than B (e4m3, or
+  // packed E2M1 read in place) and too large to stay in L2 between sweeps:
+  // measured, the 78-84 MB A of the down projection and the ViT fc2 ran 4
+  // and 7 % faster so, the 21 MB A of fc1 2 % slower.
+  const int64_t a_bytes = d.batch * d.M * sp.k_pad;
+  const int64_t b_bytes = sp.bb * d.N * (sp.b_native ? d.K / 2 : sp.k_pad);
+  const bool nf = a_bytes > b_bytes && a_bytes > ((int64_t)32 << 20);
   p.sk_tile0 = sp.sk_tile0;
   p.sk_len = sp.sk_len;
   p.sk_part = sp.split ? reinterpret_cast<float*>(base + sp.off_sk) : nullptr;
@@ -1245,10 +1273,14 @@ cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t 
   }
   const dim3 grid((unsigned)sp.grid);
   if (sp.split)
-    return sp.b_native ? launch_staged<true, true>(ma, mb, mc, p, grid, st)
-                       : launch_staged<false, true>(ma, mb, mc, p, grid, st);
-  return sp.b_native ? launch_staged<true, false>(ma, mb, mc, p, grid, st)
-                     : launch_staged<false, false>(ma, mb, mc, p, grid, st);
+    return sp.b_native ? (nf ? launch_staged<true, true, true>(ma, mb, mc, p, grid, st)
+                             : launch_staged<true, true, false>(ma, mb, mc, p, grid, st))
+                       : (nf ? launch_staged<false, true, true>(ma, mb, mc, p, grid, st)
+                             : launch_staged<false, true, false>(ma, mb, mc, p, grid, st));
+  return sp.b_native ? (nf ? launch_staged<true, false, true>(ma, mb, mc, p, grid, st)
+                           : launch_staged<true, false, false>(ma, mb, mc, p, grid, st))
+                     : (nf ? launch_staged<false, false, true>(ma, mb, mc, p, grid, st)
+                           : launch_staged<false, false, false>(ma, mb, mc, p, grid, st));
 }
 
 }  // namespace
@@ -1296,7 +1328,7 @@ cudaError_t launch_selftest_wait_timeout(void* ws, long long limit_cycles, cudaS
   p.wait_limit = limit_cycles;
   p.selftest_no_loads = 1;
   p.epi_groups = 3;
-  return launch_staged<false, false>(ma, mb, ma, p, dim3(1), st);
+  return launch_staged<false, false, false>(ma, mb, ma, p, dim3(1), st);
 }
 
 cudaError_t launch_gemm_tc(const mix_gemm_desc_t& d, void* ws, size_t ws_bytes, cudaStream_t st,
