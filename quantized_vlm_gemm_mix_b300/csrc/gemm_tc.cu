@@ -1248,11 +1248,11 @@ cudaError_t launch_staged_path(const mix_gemm_desc_t& d, void* ws, cudaStream_t 
   p.sk_nd = sp.nd;
   // The epilogue (and its quantiser above all) slows the MMAs of the next tile
   // while it runs, less so when fewer warps spread it over a longer time; a
-  // tile of 16 or more k-steps leaves time for one group of four warps, a
-  // shorter one needs two, and a tile of a few k-steps whose fp32 C is
-  // stored (the epilogue is then the bound: e.g. attention scores, K = 128)
-  // all three.
-  p.epi_groups = sp.kt >= 16 ? 1 : (sp.kt >= 4 && d.c == nullptr) ? 2 : 3;
+  // tile of 8 or more k-steps leaves time for one group of four warps (the
+  // 10-k-step ViT fc1 ran 3.5 % faster with one than with two), a shorter
+  // one needs two, and a tile of a few k-steps whose fp32 C is stored (the
+  // epilogue is then the bound: e.g. attention scores, K = 128) all three.
+  p.epi_groups = sp.kt >= 8 ? 1 : (sp.kt >= 4 && d.c == nullptr) ? 2 : 3;
   // The tile walk re-reads one operand per sweep: A (M fastest) or B (N
   // fastest).  N fastest when A (e4m3 in HBM) is larger than B (e4m3, or
   // packed E2M1 read in place) and too large to stay in L2 between sweeps:
